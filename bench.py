@@ -1,0 +1,539 @@
+"""Benchmark: decode step of one Flint-style NVFP4 MoE layer on GB300.
+
+A step is one pass of the whole hot path (router GEMV + sigmoid top-6 ->
+gate/up GEMV + SiLU -> down GEMV + weighted combine with the shared expert)
+over one batch of T tokens, through the C ABI, PDL-chained, replayed from a
+CUDA graph. Weights of `--layers` distinct seeded layers stay resident in HBM
+and the steps cycle through them, so every step reads its experts from HBM
+(the rotation's reuse distance is far larger than the 129 MB L2).
+
+value = algorithmic bytes / time, in GB/s: router weights + the packed codes,
+scales and tensor scales of the distinct selected experts + the shared expert
++ x + y, per step, as the routing of each layer actually selects them.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle on the
+same workload instead (a deliberately slow baseline).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+H, E, I, I_SHARED, TOPK = 2048, 256, 512, 512, 6
+ROUTER_BYTES = E * H * 2
+WORKLOADS = {
+    # name: (tokens, routing)
+    "moe-layer-b8-uniform": (8, "uniform"),
+    "moe-layer-b1": (1, "uniform"),
+    "moe-layer-b8-zipf": (8, "zipf"),
+}
+DEFAULT_WORKLOAD = "moe-layer-b8-uniform"
+METRIC = "NVFP4 MoE-layer decode achieved HBM GB/s (algorithmic bytes / layer time)"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=65536)
+    p.add_argument("--warmup", type=int, default=256)
+    p.add_argument("--impl", choices=["flint", "reference"], default="flint")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--layers", type=int, default=32)
+    p.add_argument("--graph-steps", type=int, default=64)
+    p.add_argument("--no-extra", action="store_true", help="skip the other two batch/routing workloads")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def expert_bytes():
+    from nvfp4_moe_decode_sigmoid_gb300 import flint as F
+    gu = 2 * I * F.flint_nvfp4_row_stride(H)
+    dn = H * F.flint_nvfp4_row_stride(I)
+    return gu, dn
+
+
+def step_bytes(n_distinct: int, T: int, with_bias: bool) -> int:
+    gu, dn = expert_bytes()
+    per_expert = gu + dn + 3 * 4  # codes + scales + the three FP32 tensor scales
+    return ROUTER_BYTES + (E * 4 if with_bias else 0) + (n_distinct + 1) * per_expert + 2 * T * H * 2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.dev), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows), "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+class Model:
+    """`n_layers` seeded MoE layers resident on the device, repacked to the kernel layout."""
+
+    def __init__(self, n_layers: int, device):
+        import torch
+        from nvfp4_moe_decode_sigmoid_gb300 import flint as F
+        from nvfp4_moe_decode_sigmoid_gb300 import synth
+        self.layers = []
+        for li in range(n_layers):
+            L = synth.Layer(1000 + li, H=H, E=E, I=I, I_shared=I_SHARED, device=device)
+            routed = F.Experts.from_gguf(L.gate, L.up, L.down, L.ts, E, H, I)
+            s = L.shared
+            shared = F.Experts.from_gguf(s["gate"], s["up"], s["down"], s["ts"].reshape(1, 3), 1, H, I_SHARED)
+            self.layers.append(dict(router_w=L.router_w, routed=routed, shared=shared, seed=1000 + li))
+            del L
+            torch.cuda.synchronize()
+        self.ws = torch.empty(F.flint_workspace_bytes(E, TOPK, I, I_SHARED), dtype=torch.uint8, device=device)
+        F.flint_workspace_init(self.ws)
+
+
+def make_inputs(model, T, routing, device):
+    import torch
+    from nvfp4_moe_decode_sigmoid_gb300 import synth
+    bias = synth.zipf_bias(7, E).to(device) if routing == "zipf" else None
+    per = []
+    for li, lay in enumerate(model.layers):
+        per.append(dict(x=synth.activations(lay["seed"] * 31 + T, T, H, device),
+                        ids=torch.empty((T, TOPK), dtype=torch.int32, device=device),
+                        w=torch.empty((T, TOPK), dtype=torch.float32, device=device),
+                        y=torch.empty((T, H), dtype=torch.bfloat16, device=device)))
+    return bias, per
+
+
+def run_step(F, model, inp, li, bias, flags):
+    lay, io = model.layers[li], inp[li]
+    F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], model.ws, bias=bias, flags=flags)
+    F.flint_moe_decode(io["x"], io["ids"], io["w"], lay["routed"], lay["shared"], io["y"], model.ws, flags=flags)
+
+
+def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, device_index, with_clocks=True):
+    import torch
+    T, routing = WORKLOADS[name]
+    nl = len(model.layers)
+    bias, inp = make_inputs(model, T, routing, "cuda")
+    flags = F.FLINT_PDL
+    for s in range(max(warmup, nl)):
+        run_step(F, model, inp, s % nl, bias, flags)
+    torch.cuda.synchronize()
+    assert F.flint_workspace_check(model.ws) == F.FLINT_OK
+    # distinct experts each layer's routing selects -> algorithmic bytes per step
+    distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
+    bytes_per_layer = [step_bytes(d, T, bias is not None) for d in distinct]
+
+    stream = torch.cuda.Stream()
+    R = max(1, min(graph_steps, steps))
+    graphs = []
+    with torch.cuda.stream(stream):
+        for count, start in ((R, 0), (steps % R, 0)):
+            if count == 0:
+                continue
+            g = torch.cuda.CUDAGraph()
+            # offset so that consecutive replays continue the layer rotation
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(count):
+                    run_step(F, model, inp, (start + s) % nl, bias, flags)
+            graphs.append((g, count))
+    main_g, main_n = graphs[0]
+    reps = steps // R
+    tail = graphs[1] if len(graphs) > 1 else None
+    # warm the graphs
+    for _ in range(2):
+        main_g.replay()
+    torch.cuda.synchronize()
+
+    total_bytes = 0
+    for r in range(reps):
+        total_bytes += sum(bytes_per_layer[s % nl] for s in range(R))
+    if tail:
+        total_bytes += sum(bytes_per_layer[s % nl] for s in range(tail[1]))
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device_index) if with_clocks else None
+    if sampler:
+        sampler.__enter__()
+    sync_all()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(reps):
+        main_g.replay()
+    if tail:
+        tail[0].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sync_all()
+    if sampler:
+        sampler.__exit__(None, None, None)
+    ms = ev0.elapsed_time(ev1)
+    assert F.flint_workspace_check(model.ws) == F.FLINT_OK
+    return dict(T=T, routing=routing, ms=ms, steps=steps, bytes=total_bytes,
+                mean_distinct=sum(distinct) / len(distinct), clocks=sampler.summary() if sampler else None,
+                bytes_per_step_mean=total_bytes / steps)
+
+
+def measure_kernels(F, model, name, rounds=4):
+    """Per-kernel durations (no PDL, events between the three launches) and the
+    gate/up kernel's algorithmic bytes per launch."""
+    import torch
+    T, routing = WORKLOADS[name]
+    nl = len(model.layers)
+    bias, inp = make_inputs(model, T, routing, "cuda")
+    stream = torch.cuda.current_stream()
+    evs = []
+    for r in range(rounds + 1):
+        for li in range(nl):
+            lay, io = model.layers[li], inp[li]
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(stream)
+            F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], model.ws, bias=bias)
+            e[1].record(stream)
+            F.flint_moe_gate_up(io["x"], io["ids"], lay["routed"], lay["shared"], model.ws)
+            e[2].record(stream)
+            F.flint_moe_down_combine(io["ids"], io["w"], lay["routed"], lay["shared"], io["y"], model.ws)
+            e[3].record(stream)
+            if r > 0:  # first round warms up
+                evs.append((li, e))
+    torch.cuda.synchronize()
+    gu_b, dn_b = expert_bytes()
+    distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
+    t_route = statistics.mean(e[0].elapsed_time(e[1]) for _, e in evs) * 1e3
+    t_gu = statistics.mean(e[1].elapsed_time(e[2]) for _, e in evs) * 1e3
+    t_dn = statistics.mean(e[2].elapsed_time(e[3]) for _, e in evs) * 1e3
+    gu_bytes = statistics.mean((distinct[li] + 1) * (gu_b + 8) + T * H * 2 for li, _ in evs)
+    dn_bytes = statistics.mean((distinct[li] + 1) * (dn_b + 4) + T * H * 2 for li, _ in evs)
+    return dict(route_us=t_route, gate_up_us=t_gu, down_us=t_dn, gate_up_bytes=gu_bytes, down_bytes=dn_bytes,
+                route_bytes=ROUTER_BYTES + T * H * 2)
+
+
+def measure_e2e(F, model, name, steps, graph_steps):
+    """Same metric through the C ABI with HOST buffers: every step copies its
+    x from pinned host memory to the device and its y back, inside the timed
+    region (captured together with the kernels in a CUDA graph)."""
+    import torch
+    T, routing = WORKLOADS[name]
+    nl = len(model.layers)
+    bias, inp = make_inputs(model, T, routing, "cuda")
+    hx = [io["x"].cpu().pin_memory() for io in inp]
+    hy = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in inp]
+    stream = torch.cuda.Stream()
+    R = max(1, min(graph_steps, steps))
+    with torch.cuda.stream(stream):
+        for s in range(nl):  # warm-up, routing for the byte count
+            li = s % nl
+            inp[li]["x"].copy_(hx[li], non_blocking=True)
+            run_step(F, model, inp, li, bias, F.FLINT_PDL)
+            hy[li].copy_(inp[li]["y"], non_blocking=True)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(R):
+                li = s % nl
+                inp[li]["x"].copy_(hx[li], non_blocking=True)
+                run_step(F, model, inp, li, bias, F.FLINT_PDL)
+                hy[li].copy_(inp[li]["y"], non_blocking=True)
+    distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
+    reps = max(1, steps // R)
+    g.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    n = reps * R
+    total = sum(step_bytes(distinct[s % nl], T, bias is not None) for s in range(R)) * reps
+    return dict(value=total / (ms * 1e-3) / 1e9, unit="GB/s", h2d_bytes_per_step=T * H * 2,
+                d2h_bytes_per_step=T * H * 2, steps=n, us_per_step=ms * 1e3 / n, path="pinned host x -> route -> "
+                "decode -> pinned host y, CUDA graph")
+
+
+def cpu_baseline(name, budget_s=20.0):
+    """The oracle, as it stands, single-threaded on this host, on a bounded
+    sample of the same workload: whole layers (router + all selected experts +
+    shared expert + combine) of the same recipe, drawn on the CPU."""
+    import oracle
+    from nvfp4_moe_decode_sigmoid_gb300 import synth
+    T, routing = WORKLOADS[name]
+    L = synth.Layer(1000, H=H, E=E, I=I, I_shared=I_SHARED, device="cpu")
+    s = L.shared
+    sh = dict(gate=s["gate"].numpy(), up=s["up"].numpy(), down=s["down"].numpy(), ts=s["ts"].numpy(), I=I_SHARED)
+    bias = synth.zipf_bias(7, E).numpy() if routing == "zipf" else None
+    wr = synth.bits(L.router_w)
+    done, total_bytes, elapsed, rep = 0, 0, 0.0, 0
+    while elapsed < budget_s and done < 64:
+        x = synth.bits(synth.activations(5000 + rep, T, H))
+        t0 = time.perf_counter()
+        ids, _, _ = oracle.moe_layer(x, wr, TOPK, E, I, L.gate.numpy(), L.up.numpy(), L.down.numpy(), L.ts.numpy(),
+                                     shared=sh, bias=bias)
+        elapsed += time.perf_counter() - t0
+        total_bytes += step_bytes(len(set(ids.reshape(-1).tolist())), T, bias is not None)
+        done += 1
+        rep += 1
+    return dict(value=total_bytes / elapsed / 1e9, unit="GB/s", cores=1, kind="oracle",
+                sample=f"{done} whole layer steps of {name} (T={T}) on a CPU-drawn layer, {elapsed:.1f} s, "
+                       f"single thread", seconds=elapsed, steps=done)
+
+
+def traffic_for(kernel_src_hash):
+    """DRAM bytes per launch of the gate/up kernel from the committed ncu summary,
+    if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "gate_up_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_sha256") != kernel_src_hash:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for fn in ("gemv.cu", "flint_device.cuh", "flint_internal.h"):
+        with open(os.path.join(ROOT, "nvfp4_moe_decode_sigmoid_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def run_flint(args):
+    import torch
+    import torch.distributed as dist
+    from nvfp4_moe_decode_sigmoid_gb300 import _build
+    _build.build()
+    from nvfp4_moe_decode_sigmoid_gb300 import flint as F
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def sync_all():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    model = Model(args.layers, "cuda")
+    dev_index = torch.cuda.current_device()
+    main = measure_workload(F, model, args.workload, args.steps, args.warmup, args.graph_steps, sync_all, dev_index)
+    ms = max_over_ranks(main["ms"])
+    value = main["bytes"] * world / (ms * 1e-3) / 1e9
+    extra = {}
+    if not args.no_extra:
+        for name in WORKLOADS:
+            if name == args.workload:
+                continue
+            r = measure_workload(F, model, name, max(1024, args.steps // 4), args.warmup, args.graph_steps, sync_all,
+                                 dev_index, with_clocks=False)
+            extra[name] = dict(us_per_layer=r["ms"] * 1e3 / r["steps"], gb_s=r["bytes"] / (r["ms"] * 1e-3) / 1e9,
+                               mean_distinct_experts=r["mean_distinct"], bytes_per_step=r["bytes_per_step_mean"])
+    kern = measure_kernels(F, model, args.workload)
+    peak, peak_src = load_peaks()
+    achieved = kern["gate_up_bytes"] / (kern["gate_up_us"] * 1e-6) / 1e9
+    traffic = traffic_for(kernel_source_hash())
+    e2e = measure_e2e(F, model, args.workload, min(args.steps, 8192), args.graph_steps)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload)
+    T, routing = WORKLOADS[args.workload]
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms / args.steps,
+            "us_per_layer": ms * 1e3 / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "tokens": T, "routing": routing, "hidden": H, "experts": E,
+                       "top_k": TOPK, "inter": I, "shared_inter": I_SHARED, "weights": "nvfp4 (e2m1 + ue4m3/16 + fp32)",
+                       "activations": "bf16", "layers_rotated": args.layers, "pdl": True,
+                       "graph_steps": args.graph_steps,
+                       "l2": f"inputs larger than L2: {args.layers} resident layers cycled, reuse distance "
+                             f"{(args.layers - 1) * main['bytes_per_step_mean'] / 1e6:.0f} MB > 129 MB L2",
+                       "parallelism": f"replicas x{world}",
+                       "mean_distinct_experts": main["mean_distinct"],
+                       "bytes_per_step": main["bytes_per_step_mean"]},
+            "roofline": {"bound": "hbm", "kernel": "gate_up_kernel", "achieved": round(achieved, 1),
+                         "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "algorithmic_bytes_per_launch": kern["gate_up_bytes"],
+                         "us_per_launch": kern["gate_up_us"]},
+            "kernels_us": {k: round(v, 3) for k, v in kern.items() if k.endswith("_us")},
+            "layer_frac_of_peak": round(value / world / peak, 4),
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 3 * args.steps,
+            "clocks": main["clocks"],
+            "extra_workloads": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle, on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from nvfp4_moe_decode_sigmoid_gb300 import synth
+    T, routing = WORKLOADS[args.workload]
+    L = synth.Layer(1000, H=H, E=E, I=I, I_shared=I_SHARED, device="cpu")
+    s = L.shared
+    sh = dict(gate=s["gate"].numpy(), up=s["up"].numpy(), down=s["down"].numpy(), ts=s["ts"].numpy(), I=I_SHARED)
+    bias = synth.zipf_bias(7, E).numpy() if routing == "zipf" else None
+    wr = synth.bits(L.router_w)
+    # Each step is a bounded sample of the workload, sized so that the whole
+    # run ends within a few minutes: one token through the whole layer when
+    # that fits the per-step budget, otherwise the oracle's expert GEMV over a
+    # slice of gate/up rows of the experts that token selects (the GEMVs carry
+    # 92% of the layer's bytes). Every step is run and timed.
+    budget = 150.0
+    total = args.steps + args.warmup
+    per_step = budget / max(total, 1)
+    gu_bytes_row = H // 64 * 36  # GGUF and kernel layouts both hold 0.5625 B per weight
+    x1 = synth.bits(synth.activations(9000, 1, H))
+    t0 = time.perf_counter()
+    ids1, _, _ = oracle.moe_layer(x1, wr, TOPK, E, I, L.gate.numpy(), L.up.numpy(), L.down.numpy(), L.ts.numpy(),
+                                  shared=sh, bias=bias)
+    t_token = time.perf_counter() - t0
+    whole = t_token <= per_step
+    gate_np = L.gate.numpy()
+    sel = [int(e) for e in ids1.reshape(-1)]
+    rows_per_step = max(1, int(I * len(sel) * per_step / max(t_token, 1e-9) / 2)) if not whole else 0
+    rows_per_step = min(rows_per_step, I)
+    timed_s, timed_b, cursor = 0.0, 0, 0
+    for i in range(total):
+        if whole:
+            x = synth.bits(synth.activations(9001 + i, 1, H))
+            t0 = time.perf_counter()
+            ids, _, _ = oracle.moe_layer(x, wr, TOPK, E, I, L.gate.numpy(), L.up.numpy(), L.down.numpy(),
+                                         L.ts.numpy(), shared=sh, bias=bias)
+            t = time.perf_counter() - t0
+            b = step_bytes(len(set(ids.reshape(-1).tolist())), 1, bias is not None)
+        else:
+            e = sel[cursor % len(sel)]
+            cursor += 1
+            W = gate_np[e][: rows_per_step * gu_bytes_row]
+            t0 = time.perf_counter()
+            oracle.dense_gemv(x1, W, rows_per_step, ts=(float(L.ts[e, 0]),))
+            t = time.perf_counter() - t0
+            b = rows_per_step * gu_bytes_row
+        if i >= args.warmup:
+            timed_s += t
+            timed_b += b
+    value = timed_b / max(timed_s, 1e-12) / 1e9
+    sample = (f"one token per step through the whole layer (router, {TOPK} routed + shared experts, combine)"
+              if whole else f"{rows_per_step} gate rows of one selected expert per step (oracle expert GEMV), "
+                            f"cycling over the {len(sel)} experts one token selects")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": timed_s * 1e3 / max(args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "routing": routing, "whole_token_steps": whole},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample + ", single thread"},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_flint(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,268 @@
+/*
+ * flint.h -- C ABI of the GB300 (sm_103a) small-batch decode path of a
+ * Flint-style MoE layer with weight-only NVFP4 (W4A16) weights.
+ *
+ * The method (sources):
+ *  - "Day-0 Support for Flint on vLLM", section "Model architecture": 256
+ *    routed experts with sigmoid top-6 selection plus a shared expert; the
+ *    NVFP4 checkpoint is a GGUF file whose blocks are NVIDIA's NVFP4 format in
+ *    a different byte order, repacked losslessly at load time and run
+ *    weight-only (W4A16) with BF16 activations; every kernel follows the
+ *    reference implementation's rounding points.
+ *  - same page, section "Optimizations": router and expert GEMVs that read
+ *    only the selected experts' weights; a small-batch dense GEMV on the same
+ *    packed NVFP4 weights; for up to 8 requests, routing and the expert
+ *    combine fused into the neighbouring GEMV kernels, each launched with
+ *    programmatic dependent launch so it loads its weights while the previous
+ *    kernel still runs.
+ *  - "vLLM 宣布首日支持 Recursive 的 Flint ...", section
+ *    "七个内核的依赖链：低延迟路径、无损重排与参考舍入": a 64-value superblock is
+ *    4 x [UE4M3 scale + 16 E2M1 codes], with one FP32 scale per tensor (per
+ *    expert for MoE weights).
+ *
+ * Conventions for every call:
+ *  - Array pointers are DEVICE pointers owned by the caller, unless a comment
+ *    says otherwise. Structs passed by pointer are read on the host during the
+ *    call and may be freed when it returns.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *    asynchronous on that stream; the library never synchronises it except
+ *    in flint_workspace_check.
+ *  - The library allocates no memory. Scratch space ("workspace") is passed
+ *    in by the caller; see flint_workspace_bytes.
+ *  - bf16 values are passed as their 16-bit patterns (flint_bf16).
+ *  - Errors are returned, never thrown. Argument errors are detected on the
+ *    host before anything is launched. FLINT_ERR_CUDA carries the CUDA error
+ *    text in flint_last_error() (thread-local). A device-side wait that gives
+ *    up (FLINT_ERR_TIMEOUT) cannot be returned by the launching call; it is
+ *    recorded in the workspace's status word and reported by
+ *    flint_workspace_check.
+ *  - The kernels are built for sm_103a only; any other device gives
+ *    FLINT_ERR_UNSUPPORTED. There is no CPU fallback.
+ */
+#ifndef FLINT_H
+#define FLINT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t flint_bf16; /* bfloat16 bit pattern */
+
+typedef enum flint_status {
+    FLINT_OK = 0,
+    FLINT_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size or shape */
+    FLINT_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle (T > 8, wrong GPU, ...) */
+    FLINT_ERR_CUDA = 3,        /* a CUDA runtime call failed; see flint_last_error() */
+    FLINT_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (from flint_workspace_check) */
+} flint_status_t;
+
+enum { FLINT_DTYPE_NVFP4 = 0, FLINT_DTYPE_BF16 = 1 };
+enum { FLINT_EPILOGUE_NONE = 0, FLINT_EPILOGUE_SWIGLU = 1 };
+/* flags: launch with programmatic dependent launch (PDL). The kernel then may
+ * start while the previous kernel on the stream still runs; it prefetches
+ * weights first and waits for the previous kernel before it reads any input
+ * that kernel could have written. */
+enum { FLINT_PDL = 1u << 0 };
+
+/* Largest batch of the decode path (the low-latency bound of up to 8 requests). */
+#define FLINT_MAX_TOKENS 8
+/* Largest top-k and largest routed expert count. */
+#define FLINT_MAX_TOPK 8
+#define FLINT_MAX_EXPERTS 1024
+
+/* ------------------------------------------------------------------------ */
+/* Packed NVFP4 weights                                                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * Source layout (GGUF superblocks), as read by this library: a [rows, cols]
+ * matrix (cols % 64 == 0) is rows * cols/64 superblocks of 36 bytes, in row
+ * order and along each row. Superblock bytes 0..3 are the UE4M3 scales of its
+ * four 16-value sub-blocks; bytes 4+8s .. 4+8s+7 are the E2M1 codes of
+ * sub-block s, byte b holding sub-block value b in its low nibble and value
+ * b+8 in its high nibble. Matrices are contiguous. The FP32 tensor scale is
+ * not part of the blocks; it is passed separately (flint_experts,
+ * flint_packed).
+ *
+ * Kernel layout (the repack target): each row is
+ *   bytes [0, cols/2)                 E2M1 codes, byte j = column 2j in the low
+ *                                     nibble, column 2j+1 in the high nibble
+ *   bytes [cols/2, cols/2 + cols/16)  UE4M3 scales, byte b covers columns
+ *                                     16b .. 16b+15
+ *   zero padding to the row stride    flint_nvfp4_row_stride(cols), the next
+ *                                     multiple of 16 bytes (no padding when
+ *                                     cols % 256 == 0)
+ * Rows are contiguous; matrix m of a repack starts at m * dst_mat_stride.
+ * A row's codes and scales sit together so that a run of rows is one
+ * contiguous block for a single bulk (TMA) copy.
+ *
+ * Element value = E2M1(code) * UE4M3(scale) * tensor_scale. UE4M3 bit 7 is
+ * ignored. UE4M3 0x7F (NaN) is outside the supported input domain.
+ */
+int64_t flint_nvfp4_row_stride(int64_t cols);
+int64_t flint_nvfp4_packed_bytes(int64_t n_mats, int64_t rows, int64_t cols);
+int64_t flint_gguf_nvfp4_bytes(int64_t n_mats, int64_t rows, int64_t cols);
+
+/*
+ * flint_nvfp4_repack -- lossless, bit-exact repack of n_mats GGUF NVFP4
+ * matrices [rows, cols] into the kernel layout (load-time step of "Model
+ * architecture": the GGUF blocks are repacked losslessly at load time).
+ *   src:  n_mats * rows * cols/64 * 36 bytes, 16-byte aligned.
+ *   dst:  matrix m at dst + m * dst_mat_stride; 16-byte aligned.
+ *         dst_mat_stride = 0 means rows * flint_nvfp4_row_stride(cols);
+ *         otherwise it must be >= that and a multiple of 16 (used to place
+ *         gate rows and up rows of one expert in a [2I, H] gate/up matrix).
+ *         Bytes between matrices are not touched.
+ *   Errors: FLINT_ERR_INVALID_ARG (null/misaligned pointer, cols % 64 != 0,
+ *   negative sizes, stride too small); FLINT_ERR_CUDA.
+ */
+flint_status_t flint_nvfp4_repack(const uint8_t* src, int64_t n_mats, int64_t rows, int64_t cols,
+                                  uint8_t* dst, int64_t dst_mat_stride, void* stream);
+
+/* Inverse of flint_nvfp4_repack (kernel layout -> GGUF superblocks); same
+ * arguments with src as the output. Used to prove the repack lossless. */
+flint_status_t flint_nvfp4_unrepack(const uint8_t* dst, int64_t n_mats, int64_t rows, int64_t cols,
+                                    int64_t dst_mat_stride, uint8_t* src, void* stream);
+
+/* Dequantise a [rows, cols] kernel-layout matrix to float (without the tensor
+ * scale), with the same decode routine the GEMV kernels use.
+ *   out: rows * cols floats, row-major. Used to prove the dequant bit-exact. */
+flint_status_t flint_nvfp4_dequant(const uint8_t* packed, int64_t rows, int64_t cols, float* out,
+                                   void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Workspace                                                                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * One workspace serves flint_moe_route, flint_moe_gate_up,
+ * flint_moe_down_combine and flint_moe_decode for one layer shape; layers of
+ * the same shape may share it when their calls are issued in order on one
+ * stream. It holds a control header (router arrival counter, status word),
+ * the router's FP32 logits [8, E] and the SwiGLU activations h of the routed
+ * [8, k, I] and shared [8, I_shared] experts (bf16).
+ *   - Must be 256-byte aligned and zero-filled before first use
+ *     (flint_workspace_init). Every call leaves the counter at 0 again.
+ *   - Calls that use one workspace must not overlap on the GPU except as the
+ *     PDL chain route -> gate_up -> down_combine -> next route allows.
+ */
+size_t flint_workspace_bytes(int num_experts, int top_k, int inter, int inter_shared);
+flint_status_t flint_workspace_init(void* ws, size_t ws_bytes, void* stream);
+/* Synchronises `stream`, reads the status word, clears it, and returns
+ * FLINT_ERR_TIMEOUT if a kernel recorded a timed-out wait, else FLINT_OK. */
+flint_status_t flint_workspace_check(void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* MoE layer                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Expert weights of one MoE layer (or of its shared expert, with
+ * num_experts = 1). */
+typedef struct flint_experts {
+    int32_t dtype;        /* FLINT_DTYPE_NVFP4 (FLINT_DTYPE_BF16 reserved) */
+    int32_t num_experts;  /* E */
+    int32_t hidden;       /* H: columns of gate/up, rows of down; % 1024 == 0 */
+    int32_t inter;        /* I: intermediate size; % 256 == 0 */
+    const void* gate_up;  /* E matrices [2I, H], kernel layout, matrix stride
+                             2I * row_stride(H); rows [0, I) gate, [I, 2I) up */
+    const void* down;     /* E matrices [H, I], kernel layout, stride H * row_stride(I) */
+    const float* tensor_scale; /* [E][3] FP32: gate, up, down */
+} flint_experts;
+
+/*
+ * flint_moe_route -- router GEMV, sigmoid, top-k and renormalisation (one
+ * kernel; "Model architecture": sigmoid top-6 over 256 experts; "Optimizations":
+ * routing fused into the GEMV kernels).
+ *   x:        bf16 [T, H] row-major, 16-byte aligned; 1 <= T <= 8; H % 256 == 0.
+ *   router_w: bf16 [E, H] row-major, 16-byte aligned; k <= E <= 1024.
+ *   bias:     FP32 [E] added to the logits before the sigmoid, or NULL.
+ *   ids:      out int32 [T, k]: per token the k experts with the largest
+ *             sigmoid(logit + bias), computed in FP32, in descending order,
+ *             ties to the lower index.
+ *   weights:  out FP32 [T, k]: the selected scores renormalised to sum 1.
+ *   ws:       workspace (flint_workspace_bytes(E, k, ...)).
+ * Logits are FP32 dot products and are not rounded to bf16. The last CTA to
+ * finish its logits performs the selection (no second kernel).
+ */
+flint_status_t flint_moe_route(const flint_bf16* x, int T, int H, const flint_bf16* router_w, int E,
+                               const float* bias, int k, int32_t* ids, float* weights, void* ws,
+                               size_t ws_bytes, unsigned flags, void* stream);
+
+/*
+ * flint_moe_gate_up -- for every token and every selected expert (and the
+ * shared expert): g = bf16(ts_g * Wg x), u = bf16(ts_u * Wu x),
+ * h = bf16(silu(g) * u), with FP32 accumulation. Reads only the distinct
+ * selected experts' gate/up rows; writes h into the workspace. One kernel.
+ *   x [T, H] bf16; ids [T, k] int32 (as from flint_moe_route); routed
+ *   required; shared may be NULL.
+ */
+flint_status_t flint_moe_gate_up(const flint_bf16* x, int T, const int32_t* ids, int k,
+                                 const flint_experts* routed, const flint_experts* shared, void* ws,
+                                 size_t ws_bytes, unsigned flags, void* stream);
+
+/*
+ * flint_moe_down_combine -- d_j = bf16(ts_d * Wd_j h_j) for every selected
+ * expert j and the shared expert, then the combine
+ * y = bf16(sum_j weights[j] * d_j + d_shared), FP32 accumulation in rank
+ * order then the shared term. Each CTA owns a slice of output rows across all
+ * selected experts, so the combine needs no atomics and is deterministic.
+ * One kernel. Reads h from the workspace written by flint_moe_gate_up.
+ *   weights [T, k] FP32; y out bf16 [T, H].
+ */
+flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* weights, int k,
+                                      const flint_experts* routed, const flint_experts* shared,
+                                      flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
+                                      void* stream);
+
+/* flint_moe_decode -- flint_moe_gate_up then flint_moe_down_combine (two
+ * kernels; the second PDL-chained to the first when flags has FLINT_PDL). */
+flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, const float* weights, int k,
+                                const flint_experts* routed, const flint_experts* shared, flint_bf16* y,
+                                void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Dense GEMV on packed weights                                              */
+/* ------------------------------------------------------------------------ */
+
+typedef struct flint_packed {
+    int32_t dtype;        /* FLINT_DTYPE_NVFP4 */
+    int32_t rows;         /* N */
+    int32_t cols;         /* K: % 256 == 0 (% 1024 == 0 for the SwiGLU epilogue) */
+    int32_t reserved;
+    const void* data;     /* [N, K] kernel layout */
+    const float* tensor_scale; /* FP32: [1] (epilogue NONE) or [2] gate, up (SWIGLU) */
+} flint_packed;
+
+/*
+ * flint_dense_gemv -- small-batch dense GEMV on packed NVFP4 weights
+ * ("Optimizations": small-batch dense GEMV on the same packed NVFP4 weights).
+ *   epilogue NONE:   y [T, N] = bf16(ts * W x)
+ *   epilogue SWIGLU: rows [0, N/2) of W are the gate projection, rows
+ *                    [N/2, N) the up projection; y [T, N/2] =
+ *                    bf16(silu(bf16(ts0 * Wg x)) * bf16(ts1 * Wu x)).
+ *   x [T, K] bf16, 1 <= T <= 8. ws may be NULL; when given (any size >= 256
+ *   bytes, initialised) a timed-out wait is recorded in its status word.
+ */
+flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* W, int epilogue, flint_bf16* y,
+                                void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostics                                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Text of the last error on this thread ("" if none). */
+const char* flint_last_error(void);
+const char* flint_status_string(flint_status_t status);
+
+/* Self-test of the bounded-wait path: launches one CTA that waits on an
+ * mbarrier nothing will complete, gives up after budget_ns nanoseconds and
+ * records a timeout in the workspace status word, which flint_workspace_check
+ * then reports as FLINT_ERR_TIMEOUT. Faults nothing; the context stays usable. */
+flint_status_t flint_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t budget_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLINT_H */

@@ -1,0 +1,425 @@
+// abi.cu -- the extern "C" entry points declared in include/flint.h:
+// argument validation on the host, workspace bookkeeping, launch.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "flint_internal.h"
+
+using flint::DevInfo;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+void set_err(const char* fmt, va_list ap) { vsnprintf(g_err, sizeof g_err, fmt, ap); }
+
+flint_status_t fail(flint_status_t st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    set_err(fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+flint_status_t cuda_fail(cudaError_t e, const char* what) {
+    snprintf(g_err, sizeof g_err, "%s: %s", what, cudaGetErrorString(e));
+    return FLINT_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Device facts, cached per device. Only sm_103 devices are accepted.
+flint_status_t device_info(DevInfo& d) {
+    static std::mutex mu;
+    static DevInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && have[dev]) {
+        d = cache[dev];
+        return FLINT_OK;
+    }
+    DevInfo n = {};
+    n.device = dev;
+    if ((e = cudaDeviceGetAttribute(&n.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&n.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&n.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&n.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (n.cc_major != 10 || n.cc_minor != 3)
+        return fail(FLINT_ERR_UNSUPPORTED, "device %d is sm_%d%d; the kernels are built for sm_103a only", dev,
+                    n.cc_major, n.cc_minor);
+    if (dev >= 0 && dev < 64) {
+        cache[dev] = n;
+        have[dev] = true;
+    }
+    d = n;
+    return FLINT_OK;
+}
+
+uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 1; }
+
+flint_status_t check_experts(const flint_experts* x, const char* name, bool need_down) {
+    if (!x) return fail(FLINT_ERR_INVALID_ARG, "%s experts: null", name);
+    if (x->dtype != FLINT_DTYPE_NVFP4)
+        return fail(FLINT_ERR_UNSUPPORTED, "%s experts: only FLINT_DTYPE_NVFP4 weights are implemented", name);
+    if (x->num_experts < 1 || x->num_experts > FLINT_MAX_EXPERTS)
+        return fail(FLINT_ERR_UNSUPPORTED, "%s experts: num_experts %d outside 1..%d", name, x->num_experts,
+                    FLINT_MAX_EXPERTS);
+    if (x->hidden <= 0 || x->hidden % 1024)
+        return fail(FLINT_ERR_UNSUPPORTED, "%s experts: hidden %d must be a positive multiple of 1024", name,
+                    x->hidden);
+    if (x->inter <= 0 || x->inter % 256)
+        return fail(FLINT_ERR_UNSUPPORTED, "%s experts: inter %d must be a positive multiple of 256", name, x->inter);
+    if (!x->tensor_scale || !aligned(x->tensor_scale, 4))
+        return fail(FLINT_ERR_INVALID_ARG, "%s experts: tensor_scale null or misaligned", name);
+    if (!x->gate_up || !aligned(x->gate_up, 16))
+        return fail(FLINT_ERR_INVALID_ARG, "%s experts: gate_up null or not 16-byte aligned", name);
+    if (need_down && (!x->down || !aligned(x->down, 16)))
+        return fail(FLINT_ERR_INVALID_ARG, "%s experts: down null or not 16-byte aligned", name);
+    return FLINT_OK;
+}
+
+flint_status_t check_ws(const void* ws, size_t ws_bytes, size_t need) {
+    if (!ws || !aligned(ws, 256)) return fail(FLINT_ERR_INVALID_ARG, "workspace null or not 256-byte aligned");
+    if (ws_bytes < need)
+        return fail(FLINT_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+    return FLINT_OK;
+}
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Launch shapes of the gate/up kernel (shared by the MoE and dense SwiGLU).
+int gate_up_stages(int sm_count, int T, int k, int I, int Is) {
+    const int items = ceil_div(Is, sm_count) + ceil_div((long long)T * k * I, sm_count) + 1;
+    int ns = ceil_div(items, flint::kWarps);
+    return ns < 1 ? 1 : (ns > 4 ? 4 : ns);
+}
+
+void down_shape(flint::DownArgs& a, int sm_count) {
+    const int kmin = (a.I > 0 && a.Is > 0) ? (a.I < a.Is ? a.I : a.Is) : (a.I > 0 ? a.I : a.Is);
+    a.lpr = 32;
+    while (a.lpr > 8 && (kmin / 32) % a.lpr) a.lpr /= 2;
+    a.rows_max = ceil_div(a.H, sm_count);
+    const long long rs_r = a.I > 0 ? flint::nvfp4_row_stride(a.I) : 0;
+    const long long rs_s = a.Is > 0 ? flint::nvfp4_row_stride(a.Is) : 0;
+    a.slot_bytes = (int)flint::align_up((size_t)a.rows_max * (size_t)(rs_r > rs_s ? rs_r : rs_s), 128);
+    int ups = 16384 / (a.slot_bytes > 0 ? a.slot_bytes : 1);
+    a.units_per_stage = ups < 1 ? 1 : (ups > 4 ? 4 : ups);
+    const int units = a.T * a.k + (a.s_down ? 1 : 0);
+    int ns = ceil_div(units > 0 ? units : 1, a.units_per_stage);
+    a.nstages = ns > 4 ? 4 : ns;
+}
+
+bool lpr_ok(int K, int lpr) { return K == 0 || ((K / 32) % lpr == 0); }
+
+}  // namespace
+
+extern "C" {
+
+const char* flint_last_error(void) { return g_err; }
+
+const char* flint_status_string(flint_status_t s) {
+    switch (s) {
+        case FLINT_OK: return "ok";
+        case FLINT_ERR_INVALID_ARG: return "invalid argument";
+        case FLINT_ERR_UNSUPPORTED: return "unsupported";
+        case FLINT_ERR_CUDA: return "CUDA error";
+        case FLINT_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int64_t flint_nvfp4_row_stride(int64_t cols) { return cols > 0 ? flint::nvfp4_row_stride(cols) : 0; }
+
+int64_t flint_nvfp4_packed_bytes(int64_t n_mats, int64_t rows, int64_t cols) {
+    return n_mats * rows * flint_nvfp4_row_stride(cols);
+}
+
+int64_t flint_gguf_nvfp4_bytes(int64_t n_mats, int64_t rows, int64_t cols) { return n_mats * rows * (cols / 64) * 36; }
+
+size_t flint_workspace_bytes(int num_experts, int top_k, int inter, int inter_shared) {
+    if (num_experts < 0 || top_k < 0 || inter < 0 || inter_shared < 0) return 0;
+    return flint::ws_layout(num_experts, top_k, inter, inter_shared).total;
+}
+
+flint_status_t flint_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws || ws_bytes < flint::kWsHeader) return fail(FLINT_ERR_INVALID_ARG, "workspace null or too small");
+    cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "cudaMemsetAsync");
+}
+
+flint_status_t flint_workspace_check(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws || ws_bytes < flint::kWsHeader) return fail(FLINT_ERR_INVALID_ARG, "workspace null or too small");
+    uint32_t st = 0;
+    cudaError_t e = cudaMemcpyAsync(&st, ws_status(ws), sizeof st, cudaMemcpyDeviceToHost, as_stream(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status");
+    if (!st) return FLINT_OK;
+    e = cudaMemsetAsync(ws_status(ws), 0, sizeof st, as_stream(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status");
+    if (st & (flint::kStatusTimeoutRoute | flint::kStatusTimeoutGateUp | flint::kStatusTimeoutDown |
+              flint::kStatusTimeoutSelftest))
+        return fail(FLINT_ERR_TIMEOUT, "device wait timed out (status 0x%x)", st);
+    return fail(FLINT_ERR_INVALID_ARG, "an expert id was outside [0, num_experts) (status 0x%x)", st);
+}
+
+flint_status_t flint_nvfp4_repack(const uint8_t* src, int64_t n_mats, int64_t rows, int64_t cols, uint8_t* dst,
+                                  int64_t dst_mat_stride, void* stream) {
+    if (n_mats < 0 || rows < 0 || cols <= 0 || cols % 64)
+        return fail(FLINT_ERR_INVALID_ARG, "repack: bad shape n_mats=%lld rows=%lld cols=%lld (cols %% 64 == 0)",
+                    (long long)n_mats, (long long)rows, (long long)cols);
+    const int64_t min_stride = rows * flint::nvfp4_row_stride(cols);
+    if (dst_mat_stride == 0) dst_mat_stride = min_stride;
+    if (dst_mat_stride < min_stride || dst_mat_stride % 16)
+        return fail(FLINT_ERR_INVALID_ARG, "repack: dst_mat_stride %lld below %lld or not a multiple of 16",
+                    (long long)dst_mat_stride, (long long)min_stride);
+    if (n_mats * rows == 0) return FLINT_OK;
+    if (!src || !dst || !aligned(src, 16) || !aligned(dst, 16))
+        return fail(FLINT_ERR_INVALID_ARG, "repack: null or misaligned pointer");
+    DevInfo d;
+    flint_status_t s = device_info(d);
+    if (s != FLINT_OK) return s;
+    cudaError_t e = flint::launch_repack(src, n_mats, rows, cols, dst, dst_mat_stride, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "repack launch");
+}
+
+flint_status_t flint_nvfp4_unrepack(const uint8_t* dst, int64_t n_mats, int64_t rows, int64_t cols,
+                                    int64_t dst_mat_stride, uint8_t* src, void* stream) {
+    if (n_mats < 0 || rows < 0 || cols <= 0 || cols % 64)
+        return fail(FLINT_ERR_INVALID_ARG, "unrepack: bad shape");
+    const int64_t min_stride = rows * flint::nvfp4_row_stride(cols);
+    if (dst_mat_stride == 0) dst_mat_stride = min_stride;
+    if (dst_mat_stride < min_stride || dst_mat_stride % 16)
+        return fail(FLINT_ERR_INVALID_ARG, "unrepack: bad dst_mat_stride");
+    if (n_mats * rows == 0) return FLINT_OK;
+    if (!src || !dst || !aligned(src, 16) || !aligned(dst, 16))
+        return fail(FLINT_ERR_INVALID_ARG, "unrepack: null or misaligned pointer");
+    DevInfo d;
+    flint_status_t s = device_info(d);
+    if (s != FLINT_OK) return s;
+    cudaError_t e = flint::launch_unrepack(dst, n_mats, rows, cols, dst_mat_stride, src, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "unrepack launch");
+}
+
+flint_status_t flint_nvfp4_dequant(const uint8_t* packed, int64_t rows, int64_t cols, float* out, void* stream) {
+    if (rows < 0 || cols <= 0 || cols % 64) return fail(FLINT_ERR_INVALID_ARG, "dequant: bad shape");
+    if (rows == 0) return FLINT_OK;
+    if (!packed || !out || !aligned(packed, 16) || !aligned(out, 16))
+        return fail(FLINT_ERR_INVALID_ARG, "dequant: null or misaligned pointer");
+    DevInfo d;
+    flint_status_t s = device_info(d);
+    if (s != FLINT_OK) return s;
+    cudaError_t e = flint::launch_dequant(packed, rows, cols, out, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "dequant launch");
+}
+
+flint_status_t flint_moe_route(const flint_bf16* x, int T, int H, const flint_bf16* router_w, int E,
+                               const float* bias, int k, int32_t* ids, float* weights, void* ws, size_t ws_bytes,
+                               unsigned flags, void* stream) {
+    if (T < 1 || T > FLINT_MAX_TOKENS) return fail(FLINT_ERR_UNSUPPORTED, "route: T=%d outside 1..%d", T, FLINT_MAX_TOKENS);
+    if (H <= 0 || H % 256) return fail(FLINT_ERR_UNSUPPORTED, "route: H=%d must be a positive multiple of 256", H);
+    if (E < 1 || E > FLINT_MAX_EXPERTS) return fail(FLINT_ERR_UNSUPPORTED, "route: E=%d outside 1..%d", E, FLINT_MAX_EXPERTS);
+    if (k < 1 || k > FLINT_MAX_TOPK || k > E) return fail(FLINT_ERR_UNSUPPORTED, "route: k=%d outside 1..min(%d, E)", k, FLINT_MAX_TOPK);
+    if (!x || !router_w || !ids || !weights || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) ||
+        !aligned(weights, 4) || (bias && !aligned(bias, 4)))
+        return fail(FLINT_ERR_INVALID_ARG, "route: null or misaligned pointer");
+    flint_status_t s = check_ws(ws, ws_bytes, flint::ws_layout(E, 0, 0, 0).h_routed_off);
+    if (s != FLINT_OK) return s;
+    DevInfo d;
+    if ((s = device_info(d)) != FLINT_OK) return s;
+    flint::RouteArgs a = {};
+    a.x = x;
+    a.T = T;
+    a.H = H;
+    a.wr = router_w;
+    a.E = E;
+    a.bias = bias;
+    a.k = k;
+    a.ids = ids;
+    a.weights = weights;
+    a.logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + flint::kWsHeader);
+    a.counter = reinterpret_cast<uint32_t*>(ws);
+    a.status = ws_status(ws);
+    a.rows_per_cta = ceil_div(E, d.sm_count);
+    const size_t smem = flint::route_smem_bytes(a);
+    if (smem > (size_t)d.smem_optin || (size_t)a.rows_per_cta * H * 2 >= (1u << 20))
+        return fail(FLINT_ERR_UNSUPPORTED, "route: H=%d too large for one CTA's shared memory", H);
+    cudaError_t e = flint::launch_route(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "route launch");
+}
+
+static flint_status_t moe_common(const char* what, int T, int k, const flint_experts* routed,
+                                 const flint_experts* shared, bool need_down) {
+    if (T < 1 || T > FLINT_MAX_TOKENS) return fail(FLINT_ERR_UNSUPPORTED, "%s: T=%d outside 1..%d", what, T, FLINT_MAX_TOKENS);
+    flint_status_t s = check_experts(routed, "routed", need_down);
+    if (s != FLINT_OK) return s;
+    if (k < 1 || k > FLINT_MAX_TOPK || k > routed->num_experts)
+        return fail(FLINT_ERR_UNSUPPORTED, "%s: k=%d outside 1..min(%d, E)", what, k, FLINT_MAX_TOPK);
+    if (shared) {
+        if ((s = check_experts(shared, "shared", need_down)) != FLINT_OK) return s;
+        if (shared->num_experts != 1 || shared->hidden != routed->hidden)
+            return fail(FLINT_ERR_INVALID_ARG, "%s: shared expert must have num_experts 1 and the routed hidden size", what);
+    }
+    return FLINT_OK;
+}
+
+flint_status_t flint_moe_gate_up(const flint_bf16* x, int T, const int32_t* ids, int k, const flint_experts* routed,
+                                 const flint_experts* shared, void* ws, size_t ws_bytes, unsigned flags,
+                                 void* stream) {
+    flint_status_t s = moe_common("gate_up", T, k, routed, shared, false);
+    if (s != FLINT_OK) return s;
+    if (!x || !ids || !aligned(x, 16) || !aligned(ids, 4))
+        return fail(FLINT_ERR_INVALID_ARG, "gate_up: null or misaligned x/ids");
+    const int Is = shared ? shared->inter : 0;
+    const flint::WsLayout L = flint::ws_layout(routed->num_experts, k, routed->inter, Is);
+    if ((s = check_ws(ws, ws_bytes, L.total)) != FLINT_OK) return s;
+    DevInfo d;
+    if ((s = device_info(d)) != FLINT_OK) return s;
+    flint::GateUpArgs a = {};
+    a.x = x;
+    a.T = T;
+    a.H = routed->hidden;
+    a.ids = ids;
+    a.k = k;
+    a.gu = static_cast<const uint8_t*>(routed->gate_up);
+    a.E = routed->num_experts;
+    a.I = routed->inter;
+    a.ts = routed->tensor_scale;
+    a.s_gu = shared ? static_cast<const uint8_t*>(shared->gate_up) : nullptr;
+    a.Is = Is;
+    a.s_ts = shared ? shared->tensor_scale : nullptr;
+    a.h_routed = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.h_routed_off);
+    a.h_shared = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.h_shared_off);
+    a.status = ws_status(ws);
+    a.nstages = gate_up_stages(d.sm_count, T, k, a.I, Is);
+    if (flint::gate_up_smem_bytes(a) > (size_t)d.smem_optin)
+        return fail(FLINT_ERR_UNSUPPORTED, "gate_up: shapes exceed one CTA's shared memory");
+    cudaError_t e = flint::launch_gate_up(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "gate_up launch");
+}
+
+flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* weights, int k,
+                                      const flint_experts* routed, const flint_experts* shared, flint_bf16* y,
+                                      void* ws, size_t ws_bytes, unsigned flags, void* stream) {
+    flint_status_t s = moe_common("down_combine", T, k, routed, shared, true);
+    if (s != FLINT_OK) return s;
+    if (!ids || !weights || !y || !aligned(ids, 4) || !aligned(weights, 4) || !aligned(y, 16))
+        return fail(FLINT_ERR_INVALID_ARG, "down_combine: null or misaligned ids/weights/y");
+    const int Is = shared ? shared->inter : 0;
+    const flint::WsLayout L = flint::ws_layout(routed->num_experts, k, routed->inter, Is);
+    if ((s = check_ws(ws, ws_bytes, L.total)) != FLINT_OK) return s;
+    DevInfo d;
+    if ((s = device_info(d)) != FLINT_OK) return s;
+    flint::DownArgs a = {};
+    a.ids = ids;
+    a.w = weights;
+    a.T = T;
+    a.k = k;
+    a.H = routed->hidden;
+    a.down = static_cast<const uint8_t*>(routed->down);
+    a.E = routed->num_experts;
+    a.I = routed->inter;
+    a.ts = routed->tensor_scale;
+    a.s_down = shared ? static_cast<const uint8_t*>(shared->down) : nullptr;
+    a.Is = Is;
+    a.s_ts = shared ? shared->tensor_scale : nullptr;
+    a.s_ts_idx = 2;
+    a.h_routed = reinterpret_cast<const uint16_t*>(static_cast<uint8_t*>(ws) + L.h_routed_off);
+    a.h_shared = reinterpret_cast<const uint16_t*>(static_cast<uint8_t*>(ws) + L.h_shared_off);
+    a.y = y;
+    a.status = ws_status(ws);
+    down_shape(a, d.sm_count);
+    if (!lpr_ok(a.I, a.lpr) || !lpr_ok(a.Is, a.lpr))
+        return fail(FLINT_ERR_UNSUPPORTED, "down_combine: inter sizes %d and %d are incompatible", a.I, a.Is);
+    if (flint::down_smem_bytes(a) > (size_t)d.smem_optin)
+        return fail(FLINT_ERR_UNSUPPORTED, "down_combine: shapes exceed one CTA's shared memory");
+    cudaError_t e = flint::launch_down(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "down_combine launch");
+}
+
+flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, const float* weights, int k,
+                                const flint_experts* routed, const flint_experts* shared, flint_bf16* y, void* ws,
+                                size_t ws_bytes, unsigned flags, void* stream) {
+    flint_status_t s = moe_common("decode", T, k, routed, shared, true);
+    if (s != FLINT_OK) return s;
+    if (!weights || !y || !aligned(weights, 4) || !aligned(y, 16))
+        return fail(FLINT_ERR_INVALID_ARG, "decode: null or misaligned weights/y");
+    s = flint_moe_gate_up(x, T, ids, k, routed, shared, ws, ws_bytes, flags, stream);
+    if (s != FLINT_OK) return s;
+    return flint_moe_down_combine(T, ids, weights, k, routed, shared, y, ws, ws_bytes, flags, stream);
+}
+
+flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* W, int epilogue, flint_bf16* y,
+                                void* ws, size_t ws_bytes, unsigned flags, void* stream) {
+    if (T < 1 || T > FLINT_MAX_TOKENS) return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: T=%d outside 1..%d", T, FLINT_MAX_TOKENS);
+    if (!W) return fail(FLINT_ERR_INVALID_ARG, "dense_gemv: W is null");
+    if (W->dtype != FLINT_DTYPE_NVFP4) return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: only NVFP4 weights");
+    const int N = W->rows, K = W->cols;
+    if (epilogue != FLINT_EPILOGUE_NONE && epilogue != FLINT_EPILOGUE_SWIGLU)
+        return fail(FLINT_ERR_INVALID_ARG, "dense_gemv: unknown epilogue %d", epilogue);
+    if (N < 1 || K < 256 || K % 256) return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: N=%d, K=%d (K %% 256 == 0)", N, K);
+    if (epilogue == FLINT_EPILOGUE_SWIGLU && (N % 2 || K % 1024))
+        return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: SwiGLU needs even N and K %% 1024 == 0");
+    if (!x || !y || !W->data || !W->tensor_scale || !aligned(x, 16) || !aligned(y, 16) || !aligned(W->data, 16) ||
+        !aligned(W->tensor_scale, 4))
+        return fail(FLINT_ERR_INVALID_ARG, "dense_gemv: null or misaligned pointer");
+    if (ws && (ws_bytes < flint::kWsHeader || !aligned(ws, 256)))
+        return fail(FLINT_ERR_INVALID_ARG, "dense_gemv: workspace too small or misaligned");
+    DevInfo d;
+    flint_status_t s = device_info(d);
+    if (s != FLINT_OK) return s;
+    uint32_t* status = ws ? ws_status(ws) : nullptr;
+    const bool pdl = (flags & FLINT_PDL) != 0;
+    cudaError_t e;
+    if (epilogue == FLINT_EPILOGUE_SWIGLU) {
+        flint::GateUpArgs a = {};
+        a.x = x;
+        a.T = T;
+        a.H = K;
+        a.s_gu = static_cast<const uint8_t*>(W->data);
+        a.Is = N / 2;
+        a.s_ts = W->tensor_scale;
+        a.h_shared = y;
+        a.status = status;
+        a.nstages = gate_up_stages(d.sm_count, T, 0, 0, a.Is);
+        if (flint::gate_up_smem_bytes(a) > (size_t)d.smem_optin)
+            return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: K=%d exceeds one CTA's shared memory", K);
+        e = flint::launch_gate_up(a, d, pdl, as_stream(stream));
+    } else {
+        flint::DownArgs a = {};
+        a.T = T;
+        a.k = 0;
+        a.H = N;
+        a.s_down = static_cast<const uint8_t*>(W->data);
+        a.Is = K;
+        a.s_ts = W->tensor_scale;
+        a.s_ts_idx = 0;
+        a.h_shared = x;
+        a.y = y;
+        a.status = status;
+        down_shape(a, d.sm_count);
+        if (!lpr_ok(a.Is, a.lpr) || flint::down_smem_bytes(a) > (size_t)d.smem_optin)
+            return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: N=%d, K=%d exceed one CTA's shared memory", N, K);
+        e = flint::launch_down(a, d, pdl, as_stream(stream));
+    }
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "dense_gemv launch");
+}
+
+flint_status_t flint_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t budget_ns, void* stream) {
+    flint_status_t s = check_ws(ws, ws_bytes, flint::kWsHeader);
+    if (s != FLINT_OK) return s;
+    DevInfo d;
+    if ((s = device_info(d)) != FLINT_OK) return s;
+    cudaError_t e = flint::launch_selftest_wait(ws_status(ws), budget_ns, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "selftest launch");
+}
+
+}  // extern "C"

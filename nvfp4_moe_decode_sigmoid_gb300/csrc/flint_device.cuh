@@ -1,0 +1,143 @@
+// flint_device.cuh -- device helpers shared by the sm_103a kernels:
+// 1-D bulk (TMA) copies into shared memory completed on an mbarrier, bounded
+// mbarrier waits, programmatic dependent launch, NVFP4 decode.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "flint_internal.h"
+
+namespace flint {
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch ("Optimizations": each kernel is launched with
+// programmatic dependent launch so it loads weights while the previous one
+// still runs). Both are no-ops when the kernel was launched without the PDL
+// attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses, mbarriers, bulk copies
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Adds `bytes` to the barrier's expected transaction count without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Arrives once and adds `bytes` to the expected transaction count.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for phase `parity` of the barrier, for at most budget_ns. Returns
+// false (and records `code` in *status) if the wait gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t code,
+                                                  uint64_t budget_ns = kWaitBudgetNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > budget_ns) {
+            if (status) atomicOr(status, code);
+            return false;
+        }
+    }
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Loads that bypass L1: data written by another kernel of the PDL chain.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int32_t ld_cg(const int32_t* p) { return __ldcg(p); }
+__device__ __forceinline__ float ld_cg(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ uint4 ld_cg(const uint4* p) { return __ldcg(p); }
+__device__ __forceinline__ uint2 ld_cg(const uint2* p) { return __ldcg(p); }
+
+// ---------------------------------------------------------------------------
+// bf16 helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+__device__ __forceinline__ float bf16_round_f32(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// ---------------------------------------------------------------------------
+// NVFP4 decode
+// ---------------------------------------------------------------------------
+// Two E2M1 codes (one byte: column 2j low nibble, 2j+1 high nibble) -> two
+// exact floats, via the hardware FP4 -> f16x2 conversion.
+__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
+    uint32_t h2;
+    asm("{\n .reg .b8 b;\n cvt.u8.u32 b, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}" : "=r"(h2) : "r"(byte));
+    return __half22float2(*reinterpret_cast<__half2*>(&h2));
+}
+
+// Two UE4M3 scale bytes (low byte = first) -> two exact floats. Bit 7 of each
+// byte is not part of the unsigned format and is cleared.
+__device__ __forceinline__ float2 ue4m3x2_to_float2(uint32_t two_bytes) {
+    uint32_t h2;
+    const uint16_t v = static_cast<uint16_t>(two_bytes & 0x7F7Fu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    return __half22float2(*reinterpret_cast<__half2*>(&h2));
+}
+
+// 32 codes of one 16-byte chunk -> 32 floats (code values, no scale).
+__device__ __forceinline__ void decode_chunk(const uint4 q, float (&w)[32]) {
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float2 v = e2m1x2_to_float2((words[i] >> (8 * b)) & 0xFFu);
+            w[8 * i + 2 * b] = v.x;
+            w[8 * i + 2 * b + 1] = v.y;
+        }
+    }
+}
+
+}  // namespace flint

@@ -1,0 +1,138 @@
+// flint_internal.h -- declarations shared by the library's translation units
+// (kernel argument blocks, workspace layout, launchers, error reporting).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "flint.h"
+
+#if defined(__CUDACC__)
+#define FLINT_HD __host__ __device__
+#else
+#define FLINT_HD
+#endif
+
+namespace flint {
+
+// A bounded device-side wait gives up after this long (a copy of a few KB
+// normally lands in microseconds; this only turns a lost copy into an error).
+constexpr uint64_t kWaitBudgetNs = 2000000000ull;
+
+// Status-word bits (workspace header, word 1).
+enum : uint32_t {
+    kStatusTimeoutRoute = 1u << 0,
+    kStatusTimeoutGateUp = 1u << 1,
+    kStatusTimeoutDown = 1u << 2,
+    kStatusTimeoutSelftest = 1u << 3,
+    kStatusBadExpertId = 1u << 4,
+};
+
+constexpr int kThreads = 256;       // every GEMV kernel: 8 warps
+constexpr int kWarps = kThreads / 32;
+constexpr size_t kWsHeader = 256;   // counter (word 0), status (word 1)
+
+FLINT_HD constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Workspace regions, from the layer shape.
+struct WsLayout {
+    size_t logits_off, h_routed_off, h_shared_off, total;
+};
+inline WsLayout ws_layout(int E, int k, int I, int Is) {
+    WsLayout L;
+    L.logits_off = kWsHeader;
+    L.h_routed_off = align_up(L.logits_off + sizeof(float) * FLINT_MAX_TOKENS * (size_t)E, 256);
+    L.h_shared_off = align_up(L.h_routed_off + 2 * (size_t)FLINT_MAX_TOKENS * k * I, 256);
+    L.total = align_up(L.h_shared_off + 2 * (size_t)FLINT_MAX_TOKENS * (size_t)Is, 256);
+    return L;
+}
+
+FLINT_HD inline int64_t nvfp4_row_stride(int64_t cols) { return (int64_t)align_up((size_t)(cols / 2 + cols / 16), 16); }
+
+// ---------------------------------------------------------------------------
+// Kernel argument blocks
+// ---------------------------------------------------------------------------
+struct RouteArgs {
+    const uint16_t* x;
+    int T, H;
+    const uint16_t* wr;
+    int E;
+    const float* bias;
+    int k;
+    int32_t* ids;
+    float* weights;
+    float* logits;     // workspace [8][E]
+    uint32_t* counter; // workspace word 0
+    uint32_t* status;  // workspace word 1
+    int rows_per_cta;
+};
+
+// Gate/up + SiLU. "routed" may be absent (dense SwiGLU); "shared" is the
+// always-on shared expert or the dense matrix.
+struct GateUpArgs {
+    const uint16_t* x;
+    int T, H;
+    const int32_t* ids;
+    int k;
+    const uint8_t* gu;  // routed: E x [2I, H]
+    int E, I;
+    const float* ts;    // [E][3]
+    const uint8_t* s_gu; // shared: [2Is, H] or null
+    int Is;
+    const float* s_ts;  // [>=2]
+    uint16_t* h_routed; // [8][k][I]
+    uint16_t* h_shared; // [T][Is]
+    uint32_t* status;
+    int nstages;        // ring depth
+};
+
+// Down + combine. "routed" may be absent (dense GEMV without epilogue).
+struct DownArgs {
+    const int32_t* ids;
+    const float* w;
+    int T, k, H;
+    const uint8_t* down; // routed: E x [H, I]
+    int E, I;
+    const float* ts;     // [E][3]; the down scale is index 2
+    const uint8_t* s_down; // shared: [H, Is] or null
+    int Is;
+    const float* s_ts;   // scale s_ts[s_ts_idx]
+    int s_ts_idx;
+    const uint16_t* h_routed; // [8][k][I]
+    const uint16_t* h_shared; // [T][Is]
+    uint16_t* y;              // [T][H]
+    uint32_t* status;
+    int lpr;                  // lanes per row: 8, 16 or 32
+    int units_per_stage;
+    int nstages;
+    int rows_max;             // largest row slice of any CTA
+    int slot_bytes;
+};
+
+// ---------------------------------------------------------------------------
+// Launchers (return the CUDA error of the launch)
+// ---------------------------------------------------------------------------
+struct DevInfo {
+    int device;
+    int sm_count;
+    int cc_major, cc_minor;
+    int smem_optin;
+};
+
+cudaError_t launch_repack(const uint8_t* src, int64_t n_mats, int64_t rows, int64_t cols, uint8_t* dst,
+                          int64_t mat_stride, cudaStream_t s);
+cudaError_t launch_unrepack(const uint8_t* dst, int64_t n_mats, int64_t rows, int64_t cols, int64_t mat_stride,
+                            uint8_t* src, cudaStream_t s);
+cudaError_t launch_dequant(const uint8_t* packed, int64_t rows, int64_t cols, float* out, cudaStream_t s);
+cudaError_t launch_route(const RouteArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
+cudaError_t launch_gate_up(const GateUpArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
+cudaError_t launch_down(const DownArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
+cudaError_t launch_selftest_wait(uint32_t* status, uint64_t budget_ns, cudaStream_t s);
+
+size_t gate_up_smem_bytes(const GateUpArgs& a);
+size_t down_smem_bytes(const DownArgs& a);
+size_t route_smem_bytes(const RouteArgs& a);
+
+}  // namespace flint

@@ -1,0 +1,89 @@
+"""Helpers for the GPU parity tests: seeded layers on the device, inputs with
+a guaranteed top-k margin, and the tolerance check."""
+import numpy as np
+import torch
+
+import oracle
+from nvfp4_moe_decode_sigmoid_gb300 import synth
+
+# Layer outputs: relative L2 error <= 1e-2 and per element
+# |gpu - ref| <= 3e-2 * (|ref| + 1e-2) against the oracle.
+REL_L2 = 1e-2
+ELEM_A, ELEM_B = 3e-2, 1e-2
+MARGIN = 1e-3
+
+
+def flint():
+    from nvfp4_moe_decode_sigmoid_gb300 import _build
+    _build.build()
+    from nvfp4_moe_decode_sigmoid_gb300 import flint as f
+    return f
+
+
+def bf16_to_f64(bits):
+    b = np.asarray(bits, np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def assert_close(y_gpu_bits, y_ref_bits, what=""):
+    a, r = bf16_to_f64(y_gpu_bits), bf16_to_f64(y_ref_bits)
+    assert np.all(np.isfinite(a)), f"{what}: non-finite GPU output"
+    rel = np.linalg.norm(a - r) / max(np.linalg.norm(r), 1e-30)
+    assert rel <= REL_L2, f"{what}: relative L2 error {rel:.3e} > {REL_L2}"
+    bad = np.abs(a - r) > ELEM_A * (np.abs(r) + ELEM_B)
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements outside tolerance, e.g. gpu {a[bad][:4]} ref {r[bad][:4]}"
+    return rel
+
+
+def margin_x(router_bits, T, H, k, bias, seed, margin=MARGIN):
+    """Seeded tokens, each resampled until its k-th and (k+1)-th sigmoid scores
+    (oracle, FP32 decision precision) differ by at least `margin`."""
+    rows = []
+    E = router_bits.shape[0]
+    for t in range(T):
+        rep = 0
+        while True:
+            x = synth.activations(seed * 100003 + t * 1009 + rep, 1, H)
+            if k >= E:
+                break
+            _, _, s = oracle.router(synth.bits(x), router_bits, k, bias)
+            ss = np.sort(s[0])[::-1]
+            if ss[k - 1] - ss[k] >= margin:
+                break
+            rep += 1
+        rows.append(x)
+    return torch.cat(rows)
+
+
+class DeviceLayer:
+    """A synth.Layer (drawn on the CPU) copied to the GPU and repacked there."""
+
+    def __init__(self, L: synth.Layer):
+        f = flint()
+        self.L = L
+        dev = "cuda"
+        self.router_w = L.router_w.to(dev)
+        self.routed = f.Experts.from_gguf(L.gate.to(dev), L.up.to(dev), L.down.to(dev), L.ts, L.E, L.H, L.I)
+        self.shared = None
+        if L.shared is not None:
+            s = L.shared
+            self.shared = f.Experts.from_gguf(s["gate"].to(dev), s["up"].to(dev), s["down"].to(dev),
+                                              s["ts"].reshape(1, 3), 1, L.H, s["I"])
+        torch.cuda.synchronize()
+
+    def oracle_args(self):
+        L = self.L
+        sh = None
+        if L.shared is not None:
+            s = L.shared
+            sh = dict(gate=s["gate"].numpy(), up=s["up"].numpy(), down=s["down"].numpy(), ts=s["ts"].numpy(),
+                      I=s["I"])
+        return dict(E=L.E, I=L.I, gate=L.gate.numpy(), up=L.up.numpy(), down=L.down.numpy(), ts=L.ts.numpy(),
+                    shared=sh)
+
+    def workspace(self, k):
+        f = flint()
+        Is = self.L.Is if self.L.shared is not None else 0
+        ws = torch.empty(f.flint_workspace_bytes(self.L.E, k, self.L.I, Is), dtype=torch.uint8, device="cuda")
+        f.flint_workspace_init(ws)
+        return ws

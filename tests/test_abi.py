@@ -1,0 +1,89 @@
+"""The C-ABI library loads, exports every function include/flint.h declares,
+and rejects bad arguments on the host before touching a GPU (CPU only)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flint.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flint_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def flint():
+    from nvfp4_moe_decode_sigmoid_gb300 import _build
+    _build.build()
+    from nvfp4_moe_decode_sigmoid_gb300 import flint as f
+    return f
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("flint_nvfp4_repack", "flint_moe_route", "flint_moe_decode", "flint_dense_gemv",
+              "flint_workspace_bytes", "flint_last_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(flint):
+    lib = C.CDLL(flint.LIBRARY_PATH)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_size_helpers(flint):
+    assert flint.flint_nvfp4_row_stride(2048) == 1152
+    assert flint.flint_nvfp4_row_stride(512) == 288
+    assert flint.flint_nvfp4_row_stride(64) == 48
+    assert flint.flint_nvfp4_packed_bytes(256, 1024, 2048) == 256 * 1024 * 1152
+    assert flint.flint_gguf_nvfp4_bytes(1, 2048, 512) == 2048 * 8 * 36
+    ws = flint.flint_workspace_bytes(256, 6, 512, 512)
+    assert ws % 256 == 0 and ws >= 256 + 8 * 256 * 4 + 2 * 8 * 6 * 512 + 2 * 8 * 512
+    assert flint.flint_status_string(4) == "device wait timed out"
+
+
+def _raw(flint):
+    return flint.raw_library()
+
+
+def test_host_validation_without_a_gpu(flint):
+    L = _raw(flint)
+    p = C.c_void_p(0x1000)  # aligned, never dereferenced: validation fails first
+    # repack: cols not a multiple of 64
+    assert L.flint_nvfp4_repack(p, 1, 4, 63, p, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    assert "cols" in flint.flint_last_error()
+    # repack: stride too small
+    assert L.flint_nvfp4_repack(p, 2, 4, 64, p, 16, None) == flint.FLINT_ERR_INVALID_ARG
+    # route: batch outside 1..8, null pointers, bad k
+    assert L.flint_moe_route(p, 9, 2048, p, 256, None, 6, p, p, p, 1 << 20, 0, None) == flint.FLINT_ERR_UNSUPPORTED
+    assert L.flint_moe_route(None, 1, 2048, p, 256, None, 6, p, p, p, 1 << 20, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    assert L.flint_moe_route(p, 1, 2048, p, 256, None, 9, p, p, p, 1 << 20, 0, None) == flint.FLINT_ERR_UNSUPPORTED
+    # route: misaligned x, small workspace
+    assert L.flint_moe_route(C.c_void_p(0x1002), 1, 2048, p, 256, None, 6, p, p, p, 1 << 20, 0, None) == \
+        flint.FLINT_ERR_INVALID_ARG
+    assert L.flint_moe_route(p, 1, 2048, p, 256, None, 6, p, p, p, 64, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    # decode: missing routed experts, bad hidden size
+    ex = flint.flint_experts(0, 256, 2048, 512, 0x1000, 0x1000, 0x1000)
+    assert L.flint_moe_decode(p, 1, p, p, 6, None, None, p, p, 1 << 24, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    bad = flint.flint_experts(0, 256, 2000, 512, 0x1000, 0x1000, 0x1000)
+    assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(bad), None, p, p, 1 << 24, 0, None) == \
+        flint.FLINT_ERR_UNSUPPORTED
+    bf = flint.flint_experts(1, 256, 2048, 512, 0x1000, 0x1000, 0x1000)
+    assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(bf), None, p, p, 1 << 24, 0, None) == \
+        flint.FLINT_ERR_UNSUPPORTED
+    sh = flint.flint_experts(0, 2, 2048, 512, 0x1000, 0x1000, 0x1000)
+    assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(ex), C.byref(sh), p, p, 1 << 24, 0, None) == \
+        flint.FLINT_ERR_INVALID_ARG
+    # decode: workspace too small
+    assert L.flint_moe_gate_up(p, 1, p, 6, C.byref(ex), None, p, 1024, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    # dense: odd N with SwiGLU, K not a multiple of 256
+    W = flint.flint_packed(0, 7, 2048, 0, 0x1000, 0x1000)
+    assert L.flint_dense_gemv(p, 1, C.byref(W), 1, p, None, 0, 0, None) == flint.FLINT_ERR_UNSUPPORTED
+    W2 = flint.flint_packed(0, 8, 200, 0, 0x1000, 0x1000)
+    assert L.flint_dense_gemv(p, 1, C.byref(W2), 0, p, None, 0, 0, None) == flint.FLINT_ERR_UNSUPPORTED

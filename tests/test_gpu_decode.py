@@ -1,0 +1,133 @@
+"""GPU MoE decode (gate/up + SiLU, down + combine) and the whole layer against
+the oracle, element by element within the layer tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from flint_testlib import DeviceLayer, assert_close, flint, margin_x
+from nvfp4_moe_decode_sigmoid_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer_run(dl, x, k, bias=None, flags=0, route_flags=None):
+    f = flint()
+    T, H = x.shape
+    ws = dl.workspace(k)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    xc = x.cuda()
+    b = bias.cuda() if bias is not None else None
+    f.flint_moe_route(xc, dl.router_w, k, ids, w, ws, bias=b, flags=flags if route_flags is None else route_flags)
+    f.flint_moe_decode(xc, ids, w, dl.routed, dl.shared, y, ws, flags=flags)
+    assert f.flint_workspace_check(ws) == f.FLINT_OK
+    return ids.cpu().numpy(), w.cpu().numpy(), synth.bits(y)
+
+
+def _check_layer(dl, x, k, bias=None, flags=0):
+    ids, w, y = _layer_run(dl, x, k, bias, flags)
+    rids, rw, ry = oracle.moe_layer(synth.bits(x), synth.bits(dl.L.router_w), k,
+                                    bias=None if bias is None else bias.numpy(), **dl.oracle_args())
+    for t in range(x.shape[0]):
+        assert set(ids[t]) == set(rids[t])
+    # the experts' outputs given the GPU's own routing (same ids, its weights)
+    ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
+    assert_close(y, ref, "layer (gpu routing)")
+    assert_close(y, ry, "layer (oracle routing)")
+    return y
+
+
+@pytest.fixture(scope="module")
+def small_layer():
+    return DeviceLayer(synth.Layer(11, H=1024, E=16, I=256, I_shared=256))
+
+
+@pytest.mark.parametrize("T,k", [(1, 6), (2, 1), (5, 4), (8, 6), (8, 8)])
+def test_small_layer(small_layer, T, k):
+    x = margin_x(synth.bits(small_layer.L.router_w), T, 1024, k, None, seed=T + 10 * k)
+    _check_layer(small_layer, x, k)
+
+
+def test_small_layer_pdl_is_bitwise_identical(small_layer):
+    f = flint()
+    x = margin_x(synth.bits(small_layer.L.router_w), 8, 1024, 6, None, seed=3)
+    a = _layer_run(small_layer, x, 6, flags=0)
+    b = _layer_run(small_layer, x, 6, flags=f.FLINT_PDL)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+def test_without_shared_expert():
+    dl = DeviceLayer(synth.Layer(12, H=1024, E=16, I=256, I_shared=0, shared=False))
+    x = margin_x(synth.bits(dl.L.router_w), 3, 1024, 6, None, seed=4)
+    _check_layer(dl, x, 6)
+
+
+def test_shared_expert_wider_than_routed():
+    dl = DeviceLayer(synth.Layer(13, H=1024, E=16, I=256, I_shared=1024))
+    x = margin_x(synth.bits(dl.L.router_w), 4, 1024, 6, None, seed=5)
+    _check_layer(dl, x, 6)
+
+
+def test_decode_with_repeated_and_shared_ids(small_layer):
+    # hand-made routing: token 0 picks expert 3 twice, tokens share experts
+    f = flint()
+    dl = small_layer
+    T, k, H = 3, 4, 1024
+    x = synth.activations(21, T, H)
+    ids = np.array([[3, 3, 7, 0], [7, 0, 15, 3], [15, 14, 13, 12]], np.int32)
+    w = np.array([[0.4, 0.3, 0.2, 0.1], [0.25, 0.25, 0.25, 0.25], [0.7, 0.1, 0.1, 0.1]], np.float32)
+    ws = dl.workspace(k)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    f.flint_moe_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), dl.routed, dl.shared, y,
+                       ws)
+    assert f.flint_workspace_check(ws) == f.FLINT_OK
+    ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
+    assert_close(synth.bits(y), ref, "repeated ids")
+
+
+def test_out_of_range_id_is_reported_not_read(small_layer):
+    f = flint()
+    dl = small_layer
+    T, k, H = 1, 2, 1024
+    ids = torch.tensor([[1, 999]], dtype=torch.int32, device="cuda")
+    w = torch.tensor([[0.5, 0.5]], dtype=torch.float32, device="cuda")
+    ws = dl.workspace(k)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    f.flint_moe_decode(synth.activations(2, T, H).cuda(), ids, w, dl.routed, dl.shared, y, ws)
+    assert f.flint_workspace_check(ws) == f.FLINT_ERR_INVALID_ARG
+    assert f.flint_workspace_check(ws) == f.FLINT_OK  # cleared
+
+
+@pytest.fixture(scope="module")
+def full_layer():
+    # one Flint-shaped layer: H 2048, 256 routed + 1 shared expert, I 512
+    return DeviceLayer(synth.Layer(1000, H=2048, E=256, I=512, I_shared=512))
+
+
+def test_full_layer_batch1(full_layer):
+    f = flint()
+    x = margin_x(synth.bits(full_layer.L.router_w), 1, 2048, 6, None, seed=7)
+    _check_layer(full_layer, x, 6, flags=f.FLINT_PDL)
+
+
+def test_full_layer_batch8_uniform(full_layer):
+    f = flint()
+    x = margin_x(synth.bits(full_layer.L.router_w), 8, 2048, 6, None, seed=8)
+    _check_layer(full_layer, x, 6, flags=f.FLINT_PDL)
+
+
+def test_full_layer_batch8_zipf(full_layer):
+    f = flint()
+    bias = synth.zipf_bias(3, 256)
+    x = margin_x(synth.bits(full_layer.L.router_w), 8, 2048, 6, bias.numpy(), seed=9)
+    _check_layer(full_layer, x, 6, bias=bias, flags=f.FLINT_PDL)
+
+
+def test_full_layer_is_deterministic(full_layer):
+    f = flint()
+    x = margin_x(synth.bits(full_layer.L.router_w), 8, 2048, 6, None, seed=10)
+    outs = [_layer_run(full_layer, x, 6, flags=f.FLINT_PDL)[2] for _ in range(3)]
+    assert all(np.array_equal(o, outs[0]) for o in outs)
