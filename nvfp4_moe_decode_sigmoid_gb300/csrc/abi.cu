@@ -250,7 +250,7 @@ flint_status_t flint_moe_route(const flint_bf16* x, int T, int H, const flint_bf
     a.status = ws_status(ws);
     a.rows_per_cta = ceil_div(E, d.sm_count);
     const size_t smem = flint::route_smem_bytes(a);
-    if (smem > (size_t)d.smem_optin || (size_t)a.rows_per_cta * H * 2 >= (1u << 20))
+    if (smem + 1024 > (size_t)d.smem_optin || (size_t)a.rows_per_cta * H * 2 >= (1u << 20))
         return fail(FLINT_ERR_UNSUPPORTED, "route: H=%d too large for one CTA's shared memory", H);
     cudaError_t e = flint::launch_route(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "route launch");

@@ -131,6 +131,20 @@ cudaError_t launch_gate_up(const GateUpArgs& a, const DevInfo& d, bool pdl, cuda
 cudaError_t launch_down(const DownArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t budget_ns, cudaStream_t s);
 
+// Allows `kernel` the device's opt-in dynamic shared memory, less its own
+// static shared memory (once per device and kernel).
+template <typename K>
+cudaError_t configure_smem(K kernel, const DevInfo& d, int& configured_for) {
+    if (configured_for == d.device) return cudaSuccess;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             d.smem_optin - (int)fa.sharedSizeBytes);
+    if (e == cudaSuccess) configured_for = d.device;
+    return e;
+}
+
 size_t gate_up_smem_bytes(const GateUpArgs& a);
 size_t down_smem_bytes(const DownArgs& a);
 size_t route_smem_bytes(const RouteArgs& a);

@@ -508,14 +508,6 @@ __global__ void __launch_bounds__(kThreads, 1) down_kernel(const DownArgs a) {
     }
 }
 
-template <typename K>
-cudaError_t configure(K kernel, const DevInfo& d, int& configured_for) {
-    if (configured_for == d.device) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem_optin);
-    if (e == cudaSuccess) configured_for = d.device;
-    return e;
-}
-
 template <typename K, typename A>
 cudaError_t launch_ex(K kernel, const A& args, unsigned grid, size_t smem, bool pdl, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -538,14 +530,14 @@ size_t down_smem_bytes(const DownArgs& a) { return down_layout(a).total; }
 
 cudaError_t launch_gate_up(const GateUpArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
     static int configured_for = -1;
-    cudaError_t e = configure(gate_up_kernel, d, configured_for);
+    cudaError_t e = configure_smem(gate_up_kernel, d, configured_for);
     if (e != cudaSuccess) return e;
     return launch_ex(gate_up_kernel, a, (unsigned)d.sm_count, gate_up_smem_bytes(a), pdl, s);
 }
 
 cudaError_t launch_down(const DownArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
     static int configured_for = -1;
-    cudaError_t e = configure(down_kernel, d, configured_for);
+    cudaError_t e = configure_smem(down_kernel, d, configured_for);
     if (e != cudaSuccess) return e;
     return launch_ex(down_kernel, a, (unsigned)d.sm_count, down_smem_bytes(a), pdl, s);
 }

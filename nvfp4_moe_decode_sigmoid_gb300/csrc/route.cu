@@ -179,11 +179,8 @@ size_t route_smem_bytes(const RouteArgs& a) {
 cudaError_t launch_route(const RouteArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
     const size_t smem = route_smem_bytes(a);
     static int configured_for = -1;
-    if (configured_for != d.device) {
-        cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem_optin);
-        if (e != cudaSuccess) return e;
-        configured_for = d.device;
-    }
+    cudaError_t e = configure_smem(route_kernel, d, configured_for);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((a.E + a.rows_per_cta - 1) / a.rows_per_cta));
     cfg.blockDim = dim3(kThreads);
