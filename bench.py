@@ -210,9 +210,10 @@ def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, devic
     main_g, main_n = graphs[0]
     reps = steps // R
     tail = graphs[1] if len(graphs) > 1 else None
-    # warm the graphs
-    for _ in range(2):
-        main_g.replay()
+    # warm the graphs (replay() launches on the current stream: keep it `stream`)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            main_g.replay()
     torch.cuda.synchronize()
 
     total_bytes = 0
@@ -227,12 +228,13 @@ def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, devic
         sampler.__enter__()
     sync_all()
     torch.cuda.synchronize()
-    ev0.record(stream)
-    for _ in range(reps):
-        main_g.replay()
-    if tail:
-        tail[0].replay()
-    ev1.record(stream)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            main_g.replay()
+        if tail:
+            tail[0].replay()
+        ev1.record(stream)
     torch.cuda.synchronize()
     sync_all()
     if sampler:
@@ -244,38 +246,49 @@ def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, devic
                 bytes_per_step_mean=total_bytes / steps)
 
 
-def measure_kernels(F, model, name, rounds=4):
-    """Per-kernel durations (no PDL, events between the three launches) and the
-    gate/up kernel's algorithmic bytes per launch."""
+def measure_kernels(F, model, name, reps=8):
+    """Average device duration of each of the three kernels: for each kernel a
+    CUDA graph of back-to-back launches (one per resident layer, no PDL) is
+    replayed `reps` times between two CUDA events on the replay stream. The
+    routing comes from a warm-up pass, so the gate/up and down launches see
+    each layer's real expert selection."""
     import torch
     T, routing = WORKLOADS[name]
     nl = len(model.layers)
     bias, inp = make_inputs(model, T, routing, "cuda")
-    stream = torch.cuda.current_stream()
-    evs = []
-    for r in range(rounds + 1):
-        for li in range(nl):
-            lay, io = model.layers[li], inp[li]
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-            e[0].record(stream)
-            F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], model.ws, bias=bias)
-            e[1].record(stream)
-            F.flint_moe_gate_up(io["x"], io["ids"], lay["routed"], lay["shared"], model.ws)
-            e[2].record(stream)
-            F.flint_moe_down_combine(io["ids"], io["w"], lay["routed"], lay["shared"], io["y"], model.ws)
-            e[3].record(stream)
-            if r > 0:  # first round warms up
-                evs.append((li, e))
+    for li in range(nl):
+        run_step(F, model, inp, li, bias, 0)
     torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    calls = {
+        "route": lambda lay, io: F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], model.ws,
+                                                   bias=bias),
+        "gate_up": lambda lay, io: F.flint_moe_gate_up(io["x"], io["ids"], lay["routed"], lay["shared"], model.ws),
+        "down": lambda lay, io: F.flint_moe_down_combine(io["ids"], io["w"], lay["routed"], lay["shared"], io["y"],
+                                                         model.ws),
+    }
+    out = {}
+    for kname, call in calls.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for li in range(nl):
+                    call(model.layers[li], inp[li])
+            g.replay()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        out[kname + "_us"] = e0.elapsed_time(e1) * 1e3 / (reps * nl)
     gu_b, dn_b = expert_bytes()
     distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
-    t_route = statistics.mean(e[0].elapsed_time(e[1]) for _, e in evs) * 1e3
-    t_gu = statistics.mean(e[1].elapsed_time(e[2]) for _, e in evs) * 1e3
-    t_dn = statistics.mean(e[2].elapsed_time(e[3]) for _, e in evs) * 1e3
-    gu_bytes = statistics.mean((distinct[li] + 1) * (gu_b + 8) + T * H * 2 for li, _ in evs)
-    dn_bytes = statistics.mean((distinct[li] + 1) * (dn_b + 4) + T * H * 2 for li, _ in evs)
-    return dict(route_us=t_route, gate_up_us=t_gu, down_us=t_dn, gate_up_bytes=gu_bytes, down_bytes=dn_bytes,
-                route_bytes=ROUTER_BYTES + T * H * 2)
+    out["gate_up_bytes"] = statistics.mean((d + 1) * (gu_b + 8) + T * H * 2 for d in distinct)
+    out["down_bytes"] = statistics.mean((d + 1) * (dn_b + 4) + T * H * 2 for d in distinct)
+    out["route_bytes"] = ROUTER_BYTES + T * H * 2
+    return out
 
 
 def measure_e2e(F, model, name, steps, graph_steps):
@@ -306,13 +319,14 @@ def measure_e2e(F, model, name, steps, graph_steps):
                 hy[li].copy_(inp[li]["y"], non_blocking=True)
     distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
     reps = max(1, steps // R)
-    g.replay()
-    torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(reps):
+    with torch.cuda.stream(stream):
         g.replay()
-    ev1.record(stream)
+        stream.synchronize()
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
     n = reps * R
@@ -447,6 +461,8 @@ def run_flint(args):
                          "traffic": traffic, "algorithmic_bytes_per_launch": kern["gate_up_bytes"],
                          "us_per_launch": kern["gate_up_us"]},
             "kernels_us": {k: round(v, 3) for k, v in kern.items() if k.endswith("_us")},
+            "kernels_gb_s": {k: round(kern[k + "_bytes"] / (kern[k + "_us"] * 1e-6) / 1e9, 1)
+                             for k in ("route", "gate_up", "down")},
             "layer_frac_of_peak": round(value / world / peak, 4),
             "cpu_baseline": cpu,
             "e2e": e2e,

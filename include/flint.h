@@ -228,7 +228,7 @@ flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, 
 typedef struct flint_packed {
     int32_t dtype;        /* FLINT_DTYPE_NVFP4 */
     int32_t rows;         /* N */
-    int32_t cols;         /* K: % 256 == 0 (% 1024 == 0 for the SwiGLU epilogue) */
+    int32_t cols;         /* K: % 1024 == 0 */
     int32_t reserved;
     const void* data;     /* [N, K] kernel layout */
     const float* tensor_scale; /* FP32: [1] (epilogue NONE) or [2] gate, up (SWIGLU) */
@@ -243,6 +243,8 @@ typedef struct flint_packed {
  *                    bf16(silu(bf16(ts0 * Wg x)) * bf16(ts1 * Wu x)).
  *   x [T, K] bf16, 1 <= T <= 8. ws may be NULL; when given (any size >= 256
  *   bytes, initialised) a timed-out wait is recorded in its status word.
+ *   One kernel per group of tokens whose FP32 copy fits in shared memory
+ *   beside the weight ring (all 8 tokens up to K = 4096).
  */
 flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* W, int epilogue, flint_bf16* y,
                                 void* ws, size_t ws_bytes, unsigned flags, void* stream);

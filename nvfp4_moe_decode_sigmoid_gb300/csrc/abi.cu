@@ -95,26 +95,42 @@ flint_status_t check_ws(const void* ws, size_t ws_bytes, size_t need) {
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-// Launch shapes of the gate/up kernel (shared by the MoE and dense SwiGLU).
-int gate_up_stages(int sm_count, int T, int k, int I, int Is) {
-    const int items = ceil_div(Is, sm_count) + ceil_div((long long)T * k * I, sm_count) + 1;
-    int ns = ceil_div(items, flint::kWarps);
-    return ns < 1 ? 1 : (ns > 4 ? 4 : ns);
+// Shared memory a launch may take, leaving room for the kernel's static data.
+constexpr size_t kSmemSlack = 1024;
+
+// Ring depth of the gate/up kernel: enough stages for the largest per-CTA
+// share of the work (at most 4), reduced until the CTA fits in shared memory.
+// Returns 0 when not even one stage fits.
+int gate_up_stages(flint::GateUpArgs& a, bool pair, int sm_count, int smem_optin) {
+    const long long items = ceil_div(a.Is, sm_count) + ceil_div((long long)a.T * a.k * a.I, sm_count) + 1;
+    int ns = ceil_div(items, flint::kConsumerWarps);
+    ns = ns < 1 ? 1 : (ns > 4 ? 4 : ns);
+    for (; ns >= 1; --ns) {
+        a.nstages = ns;
+        if (flint::gate_up_smem_bytes(a, pair) + kSmemSlack <= (size_t)smem_optin) return ns;
+    }
+    return 0;
 }
 
-void down_shape(flint::DownArgs& a, int sm_count) {
+// Shapes of the down kernel; returns false when the layer does not fit.
+bool down_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
     const int kmin = (a.I > 0 && a.Is > 0) ? (a.I < a.Is ? a.I : a.Is) : (a.I > 0 ? a.I : a.Is);
     a.lpr = 32;
     while (a.lpr > 8 && (kmin / 32) % a.lpr) a.lpr /= 2;
+    const int rows_per_task = 2 * (32 / a.lpr);
     a.rows_max = ceil_div(a.H, sm_count);
     const long long rs_r = a.I > 0 ? flint::nvfp4_row_stride(a.I) : 0;
     const long long rs_s = a.Is > 0 ? flint::nvfp4_row_stride(a.Is) : 0;
-    a.slot_bytes = (int)flint::align_up((size_t)a.rows_max * (size_t)(rs_r > rs_s ? rs_r : rs_s), 128);
-    int ups = 16384 / (a.slot_bytes > 0 ? a.slot_bytes : 1);
-    a.units_per_stage = ups < 1 ? 1 : (ups > 4 ? 4 : ups);
+    a.slot_bytes = (int)((rows_per_task < a.rows_max ? rows_per_task : a.rows_max) * (rs_r > rs_s ? rs_r : rs_s));
     const int units = a.T * a.k + (a.s_down ? 1 : 0);
-    int ns = ceil_div(units > 0 ? units : 1, a.units_per_stage);
-    a.nstages = ns > 4 ? 4 : ns;
+    const long long tasks = (long long)units * ceil_div(a.rows_max, rows_per_task);
+    int ns = ceil_div(tasks, flint::kConsumerWarps);
+    ns = ns < 1 ? 1 : (ns > 4 ? 4 : ns);
+    for (; ns >= 1; --ns) {
+        a.nstages = ns;
+        if (flint::down_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin) return true;
+    }
+    return false;
 }
 
 bool lpr_ok(int K, int lpr) { return K == 0 || ((K / 32) % lpr == 0); }
@@ -299,10 +315,9 @@ flint_status_t flint_moe_gate_up(const flint_bf16* x, int T, const int32_t* ids,
     a.h_routed = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.h_routed_off);
     a.h_shared = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.h_shared_off);
     a.status = ws_status(ws);
-    a.nstages = gate_up_stages(d.sm_count, T, k, a.I, Is);
-    if (flint::gate_up_smem_bytes(a) > (size_t)d.smem_optin)
+    if (!gate_up_stages(a, true, d.sm_count, d.smem_optin))
         return fail(FLINT_ERR_UNSUPPORTED, "gate_up: shapes exceed one CTA's shared memory");
-    cudaError_t e = flint::launch_gate_up(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
+    cudaError_t e = flint::launch_gate_up(a, true, d, (flags & FLINT_PDL) != 0, as_stream(stream));
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "gate_up launch");
 }
 
@@ -331,16 +346,14 @@ flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* we
     a.s_down = shared ? static_cast<const uint8_t*>(shared->down) : nullptr;
     a.Is = Is;
     a.s_ts = shared ? shared->tensor_scale : nullptr;
-    a.s_ts_idx = 2;
     a.h_routed = reinterpret_cast<const uint16_t*>(static_cast<uint8_t*>(ws) + L.h_routed_off);
     a.h_shared = reinterpret_cast<const uint16_t*>(static_cast<uint8_t*>(ws) + L.h_shared_off);
     a.y = y;
     a.status = ws_status(ws);
-    down_shape(a, d.sm_count);
+    if (!down_shape(a, d.sm_count, d.smem_optin))
+        return fail(FLINT_ERR_UNSUPPORTED, "down_combine: shapes exceed one CTA's shared memory");
     if (!lpr_ok(a.I, a.lpr) || !lpr_ok(a.Is, a.lpr))
         return fail(FLINT_ERR_UNSUPPORTED, "down_combine: inter sizes %d and %d are incompatible", a.I, a.Is);
-    if (flint::down_smem_bytes(a) > (size_t)d.smem_optin)
-        return fail(FLINT_ERR_UNSUPPORTED, "down_combine: shapes exceed one CTA's shared memory");
     cudaError_t e = flint::launch_down(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "down_combine launch");
 }
@@ -365,9 +378,9 @@ flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* 
     const int N = W->rows, K = W->cols;
     if (epilogue != FLINT_EPILOGUE_NONE && epilogue != FLINT_EPILOGUE_SWIGLU)
         return fail(FLINT_ERR_INVALID_ARG, "dense_gemv: unknown epilogue %d", epilogue);
-    if (N < 1 || K < 256 || K % 256) return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: N=%d, K=%d (K %% 256 == 0)", N, K);
-    if (epilogue == FLINT_EPILOGUE_SWIGLU && (N % 2 || K % 1024))
-        return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: SwiGLU needs even N and K %% 1024 == 0");
+    if (N < 1 || K < 1024 || K % 1024)
+        return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: N=%d, K=%d (K %% 1024 == 0)", N, K);
+    if (epilogue == FLINT_EPILOGUE_SWIGLU && N % 2) return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: SwiGLU needs even N");
     if (!x || !y || !W->data || !W->tensor_scale || !aligned(x, 16) || !aligned(y, 16) || !aligned(W->data, 16) ||
         !aligned(W->tensor_scale, 4))
         return fail(FLINT_ERR_INVALID_ARG, "dense_gemv: null or misaligned pointer");
@@ -378,37 +391,29 @@ flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* 
     if (s != FLINT_OK) return s;
     uint32_t* status = ws ? ws_status(ws) : nullptr;
     const bool pdl = (flags & FLINT_PDL) != 0;
-    cudaError_t e;
-    if (epilogue == FLINT_EPILOGUE_SWIGLU) {
-        flint::GateUpArgs a = {};
-        a.x = x;
-        a.T = T;
-        a.H = K;
-        a.s_gu = static_cast<const uint8_t*>(W->data);
-        a.Is = N / 2;
-        a.s_ts = W->tensor_scale;
-        a.h_shared = y;
-        a.status = status;
-        a.nstages = gate_up_stages(d.sm_count, T, 0, 0, a.Is);
-        if (flint::gate_up_smem_bytes(a) > (size_t)d.smem_optin)
+    const bool pair = epilogue == FLINT_EPILOGUE_SWIGLU;
+    const int n_out = pair ? N / 2 : N;
+    flint::GateUpArgs a = {};
+    a.H = K;
+    a.s_gu = static_cast<const uint8_t*>(W->data);
+    a.Is = n_out;
+    a.s_ts = W->tensor_scale;
+    a.status = status;
+    // Tokens go in groups small enough that their FP32 copy fits beside the ring.
+    int tg = T;
+    for (; tg >= 1; --tg) {
+        a.T = tg;
+        if (gate_up_stages(a, pair, d.sm_count, d.smem_optin)) break;
+    }
+    if (tg < 1) return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: K=%d exceeds one CTA's shared memory", K);
+    cudaError_t e = cudaSuccess;
+    for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += tg) {
+        a.T = T - t0 < tg ? T - t0 : tg;
+        a.x = x + (size_t)t0 * K;
+        a.h_shared = y + (size_t)t0 * n_out;
+        if (!gate_up_stages(a, pair, d.sm_count, d.smem_optin))
             return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: K=%d exceeds one CTA's shared memory", K);
-        e = flint::launch_gate_up(a, d, pdl, as_stream(stream));
-    } else {
-        flint::DownArgs a = {};
-        a.T = T;
-        a.k = 0;
-        a.H = N;
-        a.s_down = static_cast<const uint8_t*>(W->data);
-        a.Is = K;
-        a.s_ts = W->tensor_scale;
-        a.s_ts_idx = 0;
-        a.h_shared = x;
-        a.y = y;
-        a.status = status;
-        down_shape(a, d.sm_count);
-        if (!lpr_ok(a.Is, a.lpr) || flint::down_smem_bytes(a) > (size_t)d.smem_optin)
-            return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: N=%d, K=%d exceed one CTA's shared memory", N, K);
-        e = flint::launch_down(a, d, pdl, as_stream(stream));
+        e = flint::launch_gate_up(a, pair, d, pdl, as_stream(stream));
     }
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "dense_gemv launch");
 }

@@ -126,6 +126,29 @@ __device__ __forceinline__ float2 ue4m3x2_to_float2(uint32_t two_bytes) {
     return __half22float2(*reinterpret_cast<__half2*>(&h2));
 }
 
+// 8 codes of one 32-bit word (byte b: codes 2b, 2b+1) -> 4 exact float pairs.
+__device__ __forceinline__ void decode_word(uint32_t w, float2* f) {
+    uint32_t h0, h1, h2, h3;
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w));
+    f[0] = __half22float2(*reinterpret_cast<__half2*>(&h0));
+    f[1] = __half22float2(*reinterpret_cast<__half2*>(&h1));
+    f[2] = __half22float2(*reinterpret_cast<__half2*>(&h2));
+    f[3] = __half22float2(*reinterpret_cast<__half2*>(&h3));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier among the first `threads` threads of the CTA (hardware barrier `id`).
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // 32 codes of one 16-byte chunk -> 32 floats (code values, no scale).
 __device__ __forceinline__ void decode_chunk(const uint4 q, float (&w)[32]) {
     const uint32_t words[4] = {q.x, q.y, q.z, q.w};

@@ -30,8 +30,12 @@ enum : uint32_t {
     kStatusBadExpertId = 1u << 4,
 };
 
-constexpr int kThreads = 256;       // every GEMV kernel: 8 warps
+constexpr int kThreads = 256;       // router kernel: 8 warps
 constexpr int kWarps = kThreads / 32;
+// Expert / dense GEMV kernels: 15 consumer warps and one producer warp that
+// issues the bulk copies.
+constexpr int kConsumerWarps = 15;
+constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
 constexpr size_t kWsHeader = 256;   // counter (word 0), status (word 1)
 
 FLINT_HD constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -69,26 +73,27 @@ struct RouteArgs {
     int rows_per_cta;
 };
 
-// Gate/up + SiLU. "routed" may be absent (dense SwiGLU); "shared" is the
-// always-on shared expert or the dense matrix.
+// Gate/up + SiLU (pair mode) or plain rows (dense GEMV without epilogue).
+// "routed" may be absent (dense); "shared" is the always-on shared expert or
+// the dense matrix.
 struct GateUpArgs {
     const uint16_t* x;
-    int T, H;
+    int T, H;           // tokens, columns (K)
     const int32_t* ids;
     int k;
     const uint8_t* gu;  // routed: E x [2I, H]
     int E, I;
     const float* ts;    // [E][3]
-    const uint8_t* s_gu; // shared: [2Is, H] or null
+    const uint8_t* s_gu; // shared: [2Is, H] (pair) or [Is, H] (plain rows), or null
     int Is;
-    const float* s_ts;  // [>=2]
+    const float* s_ts;  // [>=2] (pair) or [1]
     uint16_t* h_routed; // [8][k][I]
-    uint16_t* h_shared; // [T][Is]
+    uint16_t* h_shared; // [T][Is]: h of the shared expert, or the dense output y
     uint32_t* status;
     int nstages;        // ring depth
 };
 
-// Down + combine. "routed" may be absent (dense GEMV without epilogue).
+// Down + combine of the MoE layer.
 struct DownArgs {
     const int32_t* ids;
     const float* w;
@@ -98,17 +103,15 @@ struct DownArgs {
     const float* ts;     // [E][3]; the down scale is index 2
     const uint8_t* s_down; // shared: [H, Is] or null
     int Is;
-    const float* s_ts;   // scale s_ts[s_ts_idx]
-    int s_ts_idx;
+    const float* s_ts;   // scale s_ts[2]
     const uint16_t* h_routed; // [8][k][I]
     const uint16_t* h_shared; // [T][Is]
     uint16_t* y;              // [T][H]
     uint32_t* status;
-    int lpr;                  // lanes per row: 8, 16 or 32
-    int units_per_stage;
+    int lpr;                  // lanes per row group: 8, 16 or 32
     int nstages;
     int rows_max;             // largest row slice of any CTA
-    int slot_bytes;
+    int slot_bytes;           // bytes of one task's rows in a stage
 };
 
 // ---------------------------------------------------------------------------
@@ -127,7 +130,7 @@ cudaError_t launch_unrepack(const uint8_t* dst, int64_t n_mats, int64_t rows, in
                             uint8_t* src, cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t* packed, int64_t rows, int64_t cols, float* out, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
-cudaError_t launch_gate_up(const GateUpArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
+cudaError_t launch_gate_up(const GateUpArgs& a, bool pair, const DevInfo& d, bool pdl, cudaStream_t s);
 cudaError_t launch_down(const DownArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t budget_ns, cudaStream_t s);
 
@@ -145,8 +148,10 @@ cudaError_t configure_smem(K kernel, const DevInfo& d, int& configured_for) {
     return e;
 }
 
-size_t gate_up_smem_bytes(const GateUpArgs& a);
+size_t gate_up_smem_bytes(const GateUpArgs& a, bool pair);
+size_t gate_up_stage_bytes(int H, bool pair);
 size_t down_smem_bytes(const DownArgs& a);
+size_t down_stage_bytes(const DownArgs& a);
 size_t route_smem_bytes(const RouteArgs& a);
 
 }  // namespace flint

@@ -18,7 +18,52 @@
 namespace flint {
 namespace {
 
-constexpr int kMaxLanesSlots = FLINT_MAX_EXPERTS / 32;  // experts per lane in the top-k warp
+// Top-k of one token's scores, one warp: lane holds experts lane + 32 i.
+// Sigmoid scores are positive floats, so their bit patterns order like the
+// values; the warp max of the bits picks the best score and a warp min over
+// the lanes' lowest matching index breaks ties toward the lower expert.
+template <int SLOTS>
+__device__ __forceinline__ void topk_warp(const float* logits, const float* bias, int E, int k, int lane,
+                                          int32_t* ids, float* weights) {
+    uint32_t s[SLOTS];
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i) {
+        const int e = lane + 32 * i;
+        uint32_t v = 0u;  // below every valid score bit pattern except +0
+        if (e < E) {
+            float z = ld_cg(logits + e);
+            if (bias) z = z + bias[e];
+            v = __float_as_uint(1.f / (1.f + expf(-z)));
+        }
+        s[i] = v;
+    }
+    uint32_t taken = 0;
+    float sel_s = 0.f, sum = 0.f;
+    int sel_e = 0;
+    for (int j = 0; j < k; ++j) {
+        uint32_t m = 0u;
+#pragma unroll
+        for (int i = 0; i < SLOTS; ++i)
+            if (!((taken >> i) & 1u) && lane + 32 * i < E) m = max(m, s[i]);
+        const uint32_t best = __reduce_max_sync(0xffffffffu, m);
+        uint32_t cand = 0xFFFFFFFFu;
+#pragma unroll
+        for (int i = SLOTS - 1; i >= 0; --i)
+            if (!((taken >> i) & 1u) && lane + 32 * i < E && s[i] == best) cand = (uint32_t)(lane + 32 * i);
+        const uint32_t e = __reduce_min_sync(0xffffffffu, cand);
+        if ((int)(e & 31u) == lane) taken |= 1u << (e >> 5);
+        const float sv = __uint_as_float(best);
+        sum += sv;
+        if (lane == j) {
+            sel_e = (int)e;
+            sel_s = sv;
+        }
+    }
+    if (lane < k) {
+        ids[lane] = sel_e;
+        weights[lane] = sel_s / sum;
+    }
+}
 
 __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -36,25 +81,22 @@ __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
         const uint32_t bytes = (uint32_t)(nrows * H * 2);
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s(wrows, a.wr + (size_t)r0 * H, bytes, bar);
     }
+    __syncthreads();  // the barrier is initialised before anyone waits on it
     // The gate/up kernel only prefetches static weights before its own wait.
     pdl_launch_dependents();
     pdl_wait();  // x may come from the previous kernel
 
+    const int nchunk = H / 8;
     const bool ok = mbar_wait_bounded(bar, 0, tid == 0 ? a.status : nullptr, kStatusTimeoutRoute);
     if (!__syncthreads_and(ok)) return;
 
-    // Partial dot products: thread tid covers 8-element chunks tid, tid+256, ...
     float acc[FLINT_MAX_TOKENS][2];
 #pragma unroll
     for (int t = 0; t < FLINT_MAX_TOKENS; ++t) acc[t][0] = acc[t][1] = 0.f;
-    const int nchunk = H / 8;
     for (int rb = 0; rb < nrows; rb += 2) {  // two router rows at a time
         const bool two = rb + 1 < nrows;
         for (int c = tid; c < nchunk; c += kThreads) {
@@ -102,68 +144,22 @@ __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
         for (int w = 0; w < kWarps; ++w) v += partial[(w * FLINT_MAX_TOKENS + t) * rpc + r];
         a.logits[(size_t)t * a.E + r0 + r] = v;
     }
-    __threadfence();
+    // Publish the logits, take a ticket; the last CTA does the selection.
     __syncthreads();
-    if (tid == 0) is_last = (atomicAdd(a.counter, 1u) == gridDim.x - 1);
+    if (tid == 0) {
+        __threadfence();
+        is_last = (atomicAdd(a.counter, 1u) == gridDim.x - 1);
+        if (is_last) __threadfence();
+    }
     __syncthreads();
     if (!is_last) return;
-    __threadfence();
 
-    // ---- top-k: one warp per token; lane holds experts lane, lane+32, ... ----
     if (warp < T) {
-        const int t = warp;
-        float s[kMaxLanesSlots];
-        const int nslot = (a.E + 31) / 32;
-#pragma unroll
-        for (int i = 0; i < kMaxLanesSlots; ++i) {
-            const int e = lane + 32 * i;
-            float v = -FLT_MAX;  // below every sigmoid value
-            if (i < nslot && e < a.E) {
-                float z = ld_cg(a.logits + (size_t)t * a.E + e);
-                if (a.bias) z = z + a.bias[e];
-                v = 1.f / (1.f + expf(-z));
-            }
-            s[i] = v;
-        }
-        uint32_t taken = 0;
-        float sel_s[FLINT_MAX_TOPK];
-        int sel_e[FLINT_MAX_TOPK];
-        float sum = 0.f;
-#pragma unroll
-        for (int j = 0; j < FLINT_MAX_TOPK; ++j) {
-            if (j < a.k) {
-                float bs = -FLT_MAX;
-                int be = INT32_MAX;
-#pragma unroll
-                for (int i = 0; i < kMaxLanesSlots; ++i) {
-                    // strict '>' keeps the lower index among equal scores
-                    if (i < nslot && !((taken >> i) & 1u) && s[i] > bs) {
-                        bs = s[i];
-                        be = lane + 32 * i;
-                    }
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-                    const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                    if (os > bs || (os == bs && oe < be)) {
-                        bs = os;
-                        be = oe;
-                    }
-                }
-                if ((be & 31) == lane) taken |= 1u << (be >> 5);
-                sel_s[j] = bs;
-                sel_e[j] = be;
-                sum += bs;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < FLINT_MAX_TOPK; ++j) {
-            if (j < a.k && lane == j) {
-                a.ids[t * a.k + j] = sel_e[j];
-                a.weights[t * a.k + j] = sel_s[j] / sum;
-            }
-        }
+        const float* lg = a.logits + (size_t)warp * a.E;
+        if (a.E <= 256)
+            topk_warp<8>(lg, a.bias, a.E, a.k, lane, a.ids + warp * a.k, a.weights + warp * a.k);
+        else
+            topk_warp<FLINT_MAX_EXPERTS / 32>(lg, a.bias, a.E, a.k, lane, a.ids + warp * a.k, a.weights + warp * a.k);
     }
     __syncthreads();
     if (tid == 0) atomicExch(a.counter, 0u);

@@ -85,5 +85,5 @@ def test_host_validation_without_a_gpu(flint):
     # dense: odd N with SwiGLU, K not a multiple of 256
     W = flint.flint_packed(0, 7, 2048, 0, 0x1000, 0x1000)
     assert L.flint_dense_gemv(p, 1, C.byref(W), 1, p, None, 0, 0, None) == flint.FLINT_ERR_UNSUPPORTED
-    W2 = flint.flint_packed(0, 8, 200, 0, 0x1000, 0x1000)
+    W2 = flint.flint_packed(0, 8, 512, 0, 0x1000, 0x1000)
     assert L.flint_dense_gemv(p, 1, C.byref(W2), 0, p, None, 0, 0, None) == flint.FLINT_ERR_UNSUPPORTED

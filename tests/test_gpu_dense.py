@@ -10,7 +10,7 @@ from nvfp4_moe_decode_sigmoid_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("N,K,T", [(2048, 6144, 1), (2048, 6144, 8), (300, 256, 3), (64, 1024, 2), (4096, 512, 5)])
+@pytest.mark.parametrize("N,K,T", [(2048, 6144, 1), (2048, 6144, 8), (300, 1024, 3), (64, 1024, 2), (4096, 2048, 5), (100, 3072, 7)])
 def test_dense_plain(N, K, T):
     f = flint()
     src = synth.gguf_nvfp4(N + K, 1, N, K)
