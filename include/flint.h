@@ -190,6 +190,34 @@ flint_status_t flint_moe_route(const flint_bf16* x, int T, int H, const flint_bf
                                size_t ws_bytes, unsigned flags, void* stream);
 
 /*
+ * flint_moe_route_static -- the same router as flint_moe_route, for callers
+ * that cannot hand the library any device memory of their own: for example a
+ * plug-in whose host framework owns every device allocation and forbids new
+ * ones, or a C caller that holds only its input and output buffers and no
+ * allocator. The pages describe nothing like it (it has no counterpart in the
+ * method); it exists only for such callers.
+ *   Arguments as flint_moe_route, without ws/ws_bytes. The results equal those
+ *   of flint_moe_route on the same inputs.
+ *   Scratch: a 33,024-byte array inside the library (counter, status word,
+ *   FP32 logits for at most 8 tokens x 1024 experts), held by every device that
+ *   loads the library until the process exits. Larger T x E is rejected with
+ *   FLINT_ERR_UNSUPPORTED and a message giving the limit.
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ *   Every call clears the counter and status word (an 8-byte memset on
+ *   `stream`) and then overwrites the logits. All calls share the one array:
+ *   calls issued in order on one stream follow each other (the memset waits
+ *   for the previous kernel), but calls that can run at the same time on the
+ *   GPU (different streams or threads) race on it and must be serialised by
+ *   the caller.
+ *   A timed-out wait inside the kernel leaves ids/weights unwritten and is not
+ *   reported. No memory is allocated or freed.
+ */
+flint_status_t flint_moe_route_static(const flint_bf16* x, int T, int H, const flint_bf16* router_w, int E,
+                                      const float* bias, int k, int32_t* ids, float* weights, unsigned flags,
+                                      void* stream);
+
+/*
  * flint_moe_gate_up -- for every token and every selected expert (and the
  * shared expert): g = bf16(ts_g * Wg x), u = bf16(ts_u * Wu x),
  * h = bf16(silu(g) * u), with FP32 accumulation. Reads only the distinct

@@ -428,3 +428,84 @@ flint_status_t flint_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t b
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Router without a caller-provided workspace.
+//
+// Its scratch (the router's arrival counter and status word, then FP32 logits
+// for up to FLINT_MAX_TOKENS tokens x FLINT_MAX_EXPERTS experts) lives in the
+// array below, which every device that loads this library keeps until the
+// process exits. Host code cannot use the array's name as a device address:
+// the address comes from cudaGetSymbolAddress, once per device.
+// ---------------------------------------------------------------------------
+constexpr size_t kRouteStaticScratchBytes =
+    flint::kWsHeader + sizeof(float) * FLINT_MAX_TOKENS * FLINT_MAX_EXPERTS;  // 33,024 bytes
+static __device__ __align__(256) unsigned char g_route_static_scratch[kRouteStaticScratchBytes];
+
+namespace {
+
+// Device address of the scratch array on the current device (looked up on
+// the first call on each device, with that device current).
+flint_status_t route_static_scratch(const DevInfo& d, void** out) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (d.device < 0 || d.device >= 64) return fail(FLINT_ERR_UNSUPPORTED, "device index %d above 63", d.device);
+    if (!addr[d.device]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_route_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the router scratch");
+        addr[d.device] = p;
+    }
+    *out = addr[d.device];
+    return FLINT_OK;
+}
+
+}  // namespace
+
+extern "C" flint_status_t flint_moe_route_static(const flint_bf16* x, int T, int H, const flint_bf16* router_w, int E,
+                                                 const float* bias, int k, int32_t* ids, float* weights,
+                                                 unsigned flags, void* stream) {
+    if (T < 1 || T > FLINT_MAX_TOKENS)
+        return fail(FLINT_ERR_UNSUPPORTED, "route_static: T=%d outside 1..%d", T, FLINT_MAX_TOKENS);
+    if (H <= 0 || H % 256) return fail(FLINT_ERR_UNSUPPORTED, "route_static: H=%d must be a positive multiple of 256", H);
+    if (E < 1) return fail(FLINT_ERR_INVALID_ARG, "route_static: E=%d", E);
+    if (flint::kWsHeader + sizeof(float) * (size_t)T * (size_t)E > kRouteStaticScratchBytes)
+        return fail(FLINT_ERR_UNSUPPORTED,
+                    "route_static: %d tokens x %d experts need %zu bytes of scratch; the static scratch holds %zu "
+                    "(at most %d experts for %d tokens)",
+                    T, E, flint::kWsHeader + sizeof(float) * (size_t)T * (size_t)E, kRouteStaticScratchBytes,
+                    (int)((kRouteStaticScratchBytes - flint::kWsHeader) / sizeof(float) / T), T);
+    if (k < 1 || k > FLINT_MAX_TOPK || k > E)
+        return fail(FLINT_ERR_UNSUPPORTED, "route_static: k=%d outside 1..min(%d, E)", k, FLINT_MAX_TOPK);
+    if (!x || !router_w || !ids || !weights || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) ||
+        !aligned(weights, 4) || (bias && !aligned(bias, 4)))
+        return fail(FLINT_ERR_INVALID_ARG, "route_static: null or misaligned pointer");
+    DevInfo d;
+    flint_status_t s = device_info(d);
+    if (s != FLINT_OK) return s;
+    void* scratch = nullptr;
+    if ((s = route_static_scratch(d, &scratch)) != FLINT_OK) return s;
+    // The counter must start at zero; the array keeps whatever the last call left.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, flint::kWsHeader, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "route_static: clearing the scratch header");
+    flint::RouteArgs a = {};
+    a.x = x;
+    a.T = T;
+    a.H = H;
+    a.wr = router_w;
+    a.E = E;
+    a.bias = bias;
+    a.k = k;
+    a.ids = ids;
+    a.weights = weights;
+    a.logits = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + flint::kWsHeader);
+    a.counter = reinterpret_cast<uint32_t*>(scratch);
+    a.status = ws_status(scratch);
+    a.rows_per_cta = ceil_div(E, d.sm_count);
+    const size_t smem = flint::route_smem_bytes(a);
+    if (smem + 1024 > (size_t)d.smem_optin || (size_t)a.rows_per_cta * H * 2 >= (1u << 20))
+        return fail(FLINT_ERR_UNSUPPORTED, "route_static: H=%d too large for one CTA's shared memory", H);
+    e = flint::launch_route(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "route_static launch");
+}

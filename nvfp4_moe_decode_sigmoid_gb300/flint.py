@@ -75,6 +75,7 @@ def _load():
                                    sz, u32, vp]),
         "flint_dense_gemv": (i32, [vp, i32, C.POINTER(flint_packed), i32, vp, vp, sz, u32, vp]),
         "flint_selftest_wait_timeout": (i32, [vp, sz, C.c_uint64, vp]),
+        "flint_moe_route_static": (i32, [vp, i32, i32, vp, i32, vp, i32, vp, vp, u32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -256,6 +257,15 @@ def flint_dense_gemv(x, W: Packed, y, epilogue=FLINT_EPILOGUE_NONE, ws=None, fla
     wsb = ws.numel() * ws.element_size() if ws is not None else 0
     _check(_lib.flint_dense_gemv(_ptr(x), T, C.byref(W.struct), epilogue, _ptr(y), _ptr(ws), wsb, flags,
                                  _stream(stream)), "dense_gemv")
+
+
+def flint_moe_route_static(x, router_w, k, ids, weights, bias=None, flags=0, stream=None):
+    """flint_moe_route for callers that cannot hand the library a workspace:
+    the scratch is a fixed array inside the library (see include/flint.h)."""
+    T, H = x.shape
+    E = router_w.shape[0]
+    _check(_lib.flint_moe_route_static(_ptr(x), T, H, _ptr(router_w), E, _ptr(bias), k, _ptr(ids), _ptr(weights),
+                                       flags, _stream(stream)), "moe_route_static")
 
 
 def flint_selftest_wait_timeout(ws, budget_ns: int, stream=None):
