@@ -98,42 +98,60 @@ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 // Shared memory a launch may take, leaving room for the kernel's static data.
 constexpr size_t kSmemSlack = 1024;
 
-// Ring depth of the gate/up kernel: enough stages for the largest per-CTA
-// share of the work (at most 4), reduced until the CTA fits in shared memory.
-// Returns 0 when not even one stage fits.
-int gate_up_stages(flint::GateUpArgs& a, bool pair, int sm_count, int smem_optin) {
-    const long long items = ceil_div(a.Is, sm_count) + ceil_div((long long)a.T * a.k * a.I, sm_count) + 1;
-    int ns = ceil_div(items, flint::kConsumerWarps);
-    ns = ns < 1 ? 1 : (ns > 4 ? 4 : ns);
-    for (; ns >= 1; --ns) {
-        a.nstages = ns;
-        if (flint::gate_up_smem_bytes(a, pair) + kSmemSlack <= (size_t)smem_optin) return ns;
-    }
-    return 0;
-}
-
-// Shapes of the down kernel; returns false when the layer does not fit.
-bool down_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
-    const int kmin = (a.I > 0 && a.Is > 0) ? (a.I < a.Is ? a.I : a.Is) : (a.I > 0 ? a.I : a.Is);
-    a.lpr = 32;
-    while (a.lpr > 8 && (kmin / 32) % a.lpr) a.lpr /= 2;
-    const int rows_per_task = 2 * (32 / a.lpr);
-    a.rows_max = ceil_div(a.H, sm_count);
-    const long long rs_r = a.I > 0 ? flint::nvfp4_row_stride(a.I) : 0;
-    const long long rs_s = a.Is > 0 ? flint::nvfp4_row_stride(a.Is) : 0;
-    a.slot_bytes = (int)((rows_per_task < a.rows_max ? rows_per_task : a.rows_max) * (rs_r > rs_s ? rs_r : rs_s));
-    const int units = a.T * a.k + (a.s_down ? 1 : 0);
-    const long long tasks = (long long)units * ceil_div(a.rows_max, rows_per_task);
-    int ns = ceil_div(tasks, flint::kConsumerWarps);
-    ns = ns < 1 ? 1 : (ns > 4 ? 4 : ns);
-    for (; ns >= 1; --ns) {
-        a.nstages = ns;
-        if (flint::down_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin) return true;
+// Per-warp ring of the gate/up kernel: prefers two or three slots per warp
+// (a copy in flight while the previous slot is computed) of one pair each,
+// then fewer, until the CTA fits in shared memory. `items` bounds the work
+// items of one CTA (their raw sums stay in shared memory). Returns false when
+// nothing fits.
+bool gate_up_shape(flint::GateUpArgs& a, bool pair, int sm_count, int smem_optin, long long items) {
+    a.res_items = (int)items;
+    const long long per_cta = items;
+    const int per_warp = ceil_div(per_cta, flint::kGemvWarps);
+    const int want = per_warp < 1 ? 1 : (per_warp > 3 ? 3 : per_warp);
+    for (int ns = want; ns >= 1; --ns) {
+        for (int sp = 1; sp <= 2; ++sp) {
+            if (sp > 1 && ns > 1) continue;  // two pairs per slot only as a last resort
+            a.slot_pairs = sp;
+            a.nslots = ns;
+            if (flint::gate_up_smem_bytes(a, pair, sm_count) + kSmemSlack <= (size_t)smem_optin) return true;
+        }
     }
     return false;
 }
 
-bool lpr_ok(int K, int lpr) { return K == 0 || ((K / 32) % lpr == 0); }
+// Shapes of the down kernel: tasks of 16 rows when every task of a warp can
+// be in flight at once, else whichever of 16 or 8 rows keeps the larger share
+// of a warp's tasks in flight (up to 3 slots per warp). Returns false when
+// the layer does not fit.
+bool down_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
+    a.rows_max = ceil_div(a.H, sm_count);
+    const long long rs_r = a.I > 0 ? flint::nvfp4_row_stride(a.I) : 0;
+    const long long rs_s = a.Is > 0 ? flint::nvfp4_row_stride(a.Is) : 0;
+    const long long rs = rs_r > rs_s ? rs_r : rs_s;
+    const int units = (a.T * a.k < a.E ? a.T * a.k : a.E) + (a.Is > 0 ? 1 : 0);
+    bool found = false;
+    double best_cover = -1.0;
+    flint::DownArgs best = a;
+    for (int rg : {16, 8}) {
+        const int per_warp = ceil_div((long long)units * ceil_div(a.rows_max, rg), flint::kGemvWarps);
+        for (int ns = per_warp < 3 ? per_warp : 3; ns >= 1; --ns) {
+            flint::DownArgs t = a;
+            t.rg = rg;
+            t.nslots = ns;
+            t.slot_bytes = (int)(rg * rs);
+            if (flint::down_smem_bytes(t) + kSmemSlack > (size_t)smem_optin) continue;
+            const double cover = (double)ns / per_warp;
+            if (cover > best_cover + 1e-9) {
+                best = t;
+                best_cover = cover;
+                found = true;
+            }
+            break;
+        }
+    }
+    if (found) a = best;
+    return found;
+}
 
 }  // namespace
 
@@ -315,7 +333,10 @@ flint_status_t flint_moe_gate_up(const flint_bf16* x, int T, const int32_t* ids,
     a.h_routed = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.h_routed_off);
     a.h_shared = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.h_shared_off);
     a.status = ws_status(ws);
-    if (!gate_up_stages(a, true, d.sm_count, d.smem_optin))
+    a.x_early = (flags & FLINT_PDL) && (flags & FLINT_PDL_AFTER_ROUTE);
+    const long long routed_pairs = (long long)(T * k < a.E ? T * k : a.E) * a.I;
+    if (!gate_up_shape(a, true, d.sm_count, d.smem_optin,
+                       ceil_div(a.Is, d.sm_count) + ceil_div(routed_pairs, d.sm_count)))
         return fail(FLINT_ERR_UNSUPPORTED, "gate_up: shapes exceed one CTA's shared memory");
     cudaError_t e = flint::launch_gate_up(a, true, d, (flags & FLINT_PDL) != 0, as_stream(stream));
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "gate_up launch");
@@ -352,8 +373,6 @@ flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* we
     a.status = ws_status(ws);
     if (!down_shape(a, d.sm_count, d.smem_optin))
         return fail(FLINT_ERR_UNSUPPORTED, "down_combine: shapes exceed one CTA's shared memory");
-    if (!lpr_ok(a.I, a.lpr) || !lpr_ok(a.Is, a.lpr))
-        return fail(FLINT_ERR_UNSUPPORTED, "down_combine: inter sizes %d and %d are incompatible", a.I, a.Is);
     cudaError_t e = flint::launch_down(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "down_combine launch");
 }
@@ -400,10 +419,11 @@ flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* 
     a.s_ts = W->tensor_scale;
     a.status = status;
     // Tokens go in groups small enough that their FP32 copy fits beside the ring.
+    const int items = ceil_div(n_out, d.sm_count);
     int tg = T;
     for (; tg >= 1; --tg) {
         a.T = tg;
-        if (gate_up_stages(a, pair, d.sm_count, d.smem_optin)) break;
+        if (gate_up_shape(a, pair, d.sm_count, d.smem_optin, items)) break;
     }
     if (tg < 1) return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: K=%d exceeds one CTA's shared memory", K);
     cudaError_t e = cudaSuccess;
@@ -411,7 +431,7 @@ flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* 
         a.T = T - t0 < tg ? T - t0 : tg;
         a.x = x + (size_t)t0 * K;
         a.h_shared = y + (size_t)t0 * n_out;
-        if (!gate_up_stages(a, pair, d.sm_count, d.smem_optin))
+        if (!gate_up_shape(a, pair, d.sm_count, d.smem_optin, items))
             return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: K=%d exceeds one CTA's shared memory", K);
         e = flint::launch_gate_up(a, pair, d, pdl, as_stream(stream));
     }

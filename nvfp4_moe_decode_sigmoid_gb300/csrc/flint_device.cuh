@@ -47,14 +47,22 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// One bounded try: the thread may sleep up to ~20 us inside the instruction
+// until the phase completes (so waiting warps do not spin on the issue slots).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
         : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000)
         : "memory");
     return done != 0;
+}
+
+// Orders this thread's earlier generic-proxy accesses of shared memory before
+// later async-proxy (bulk copy) writes to it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -148,6 +156,44 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+
+// 8 codes of one 32-bit word -> 4 f16x2 registers (exact; byte b: codes 2b, 2b+1).
+__device__ __forceinline__ void decode_word_h2(uint32_t w, uint32_t (&h)[4]) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
+// acc + a.lo * b.lo and acc + a.hi * b.hi for f16x2 operands, FP32 accumulate.
+// The f16 x f16 product is exact in FP32, so each step rounds once, like an
+// FP32 FMA of the same values.
+__device__ __forceinline__ float fma_lo_f16(uint32_t a, uint32_t b, float acc) {
+    float d;
+    asm("{\n .reg .f16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
+        " fma.rn.f32.f16 %0, a0, b0, %3;\n}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(acc));
+    return d;
+}
+__device__ __forceinline__ float fma_hi_f16(uint32_t a, uint32_t b, float acc) {
+    float d;
+    asm("{\n .reg .f16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
+        " fma.rn.f32.f16 %0, a1, b1, %3;\n}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(acc));
+    return d;
+}
+
+// Two floats -> f16x2 (round to nearest; exact for the scaled activations).
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// One UE4M3 scale byte -> exact float (bit 7 cleared).
+__device__ __forceinline__ float ue4m3_to_float(uint32_t byte) { return ue4m3x2_to_float2(byte & 0xFFu).x; }
 
 // 32 codes of one 16-byte chunk -> 32 floats (code values, no scale).
 __device__ __forceinline__ void decode_chunk(const uint4 q, float (&w)[32]) {

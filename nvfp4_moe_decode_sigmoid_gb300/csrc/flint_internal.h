@@ -32,10 +32,12 @@ enum : uint32_t {
 
 constexpr int kThreads = 256;       // router kernel: 8 warps
 constexpr int kWarps = kThreads / 32;
-// Expert / dense GEMV kernels: 15 consumer warps and one producer warp that
-// issues the bulk copies.
-constexpr int kConsumerWarps = 15;
-constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
+// Expert / dense GEMV kernels: 32 warps, each streaming its own share of the
+// weight rows through a private ring of shared-memory slots (so 32 threads per
+// SM issue bulk copies: one issuing thread alone cannot keep HBM busy).
+constexpr int kGemvWarps = 32;
+constexpr int kGemvThreads = kGemvWarps * 32;
+constexpr int kMaxSlotsPerWarp = 4;
 constexpr size_t kWsHeader = 256;   // counter (word 0), status (word 1)
 
 FLINT_HD constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -90,7 +92,10 @@ struct GateUpArgs {
     uint16_t* h_routed; // [8][k][I]
     uint16_t* h_shared; // [T][Is]: h of the shared expert, or the dense output y
     uint32_t* status;
-    int nstages;        // ring depth
+    int nslots;         // ring slots per warp
+    int slot_pairs;     // items (pairs or rows) per slot
+    int res_items;      // bound on the items of one CTA (shared-memory sums)
+    int x_early;        // x is complete before the PDL wait (previous kernel: the router)
 };
 
 // Down + combine of the MoE layer.
@@ -108,10 +113,10 @@ struct DownArgs {
     const uint16_t* h_shared; // [T][Is]
     uint16_t* y;              // [T][H]
     uint32_t* status;
-    int lpr;                  // lanes per row group: 8, 16 or 32
-    int nstages;
+    int rg;                   // rows per task: 8 or 16
+    int nslots;               // ring slots per warp
     int rows_max;             // largest row slice of any CTA
-    int slot_bytes;           // bytes of one task's rows in a stage
+    int slot_bytes;           // bytes of one slot
 };
 
 // ---------------------------------------------------------------------------
@@ -148,10 +153,8 @@ cudaError_t configure_smem(K kernel, const DevInfo& d, int& configured_for) {
     return e;
 }
 
-size_t gate_up_smem_bytes(const GateUpArgs& a, bool pair);
-size_t gate_up_stage_bytes(int H, bool pair);
+size_t gate_up_smem_bytes(const GateUpArgs& a, bool pair, int grid);
 size_t down_smem_bytes(const DownArgs& a);
-size_t down_stage_bytes(const DownArgs& a);
 size_t route_smem_bytes(const RouteArgs& a);
 
 }  // namespace flint

@@ -8,33 +8,48 @@
 // rounding. Section "Model architecture": weight-only NVFP4 (W4A16) with bf16
 // activations; every kernel follows the reference's rounding points.
 //
-// Both kernels are warp-specialised: one producer warp streams weight rows
-// from HBM into a ring of shared-memory stages with 1-D bulk (TMA) copies
-// (full/empty mbarriers), and 15 consumer warps dequantise in registers
-// (cvt e2m1x2 -> f16x2 -> f32 pairs, UE4M3 block scale once per 16 values)
-// and accumulate exact products in FP32 with packed f32x2 FMAs. Activations
-// are staged in shared memory as FP32 in a lane-interleaved order, so lane l
-// reads consecutive 16-byte words (no bank conflicts, no address math).
+// Both kernels run one CTA of 32 warps per SM. Each warp streams its own work
+// items (weight rows) through a private ring of shared-memory slots with 1-D
+// bulk (TMA) copies completed on per-slot mbarriers, so 32 threads per SM
+// issue copies (one issuing thread manages only a few copies per
+// microsecond). Dequantisation happens in registers: cvt e2m1x2 gives exact
+// f16 code values, which multiply f16 activations in mixed-precision FMAs
+// accumulating in FP32 (an f16 x f16 product is exact in FP32, so every step
+// rounds once, as an FP32 FMA of the same values would). The UE4M3 block
+// scale is applied once per 16 values.
 //
-// gate_up_kernel<PAIR=true>: per (selected expert, h index i) "pair" one warp
-//   dots gate row i and up row i with every token that selected the expert,
-//   then g = bf16(ts_g acc_g), u = bf16(ts_u acc_u), h = bf16(silu(g) u).
-//   The pair space (shared expert first, then the distinct selected experts in
-//   ascending id order) is split evenly over one CTA per SM. The shared
-//   expert's rows are requested before the PDL wait.
+// Activations (x for gate/up, h for down) are staged in shared memory as f16:
+// every 32-value chunk is multiplied by the power of two that puts its largest
+// magnitude in [2^14, 2^15), which keeps every bf16 value of the chunk down to
+// 2^-31 of that maximum exact (smaller ones are off by at most 2^-39 of it),
+// and the chunk's partial dot product is multiplied back by the inverse power
+// of two (exact). The staging order puts each lane's 16-byte words side by
+// side, so the warp's shared-memory loads are conflict-free.
+//
+// gate_up_kernel<PAIR=true>: per (selected expert, h index p) "pair" one warp
+//   dots gate row p and up row p with every token that selected the expert
+//   (two tokens per pass), the lanes splitting the columns. The pairs of the
+//   distinct selected experts (ascending id) are split evenly over the CTAs
+//   and then over the warps; the CTA's slice of the shared expert is
+//   requested before the PDL wait. The raw sums go to shared memory; once the
+//   CTA is done, all its threads apply g = bf16(ts_g acc_g),
+//   u = bf16(ts_u acc_u), h = bf16(silu(g) u) and write h.
 // gate_up_kernel<PAIR=false>: the same machinery over plain rows: the dense
 //   GEMV y = bf16(ts W x).
-// down_kernel: each CTA owns a slice of output rows of every selected expert's
-//   down matrix (and the shared one), computes d = bf16(ts_d Wd h) for all of
-//   them, then the combine y = bf16(sum_j w_j d_j + d_shared) in rank order.
-//   No atomics: the result is deterministic. Its weight rows are requested
-//   before the PDL wait (the routing is final by then).
+// down_kernel: each CTA owns a slice of output rows of every selected
+//   expert's down matrix (and the shared one). A task is (expert, group of up
+//   to 16 of those rows); one warp computes d = bf16(ts_d Wd h) for the group,
+//   the lanes splitting the 16-value blocks of the row, and a reduce-scatter
+//   of the per-row sums over the lanes. Then the CTA combines
+//   y = bf16(sum_j w_j d_j + d_shared) in rank order. No atomics: the result is
+//   deterministic. Weight rows are requested before the PDL wait (the routing
+//   is final by then).
 #include "flint_device.cuh"
 
 namespace flint {
 namespace {
 
-constexpr int kCW = kConsumerWarps;
+constexpr int kW = kGemvWarps;
 constexpr int kMaxDistinct = FLINT_MAX_TOKENS * FLINT_MAX_TOPK;
 
 // Per-CTA view of the routing: the distinct selected experts in ascending id
@@ -44,6 +59,7 @@ struct RouteInfo {
     uint32_t base[FLINT_MAX_EXPERTS / 32];
     int32_t dlist[kMaxDistinct];
     unsigned long long dmask[kMaxDistinct];  // byte t: ranks j with ids[t][j] == dlist[d]
+    uint32_t tmask[kMaxDistinct];            // bit t: token t chose dlist[d]
     int32_t ids[kMaxDistinct];               // ids[t*k+j], -1 if out of range
     int D;
 };
@@ -51,7 +67,10 @@ struct RouteInfo {
 __device__ void build_route_info(RouteInfo& ri, const int32_t* ids, int T, int k, int E, uint32_t* status) {
     const int tid = threadIdx.x, nt = blockDim.x;
     for (int i = tid; i < FLINT_MAX_EXPERTS / 32; i += nt) ri.bitmap[i] = 0;
-    for (int i = tid; i < kMaxDistinct; i += nt) ri.dmask[i] = 0ull;
+    for (int i = tid; i < kMaxDistinct; i += nt) {
+        ri.dmask[i] = 0ull;
+        ri.tmask[i] = 0u;
+    }
     __syncthreads();
     int e = -1;
     if (tid < T * k) {
@@ -83,305 +102,437 @@ __device__ void build_route_info(RouteInfo& ri, const int32_t* ids, int T, int k
         const int t = tid / k, j = tid % k;
         ri.dlist[d] = e;
         atomicOr(&ri.dmask[d], 1ull << (8 * t + j));
+        atomicOr(&ri.tmask[d], 1u << t);
     }
     __syncthreads();
-}
-
-__device__ __forceinline__ uint32_t token_mask(unsigned long long dm) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int t = 0; t < FLINT_MAX_TOKENS; ++t) m |= ((dm >> (8 * t)) & 0xFFull) ? (1u << t) : 0u;
-    return m;
 }
 
 __device__ __forceinline__ uint32_t rank_bits(unsigned long long dm, int t) {
     return (uint32_t)((dm >> (8 * t)) & 0xFFull);
 }
 
-template <int W>
-__device__ __forceinline__ float group_sum(float v) {
-#pragma unroll
-    for (int off = W / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    return v;
-}
-
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.f + expf(-g)); }
 
-// Token list of a bitmask, in ascending order, into compile-time slots.
-template <int NT>
-__device__ __forceinline__ void token_list(uint32_t mask, int (&tok)[NT]) {
+// acc0/acc1 += the 8 products of one code word (4 f16x2) with its 8
+// activations (one 16-byte word of 4 f16x2).
+__device__ __forceinline__ void fma8(const uint32_t (&c)[4], const uint4 xv, float& acc0, float& acc1) {
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        tok[j] = mask ? __ffs(mask) - 1 : 0;
-        mask &= mask - 1u;
+    for (int q = 0; q < 4; ++q) {
+        acc0 = fma_lo_f16(c[q], xw[q], acc0);
+        acc1 = fma_hi_f16(c[q], xw[q], acc1);
     }
 }
 
-// FP32 activations of one token, lane-interleaved for `lanes` lanes per row:
-// 16-byte word i (0..7) of the 32-value chunk cidx = gl + lanes * m sits at
-// word index (m * 8 + i) * lanes + gl.
-__device__ __forceinline__ int interleaved_word(int g, int lanes) {
-    const int cidx = g >> 3, i = g & 7;
-    return ((cidx / lanes) * 8 + i) * lanes + (cidx % lanes);
+// Sums each of M values (M a power of two, at most 32) over the warp's lanes.
+// Halving steps: at offset 16 >> s the lanes with that bit set keep the upper
+// half of their remaining values and hand the lower half to their partner
+// (one shuffle per value kept), so M sums cost about M shuffles instead of
+// 5 M. Lane l ends up with the sum of value rs_index<M>(l); 32 / M lanes hold
+// each value.
+template <int M>
+__device__ __forceinline__ float reduce_scatter(float (&v)[M], int lane) {
+#pragma unroll
+    for (int s = 0; (M >> s) > 1; ++s) {
+        const int w = M >> s, off = 16 >> s;
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < w / 2; ++i) {
+            const float keep = up ? v[i + w / 2] : v[i];
+            const float send = up ? v[i] : v[i + w / 2];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int off = 16 / M; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    return r;
 }
 
-// Dot products of 8 decoded code pairs (16 values, one scale block) with 16
-// activations (4 float4 words, stride `ws` float4 between words).
-__device__ __forceinline__ float dot16(const float2* w, const float4* x, int ws) {
-    float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
+template <int M>
+__device__ __forceinline__ int rs_index(int lane) {
+    int idx = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 x4 = x[i * ws];
-        a = __ffma2_rn(w[2 * i], make_float2(x4.x, x4.y), a);
-        b = __ffma2_rn(w[2 * i + 1], make_float2(x4.z, x4.w), b);
+    for (int s = 0; (M >> s) > 1; ++s)
+        if (lane & (16 >> s)) idx += M >> (s + 1);
+    return idx;
+}
+
+// ===========================================================================
+// Activation staging: bf16 vectors in global memory -> chunk-scaled f16 in
+// shared memory. One thread moves one 32-value chunk (its four 16-byte loads
+// issued together). csc[v * (K / 32) + c] = 2^s multiplies chunk c's partial
+// dot product back.
+//   GATE order (K % 1024 == 0): word w (0..3, 8 values each) of chunk c at
+//     16-byte index (c / 32) * 128 + w * 32 + c % 32 of the vector: lane l
+//     reads chunk l + 32 m's words at (m * 4 + w) * 32 + l.
+//   DOWN order (K % 32 == 0): the two words of 16-value block b at indices b
+//     and nb + b (nb = K / 16): lane l reads block l + 32 m at l + 32 m and
+//     nb + l + 32 m.
+// ===========================================================================
+template <bool DOWN_ORDER>
+__device__ __forceinline__ void stage_f16(uint4* dst, float* csc, const uint16_t* src, int nvec, int K) {
+    const int cpv = K / 32;
+    for (int q = threadIdx.x; q < nvec * cpv; q += kGemvThreads) {
+        const int v = q / cpv, c = q - v * cpv;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)v * K + 32 * c);
+        uint4 w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = ld_cg(s4 + i);
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m2 = __vmaxu2(m2, w[i].x & 0x7FFF7FFFu);
+            m2 = __vmaxu2(m2, w[i].y & 0x7FFF7FFFu);
+            m2 = __vmaxu2(m2, w[i].z & 0x7FFF7FFFu);
+            m2 = __vmaxu2(m2, w[i].w & 0x7FFF7FFFu);
+        }
+        // bf16 exponent field of the largest magnitude -> s with max * 2^-s in [2^14, 2^15)
+        const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+        const int s = min(126, max(-126, (int)(m >> 7) - 141));
+        const float down = __int_as_float((127 - s) << 23);
+        csc[q] = __int_as_float((127 + s) << 23);
+        uint4* d = dst + (size_t)v * (K / 8);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            int idx;
+            if (DOWN_ORDER) {
+                idx = (i & 1) * (K / 16) + 2 * c + (i >> 1);
+            } else {
+                idx = (c / 32) * 128 + i * 32 + c % 32;
+            }
+            d[idx] = make_uint4(f32x2_to_f16x2(bf16_lo(w[i].x) * down, bf16_hi(w[i].x) * down),
+                                f32x2_to_f16x2(bf16_lo(w[i].y) * down, bf16_hi(w[i].y) * down),
+                                f32x2_to_f16x2(bf16_lo(w[i].z) * down, bf16_hi(w[i].z) * down),
+                                f32x2_to_f16x2(bf16_lo(w[i].w) * down, bf16_hi(w[i].w) * down));
+        }
     }
-    const float2 s = __fadd2_rn(a, b);
-    return s.x + s.y;
+}
+
+// Lane 0 of a warp whose bounded wait gave up: waits (again bounded) for the
+// copies it still has in flight, slots [k0, k1) of its ring, so that none
+// lands in shared memory after the CTA has exited.
+__device__ __forceinline__ void drain_slots(uint64_t* bar, int nslots, int k0, int k1) {
+    for (int k = k0; k < k1; ++k) mbar_wait_bounded(&bar[k % nslots], (uint32_t)((k / nslots) & 1), nullptr, 0u);
 }
 
 // ===========================================================================
 // gate/up + SiLU (PAIR) or plain rows
 // ===========================================================================
+// Shared memory: mbarriers (kMaxSlotsPerWarp per warp + one for the shared
+// expert), routing view, chunk scales, f16 activations, raw sums [item][T]
+// (gate, then up), the CTA's slice of the shared expert (MoE only), the
+// warps' slot rings.
 struct GateUpSmem {
-    size_t route, xs, ring, stage, total;
+    size_t route, csc, xs, resg, resu, shared, ring, slot, total;
 };
 template <bool PAIR>
-__host__ __device__ inline GateUpSmem gate_up_layout(int T, int H, int nstages) {
+__host__ __device__ inline GateUpSmem gate_up_layout(int T, int H, int shared_pairs, int items, int nslots,
+                                                     int slot_pairs) {
     GateUpSmem L;
-    L.route = 128;
-    L.xs = align_up(L.route + sizeof(RouteInfo), 128);
-    L.ring = align_up(L.xs + sizeof(float) * (size_t)T * H, 128);
-    L.stage = (size_t)(PAIR ? 2 : 1) * kCW * nvfp4_row_stride(H);
-    L.total = L.ring + (size_t)nstages * L.stage;
+    L.route = align_up(8 * (kW * kMaxSlotsPerWarp + 1), 128);
+    L.csc = align_up(L.route + sizeof(RouteInfo), 128);
+    L.xs = align_up(L.csc + sizeof(float) * (size_t)T * (H / 32), 128);
+    L.resg = align_up(L.xs + 2 * (size_t)T * H, 128);
+    L.resu = align_up(L.resg + sizeof(float) * (size_t)items * T, 128);
+    L.shared = align_up(L.resu + (PAIR ? sizeof(float) * (size_t)items * T : 0), 128);
+    L.ring = align_up(L.shared + (size_t)(PAIR ? 2 : 1) * shared_pairs * nvfp4_row_stride(H), 128);
+    L.slot = (size_t)(PAIR ? 2 : 1) * slot_pairs * nvfp4_row_stride(H);
+    L.total = L.ring + (size_t)kW * nslots * L.slot;
     return L;
 }
 
-// One item: rows grow (and urow) against the NT tokens of `mask`; lane t < n
-// ends up holding the warp-reduced sums of token tok[t].
+// One pass of a warp over gate row `grow` (and up row `urow`) against the NT
+// (1 or 2) tokens tk[]: the lanes split the row into 32-value chunks
+// (lane l: chunks l, l + 32, ...); the per-lane sums are reduce-scattered and
+// the lanes holding them store the raw sums (before the tensor scale) at
+// resg[t] / resu[t].
 template <bool PAIR, int NT>
-__device__ __forceinline__ void gate_up_item(const uint8_t* grow, const uint8_t* urow, int H, const float* xs,
-                                             uint32_t mask, int lane, int (&tok)[8], float& gout, float& uout) {
-    int tk[NT];
-    token_list<NT>(mask, tk);
-    const int n = __popc(mask);
-    float ga[NT], ua[NT];
+__device__ __forceinline__ void gate_up_pass(const uint8_t* grow, const uint8_t* urow, int H, const uint4* xh,
+                                             const float* csc, const int (&tk)[NT], int lane, float* resg,
+                                             float* resu) {
+    constexpr int M = PAIR ? 2 * NT : NT;
+    const uint4* xb[NT];
+    const float* cb[NT];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) ga[j] = ua[j] = 0.f;
+    for (int j = 0; j < NT; ++j) {
+        xb[j] = xh + (size_t)tk[j] * (H / 8) + lane;
+        cb[j] = csc + (size_t)tk[j] * (H / 32) + lane;
+    }
+    const uint4* g4 = reinterpret_cast<const uint4*>(grow) + lane;
+    const uint4* u4 = reinterpret_cast<const uint4*>(urow) + lane;
+    const uint16_t* gsc = reinterpret_cast<const uint16_t*>(grow + H / 2) + lane;
+    const uint16_t* usc = reinterpret_cast<const uint16_t*>(urow + H / 2) + lane;
+    float acc[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) acc[i] = 0.f;
     const int nch = H >> 10;
-    const float4* xs4 = reinterpret_cast<const float4*>(xs);
+#pragma unroll 1
     for (int ch = 0; ch < nch; ++ch) {
-        const int c = lane + 32 * ch;
-        const uint4 gq = reinterpret_cast<const uint4*>(grow)[c];
-        const float2 gs = ue4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(grow + H / 2 + 2 * c));
-        uint4 uq = make_uint4(0, 0, 0, 0);
+        const uint4 gq = g4[32 * ch];
+        const float2 gs = ue4m3x2_to_float2(gsc[32 * ch]);
+        uint4 uq = make_uint4(0u, 0u, 0u, 0u);
         float2 us = make_float2(0.f, 0.f);
         if (PAIR) {
-            uq = reinterpret_cast<const uint4*>(urow)[c];
-            us = ue4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(urow + H / 2 + 2 * c));
+            uq = u4[32 * ch];
+            us = ue4m3x2_to_float2(usc[32 * ch]);
         }
+        const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w}, uw[4] = {uq.x, uq.y, uq.z, uq.w};
+        float cg[NT], cu[NT];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            float2 wg[8], wu[8];
-            decode_word(hf ? gq.z : gq.x, wg);
-            decode_word(hf ? gq.w : gq.y, wg + 4);
-            if (PAIR) {
-                decode_word(hf ? uq.z : uq.x, wu);
-                decode_word(hf ? uq.w : uq.y, wu + 4);
+        for (int hf = 0; hf < 2; ++hf) {  // one scale block: code words 2 hf, 2 hf + 1
+            float g0[NT], g1[NT], u0[NT], u1[NT];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) g0[j] = g1[j] = u0[j] = u1[j] = 0.f;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int w = 2 * hf + h2;
+                uint32_t hg[4], hu[4];
+                decode_word_h2(gw[w], hg);
+                if (PAIR) decode_word_h2(uw[w], hu);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const uint4 xv = xb[j][(ch * 4 + w) * 32];
+                    fma8(hg, xv, g0[j], g1[j]);
+                    if (PAIR) fma8(hu, xv, u0[j], u1[j]);
+                }
             }
-            const float sg = hf ? gs.y : gs.x, su = hf ? us.y : us.x;
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-                if (j < n) {
-                    const float4* xp = xs4 + (size_t)tk[j] * (H / 4) + (ch * 8 + hf * 4) * 32 + lane;
-                    ga[j] = fmaf(sg, dot16(wg, xp, 32), ga[j]);
-                    if (PAIR) ua[j] = fmaf(su, dot16(wu, xp, 32), ua[j]);
+                if (hf == 0) {
+                    cg[j] = gs.x * (g0[j] + g1[j]);
+                    if (PAIR) cu[j] = us.x * (u0[j] + u1[j]);
+                } else {
+                    cg[j] = fmaf(gs.y, g0[j] + g1[j], cg[j]);
+                    if (PAIR) cu[j] = fmaf(us.y, u0[j] + u1[j], cu[j]);
                 }
             }
         }
-    }
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        if (j < n) {
-            const float gsum = group_sum<32>(ga[j]);
-            const float usum = PAIR ? group_sum<32>(ua[j]) : 0.f;
-            if (lane == j) {
-                gout = gsum;
-                uout = usum;
-            }
-            tok[j] = tk[j];
+        for (int j = 0; j < NT; ++j) {
+            const float xs = cb[j][32 * ch];
+            acc[j] = fmaf(xs, cg[j], acc[j]);
+            if (PAIR) acc[NT + j] = fmaf(xs, cu[j], acc[NT + j]);
+        }
+    }
+    const float r = reduce_scatter<M>(acc, lane);
+    if (lane % (32 / M) == 0) {
+        const int idx = rs_index<M>(lane);  // [gate of tk[0..NT), up of tk[0..NT)]
+        const int j = idx % NT;
+        int t = tk[0];
+#pragma unroll
+        for (int jj = 1; jj < NT; ++jj)
+            if (j == jj) t = tk[jj];
+        (idx < NT ? resg : resu)[t] = r;
+    }
+}
+
+// All tokens of `tmask` against one item, two per pass.
+template <bool PAIR>
+__device__ __forceinline__ void gate_up_item(const uint8_t* grow, const uint8_t* urow, int H, const uint4* xh,
+                                             const float* csc, uint32_t tmask, int lane, float* resg,
+                                             float* resu) {
+    while (tmask) {
+        const int t0 = __ffs(tmask) - 1;
+        tmask &= tmask - 1u;
+        if (tmask) {
+            const int tk[2] = {t0, __ffs(tmask) - 1};
+            tmask &= tmask - 1u;
+            gate_up_pass<PAIR, 2>(grow, urow, H, xh, csc, tk, lane, resg, resu);
+        } else {
+            const int tk[1] = {t0};
+            gate_up_pass<PAIR, 1>(grow, urow, H, xh, csc, tk, lane, resg, resu);
         }
     }
 }
 
+// MoE (a.gu set): the CTA's slice of the shared expert (pairs [sp0, sp1)) is
+// requested into its own region before the PDL wait and computed by the last
+// warps; the CTA's share of the routed pairs is split over the warps' rings
+// once the routing is read. Dense (a.gu null): the CTA's rows (pairs)
+// [sp0, sp1) of the matrix are split over the warps' rings before the wait.
+// Item i of the CTA (shared-expert pair or dense row i < n_sh, then routed
+// pair n_sh + j) keeps its raw sums at res[i * T + t].
 template <bool PAIR>
 __global__ void __launch_bounds__(kGemvThreads, 1) gate_up_kernel(const GateUpArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int NS = a.nstages, H = a.H, T = a.T, I = a.I, Is = a.Is;
-    const GateUpSmem L = gate_up_layout<PAIR>(T, H, NS);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + 4;
-    RouteInfo& ri = *reinterpret_cast<RouteInfo*>(smem + L.route);
-    float* xs = reinterpret_cast<float*>(smem + L.xs);
-    uint8_t* ring = smem + L.ring;
-    const int RS = (int)nvfp4_row_stride(H);
-    const int half = kCW * RS;  // gate rows of one stage; up rows follow (PAIR)
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int NSW = a.nslots, SP = a.slot_pairs, H = a.H, T = a.T, I = a.I, Is = a.Is;
+    const bool moe = a.gu != nullptr;
     const int c = blockIdx.x, G = gridDim.x;
     const int sp0 = (int)((long long)c * Is / G), sp1 = (int)((long long)(c + 1) * Is / G);
     const int n_sh = a.s_gu ? sp1 - sp0 : 0;
+    const int shp = moe ? (Is + G - 1) / G : 0;
+    const GateUpSmem L = gate_up_layout<PAIR>(T, H, shp, a.res_items, NSW, SP);
+    RouteInfo& ri = *reinterpret_cast<RouteInfo*>(smem + L.route);
+    float* csc = reinterpret_cast<float*>(smem + L.csc);
+    uint4* xh = reinterpret_cast<uint4*>(smem + L.xs);
+    float* resg = reinterpret_cast<float*>(smem + L.resg);
+    float* resu = reinterpret_cast<float*>(smem + L.resu);
+    uint8_t* shreg = smem + L.shared;
+    const int RS = (int)nvfp4_row_stride(H);
+    const int half = SP * RS;  // gate rows of one slot; up rows follow (PAIR)
 
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kCW);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + warp * kMaxSlotsPerWarp;
+    uint64_t* shbar = reinterpret_cast<uint64_t*>(smem) + kW * kMaxSlotsPerWarp;
+    uint8_t* ring = smem + L.ring + (size_t)warp * NSW * L.slot;
+
+    // This warp's list items [lw0, lw1): routed pairs of the CTA (MoE) or rows
+    // of the dense matrix. List item j -> rows of its gate (and up) part.
+    int rp0 = 0, lw0 = 0, lw1 = 0, nl = 0;
+    auto item_rows = [&](int j, const uint8_t*& g, const uint8_t*& u) {
+        if (moe) {
+            const int q = rp0 + j, d = q / I, p = q - d * I;
+            g = a.gu + ((size_t)ri.dlist[d] * 2 * I + p) * RS;
+            u = g + (size_t)I * RS;
+        } else {
+            g = a.s_gu + (size_t)(sp0 + j) * RS;
+            u = a.s_gu + (size_t)(Is + sp0 + j) * RS;
         }
+    };
+    // Lane 0: request slot k (list items [lw0 + k SP, ...)) in runs of
+    // consecutive rows of one matrix; one arrival with the byte count.
+    auto issue = [&](int k) {
+        const int i0 = lw0 + k * SP, i1 = min(lw1, i0 + SP);
+        uint8_t* g = ring + (size_t)(k % NSW) * L.slot;
+        uint64_t* b = &bar[k % NSW];
+        mbar_arrive_expect_tx(b, (uint32_t)((PAIR ? 2 : 1) * (i1 - i0) * RS));
+        int i = i0;
+        while (i < i1) {
+            const uint8_t *g0, *u0;
+            item_rows(i, g0, u0);
+            int j = i + 1;
+            while (j < i1) {
+                const uint8_t *gj, *uj;
+                item_rows(j, gj, uj);
+                if (gj != g0 + (size_t)(j - i) * RS) break;
+                ++j;
+            }
+            const uint32_t n = (uint32_t)((j - i) * RS);
+            bulk_g2s(g + (size_t)(i - i0) * RS, g0, n, b);
+            if (PAIR) bulk_g2s(g + half + (size_t)(i - i0) * RS, u0, n, b);
+            i = j;
+        }
+    };
+
+    if (lane == 0) {
+        for (int s = 0; s < NSW; ++s) mbar_init(&bar[s], 1);
+        if (tid == 0) mbar_init(shbar, 1);
         fence_mbar_init();
     }
     __syncthreads();
-    // Before the wait: the shared expert's (or dense matrix's) rows do not
-    // depend on the routing or on any earlier kernel.
-    if (warp == kCW && lane == 0) {
-        for (int st = 0; st < NS && st * kCW < n_sh; ++st) {
-            const int i0 = st * kCW, n = min(n_sh - i0, kCW);
-            const uint32_t bytes = (uint32_t)(n * RS);
-            uint8_t* g = ring + (size_t)st * L.stage;
-            mbar_expect_tx(&full[st], PAIR ? 2 * bytes : bytes);
-            bulk_g2s(g, a.s_gu + (size_t)(sp0 + i0) * RS, bytes, &full[st]);
-            if (PAIR) bulk_g2s(g + half, a.s_gu + (size_t)(Is + sp0 + i0) * RS, bytes, &full[st]);
+    // Before the wait: weights that depend on no earlier kernel.
+    if (moe) {
+        if (tid == 0 && n_sh > 0) {
+            const uint32_t n = (uint32_t)(n_sh * RS);
+            mbar_arrive_expect_tx(shbar, PAIR ? 2 * n : n);
+            bulk_g2s(shreg, a.s_gu + (size_t)sp0 * RS, n, shbar);
+            if (PAIR) bulk_g2s(shreg + (size_t)shp * RS, a.s_gu + (size_t)(Is + sp0) * RS, n, shbar);
         }
-    }
-    pdl_wait();  // ids and x are written by earlier kernels
-    if (a.gu) {
-        build_route_info(ri, a.ids, T, a.k, a.E, a.status);
     } else {
-        if (tid == 0) ri.D = 0;
-        __syncthreads();
+        lw0 = (int)((long long)warp * n_sh / kW);
+        lw1 = (int)((long long)(warp + 1) * n_sh / kW);
+        if (lane == 0)
+            for (int k = 0; k < NSW && lw0 + k * SP < lw1; ++k) issue(k);
+    }
+    if (a.x_early) stage_f16<false>(xh, csc, a.x, T, H);
+    pdl_wait();  // ids (and x, unless staged already) are written by earlier kernels
+    if (moe) {
+        build_route_info(ri, a.ids, T, a.k, a.E, a.status);
+        const int RP = ri.D * I;
+        rp0 = (int)((long long)c * RP / G);
+        nl = (int)((long long)(c + 1) * RP / G) - rp0;
+        lw0 = (int)((long long)warp * nl / kW);
+        lw1 = (int)((long long)(warp + 1) * nl / kW);
     }
     pdl_launch_dependents();
+    if (moe && lane == 0)
+        for (int k = 0; k < NSW && lw0 + k * SP < lw1; ++k) issue(k);
+    if (!a.x_early) stage_f16<false>(xh, csc, a.x, T, H);
+    __syncthreads();  // activations (and the routing view) visible to all warps
 
-    const int D = ri.D;
-    const long long RP = (long long)D * I;
-    const long long rp0 = (long long)c * RP / G, rp1 = (long long)(c + 1) * RP / G;
-    const int n_items = n_sh + (int)(rp1 - rp0);
-    const int n_stages = (n_items + kCW - 1) / kCW;
-
-    if (warp == kCW) {
-        // ---------------- producer ----------------
-        if (lane == 0) {
-            for (int st = 0; st < n_stages; ++st) {
-                const int b = st % NS;
-                if (st >= NS &&
-                    !mbar_wait_bounded(&empty[b], (uint32_t)(((st / NS) - 1) & 1), a.status, kStatusTimeoutGateUp))
-                    break;
-                uint8_t* g = ring + (size_t)b * L.stage;
-                const int i0 = st * kCW, i1 = min(n_items, i0 + kCW);
-                const bool with_shared = st >= NS;  // the first NS stages' shared rows are in flight
-                for (int pass = 0; pass < 2; ++pass) {  // pass 0 counts bytes, pass 1 copies
-                    uint32_t bytes = 0;
-                    if (with_shared && i0 < n_sh) {
-                        const int n = min(i1, n_sh) - i0;
-                        if (pass) {
-                            bulk_g2s(g, a.s_gu + (size_t)(sp0 + i0) * RS, n * RS, &full[b]);
-                            if (PAIR) bulk_g2s(g + half, a.s_gu + (size_t)(Is + sp0 + i0) * RS, n * RS, &full[b]);
-                        }
-                        bytes += (PAIR ? 2u : 1u) * n * RS;
-                    }
-                    const int ir = max(i0, n_sh);
-                    long long q0 = rp0 + (ir - n_sh);
-                    const long long q1 = rp0 + (i1 - n_sh);
-                    int slot = ir - i0;
-                    while (q0 < q1) {
-                        const int d = (int)(q0 / I), p0 = (int)(q0 % I);
-                        const int n = (int)min((long long)(I - p0), q1 - q0);
-                        if (pass) {
-                            const uint8_t* base = a.gu + (size_t)ri.dlist[d] * 2 * I * RS;
-                            bulk_g2s(g + slot * RS, base + (size_t)p0 * RS, n * RS, &full[b]);
-                            bulk_g2s(g + half + slot * RS, base + (size_t)(I + p0) * RS, n * RS, &full[b]);
-                        }
-                        bytes += 2u * n * RS;
-                        slot += n;
-                        q0 += n;
-                    }
-                    if (!pass) mbar_arrive_expect_tx(&full[b], bytes);
-                }
-            }
+    const uint32_t all_tokens = (1u << T) - 1u;
+    const int n_slots = (lw1 - lw0 + SP - 1) / SP;
+    int k = 0;  // this warp's next slot
+    bool ok = true;
+    // The CTA's shared-expert pairs: pair i is computed by warp kW - 1 - i.
+    if (moe) {
+        for (int i = kW - 1 - warp; i < n_sh && ok; i += kW) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_bounded(shbar, 0, lane == 0 ? a.status : nullptr, kStatusTimeoutGateUp));
+            if (!ok) break;
+            const uint8_t* grow = shreg + (size_t)i * RS;
+            gate_up_item<PAIR>(grow, grow + (size_t)shp * RS, H, xh, csc, all_tokens, lane, resg + i * T,
+                               resu + i * T);
         }
-        return;
     }
-
-    // ---------------- consumers ----------------
-    for (int i = tid; i < T * H / 4; i += kCW * 32) {  // x -> FP32, lane-interleaved
-        const int t = i / (H / 4), g = i % (H / 4);
-        const uint2 v = ld_cg(reinterpret_cast<const uint2*>(a.x + (size_t)t * H) + g);
-        reinterpret_cast<float4*>(xs + (size_t)t * H)[interleaved_word(g, 32)] =
-            make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+    // This warp's slots.
+    int d = 0, p = 0;  // expert index and pair index of the next list item (MoE)
+    if (moe && lw1 > lw0) {
+        d = (rp0 + lw0) / I;
+        p = rp0 + lw0 - d * I;
     }
-    named_sync(1, kCW * 32);
-
-    for (int st = 0; st < n_stages; ++st) {
-        const int b = st % NS;
-        bool ok = mbar_wait_bounded(&full[b], (uint32_t)((st / NS) & 1), lane == 0 ? a.status : nullptr,
-                                    kStatusTimeoutGateUp);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const int item = st * kCW + warp;
-        if (item < n_items) {
-            const uint8_t* grow = ring + (size_t)b * L.stage + warp * RS;
-            const uint8_t* urow = grow + half;
-            const bool shared_item = item < n_sh;
-            int p, e = -1;
-            unsigned long long dm = 0;
-            uint32_t tmask;
-            float tsg, tsu;
-            if (shared_item) {
-                p = sp0 + item;
-                tmask = (1u << T) - 1u;
-                tsg = a.s_ts[0];
-                tsu = PAIR ? a.s_ts[1] : 0.f;
-            } else {
-                const long long q = rp0 + (item - n_sh);
-                const int d = (int)(q / I);
-                p = (int)(q % I);
-                e = ri.dlist[d];
-                dm = ri.dmask[d];
-                tmask = token_mask(dm);
-                tsg = a.ts[3 * e + 0];
-                tsu = a.ts[3 * e + 1];
-            }
-            const int n = __popc(tmask);
-            int tok[8];
-            float gsum = 0.f, usum = 0.f;
-            if (n == 1)
-                gate_up_item<PAIR, 1>(grow, urow, H, xs, tmask, lane, tok, gsum, usum);
-            else if (n == 2)
-                gate_up_item<PAIR, 2>(grow, urow, H, xs, tmask, lane, tok, gsum, usum);
-            else if (n <= 4)
-                gate_up_item<PAIR, 4>(grow, urow, H, xs, tmask, lane, tok, gsum, usum);
-            else
-                gate_up_item<PAIR, 8>(grow, urow, H, xs, tmask, lane, tok, gsum, usum);
-            if (lane < n) {
-                int t = tok[0];
-#pragma unroll
-                for (int j = 1; j < 8; ++j)
-                    if (lane == j) t = tok[j];
-                const float g = bf16_round_f32(tsg * gsum);
-                if (!PAIR) {
-                    a.h_shared[(size_t)t * Is + p] = f32_to_bf16_bits(g);
-                } else {
-                    const float u = bf16_round_f32(tsu * usum);
-                    const uint16_t h = f32_to_bf16_bits(silu_f32(g) * u);
-                    if (shared_item) {
-                        a.h_shared[(size_t)t * Is + p] = h;
-                    } else {
-                        const uint32_t ranks = rank_bits(dm, t);
-                        for (int j = 0; j < a.k; ++j)
-                            if ((ranks >> j) & 1u) a.h_routed[((size_t)t * a.k + j) * I + p] = h;
-                    }
-                }
+    for (; k < n_slots && ok; ++k) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar[k % NSW], (uint32_t)((k / NSW) & 1),
+                                                       lane == 0 ? a.status : nullptr, kStatusTimeoutGateUp));
+        if (!ok) break;
+        const int i0 = lw0 + k * SP, i1 = min(lw1, i0 + SP);
+        const uint8_t* sbuf = ring + (size_t)(k % NSW) * L.slot;
+        for (int j = i0; j < i1; ++j) {
+            const uint8_t* grow = sbuf + (size_t)(j - i0) * RS;
+            const int item = moe ? n_sh + j : j;
+            gate_up_item<PAIR>(grow, grow + half, H, xh, csc, moe ? ri.tmask[d] : all_tokens, lane,
+                               resg + item * T, resu + item * T);
+            if (++p == I) {
+                p = 0;
+                ++d;
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[b]);
+        if (lane == 0 && k + NSW < n_slots) {
+            fence_proxy_async_smem();
+            issue(k + NSW);
+        }
+    }
+    if (__syncthreads_or(!ok)) {  // a wait gave up (the status word says which)
+        if (lane == 0) drain_slots(bar, NSW, k, min(n_slots, k + NSW));
+        if (tid == 0 && n_sh > 0 && moe) mbar_wait_bounded(shbar, 0, nullptr, 0u);
+        return;
+    }
+    // Epilogue over (token, item): tensor scales, bf16 rounding points, SiLU.
+    const int n_items = n_sh + nl;
+    for (int e = tid; e < n_items * T; e += kGemvThreads) {
+        const int t = e / n_items, i = e - t * n_items;
+        float tsg, tsu;
+        int pp;
+        uint32_t ranks = 0;
+        if (i < n_sh) {
+            pp = sp0 + i;
+            tsg = a.s_ts[0];
+            tsu = PAIR ? a.s_ts[1] : 0.f;
+        } else {
+            const int q = rp0 + i - n_sh, dd = q / I;
+            pp = q - dd * I;
+            ranks = rank_bits(ri.dmask[dd], t);
+            if (!ranks) continue;
+            const int ex = ri.dlist[dd];
+            tsg = a.ts[3 * ex + 0];
+            tsu = a.ts[3 * ex + 1];
+        }
+        const float g = bf16_round_f32(tsg * resg[i * T + t]);
+        uint16_t out;
+        if (PAIR) {
+            const float u = bf16_round_f32(tsu * resu[i * T + t]);
+            out = f32_to_bf16_bits(silu_f32(g) * u);
+        } else {
+            out = f32_to_bf16_bits(g);
+        }
+        if (i < n_sh) {
+            a.h_shared[(size_t)t * Is + pp] = out;
+        } else {
+            for (int j = 0; j < a.k; ++j)
+                if ((ranks >> j) & 1u) a.h_routed[((size_t)t * a.k + j) * I + pp] = out;
+        }
     }
 }
 
@@ -389,233 +540,199 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gate_up_kernel(const GateUpAr
 // down + combine
 // ===========================================================================
 struct DownSmem {
-    size_t route, w, dval, hr, hs, ring, stage, total;
+    size_t route, w, csr, css, dval, hr, hs, ring, total;
 };
 __host__ __device__ inline DownSmem down_layout(const DownArgs& a) {
     DownSmem L;
-    L.route = 128;
+    L.route = align_up(8 * kW * kMaxSlotsPerWarp, 128);
     L.w = align_up(L.route + sizeof(RouteInfo), 128);
-    L.dval = align_up(L.w + sizeof(float) * kMaxDistinct, 128);
-    L.hr = align_up(L.dval + sizeof(float) * FLINT_MAX_TOKENS * (FLINT_MAX_TOPK + 1) * (size_t)a.rows_max, 128);
-    L.hs = align_up(L.hr + sizeof(float) * (size_t)a.T * a.k * a.I, 128);
-    L.ring = align_up(L.hs + sizeof(float) * (size_t)a.T * a.Is, 128);
-    L.stage = (size_t)kCW * a.slot_bytes;
-    L.total = L.ring + (size_t)a.nstages * L.stage;
+    L.csr = align_up(L.w + sizeof(float) * kMaxDistinct, 128);
+    L.css = align_up(L.csr + sizeof(float) * (size_t)a.T * a.k * (a.I / 32), 128);
+    L.dval = align_up(L.css + sizeof(float) * (size_t)a.T * (a.Is / 32), 128);
+    L.hr = align_up(L.dval + sizeof(float) * (size_t)a.T * (a.k + 1) * a.rows_max, 128);
+    L.hs = align_up(L.hr + 2 * (size_t)a.T * a.k * a.I, 128);
+    L.ring = align_up(L.hs + 2 * (size_t)a.T * a.Is, 128);
+    L.total = L.ring + (size_t)kW * a.nslots * a.slot_bytes;
     return L;
 }
 
-// One task: rows ra (and rb = ra + 1) of a unit's slice against NT tokens.
-// Lanes of one LPR-group split the row's chunks; every lane does two rows.
-template <int LPR, int NT>
-__device__ __forceinline__ void down_task(const uint8_t* row_a, const uint8_t* row_b, bool has_b, int K,
-                                          const float* const (&hv)[NT], int n, int gl, float (&out_a)[8],
-                                          float (&out_b)[8]) {
-    float aa[NT], ab[NT];
+// One pass of a warp over RP rows (row r at rows + r RS, r < nr valid) of K
+// columns against NT tokens whose staged h vectors are hv[] (DOWN order) with
+// chunk scales cv[]: lane l takes the 16-value blocks l, l + 32, ...
+// acc[j * RP + r] gets the lane's part of row r . h_j.
+template <int RP, int NT>
+__device__ __forceinline__ void down_pass(const uint8_t* rows, int RS, int nr, int K, const uint4* const (&hv)[NT],
+                                          const float* const (&cv)[NT], int lane, float (&acc)[RP * NT]) {
 #pragma unroll
-    for (int j = 0; j < NT; ++j) aa[j] = ab[j] = 0.f;
-    const int cpl = K / 32 / LPR;
-    for (int m = 0; m < cpl; ++m) {
-        const int cidx = gl + LPR * m;
-        const uint4 qa = reinterpret_cast<const uint4*>(row_a)[cidx];
-        const uint4 qb = has_b ? reinterpret_cast<const uint4*>(row_b)[cidx] : make_uint4(0, 0, 0, 0);
-        const float2 sa = ue4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(row_a + K / 2 + 2 * cidx));
-        const float2 sb =
-            has_b ? ue4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(row_b + K / 2 + 2 * cidx)) : make_float2(0, 0);
+    for (int i = 0; i < RP * NT; ++i) acc[i] = 0.f;
+    const int nb = K / 16;
+    for (int b = lane; b < nb; b += 32) {
+        uint4 x0[NT], x1[NT];
+        float xs[NT];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            float2 wa[8], wb[8];
-            decode_word(hf ? qa.z : qa.x, wa);
-            decode_word(hf ? qa.w : qa.y, wa + 4);
-            decode_word(hf ? qb.z : qb.x, wb);
-            decode_word(hf ? qb.w : qb.y, wb + 4);
-            const float s_a = hf ? sa.y : sa.x, s_b = hf ? sb.y : sb.x;
+        for (int j = 0; j < NT; ++j) {
+            x0[j] = hv[j][b];
+            x1[j] = hv[j][nb + b];
+            xs[j] = cv[j][b >> 1];
+        }
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                if (j < n) {
-                    const float4* xp = reinterpret_cast<const float4*>(hv[j]) + (m * 8 + hf * 4) * LPR + gl;
-                    aa[j] = fmaf(s_a, dot16(wa, xp, LPR), aa[j]);
-                    ab[j] = fmaf(s_b, dot16(wb, xp, LPR), ab[j]);
+        for (int r = 0; r < RP; ++r) {
+            if (r < nr) {
+                const uint8_t* row = rows + (size_t)r * RS;
+                const uint2 q = *reinterpret_cast<const uint2*>(row + 8 * b);
+                const float s = ue4m3_to_float(row[K / 2 + b]);
+                uint32_t c0[4], c1[4];
+                decode_word_h2(q.x, c0);
+                decode_word_h2(q.y, c1);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    float p0 = 0.f, p1 = 0.f;
+                    fma8(c0, x0[j], p0, p1);
+                    fma8(c1, x1[j], p0, p1);
+                    acc[j * RP + r] = fmaf(s * xs[j], p0 + p1, acc[j * RP + r]);
                 }
             }
         }
     }
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        if (j < n) {
-            out_a[j] = group_sum<LPR>(aa[j]);
-            out_b[j] = group_sum<LPR>(ab[j]);
-        }
-    }
 }
 
-template <int LPR>
+// Each CTA owns output rows [n0, n1). Units are the distinct selected experts
+// (ascending id) and the shared expert; a task is a group of up to RG of the
+// CTA's rows of one unit. Warp w takes tasks w, w + kW, ... through its own
+// ring; the routing is final before this kernel starts (the gate/up kernel
+// triggers it only after its own wait), so the first slots are requested
+// before the PDL wait.
+template <int RG>
 __global__ void __launch_bounds__(kGemvThreads, 1) down_kernel(const DownArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const DownSmem L = down_layout(a);
-    const int NS = a.nstages;
+    const int NSW = a.nslots;
     const int T = a.T, k = a.k, H = a.H, I = a.I, Is = a.Is, RM = a.rows_max;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + 4;
     RouteInfo& ri = *reinterpret_cast<RouteInfo*>(smem + L.route);
     float* wsm = reinterpret_cast<float*>(smem + L.w);
+    float* csr = reinterpret_cast<float*>(smem + L.csr);    // chunk scales of h_routed [t*k + j][I / 32]
+    float* css = reinterpret_cast<float*>(smem + L.css);    // chunk scales of h_shared [t][Is / 32]
     float* dval = reinterpret_cast<float*>(smem + L.dval);  // [t][j (k = shared)][row]
-    float* hr = reinterpret_cast<float*>(smem + L.hr);      // [t*k + j][I], lane-interleaved
-    float* hs = reinterpret_cast<float*>(smem + L.hs);      // [t][Is], lane-interleaved
-    uint8_t* ring = smem + L.ring;
-    constexpr int kRowsPerTask = 2 * (32 / LPR);
+    uint4* hr = reinterpret_cast<uint4*>(smem + L.hr);      // [t*k + j][I] f16, DOWN order
+    uint4* hs = reinterpret_cast<uint4*>(smem + L.hs);      // [t][Is] f16, DOWN order
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + warp * kMaxSlotsPerWarp;
+    uint8_t* ring = smem + L.ring + (size_t)warp * NSW * a.slot_bytes;
     const int c = blockIdx.x, G = gridDim.x;
     const int n0 = (int)((long long)c * H / G), n1 = (int)((long long)(c + 1) * H / G), nr = n1 - n0;
     const int RSr = (int)nvfp4_row_stride(I), RSs = Is ? (int)nvfp4_row_stride(Is) : 0;
     if (nr == 0) return;  // more CTAs than output rows: nothing to copy or compute
 
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kCW);
-        }
+    if (lane == 0) {
+        for (int s = 0; s < NSW; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
     }
-    // The routing is final before this kernel can start: the gate/up kernel
-    // triggers its dependents only after its own wait on the router.
-    build_route_info(ri, a.ids, T, k, a.E, a.status);  // (contains __syncthreads)
+    build_route_info(ri, a.ids, T, k, a.E, a.status);  // (its __syncthreads also publish the barriers)
     const int D = ri.D;
     const bool has_sh = a.s_down != nullptr;
     const int n_units = D + (has_sh ? 1 : 0);
-    const int tpu = (nr + kRowsPerTask - 1) / kRowsPerTask;  // tasks per unit
-    const int n_tasks = n_units * tpu;
-    const int n_stages = (n_tasks + kCW - 1) / kCW;
+    const int ngr = (nr + RG - 1) / RG;  // row groups per unit
+    const int n_tasks = n_units * ngr;
+    const int my_tasks = n_tasks > warp ? (n_tasks - warp + kW - 1) / kW : 0;
 
-    if (warp == kCW) {
-        // ---------------- producer: weights do not depend on h ----------------
-        if (lane == 0) {
-            for (int st = 0; st < n_stages; ++st) {
-                const int b = st % NS;
-                if (st >= NS &&
-                    !mbar_wait_bounded(&empty[b], (uint32_t)(((st / NS) - 1) & 1), a.status, kStatusTimeoutDown))
-                    break;
-                const int q0 = st * kCW, q1 = min(n_tasks, q0 + kCW);
-                uint32_t bytes = 0;
-                for (int q = q0; q < q1; ++q) {
-                    const int u = q / tpu, r0 = (q % tpu) * kRowsPerTask, r1 = min(nr, r0 + kRowsPerTask);
-                    bytes += (uint32_t)((r1 - r0) * (u < D ? RSr : RSs));
-                }
-                mbar_arrive_expect_tx(&full[b], bytes);
-                for (int q = q0; q < q1; ++q) {
-                    const int u = q / tpu, r0 = (q % tpu) * kRowsPerTask, r1 = min(nr, r0 + kRowsPerTask);
-                    uint8_t* dst = ring + (size_t)b * L.stage + (size_t)(q - q0) * a.slot_bytes;
-                    if (u < D)
-                        bulk_g2s(dst, a.down + ((size_t)ri.dlist[u] * H + n0 + r0) * RSr, (uint32_t)((r1 - r0) * RSr),
-                                 &full[b]);
-                    else
-                        bulk_g2s(dst, a.s_down + (size_t)(n0 + r0) * RSs, (uint32_t)((r1 - r0) * RSs), &full[b]);
-                }
-            }
-        }
-        pdl_wait();
-        pdl_launch_dependents();
-        return;
-    }
+    auto issue = [&](int kk) {  // this warp's kk-th task
+        const int q = warp + kk * kW, u = q / ngr, r0 = (q - u * ngr) * RG, r1 = min(nr, r0 + RG);
+        uint64_t* b = &bar[kk % NSW];
+        uint8_t* dst = ring + (size_t)(kk % NSW) * a.slot_bytes;
+        const int RS = u < D ? RSr : RSs;
+        mbar_arrive_expect_tx(b, (uint32_t)((r1 - r0) * RS));
+        if (u < D)
+            bulk_g2s(dst, a.down + ((size_t)ri.dlist[u] * H + n0 + r0) * RSr, (uint32_t)((r1 - r0) * RSr), b);
+        else
+            bulk_g2s(dst, a.s_down + (size_t)(n0 + r0) * RSs, (uint32_t)((r1 - r0) * RSs), b);
+    };
+    if (lane == 0)
+        for (int kk = 0; kk < min(NSW, my_tasks); ++kk) issue(kk);
 
-    // ---------------- consumers ----------------
     pdl_wait();  // h comes from the gate/up kernel
     pdl_launch_dependents();
-    {  // h -> FP32 in shared memory, lane-interleaved for LPR lanes per row
-        const int gr = I / 4, gsh = Is / 4;
-        for (int i = tid; i < T * k * gr; i += kCW * 32) {
-            const int v = i / gr, g = i % gr;
-            const uint2 hv = ld_cg(reinterpret_cast<const uint2*>(a.h_routed + (size_t)v * I) + g);
-            reinterpret_cast<float4*>(hr + (size_t)v * I)[interleaved_word(g, LPR)] =
-                make_float4(bf16_lo(hv.x), bf16_hi(hv.x), bf16_lo(hv.y), bf16_hi(hv.y));
-        }
-        if (has_sh) {
-            for (int i = tid; i < T * gsh; i += kCW * 32) {
-                const int v = i / gsh, g = i % gsh;
-                const uint2 hv = ld_cg(reinterpret_cast<const uint2*>(a.h_shared + (size_t)v * Is) + g);
-                reinterpret_cast<float4*>(hs + (size_t)v * Is)[interleaved_word(g, LPR)] =
-                    make_float4(bf16_lo(hv.x), bf16_hi(hv.x), bf16_lo(hv.y), bf16_hi(hv.y));
-            }
-        }
-        for (int i = tid; i < T * k; i += kCW * 32) wsm[i] = ld_cg(a.w + i);
-    }
-    named_sync(1, kCW * 32);
+    stage_f16<true>(hr, csr, a.h_routed, T * k, I);
+    if (has_sh) stage_f16<true>(hs, css, a.h_shared, T, Is);
+    for (int i = tid; i < T * k; i += kGemvThreads) wsm[i] = ld_cg(a.w + i);
+    __syncthreads();
 
-    const int grp = lane / LPR, gl = lane % LPR;
-    for (int st = 0; st < n_stages; ++st) {
-        const int b = st % NS;
-        bool ok = mbar_wait_bounded(&full[b], (uint32_t)((st / NS) & 1), lane == 0 ? a.status : nullptr,
-                                    kStatusTimeoutDown);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const int q = st * kCW + warp;
-        if (q < n_tasks) {
-            const int u = q / tpu, r0 = (q % tpu) * kRowsPerTask, r1 = min(nr, r0 + kRowsPerTask);
-            const bool sh = u >= D;
-            const int K = sh ? Is : I, RS = sh ? RSs : RSr;
-            const uint8_t* slot = ring + (size_t)b * L.stage + (size_t)warp * a.slot_bytes;
-            const int ra = r0 + 2 * grp;  // this group's two rows
-            const bool has_a = ra < r1, has_b = ra + 1 < r1;
-            const uint8_t* row_a = slot + (size_t)(has_a ? ra - r0 : 0) * RS;
-            const uint8_t* row_b = slot + (size_t)(has_b ? ra + 1 - r0 : 0) * RS;
-            unsigned long long dm = 0;
-            uint32_t tmask;
-            float tsd;
+    int kk = 0;
+    bool ok = true;
+    for (; kk < my_tasks; ++kk) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar[kk % NSW], (uint32_t)((kk / NSW) & 1),
+                                                       lane == 0 ? a.status : nullptr, kStatusTimeoutDown));
+        if (!ok) break;
+        const int q = warp + kk * kW, u = q / ngr, r0 = (q - u * ngr) * RG, r1 = min(nr, r0 + RG);
+        const bool sh = u >= D;
+        const int K = sh ? Is : I, RS = sh ? RSs : RSr;
+        const uint8_t* slot = ring + (size_t)(kk % NSW) * a.slot_bytes;
+        const unsigned long long dm = sh ? 0ull : ri.dmask[u];
+        uint32_t rest = sh ? (1u << T) - 1u : ri.tmask[u];
+        const float tsd = sh ? a.s_ts[2] : a.ts[3 * ri.dlist[u] + 2];
+        // Token t's staged h vector (and chunk scales) for this unit.
+        auto vec = [&](int t, const uint4*& h, const float*& cs) {
             if (sh) {
-                tmask = (1u << T) - 1u;
-                tsd = a.s_ts[2];
+                h = hs + (size_t)t * (Is / 8);
+                cs = css + (size_t)t * (Is / 32);
             } else {
-                dm = ri.dmask[u];
-                tmask = token_mask(dm);
-                tsd = a.ts[3 * ri.dlist[u] + 2];
+                const int j = __ffs(rank_bits(dm, t)) - 1;
+                h = hr + ((size_t)t * k + j) * (I / 8);
+                cs = csr + ((size_t)t * k + j) * (I / 32);
             }
-            const int n = __popc(tmask);
-            int tok[8];
-            token_list<8>(tmask, tok);
-            float oa[8], ob[8];
-#define FLINT_DOWN_CALL(NTV)                                                                                   \
-    {                                                                                                          \
-        const float* hv[NTV];                                                                                  \
-        _Pragma("unroll") for (int j = 0; j < NTV; ++j) {                                                      \
-            const int t = tok[j];                                                                              \
-            hv[j] = sh ? hs + (size_t)t * Is : hr + ((size_t)t * k + (__ffs(rank_bits(dm, t) | 0x100u) - 1)) * I; \
-        }                                                                                                      \
-        down_task<LPR, NTV>(row_a, row_b, has_b, K, hv, n, gl, oa, ob);                                       \
-    }
-            if (n == 1) FLINT_DOWN_CALL(1)
-            else if (n == 2) FLINT_DOWN_CALL(2)
-            else if (n <= 4) FLINT_DOWN_CALL(4)
-            else FLINT_DOWN_CALL(8)
-#undef FLINT_DOWN_CALL
-            if (gl == 0 && has_a) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (j < n) {
-                        const int t = tok[j];
-                        const float da = bf16_round_f32(tsd * oa[j]);
-                        const float db = bf16_round_f32(tsd * ob[j]);
-                        if (sh) {
-                            dval[((size_t)t * (k + 1) + k) * RM + ra] = da;
-                            if (has_b) dval[((size_t)t * (k + 1) + k) * RM + ra + 1] = db;
-                        } else {
-                            const uint32_t ranks = rank_bits(dm, t);
-                            for (int jj = 0; jj < k; ++jj) {
-                                if ((ranks >> jj) & 1u) {
-                                    dval[((size_t)t * (k + 1) + jj) * RM + ra] = da;
-                                    if (has_b) dval[((size_t)t * (k + 1) + jj) * RM + ra + 1] = db;
-                                }
-                            }
-                        }
-                    }
+        };
+        // d value of row r (of the CTA's rows) for token t, for every rank of t.
+        auto put = [&](float v, int r, int t) {
+            const float dv = bf16_round_f32(tsd * v);
+            if (sh) {
+                dval[((size_t)t * (k + 1) + k) * RM + r] = dv;
+            } else {
+                const uint32_t ranks = rank_bits(dm, t);
+                for (int jj = 0; jj < k; ++jj)
+                    if ((ranks >> jj) & 1u) dval[((size_t)t * (k + 1) + jj) * RM + r] = dv;
+            }
+        };
+        while (rest) {
+            const int t0 = __ffs(rest) - 1;
+            rest &= rest - 1u;
+            if (rest) {  // two tokens, rows in groups of 8
+                const int t1 = __ffs(rest) - 1;
+                rest &= rest - 1u;
+                const uint4* hv[2];
+                const float* cv[2];
+                vec(t0, hv[0], cv[0]);
+                vec(t1, hv[1], cv[1]);
+                for (int hb = 0; hb < RG && r0 + hb < r1; hb += 8) {
+                    float acc[16];
+                    down_pass<8, 2>(slot + (size_t)hb * RS, RS, r1 - r0 - hb, K, hv, cv, lane, acc);
+                    const float v = reduce_scatter<16>(acc, lane);
+                    const int idx = rs_index<16>(lane), r = r0 + hb + (idx & 7);
+                    if ((lane & 1) == 0 && r < r1) put(v, r, (idx >> 3) ? t1 : t0);
                 }
+            } else {
+                const uint4* hv[1];
+                const float* cv[1];
+                vec(t0, hv[0], cv[0]);
+                float acc[RG];
+                down_pass<RG, 1>(slot, RS, r1 - r0, K, hv, cv, lane, acc);
+                const float v = reduce_scatter<RG>(acc, lane);
+                const int r = r0 + rs_index<RG>(lane);
+                if (lane % (32 / RG) == 0 && r < r1) put(v, r, t0);
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[b]);
+        if (lane == 0 && kk + NSW < my_tasks) {
+            fence_proxy_async_smem();
+            issue(kk + NSW);
+        }
     }
-    named_sync(1, kCW * 32);
+    if (__syncthreads_or(!ok)) {  // a wait gave up (the status word says which)
+        if (lane == 0) drain_slots(bar, NSW, kk, min(my_tasks, kk + NSW));
+        return;
+    }
     // combine, in rank order then the shared expert
-    for (int i = tid; i < T * nr; i += kCW * 32) {
-        const int t = i / nr, r = i % nr;
+    for (int i = tid; i < T * nr; i += kGemvThreads) {
+        const int t = i / nr, r = i - t * nr;
         float acc = 0.f;
         for (int j = 0; j < k; ++j)
             if (ri.ids[t * k + j] >= 0) acc = fmaf(wsm[t * k + j], dval[((size_t)t * (k + 1) + j) * RM + r], acc);
@@ -641,38 +758,33 @@ cudaError_t launch_ex(K kernel, const A& args, unsigned grid, size_t smem, bool 
 
 }  // namespace
 
-size_t gate_up_smem_bytes(const GateUpArgs& a, bool pair) {
-    return pair ? gate_up_layout<true>(a.T, a.H, a.nstages).total : gate_up_layout<false>(a.T, a.H, a.nstages).total;
+size_t gate_up_smem_bytes(const GateUpArgs& a, bool pair, int grid) {
+    const int shp = a.gu ? (a.Is + grid - 1) / grid : 0;
+    return pair ? gate_up_layout<true>(a.T, a.H, shp, a.res_items, a.nslots, a.slot_pairs).total
+                : gate_up_layout<false>(a.T, a.H, shp, a.res_items, a.nslots, a.slot_pairs).total;
 }
-size_t gate_up_stage_bytes(int H, bool pair) { return (size_t)(pair ? 2 : 1) * kCW * nvfp4_row_stride(H); }
 size_t down_smem_bytes(const DownArgs& a) { return down_layout(a).total; }
-size_t down_stage_bytes(const DownArgs& a) { return (size_t)kCW * a.slot_bytes; }
 
 cudaError_t launch_gate_up(const GateUpArgs& a, bool pair, const DevInfo& d, bool pdl, cudaStream_t s) {
     static int cfg_pair = -1, cfg_rows = -1;
     cudaError_t e = pair ? configure_smem(gate_up_kernel<true>, d, cfg_pair)
                          : configure_smem(gate_up_kernel<false>, d, cfg_rows);
     if (e != cudaSuccess) return e;
-    const size_t smem = gate_up_smem_bytes(a, pair);
+    const size_t smem = gate_up_smem_bytes(a, pair, d.sm_count);
     return pair ? launch_ex(gate_up_kernel<true>, a, (unsigned)d.sm_count, smem, pdl, s)
                 : launch_ex(gate_up_kernel<false>, a, (unsigned)d.sm_count, smem, pdl, s);
 }
 
 cudaError_t launch_down(const DownArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
-    static int cfg8 = -1, cfg16 = -1, cfg32 = -1;
+    static int cfg8 = -1, cfg16 = -1;
     const size_t smem = down_smem_bytes(a);
     cudaError_t e;
-    switch (a.lpr) {
-        case 8:
-            if ((e = configure_smem(down_kernel<8>, d, cfg8)) != cudaSuccess) return e;
-            return launch_ex(down_kernel<8>, a, (unsigned)d.sm_count, smem, pdl, s);
-        case 16:
-            if ((e = configure_smem(down_kernel<16>, d, cfg16)) != cudaSuccess) return e;
-            return launch_ex(down_kernel<16>, a, (unsigned)d.sm_count, smem, pdl, s);
-        default:
-            if ((e = configure_smem(down_kernel<32>, d, cfg32)) != cudaSuccess) return e;
-            return launch_ex(down_kernel<32>, a, (unsigned)d.sm_count, smem, pdl, s);
+    if (a.rg == 8) {
+        if ((e = configure_smem(down_kernel<8>, d, cfg8)) != cudaSuccess) return e;
+        return launch_ex(down_kernel<8>, a, (unsigned)d.sm_count, smem, pdl, s);
     }
+    if ((e = configure_smem(down_kernel<16>, d, cfg16)) != cudaSuccess) return e;
+    return launch_ex(down_kernel<16>, a, (unsigned)d.sm_count, smem, pdl, s);
 }
 
 }  // namespace flint

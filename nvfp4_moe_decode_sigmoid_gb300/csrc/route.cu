@@ -86,9 +86,10 @@ __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
         bulk_g2s(wrows, a.wr + (size_t)r0 * H, bytes, bar);
     }
     __syncthreads();  // the barrier is initialised before anyone waits on it
-    // The gate/up kernel only prefetches static weights before its own wait.
-    pdl_launch_dependents();
     pdl_wait();  // x may come from the previous kernel
+    // Dependents start only now: the gate/up kernel may then read x before its
+    // own wait (x is complete once this kernel has passed its wait).
+    pdl_launch_dependents();
 
     const int nchunk = H / 8;
     const bool ok = mbar_wait_bounded(bar, 0, tid == 0 ? a.status : nullptr, kStatusTimeoutRoute);
