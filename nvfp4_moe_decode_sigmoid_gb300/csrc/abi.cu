@@ -98,23 +98,17 @@ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 // Shared memory a launch may take, leaving room for the kernel's static data.
 constexpr size_t kSmemSlack = 1024;
 
-// Per-warp ring of the gate/up kernel: prefers two or three slots per warp
-// (a copy in flight while the previous slot is computed) of one pair each,
-// then fewer, until the CTA fits in shared memory. `items` bounds the work
+// Per-warp ring of the gate/up kernel: up to 3 slots of one item (a copy in
+// flight while the previous item is computed), fewer when a warp has less
+// work or the CTA would not fit in shared memory. `items` bounds the work
 // items of one CTA (their raw sums stay in shared memory). Returns false when
 // nothing fits.
-bool gate_up_shape(flint::GateUpArgs& a, bool pair, int sm_count, int smem_optin, long long items) {
+bool gate_up_shape(flint::GateUpArgs& a, bool pair, int smem_optin, long long items) {
     a.res_items = (int)items;
-    const long long per_cta = items;
-    const int per_warp = ceil_div(per_cta, flint::kGemvWarps);
-    const int want = per_warp < 1 ? 1 : (per_warp > 3 ? 3 : per_warp);
-    for (int ns = want; ns >= 1; --ns) {
-        for (int sp = 1; sp <= 2; ++sp) {
-            if (sp > 1 && ns > 1) continue;  // two pairs per slot only as a last resort
-            a.slot_pairs = sp;
-            a.nslots = ns;
-            if (flint::gate_up_smem_bytes(a, pair, sm_count) + kSmemSlack <= (size_t)smem_optin) return true;
-        }
+    const int per_warp = ceil_div(items, flint::kGemvWarps);
+    for (int ns = per_warp < 1 ? 1 : (per_warp > 3 ? 3 : per_warp); ns >= 1; --ns) {
+        a.nslots = ns;
+        if (flint::gate_up_smem_bytes(a, pair) + kSmemSlack <= (size_t)smem_optin) return true;
     }
     return false;
 }
@@ -335,7 +329,7 @@ flint_status_t flint_moe_gate_up(const flint_bf16* x, int T, const int32_t* ids,
     a.status = ws_status(ws);
     a.x_early = (flags & FLINT_PDL) && (flags & FLINT_PDL_AFTER_ROUTE);
     const long long routed_pairs = (long long)(T * k < a.E ? T * k : a.E) * a.I;
-    if (!gate_up_shape(a, true, d.sm_count, d.smem_optin,
+    if (!gate_up_shape(a, true, d.smem_optin,
                        ceil_div(a.Is, d.sm_count) + ceil_div(routed_pairs, d.sm_count)))
         return fail(FLINT_ERR_UNSUPPORTED, "gate_up: shapes exceed one CTA's shared memory");
     cudaError_t e = flint::launch_gate_up(a, true, d, (flags & FLINT_PDL) != 0, as_stream(stream));
@@ -423,7 +417,7 @@ flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* 
     int tg = T;
     for (; tg >= 1; --tg) {
         a.T = tg;
-        if (gate_up_shape(a, pair, d.sm_count, d.smem_optin, items)) break;
+        if (gate_up_shape(a, pair, d.smem_optin, items)) break;
     }
     if (tg < 1) return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: K=%d exceeds one CTA's shared memory", K);
     cudaError_t e = cudaSuccess;
@@ -431,7 +425,7 @@ flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* 
         a.T = T - t0 < tg ? T - t0 : tg;
         a.x = x + (size_t)t0 * K;
         a.h_shared = y + (size_t)t0 * n_out;
-        if (!gate_up_shape(a, pair, d.sm_count, d.smem_optin, items))
+        if (!gate_up_shape(a, pair, d.smem_optin, items))
             return fail(FLINT_ERR_UNSUPPORTED, "dense_gemv: K=%d exceeds one CTA's shared memory", K);
         e = flint::launch_gate_up(a, pair, d, pdl, as_stream(stream));
     }

@@ -97,6 +97,48 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
 }
 
 // ---------------------------------------------------------------------------
+// 16-byte asynchronous copies global -> shared (cp.async, L2 only), grouped
+// per thread: commit closes a group; wait_groups<N> returns once at most N of
+// the thread's groups are still in flight. Both addresses 16-byte aligned.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Runtime N in 0..3.
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+    switch (n) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        default: cp_async_wait<3>(); break;
+    }
+}
+// The warp copies `bytes` (a multiple of 16) from src to dst, lane l taking
+// the 16-byte words l, l + 32, ...
+__device__ __forceinline__ void warp_copy_async(void* dst, const void* src, int bytes, int lane) {
+    uint8_t* d = static_cast<uint8_t*>(dst);
+    const uint8_t* s = static_cast<const uint8_t*>(src);
+    for (int o = 16 * lane; o < bytes; o += 512) cp_async16(d + o, s + o);
+}
+
+// Warms the address translation (and L2) for the bytes [p, p + n): a
+// prefetch of the first and the last byte, neither of which blocks. Kernels
+// issue these at their start for the small buffers they touch late (outputs,
+// scales, activations), so the page walks overlap other work instead of
+// stalling the first access behind the weight stream.
+__device__ __forceinline__ void prefetch_range(const void* p, size_t n) {
+    if (!p || n == 0) return;
+    const char* c = static_cast<const char*>(p);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(c));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(c + n - 1));
+}
+
+// ---------------------------------------------------------------------------
 // Loads that bypass L1: data written by another kernel of the PDL chain.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int32_t ld_cg(const int32_t* p) { return __ldcg(p); }

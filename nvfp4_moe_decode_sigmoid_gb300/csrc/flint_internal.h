@@ -92,8 +92,7 @@ struct GateUpArgs {
     uint16_t* h_routed; // [8][k][I]
     uint16_t* h_shared; // [T][Is]: h of the shared expert, or the dense output y
     uint32_t* status;
-    int nslots;         // ring slots per warp
-    int slot_pairs;     // items (pairs or rows) per slot
+    int nslots;         // ring slots per warp (one item each)
     int res_items;      // bound on the items of one CTA (shared-memory sums)
     int x_early;        // x is complete before the PDL wait (previous kernel: the router)
 };
@@ -153,7 +152,7 @@ cudaError_t configure_smem(K kernel, const DevInfo& d, int& configured_for) {
     return e;
 }
 
-size_t gate_up_smem_bytes(const GateUpArgs& a, bool pair, int grid);
+size_t gate_up_smem_bytes(const GateUpArgs& a, bool pair);
 size_t down_smem_bytes(const DownArgs& a);
 size_t route_smem_bytes(const RouteArgs& a);
 

@@ -9,14 +9,15 @@
 // activations; every kernel follows the reference's rounding points.
 //
 // Both kernels run one CTA of 32 warps per SM. Each warp streams its own work
-// items (weight rows) through a private ring of shared-memory slots with 1-D
-// bulk (TMA) copies completed on per-slot mbarriers, so 32 threads per SM
-// issue copies (one issuing thread manages only a few copies per
-// microsecond). Dequantisation happens in registers: cvt e2m1x2 gives exact
-// f16 code values, which multiply f16 activations in mixed-precision FMAs
-// accumulating in FP32 (an f16 x f16 product is exact in FP32, so every step
-// rounds once, as an FP32 FMA of the same values would). The UE4M3 block
-// scale is applied once per 16 values.
+// items (weight rows) through a private ring of shared-memory slots, copied
+// by all 32 of its lanes with 16-byte cp.async (one commit group per item).
+// 1-D bulk copies were tried first: one item's rows are only 1-4 KB, and at
+// that size the bulk-copy path delivered well under half of the HBM
+// bandwidth, while per-lane 16-byte copies saturate it. Dequantisation happens
+// in registers: cvt e2m1x2 gives exact f16 code values, which multiply f16
+// activations in mixed-precision FMAs accumulating in FP32 (an f16 x f16
+// product is exact in FP32, so every step rounds once, as an FP32 FMA of the
+// same values would). The UE4M3 block scale is applied once per 16 values.
 //
 // Activations (x for gate/up, h for down) are staged in shared memory as f16:
 // every 32-value chunk is multiplied by the power of two that puts its largest
@@ -170,74 +171,109 @@ __device__ __forceinline__ int rs_index(int lane) {
 //     and nb + b (nb = K / 16): lane l reads block l + 32 m at l + 32 m and
 //     nb + l + 32 m.
 // ===========================================================================
+// One staging source: nvec bf16 vectors of K values.
+struct StageSrc {
+    const uint16_t* src;
+    uint4* dst;
+    float* csc;
+    int nvec, K;
+};
+
+// Chunk q of the concatenated sources: its source and offset; false past the end.
+template <int NS>
+__device__ __forceinline__ bool stage_locate(const StageSrc (&ss)[NS], int q, int& s, int& v, int& c) {
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        const int cpv = ss[i].K / 32, n = ss[i].nvec * cpv;
+        if (q < n) {
+            s = i;
+            v = q / cpv;
+            c = q - v * cpv;
+            return true;
+        }
+        q -= n;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void stage_load(const StageSrc& ss, int v, int c, uint4 (&w)[4]) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(ss.src + (size_t)v * ss.K + 32 * c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = ld_cg(s4 + i);
+}
+
 template <bool DOWN_ORDER>
-__device__ __forceinline__ void stage_f16(uint4* dst, float* csc, const uint16_t* src, int nvec, int K) {
-    const int cpv = K / 32;
-    for (int q = threadIdx.x; q < nvec * cpv; q += kGemvThreads) {
-        const int v = q / cpv, c = q - v * cpv;
-        const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)v * K + 32 * c);
-        uint4 w[4];
+__device__ __forceinline__ void stage_store(const StageSrc& ss, int v, int c, const uint4 (&w)[4]) {
+    uint32_t m2 = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = ld_cg(s4 + i);
-        uint32_t m2 = 0;
+    for (int i = 0; i < 4; ++i) {
+        m2 = __vmaxu2(m2, w[i].x & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, w[i].y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, w[i].z & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, w[i].w & 0x7FFF7FFFu);
+    }
+    // bf16 exponent field of the largest magnitude -> s with max * 2^-s in [2^14, 2^15)
+    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    const int sh = min(126, max(-126, (int)(m >> 7) - 141));
+    const float down = __int_as_float((127 - sh) << 23);
+    const int K = ss.K;
+    ss.csc[v * (K / 32) + c] = __int_as_float((127 + sh) << 23);
+    uint4* d = ss.dst + (size_t)v * (K / 8);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            m2 = __vmaxu2(m2, w[i].x & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, w[i].y & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, w[i].z & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, w[i].w & 0x7FFF7FFFu);
+    for (int i = 0; i < 4; ++i) {
+        int idx;
+        if (DOWN_ORDER) {
+            idx = (i & 1) * (K / 16) + 2 * c + (i >> 1);
+        } else {
+            idx = (c / 32) * 128 + i * 32 + c % 32;
         }
-        // bf16 exponent field of the largest magnitude -> s with max * 2^-s in [2^14, 2^15)
-        const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-        const int s = min(126, max(-126, (int)(m >> 7) - 141));
-        const float down = __int_as_float((127 - s) << 23);
-        csc[q] = __int_as_float((127 + s) << 23);
-        uint4* d = dst + (size_t)v * (K / 8);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            int idx;
-            if (DOWN_ORDER) {
-                idx = (i & 1) * (K / 16) + 2 * c + (i >> 1);
-            } else {
-                idx = (c / 32) * 128 + i * 32 + c % 32;
-            }
-            d[idx] = make_uint4(f32x2_to_f16x2(bf16_lo(w[i].x) * down, bf16_hi(w[i].x) * down),
-                                f32x2_to_f16x2(bf16_lo(w[i].y) * down, bf16_hi(w[i].y) * down),
-                                f32x2_to_f16x2(bf16_lo(w[i].z) * down, bf16_hi(w[i].z) * down),
-                                f32x2_to_f16x2(bf16_lo(w[i].w) * down, bf16_hi(w[i].w) * down));
-        }
+        d[idx] = make_uint4(f32x2_to_f16x2(bf16_lo(w[i].x) * down, bf16_hi(w[i].x) * down),
+                            f32x2_to_f16x2(bf16_lo(w[i].y) * down, bf16_hi(w[i].y) * down),
+                            f32x2_to_f16x2(bf16_lo(w[i].z) * down, bf16_hi(w[i].z) * down),
+                            f32x2_to_f16x2(bf16_lo(w[i].w) * down, bf16_hi(w[i].w) * down));
     }
 }
 
-// Lane 0 of a warp whose bounded wait gave up: waits (again bounded) for the
-// copies it still has in flight, slots [k0, k1) of its ring, so that none
-// lands in shared memory after the CTA has exited.
-__device__ __forceinline__ void drain_slots(uint64_t* bar, int nslots, int k0, int k1) {
-    for (int k = k0; k < k1; ++k) mbar_wait_bounded(&bar[k % nslots], (uint32_t)((k / nslots) & 1), nullptr, 0u);
+// Stages the sources; every thread first issues the loads of its first chunk,
+// then runs `between` (the callers issue their weight copies there, so that
+// these small loads are not queued behind the weight stream), then converts.
+// Further chunks (more than one per thread) are loaded and converted after.
+template <bool DOWN_ORDER, int NS, typename F>
+__device__ __forceinline__ void stage_f16(const StageSrc (&ss)[NS], F&& between) {
+    int s0 = 0, v0 = 0, c0 = 0;
+    uint4 w[4];
+    const bool have = stage_locate(ss, threadIdx.x, s0, v0, c0);
+    if (have) stage_load(ss[s0], v0, c0, w);
+    between();
+    if (have) stage_store<DOWN_ORDER>(ss[s0], v0, c0, w);
+    for (int q = threadIdx.x + kGemvThreads;; q += kGemvThreads) {
+        int s, v, c;
+        if (!stage_locate(ss, q, s, v, c)) break;
+        stage_load(ss[s], v, c, w);
+        stage_store<DOWN_ORDER>(ss[s], v, c, w);
+    }
 }
 
 // ===========================================================================
 // gate/up + SiLU (PAIR) or plain rows
 // ===========================================================================
-// Shared memory: mbarriers (kMaxSlotsPerWarp per warp + one for the shared
-// expert), routing view, chunk scales, f16 activations, raw sums [item][T]
-// (gate, then up), the CTA's slice of the shared expert (MoE only), the
-// warps' slot rings.
+// Shared memory: routing view, chunk scales, f16 activations, raw sums
+// [item][T] (gate, then up), the warps' slot rings (one item per slot: its
+// gate row, then its up row).
 struct GateUpSmem {
-    size_t route, csc, xs, resg, resu, shared, ring, slot, total;
+    size_t route, tss, csc, xs, resg, resu, ring, slot, total;
 };
 template <bool PAIR>
-__host__ __device__ inline GateUpSmem gate_up_layout(int T, int H, int shared_pairs, int items, int nslots,
-                                                     int slot_pairs) {
+__host__ __device__ inline GateUpSmem gate_up_layout(int T, int H, int items, int nslots) {
     GateUpSmem L;
-    L.route = align_up(8 * (kW * kMaxSlotsPerWarp + 1), 128);
-    L.csc = align_up(L.route + sizeof(RouteInfo), 128);
+    L.route = 0;
+    L.tss = align_up(L.route + sizeof(RouteInfo), 128);
+    L.csc = align_up(L.tss + sizeof(float) * (2 * kMaxDistinct + 2), 128);
     L.xs = align_up(L.csc + sizeof(float) * (size_t)T * (H / 32), 128);
     L.resg = align_up(L.xs + 2 * (size_t)T * H, 128);
     L.resu = align_up(L.resg + sizeof(float) * (size_t)items * T, 128);
-    L.shared = align_up(L.resu + (PAIR ? sizeof(float) * (size_t)items * T : 0), 128);
-    L.ring = align_up(L.shared + (size_t)(PAIR ? 2 : 1) * shared_pairs * nvfp4_row_stride(H), 128);
-    L.slot = (size_t)(PAIR ? 2 : 1) * slot_pairs * nvfp4_row_stride(H);
+    L.ring = align_up(L.resu + (PAIR ? sizeof(float) * (size_t)items * T : 0), 128);
+    L.slot = (size_t)(PAIR ? 2 : 1) * nvfp4_row_stride(H);
     L.total = L.ring + (size_t)kW * nslots * L.slot;
     return L;
 }
@@ -346,96 +382,82 @@ __device__ __forceinline__ void gate_up_item(const uint8_t* grow, const uint8_t*
     }
 }
 
-// MoE (a.gu set): the CTA's slice of the shared expert (pairs [sp0, sp1)) is
-// requested into its own region before the PDL wait and computed by the last
-// warps; the CTA's share of the routed pairs is split over the warps' rings
-// once the routing is read. Dense (a.gu null): the CTA's rows (pairs)
-// [sp0, sp1) of the matrix are split over the warps' rings before the wait.
-// Item i of the CTA (shared-expert pair or dense row i < n_sh, then routed
-// pair n_sh + j) keeps its raw sums at res[i * T + t].
+// Work items of a CTA: its slice [sp0, sp1) of the shared expert's pairs (or
+// of the dense matrix's rows / pairs), then (MoE) its share of the routed
+// pairs of the distinct selected experts. Warp w's list: shared items
+// kW-1-w, 2 kW-1-w, ... (known before the PDL wait, so requested then), then
+// the routed list items [lw0, lw1) once the routing is read. Dense: rows
+// [lw0, lw1) of the CTA's slice, requested before the wait. Each item goes
+// through the warp's ring of nslots slots with 16-byte cp.async copies by
+// all its lanes (one commit group per item). Item i of the CTA (shared pair /
+// dense row i < n_sh, then routed pair n_sh + j) keeps its raw sums at
+// res[i * T + t].
 template <bool PAIR>
 __global__ void __launch_bounds__(kGemvThreads, 1) gate_up_kernel(const GateUpArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int NSW = a.nslots, SP = a.slot_pairs, H = a.H, T = a.T, I = a.I, Is = a.Is;
+    const int NSW = a.nslots, H = a.H, T = a.T, I = a.I, Is = a.Is;
     const bool moe = a.gu != nullptr;
     const int c = blockIdx.x, G = gridDim.x;
     const int sp0 = (int)((long long)c * Is / G), sp1 = (int)((long long)(c + 1) * Is / G);
     const int n_sh = a.s_gu ? sp1 - sp0 : 0;
-    const int shp = moe ? (Is + G - 1) / G : 0;
-    const GateUpSmem L = gate_up_layout<PAIR>(T, H, shp, a.res_items, NSW, SP);
+    const GateUpSmem L = gate_up_layout<PAIR>(T, H, a.res_items, NSW);
     RouteInfo& ri = *reinterpret_cast<RouteInfo*>(smem + L.route);
     float* csc = reinterpret_cast<float*>(smem + L.csc);
     uint4* xh = reinterpret_cast<uint4*>(smem + L.xs);
     float* resg = reinterpret_cast<float*>(smem + L.resg);
     float* resu = reinterpret_cast<float*>(smem + L.resu);
-    uint8_t* shreg = smem + L.shared;
+    float* tss = reinterpret_cast<float*>(smem + L.tss);  // [d][2] routed, then the shared pair
     const int RS = (int)nvfp4_row_stride(H);
-    const int half = SP * RS;  // gate rows of one slot; up rows follow (PAIR)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + warp * kMaxSlotsPerWarp;
-    uint64_t* shbar = reinterpret_cast<uint64_t*>(smem) + kW * kMaxSlotsPerWarp;
     uint8_t* ring = smem + L.ring + (size_t)warp * NSW * L.slot;
 
-    // This warp's list items [lw0, lw1): routed pairs of the CTA (MoE) or rows
-    // of the dense matrix. List item j -> rows of its gate (and up) part.
+    // This warp's list: n_sw shared items, then routed list items [lw0, lw1)
+    // (MoE); or dense rows [lw0, lw1).
+    const int n_sw = moe && n_sh > kW - 1 - warp ? (n_sh - (kW - 1 - warp) + kW - 1) / kW : 0;
     int rp0 = 0, lw0 = 0, lw1 = 0, nl = 0;
-    auto item_rows = [&](int j, const uint8_t*& g, const uint8_t*& u) {
-        if (moe) {
-            const int q = rp0 + j, d = q / I, p = q - d * I;
+    if (!moe) {
+        lw0 = (int)((long long)warp * n_sh / kW);
+        lw1 = (int)((long long)(warp + 1) * n_sh / kW);
+    }
+    // Requests item m of the list into slot m % NSW (one commit group).
+    auto issue = [&](int m) {
+        const uint8_t *g, *u;
+        if (m < n_sw) {
+            const int i = kW - 1 - warp + kW * m;
+            g = a.s_gu + (size_t)(sp0 + i) * RS;
+            u = a.s_gu + (size_t)(Is + sp0 + i) * RS;
+        } else if (moe) {
+            const int q = rp0 + lw0 + m - n_sw, d = q / I, p = q - d * I;
             g = a.gu + ((size_t)ri.dlist[d] * 2 * I + p) * RS;
             u = g + (size_t)I * RS;
         } else {
+            const int j = lw0 + m;
             g = a.s_gu + (size_t)(sp0 + j) * RS;
             u = a.s_gu + (size_t)(Is + sp0 + j) * RS;
         }
-    };
-    // Lane 0: request slot k (list items [lw0 + k SP, ...)) in runs of
-    // consecutive rows of one matrix; one arrival with the byte count.
-    auto issue = [&](int k) {
-        const int i0 = lw0 + k * SP, i1 = min(lw1, i0 + SP);
-        uint8_t* g = ring + (size_t)(k % NSW) * L.slot;
-        uint64_t* b = &bar[k % NSW];
-        mbar_arrive_expect_tx(b, (uint32_t)((PAIR ? 2 : 1) * (i1 - i0) * RS));
-        int i = i0;
-        while (i < i1) {
-            const uint8_t *g0, *u0;
-            item_rows(i, g0, u0);
-            int j = i + 1;
-            while (j < i1) {
-                const uint8_t *gj, *uj;
-                item_rows(j, gj, uj);
-                if (gj != g0 + (size_t)(j - i) * RS) break;
-                ++j;
-            }
-            const uint32_t n = (uint32_t)((j - i) * RS);
-            bulk_g2s(g + (size_t)(i - i0) * RS, g0, n, b);
-            if (PAIR) bulk_g2s(g + half + (size_t)(i - i0) * RS, u0, n, b);
-            i = j;
-        }
+        uint8_t* slot = ring + (size_t)(m % NSW) * L.slot;
+        warp_copy_async(slot, g, RS, lane);
+        if (PAIR) warp_copy_async(slot + RS, u, RS, lane);
+        cp_async_commit();
     };
 
-    if (lane == 0) {
-        for (int s = 0; s < NSW; ++s) mbar_init(&bar[s], 1);
-        if (tid == 0) mbar_init(shbar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    // Before the wait: weights that depend on no earlier kernel.
-    if (moe) {
-        if (tid == 0 && n_sh > 0) {
-            const uint32_t n = (uint32_t)(n_sh * RS);
-            mbar_arrive_expect_tx(shbar, PAIR ? 2 * n : n);
-            bulk_g2s(shreg, a.s_gu + (size_t)sp0 * RS, n, shbar);
-            if (PAIR) bulk_g2s(shreg + (size_t)shp * RS, a.s_gu + (size_t)(Is + sp0) * RS, n, shbar);
+    if (tid == kGemvThreads - 1) {
+        prefetch_range(a.x, 2 * (size_t)T * H);
+        prefetch_range(a.s_ts, 8);
+        prefetch_range(a.h_shared, 2 * (size_t)T * Is);
+        if (moe) {
+            prefetch_range(a.ids, 4 * (size_t)T * a.k);
+            prefetch_range(a.ts, 12 * (size_t)a.E);
+            prefetch_range(a.h_routed, 2 * (size_t)T * a.k * I);
         }
-    } else {
-        lw0 = (int)((long long)warp * n_sh / kW);
-        lw1 = (int)((long long)(warp + 1) * n_sh / kW);
-        if (lane == 0)
-            for (int k = 0; k < NSW && lw0 + k * SP < lw1; ++k) issue(k);
     }
-    if (a.x_early) stage_f16<false>(xh, csc, a.x, T, H);
+    // Before the wait: weights that depend on no earlier kernel.
+    const int n_pre = moe ? n_sw : lw1 - lw0;
+    int issued = 0;
+    for (; issued < NSW && issued < n_pre; ++issued) issue(issued);
+    const StageSrc xsrc[1] = {{a.x, xh, csc, T, H}};
+    if (a.x_early) stage_f16<false>(xsrc, [] {});
     pdl_wait();  // ids (and x, unless staged already) are written by earlier kernels
     if (moe) {
         build_route_info(ri, a.ids, T, a.k, a.E, a.status);
@@ -446,42 +468,44 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gate_up_kernel(const GateUpAr
         lw1 = (int)((long long)(warp + 1) * nl / kW);
     }
     pdl_launch_dependents();
-    if (moe && lane == 0)
-        for (int k = 0; k < NSW && lw0 + k * SP < lw1; ++k) issue(k);
-    if (!a.x_early) stage_f16<false>(xh, csc, a.x, T, H);
-    __syncthreads();  // activations (and the routing view) visible to all warps
+    // The small loads first (tensor scales, activations): behind the routed
+    // weight copies they would wait for the whole stream ahead of them.
+    const int D = moe ? ri.D : 0;
+    float tsv = 0.f;
+    if (tid < 2 * D) tsv = ld_cg(a.ts + 3 * ri.dlist[tid >> 1] + (tid & 1));
+    else if (tid < 2 * D + 2 && a.s_ts) tsv = ld_cg(a.s_ts + (PAIR ? tid - 2 * D : 0));
+    const int n_items_w = moe ? n_sw + lw1 - lw0 : lw1 - lw0;
+    auto burst = [&] {
+        for (; issued < NSW; ++issued) {
+            if (issued < n_items_w)
+                issue(issued);
+            else
+                cp_async_commit();  // empty group: NSW groups ahead of the first wait
+        }
+    };
+    if (a.x_early)
+        burst();
+    else
+        stage_f16<false>(xsrc, burst);
+    if (tid < 2 * D + 2) tss[tid] = tsv;
+    __syncthreads();  // activations, scales and the routing view visible to all warps
 
     const uint32_t all_tokens = (1u << T) - 1u;
-    const int n_slots = (lw1 - lw0 + SP - 1) / SP;
-    int k = 0;  // this warp's next slot
-    bool ok = true;
-    // The CTA's shared-expert pairs: pair i is computed by warp kW - 1 - i.
-    if (moe) {
-        for (int i = kW - 1 - warp; i < n_sh && ok; i += kW) {
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait_bounded(shbar, 0, lane == 0 ? a.status : nullptr, kStatusTimeoutGateUp));
-            if (!ok) break;
-            const uint8_t* grow = shreg + (size_t)i * RS;
-            gate_up_item<PAIR>(grow, grow + (size_t)shp * RS, H, xh, csc, all_tokens, lane, resg + i * T,
-                               resu + i * T);
-        }
-    }
-    // This warp's slots.
-    int d = 0, p = 0;  // expert index and pair index of the next list item (MoE)
+    int d = 0, p = 0;  // expert index and pair index of the next routed item (MoE)
     if (moe && lw1 > lw0) {
         d = (rp0 + lw0) / I;
         p = rp0 + lw0 - d * I;
     }
-    for (; k < n_slots && ok; ++k) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar[k % NSW], (uint32_t)((k / NSW) & 1),
-                                                       lane == 0 ? a.status : nullptr, kStatusTimeoutGateUp));
-        if (!ok) break;
-        const int i0 = lw0 + k * SP, i1 = min(lw1, i0 + SP);
-        const uint8_t* sbuf = ring + (size_t)(k % NSW) * L.slot;
-        for (int j = i0; j < i1; ++j) {
-            const uint8_t* grow = sbuf + (size_t)(j - i0) * RS;
-            const int item = moe ? n_sh + j : j;
-            gate_up_item<PAIR>(grow, grow + half, H, xh, csc, moe ? ri.tmask[d] : all_tokens, lane,
+    for (int m = 0; m < n_items_w; ++m) {
+        cp_async_wait_n(NSW - 1);
+        __syncwarp();
+        const uint8_t* grow = ring + (size_t)(m % NSW) * L.slot;
+        if (m < n_sw) {
+            const int i = kW - 1 - warp + kW * m;
+            gate_up_item<PAIR>(grow, grow + RS, H, xh, csc, all_tokens, lane, resg + i * T, resu + i * T);
+        } else {
+            const int item = moe ? n_sh + lw0 + m - n_sw : lw0 + m;
+            gate_up_item<PAIR>(grow, grow + RS, H, xh, csc, moe ? ri.tmask[d] : all_tokens, lane,
                                resg + item * T, resu + item * T);
             if (++p == I) {
                 p = 0;
@@ -489,16 +513,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gate_up_kernel(const GateUpAr
             }
         }
         __syncwarp();
-        if (lane == 0 && k + NSW < n_slots) {
-            fence_proxy_async_smem();
-            issue(k + NSW);
-        }
+        if (m + NSW < n_items_w)
+            issue(m + NSW);
+        else
+            cp_async_commit();
     }
-    if (__syncthreads_or(!ok)) {  // a wait gave up (the status word says which)
-        if (lane == 0) drain_slots(bar, NSW, k, min(n_slots, k + NSW));
-        if (tid == 0 && n_sh > 0 && moe) mbar_wait_bounded(shbar, 0, nullptr, 0u);
-        return;
-    }
+    cp_async_wait<0>();  // retire the trailing empty groups before warps exit
+    __syncthreads();
     // Epilogue over (token, item): tensor scales, bf16 rounding points, SiLU.
     const int n_items = n_sh + nl;
     for (int e = tid; e < n_items * T; e += kGemvThreads) {
@@ -508,16 +529,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gate_up_kernel(const GateUpAr
         uint32_t ranks = 0;
         if (i < n_sh) {
             pp = sp0 + i;
-            tsg = a.s_ts[0];
-            tsu = PAIR ? a.s_ts[1] : 0.f;
+            tsg = tss[2 * D];
+            tsu = tss[2 * D + 1];
         } else {
             const int q = rp0 + i - n_sh, dd = q / I;
             pp = q - dd * I;
             ranks = rank_bits(ri.dmask[dd], t);
             if (!ranks) continue;
-            const int ex = ri.dlist[dd];
-            tsg = a.ts[3 * ex + 0];
-            tsu = a.ts[3 * ex + 1];
+            tsg = tss[2 * dd];
+            tsu = tss[2 * dd + 1];
         }
         const float g = bf16_round_f32(tsg * resg[i * T + t]);
         uint16_t out;
@@ -544,9 +564,9 @@ struct DownSmem {
 };
 __host__ __device__ inline DownSmem down_layout(const DownArgs& a) {
     DownSmem L;
-    L.route = align_up(8 * kW * kMaxSlotsPerWarp, 128);
+    L.route = 0;
     L.w = align_up(L.route + sizeof(RouteInfo), 128);
-    L.csr = align_up(L.w + sizeof(float) * kMaxDistinct, 128);
+    L.csr = align_up(L.w + sizeof(float) * (2 * kMaxDistinct + 1), 128);
     L.css = align_up(L.csr + sizeof(float) * (size_t)a.T * a.k * (a.I / 32), 128);
     L.dval = align_up(L.css + sizeof(float) * (size_t)a.T * (a.Is / 32), 128);
     L.hr = align_up(L.dval + sizeof(float) * (size_t)a.T * (a.k + 1) * a.rows_max, 128);
@@ -599,7 +619,8 @@ __device__ __forceinline__ void down_pass(const uint8_t* rows, int RS, int nr, i
 // Each CTA owns output rows [n0, n1). Units are the distinct selected experts
 // (ascending id) and the shared expert; a task is a group of up to RG of the
 // CTA's rows of one unit. Warp w takes tasks w, w + kW, ... through its own
-// ring; the routing is final before this kernel starts (the gate/up kernel
+// ring (16-byte cp.async copies by all its lanes, one commit group per
+// task); the routing is final before this kernel starts (the gate/up kernel
 // triggers it only after its own wait), so the first slots are requested
 // before the PDL wait.
 template <int RG>
@@ -609,7 +630,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) down_kernel(const DownArgs a)
     const int NSW = a.nslots;
     const int T = a.T, k = a.k, H = a.H, I = a.I, Is = a.Is, RM = a.rows_max;
     RouteInfo& ri = *reinterpret_cast<RouteInfo*>(smem + L.route);
-    float* wsm = reinterpret_cast<float*>(smem + L.w);
+    float* wsm = reinterpret_cast<float*>(smem + L.w);            // [t*k + j]
+    float* tsd_s = reinterpret_cast<float*>(smem + L.w) + kMaxDistinct;  // down scale of unit u
     float* csr = reinterpret_cast<float*>(smem + L.csr);    // chunk scales of h_routed [t*k + j][I / 32]
     float* css = reinterpret_cast<float*>(smem + L.css);    // chunk scales of h_shared [t][Is / 32]
     float* dval = reinterpret_cast<float*>(smem + L.dval);  // [t][j (k = shared)][row]
@@ -617,18 +639,22 @@ __global__ void __launch_bounds__(kGemvThreads, 1) down_kernel(const DownArgs a)
     uint4* hs = reinterpret_cast<uint4*>(smem + L.hs);      // [t][Is] f16, DOWN order
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + warp * kMaxSlotsPerWarp;
     uint8_t* ring = smem + L.ring + (size_t)warp * NSW * a.slot_bytes;
     const int c = blockIdx.x, G = gridDim.x;
     const int n0 = (int)((long long)c * H / G), n1 = (int)((long long)(c + 1) * H / G), nr = n1 - n0;
     const int RSr = (int)nvfp4_row_stride(I), RSs = Is ? (int)nvfp4_row_stride(Is) : 0;
     if (nr == 0) return;  // more CTAs than output rows: nothing to copy or compute
 
-    if (lane == 0) {
-        for (int s = 0; s < NSW; ++s) mbar_init(&bar[s], 1);
-        fence_mbar_init();
+    if (tid == kGemvThreads - 1) {
+        prefetch_range(a.ids, 4 * (size_t)T * k);
+        prefetch_range(a.w, 4 * (size_t)T * k);
+        prefetch_range(a.ts, 12 * (size_t)a.E);
+        prefetch_range(a.s_ts, 12);
+        prefetch_range(a.h_routed, 2 * (size_t)T * k * I);
+        prefetch_range(a.h_shared, 2 * (size_t)T * Is);
+        prefetch_range(a.y + (size_t)n0, 2 * ((size_t)(T - 1) * H + nr));
     }
-    build_route_info(ri, a.ids, T, k, a.E, a.status);  // (its __syncthreads also publish the barriers)
+    build_route_info(ri, a.ids, T, k, a.E, a.status);
     const int D = ri.D;
     const bool has_sh = a.s_down != nullptr;
     const int n_units = D + (has_sh ? 1 : 0);
@@ -636,40 +662,48 @@ __global__ void __launch_bounds__(kGemvThreads, 1) down_kernel(const DownArgs a)
     const int n_tasks = n_units * ngr;
     const int my_tasks = n_tasks > warp ? (n_tasks - warp + kW - 1) / kW : 0;
 
-    auto issue = [&](int kk) {  // this warp's kk-th task
+    auto issue = [&](int kk) {  // this warp's kk-th task (one commit group)
         const int q = warp + kk * kW, u = q / ngr, r0 = (q - u * ngr) * RG, r1 = min(nr, r0 + RG);
-        uint64_t* b = &bar[kk % NSW];
         uint8_t* dst = ring + (size_t)(kk % NSW) * a.slot_bytes;
-        const int RS = u < D ? RSr : RSs;
-        mbar_arrive_expect_tx(b, (uint32_t)((r1 - r0) * RS));
         if (u < D)
-            bulk_g2s(dst, a.down + ((size_t)ri.dlist[u] * H + n0 + r0) * RSr, (uint32_t)((r1 - r0) * RSr), b);
+            warp_copy_async(dst, a.down + ((size_t)ri.dlist[u] * H + n0 + r0) * RSr, (r1 - r0) * RSr, lane);
         else
-            bulk_g2s(dst, a.s_down + (size_t)(n0 + r0) * RSs, (uint32_t)((r1 - r0) * RSs), b);
+            warp_copy_async(dst, a.s_down + (size_t)(n0 + r0) * RSs, (r1 - r0) * RSs, lane);
+        cp_async_commit();
     };
-    if (lane == 0)
-        for (int kk = 0; kk < min(NSW, my_tasks); ++kk) issue(kk);
-
     pdl_wait();  // h comes from the gate/up kernel
     pdl_launch_dependents();
-    stage_f16<true>(hr, csr, a.h_routed, T * k, I);
-    if (has_sh) stage_f16<true>(hs, css, a.h_shared, T, Is);
-    for (int i = tid; i < T * k; i += kGemvThreads) wsm[i] = ld_cg(a.w + i);
+    // The small loads first (combine weights, tensor scales, h); then this
+    // warp's first weight copies; then h is converted. (Requesting the weights
+    // before the wait gains nothing here: this kernel's CTAs do not fit on an
+    // SM beside the gate/up kernel's, and h queued behind the whole weight
+    // stream would arrive last.)
+    float wv = 0.f;
+    if (tid < T * k) wv = ld_cg(a.w + tid);
+    else if (tid >= 64 && tid < 64 + n_units) wv = tid - 64 < D ? ld_cg(a.ts + 3 * ri.dlist[tid - 64] + 2) : ld_cg(a.s_ts + 2);
+    const StageSrc hsrc[2] = {{a.h_routed, hr, csr, T * k, I}, {a.h_shared, hs, css, has_sh ? T : 0, Is ? Is : 32}};
+    stage_f16<true>(hsrc, [&] {
+        for (int kk = 0; kk < NSW; ++kk) {
+            if (kk < my_tasks)
+                issue(kk);
+            else
+                cp_async_commit();  // empty group: NSW groups ahead of the first wait
+        }
+    });
+    if (tid < T * k) wsm[tid] = wv;
+    else if (tid >= 64 && tid < 64 + n_units) tsd_s[tid - 64] = wv;
     __syncthreads();
 
-    int kk = 0;
-    bool ok = true;
-    for (; kk < my_tasks; ++kk) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar[kk % NSW], (uint32_t)((kk / NSW) & 1),
-                                                       lane == 0 ? a.status : nullptr, kStatusTimeoutDown));
-        if (!ok) break;
+    for (int kk = 0; kk < my_tasks; ++kk) {
+        cp_async_wait_n(NSW - 1);
+        __syncwarp();
         const int q = warp + kk * kW, u = q / ngr, r0 = (q - u * ngr) * RG, r1 = min(nr, r0 + RG);
         const bool sh = u >= D;
         const int K = sh ? Is : I, RS = sh ? RSs : RSr;
         const uint8_t* slot = ring + (size_t)(kk % NSW) * a.slot_bytes;
         const unsigned long long dm = sh ? 0ull : ri.dmask[u];
         uint32_t rest = sh ? (1u << T) - 1u : ri.tmask[u];
-        const float tsd = sh ? a.s_ts[2] : a.ts[3 * ri.dlist[u] + 2];
+        const float tsd = tsd_s[u];
         // Token t's staged h vector (and chunk scales) for this unit.
         auto vec = [&](int t, const uint4*& h, const float*& cs) {
             if (sh) {
@@ -721,15 +755,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1) down_kernel(const DownArgs a)
             }
         }
         __syncwarp();
-        if (lane == 0 && kk + NSW < my_tasks) {
-            fence_proxy_async_smem();
+        if (kk + NSW < my_tasks)
             issue(kk + NSW);
-        }
+        else
+            cp_async_commit();
     }
-    if (__syncthreads_or(!ok)) {  // a wait gave up (the status word says which)
-        if (lane == 0) drain_slots(bar, NSW, kk, min(my_tasks, kk + NSW));
-        return;
-    }
+    cp_async_wait<0>();  // retire the trailing empty groups before warps exit
+    __syncthreads();
     // combine, in rank order then the shared expert
     for (int i = tid; i < T * nr; i += kGemvThreads) {
         const int t = i / nr, r = i - t * nr;
@@ -758,10 +790,9 @@ cudaError_t launch_ex(K kernel, const A& args, unsigned grid, size_t smem, bool 
 
 }  // namespace
 
-size_t gate_up_smem_bytes(const GateUpArgs& a, bool pair, int grid) {
-    const int shp = a.gu ? (a.Is + grid - 1) / grid : 0;
-    return pair ? gate_up_layout<true>(a.T, a.H, shp, a.res_items, a.nslots, a.slot_pairs).total
-                : gate_up_layout<false>(a.T, a.H, shp, a.res_items, a.nslots, a.slot_pairs).total;
+size_t gate_up_smem_bytes(const GateUpArgs& a, bool pair) {
+    return pair ? gate_up_layout<true>(a.T, a.H, a.res_items, a.nslots).total
+                : gate_up_layout<false>(a.T, a.H, a.res_items, a.nslots).total;
 }
 size_t down_smem_bytes(const DownArgs& a) { return down_layout(a).total; }
 
@@ -770,7 +801,7 @@ cudaError_t launch_gate_up(const GateUpArgs& a, bool pair, const DevInfo& d, boo
     cudaError_t e = pair ? configure_smem(gate_up_kernel<true>, d, cfg_pair)
                          : configure_smem(gate_up_kernel<false>, d, cfg_rows);
     if (e != cudaSuccess) return e;
-    const size_t smem = gate_up_smem_bytes(a, pair, d.sm_count);
+    const size_t smem = gate_up_smem_bytes(a, pair);
     return pair ? launch_ex(gate_up_kernel<true>, a, (unsigned)d.sm_count, smem, pdl, s)
                 : launch_ex(gate_up_kernel<false>, a, (unsigned)d.sm_count, smem, pdl, s);
 }

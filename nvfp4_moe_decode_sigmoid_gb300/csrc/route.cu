@@ -85,6 +85,14 @@ __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s(wrows, a.wr + (size_t)r0 * H, bytes, bar);
     }
+    if (tid == kThreads - 1) {
+        prefetch_range(a.x, 2 * (size_t)T * H);
+        prefetch_range(a.bias, 4 * (size_t)a.E);
+        prefetch_range(a.logits, 4 * (size_t)T * a.E);
+        prefetch_range(a.counter, 8);
+        prefetch_range(a.ids, 4 * (size_t)T * a.k);
+        prefetch_range(a.weights, 4 * (size_t)T * a.k);
+    }
     __syncthreads();  // the barrier is initialised before anyone waits on it
     pdl_wait();  // x may come from the previous kernel
     // Dependents start only now: the gate/up kernel may then read x before its
