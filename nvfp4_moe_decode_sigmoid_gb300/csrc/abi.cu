@@ -98,7 +98,7 @@ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 // Shared memory a launch may take, leaving room for the kernel's static data.
 constexpr size_t kSmemSlack = 1024;
 
-// Per-warp ring of the gate/up kernel: up to 3 slots of one item (a copy in
+// Per-warp ring of the gate/up kernel: up to 4 slots of one item (a copy in
 // flight while the previous item is computed), fewer when a warp has less
 // work or the CTA would not fit in shared memory. `items` bounds the work
 // items of one CTA (their raw sums stay in shared memory). Returns false when
@@ -106,7 +106,7 @@ constexpr size_t kSmemSlack = 1024;
 bool gate_up_shape(flint::GateUpArgs& a, bool pair, int smem_optin, long long items) {
     a.res_items = (int)items;
     const int per_warp = ceil_div(items, flint::kGemvWarps);
-    for (int ns = per_warp < 1 ? 1 : (per_warp > 3 ? 3 : per_warp); ns >= 1; --ns) {
+    for (int ns = per_warp < 1 ? 1 : (per_warp > 4 ? 4 : per_warp); ns >= 1; --ns) {
         a.nslots = ns;
         if (flint::gate_up_smem_bytes(a, pair) + kSmemSlack <= (size_t)smem_optin) return true;
     }
@@ -115,7 +115,7 @@ bool gate_up_shape(flint::GateUpArgs& a, bool pair, int smem_optin, long long it
 
 // Shapes of the down kernel: tasks of 16 rows when every task of a warp can
 // be in flight at once, else whichever of 16 or 8 rows keeps the larger share
-// of a warp's tasks in flight (up to 3 slots per warp). Returns false when
+// of a warp's tasks in flight (up to 4 slots per warp). Returns false when
 // the layer does not fit.
 bool down_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
     a.rows_max = ceil_div(a.H, sm_count);
@@ -128,7 +128,7 @@ bool down_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
     flint::DownArgs best = a;
     for (int rg : {16, 8}) {
         const int per_warp = ceil_div((long long)units * ceil_div(a.rows_max, rg), flint::kGemvWarps);
-        for (int ns = per_warp < 3 ? per_warp : 3; ns >= 1; --ns) {
+        for (int ns = per_warp < 4 ? per_warp : 4; ns >= 1; --ns) {
             flint::DownArgs t = a;
             t.rg = rg;
             t.nslots = ns;

@@ -8,9 +8,9 @@
 // rounding. Section "Model architecture": weight-only NVFP4 (W4A16) with bf16
 // activations; every kernel follows the reference's rounding points.
 //
-// Both kernels run one CTA of 32 warps per SM. Each warp streams its own work
+// Both kernels run one CTA of 24 warps per SM. Each warp streams its own work
 // items (weight rows) through a private ring of shared-memory slots, copied
-// by all 32 of its lanes with 16-byte cp.async (one commit group per item).
+// by all its lanes with 16-byte cp.async (one commit group per item).
 // 1-D bulk copies were tried first: one item's rows are only 1-4 KB, and at
 // that size the bulk-copy path delivered well under half of the HBM
 // bandwidth, while per-lane 16-byte copies saturate it. Dequantisation happens
