@@ -66,6 +66,12 @@ enum { FLINT_EPILOGUE_NONE = 0, FLINT_EPILOGUE_SWIGLU = 1 };
  * weights first and waits for the previous kernel before it reads any input
  * that kernel could have written. */
 enum { FLINT_PDL = 1u << 0 };
+/* flags, with FLINT_PDL, for flint_moe_gate_up / flint_moe_decode: the
+ * previous kernel on the stream is flint_moe_route on the same x. The router
+ * triggers its dependents only after its own wait, so x is complete when the
+ * gate/up kernel starts and is staged before that kernel's wait. Do not set it
+ * after any other kernel. */
+enum { FLINT_PDL_AFTER_ROUTE = 1u << 1 };
 
 /* Largest batch of the decode path (the low-latency bound of up to 8 requests). */
 #define FLINT_MAX_TOKENS 8
@@ -248,6 +254,33 @@ flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* we
 flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, const float* weights, int k,
                                 const flint_experts* routed, const flint_experts* shared, flint_bf16* y,
                                 void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/*
+ * flint_moe_layer -- the whole decode step of one MoE layer in ONE kernel:
+ * router GEMV + sigmoid top-k + renormalisation (as flint_moe_route), the
+ * gate/up GEMVs + SiLU and the down GEMVs + combine (as flint_moe_decode).
+ * ("Optimizations": the small-batch MoE path fuses the routing and the
+ * combine into the neighbouring expert GEMVs and chains them with PDL; here
+ * the three steps meet at two grid-wide barriers inside one launch, one CTA
+ * per SM, all CTAs resident by a cooperative launch.)
+ *   x [T, H] bf16 (H = routed->hidden), router_w [E, H] bf16 with E =
+ *   routed->num_experts, bias [E] FP32 or NULL, 1 <= k <= min(8, E).
+ *   ids [T, k] int32 and weights [T, k] FP32 are written (as flint_moe_route
+ *   would); y [T, H] bf16 out. shared may be NULL.
+ *   ws: the layer's workspace (flint_workspace_bytes(E, k, inter, inter_shared)),
+ *   initialised once; its header also holds the grid barrier's counters, which
+ *   a completed call leaves ready for the next. A grid barrier that waits too
+ *   long records FLINT_ERR_TIMEOUT in the status word (flint_workspace_check)
+ *   instead of hanging; re-initialise the workspace after such an error.
+ *   flags: FLINT_PDL lets the launch overlap the previous kernel of the stream
+ *   (this kernel waits for it before reading x).
+ *   Errors: FLINT_ERR_UNSUPPORTED when one CTA's shared memory cannot hold
+ *   the layer's working set or the device cannot co-schedule one CTA per SM.
+ */
+flint_status_t flint_moe_layer(const flint_bf16* x, int T, const flint_bf16* router_w, int E, const float* bias,
+                               int k, const flint_experts* routed, const flint_experts* shared, int32_t* ids,
+                               float* weights, flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
+                               void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Dense GEMV on packed weights                                              */

@@ -147,6 +147,33 @@ bool down_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
     return found;
 }
 
+// Shapes of the fused layer kernel: gate/up ring slots (up to 4 per warp),
+// down tasks of 16 or 8 rows with up to 4 slots, shrunk until the CTA fits.
+bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
+    const int G = sm_count;
+    const long long units = a.T * a.k < a.E ? a.T * a.k : a.E;
+    a.rpc = ceil_div(a.E, G);
+    a.shp = a.Is > 0 ? ceil_div(a.Is, G) : 0;
+    a.rows_max = ceil_div(a.H, G);
+    const int routed_items = ceil_div(units * a.I, G);
+    a.res_items = a.shp + routed_items;
+    const int per_warp3 = ceil_div(routed_items, flint::kLayerWarps);
+    const long long rs_r = flint::nvfp4_row_stride(a.I);
+    for (int rg : {16, 8}) {
+        const int per_warp4 = ceil_div(units * ceil_div(a.rows_max, rg), flint::kLayerWarps);
+        for (int ns3 = per_warp3 < 1 ? 1 : (per_warp3 > 4 ? 4 : per_warp3); ns3 >= 1; --ns3) {
+            for (int ns4 = per_warp4 < 1 ? 1 : (per_warp4 > 4 ? 4 : per_warp4); ns4 >= 1; --ns4) {
+                a.ns3 = ns3;
+                a.rg = rg;
+                a.ns4 = ns4;
+                a.slot4 = (int)(rg * rs_r);
+                if (flint::layer_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin) return true;
+            }
+        }
+    }
+    return false;
+}
+
 }  // namespace
 
 extern "C" {
@@ -194,7 +221,7 @@ flint_status_t flint_workspace_check(void* ws, size_t ws_bytes, void* stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status");
     if (st & (flint::kStatusTimeoutRoute | flint::kStatusTimeoutGateUp | flint::kStatusTimeoutDown |
-              flint::kStatusTimeoutSelftest))
+              flint::kStatusTimeoutSelftest | flint::kStatusTimeoutLayer))
         return fail(FLINT_ERR_TIMEOUT, "device wait timed out (status 0x%x)", st);
     return fail(FLINT_ERR_INVALID_ARG, "an expert id was outside [0, num_experts) (status 0x%x)", st);
 }
@@ -381,6 +408,51 @@ flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, 
     s = flint_moe_gate_up(x, T, ids, k, routed, shared, ws, ws_bytes, flags, stream);
     if (s != FLINT_OK) return s;
     return flint_moe_down_combine(T, ids, weights, k, routed, shared, y, ws, ws_bytes, flags, stream);
+}
+
+flint_status_t flint_moe_layer(const flint_bf16* x, int T, const flint_bf16* router_w, int E, const float* bias, int k,
+                               const flint_experts* routed, const flint_experts* shared, int32_t* ids, float* weights,
+                               flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags, void* stream) {
+    flint_status_t s = moe_common("layer", T, k, routed, shared, true);
+    if (s != FLINT_OK) return s;
+    if (E != routed->num_experts)
+        return fail(FLINT_ERR_INVALID_ARG, "layer: router has %d rows, routed experts %d", E, routed->num_experts);
+    if (!x || !router_w || !ids || !weights || !y || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) ||
+        !aligned(weights, 4) || !aligned(y, 16) || (bias && !aligned(bias, 4)))
+        return fail(FLINT_ERR_INVALID_ARG, "layer: null or misaligned pointer");
+    const int Is = shared ? shared->inter : 0;
+    const flint::WsLayout W = flint::ws_layout(E, k, routed->inter, Is);
+    if ((s = check_ws(ws, ws_bytes, W.total)) != FLINT_OK) return s;
+    DevInfo d;
+    if ((s = device_info(d)) != FLINT_OK) return s;
+    flint::LayerArgs a = {};
+    a.x = x;
+    a.T = T;
+    a.H = routed->hidden;
+    a.wr = router_w;
+    a.E = E;
+    a.bias = bias;
+    a.k = k;
+    a.ids = ids;
+    a.weights = weights;
+    a.logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + W.logits_off);
+    a.status = ws_status(ws);
+    a.bar_ticket = reinterpret_cast<uint32_t*>(ws) + 2;
+    a.gu = static_cast<const uint8_t*>(routed->gate_up);
+    a.down = static_cast<const uint8_t*>(routed->down);
+    a.I = routed->inter;
+    a.ts = routed->tensor_scale;
+    a.s_gu = shared ? static_cast<const uint8_t*>(shared->gate_up) : nullptr;
+    a.s_down = shared ? static_cast<const uint8_t*>(shared->down) : nullptr;
+    a.Is = Is;
+    a.s_ts = shared ? shared->tensor_scale : nullptr;
+    a.h_routed = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + W.h_routed_off);
+    a.h_shared = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + W.h_shared_off);
+    a.y = y;
+    if (!layer_shape(a, d.sm_count, d.smem_optin))
+        return fail(FLINT_ERR_UNSUPPORTED, "layer: shapes exceed one CTA's shared memory");
+    cudaError_t e = flint::launch_layer(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "layer launch");
 }
 
 flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* W, int epilogue, flint_bf16* y,

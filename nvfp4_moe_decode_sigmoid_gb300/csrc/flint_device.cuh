@@ -146,6 +146,51 @@ __device__ __forceinline__ float ld_cg(const float* p) { return __ldcg(p); }
 __device__ __forceinline__ uint4 ld_cg(const uint4* p) { return __ldcg(p); }
 __device__ __forceinline__ uint2 ld_cg(const uint2* p) { return __ldcg(p); }
 
+// Acquire load at GPU scope (a flag written by another CTA).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid-wide barrier for a grid whose CTAs are all resident at once (a
+// cooperative launch), on a ticket counter that only ever grows: thread 0 of
+// each CTA takes a ticket with a release add (publishing the CTA's writes,
+// which the __syncthreads before it ordered) and waits with acquire loads
+// until all gridDim.x tickets of its round are taken. One atomic round trip
+// and no reset (measured about half the cost of a count + generation pair).
+// The counter must start at a multiple of gridDim.x and only this barrier may
+// touch it. The wait gives up after kWaitBudgetNs: `code` is set in *status,
+// false is returned and the CTA stops instead of hanging.
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ bool grid_sync(uint32_t* ticket, uint32_t* status, uint32_t code) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        const uint32_t t = atom_add_release_gpu(ticket, 1u);
+        const uint32_t target = (t / gridDim.x + 1u) * gridDim.x;
+        if ((int)(ld_acquire_gpu(ticket) - target) < 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while ((int)(ld_acquire_gpu(ticket) - target) < 0) {
+                if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+                    atomicOr(status, code);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
 // ---------------------------------------------------------------------------
 // bf16 helpers
 // ---------------------------------------------------------------------------

@@ -28,6 +28,7 @@ enum : uint32_t {
     kStatusTimeoutDown = 1u << 2,
     kStatusTimeoutSelftest = 1u << 3,
     kStatusBadExpertId = 1u << 4,
+    kStatusTimeoutLayer = 1u << 5,
 };
 
 constexpr int kThreads = 256;       // router kernel: 8 warps
@@ -38,7 +39,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kGemvWarps = 24;
 constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kMaxSlotsPerWarp = 4;
-constexpr size_t kWsHeader = 256;   // counter (word 0), status (word 1)
+constexpr size_t kWsHeader = 256;   // router counter (word 0), status (word 1), grid barrier tickets (word 2)
+// Fused layer kernel: one cooperative CTA per SM.
+constexpr int kLayerWarps = 24;
+constexpr int kLayerThreads = kLayerWarps * 32;
 
 FLINT_HD constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -118,6 +122,38 @@ struct DownArgs {
     int slot_bytes;           // bytes of one slot
 };
 
+// The whole MoE decode step of one layer (router, gate/up, down, combine).
+struct LayerArgs {
+    const uint16_t* x;
+    int T, H;
+    const uint16_t* wr;  // router [E, H] bf16
+    int E;
+    const float* bias;   // [E] or null
+    int k;
+    int32_t* ids;        // [T][k] out
+    float* weights;      // [T][k] out
+    float* logits;       // workspace [8][E]
+    uint32_t* bar_ticket; // workspace word 2: grid barrier tickets (a multiple of the grid size between calls)
+    uint32_t* status;    // workspace word 1
+    const uint8_t* gu;   // routed E x [2I, H]
+    const uint8_t* down; // routed E x [H, I]
+    int I;
+    const float* ts;     // [E][3]
+    const uint8_t* s_gu; // shared [2Is, H] or null
+    const uint8_t* s_down;
+    int Is;
+    const float* s_ts;
+    uint16_t* h_routed;  // workspace [8][k][I]
+    uint16_t* h_shared;  // workspace [8][Is]
+    uint16_t* y;         // [T][H] out
+    int rpc;             // router rows per CTA
+    int shp;             // shared-expert pairs per CTA (bound)
+    int rows_max;        // output rows per CTA (bound)
+    int res_items;       // gate/up items per CTA (bound)
+    int ns3;             // gate/up ring slots per warp
+    int rg, ns4, slot4;  // down: rows per task, ring slots per warp, bytes per slot
+};
+
 // ---------------------------------------------------------------------------
 // Launchers (return the CUDA error of the launch)
 // ---------------------------------------------------------------------------
@@ -137,6 +173,10 @@ cudaError_t launch_route(const RouteArgs& a, const DevInfo& d, bool pdl, cudaStr
 cudaError_t launch_gate_up(const GateUpArgs& a, bool pair, const DevInfo& d, bool pdl, cudaStream_t s);
 cudaError_t launch_down(const DownArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t budget_ns, cudaStream_t s);
+// Cooperative launch of the fused layer kernel, one CTA on every SM (with the
+// programmatic-dependent-launch attribute when `pdl`).
+cudaError_t launch_layer(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
+size_t layer_smem_bytes(const LayerArgs& a);
 
 // Allows `kernel` the device's opt-in dynamic shared memory, less its own
 // static shared memory (once per device and kernel).

@@ -43,216 +43,14 @@
 //   the lanes splitting the 16-value blocks of the row, and a reduce-scatter
 //   of the per-row sums over the lanes. Then the CTA combines
 //   y = bf16(sum_j w_j d_j + d_shared) in rank order. No atomics: the result is
-//   deterministic. Weight rows are requested before the PDL wait (the routing
-//   is final by then).
-#include "flint_device.cuh"
+//   deterministic. Weight rows are requested right after the PDL wait, behind
+//   the small loads of h and the scales.
+#include "expert_common.cuh"
 
 namespace flint {
 namespace {
 
 constexpr int kW = kGemvWarps;
-constexpr int kMaxDistinct = FLINT_MAX_TOKENS * FLINT_MAX_TOPK;
-
-// Per-CTA view of the routing: the distinct selected experts in ascending id
-// order and, for each, which ranks of which tokens chose it.
-struct RouteInfo {
-    uint32_t bitmap[FLINT_MAX_EXPERTS / 32];
-    uint32_t base[FLINT_MAX_EXPERTS / 32];
-    int32_t dlist[kMaxDistinct];
-    unsigned long long dmask[kMaxDistinct];  // byte t: ranks j with ids[t][j] == dlist[d]
-    uint32_t tmask[kMaxDistinct];            // bit t: token t chose dlist[d]
-    int32_t ids[kMaxDistinct];               // ids[t*k+j], -1 if out of range
-    int D;
-};
-
-__device__ void build_route_info(RouteInfo& ri, const int32_t* ids, int T, int k, int E, uint32_t* status) {
-    const int tid = threadIdx.x, nt = blockDim.x;
-    for (int i = tid; i < FLINT_MAX_EXPERTS / 32; i += nt) ri.bitmap[i] = 0;
-    for (int i = tid; i < kMaxDistinct; i += nt) {
-        ri.dmask[i] = 0ull;
-        ri.tmask[i] = 0u;
-    }
-    __syncthreads();
-    int e = -1;
-    if (tid < T * k) {
-        e = ld_cg(ids + tid);
-        if (e >= 0 && e < E) {
-            atomicOr(&ri.bitmap[e >> 5], 1u << (e & 31));
-        } else {
-            if (status) atomicOr(status, kStatusBadExpertId);
-            e = -1;
-        }
-        ri.ids[tid] = e;
-    }
-    __syncthreads();
-    if (tid < 32) {  // exclusive prefix sum of popcounts over the bitmap words
-        const int nb = (E + 31) / 32;
-        const uint32_t cnt = tid < nb ? __popc(ri.bitmap[tid]) : 0u;
-        uint32_t incl = cnt;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (tid >= off) incl += v;
-        }
-        ri.base[tid] = incl - cnt;
-        if (tid == 31) ri.D = (int)incl;
-    }
-    __syncthreads();
-    if (e >= 0) {
-        const int d = (int)(ri.base[e >> 5] + __popc(ri.bitmap[e >> 5] & ((1u << (e & 31)) - 1u)));
-        const int t = tid / k, j = tid % k;
-        ri.dlist[d] = e;
-        atomicOr(&ri.dmask[d], 1ull << (8 * t + j));
-        atomicOr(&ri.tmask[d], 1u << t);
-    }
-    __syncthreads();
-}
-
-__device__ __forceinline__ uint32_t rank_bits(unsigned long long dm, int t) {
-    return (uint32_t)((dm >> (8 * t)) & 0xFFull);
-}
-
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.f + expf(-g)); }
-
-// acc0/acc1 += the 8 products of one code word (4 f16x2) with its 8
-// activations (one 16-byte word of 4 f16x2).
-__device__ __forceinline__ void fma8(const uint32_t (&c)[4], const uint4 xv, float& acc0, float& acc1) {
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        acc0 = fma_lo_f16(c[q], xw[q], acc0);
-        acc1 = fma_hi_f16(c[q], xw[q], acc1);
-    }
-}
-
-// Sums each of M values (M a power of two, at most 32) over the warp's lanes.
-// Halving steps: at offset 16 >> s the lanes with that bit set keep the upper
-// half of their remaining values and hand the lower half to their partner
-// (one shuffle per value kept), so M sums cost about M shuffles instead of
-// 5 M. Lane l ends up with the sum of value rs_index<M>(l); 32 / M lanes hold
-// each value.
-template <int M>
-__device__ __forceinline__ float reduce_scatter(float (&v)[M], int lane) {
-#pragma unroll
-    for (int s = 0; (M >> s) > 1; ++s) {
-        const int w = M >> s, off = 16 >> s;
-        const bool up = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < w / 2; ++i) {
-            const float keep = up ? v[i + w / 2] : v[i];
-            const float send = up ? v[i] : v[i + w / 2];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-    }
-    float r = v[0];
-#pragma unroll
-    for (int off = 16 / M; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
-    return r;
-}
-
-template <int M>
-__device__ __forceinline__ int rs_index(int lane) {
-    int idx = 0;
-#pragma unroll
-    for (int s = 0; (M >> s) > 1; ++s)
-        if (lane & (16 >> s)) idx += M >> (s + 1);
-    return idx;
-}
-
-// ===========================================================================
-// Activation staging: bf16 vectors in global memory -> chunk-scaled f16 in
-// shared memory. One thread moves one 32-value chunk (its four 16-byte loads
-// issued together). csc[v * (K / 32) + c] = 2^s multiplies chunk c's partial
-// dot product back.
-//   GATE order (K % 1024 == 0): word w (0..3, 8 values each) of chunk c at
-//     16-byte index (c / 32) * 128 + w * 32 + c % 32 of the vector: lane l
-//     reads chunk l + 32 m's words at (m * 4 + w) * 32 + l.
-//   DOWN order (K % 32 == 0): the two words of 16-value block b at indices b
-//     and nb + b (nb = K / 16): lane l reads block l + 32 m at l + 32 m and
-//     nb + l + 32 m.
-// ===========================================================================
-// One staging source: nvec bf16 vectors of K values.
-struct StageSrc {
-    const uint16_t* src;
-    uint4* dst;
-    float* csc;
-    int nvec, K;
-};
-
-// Chunk q of the concatenated sources: its source and offset; false past the end.
-template <int NS>
-__device__ __forceinline__ bool stage_locate(const StageSrc (&ss)[NS], int q, int& s, int& v, int& c) {
-#pragma unroll
-    for (int i = 0; i < NS; ++i) {
-        const int cpv = ss[i].K / 32, n = ss[i].nvec * cpv;
-        if (q < n) {
-            s = i;
-            v = q / cpv;
-            c = q - v * cpv;
-            return true;
-        }
-        q -= n;
-    }
-    return false;
-}
-
-__device__ __forceinline__ void stage_load(const StageSrc& ss, int v, int c, uint4 (&w)[4]) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(ss.src + (size_t)v * ss.K + 32 * c);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) w[i] = ld_cg(s4 + i);
-}
-
-template <bool DOWN_ORDER>
-__device__ __forceinline__ void stage_store(const StageSrc& ss, int v, int c, const uint4 (&w)[4]) {
-    uint32_t m2 = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        m2 = __vmaxu2(m2, w[i].x & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, w[i].y & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, w[i].z & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, w[i].w & 0x7FFF7FFFu);
-    }
-    // bf16 exponent field of the largest magnitude -> s with max * 2^-s in [2^14, 2^15)
-    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-    const int sh = min(126, max(-126, (int)(m >> 7) - 141));
-    const float down = __int_as_float((127 - sh) << 23);
-    const int K = ss.K;
-    ss.csc[v * (K / 32) + c] = __int_as_float((127 + sh) << 23);
-    uint4* d = ss.dst + (size_t)v * (K / 8);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int idx;
-        if (DOWN_ORDER) {
-            idx = (i & 1) * (K / 16) + 2 * c + (i >> 1);
-        } else {
-            idx = (c / 32) * 128 + i * 32 + c % 32;
-        }
-        d[idx] = make_uint4(f32x2_to_f16x2(bf16_lo(w[i].x) * down, bf16_hi(w[i].x) * down),
-                            f32x2_to_f16x2(bf16_lo(w[i].y) * down, bf16_hi(w[i].y) * down),
-                            f32x2_to_f16x2(bf16_lo(w[i].z) * down, bf16_hi(w[i].z) * down),
-                            f32x2_to_f16x2(bf16_lo(w[i].w) * down, bf16_hi(w[i].w) * down));
-    }
-}
-
-// Stages the sources; every thread first issues the loads of its first chunk,
-// then runs `between` (the callers issue their weight copies there, so that
-// these small loads are not queued behind the weight stream), then converts.
-// Further chunks (more than one per thread) are loaded and converted after.
-template <bool DOWN_ORDER, int NS, typename F>
-__device__ __forceinline__ void stage_f16(const StageSrc (&ss)[NS], F&& between) {
-    int s0 = 0, v0 = 0, c0 = 0;
-    uint4 w[4];
-    const bool have = stage_locate(ss, threadIdx.x, s0, v0, c0);
-    if (have) stage_load(ss[s0], v0, c0, w);
-    between();
-    if (have) stage_store<DOWN_ORDER>(ss[s0], v0, c0, w);
-    for (int q = threadIdx.x + kGemvThreads;; q += kGemvThreads) {
-        int s, v, c;
-        if (!stage_locate(ss, q, s, v, c)) break;
-        stage_load(ss[s], v, c, w);
-        stage_store<DOWN_ORDER>(ss[s], v, c, w);
-    }
-}
 
 // ===========================================================================
 // gate/up + SiLU (PAIR) or plain rows
@@ -276,110 +74,6 @@ __host__ __device__ inline GateUpSmem gate_up_layout(int T, int H, int items, in
     L.slot = (size_t)(PAIR ? 2 : 1) * nvfp4_row_stride(H);
     L.total = L.ring + (size_t)kW * nslots * L.slot;
     return L;
-}
-
-// One pass of a warp over gate row `grow` (and up row `urow`) against the NT
-// (1 or 2) tokens tk[]: the lanes split the row into 32-value chunks
-// (lane l: chunks l, l + 32, ...); the per-lane sums are reduce-scattered and
-// the lanes holding them store the raw sums (before the tensor scale) at
-// resg[t] / resu[t].
-template <bool PAIR, int NT>
-__device__ __forceinline__ void gate_up_pass(const uint8_t* grow, const uint8_t* urow, int H, const uint4* xh,
-                                             const float* csc, const int (&tk)[NT], int lane, float* resg,
-                                             float* resu) {
-    constexpr int M = PAIR ? 2 * NT : NT;
-    const uint4* xb[NT];
-    const float* cb[NT];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        xb[j] = xh + (size_t)tk[j] * (H / 8) + lane;
-        cb[j] = csc + (size_t)tk[j] * (H / 32) + lane;
-    }
-    const uint4* g4 = reinterpret_cast<const uint4*>(grow) + lane;
-    const uint4* u4 = reinterpret_cast<const uint4*>(urow) + lane;
-    const uint16_t* gsc = reinterpret_cast<const uint16_t*>(grow + H / 2) + lane;
-    const uint16_t* usc = reinterpret_cast<const uint16_t*>(urow + H / 2) + lane;
-    float acc[M];
-#pragma unroll
-    for (int i = 0; i < M; ++i) acc[i] = 0.f;
-    const int nch = H >> 10;
-#pragma unroll 1
-    for (int ch = 0; ch < nch; ++ch) {
-        const uint4 gq = g4[32 * ch];
-        const float2 gs = ue4m3x2_to_float2(gsc[32 * ch]);
-        uint4 uq = make_uint4(0u, 0u, 0u, 0u);
-        float2 us = make_float2(0.f, 0.f);
-        if (PAIR) {
-            uq = u4[32 * ch];
-            us = ue4m3x2_to_float2(usc[32 * ch]);
-        }
-        const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w}, uw[4] = {uq.x, uq.y, uq.z, uq.w};
-        float cg[NT], cu[NT];
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {  // one scale block: code words 2 hf, 2 hf + 1
-            float g0[NT], g1[NT], u0[NT], u1[NT];
-#pragma unroll
-            for (int j = 0; j < NT; ++j) g0[j] = g1[j] = u0[j] = u1[j] = 0.f;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int w = 2 * hf + h2;
-                uint32_t hg[4], hu[4];
-                decode_word_h2(gw[w], hg);
-                if (PAIR) decode_word_h2(uw[w], hu);
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const uint4 xv = xb[j][(ch * 4 + w) * 32];
-                    fma8(hg, xv, g0[j], g1[j]);
-                    if (PAIR) fma8(hu, xv, u0[j], u1[j]);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                if (hf == 0) {
-                    cg[j] = gs.x * (g0[j] + g1[j]);
-                    if (PAIR) cu[j] = us.x * (u0[j] + u1[j]);
-                } else {
-                    cg[j] = fmaf(gs.y, g0[j] + g1[j], cg[j]);
-                    if (PAIR) cu[j] = fmaf(us.y, u0[j] + u1[j], cu[j]);
-                }
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const float xs = cb[j][32 * ch];
-            acc[j] = fmaf(xs, cg[j], acc[j]);
-            if (PAIR) acc[NT + j] = fmaf(xs, cu[j], acc[NT + j]);
-        }
-    }
-    const float r = reduce_scatter<M>(acc, lane);
-    if (lane % (32 / M) == 0) {
-        const int idx = rs_index<M>(lane);  // [gate of tk[0..NT), up of tk[0..NT)]
-        const int j = idx % NT;
-        int t = tk[0];
-#pragma unroll
-        for (int jj = 1; jj < NT; ++jj)
-            if (j == jj) t = tk[jj];
-        (idx < NT ? resg : resu)[t] = r;
-    }
-}
-
-// All tokens of `tmask` against one item, two per pass.
-template <bool PAIR>
-__device__ __forceinline__ void gate_up_item(const uint8_t* grow, const uint8_t* urow, int H, const uint4* xh,
-                                             const float* csc, uint32_t tmask, int lane, float* resg,
-                                             float* resu) {
-    while (tmask) {
-        const int t0 = __ffs(tmask) - 1;
-        tmask &= tmask - 1u;
-        if (tmask) {
-            const int tk[2] = {t0, __ffs(tmask) - 1};
-            tmask &= tmask - 1u;
-            gate_up_pass<PAIR, 2>(grow, urow, H, xh, csc, tk, lane, resg, resu);
-        } else {
-            const int tk[1] = {t0};
-            gate_up_pass<PAIR, 1>(grow, urow, H, xh, csc, tk, lane, resg, resu);
-        }
-    }
 }
 
 // Work items of a CTA: its slice [sp0, sp1) of the shared expert's pairs (or
@@ -574,46 +268,6 @@ __host__ __device__ inline DownSmem down_layout(const DownArgs& a) {
     L.ring = align_up(L.hs + 2 * (size_t)a.T * a.Is, 128);
     L.total = L.ring + (size_t)kW * a.nslots * a.slot_bytes;
     return L;
-}
-
-// One pass of a warp over RP rows (row r at rows + r RS, r < nr valid) of K
-// columns against NT tokens whose staged h vectors are hv[] (DOWN order) with
-// chunk scales cv[]: lane l takes the 16-value blocks l, l + 32, ...
-// acc[j * RP + r] gets the lane's part of row r . h_j.
-template <int RP, int NT>
-__device__ __forceinline__ void down_pass(const uint8_t* rows, int RS, int nr, int K, const uint4* const (&hv)[NT],
-                                          const float* const (&cv)[NT], int lane, float (&acc)[RP * NT]) {
-#pragma unroll
-    for (int i = 0; i < RP * NT; ++i) acc[i] = 0.f;
-    const int nb = K / 16;
-    for (int b = lane; b < nb; b += 32) {
-        uint4 x0[NT], x1[NT];
-        float xs[NT];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            x0[j] = hv[j][b];
-            x1[j] = hv[j][nb + b];
-            xs[j] = cv[j][b >> 1];
-        }
-#pragma unroll
-        for (int r = 0; r < RP; ++r) {
-            if (r < nr) {
-                const uint8_t* row = rows + (size_t)r * RS;
-                const uint2 q = *reinterpret_cast<const uint2*>(row + 8 * b);
-                const float s = ue4m3_to_float(row[K / 2 + b]);
-                uint32_t c0[4], c1[4];
-                decode_word_h2(q.x, c0);
-                decode_word_h2(q.y, c1);
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    float p0 = 0.f, p1 = 0.f;
-                    fma8(c0, x0[j], p0, p1);
-                    fma8(c1, x1[j], p0, p1);
-                    acc[j * RP + r] = fmaf(s * xs[j], p0 + p1, acc[j * RP + r]);
-                }
-            }
-        }
-    }
 }
 
 // Each CTA owns output rows [n0, n1). Units are the distinct selected experts

@@ -1,0 +1,419 @@
+// layer.cu -- the whole decode step of one MoE layer in one cooperative
+// kernel: router GEMV + sigmoid top-k, gate/up + SiLU, down + weighted
+// combine with the shared expert.
+//
+// "Day-0 Support for Flint on vLLM", section "Optimizations": the small-batch
+// MoE path is a short chain of kernels whose expert GEMVs read only the
+// selected experts' weights, with routing and the combine fused into the
+// neighbouring GEMVs. Here the chain is one launch: at batch 1 to 8 the
+// layer moves 13-80 MB, a few microseconds of HBM time, so the fixed cost of
+// each kernel boundary (launch, prologue, drain) is a large share; inside one
+// kernel the three steps meet at two grid-wide barriers instead.
+//
+// One CTA per SM, all resident (cooperative launch):
+//   0. Before the PDL wait: this CTA's router rows, its slice of the shared
+//      expert's gate/up pairs and its slice of the shared expert's down rows
+//      are copied into shared memory (static weights).
+//   1. x is staged (chunk-scaled f16, for gate/up); the CTA's router logits
+//      are computed in FP32 from bf16 x and bf16 router rows and written to
+//      the workspace. Grid barrier.
+//   2. Every CTA reads all logits and selects the top-k of every token itself
+//      (one warp per token), so no second barrier is needed to share the
+//      routing; CTA 0 also writes ids and weights out.
+//   3. gate/up + SiLU as in gate_up_kernel: the CTA's share of the routed
+//      pairs through per-warp cp.async rings, its shared-expert pairs from
+//      shared memory; h goes to the workspace. Grid barrier.
+//   4. down + combine as in down_kernel: h is staged, the CTA's output rows of
+//      every selected expert stream through per-warp rings (the shared
+//      expert's rows are already resident), then y = bf16(sum_j w_j d_j +
+//      d_shared) in rank order.
+#include "expert_common.cuh"
+#include "router_common.cuh"
+
+namespace flint {
+namespace {
+
+constexpr int kLW = kLayerWarps;
+constexpr int kLT = kLayerThreads;
+
+// Small per-CTA arrays: tensor scales (gate, up) of the distinct experts then
+// of the shared expert; down scales of the units; combine weights; ids.
+struct LayerSmall {
+    float tss[2 * kMaxDistinct + 2];
+    float tsd[kMaxDistinct + 1];
+    float w[kMaxDistinct];
+    int32_t ids[kMaxDistinct];
+};
+
+struct LayerSmem {
+    size_t ri, small, xs, csc, wrows, shgu, shdn, B;
+    size_t resg, resu, ring3, end3;
+    size_t hr, hs, csr, css, dval, ring4, end4;
+    size_t total;
+};
+
+__host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
+    LayerSmem L;
+    const size_t RS = (size_t)nvfp4_row_stride(a.H), RSs = a.Is ? (size_t)nvfp4_row_stride(a.Is) : 0;
+    const size_t T = a.T, H = a.H;
+    L.ri = 0;
+    L.small = align_up(sizeof(RouteInfo), 128);
+    L.xs = align_up(L.small + sizeof(LayerSmall), 128);
+    L.csc = align_up(L.xs + 2 * T * H, 128);
+    L.wrows = align_up(L.csc + sizeof(float) * T * (H / 32), 128);
+    L.shgu = align_up(L.wrows + 2 * (size_t)a.rpc * H, 128);
+    L.shdn = align_up(L.shgu + 2 * (size_t)a.shp * RS, 128);
+    L.B = align_up(L.shdn + (size_t)a.rows_max * RSs, 128);
+    // phase 3 (gate/up)
+    L.resg = L.B;
+    L.resu = align_up(L.resg + sizeof(float) * (size_t)a.res_items * T, 128);
+    L.ring3 = align_up(L.resu + sizeof(float) * (size_t)a.res_items * T, 128);
+    L.end3 = L.ring3 + (size_t)kLW * a.ns3 * 2 * RS;
+    // phase 4 (down), over the phase-3 region
+    L.hr = L.B;
+    L.hs = align_up(L.hr + 2 * T * a.k * a.I, 128);
+    L.csr = align_up(L.hs + 2 * T * a.Is, 128);
+    L.css = align_up(L.csr + sizeof(float) * T * a.k * (a.I / 32), 128);
+    L.dval = align_up(L.css + sizeof(float) * T * (a.Is / 32), 128);
+    L.ring4 = align_up(L.dval + sizeof(float) * T * (a.k + 1) * a.rows_max, 128);
+    L.end4 = L.ring4 + (size_t)kLW * a.ns4 * a.slot4;
+    L.total = L.end3 > L.end4 ? L.end3 : L.end4;
+    const size_t end2 = L.B + sizeof(uint32_t) * T * a.E;  // phase 2: sigmoid scores
+    if (L.total < end2) L.total = end2;
+    return L;
+}
+
+// All threads of the CTA copy `bytes` (a multiple of 16) from src to dst with
+// 16-byte cp.async (no commit).
+__device__ __forceinline__ void block_copy_async(void* dst, const void* src, size_t bytes) {
+    uint8_t* d = static_cast<uint8_t*>(dst);
+    const uint8_t* s = static_cast<const uint8_t*>(src);
+    for (size_t o = 16 * (size_t)threadIdx.x; o < bytes; o += 16 * (size_t)kLT) cp_async16(d + o, s + o);
+}
+
+__global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const LayerSmem L = layer_layout(a);
+    const int T = a.T, H = a.H, E = a.E, k = a.k, I = a.I, Is = a.Is, RM = a.rows_max;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x, G = gridDim.x;
+    RouteInfo& ri = *reinterpret_cast<RouteInfo*>(smem + L.ri);
+    LayerSmall& sm = *reinterpret_cast<LayerSmall*>(smem + L.small);
+    uint4* xh = reinterpret_cast<uint4*>(smem + L.xs);
+    float* csc = reinterpret_cast<float*>(smem + L.csc);
+    const uint16_t* wrows = reinterpret_cast<const uint16_t*>(smem + L.wrows);
+    uint8_t* shgu = smem + L.shgu;
+    uint8_t* shdn = smem + L.shdn;
+    const int RS = (int)nvfp4_row_stride(H), RSr = (int)nvfp4_row_stride(I);
+    const int RSs = Is ? (int)nvfp4_row_stride(Is) : 0;
+    const bool has_sh = a.s_gu != nullptr;
+
+    // This CTA's router rows, shared-expert pairs and output rows.
+    const int r0 = c * a.rpc, nrr = max(0, min(a.rpc, E - r0));
+    const int sp0 = (int)((unsigned)c * (unsigned)Is / (unsigned)G);
+    const int n_sh = has_sh ? (int)((unsigned)(c + 1) * (unsigned)Is / (unsigned)G) - sp0 : 0;
+    const int n0 = (int)((unsigned)c * (unsigned)H / (unsigned)G);
+    const int nr = (int)((unsigned)(c + 1) * (unsigned)H / (unsigned)G) - n0;
+
+    // ---- 0: static weights, before the PDL wait ------------------------------------
+    block_copy_async(smem + L.wrows, a.wr + (size_t)r0 * H, (size_t)nrr * H * 2);
+    if (n_sh > 0) {
+        block_copy_async(shgu, a.s_gu + (size_t)sp0 * RS, (size_t)n_sh * RS);
+        block_copy_async(shgu + (size_t)a.shp * RS, a.s_gu + (size_t)(Is + sp0) * RS, (size_t)n_sh * RS);
+        block_copy_async(shdn, a.s_down + (size_t)n0 * RSs, (size_t)nr * RSs);
+    }
+    cp_async_commit();
+    if (tid < 2 * kMaxDistinct + 2) sm.tss[tid] = 0.f;
+
+    pdl_wait();  // x comes from the previous kernel
+
+    // ---- 1: stage x; this CTA's router logits --------------------------------------
+    const StageSrc xsrc[1] = {{a.x, xh, csc, T, H}};
+    stage_f16<false>(xsrc, [] {});
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int q = warp; q < nrr * T; q += kLW) {
+        const int r = q / T, t = q - r * T;
+        const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
+        const uint4* wv = reinterpret_cast<const uint4*>(wrows + (size_t)r * H);
+        float s0 = 0.f, s1 = 0.f;
+        for (int ch = lane; ch < H / 8; ch += 32) {
+            const uint4 xv = ld_cg(xr + ch), w = wv[ch];
+            const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                s0 = fmaf(bf16_lo(wa[i]), bf16_lo(xa[i]), s0);
+                s1 = fmaf(bf16_hi(wa[i]), bf16_hi(xa[i]), s1);
+            }
+        }
+        float v = s0 + s1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) a.logits[(size_t)t * E + r0 + r] = v;
+    }
+    if (!grid_sync(a.bar_ticket, a.status, kStatusTimeoutLayer)) return;
+
+    // ---- 2: top-k of every token, in every CTA ------------------------------------
+    float* wsel = sm.w;
+    {
+        uint32_t* scores = reinterpret_cast<uint32_t*>(smem + L.B);  // region B is free until phase 3
+        sigmoid_scores(a.logits, a.bias, T, E, scores);
+        __syncthreads();
+        if (warp < T) {
+            const uint32_t* sc = scores + (size_t)warp * E;
+            if (E <= 256)
+                topk_warp<8>(sc, E, k, lane, sm.ids + warp * k, wsel + warp * k);
+            else
+                topk_warp<FLINT_MAX_EXPERTS / 32>(sc, E, k, lane, sm.ids + warp * k, wsel + warp * k);
+        }
+        __syncthreads();
+    }
+    if (c == 0 && tid < T * k) {
+        a.ids[tid] = sm.ids[tid];
+        a.weights[tid] = wsel[tid];
+    }
+    build_route_info<true>(ri, sm.ids, T, k, E, a.status);
+    const int D = ri.D;
+
+    // ---- 3: gate/up + SiLU ---------------------------------------------------------
+    {
+        float* resg = reinterpret_cast<float*>(smem + L.resg);
+        float* resu = reinterpret_cast<float*>(smem + L.resu);
+        const int NSW = a.ns3;
+        uint8_t* ring = smem + L.ring3 + (size_t)warp * NSW * 2 * RS;
+        const int RP = D * I;
+        const int rp0 = (int)((unsigned)c * (unsigned)RP / (unsigned)G);
+        const int nl = (int)((unsigned)(c + 1) * (unsigned)RP / (unsigned)G) - rp0;
+        const int lw0 = (int)((unsigned)warp * (unsigned)nl / (unsigned)kLW);
+        const int lw1 = (int)((unsigned)(warp + 1) * (unsigned)nl / (unsigned)kLW);
+        const int n_items_w = lw1 - lw0;
+        auto issue = [&](int m) {  // routed list item lw0 + m into slot m % NSW
+            const int q = rp0 + lw0 + m, d = q / I, p = q - d * I;
+            const uint8_t* g = a.gu + ((size_t)ri.dlist[d] * 2 * I + p) * RS;
+            uint8_t* slot = ring + (size_t)(m % NSW) * 2 * RS;
+            warp_copy_async(slot, g, RS, lane);
+            warp_copy_async(slot + RS, g + (size_t)I * RS, RS, lane);
+            cp_async_commit();
+        };
+        // scales first, then this warp's first copies
+        float tsv = 0.f;
+        if (tid < 2 * D) tsv = ld_cg(a.ts + 3 * ri.dlist[tid >> 1] + (tid & 1));
+        else if (tid < 2 * D + 2 && has_sh) tsv = ld_cg(a.s_ts + tid - 2 * D);
+        float tdv = 0.f;
+        if (tid >= 256 && tid < 256 + D) tdv = ld_cg(a.ts + 3 * ri.dlist[tid - 256] + 2);
+        else if (tid == 256 + D && has_sh) tdv = ld_cg(a.s_ts + 2);
+        for (int m = 0; m < NSW; ++m) {
+            if (m < n_items_w)
+                issue(m);
+            else
+                cp_async_commit();
+        }
+        if (tid < 2 * D + 2) sm.tss[tid] = tsv;
+        if (tid >= 256 && tid <= 256 + D) sm.tsd[tid - 256] = tdv;
+        const uint32_t all_tokens = (1u << T) - 1u;
+        // shared-expert pairs (resident): pair i by warp kLW - 1 - i
+        for (int i = kLW - 1 - warp; i < n_sh; i += kLW) {
+            const uint8_t* grow = shgu + (size_t)i * RS;
+            gate_up_item<true>(grow, grow + (size_t)a.shp * RS, H, xh, csc, all_tokens, lane, resg + i * T,
+                               resu + i * T);
+        }
+        int d = 0, p = 0;
+        if (n_items_w > 0) {
+            d = (rp0 + lw0) / I;
+            p = rp0 + lw0 - d * I;
+        }
+        for (int m = 0; m < n_items_w; ++m) {
+            cp_async_wait_n(NSW - 1);
+            __syncwarp();
+            const uint8_t* grow = ring + (size_t)(m % NSW) * 2 * RS;
+            const int item = n_sh + lw0 + m;
+            gate_up_item<true>(grow, grow + RS, H, xh, csc, ri.tmask[d], lane, resg + item * T, resu + item * T);
+            if (++p == I) {
+                p = 0;
+                ++d;
+            }
+            __syncwarp();
+            if (m + NSW < n_items_w)
+                issue(m + NSW);
+            else
+                cp_async_commit();
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+        const int n_items = n_sh + nl;
+        for (int e = tid; e < n_items * T; e += kLT) {
+            const int t = e / n_items, i = e - t * n_items;
+            float tsg, tsu;
+            int pp;
+            uint32_t ranks = 0;
+            if (i < n_sh) {
+                pp = sp0 + i;
+                tsg = sm.tss[2 * D];
+                tsu = sm.tss[2 * D + 1];
+            } else {
+                const int q = rp0 + i - n_sh, dd = q / I;
+                pp = q - dd * I;
+                ranks = rank_bits(ri.dmask[dd], t);
+                if (!ranks) continue;
+                tsg = sm.tss[2 * dd];
+                tsu = sm.tss[2 * dd + 1];
+            }
+            const float g = bf16_round_f32(tsg * resg[i * T + t]);
+            const float u = bf16_round_f32(tsu * resu[i * T + t]);
+            const uint16_t out = f32_to_bf16_bits(silu_f32(g) * u);
+            if (i < n_sh) {
+                a.h_shared[(size_t)t * Is + pp] = out;
+            } else {
+                for (int j = 0; j < k; ++j)
+                    if ((ranks >> j) & 1u) a.h_routed[((size_t)t * k + j) * I + pp] = out;
+            }
+        }
+    }
+    if (!grid_sync(a.bar_ticket, a.status, kStatusTimeoutLayer)) return;
+    pdl_launch_dependents();
+
+    // ---- 4: down + combine ---------------------------------------------------------
+    if (nr == 0) return;
+    {
+        uint4* hr = reinterpret_cast<uint4*>(smem + L.hr);
+        uint4* hs = reinterpret_cast<uint4*>(smem + L.hs);
+        float* csr = reinterpret_cast<float*>(smem + L.csr);
+        float* css = reinterpret_cast<float*>(smem + L.css);
+        float* dval = reinterpret_cast<float*>(smem + L.dval);
+        const int NSW = a.ns4, RG = a.rg;
+        uint8_t* ring = smem + L.ring4 + (size_t)warp * NSW * a.slot4;
+        const int ngr = (nr + RG - 1) / RG;
+        const int n_tasks = D * ngr;  // routed; the shared expert's groups are resident
+        const int my_tasks = n_tasks > warp ? (n_tasks - warp + kLW - 1) / kLW : 0;
+        auto issue = [&](int kk) {
+            const int q = warp + kk * kLW, u = q / ngr, r0g = (q - u * ngr) * RG, r1g = min(nr, r0g + RG);
+            uint8_t* dst = ring + (size_t)(kk % NSW) * a.slot4;
+            warp_copy_async(dst, a.down + ((size_t)ri.dlist[u] * H + n0 + r0g) * RSr, (r1g - r0g) * RSr, lane);
+            cp_async_commit();
+        };
+        const StageSrc hsrc[2] = {{a.h_routed, hr, csr, T * k, I}, {a.h_shared, hs, css, has_sh ? T : 0, Is ? Is : 32}};
+        stage_f16<true>(hsrc, [&] {
+            for (int kk = 0; kk < NSW; ++kk) {
+                if (kk < my_tasks)
+                    issue(kk);
+                else
+                    cp_async_commit();
+            }
+        });
+        __syncthreads();
+        // One task: rows [r0g, r1g) of unit u (u < D routed, from `rows`; u == D shared).
+        auto task = [&](int u, int r0g, int r1g, const uint8_t* rows) {
+            const bool sh = u >= D;
+            const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
+            const unsigned long long dm = sh ? 0ull : ri.dmask[u];
+            uint32_t rest = sh ? (1u << T) - 1u : ri.tmask[u];
+            const float tsd = sm.tsd[u];
+            auto vec = [&](int t, const uint4*& h, const float*& cs) {
+                if (sh) {
+                    h = hs + (size_t)t * (Is / 8);
+                    cs = css + (size_t)t * (Is / 32);
+                } else {
+                    const int j = __ffs(rank_bits(dm, t)) - 1;
+                    h = hr + ((size_t)t * k + j) * (I / 8);
+                    cs = csr + ((size_t)t * k + j) * (I / 32);
+                }
+            };
+            auto put = [&](float v, int r, int t) {
+                const float dv = bf16_round_f32(tsd * v);
+                if (sh) {
+                    dval[((size_t)t * (k + 1) + k) * RM + r] = dv;
+                } else {
+                    const uint32_t ranks = rank_bits(dm, t);
+                    for (int jj = 0; jj < k; ++jj)
+                        if ((ranks >> jj) & 1u) dval[((size_t)t * (k + 1) + jj) * RM + r] = dv;
+                }
+            };
+            while (rest) {
+                const int t0 = __ffs(rest) - 1;
+                rest &= rest - 1u;
+                if (rest) {  // two tokens, rows in groups of 8
+                    const int t1 = __ffs(rest) - 1;
+                    rest &= rest - 1u;
+                    const uint4* hv[2];
+                    const float* cv[2];
+                    vec(t0, hv[0], cv[0]);
+                    vec(t1, hv[1], cv[1]);
+                    for (int hb = 0; hb < RG && r0g + hb < r1g; hb += 8) {
+                        float acc[16];
+                        down_pass<8, 2>(rows + (size_t)hb * RSu, RSu, r1g - r0g - hb, K, hv, cv, lane, acc);
+                        const float v = reduce_scatter<16>(acc, lane);
+                        const int idx = rs_index<16>(lane), r = r0g + hb + (idx & 7);
+                        if ((lane & 1) == 0 && r < r1g) put(v, r, (idx >> 3) ? t1 : t0);
+                    }
+                } else {
+                    const uint4* hv[1];
+                    const float* cv[1];
+                    vec(t0, hv[0], cv[0]);
+                    for (int hb = 0; hb < RG && r0g + hb < r1g; hb += 8) {
+                        float acc[8];
+                        down_pass<8, 1>(rows + (size_t)hb * RSu, RSu, r1g - r0g - hb, K, hv, cv, lane, acc);
+                        const float v = reduce_scatter<8>(acc, lane);
+                        const int r = r0g + hb + rs_index<8>(lane);
+                        if ((lane & 3) == 0 && r < r1g) put(v, r, t0);
+                    }
+                }
+            }
+        };
+        // the shared expert's row groups (resident): group g by warp kLW - 1 - g
+        if (has_sh)
+            for (int g = kLW - 1 - warp; g < ngr; g += kLW)
+                task(D, g * RG, min(nr, (g + 1) * RG), shdn + (size_t)g * RG * RSs);
+        for (int kk = 0; kk < my_tasks; ++kk) {
+            cp_async_wait_n(NSW - 1);
+            __syncwarp();
+            const int q = warp + kk * kLW, u = q / ngr, r0g = (q - u * ngr) * RG;
+            task(u, r0g, min(nr, r0g + RG), ring + (size_t)(kk % NSW) * a.slot4);
+            __syncwarp();
+            if (kk + NSW < my_tasks)
+                issue(kk + NSW);
+            else
+                cp_async_commit();
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+        // combine, in rank order then the shared expert
+        for (int i = tid; i < T * nr; i += kLT) {
+            const int t = i / nr, r = i - t * nr;
+            float acc = 0.f;
+            for (int j = 0; j < k; ++j)
+                if (ri.ids[t * k + j] >= 0) acc = fmaf(wsel[t * k + j], dval[((size_t)t * (k + 1) + j) * RM + r], acc);
+            if (has_sh) acc += dval[((size_t)t * (k + 1) + k) * RM + r];
+            a.y[(size_t)t * H + n0 + r] = f32_to_bf16_bits(acc);
+        }
+    }
+}
+
+}  // namespace
+
+size_t layer_smem_bytes(const LayerArgs& a) { return layer_layout(a).total; }
+
+cudaError_t launch_layer(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
+    static int configured_for = -1;
+    cudaError_t e = configure_smem(layer_kernel, d, configured_for);
+    if (e != cudaSuccess) return e;
+    const size_t smem = layer_smem_bytes(a);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_kernel, kLT, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)d.sm_count);
+    cfg.blockDim = dim3(kLT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, layer_kernel, a);
+}
+
+}  // namespace flint

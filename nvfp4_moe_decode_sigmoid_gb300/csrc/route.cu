@@ -13,56 +13,16 @@
 // one warp per token, and leaves the ticket counter at zero.
 #include <cfloat>
 
-#include "flint_device.cuh"
+#include "router_common.cuh"
 
 namespace flint {
 namespace {
 
-// Top-k of one token's scores, one warp: lane holds experts lane + 32 i.
-// Sigmoid scores are positive floats, so their bit patterns order like the
-// values; the warp max of the bits picks the best score and a warp min over
-// the lanes' lowest matching index breaks ties toward the lower expert.
-template <int SLOTS>
-__device__ __forceinline__ void topk_warp(const float* logits, const float* bias, int E, int k, int lane,
-                                          int32_t* ids, float* weights) {
-    uint32_t s[SLOTS];
-#pragma unroll
-    for (int i = 0; i < SLOTS; ++i) {
-        const int e = lane + 32 * i;
-        uint32_t v = 0u;  // below every valid score bit pattern except +0
-        if (e < E) {
-            float z = ld_cg(logits + e);
-            if (bias) z = z + bias[e];
-            v = __float_as_uint(1.f / (1.f + expf(-z)));
-        }
-        s[i] = v;
-    }
-    uint32_t taken = 0;
-    float sel_s = 0.f, sum = 0.f;
-    int sel_e = 0;
-    for (int j = 0; j < k; ++j) {
-        uint32_t m = 0u;
-#pragma unroll
-        for (int i = 0; i < SLOTS; ++i)
-            if (!((taken >> i) & 1u) && lane + 32 * i < E) m = max(m, s[i]);
-        const uint32_t best = __reduce_max_sync(0xffffffffu, m);
-        uint32_t cand = 0xFFFFFFFFu;
-#pragma unroll
-        for (int i = SLOTS - 1; i >= 0; --i)
-            if (!((taken >> i) & 1u) && lane + 32 * i < E && s[i] == best) cand = (uint32_t)(lane + 32 * i);
-        const uint32_t e = __reduce_min_sync(0xffffffffu, cand);
-        if ((int)(e & 31u) == lane) taken |= 1u << (e >> 5);
-        const float sv = __uint_as_float(best);
-        sum += sv;
-        if (lane == j) {
-            sel_e = (int)e;
-            sel_s = sv;
-        }
-    }
-    if (lane < k) {
-        ids[lane] = sel_e;
-        weights[lane] = sel_s / sum;
-    }
+// Shared memory: mbarrier, per-warp partial logits, the CTA's router rows,
+// then (last CTA) the sigmoid scores of all tokens.
+__host__ __device__ inline size_t route_scores_offset(const RouteArgs& a) {
+    return 128 + align_up(sizeof(float) * kWarps * FLINT_MAX_TOKENS * a.rows_per_cta, 128) +
+           align_up((size_t)a.rows_per_cta * a.H * 2, 128);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
@@ -163,12 +123,15 @@ __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
     __syncthreads();
     if (!is_last) return;
 
+    uint32_t* scores = reinterpret_cast<uint32_t*>(smem + route_scores_offset(a));
+    sigmoid_scores(a.logits, a.bias, T, a.E, scores);
+    __syncthreads();
     if (warp < T) {
-        const float* lg = a.logits + (size_t)warp * a.E;
+        const uint32_t* sc = scores + (size_t)warp * a.E;
         if (a.E <= 256)
-            topk_warp<8>(lg, a.bias, a.E, a.k, lane, a.ids + warp * a.k, a.weights + warp * a.k);
+            topk_warp<8>(sc, a.E, a.k, lane, a.ids + warp * a.k, a.weights + warp * a.k);
         else
-            topk_warp<FLINT_MAX_EXPERTS / 32>(lg, a.bias, a.E, a.k, lane, a.ids + warp * a.k, a.weights + warp * a.k);
+            topk_warp<FLINT_MAX_EXPERTS / 32>(sc, a.E, a.k, lane, a.ids + warp * a.k, a.weights + warp * a.k);
     }
     __syncthreads();
     if (tid == 0) atomicExch(a.counter, 0u);
@@ -177,8 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
 }  // namespace
 
 size_t route_smem_bytes(const RouteArgs& a) {
-    return 128 + align_up(sizeof(float) * kWarps * FLINT_MAX_TOKENS * a.rows_per_cta, 128) +
-           align_up((size_t)a.rows_per_cta * a.H * 2, 128);
+    return route_scores_offset(a) + sizeof(uint32_t) * (size_t)a.T * a.E;
 }
 
 cudaError_t launch_route(const RouteArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {

@@ -30,6 +30,7 @@ FLINT_DTYPE_BF16 = 1
 FLINT_EPILOGUE_NONE = 0
 FLINT_EPILOGUE_SWIGLU = 1
 FLINT_PDL = 1
+FLINT_PDL_AFTER_ROUTE = 2
 FLINT_MAX_TOKENS = 8
 
 
@@ -76,6 +77,8 @@ def _load():
         "flint_dense_gemv": (i32, [vp, i32, C.POINTER(flint_packed), i32, vp, vp, sz, u32, vp]),
         "flint_selftest_wait_timeout": (i32, [vp, sz, C.c_uint64, vp]),
         "flint_moe_route_static": (i32, [vp, i32, i32, vp, i32, vp, i32, vp, vp, u32, vp]),
+        "flint_moe_layer": (i32, [vp, i32, vp, i32, vp, i32, C.POINTER(flint_experts), C.POINTER(flint_experts), vp,
+                                  vp, vp, vp, sz, u32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -250,6 +253,16 @@ def flint_moe_decode(x, ids, weights, routed: Experts, shared: Experts | None, y
     k = ids.shape[1]
     _check(_lib.flint_moe_decode(_ptr(x), T, _ptr(ids), _ptr(weights), k, _ex(routed), _ex(shared), _ptr(y),
                                  _ptr(ws), ws.numel() * ws.element_size(), flags, _stream(stream)), "moe_decode")
+
+
+def flint_moe_layer(x, router_w, k, routed: Experts, shared: Experts | None, ids, weights, y, ws, bias=None, flags=0,
+                    stream=None):
+    """The whole layer in one launch: routing (ids, weights written) and y."""
+    T = x.shape[0]
+    E = router_w.shape[0]
+    _check(_lib.flint_moe_layer(_ptr(x), T, _ptr(router_w), E, _ptr(bias), k, _ex(routed), _ex(shared), _ptr(ids),
+                                _ptr(weights), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(), flags,
+                                _stream(stream)), "moe_layer")
 
 
 def flint_dense_gemv(x, W: Packed, y, epilogue=FLINT_EPILOGUE_NONE, ws=None, flags=0, stream=None):

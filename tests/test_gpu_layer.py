@@ -1,0 +1,123 @@
+"""The fused layer kernel (flint_moe_layer: routing, gate/up, down and combine
+in one cooperative launch) against the oracle: selection bit-exact, weights
+to FP32 rounding, y within the layer tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from flint_testlib import DeviceLayer, assert_close, flint, margin_x
+from nvfp4_moe_decode_sigmoid_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(dl, x, k, bias=None, flags=0, ws=None):
+    f = flint()
+    T, H = x.shape
+    ws = dl.workspace(k) if ws is None else ws
+    ids = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda")
+    y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    b = bias.cuda() if bias is not None else None
+    f.flint_moe_layer(x.cuda(), dl.router_w, k, dl.routed, dl.shared, ids, w, y, ws, bias=b, flags=flags)
+    assert f.flint_workspace_check(ws) == f.FLINT_OK
+    return ids.cpu().numpy(), w.cpu().numpy(), synth.bits(y)
+
+
+def _check(dl, x, k, bias=None, flags=0):
+    ids, w, y = _run(dl, x, k, bias, flags)
+    rids, rw, ry = oracle.moe_layer(synth.bits(x), synth.bits(dl.L.router_w), k,
+                                    bias=None if bias is None else bias.numpy(), **dl.oracle_args())
+    assert np.array_equal(ids, rids), f"selection differs: {ids} vs {rids}"
+    assert np.allclose(w, rw, rtol=2e-6, atol=1e-7), f"weights differ: {w} vs {rw}"
+    ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
+    assert_close(y, ref, "fused layer (gpu routing)")
+    assert_close(y, ry, "fused layer (oracle routing)")
+    return ids, w, y
+
+
+@pytest.fixture(scope="module")
+def small_layer():
+    return DeviceLayer(synth.Layer(11, H=1024, E=16, I=256, I_shared=256))
+
+
+@pytest.mark.parametrize("T,k", [(1, 6), (2, 1), (5, 4), (8, 6), (8, 8)])
+def test_small_layer(small_layer, T, k):
+    x = margin_x(synth.bits(small_layer.L.router_w), T, 1024, k, None, seed=T + 10 * k)
+    _check(small_layer, x, k)
+
+
+def test_small_layer_with_bias_and_pdl(small_layer):
+    f = flint()
+    bias = synth.zipf_bias(5, 16)
+    x = margin_x(synth.bits(small_layer.L.router_w), 6, 1024, 6, bias.numpy(), seed=31)
+    _check(small_layer, x, 6, bias=bias, flags=f.FLINT_PDL)
+
+
+def test_without_shared_expert():
+    dl = DeviceLayer(synth.Layer(12, H=1024, E=16, I=256, I_shared=0, shared=False))
+    x = margin_x(synth.bits(dl.L.router_w), 3, 1024, 6, None, seed=4)
+    _check(dl, x, 6)
+
+
+def test_shared_expert_wider_than_routed():
+    dl = DeviceLayer(synth.Layer(13, H=1024, E=16, I=256, I_shared=1024))
+    x = margin_x(synth.bits(dl.L.router_w), 4, 1024, 6, None, seed=5)
+    _check(dl, x, 6)
+
+
+def test_many_experts_wide_topk():
+    # E above 256: the top-k warp takes 32 scores per lane
+    dl = DeviceLayer(synth.Layer(14, H=1024, E=600, I=256, I_shared=256))
+    x = margin_x(synth.bits(dl.L.router_w), 3, 1024, 8, None, seed=6)
+    _check(dl, x, 8)
+
+
+@pytest.fixture(scope="module")
+def full_layer():
+    return DeviceLayer(synth.Layer(1000, H=2048, E=256, I=512, I_shared=512))
+
+
+def test_full_layer_batch1(full_layer):
+    f = flint()
+    x = margin_x(synth.bits(full_layer.L.router_w), 1, 2048, 6, None, seed=7)
+    _check(full_layer, x, 6, flags=f.FLINT_PDL)
+
+
+def test_full_layer_batch8_uniform(full_layer):
+    x = margin_x(synth.bits(full_layer.L.router_w), 8, 2048, 6, None, seed=8)
+    _check(full_layer, x, 6)
+
+
+def test_full_layer_batch8_zipf(full_layer):
+    f = flint()
+    bias = synth.zipf_bias(3, 256)
+    x = margin_x(synth.bits(full_layer.L.router_w), 8, 2048, 6, bias.numpy(), seed=9)
+    _check(full_layer, x, 6, bias=bias, flags=f.FLINT_PDL)
+
+
+def test_repeated_calls_on_one_workspace_are_deterministic(full_layer):
+    # the grid barrier's counters are left ready for the next call
+    x = margin_x(synth.bits(full_layer.L.router_w), 8, 2048, 6, None, seed=10)
+    ws = full_layer.workspace(6)
+    outs = [_run(full_layer, x, 6, ws=ws) for _ in range(4)]
+    for o in outs[1:]:
+        for u, v in zip(o, outs[0]):
+            assert np.array_equal(u, v)
+
+
+def test_matches_the_three_kernel_path(full_layer):
+    f = flint()
+    x = margin_x(synth.bits(full_layer.L.router_w), 8, 2048, 6, None, seed=12)
+    ids, w, y = _run(full_layer, x, 6)
+    ws = full_layer.workspace(6)
+    ids2 = torch.empty((8, 6), dtype=torch.int32, device="cuda")
+    w2 = torch.empty((8, 6), dtype=torch.float32, device="cuda")
+    y2 = torch.empty((8, 2048), dtype=torch.bfloat16, device="cuda")
+    xc = x.cuda()
+    f.flint_moe_route(xc, full_layer.router_w, 6, ids2, w2, ws)
+    f.flint_moe_decode(xc, ids2, w2, full_layer.routed, full_layer.shared, y2, ws)
+    assert np.array_equal(ids, ids2.cpu().numpy())
+    assert np.allclose(w, w2.cpu().numpy(), rtol=2e-6, atol=1e-7)
+    assert_close(y, synth.bits(y2), "fused vs three kernels")
