@@ -2,8 +2,10 @@
 
 A step is one pass of the whole hot path (router GEMV + sigmoid top-6 ->
 gate/up GEMV + SiLU -> down GEMV + weighted combine with the shared expert)
-over one batch of T tokens, through the C ABI, PDL-chained, replayed from a
-CUDA graph. Weights of `--layers` distinct seeded layers stay resident in HBM
+over one batch of T tokens, through the C ABI: one flint_moe_layer launch per
+layer (all steps in one cooperative kernel), PDL-chained to the previous
+layer's, replayed from a CUDA graph. The three-kernel chain (flint_moe_route
+-> flint_moe_decode) is timed on the same workload for comparison. Weights of `--layers` distinct seeded layers stay resident in HBM
 and the steps cycle through them, so every step reads its experts from HBM
 (the rotation's reuse distance is far larger than the 129 MB L2).
 
@@ -174,20 +176,27 @@ def make_inputs(model, T, routing, device):
     return bias, per
 
 
-def run_step(F, model, inp, li, bias, flags):
+def run_step(F, model, inp, li, bias, flags, path="fused"):
+    """One layer step: the fused kernel, or the router + decode chain."""
     lay, io = model.layers[li], inp[li]
+    if path == "fused":
+        F.flint_moe_layer(io["x"], lay["router_w"], TOPK, lay["routed"], lay["shared"], io["ids"], io["w"], io["y"],
+                          model.ws, bias=bias, flags=flags)
+        return
     F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], model.ws, bias=bias, flags=flags)
-    F.flint_moe_decode(io["x"], io["ids"], io["w"], lay["routed"], lay["shared"], io["y"], model.ws, flags=flags)
+    dflags = flags | (F.FLINT_PDL_AFTER_ROUTE if flags & F.FLINT_PDL else 0)
+    F.flint_moe_decode(io["x"], io["ids"], io["w"], lay["routed"], lay["shared"], io["y"], model.ws, flags=dflags)
 
 
-def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, device_index, with_clocks=True):
+def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, device_index, with_clocks=True,
+                     path="fused"):
     import torch
     T, routing = WORKLOADS[name]
     nl = len(model.layers)
     bias, inp = make_inputs(model, T, routing, "cuda")
     flags = F.FLINT_PDL
     for s in range(max(warmup, nl)):
-        run_step(F, model, inp, s % nl, bias, flags)
+        run_step(F, model, inp, s % nl, bias, flags, path)
     torch.cuda.synchronize()
     assert F.flint_workspace_check(model.ws) == F.FLINT_OK
     # distinct experts each layer's routing selects -> algorithmic bytes per step
@@ -205,7 +214,7 @@ def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, devic
             # offset so that consecutive replays continue the layer rotation
             with torch.cuda.graph(g, stream=stream):
                 for s in range(count):
-                    run_step(F, model, inp, (start + s) % nl, bias, flags)
+                    run_step(F, model, inp, (start + s) % nl, bias, flags, path)
             graphs.append((g, count))
     main_g, main_n = graphs[0]
     reps = steps // R
@@ -247,20 +256,22 @@ def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, devic
 
 
 def measure_kernels(F, model, name, reps=8):
-    """Average device duration of each of the three kernels: for each kernel a
-    CUDA graph of back-to-back launches (one per resident layer, no PDL) is
-    replayed `reps` times between two CUDA events on the replay stream. The
-    routing comes from a warm-up pass, so the gate/up and down launches see
-    each layer's real expert selection."""
+    """Average device duration of each kernel: the fused layer kernel and the
+    three kernels of the chain. For each, a CUDA graph of back-to-back
+    launches (one per resident layer, no PDL) is replayed `reps` times between
+    two CUDA events on the replay stream. The routing comes from a warm-up
+    pass, so the gate/up and down launches see each layer's real selection."""
     import torch
     T, routing = WORKLOADS[name]
     nl = len(model.layers)
     bias, inp = make_inputs(model, T, routing, "cuda")
     for li in range(nl):
-        run_step(F, model, inp, li, bias, 0)
+        run_step(F, model, inp, li, bias, 0, "chain")
     torch.cuda.synchronize()
     stream = torch.cuda.Stream()
     calls = {
+        "layer": lambda lay, io: F.flint_moe_layer(io["x"], lay["router_w"], TOPK, lay["routed"], lay["shared"],
+                                                   io["ids"], io["w"], io["y"], model.ws, bias=bias),
         "route": lambda lay, io: F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], model.ws,
                                                    bias=bias),
         "gate_up": lambda lay, io: F.flint_moe_gate_up(io["x"], io["ids"], lay["routed"], lay["shared"], model.ws),
@@ -288,6 +299,7 @@ def measure_kernels(F, model, name, reps=8):
     out["gate_up_bytes"] = statistics.mean((d + 1) * (gu_b + 8) + T * H * 2 for d in distinct)
     out["down_bytes"] = statistics.mean((d + 1) * (dn_b + 4) + T * H * 2 for d in distinct)
     out["route_bytes"] = ROUTER_BYTES + T * H * 2
+    out["layer_bytes"] = statistics.mean(step_bytes(d, T, bias is not None) for d in distinct)
     return out
 
 
@@ -307,7 +319,7 @@ def measure_e2e(F, model, name, steps, graph_steps):
         for s in range(nl):  # warm-up, routing for the byte count
             li = s % nl
             inp[li]["x"].copy_(hx[li], non_blocking=True)
-            run_step(F, model, inp, li, bias, F.FLINT_PDL)
+            run_step(F, model, inp, li, bias, F.FLINT_PDL, "fused")
             hy[li].copy_(inp[li]["y"], non_blocking=True)
         stream.synchronize()
         g = torch.cuda.CUDAGraph()
@@ -315,7 +327,7 @@ def measure_e2e(F, model, name, steps, graph_steps):
             for s in range(R):
                 li = s % nl
                 inp[li]["x"].copy_(hx[li], non_blocking=True)
-                run_step(F, model, inp, li, bias, F.FLINT_PDL)
+                run_step(F, model, inp, li, bias, F.FLINT_PDL, "fused")
                 hy[li].copy_(inp[li]["y"], non_blocking=True)
     distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
     reps = max(1, steps // R)
@@ -332,8 +344,8 @@ def measure_e2e(F, model, name, steps, graph_steps):
     n = reps * R
     total = sum(step_bytes(distinct[s % nl], T, bias is not None) for s in range(R)) * reps
     return dict(value=total / (ms * 1e-3) / 1e9, unit="GB/s", h2d_bytes_per_step=T * H * 2,
-                d2h_bytes_per_step=T * H * 2, steps=n, us_per_step=ms * 1e3 / n, path="pinned host x -> route -> "
-                "decode -> pinned host y, CUDA graph")
+                d2h_bytes_per_step=T * H * 2, steps=n, us_per_step=ms * 1e3 / n, path="pinned host x -> "
+                "flint_moe_layer -> pinned host y, CUDA graph")
 
 
 def cpu_baseline(name, budget_s=20.0):
@@ -364,9 +376,9 @@ def cpu_baseline(name, budget_s=20.0):
 
 
 def traffic_for(kernel_src_hash):
-    """DRAM bytes per launch of the gate/up kernel from the committed ncu summary,
-    if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "gate_up_traffic.json")
+    """DRAM bytes per launch of the fused layer kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "layer_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
@@ -380,7 +392,7 @@ def traffic_for(kernel_src_hash):
 def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
-    for fn in ("gemv.cu", "flint_device.cuh", "flint_internal.h"):
+    for fn in ("layer.cu", "expert_common.cuh", "router_common.cuh", "flint_device.cuh", "flint_internal.h"):
         with open(os.path.join(ROOT, "nvfp4_moe_decode_sigmoid_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -414,6 +426,8 @@ def run_flint(args):
     main = measure_workload(F, model, args.workload, args.steps, args.warmup, args.graph_steps, sync_all, dev_index)
     ms = max_over_ranks(main["ms"])
     value = main["bytes"] * world / (ms * 1e-3) / 1e9
+    chain = measure_workload(F, model, args.workload, max(1024, args.steps // 4), args.warmup, args.graph_steps,
+                             sync_all, dev_index, with_clocks=False, path="chain")
     extra = {}
     if not args.no_extra:
         for name in WORKLOADS:
@@ -425,7 +439,7 @@ def run_flint(args):
                                mean_distinct_experts=r["mean_distinct"], bytes_per_step=r["bytes_per_step_mean"])
     kern = measure_kernels(F, model, args.workload)
     peak, peak_src = load_peaks()
-    achieved = kern["gate_up_bytes"] / (kern["gate_up_us"] * 1e-6) / 1e9
+    achieved = kern["layer_bytes"] / (kern["layer_us"] * 1e-6) / 1e9
     traffic = traffic_for(kernel_source_hash())
     e2e = measure_e2e(F, model, args.workload, min(args.steps, 8192), args.graph_steps)
     cpu = None
@@ -450,23 +464,27 @@ def run_flint(args):
             "config": {"workload": args.workload, "tokens": T, "routing": routing, "hidden": H, "experts": E,
                        "top_k": TOPK, "inter": I, "shared_inter": I_SHARED, "weights": "nvfp4 (e2m1 + ue4m3/16 + fp32)",
                        "activations": "bf16", "layers_rotated": args.layers, "pdl": True,
+                       "path": "flint_moe_layer: one cooperative kernel per layer",
                        "graph_steps": args.graph_steps,
                        "l2": f"inputs larger than L2: {args.layers} resident layers cycled, reuse distance "
                              f"{(args.layers - 1) * main['bytes_per_step_mean'] / 1e6:.0f} MB > 129 MB L2",
                        "parallelism": f"replicas x{world}",
                        "mean_distinct_experts": main["mean_distinct"],
                        "bytes_per_step": main["bytes_per_step_mean"]},
-            "roofline": {"bound": "hbm", "kernel": "gate_up_kernel", "achieved": round(achieved, 1),
+            "roofline": {"bound": "hbm", "kernel": "layer_kernel", "achieved": round(achieved, 1),
                          "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": traffic, "algorithmic_bytes_per_launch": kern["gate_up_bytes"],
-                         "us_per_launch": kern["gate_up_us"]},
+                         "traffic": traffic, "algorithmic_bytes_per_launch": kern["layer_bytes"],
+                         "us_per_launch": kern["layer_us"]},
             "kernels_us": {k: round(v, 3) for k, v in kern.items() if k.endswith("_us")},
             "kernels_gb_s": {k: round(kern[k + "_bytes"] / (kern[k + "_us"] * 1e-6) / 1e9, 1)
-                             for k in ("route", "gate_up", "down")},
+                             for k in ("layer", "route", "gate_up", "down")},
+            "three_kernel_chain": {"us_per_layer": round(chain["ms"] * 1e3 / chain["steps"], 3),
+                                   "gb_s": round(chain["bytes"] / (chain["ms"] * 1e-3) / 1e9, 1),
+                                   "path": "flint_moe_route -> flint_moe_decode (gate/up, down), PDL"},
             "layer_frac_of_peak": round(value / world / peak, 4),
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": args.steps,
             "clocks": main["clocks"],
             "extra_workloads": extra,
         }
