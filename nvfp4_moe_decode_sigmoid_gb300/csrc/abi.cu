@@ -159,6 +159,18 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     a.res_items = a.shp + routed_items;
     const int per_warp3 = ceil_div(routed_items, flint::kLayerWarps);
     const long long rs_r = flint::nvfp4_row_stride(a.I);
+    // Small batches: prefetch every routed down row right after routing, in
+    // groups of 8 rows when 16-row groups would leave warps idle.
+    for (int ns3 = per_warp3 < 1 ? 1 : (per_warp3 > 4 ? 4 : per_warp3); ns3 >= 1; --ns3) {
+        a.ns3 = ns3;
+        a.rg = units * ceil_div(a.rows_max, 16) < flint::kLayerWarps ? 8 : 16;
+        a.ns4 = 0;
+        a.slot4 = 0;
+        a.dpre = 1;
+        if (flint::layer_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin && ns3 >= (per_warp3 < 2 ? per_warp3 : 2))
+            return true;
+    }
+    a.dpre = 0;
     for (int rg : {16, 8}) {
         const int per_warp4 = ceil_div(units * ceil_div(a.rows_max, rg), flint::kLayerWarps);
         for (int ns3 = per_warp3 < 1 ? 1 : (per_warp3 > 4 ? 4 : per_warp3); ns3 >= 1; --ns3) {

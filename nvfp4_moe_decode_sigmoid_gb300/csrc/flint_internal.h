@@ -152,6 +152,7 @@ struct LayerArgs {
     int res_items;       // gate/up items per CTA (bound)
     int ns3;             // gate/up ring slots per warp
     int rg, ns4, slot4;  // down: rows per task, ring slots per warp, bytes per slot
+    int dpre;            // 1: all of the CTA's routed down rows are prefetched after routing
 };
 
 // ---------------------------------------------------------------------------

@@ -39,16 +39,28 @@ constexpr int kLT = kLayerThreads;
 // Small per-CTA arrays: tensor scales (gate, up) of the distinct experts then
 // of the shared expert; down scales of the units; combine weights; ids.
 struct LayerSmall {
+    uint64_t dbar;  // completion of the prefetched down rows
     float tss[2 * kMaxDistinct + 2];
     float tsd[kMaxDistinct + 1];
     float w[kMaxDistinct];
     int32_t ids[kMaxDistinct];
 };
 
+// Shared memory, by lifetime:
+//   persistent: routing view, small arrays, the shared expert's down rows;
+//   phases 0-3 (region U1): staged x and its chunk scales, the shared
+//     expert's gate/up pairs, then one of: router rows (phases 0-1), sigmoid
+//     scores (phase 2), raw gate/up sums + the gate/up rings (phase 3);
+//   phase 4 (region U4, over U1): staged h and its chunk scales, d values,
+//     the down rings;
+//   the prefetched down rows (a.dpre), beside both.
 struct LayerSmem {
-    size_t ri, small, xs, csc, wrows, shgu, shdn, B;
-    size_t resg, resu, ring3, end3;
-    size_t hr, hs, csr, css, dval, ring4, end4;
+    size_t ri, small, shdn, U;
+    size_t xs, csc, shgu, V;
+    size_t wrows, scores;
+    size_t resg, resu, ring3;
+    size_t hr, hs, csr, css, dval, ring4;
+    size_t dpre;
     size_t total;
 };
 
@@ -58,28 +70,36 @@ __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     const size_t T = a.T, H = a.H;
     L.ri = 0;
     L.small = align_up(sizeof(RouteInfo), 128);
-    L.xs = align_up(L.small + sizeof(LayerSmall), 128);
+    L.shdn = align_up(L.small + sizeof(LayerSmall), 128);
+    L.U = align_up(L.shdn + (size_t)a.rows_max * RSs, 128);
+    // U1
+    L.xs = L.U;
     L.csc = align_up(L.xs + 2 * T * H, 128);
-    L.wrows = align_up(L.csc + sizeof(float) * T * (H / 32), 128);
-    L.shgu = align_up(L.wrows + 2 * (size_t)a.rpc * H, 128);
-    L.shdn = align_up(L.shgu + 2 * (size_t)a.shp * RS, 128);
-    L.B = align_up(L.shdn + (size_t)a.rows_max * RSs, 128);
-    // phase 3 (gate/up)
-    L.resg = L.B;
+    L.shgu = align_up(L.csc + sizeof(float) * T * (H / 32), 128);
+    L.V = align_up(L.shgu + 2 * (size_t)a.shp * RS, 128);
+    L.wrows = L.V;
+    L.scores = L.V;
+    L.resg = L.V;
     L.resu = align_up(L.resg + sizeof(float) * (size_t)a.res_items * T, 128);
     L.ring3 = align_up(L.resu + sizeof(float) * (size_t)a.res_items * T, 128);
-    L.end3 = L.ring3 + (size_t)kLW * a.ns3 * 2 * RS;
-    // phase 4 (down), over the phase-3 region
-    L.hr = L.B;
+    size_t end1 = L.ring3 + (size_t)kLW * a.ns3 * 2 * RS;
+    const size_t e_rows = L.wrows + 2 * (size_t)a.rpc * H, e_scores = L.scores + sizeof(uint32_t) * T * a.E;
+    if (end1 < e_rows) end1 = e_rows;
+    if (end1 < e_scores) end1 = e_scores;
+    // U4
+    L.hr = L.U;
     L.hs = align_up(L.hr + 2 * T * a.k * a.I, 128);
     L.csr = align_up(L.hs + 2 * T * a.Is, 128);
     L.css = align_up(L.csr + sizeof(float) * T * a.k * (a.I / 32), 128);
     L.dval = align_up(L.css + sizeof(float) * T * (a.Is / 32), 128);
     L.ring4 = align_up(L.dval + sizeof(float) * T * (a.k + 1) * a.rows_max, 128);
-    L.end4 = L.ring4 + (size_t)kLW * a.ns4 * a.slot4;
-    L.total = L.end3 > L.end4 ? L.end3 : L.end4;
-    const size_t end2 = L.B + sizeof(uint32_t) * T * a.E;  // phase 2: sigmoid scores
-    if (L.total < end2) L.total = end2;
+    const size_t end4 = L.ring4 + (size_t)kLW * a.ns4 * a.slot4;
+    L.total = end1 > end4 ? end1 : end4;
+    L.dpre = align_up(L.total, 128);
+    if (a.dpre) {
+        const size_t units = (size_t)(a.T * a.k < a.E ? a.T * a.k : a.E);
+        L.total = L.dpre + units * a.rows_max * (size_t)nvfp4_row_stride(a.I);
+    }
     return L;
 }
 
@@ -124,6 +144,10 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     }
     cp_async_commit();
     if (tid < 2 * kMaxDistinct + 2) sm.tss[tid] = 0.f;
+    if (tid == 0) {
+        mbar_init(&sm.dbar, 1);
+        fence_mbar_init();
+    }
 
     pdl_wait();  // x comes from the previous kernel
 
@@ -132,21 +156,31 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     stage_f16<false>(xsrc, [] {});
     cp_async_wait<0>();
     __syncthreads();
+    // logits from the staged (exact, chunk-scaled f16) x: lane l takes the
+    // 32-value chunks l, l + 32, ...; each chunk's FP32 partial sum is
+    // multiplied back by its power-of-two scale
     for (int q = warp; q < nrr * T; q += kLW) {
         const int r = q / T, t = q - r * T;
-        const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
+        const uint4* xb = xh + (size_t)t * (H / 8) + lane;
+        const float* cb = csc + (size_t)t * (H / 32) + lane;
         const uint4* wv = reinterpret_cast<const uint4*>(wrows + (size_t)r * H);
-        float s0 = 0.f, s1 = 0.f;
-        for (int ch = lane; ch < H / 8; ch += 32) {
-            const uint4 xv = ld_cg(xr + ch), w = wv[ch];
-            const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {w.x, w.y, w.z, w.w};
+        float v = 0.f;
+        for (int m = 0; m < H / 1024; ++m) {
+            const int ch = lane + 32 * m;
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                s0 = fmaf(bf16_lo(wa[i]), bf16_lo(xa[i]), s0);
-                s1 = fmaf(bf16_hi(wa[i]), bf16_hi(xa[i]), s1);
+            for (int w = 0; w < 4; ++w) {
+                const uint4 xv = xb[(m * 4 + w) * 32], wq = wv[4 * ch + w];
+                const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xa[i]));
+                    s0 = fmaf(bf16_lo(wa[i]), xf.x, s0);
+                    s1 = fmaf(bf16_hi(wa[i]), xf.y, s1);
+                }
             }
+            v = fmaf(cb[32 * m], s0 + s1, v);
         }
-        float v = s0 + s1;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
         if (lane == 0) a.logits[(size_t)t * E + r0 + r] = v;
@@ -156,7 +190,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     // ---- 2: top-k of every token, in every CTA ------------------------------------
     float* wsel = sm.w;
     {
-        uint32_t* scores = reinterpret_cast<uint32_t*>(smem + L.B);  // region B is free until phase 3
+        uint32_t* scores = reinterpret_cast<uint32_t*>(smem + L.scores);
         sigmoid_scores(a.logits, a.bias, T, E, scores);
         __syncthreads();
         if (warp < T) {
@@ -174,6 +208,16 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     }
     build_route_info<true>(ri, sm.ids, T, k, E, a.status);
     const int D = ri.D;
+    // The routing is known: this CTA's down rows of every selected expert can
+    // stream in now, behind gate/up, when they fit (one bulk copy per expert).
+    uint8_t* dpre = smem + L.dpre;
+    if (a.dpre && nr > 0 && warp == 0) {
+        if (lane == 0) mbar_arrive_expect_tx(&sm.dbar, (uint32_t)(D * nr * RSr));
+        __syncwarp();
+        for (int u = lane; u < D; u += 32)
+            bulk_g2s(dpre + (size_t)u * nr * RSr, a.down + ((size_t)ri.dlist[u] * H + n0) * RSr,
+                     (uint32_t)(nr * RSr), &sm.dbar);
+    }
 
     // ---- 3: gate/up + SiLU ---------------------------------------------------------
     {
@@ -210,12 +254,22 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         }
         if (tid < 2 * D + 2) sm.tss[tid] = tsv;
         if (tid >= 256 && tid <= 256 + D) sm.tsd[tid - 256] = tdv;
-        const uint32_t all_tokens = (1u << T) - 1u;
-        // shared-expert pairs (resident): pair i by warp kLW - 1 - i
-        for (int i = kLW - 1 - warp; i < n_sh; i += kLW) {
+        // shared-expert pairs (resident), one unit per (pair, two tokens), spread
+        // over the warps from the last one: every token reads every shared row,
+        // so at T = 8 this is four times the work of a routed pair
+        const int ntp = (T + 1) >> 1;
+        for (int q = kLW - 1 - warp; q < n_sh * ntp; q += kLW) {
+            const int i = q / ntp, t0 = 2 * (q - i * ntp);
             const uint8_t* grow = shgu + (size_t)i * RS;
-            gate_up_item<true>(grow, grow + (size_t)a.shp * RS, H, xh, csc, all_tokens, lane, resg + i * T,
-                               resu + i * T);
+            if (t0 + 1 < T) {
+                const int tk[2] = {t0, t0 + 1};
+                gate_up_pass<true, 2>(grow, grow + (size_t)a.shp * RS, H, xh, csc, tk, lane, resg + i * T,
+                                      resu + i * T);
+            } else {
+                const int tk[1] = {t0};
+                gate_up_pass<true, 1>(grow, grow + (size_t)a.shp * RS, H, xh, csc, tk, lane, resg + i * T,
+                                      resu + i * T);
+            }
         }
         int d = 0, p = 0;
         if (n_items_w > 0) {
@@ -284,7 +338,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         uint8_t* ring = smem + L.ring4 + (size_t)warp * NSW * a.slot4;
         const int ngr = (nr + RG - 1) / RG;
         const int n_tasks = D * ngr;  // routed; the shared expert's groups are resident
-        const int my_tasks = n_tasks > warp ? (n_tasks - warp + kLW - 1) / kLW : 0;
+        const int my_tasks = a.dpre ? 0 : (n_tasks > warp ? (n_tasks - warp + kLW - 1) / kLW : 0);
         auto issue = [&](int kk) {
             const int q = warp + kk * kLW, u = q / ngr, r0g = (q - u * ngr) * RG, r1g = min(nr, r0g + RG);
             uint8_t* dst = ring + (size_t)(kk % NSW) * a.slot4;
@@ -359,10 +413,42 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 }
             }
         };
-        // the shared expert's row groups (resident): group g by warp kLW - 1 - g
-        if (has_sh)
-            for (int g = kLW - 1 - warp; g < ngr; g += kLW)
-                task(D, g * RG, min(nr, (g + 1) * RG), shdn + (size_t)g * RG * RSs);
+        // the shared expert's rows (resident), one unit per (8 rows, two tokens),
+        // spread over the warps from the last one
+        if (has_sh) {
+            const int ng8 = (nr + 7) >> 3, ntp = (T + 1) >> 1;
+            for (int q = kLW - 1 - warp; q < ng8 * ntp; q += kLW) {
+                const int g = q / ntp, t0 = 2 * (q - g * ntp), r0g = 8 * g;
+                const uint8_t* rows = shdn + (size_t)r0g * RSs;
+                const float tsd = sm.tsd[D];
+                const uint4* hv[2] = {hs + (size_t)t0 * (Is / 8), hs + (size_t)min(t0 + 1, T - 1) * (Is / 8)};
+                const float* cv[2] = {css + (size_t)t0 * (Is / 32), css + (size_t)min(t0 + 1, T - 1) * (Is / 32)};
+                if (t0 + 1 < T) {
+                    float acc[16];
+                    down_pass<8, 2>(rows, RSs, nr - r0g, Is, hv, cv, lane, acc);
+                    const float v = reduce_scatter<16>(acc, lane);
+                    const int idx = rs_index<16>(lane), r = r0g + (idx & 7);
+                    if ((lane & 1) == 0 && r < nr)
+                        dval[((size_t)(t0 + (idx >> 3)) * (k + 1) + k) * RM + r] = bf16_round_f32(tsd * v);
+                } else {
+                    const uint4* hv1[1] = {hv[0]};
+                    const float* cv1[1] = {cv[0]};
+                    float acc[8];
+                    down_pass<8, 1>(rows, RSs, nr - r0g, Is, hv1, cv1, lane, acc);
+                    const float v = reduce_scatter<8>(acc, lane);
+                    const int r = r0g + rs_index<8>(lane);
+                    if ((lane & 3) == 0 && r < nr) dval[((size_t)t0 * (k + 1) + k) * RM + r] = bf16_round_f32(tsd * v);
+                }
+            }
+        }
+        if (a.dpre) {  // every routed group is resident once the prefetch lands
+            const bool ok = mbar_wait_bounded(&sm.dbar, 0, tid == 0 ? a.status : nullptr, kStatusTimeoutLayer);
+            if (!__syncthreads_and(ok)) return;
+            for (int q = warp; q < n_tasks; q += kLW) {
+                const int u = q / ngr, g = q - u * ngr;
+                task(u, g * RG, min(nr, (g + 1) * RG), dpre + ((size_t)u * nr + (size_t)g * RG) * RSr);
+            }
+        }
         for (int kk = 0; kk < my_tasks; ++kk) {
             cp_async_wait_n(NSW - 1);
             __syncwarp();
