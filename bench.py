@@ -52,6 +52,7 @@ def parse():
     p.add_argument("--graph-steps", type=int, default=64)
     p.add_argument("--no-extra", action="store_true", help="skip the other two batch/routing workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-bf16", action="store_true", help="skip the BF16-expert variant")
     return p.parse_args()
 
 
@@ -144,23 +145,35 @@ class ClockSampler:
 # GPU arm
 # ---------------------------------------------------------------------------
 class Model:
-    """`n_layers` seeded MoE layers resident on the device, repacked to the kernel layout."""
+    """`n_layers` seeded MoE layers resident on the device: NVFP4 experts
+    repacked to the kernel layout, or (wdtype "bf16") the 16-bit variant."""
 
-    def __init__(self, n_layers: int, device):
+    def __init__(self, n_layers: int, device, wdtype: str = "nvfp4"):
         import torch
         from nvfp4_moe_decode_sigmoid_gb300 import flint as F
         from nvfp4_moe_decode_sigmoid_gb300 import synth
+        self.wdtype = wdtype
         self.layers = []
         for li in range(n_layers):
-            L = synth.Layer(1000 + li, H=H, E=E, I=I, I_shared=I_SHARED, device=device)
-            routed = F.Experts.from_gguf(L.gate, L.up, L.down, L.ts, E, H, I)
+            L = synth.Layer(1000 + li, H=H, E=E, I=I, I_shared=I_SHARED, device=device, wdtype=wdtype)
             s = L.shared
-            shared = F.Experts.from_gguf(s["gate"], s["up"], s["down"], s["ts"].reshape(1, 3), 1, H, I_SHARED)
+            if wdtype == "nvfp4":
+                routed = F.Experts.from_gguf(L.gate, L.up, L.down, L.ts, E, H, I)
+                shared = F.Experts.from_gguf(s["gate"], s["up"], s["down"], s["ts"].reshape(1, 3), 1, H, I_SHARED)
+            else:
+                routed = F.Experts.from_bf16(L.gate, L.up, L.down, E, H, I)
+                shared = F.Experts.from_bf16(s["gate"], s["up"], s["down"], 1, H, I_SHARED)
             self.layers.append(dict(router_w=L.router_w, routed=routed, shared=shared, seed=1000 + li))
-            del L
+            del L, s
             torch.cuda.synchronize()
         self.ws = torch.empty(F.flint_workspace_bytes(E, TOPK, I, I_SHARED), dtype=torch.uint8, device=device)
         F.flint_workspace_init(self.ws)
+
+    def step_bytes(self, n_distinct: int, T: int, with_bias: bool) -> int:
+        if self.wdtype == "nvfp4":
+            return step_bytes(n_distinct, T, with_bias)
+        per_expert = 3 * I * H * 2  # bf16 gate, up, down; no tensor scales
+        return ROUTER_BYTES + (E * 4 if with_bias else 0) + (n_distinct + 1) * per_expert + 2 * T * H * 2
 
 
 def make_inputs(model, T, routing, device):
@@ -201,7 +214,7 @@ def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, devic
     assert F.flint_workspace_check(model.ws) == F.FLINT_OK
     # distinct experts each layer's routing selects -> algorithmic bytes per step
     distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
-    bytes_per_layer = [step_bytes(d, T, bias is not None) for d in distinct]
+    bytes_per_layer = [model.step_bytes(d, T, bias is not None) for d in distinct]
 
     stream = torch.cuda.Stream()
     R = max(1, min(graph_steps, steps))
@@ -253,6 +266,34 @@ def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, devic
     return dict(T=T, routing=routing, ms=ms, steps=steps, bytes=total_bytes,
                 mean_distinct=sum(distinct) / len(distinct), clocks=sampler.summary() if sampler else None,
                 bytes_per_step_mean=total_bytes / steps)
+
+
+def measure_bf16(F, nvfp4_model, args, sync_all, dev_index, n_layers=6):
+    """The BF16-weight variant of the same layer (router -> gate/up -> down,
+    three PDL-chained kernels; the one-kernel layer is NVFP4-only), at T = 1
+    and T = 8, beside the NVFP4 three-kernel chain on the same workloads.
+    `n_layers` BF16 layers (1.5 GB each) rotate, so every step reads HBM."""
+    import torch
+    bmodel = Model(n_layers, "cuda", "bf16")
+    peak, _ = load_peaks()
+    out = {}
+    for name in ("moe-layer-b1", "moe-layer-b8-uniform"):
+        steps = max(512, min(4096, args.steps // 8))
+        r = measure_workload(F, bmodel, name, steps, args.warmup, args.graph_steps, sync_all, dev_index,
+                             with_clocks=False, path="chain")
+        q = measure_workload(F, nvfp4_model, name, steps, args.warmup, args.graph_steps, sync_all, dev_index,
+                             with_clocks=False, path="chain")
+        gbs = r["bytes"] / (r["ms"] * 1e-3) / 1e9
+        out[name] = dict(us_per_layer=round(r["ms"] * 1e3 / r["steps"], 3), gb_s=round(gbs, 1),
+                         frac_of_peak=round(gbs / peak, 4), bytes_per_step=r["bytes_per_step_mean"],
+                         mean_distinct_experts=r["mean_distinct"],
+                         nvfp4_chain_us_per_layer=round(q["ms"] * 1e3 / q["steps"], 3),
+                         nvfp4_chain_bytes_per_step=q["bytes_per_step_mean"])
+    del bmodel
+    torch.cuda.empty_cache()
+    out["path"] = "flint_moe_route -> flint_moe_decode (bf16 gate/up, bf16 down), PDL, CUDA graph"
+    out["layers_rotated"] = n_layers
+    return out
 
 
 def measure_kernels(F, model, name, reps=8):
@@ -438,6 +479,9 @@ def run_flint(args):
             extra[name] = dict(us_per_layer=r["ms"] * 1e3 / r["steps"], gb_s=r["bytes"] / (r["ms"] * 1e-3) / 1e9,
                                mean_distinct_experts=r["mean_distinct"], bytes_per_step=r["bytes_per_step_mean"])
     kern = measure_kernels(F, model, args.workload)
+    bf16 = {}
+    if not args.no_bf16:
+        bf16 = measure_bf16(F, model, args, sync_all, dev_index)
     peak, peak_src = load_peaks()
     achieved = kern["layer_bytes"] / (kern["layer_us"] * 1e-6) / 1e9
     traffic = traffic_for(kernel_source_hash())
@@ -487,6 +531,7 @@ def run_flint(args):
             "gpu_launches": args.steps,
             "clocks": main["clocks"],
             "extra_workloads": extra,
+            "bf16_experts": bf16,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -164,16 +164,25 @@ flint_status_t flint_workspace_check(void* ws, size_t ws_bytes, void* stream);
 /* ------------------------------------------------------------------------ */
 
 /* Expert weights of one MoE layer (or of its shared expert, with
- * num_experts = 1). */
+ * num_experts = 1).
+ *
+ * FLINT_DTYPE_BF16 ("Day-0 Support for Flint on vLLM", section
+ * "Optimizations": the decode path also serves the BF16 checkpoint): gate_up
+ * is E bf16 matrices [2I, H] row-major (rows [0, I) gate, [I, 2I) up), down E
+ * bf16 matrices [H, I] row-major; tensor_scale may be NULL (every scale 1).
+ * The arithmetic and rounding points are those of the NVFP4 path with the
+ * weight equal to the bf16 value. Taken by flint_moe_gate_up,
+ * flint_moe_down_combine and flint_moe_decode (not by flint_moe_layer);
+ * routed and shared experts must have the same dtype. */
 typedef struct flint_experts {
-    int32_t dtype;        /* FLINT_DTYPE_NVFP4 (FLINT_DTYPE_BF16 reserved) */
+    int32_t dtype;        /* FLINT_DTYPE_NVFP4 or FLINT_DTYPE_BF16 */
     int32_t num_experts;  /* E */
     int32_t hidden;       /* H: columns of gate/up, rows of down; % 1024 == 0 */
     int32_t inter;        /* I: intermediate size; % 256 == 0 */
-    const void* gate_up;  /* E matrices [2I, H], kernel layout, matrix stride
-                             2I * row_stride(H); rows [0, I) gate, [I, 2I) up */
-    const void* down;     /* E matrices [H, I], kernel layout, stride H * row_stride(I) */
-    const float* tensor_scale; /* [E][3] FP32: gate, up, down */
+    const void* gate_up;  /* NVFP4: E matrices [2I, H], kernel layout, matrix
+                             stride 2I * row_stride(H); rows [0, I) gate, [I, 2I) up */
+    const void* down;     /* NVFP4: E matrices [H, I], kernel layout, stride H * row_stride(I) */
+    const float* tensor_scale; /* [E][3] FP32: gate, up, down (NVFP4: required) */
 } flint_experts;
 
 /*
@@ -275,7 +284,8 @@ flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, 
  *   flags: FLINT_PDL lets the launch overlap the previous kernel of the stream
  *   (this kernel waits for it before reading x).
  *   Errors: FLINT_ERR_UNSUPPORTED when one CTA's shared memory cannot hold
- *   the layer's working set or the device cannot co-schedule one CTA per SM.
+ *   the layer's working set, the device cannot co-schedule one CTA per SM, or
+ *   the experts are not NVFP4.
  */
 flint_status_t flint_moe_layer(const flint_bf16* x, int T, const flint_bf16* router_w, int E, const float* bias,
                                int k, const flint_experts* routed, const flint_experts* shared, int32_t* ids,

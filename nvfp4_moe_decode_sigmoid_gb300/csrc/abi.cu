@@ -67,8 +67,8 @@ uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 1; }
 
 flint_status_t check_experts(const flint_experts* x, const char* name, bool need_down) {
     if (!x) return fail(FLINT_ERR_INVALID_ARG, "%s experts: null", name);
-    if (x->dtype != FLINT_DTYPE_NVFP4)
-        return fail(FLINT_ERR_UNSUPPORTED, "%s experts: only FLINT_DTYPE_NVFP4 weights are implemented", name);
+    if (x->dtype != FLINT_DTYPE_NVFP4 && x->dtype != FLINT_DTYPE_BF16)
+        return fail(FLINT_ERR_UNSUPPORTED, "%s experts: unknown dtype %d", name, x->dtype);
     if (x->num_experts < 1 || x->num_experts > FLINT_MAX_EXPERTS)
         return fail(FLINT_ERR_UNSUPPORTED, "%s experts: num_experts %d outside 1..%d", name, x->num_experts,
                     FLINT_MAX_EXPERTS);
@@ -77,7 +77,7 @@ flint_status_t check_experts(const flint_experts* x, const char* name, bool need
                     x->hidden);
     if (x->inter <= 0 || x->inter % 256)
         return fail(FLINT_ERR_UNSUPPORTED, "%s experts: inter %d must be a positive multiple of 256", name, x->inter);
-    if (!x->tensor_scale || !aligned(x->tensor_scale, 4))
+    if ((x->dtype == FLINT_DTYPE_NVFP4 && !x->tensor_scale) || (x->tensor_scale && !aligned(x->tensor_scale, 4)))
         return fail(FLINT_ERR_INVALID_ARG, "%s experts: tensor_scale null or misaligned", name);
     if (!x->gate_up || !aligned(x->gate_up, 16))
         return fail(FLINT_ERR_INVALID_ARG, "%s experts: gate_up null or not 16-byte aligned", name);
@@ -134,6 +134,47 @@ bool down_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
             t.nslots = ns;
             t.slot_bytes = (int)(rg * rs);
             if (flint::down_smem_bytes(t) + kSmemSlack > (size_t)smem_optin) continue;
+            const double cover = (double)ns / per_warp;
+            if (cover > best_cover + 1e-9) {
+                best = t;
+                best_cover = cover;
+                found = true;
+            }
+            break;
+        }
+    }
+    if (found) a = best;
+    return found;
+}
+
+// BF16 gate/up: ring slots per warp (one row each, up to 4), as many as fit.
+bool gate_up_bf16_shape(flint::GateUpArgs& a, int smem_optin, long long pairs) {
+    a.res_items = (int)pairs;
+    const int per_warp = ceil_div(2 * pairs, flint::kBf16Warps);
+    for (int ns = per_warp < 1 ? 1 : (per_warp > 4 ? 4 : per_warp); ns >= 1; --ns) {
+        a.nslots = ns;
+        if (flint::gate_up_bf16_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin) return true;
+    }
+    return false;
+}
+
+// BF16 down: tasks of 8 or 4 rows; whichever keeps the larger share of a
+// warp's tasks in flight (8 on a tie), up to 4 slots per warp.
+bool down_bf16_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
+    a.rows_max = ceil_div(a.H, sm_count);
+    const int kmax = a.I > a.Is ? a.I : a.Is;
+    const int units = (a.T * a.k < a.E ? a.T * a.k : a.E) + (a.Is > 0 ? 1 : 0);
+    bool found = false;
+    double best_cover = -1.0;
+    flint::DownArgs best = a;
+    for (int rg : {8, 4}) {
+        const int per_warp = ceil_div((long long)units * ceil_div(a.rows_max, rg), flint::kBf16Warps);
+        for (int ns = per_warp < 4 ? per_warp : 4; ns >= 1; --ns) {
+            flint::DownArgs t = a;
+            t.rg = rg;
+            t.nslots = ns;
+            t.slot_bytes = 2 * rg * kmax;
+            if (flint::down_bf16_smem_bytes(t) + kSmemSlack > (size_t)smem_optin) continue;
             const double cover = (double)ns / per_warp;
             if (cover > best_cover + 1e-9) {
                 best = t;
@@ -334,6 +375,8 @@ static flint_status_t moe_common(const char* what, int T, int k, const flint_exp
         if ((s = check_experts(shared, "shared", need_down)) != FLINT_OK) return s;
         if (shared->num_experts != 1 || shared->hidden != routed->hidden)
             return fail(FLINT_ERR_INVALID_ARG, "%s: shared expert must have num_experts 1 and the routed hidden size", what);
+        if (shared->dtype != routed->dtype)
+            return fail(FLINT_ERR_UNSUPPORTED, "%s: shared and routed experts must have the same dtype", what);
     }
     return FLINT_OK;
 }
@@ -367,6 +410,14 @@ flint_status_t flint_moe_gate_up(const flint_bf16* x, int T, const int32_t* ids,
     a.h_shared = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.h_shared_off);
     a.status = ws_status(ws);
     a.x_early = (flags & FLINT_PDL) && (flags & FLINT_PDL_AFTER_ROUTE);
+    if (routed->dtype == FLINT_DTYPE_BF16) {
+        const long long pairs = ceil_div(a.Is, d.sm_count) +
+                                ceil_div((long long)(T * k < a.E ? T * k : a.E) * a.I, d.sm_count);
+        if (!gate_up_bf16_shape(a, d.smem_optin, pairs))
+            return fail(FLINT_ERR_UNSUPPORTED, "gate_up: shapes exceed one CTA's shared memory");
+        cudaError_t e = flint::launch_gate_up_bf16(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
+        return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "gate_up (bf16) launch");
+    }
     const long long routed_pairs = (long long)(T * k < a.E ? T * k : a.E) * a.I;
     if (!gate_up_shape(a, true, d.smem_optin,
                        ceil_div(a.Is, d.sm_count) + ceil_div(routed_pairs, d.sm_count)))
@@ -404,6 +455,12 @@ flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* we
     a.h_shared = reinterpret_cast<const uint16_t*>(static_cast<uint8_t*>(ws) + L.h_shared_off);
     a.y = y;
     a.status = ws_status(ws);
+    if (routed->dtype == FLINT_DTYPE_BF16) {
+        if (!down_bf16_shape(a, d.sm_count, d.smem_optin))
+            return fail(FLINT_ERR_UNSUPPORTED, "down_combine: shapes exceed one CTA's shared memory");
+        cudaError_t e = flint::launch_down_bf16(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
+        return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "down_combine (bf16) launch");
+    }
     if (!down_shape(a, d.sm_count, d.smem_optin))
         return fail(FLINT_ERR_UNSUPPORTED, "down_combine: shapes exceed one CTA's shared memory");
     cudaError_t e = flint::launch_down(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
@@ -429,6 +486,10 @@ flint_status_t flint_moe_layer(const flint_bf16* x, int T, const flint_bf16* rou
     if (s != FLINT_OK) return s;
     if (E != routed->num_experts)
         return fail(FLINT_ERR_INVALID_ARG, "layer: router has %d rows, routed experts %d", E, routed->num_experts);
+    if (routed->dtype != FLINT_DTYPE_NVFP4)
+        return fail(FLINT_ERR_UNSUPPORTED,
+                    "layer: the one-kernel layer takes NVFP4 experts; run BF16 experts with flint_moe_route + "
+                    "flint_moe_decode");
     if (!x || !router_w || !ids || !weights || !y || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) ||
         !aligned(weights, 4) || !aligned(y, 16) || (bias && !aligned(bias, 4)))
         return fail(FLINT_ERR_INVALID_ARG, "layer: null or misaligned pointer");

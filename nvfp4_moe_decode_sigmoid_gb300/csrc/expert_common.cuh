@@ -216,6 +216,116 @@ __device__ __forceinline__ void stage_f16(const StageSrc (&ss)[NS], F&& between)
     }
 }
 
+// ===========================================================================
+// Residual add + RMSNorm ahead of a block, fused into the activation staging
+// ("Flint 是什么": pre-norm blocks; "Optimizations": norm kernels that follow
+// the reference's rounding). Per token: r' = bf16(r + y), x =
+// bf16(r' / sqrt(mean(r'^2) + eps) * gamma), in FP32. Every CTA normalises the
+// whole [T, H] input itself (its sums run in one fixed order, so all CTAs get
+// the same x); the CTA `cta` of G writes the chunks q with q % G == cta of r'
+// (and of x) out.
+// ===========================================================================
+// r' of the 32 values at `off` into w (bf16 words) and their sum of squares.
+__device__ __forceinline__ float norm_residual_chunk(const NormArgs& n, size_t off, uint4 (&w)[4]) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(n.r + off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = ld_cg(r4 + i);
+    if (n.y) {
+        const uint4* y4 = reinterpret_cast<const uint4*>(n.y + off);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 yv = ld_cg(y4 + i);
+            uint32_t* wa = reinterpret_cast<uint32_t*>(&w[i]);
+            const uint32_t ya[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                wa[j] = (uint32_t)f32_to_bf16_bits(bf16_lo(wa[j]) + bf16_lo(ya[j])) |
+                        ((uint32_t)f32_to_bf16_bits(bf16_hi(wa[j]) + bf16_hi(ya[j])) << 16);
+        }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t wa[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            ss = fmaf(bf16_lo(wa[j]), bf16_lo(wa[j]), ss);
+            ss = fmaf(bf16_hi(wa[j]), bf16_hi(wa[j]), ss);
+        }
+    }
+    return ss;
+}
+
+// w (r' words of the 32 values at column `col`) := bf16(r' * inv * gamma).
+__device__ __forceinline__ void norm_scale_chunk(const NormArgs& n, int col, float inv, uint4 (&w)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t g[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // bf16 1.0 pairs
+        if (n.gamma) {
+            const uint4 gv = ld_cg(reinterpret_cast<const uint4*>(n.gamma + col) + i);
+            g[0] = gv.x;
+            g[1] = gv.y;
+            g[2] = gv.z;
+            g[3] = gv.w;
+        }
+        uint32_t* wa = reinterpret_cast<uint32_t*>(&w[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            wa[j] = (uint32_t)f32_to_bf16_bits(bf16_lo(wa[j]) * inv * bf16_lo(g[j])) |
+                    ((uint32_t)f32_to_bf16_bits(bf16_hi(wa[j]) * inv * bf16_hi(g[j])) << 16);
+    }
+}
+
+// Stages x = norm(r (+ y)) of all ss.nvec tokens as chunk-scaled f16 (GATE
+// order). red: shared memory for ss.nvec * ss.K / 32 floats; inv: for
+// ss.nvec floats.
+__device__ void stage_norm_f16(const NormArgs& n, const StageSrc& ss, float* red, float* inv, int cta, int G) {
+    const int cpv = ss.K / 32, nq = ss.nvec * cpv;
+    const int q0 = threadIdx.x, nt = blockDim.x;
+    uint4 w0[4] = {};
+    for (int q = q0; q < nq; q += nt) {
+        uint4 w[4];
+        const int t = q / cpv, c = q - t * cpv;
+        const size_t off = (size_t)t * ss.K + 32 * c;
+        red[q] = norm_residual_chunk(n, off, w);
+        if (n.r_out && q % G == cta) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(n.r_out + off)[i] = w[i];
+        }
+        if (q == q0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w0[i] = w[i];
+        }
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = warp; t < ss.nvec; t += nt >> 5) {
+        float s = 0.f;
+        for (int c = lane; c < cpv; c += 32) s += red[t * cpv + c];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) inv[t] = 1.f / sqrtf(s / (float)ss.K + n.eps);
+    }
+    __syncthreads();
+    for (int q = q0; q < nq; q += nt) {
+        uint4 w[4];
+        const int t = q / cpv, c = q - t * cpv;
+        const size_t off = (size_t)t * ss.K + 32 * c;
+        if (q == q0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = w0[i];
+        } else {
+            norm_residual_chunk(n, off, w);
+        }
+        norm_scale_chunk(n, 32 * c, inv[t], w);
+        if (n.x_out && q % G == cta) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(n.x_out + off)[i] = w[i];
+        }
+        stage_store<false>(ss, t, c, w);
+    }
+}
+
 // One pass of a warp over gate row `grow` (and up row `urow`) against the NT
 // (1 or 2) tokens tk[]: the lanes split the row into 32-value chunks
 // (lane l: chunks l, l + 32, ...); the per-lane sums are reduce-scattered and

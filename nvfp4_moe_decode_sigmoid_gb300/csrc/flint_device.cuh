@@ -109,13 +109,14 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// Runtime N in 0..3.
+// Runtime N in 0..4.
 __device__ __forceinline__ void cp_async_wait_n(int n) {
     switch (n) {
         case 0: cp_async_wait<0>(); break;
         case 1: cp_async_wait<1>(); break;
         case 2: cp_async_wait<2>(); break;
-        default: cp_async_wait<3>(); break;
+        case 3: cp_async_wait<3>(); break;
+        default: cp_async_wait<4>(); break;
     }
 }
 // The warp copies `bytes` (a multiple of 16) from src to dst, lane l taking

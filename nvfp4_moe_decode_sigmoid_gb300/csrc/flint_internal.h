@@ -40,6 +40,10 @@ constexpr int kGemvWarps = 24;
 constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kMaxSlotsPerWarp = 4;
 constexpr size_t kWsHeader = 256;   // router counter (word 0), status (word 1), grid barrier tickets (word 2)
+// Expert GEMV kernels for BF16 weights: 16 warps (a BF16 row is 4x the bytes
+// of an NVFP4 row, so fewer, larger ring slots per SM).
+constexpr int kBf16Warps = 16;
+constexpr int kBf16Threads = kBf16Warps * 32;
 // Fused layer kernel: one cooperative CTA per SM.
 constexpr int kLayerWarps = 24;
 constexpr int kLayerThreads = kLayerWarps * 32;
@@ -122,6 +126,19 @@ struct DownArgs {
     int slot_bytes;           // bytes of one slot
 };
 
+// Residual add + RMSNorm ahead of a block: per token r' = bf16(r + y) (r' = r
+// without y), x = bf16(r' / sqrt(mean(r'^2) + eps) * gamma) (gamma = 1 without
+// it). r_out / x_out receive r' / x when given.
+struct NormArgs {
+    const uint16_t* r;      // [T][H]; null: no norm
+    const uint16_t* y;      // [T][H] or null
+    const uint16_t* gamma;  // [H] or null
+    float eps;
+    uint16_t* r_out;        // [T][H] or null
+    uint16_t* x_out;        // [T][H] or null
+    int T, H;
+};
+
 // The whole MoE decode step of one layer (router, gate/up, down, combine).
 struct LayerArgs {
     const uint16_t* x;
@@ -153,6 +170,7 @@ struct LayerArgs {
     int ns3;             // gate/up ring slots per warp
     int rg, ns4, slot4;  // down: rows per task, ring slots per warp, bytes per slot
     int dpre;            // 1: all of the CTA's routed down rows are prefetched after routing
+    NormArgs norm;       // norm.r set: x = the norm of the residual stream (x unused)
 };
 
 // ---------------------------------------------------------------------------
@@ -173,6 +191,14 @@ cudaError_t launch_dequant(const uint8_t* packed, int64_t rows, int64_t cols, fl
 cudaError_t launch_route(const RouteArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
 cudaError_t launch_gate_up(const GateUpArgs& a, bool pair, const DevInfo& d, bool pdl, cudaStream_t s);
 cudaError_t launch_down(const DownArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
+// BF16 expert weights (same argument blocks; gu/down/s_gu/s_down hold bf16
+// matrices, ts/s_ts may be null for 1).
+cudaError_t launch_gate_up_bf16(const GateUpArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
+cudaError_t launch_down_bf16(const DownArgs& a, const DevInfo& d, bool pdl, cudaStream_t s);
+size_t gate_up_bf16_smem_bytes(const GateUpArgs& a);
+size_t down_bf16_smem_bytes(const DownArgs& a);
+// Standalone residual add + RMSNorm (x_out required), one CTA per token.
+cudaError_t launch_rmsnorm(const NormArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t budget_ns, cudaStream_t s);
 // Cooperative launch of the fused layer kernel, one CTA on every SM (with the
 // programmatic-dependent-launch attribute when `pdl`).

@@ -183,7 +183,8 @@ class Experts:
         self.gate_up, self.down, self.tensor_scale = gate_up, down, tensor_scale
         self.num_experts, self.hidden, self.inter, self.dtype = num_experts, hidden, inter, dtype
         self.struct = flint_experts(dtype, num_experts, hidden, inter, gate_up.data_ptr(),
-                                    down.data_ptr() if down is not None else None, tensor_scale.data_ptr())
+                                    down.data_ptr() if down is not None else None,
+                                    tensor_scale.data_ptr() if tensor_scale is not None else None)
 
     @property
     def packed_bytes(self) -> int:
@@ -204,6 +205,18 @@ class Experts:
         flint_nvfp4_repack(down, num_experts, hidden, inter, dn, 0, 0, stream)
         ts = tensor_scale.to(device=dev, dtype=torch.float32).contiguous()
         return Experts(gu, dn, ts, num_experts, hidden, inter)
+
+
+    @staticmethod
+    def from_bf16(gate, up, down, num_experts, hidden, inter, tensor_scale=None):
+        """BF16 experts: gate [E, I, H], up [E, I, H], down [E, H, I] (device
+        bf16 tensors) -> the [E, 2I, H] gate/up matrices (gate rows first) and
+        down as given. tensor_scale: None (all 1) or float32 [E, 3]."""
+        E, I, H = num_experts, inter, hidden
+        gu = torch.cat([gate.reshape(E, I, H), up.reshape(E, I, H)], dim=1).contiguous()
+        dn = down.reshape(E, H, I).contiguous()
+        ts = tensor_scale.to(device=gu.device, dtype=torch.float32).contiguous() if tensor_scale is not None else None
+        return Experts(gu, dn, ts, E, H, I, dtype=FLINT_DTYPE_BF16)
 
 
 class Packed:

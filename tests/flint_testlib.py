@@ -63,23 +63,37 @@ class DeviceLayer:
         self.L = L
         dev = "cuda"
         self.router_w = L.router_w.to(dev)
-        self.routed = f.Experts.from_gguf(L.gate.to(dev), L.up.to(dev), L.down.to(dev), L.ts, L.E, L.H, L.I)
         self.shared = None
-        if L.shared is not None:
-            s = L.shared
-            self.shared = f.Experts.from_gguf(s["gate"].to(dev), s["up"].to(dev), s["down"].to(dev),
-                                              s["ts"].reshape(1, 3), 1, L.H, s["I"])
+        if L.wdtype == "nvfp4":
+            self.routed = f.Experts.from_gguf(L.gate.to(dev), L.up.to(dev), L.down.to(dev), L.ts, L.E, L.H, L.I)
+            if L.shared is not None:
+                s = L.shared
+                self.shared = f.Experts.from_gguf(s["gate"].to(dev), s["up"].to(dev), s["down"].to(dev),
+                                                  s["ts"].reshape(1, 3), 1, L.H, s["I"])
+        else:
+            self.routed = f.Experts.from_bf16(L.gate.to(dev), L.up.to(dev), L.down.to(dev), L.E, L.H, L.I,
+                                              None if L.ts is None else L.ts.to(dev))
+            if L.shared is not None:
+                s = L.shared
+                self.shared = f.Experts.from_bf16(s["gate"].to(dev), s["up"].to(dev), s["down"].to(dev), 1, L.H,
+                                                  s["I"], None if s["ts"] is None else s["ts"].reshape(1, 3).to(dev))
         torch.cuda.synchronize()
 
     def oracle_args(self):
         L = self.L
+        if L.wdtype == "nvfp4":
+            w = lambda t: t.numpy()  # noqa: E731
+            wdtype = oracle.W_NVFP4
+        else:
+            w = synth.bits
+            wdtype = oracle.W_BF16
+        opt = lambda t: None if t is None else t.numpy()  # noqa: E731
         sh = None
         if L.shared is not None:
             s = L.shared
-            sh = dict(gate=s["gate"].numpy(), up=s["up"].numpy(), down=s["down"].numpy(), ts=s["ts"].numpy(),
-                      I=s["I"])
-        return dict(E=L.E, I=L.I, gate=L.gate.numpy(), up=L.up.numpy(), down=L.down.numpy(), ts=L.ts.numpy(),
-                    shared=sh)
+            sh = dict(gate=w(s["gate"]), up=w(s["up"]), down=w(s["down"]), ts=opt(s["ts"]), I=s["I"])
+        return dict(E=L.E, I=L.I, gate=w(L.gate), up=w(L.up), down=w(L.down), ts=opt(L.ts), shared=sh,
+                    wdtype=wdtype)
 
     def workspace(self, k):
         f = flint()

@@ -74,9 +74,22 @@ def test_host_validation_without_a_gpu(flint):
     bad = flint.flint_experts(0, 256, 2000, 512, 0x1000, 0x1000, 0x1000)
     assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(bad), None, p, p, 1 << 24, 0, None) == \
         flint.FLINT_ERR_UNSUPPORTED
-    bf = flint.flint_experts(1, 256, 2048, 512, 0x1000, 0x1000, 0x1000)
-    assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(bf), None, p, p, 1 << 24, 0, None) == \
+    unk = flint.flint_experts(7, 256, 2048, 512, 0x1000, 0x1000, 0x1000)
+    assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(unk), None, p, p, 1 << 24, 0, None) == \
         flint.FLINT_ERR_UNSUPPORTED
+    # BF16 experts: routed and shared must share the dtype; the one-kernel layer is NVFP4-only
+    bf = flint.flint_experts(1, 256, 2048, 512, 0x1000, 0x1000, None)
+    bf_sh = flint.flint_experts(0, 1, 2048, 512, 0x1000, 0x1000, 0x1000)
+    assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(bf), C.byref(bf_sh), p, p, 1 << 24, 0, None) == \
+        flint.FLINT_ERR_UNSUPPORTED
+    assert "same dtype" in flint.flint_last_error()
+    assert L.flint_moe_layer(p, 1, p, 256, None, 6, C.byref(bf), None, p, p, p, p, 1 << 24, 0, None) == \
+        flint.FLINT_ERR_UNSUPPORTED
+    assert "NVFP4" in flint.flint_last_error()
+    # NVFP4 experts need their tensor scales
+    nots = flint.flint_experts(0, 256, 2048, 512, 0x1000, 0x1000, None)
+    assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(nots), None, p, p, 1 << 24, 0, None) == \
+        flint.FLINT_ERR_INVALID_ARG
     sh = flint.flint_experts(0, 2, 2048, 512, 0x1000, 0x1000, 0x1000)
     assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(ex), C.byref(sh), p, p, 1 << 24, 0, None) == \
         flint.FLINT_ERR_INVALID_ARG

@@ -55,8 +55,9 @@ def test_small_layer_pdl_is_bitwise_identical(small_layer):
     x = margin_x(synth.bits(small_layer.L.router_w), 8, 1024, 6, None, seed=3)
     a = _layer_run(small_layer, x, 6, flags=0)
     b = _layer_run(small_layer, x, 6, flags=f.FLINT_PDL)
-    for u, v in zip(a, b):
-        assert np.array_equal(u, v)
+    c = _layer_run(small_layer, x, 6, flags=f.FLINT_PDL | f.FLINT_PDL_AFTER_ROUTE, route_flags=f.FLINT_PDL)
+    for u, v, w in zip(a, b, c):
+        assert np.array_equal(u, v) and np.array_equal(u, w)
 
 
 def test_without_shared_expert():
@@ -113,10 +114,18 @@ def test_full_layer_batch1(full_layer):
     _check_layer(full_layer, x, 6, flags=f.FLINT_PDL)
 
 
+def test_full_layer_batch1_after_route(full_layer):
+    f = flint()
+    x = margin_x(synth.bits(full_layer.L.router_w), 1, 2048, 6, None, seed=17)
+    ids, w, y = _layer_run(full_layer, x, 6, flags=f.FLINT_PDL | f.FLINT_PDL_AFTER_ROUTE, route_flags=f.FLINT_PDL)
+    ref = oracle.moe_experts(synth.bits(x), ids, w, **full_layer.oracle_args())
+    assert_close(y, ref, "layer (x staged before the wait)")
+
+
 def test_full_layer_batch8_uniform(full_layer):
     f = flint()
     x = margin_x(synth.bits(full_layer.L.router_w), 8, 2048, 6, None, seed=8)
-    _check_layer(full_layer, x, 6, flags=f.FLINT_PDL)
+    _check_layer(full_layer, x, 6, flags=f.FLINT_PDL | f.FLINT_PDL_AFTER_ROUTE)
 
 
 def test_full_layer_batch8_zipf(full_layer):
