@@ -65,6 +65,9 @@ def lib():
         L.fo_dense_gemv.restype = C.c_int
         L.fo_dense_gemv.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
                                     C.c_int, C.c_void_p]
+        L.fo_residual_rmsnorm.restype = C.c_int
+        L.fo_residual_rmsnorm.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_double,
+                                          C.c_void_p, C.c_void_p]
         _lib = L
     return _lib
 
@@ -217,3 +220,44 @@ def dense_gemv(x, W, N, ts=(1.0, 1.0), epilogue=EPI_NONE, wdtype=W_NVFP4):
     _check(lib().fo_dense_gemv(_p(x), T, K, wdtype, _p(np.ascontiguousarray(W)), N, _p(tsa), epilogue, _p(y)),
            "dense_gemv")
     return y
+
+
+# ---- the decode stack: residual add + RMSNorm between blocks ----------------
+
+def residual_rmsnorm(r, y=None, gamma=None, eps=1e-6):
+    """r, y: uint16 bf16 bits [T, H] (y may be None); gamma: uint16 [H] or None.
+    Returns (r' = bf16(r + y), x = bf16(rmsnorm(r') * gamma)) as bf16 bits."""
+    r = np.ascontiguousarray(r, np.uint16)
+    T, H = r.shape
+    yy = None if y is None else np.ascontiguousarray(y, np.uint16)
+    g = None if gamma is None else np.ascontiguousarray(gamma, np.uint16)
+    r_out = np.zeros((T, H), np.uint16)
+    x_out = np.zeros((T, H), np.uint16)
+    _check(lib().fo_residual_rmsnorm(_p(r), _p(yy), T, H, _p(g), float(eps), _p(r_out), _p(x_out)),
+           "residual_rmsnorm")
+    return r_out, x_out
+
+
+def decode_stack(x0, blocks, eps=1e-6):
+    """One decode step of a pre-norm stack of MLP blocks (the attention of the
+    model is outside this path): r = x0; for each block: r, x = norm(r + y),
+    y = block(x); finally r = bf16(r + y). `blocks` holds dicts with kind
+    "dense" (keys gate_up: GGUF bytes of the [2F, H] SwiGLU matrix, ts_gu: 2
+    floats, down: GGUF bytes of [H, F], ts_down: 1 float, F) or kind "moe"
+    (the keyword arguments of moe_layer plus wr and k). Returns (r_final, per
+    block (x, y) bf16 bits, per MoE block ids)."""
+    r = np.ascontiguousarray(x0, np.uint16)
+    y = None
+    trace, ids_all = [], []
+    for b in blocks:
+        r, x = residual_rmsnorm(r, y, None, eps)
+        if b["kind"] == "dense":
+            h = dense_gemv(x, b["gate_up"], 2 * b["F"], ts=b["ts_gu"], epilogue=EPI_SWIGLU)
+            y = dense_gemv(h, b["down"], x.shape[1], ts=b["ts_down"], epilogue=EPI_NONE)
+        else:
+            args = {k: v for k, v in b.items() if k not in ("kind", "wr", "k")}
+            ids, _, y = moe_layer(x, b["wr"], b["k"], **args)
+            ids_all.append(ids)
+        trace.append((x, y))
+    r, _ = residual_rmsnorm(r, y, None, eps)
+    return r, trace, ids_all

@@ -428,3 +428,42 @@ int fo_dense_gemv(const uint16_t* x, int T, int K, int wdtype, const void* W, in
     free(xd);
     return FO_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Residual add + RMSNorm between the blocks of the decode stack             */
+/* ------------------------------------------------------------------------ */
+
+/* [News] section "Flint 是什么": Flint is a pre-norm Transformer of 49 blocks
+ * (2 dense MLP blocks, then 47 MoE blocks) on a hidden size of 2048; [Blog]
+ * section "Optimizations": norm kernels that follow the reference's rounding
+ * points. The pages fix neither the norm's epsilon nor its scale vector, nor
+ * its internal precision (the workloads use eps = 1e-6 and gamma = 1).
+ * Per token t:
+ *   r'[h] = bf16(r[h] + y[h])                  (r' = r when y is NULL)
+ *   x[h]  = bf16(r'[h] / sqrt(mean_h(r'^2) + eps) * gamma[h])   (gamma = 1 when NULL)
+ * with the sum, the mean, the square root and the products in double.
+ * r_out (may be NULL) receives r'; x_out receives x. */
+int fo_residual_rmsnorm(const uint16_t* r, const uint16_t* y, int T, int H, const uint16_t* gamma, double eps,
+                        uint16_t* r_out, uint16_t* x_out) {
+    if (!r || !x_out || T < 0 || H <= 0 || eps < 0.0) return FO_BAD_ARG;
+    double* rr = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!rr) return FO_BAD_ARG;
+    for (int t = 0; t < T; ++t) {
+        double ss = 0.0;
+        for (int h = 0; h < H; ++h) {
+            int64_t i = (int64_t)t * H + h;
+            double v = fo_bf16_value(r[i]);
+            if (y) v = fo_bf16_value(fo_bf16_round(v + fo_bf16_value(y[i])));
+            rr[h] = v;
+            ss += v * v;
+            if (r_out) r_out[i] = fo_bf16_round(v);
+        }
+        double inv = 1.0 / sqrt(ss / (double)H + eps);
+        for (int h = 0; h < H; ++h) {
+            double g = gamma ? fo_bf16_value(gamma[h]) : 1.0;
+            x_out[(int64_t)t * H + h] = fo_bf16_round(rr[h] * inv * g);
+        }
+    }
+    free(rr);
+    return FO_OK;
+}
