@@ -53,6 +53,7 @@ def parse():
     p.add_argument("--no-extra", action="store_true", help="skip the other two batch/routing workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-bf16", action="store_true", help="skip the BF16-expert variant")
+    p.add_argument("--no-stack", action="store_true", help="skip the 49-block decode stack")
     return p.parse_args()
 
 
@@ -296,6 +297,128 @@ def measure_bf16(F, nvfp4_model, args, sync_all, dev_index, n_layers=6):
     return out
 
 
+DENSE_F, N_DENSE, N_MOE = 6144, 2, 47
+
+
+class Stack:
+    """The decode stack of the model: N_DENSE dense SwiGLU MLP blocks
+    (H -> DENSE_F -> H, NVFP4) then N_MOE MoE blocks, each seeded (block b from
+    seed 1000 + b), resident on the device; residual add + RMSNorm (eps 1e-6,
+    gamma 1) ahead of every block and once after the last."""
+
+    def __init__(self, device):
+        import torch
+        from nvfp4_moe_decode_sigmoid_gb300 import flint as F
+        from nvfp4_moe_decode_sigmoid_gb300 import synth
+        self.dense, self.moe = [], []
+        for b in range(N_DENSE):
+            seed = 1000 + b
+            gu = synth.gguf_nvfp4(synth._mix(seed, 20), 1, 2 * DENSE_F, H, device)
+            dn = synth.gguf_nvfp4(synth._mix(seed, 21), 1, H, DENSE_F, device)
+            ts = synth.tensor_scales(synth._mix(seed, 22), (3,), device)
+            self.dense.append((F.Packed.from_gguf(gu, 2 * DENSE_F, H, ts[:2].contiguous()),
+                               F.Packed.from_gguf(dn, H, DENSE_F, ts[2:].contiguous())))
+            del gu, dn
+        for b in range(N_DENSE, N_DENSE + N_MOE):
+            L = synth.Layer(1000 + b, H=H, E=E, I=I, I_shared=I_SHARED, device=device)
+            s = L.shared
+            self.moe.append(dict(router_w=L.router_w,
+                                 routed=F.Experts.from_gguf(L.gate, L.up, L.down, L.ts, E, H, I),
+                                 shared=F.Experts.from_gguf(s["gate"], s["up"], s["down"], s["ts"].reshape(1, 3), 1,
+                                                            H, I_SHARED)))
+            del L, s
+            torch.cuda.synchronize()
+        self.ws = torch.empty(F.flint_workspace_bytes(E, TOPK, I, I_SHARED), dtype=torch.uint8, device=device)
+        F.flint_workspace_init(self.ws)
+
+    def dense_bytes(self):
+        from nvfp4_moe_decode_sigmoid_gb300 import flint as F
+        return (2 * DENSE_F * F.flint_nvfp4_row_stride(H) + H * F.flint_nvfp4_row_stride(DENSE_F) + 12)
+
+    def step(self, F, io, flags):
+        """One decode step of T tokens: 2 x (norm, SwiGLU GEMV, GEMV) + N_MOE
+        fused blocks + the final residual add and norm."""
+        r, y, x, h, ids, w = io["r"], io["y"], io["x"], io["h"], io["ids"], io["w"]
+        src, nxt, y_prev = io["x0"], 0, None  # the embedding x0 is only read
+        for b, (Wgu, Wdn) in enumerate(self.dense):
+            if y_prev is None:
+                F.flint_residual_rmsnorm(src, x, flags=flags)
+            else:
+                F.flint_residual_rmsnorm(src, x, y_prev=y_prev, residual_out=r[nxt], flags=flags)
+                src, nxt = r[nxt], 1 - nxt
+            F.flint_dense_gemv(x, Wgu, h, epilogue=F.FLINT_EPILOGUE_SWIGLU, flags=flags)
+            F.flint_dense_gemv(h, Wdn, y[b % 2], flags=flags)
+            y_prev = y[b % 2]
+        for i, lay in enumerate(self.moe):
+            yo = y[(N_DENSE + i) % 2]
+            F.flint_moe_block(src, lay["router_w"], TOPK, lay["routed"], lay["shared"], ids[i], w[i], yo, self.ws,
+                              y_prev=y_prev, residual_out=r[nxt], flags=flags)
+            src, nxt = r[nxt], 1 - nxt
+            y_prev = yo
+        F.flint_residual_rmsnorm(src, io["xf"], y_prev=y_prev, residual_out=io["r_final"], flags=flags)
+
+
+def measure_stack(F, args, reps=20):
+    """The full decode stack (49 blocks) per token step, PDL on and off, at
+    T = 1 and (PDL on) T = 8, each step replayed from one CUDA graph."""
+    import torch
+    from nvfp4_moe_decode_sigmoid_gb300 import synth
+    st = Stack("cuda")
+    peak, _ = load_peaks()
+    out = {}
+    for T, pdl_modes in ((1, (True, False)), (8, (True,))):
+        dev = "cuda"
+        io = dict(x0=synth.activations(4242 + T, T, H, dev),
+                  r=[torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(2)],
+                  y=[torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(2)],
+                  x=torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+                  h=torch.empty((T, DENSE_F), dtype=torch.bfloat16, device=dev),
+                  xf=torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+                  r_final=torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+                  ids=[torch.empty((T, TOPK), dtype=torch.int32, device=dev) for _ in range(N_MOE)],
+                  w=[torch.empty((T, TOPK), dtype=torch.float32, device=dev) for _ in range(N_MOE)])
+        stream = torch.cuda.Stream()
+        res = {}
+        for pdl in pdl_modes:
+            flags = F.FLINT_PDL if pdl else 0
+            with torch.cuda.stream(stream):
+                st.step(F, io, flags)  # warm-up; the routing of every block for the byte count
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    st.step(F, io, flags)
+                for _ in range(3):
+                    g.replay()
+                stream.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            assert F.flint_workspace_check(st.ws) == F.FLINT_OK
+            res[pdl] = e0.elapsed_time(e1) * 1e3 / reps
+        distinct = [len(set(i.cpu().numpy().reshape(-1).tolist())) for i in io["ids"]]
+        act = 2 * T * H * 2  # per block: residual + previous output in, new residual + output out (x, y)
+        total = (N_DENSE * (st.dense_bytes() + act) + sum(step_bytes(d, T, False) + act for d in distinct)
+                 + 2 * T * H * 2 * 2)
+        us = res[True]
+        ent = dict(us_per_step_pdl=round(us, 2), gb_s=round(total / (us * 1e-6) / 1e9, 1),
+                   frac_of_peak=round(total / (us * 1e-6) / 1e9 / peak, 4), bytes_per_step=total,
+                   mean_distinct_experts=round(sum(distinct) / len(distinct), 2),
+                   launches_per_step=3 * N_DENSE + N_MOE + 1)
+        if False in res:
+            ent["us_per_step_no_pdl"] = round(res[False], 2)
+        out[f"T{T}"] = ent
+    del st
+    torch.cuda.empty_cache()
+    out["blocks"] = f"{N_DENSE} dense SwiGLU MLP ({H}->{DENSE_F}->{H}, NVFP4) + {N_MOE} MoE blocks, residual + RMSNorm"
+    out["path"] = ("dense: flint_residual_rmsnorm -> flint_dense_gemv (SwiGLU) -> flint_dense_gemv; MoE: "
+                   "flint_moe_block (norm fused, one cooperative kernel); final flint_residual_rmsnorm; one CUDA "
+                   "graph per step")
+    return out
+
+
 def measure_kernels(F, model, name, reps=8):
     """Average device duration of each kernel: the fused layer kernel and the
     three kernels of the chain. For each, a CUDA graph of back-to-back
@@ -482,10 +605,16 @@ def run_flint(args):
     bf16 = {}
     if not args.no_bf16:
         bf16 = measure_bf16(F, model, args, sync_all, dev_index)
+
     peak, peak_src = load_peaks()
     achieved = kern["layer_bytes"] / (kern["layer_us"] * 1e-6) / 1e9
     traffic = traffic_for(kernel_source_hash())
     e2e = measure_e2e(F, model, args.workload, min(args.steps, 8192), args.graph_steps)
+    stack = {}
+    if not args.no_stack:
+        del model
+        torch.cuda.empty_cache()
+        stack = measure_stack(F, args)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload)
@@ -532,6 +661,7 @@ def run_flint(args):
             "clocks": main["clocks"],
             "extra_workloads": extra,
             "bf16_experts": bf16,
+            "decode_stack": stack,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

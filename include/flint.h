@@ -293,6 +293,51 @@ flint_status_t flint_moe_layer(const flint_bf16* x, int T, const flint_bf16* rou
                                void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Residual stream of the decode stack                                       */
+/* ------------------------------------------------------------------------ */
+/*
+ * "vLLM 宣布首日支持 Recursive 的 Flint ...", section "Flint 是什么": the model
+ * is a pre-norm Transformer of 49 blocks, 2 dense MLP blocks then 47 MoE
+ * blocks, on a hidden size of 2048; "Day-0 Support for Flint on vLLM",
+ * section "Optimizations": norm kernels that follow the reference's rounding.
+ * Ahead of every block, per token:
+ *   r' = bf16(r + y)                                 (r' = r when y is NULL)
+ *   x  = bf16(r' / sqrt(mean(r'^2) + eps) * gamma)   (gamma = 1 when NULL)
+ * in FP32; r' is the residual stream the next block adds its output to.
+ */
+typedef struct flint_norm {
+    const flint_bf16* residual;  /* r [T, H], required */
+    const flint_bf16* y;         /* the previous block's output [T, H], or NULL */
+    const flint_bf16* gamma;     /* [H], or NULL for all ones */
+    float eps;                   /* >= 0 (the workloads use 1e-6) */
+    float reserved;
+    flint_bf16* residual_out;    /* r' [T, H], or NULL; must not overlap residual or y */
+    flint_bf16* x_out;           /* x [T, H], or NULL */
+} flint_norm;
+
+/*
+ * flint_residual_rmsnorm -- r' and x of the definition above, one small kernel
+ * (one CTA per token). x_out is required.
+ *   H % 256 == 0, H <= 32768; 1 <= T <= 8; all arrays 16-byte aligned.
+ *   flags: FLINT_PDL (the kernel waits for the previous kernel before reading r and y).
+ */
+flint_status_t flint_residual_rmsnorm(const flint_norm* norm, int T, int H, unsigned flags, void* stream);
+
+/*
+ * flint_moe_block -- one pre-norm MoE block in ONE kernel: the residual add +
+ * RMSNorm above, fused into the input staging of flint_moe_layer (every CTA
+ * normalises the whole input itself; no extra launch, no extra barrier), then
+ * the MoE layer on x. Arguments as flint_moe_layer, with `norm` in place of x
+ * (norm->x_out may be NULL; when given, x is written too). y must not overlap
+ * norm->residual, norm->y or norm->residual_out. Chained blocks alternate two
+ * residual buffers (a block reads one and writes the other).
+ */
+flint_status_t flint_moe_block(const flint_norm* norm, int T, const flint_bf16* router_w, int E, const float* bias,
+                               int k, const flint_experts* routed, const flint_experts* shared, int32_t* ids,
+                               float* weights, flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
+                               void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Dense GEMV on packed weights                                              */
 /* ------------------------------------------------------------------------ */
 

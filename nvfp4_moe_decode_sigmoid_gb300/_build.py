@@ -12,7 +12,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libflint.so")
-SOURCES = ["abi.cu", "repack.cu", "route.cu", "gemv.cu", "layer.cu", "bf16.cu"]
+SOURCES = ["abi.cu", "repack.cu", "route.cu", "gemv.cu", "layer.cu", "bf16.cu", "norm.cu"]
 HEADERS = ["flint_device.cuh", "flint_internal.h", "expert_common.cuh", "router_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")

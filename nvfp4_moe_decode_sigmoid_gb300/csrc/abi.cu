@@ -479,20 +479,76 @@ flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, 
     return flint_moe_down_combine(T, ids, weights, k, routed, shared, y, ws, ws_bytes, flags, stream);
 }
 
-flint_status_t flint_moe_layer(const flint_bf16* x, int T, const flint_bf16* router_w, int E, const float* bias, int k,
-                               const flint_experts* routed, const flint_experts* shared, int32_t* ids, float* weights,
-                               flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags, void* stream) {
-    flint_status_t s = moe_common("layer", T, k, routed, shared, true);
+// Validates a flint_norm for T tokens of H values and fills the kernel's view.
+static flint_status_t norm_args(const char* what, const flint_norm* n, int T, int H, bool need_x,
+                                flint::NormArgs& a) {
+    if (!n) return fail(FLINT_ERR_INVALID_ARG, "%s: norm is null", what);
+    if (H <= 0 || H % 256 || H > 32768)
+        return fail(FLINT_ERR_UNSUPPORTED, "%s: H=%d must be a multiple of 256 up to 32768", what, H);
+    if (!(n->eps >= 0.f)) return fail(FLINT_ERR_INVALID_ARG, "%s: eps must be >= 0", what);
+    if (!n->residual || !aligned(n->residual, 16) || (n->y && !aligned(n->y, 16)) ||
+        (n->gamma && !aligned(n->gamma, 16)) || (n->residual_out && !aligned(n->residual_out, 16)) ||
+        (n->x_out && !aligned(n->x_out, 16)) || (need_x && !n->x_out))
+        return fail(FLINT_ERR_INVALID_ARG, "%s: null or misaligned norm pointer", what);
+    const size_t bytes = (size_t)T * H * 2;
+    auto overlap = [bytes](const void* p, const void* q) {
+        if (!p || !q) return false;
+        const uint8_t *a = static_cast<const uint8_t*>(p), *b = static_cast<const uint8_t*>(q);
+        return a < b + bytes && b < a + bytes;
+    };
+    if (overlap(n->residual_out, n->residual) || overlap(n->residual_out, n->y))
+        return fail(FLINT_ERR_INVALID_ARG, "%s: residual_out overlaps residual or y", what);
+    a = {};
+    a.r = n->residual;
+    a.y = n->y;
+    a.gamma = n->gamma;
+    a.eps = n->eps;
+    a.r_out = n->residual_out;
+    a.x_out = n->x_out;
+    a.T = T;
+    a.H = H;
+    return FLINT_OK;
+}
+
+flint_status_t flint_residual_rmsnorm(const flint_norm* norm, int T, int H, unsigned flags, void* stream) {
+    if (T < 1 || T > FLINT_MAX_TOKENS) return fail(FLINT_ERR_UNSUPPORTED, "rmsnorm: T=%d outside 1..%d", T, FLINT_MAX_TOKENS);
+    flint::NormArgs a;
+    flint_status_t s = norm_args("rmsnorm", norm, T, H, true, a);
     if (s != FLINT_OK) return s;
+    DevInfo d;
+    if ((s = device_info(d)) != FLINT_OK) return s;
+    cudaError_t e = flint::launch_rmsnorm(a, (flags & FLINT_PDL) != 0, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "rmsnorm launch");
+}
+
+static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, const flint_norm* norm, int T,
+                                     const flint_bf16* router_w, int E, const float* bias, int k,
+                                     const flint_experts* routed, const flint_experts* shared, int32_t* ids,
+                                     float* weights, flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
+                                     void* stream) {
+    flint_status_t s = moe_common(what, T, k, routed, shared, true);
+    if (s != FLINT_OK) return s;
+    flint::NormArgs na = {};
+    if (norm) {
+        if ((s = norm_args(what, norm, T, routed->hidden, false, na)) != FLINT_OK) return s;
+        const size_t bytes = (size_t)T * routed->hidden * 2;
+        for (const void* p : {static_cast<const void*>(norm->residual), static_cast<const void*>(norm->y),
+                              static_cast<const void*>(norm->residual_out), static_cast<const void*>(norm->x_out)}) {
+            const uint8_t *a = static_cast<const uint8_t*>(p), *b = reinterpret_cast<const uint8_t*>(y);
+            if (p && y && a < b + bytes && b < a + bytes)
+                return fail(FLINT_ERR_INVALID_ARG, "%s: y overlaps a buffer of the norm", what);
+        }
+        x = norm->residual;  // checked below like x; the kernel reads the norm's buffers
+    }
     if (E != routed->num_experts)
-        return fail(FLINT_ERR_INVALID_ARG, "layer: router has %d rows, routed experts %d", E, routed->num_experts);
+        return fail(FLINT_ERR_INVALID_ARG, "%s: router has %d rows, routed experts %d", what, E, routed->num_experts);
     if (routed->dtype != FLINT_DTYPE_NVFP4)
         return fail(FLINT_ERR_UNSUPPORTED,
-                    "layer: the one-kernel layer takes NVFP4 experts; run BF16 experts with flint_moe_route + "
-                    "flint_moe_decode");
+                    "%s: the one-kernel layer takes NVFP4 experts; run BF16 experts with flint_moe_route + "
+                    "flint_moe_decode", what);
     if (!x || !router_w || !ids || !weights || !y || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) ||
         !aligned(weights, 4) || !aligned(y, 16) || (bias && !aligned(bias, 4)))
-        return fail(FLINT_ERR_INVALID_ARG, "layer: null or misaligned pointer");
+        return fail(FLINT_ERR_INVALID_ARG, "%s: null or misaligned pointer", what);
     const int Is = shared ? shared->inter : 0;
     const flint::WsLayout W = flint::ws_layout(E, k, routed->inter, Is);
     if ((s = check_ws(ws, ws_bytes, W.total)) != FLINT_OK) return s;
@@ -522,10 +578,27 @@ flint_status_t flint_moe_layer(const flint_bf16* x, int T, const flint_bf16* rou
     a.h_routed = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + W.h_routed_off);
     a.h_shared = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + W.h_shared_off);
     a.y = y;
+    a.norm = na;
     if (!layer_shape(a, d.sm_count, d.smem_optin))
-        return fail(FLINT_ERR_UNSUPPORTED, "layer: shapes exceed one CTA's shared memory");
+        return fail(FLINT_ERR_UNSUPPORTED, "%s: shapes exceed one CTA's shared memory", what);
     cudaError_t e = flint::launch_layer(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "layer launch");
+}
+
+flint_status_t flint_moe_layer(const flint_bf16* x, int T, const flint_bf16* router_w, int E, const float* bias, int k,
+                               const flint_experts* routed, const flint_experts* shared, int32_t* ids, float* weights,
+                               flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags, void* stream) {
+    return moe_layer_impl("layer", x, nullptr, T, router_w, E, bias, k, routed, shared, ids, weights, y, ws, ws_bytes,
+                          flags, stream);
+}
+
+flint_status_t flint_moe_block(const flint_norm* norm, int T, const flint_bf16* router_w, int E, const float* bias,
+                               int k, const flint_experts* routed, const flint_experts* shared, int32_t* ids,
+                               float* weights, flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
+                               void* stream) {
+    if (!norm) return fail(FLINT_ERR_INVALID_ARG, "block: norm is null");
+    return moe_layer_impl("block", nullptr, norm, T, router_w, E, bias, k, routed, shared, ids, weights, y, ws,
+                          ws_bytes, flags, stream);
 }
 
 flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* W, int epilogue, flint_bf16* y,

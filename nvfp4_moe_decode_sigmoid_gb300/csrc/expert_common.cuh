@@ -225,6 +225,21 @@ __device__ __forceinline__ void stage_f16(const StageSrc (&ss)[NS], F&& between)
 // the same x); the CTA `cta` of G writes the chunks q with q % G == cta of r'
 // (and of x) out.
 // ===========================================================================
+// bf16(a + b) of the two bf16 pairs of a word (FP32 add, round to nearest even).
+__device__ __forceinline__ uint32_t bf16x2_add_round(uint32_t a, uint32_t b) {
+    return (uint32_t)f32_to_bf16_bits(bf16_lo(a) + bf16_lo(b)) |
+           ((uint32_t)f32_to_bf16_bits(bf16_hi(a) + bf16_hi(b)) << 16);
+}
+// bf16(a * inv * g) of the two bf16 pairs of a word.
+__device__ __forceinline__ uint32_t bf16x2_scale_round(uint32_t a, float inv, uint32_t g) {
+    return (uint32_t)f32_to_bf16_bits(bf16_lo(a) * inv * bf16_lo(g)) |
+           ((uint32_t)f32_to_bf16_bits(bf16_hi(a) * inv * bf16_hi(g)) << 16);
+}
+__device__ __forceinline__ float bf16x2_sumsq(uint32_t a, float ss) {
+    ss = fmaf(bf16_lo(a), bf16_lo(a), ss);
+    return fmaf(bf16_hi(a), bf16_hi(a), ss);
+}
+
 // r' of the 32 values at `off` into w (bf16 words) and their sum of squares.
 __device__ __forceinline__ float norm_residual_chunk(const NormArgs& n, size_t off, uint4 (&w)[4]) {
     const uint4* r4 = reinterpret_cast<const uint4*>(n.r + off);
@@ -235,23 +250,17 @@ __device__ __forceinline__ float norm_residual_chunk(const NormArgs& n, size_t o
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint4 yv = ld_cg(y4 + i);
-            uint32_t* wa = reinterpret_cast<uint32_t*>(&w[i]);
-            const uint32_t ya[4] = {yv.x, yv.y, yv.z, yv.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                wa[j] = (uint32_t)f32_to_bf16_bits(bf16_lo(wa[j]) + bf16_lo(ya[j])) |
-                        ((uint32_t)f32_to_bf16_bits(bf16_hi(wa[j]) + bf16_hi(ya[j])) << 16);
+            w[i] = make_uint4(bf16x2_add_round(w[i].x, yv.x), bf16x2_add_round(w[i].y, yv.y),
+                              bf16x2_add_round(w[i].z, yv.z), bf16x2_add_round(w[i].w, yv.w));
         }
     }
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t wa[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            ss = fmaf(bf16_lo(wa[j]), bf16_lo(wa[j]), ss);
-            ss = fmaf(bf16_hi(wa[j]), bf16_hi(wa[j]), ss);
-        }
+        ss = bf16x2_sumsq(w[i].x, ss);
+        ss = bf16x2_sumsq(w[i].y, ss);
+        ss = bf16x2_sumsq(w[i].z, ss);
+        ss = bf16x2_sumsq(w[i].w, ss);
     }
     return ss;
 }
@@ -260,19 +269,10 @@ __device__ __forceinline__ float norm_residual_chunk(const NormArgs& n, size_t o
 __device__ __forceinline__ void norm_scale_chunk(const NormArgs& n, int col, float inv, uint4 (&w)[4]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        uint32_t g[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // bf16 1.0 pairs
-        if (n.gamma) {
-            const uint4 gv = ld_cg(reinterpret_cast<const uint4*>(n.gamma + col) + i);
-            g[0] = gv.x;
-            g[1] = gv.y;
-            g[2] = gv.z;
-            g[3] = gv.w;
-        }
-        uint32_t* wa = reinterpret_cast<uint32_t*>(&w[i]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            wa[j] = (uint32_t)f32_to_bf16_bits(bf16_lo(wa[j]) * inv * bf16_lo(g[j])) |
-                    ((uint32_t)f32_to_bf16_bits(bf16_hi(wa[j]) * inv * bf16_hi(g[j])) << 16);
+        uint4 g = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // bf16 1.0 pairs
+        if (n.gamma) g = ld_cg(reinterpret_cast<const uint4*>(n.gamma + col) + i);
+        w[i] = make_uint4(bf16x2_scale_round(w[i].x, inv, g.x), bf16x2_scale_round(w[i].y, inv, g.y),
+                          bf16x2_scale_round(w[i].z, inv, g.z), bf16x2_scale_round(w[i].w, inv, g.w));
     }
 }
 

@@ -14,9 +14,11 @@
 //   0. Before the PDL wait: this CTA's router rows, its slice of the shared
 //      expert's gate/up pairs and its slice of the shared expert's down rows
 //      are copied into shared memory (static weights).
-//   1. x is staged (chunk-scaled f16, for gate/up); the CTA's router logits
-//      are computed in FP32 from bf16 x and bf16 router rows and written to
-//      the workspace. Grid barrier.
+//   1. x is staged (chunk-scaled f16, for gate/up); for a pre-norm block
+//      every CTA first computes x = rmsnorm(r + y_prev) itself from the
+//      residual stream and writes its share of the new residual out. The
+//      CTA's router logits are computed in FP32 from the staged x and bf16
+//      router rows and written to the workspace. Grid barrier.
 //   2. Every CTA reads all logits and selects the top-k of every token itself
 //      (one warp per token), so no second barrier is needed to share the
 //      routing; CTA 0 also writes ids and weights out.
@@ -44,11 +46,13 @@ struct LayerSmall {
     float tsd[kMaxDistinct + 1];
     float w[kMaxDistinct];
     int32_t ids[kMaxDistinct];
+    float ninv[FLINT_MAX_TOKENS];  // per-token 1 / rms of the normalised input
 };
 
 // Shared memory, by lifetime:
 //   persistent: routing view, small arrays, the shared expert's down rows;
-//   phases 0-3 (region U1): staged x and its chunk scales, the shared
+//   phases 0-3 (region U1): staged x and its chunk scales (and the norm's
+//     per-chunk sums of squares when the input is normalised here), the shared
 //     expert's gate/up pairs, then one of: router rows (phases 0-1), sigmoid
 //     scores (phase 2), raw gate/up sums + the gate/up rings (phase 3);
 //   phase 4 (region U4, over U1): staged h and its chunk scales, d values,
@@ -56,7 +60,7 @@ struct LayerSmall {
 //   the prefetched down rows (a.dpre), beside both.
 struct LayerSmem {
     size_t ri, small, shdn, U;
-    size_t xs, csc, shgu, V;
+    size_t xs, csc, nred, shgu, V;
     size_t wrows, scores;
     size_t resg, resu, ring3;
     size_t hr, hs, csr, css, dval, ring4;
@@ -75,7 +79,8 @@ __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     // U1
     L.xs = L.U;
     L.csc = align_up(L.xs + 2 * T * H, 128);
-    L.shgu = align_up(L.csc + sizeof(float) * T * (H / 32), 128);
+    L.nred = align_up(L.csc + sizeof(float) * T * (H / 32), 128);
+    L.shgu = align_up(L.nred + (a.norm.r ? sizeof(float) * T * (H / 32) : 0), 128);
     L.V = align_up(L.shgu + 2 * (size_t)a.shp * RS, 128);
     L.wrows = L.V;
     L.scores = L.V;
@@ -151,9 +156,12 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 
     pdl_wait();  // x comes from the previous kernel
 
-    // ---- 1: stage x; this CTA's router logits --------------------------------------
+    // ---- 1: stage x (or the norm of the residual stream); this CTA's router logits --
     const StageSrc xsrc[1] = {{a.x, xh, csc, T, H}};
-    stage_f16<false>(xsrc, [] {});
+    if (a.norm.r)
+        stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), sm.ninv, c, G);
+    else
+        stage_f16<false>(xsrc, [] {});
     cp_async_wait<0>();
     __syncthreads();
     // logits from the staged (exact, chunk-scaled f16) x: lane l takes the

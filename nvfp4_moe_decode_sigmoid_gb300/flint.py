@@ -50,6 +50,11 @@ class flint_packed(C.Structure):
                 ("data", C.c_void_p), ("tensor_scale", C.c_void_p)]
 
 
+class flint_norm(C.Structure):
+    _fields_ = [("residual", C.c_void_p), ("y", C.c_void_p), ("gamma", C.c_void_p), ("eps", C.c_float),
+                ("reserved", C.c_float), ("residual_out", C.c_void_p), ("x_out", C.c_void_p)]
+
+
 def _load():
     if not os.path.exists(_LIB_PATH):
         raise ImportError(f"libflint.so is not built ({_LIB_PATH}); run __graft_entry__.build() first")
@@ -79,6 +84,9 @@ def _load():
         "flint_moe_route_static": (i32, [vp, i32, i32, vp, i32, vp, i32, vp, vp, u32, vp]),
         "flint_moe_layer": (i32, [vp, i32, vp, i32, vp, i32, C.POINTER(flint_experts), C.POINTER(flint_experts), vp,
                                   vp, vp, vp, sz, u32, vp]),
+        "flint_residual_rmsnorm": (i32, [C.POINTER(flint_norm), i32, i32, u32, vp]),
+        "flint_moe_block": (i32, [C.POINTER(flint_norm), i32, vp, i32, vp, i32, C.POINTER(flint_experts),
+                                  C.POINTER(flint_experts), vp, vp, vp, vp, sz, u32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -276,6 +284,35 @@ def flint_moe_layer(x, router_w, k, routed: Experts, shared: Experts | None, ids
     _check(_lib.flint_moe_layer(_ptr(x), T, _ptr(router_w), E, _ptr(bias), k, _ex(routed), _ex(shared), _ptr(ids),
                                 _ptr(weights), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(), flags,
                                 _stream(stream)), "moe_layer")
+
+
+def _norm(residual, y_prev, gamma, eps, residual_out, x_out):
+    return flint_norm(residual.data_ptr(), y_prev.data_ptr() if y_prev is not None else None,
+                      gamma.data_ptr() if gamma is not None else None, float(eps), 0.0,
+                      residual_out.data_ptr() if residual_out is not None else None,
+                      x_out.data_ptr() if x_out is not None else None)
+
+
+def flint_residual_rmsnorm(residual, x_out, y_prev=None, residual_out=None, gamma=None, eps=1e-6, flags=0,
+                           stream=None):
+    """r' = bf16(residual + y_prev) into residual_out (when given) and
+    x = bf16(rmsnorm(r') * gamma) into x_out; all [T, H] bf16 (gamma [H])."""
+    T, H = residual.shape
+    n = _norm(residual, y_prev, gamma, eps, residual_out, x_out)
+    _check(_lib.flint_residual_rmsnorm(C.byref(n), T, H, flags, _stream(stream)), "residual_rmsnorm")
+
+
+def flint_moe_block(residual, router_w, k, routed: Experts, shared: Experts | None, ids, weights, y, ws,
+                    y_prev=None, residual_out=None, x_out=None, gamma=None, eps=1e-6, bias=None, flags=0,
+                    stream=None):
+    """One pre-norm MoE block in one launch: x = rmsnorm(residual + y_prev)
+    (residual_out receives the sum), then the MoE layer on x into y."""
+    T = residual.shape[0]
+    E = router_w.shape[0]
+    n = _norm(residual, y_prev, gamma, eps, residual_out, x_out)
+    _check(_lib.flint_moe_block(C.byref(n), T, _ptr(router_w), E, _ptr(bias), k, _ex(routed), _ex(shared),
+                                _ptr(ids), _ptr(weights), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(), flags,
+                                _stream(stream)), "moe_block")
 
 
 def flint_dense_gemv(x, W: Packed, y, epilogue=FLINT_EPILOGUE_NONE, ws=None, flags=0, stream=None):

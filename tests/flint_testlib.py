@@ -25,14 +25,61 @@ def bf16_to_f64(bits):
     return b.view(np.float32).astype(np.float64)
 
 
-def assert_close(y_gpu_bits, y_ref_bits, what=""):
+def bf16_ulp(v):
+    """One unit in the last place of bf16 at magnitude |v| (8 significant bits)."""
+    mag = np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(mag)) - 7)
+
+
+def assert_close(y_gpu_bits, y_ref_bits, what="", terms=None):
+    """The layer tolerance: relative L2 error <= REL_L2 and per element
+    |gpu - ref| <= ELEM_A (|ref| + ELEM_B).
+
+    terms (optional, [T, H]): sum_j |w_j d_j| + |d_shared| per output element
+    (from the oracle). y is a sum of bf16-rounded terms; a term whose FP32 and
+    double sums straddle a bf16 rounding boundary rounds one ulp apart, which
+    moves y by up to w_j ulp(d_j). Where the terms cancel (|y| much smaller
+    than the terms) that exceeds the relative bound without being an error.
+    With `terms`, an element outside the per-element bound still passes if
+    its error is within 2 ulp(terms), and such elements must be rare (<= 0.1 %)."""
     a, r = bf16_to_f64(y_gpu_bits), bf16_to_f64(y_ref_bits)
     assert np.all(np.isfinite(a)), f"{what}: non-finite GPU output"
     rel = np.linalg.norm(a - r) / max(np.linalg.norm(r), 1e-30)
     assert rel <= REL_L2, f"{what}: relative L2 error {rel:.3e} > {REL_L2}"
-    bad = np.abs(a - r) > ELEM_A * (np.abs(r) + ELEM_B)
+    err = np.abs(a - r)
+    bad = err > ELEM_A * (np.abs(r) + ELEM_B)
+    if terms is not None and bad.any():
+        cancel = bad & (err <= 2.0 * bf16_ulp(terms))
+        assert cancel.sum() <= max(1, 1e-3 * bad.size), f"{what}: {int(cancel.sum())} cancellation outliers"
+        bad = bad & ~cancel
     assert not bad.any(), f"{what}: {int(bad.sum())} elements outside tolerance, e.g. gpu {a[bad][:4]} ref {r[bad][:4]}"
     return rel
+
+
+def combine_terms(x_bits, ids, weights, dl):
+    """sum_j |w_j d_j| + |d_shared| per token and output row, from the oracle's
+    per-expert outputs (for assert_close's cancellation allowance)."""
+    args = dl.oracle_args()
+    L = dl.L
+    H, I = L.H, L.I
+    x_bits = np.asarray(x_bits, np.uint16)
+    T, k = ids.shape
+    per = lambda a, e: np.ascontiguousarray(a.reshape(L.E, -1)[e])  # noqa: E731
+    out = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            e = int(ids[t, j])
+            ts = args["ts"][e] if args["ts"] is not None else (1.0, 1.0, 1.0)
+            _, _, _, d = oracle.expert(x_bits[t], per(args["gate"], e), per(args["up"], e),
+                                       per(args["down"], e), H, I, ts=ts, wdtype=args["wdtype"])
+            out[t] += abs(float(weights[t, j])) * np.abs(bf16_to_f64(d))
+        sh = args["shared"]
+        if sh is not None:
+            ts = sh["ts"] if sh["ts"] is not None else (1.0, 1.0, 1.0)
+            _, _, _, d = oracle.expert(x_bits[t], sh["gate"].reshape(-1), sh["up"].reshape(-1),
+                                       sh["down"].reshape(-1), H, sh["I"], ts=ts, wdtype=args["wdtype"])
+            out[t] += np.abs(bf16_to_f64(d))
+    return out
 
 
 def margin_x(router_bits, T, H, k, bias, seed, margin=MARGIN):

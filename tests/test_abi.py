@@ -100,3 +100,30 @@ def test_host_validation_without_a_gpu(flint):
     assert L.flint_dense_gemv(p, 1, C.byref(W), 1, p, None, 0, 0, None) == flint.FLINT_ERR_UNSUPPORTED
     W2 = flint.flint_packed(0, 8, 512, 0, 0x1000, 0x1000)
     assert L.flint_dense_gemv(p, 1, C.byref(W2), 0, p, None, 0, 0, None) == flint.FLINT_ERR_UNSUPPORTED
+
+
+def test_norm_validation_without_a_gpu(flint):
+    L = _raw(flint)
+    p = C.c_void_p(0x10000)
+    q = C.c_void_p(0x20000)
+    o = C.c_void_p(0x30000)
+    n = flint.flint_norm(0x10000, None, None, 1e-6, 0.0, 0x20000, 0x30000)
+    # x_out required for the standalone norm; H must be a multiple of 256
+    nx = flint.flint_norm(0x10000, None, None, 1e-6, 0.0, 0x20000, None)
+    assert L.flint_residual_rmsnorm(C.byref(nx), 1, 2048, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    assert L.flint_residual_rmsnorm(C.byref(n), 1, 2000, 0, None) == flint.FLINT_ERR_UNSUPPORTED
+    assert L.flint_residual_rmsnorm(C.byref(n), 9, 2048, 0, None) == flint.FLINT_ERR_UNSUPPORTED
+    assert L.flint_residual_rmsnorm(None, 1, 2048, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    # residual_out may not overlap the residual it is computed from
+    ov = flint.flint_norm(0x10000, None, None, 1e-6, 0.0, 0x10400, 0x30000)
+    assert L.flint_residual_rmsnorm(C.byref(ov), 1, 2048, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    assert "overlaps" in flint.flint_last_error()
+    neg = flint.flint_norm(0x10000, None, None, -1.0, 0.0, 0x20000, 0x30000)
+    assert L.flint_residual_rmsnorm(C.byref(neg), 1, 2048, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    # block: y may not overlap the norm's buffers
+    ex = flint.flint_experts(0, 256, 2048, 512, 0x1000, 0x1000, 0x1000)
+    assert L.flint_moe_block(C.byref(n), 1, p, 256, None, 6, C.byref(ex), None, p, p, C.c_void_p(0x20000), p,
+                             1 << 24, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    assert L.flint_moe_block(None, 1, p, 256, None, 6, C.byref(ex), None, p, p, o, p, 1 << 24, 0, None) == \
+        flint.FLINT_ERR_INVALID_ARG
+    del q
