@@ -196,19 +196,24 @@ __device__ __forceinline__ void stage_store(const StageSrc& ss, int v, int c, co
     }
 }
 
-// Stages the sources; every thread first issues the loads of its first chunk,
+// Stages the sources; every thread first issues the loads of its first chunk
+// (first two in DOWN order: h of 8 tokens is more than one chunk per thread),
 // then runs `between` (the callers issue their weight copies there, so that
 // these small loads are not queued behind the weight stream), then converts.
-// Further chunks (more than one per thread) are loaded and converted after.
+// Further chunks are loaded and converted after.
 template <bool DOWN_ORDER, int NS, typename F>
 __device__ __forceinline__ void stage_f16(const StageSrc (&ss)[NS], F&& between) {
-    int s0 = 0, v0 = 0, c0 = 0;
-    uint4 w[4];
+    constexpr int AHEAD = DOWN_ORDER ? 2 : 1;  // chunks loaded ahead of `between` (h: up to two per thread)
+    int s0 = 0, v0 = 0, c0 = 0, s1 = 0, v1 = 0, c1 = 0;
+    uint4 w[4], w1[4];
     const bool have = stage_locate(ss, threadIdx.x, s0, v0, c0);
+    const bool have1 = AHEAD > 1 && stage_locate(ss, threadIdx.x + (int)blockDim.x, s1, v1, c1);
     if (have) stage_load(ss[s0], v0, c0, w);
+    if (have1) stage_load(ss[s1], v1, c1, w1);
     between();
     if (have) stage_store<DOWN_ORDER>(ss[s0], v0, c0, w);
-    for (int q = threadIdx.x + (int)blockDim.x;; q += (int)blockDim.x) {
+    if (have1) stage_store<DOWN_ORDER>(ss[s1], v1, c1, w1);
+    for (int q = threadIdx.x + AHEAD * (int)blockDim.x;; q += (int)blockDim.x) {
         int s, v, c;
         if (!stage_locate(ss, q, s, v, c)) break;
         stage_load(ss[s], v, c, w);

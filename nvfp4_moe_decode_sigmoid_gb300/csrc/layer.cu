@@ -116,6 +116,10 @@ __device__ __forceinline__ void block_copy_async(void* dst, const void* src, siz
     for (size_t o = 16 * (size_t)threadIdx.x; o < bytes; o += 16 * (size_t)kLT) cp_async16(d + o, s + o);
 }
 
+// NORM: the input is rmsnorm(r + y_prev) of the residual stream (a.norm), not
+// a.x. Two instantiations, so that the plain layer carries none of the norm's
+// code (measured: the never-taken branch alone cost 3-4 us at T = 8).
+template <bool NORM>
 __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const LayerSmem L = layer_layout(a);
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 
     // ---- 1: stage x (or the norm of the residual stream); this CTA's router logits --
     const StageSrc xsrc[1] = {{a.x, xh, csc, T, H}};
-    if (a.norm.r)
+    if constexpr (NORM)
         stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), sm.ninv, c, G);
     else
         stage_f16<false>(xsrc, [] {});
@@ -486,13 +490,15 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 
 size_t layer_smem_bytes(const LayerArgs& a) { return layer_layout(a).total; }
 
-cudaError_t launch_layer(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
+namespace {
+template <bool NORM>
+cudaError_t launch_layer_t(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
     static int configured_for = -1;
-    cudaError_t e = configure_smem(layer_kernel, d, configured_for);
+    cudaError_t e = configure_smem(layer_kernel<NORM>, d, configured_for);
     if (e != cudaSuccess) return e;
     const size_t smem = layer_smem_bytes(a);
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_kernel, kLT, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_kernel<NORM>, kLT, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     cudaLaunchConfig_t cfg = {};
@@ -507,7 +513,12 @@ cudaError_t launch_layer(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStr
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, layer_kernel, a);
+    return cudaLaunchKernelEx(&cfg, layer_kernel<NORM>, a);
+}
+}  // namespace
+
+cudaError_t launch_layer(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
+    return a.norm.r ? launch_layer_t<true>(a, d, pdl, s) : launch_layer_t<false>(a, d, pdl, s);
 }
 
 }  // namespace flint
