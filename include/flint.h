@@ -338,6 +338,36 @@ flint_status_t flint_moe_block(const flint_norm* norm, int T, const flint_bf16* 
                                void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Prefill: the MoE layer over many tokens, on the tensor cores               */
+/* ------------------------------------------------------------------------ */
+/*
+ * flint_moe_prefill -- the same MoE layer as flint_moe_layer over T tokens at
+ * once ("Day-0 Support for Flint on vLLM", section "Optimizations": the
+ * MoE-kernel rewrite that reads only the selected experts' weights was also
+ * the largest gain of the 8K-token prefill). Same arithmetic and rounding
+ * points as the decode path; the contractions run on the 5th-generation
+ * tensor cores (tcgen05.mma, bf16 operands with the NVFP4 weights
+ * dequantised exactly in shared memory, FP32 accumulation in tensor memory):
+ * router GEMM -> sigmoid top-k per token -> (token, rank) pairs sorted by
+ * expert (token order kept within an expert) -> grouped gate/up GEMM + SiLU ->
+ * grouped down GEMM -> y = bf16(sum_j w_j d_j + d_shared) gathered per token
+ * (no atomics: deterministic). Eight launches in stream order.
+ *   x [T, H] bf16, T >= 1; router_w [E, H] bf16, E % 16 == 0, E <= 1024;
+ *   bias [E] or NULL; 1 <= k <= min(8, E); NVFP4 experts only (H % 1024 == 0,
+ *   I % 256 == 0); shared may be NULL. ids [T, k], weights [T, k], y [T, H] out.
+ *   ws: flint_prefill_workspace_bytes(...) bytes, 256-byte aligned,
+ *   initialised once (flint_workspace_init); it holds the logits, the sort and
+ *   the intermediate h and d of every (token, rank) pair.
+ *   flags: 0 (PDL is not used on this path).
+ *   A timed-out wait inside a GEMM is reported by flint_workspace_check.
+ */
+size_t flint_prefill_workspace_bytes(int tokens, int num_experts, int top_k, int hidden, int inter, int inter_shared);
+flint_status_t flint_moe_prefill(const flint_bf16* x, int T, const flint_bf16* router_w, int E, const float* bias,
+                                 int k, const flint_experts* routed, const flint_experts* shared, int32_t* ids,
+                                 float* weights, flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
+                                 void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Dense GEMV on packed weights                                              */
 /* ------------------------------------------------------------------------ */
 

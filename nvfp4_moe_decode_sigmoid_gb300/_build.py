@@ -12,8 +12,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libflint.so")
-SOURCES = ["abi.cu", "repack.cu", "route.cu", "gemv.cu", "layer.cu", "bf16.cu", "norm.cu"]
-HEADERS = ["flint_device.cuh", "flint_internal.h", "expert_common.cuh", "router_common.cuh"]
+SOURCES = ["abi.cu", "repack.cu", "route.cu", "gemv.cu", "layer.cu", "bf16.cu", "norm.cu", "prefill.cu"]
+HEADERS = ["flint_device.cuh", "flint_internal.h", "expert_common.cuh", "router_common.cuh", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "--expt-relaxed-constexpr",

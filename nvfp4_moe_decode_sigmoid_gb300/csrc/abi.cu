@@ -274,7 +274,7 @@ flint_status_t flint_workspace_check(void* ws, size_t ws_bytes, void* stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status");
     if (st & (flint::kStatusTimeoutRoute | flint::kStatusTimeoutGateUp | flint::kStatusTimeoutDown |
-              flint::kStatusTimeoutSelftest | flint::kStatusTimeoutLayer))
+              flint::kStatusTimeoutSelftest | flint::kStatusTimeoutLayer | flint::kStatusTimeoutPrefill))
         return fail(FLINT_ERR_TIMEOUT, "device wait timed out (status 0x%x)", st);
     return fail(FLINT_ERR_INVALID_ARG, "an expert id was outside [0, num_experts) (status 0x%x)", st);
 }
@@ -599,6 +599,61 @@ flint_status_t flint_moe_block(const flint_norm* norm, int T, const flint_bf16* 
     if (!norm) return fail(FLINT_ERR_INVALID_ARG, "block: norm is null");
     return moe_layer_impl("block", nullptr, norm, T, router_w, E, bias, k, routed, shared, ids, weights, y, ws,
                           ws_bytes, flags, stream);
+}
+
+size_t flint_prefill_workspace_bytes(int tokens, int num_experts, int top_k, int hidden, int inter, int inter_shared) {
+    if (tokens < 0 || num_experts < 0 || top_k < 0 || hidden < 0 || inter < 0 || inter_shared < 0) return 0;
+    return flint::prefill_ws_layout(tokens, num_experts, top_k, hidden, inter, inter_shared).total;
+}
+
+flint_status_t flint_moe_prefill(const flint_bf16* x, int T, const flint_bf16* router_w, int E, const float* bias,
+                                 int k, const flint_experts* routed, const flint_experts* shared, int32_t* ids,
+                                 float* weights, flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
+                                 void* stream) {
+    (void)flags;
+    if (T < 1) return fail(FLINT_ERR_INVALID_ARG, "prefill: T=%d", T);
+    flint_status_t s = check_experts(routed, "routed", true);
+    if (s != FLINT_OK) return s;
+    if (shared && (s = check_experts(shared, "shared", true)) != FLINT_OK) return s;
+    if (routed->dtype != FLINT_DTYPE_NVFP4 || (shared && shared->dtype != FLINT_DTYPE_NVFP4))
+        return fail(FLINT_ERR_UNSUPPORTED, "prefill: NVFP4 experts only");
+    if (shared && (shared->num_experts != 1 || shared->hidden != routed->hidden))
+        return fail(FLINT_ERR_INVALID_ARG, "prefill: shared expert must have num_experts 1 and the routed hidden size");
+    if (E != routed->num_experts)
+        return fail(FLINT_ERR_INVALID_ARG, "prefill: router has %d rows, routed experts %d", E, routed->num_experts);
+    if (E % 16 || E > FLINT_MAX_EXPERTS)
+        return fail(FLINT_ERR_UNSUPPORTED, "prefill: E=%d must be a multiple of 16 up to %d", E, FLINT_MAX_EXPERTS);
+    if (k < 1 || k > FLINT_MAX_TOPK || k > E) return fail(FLINT_ERR_UNSUPPORTED, "prefill: k=%d", k);
+    if ((long long)T * k >= (1ll << 30)) return fail(FLINT_ERR_UNSUPPORTED, "prefill: T*k too large");
+    if (!x || !router_w || !ids || !weights || !y || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) ||
+        !aligned(weights, 4) || !aligned(y, 16) || (bias && !aligned(bias, 4)))
+        return fail(FLINT_ERR_INVALID_ARG, "prefill: null or misaligned pointer");
+    const int H = routed->hidden, I = routed->inter, Is = shared ? shared->inter : 0;
+    if ((s = check_ws(ws, ws_bytes, flint::prefill_ws_layout(T, E, k, H, I, Is).total)) != FLINT_OK) return s;
+    DevInfo d;
+    if ((s = device_info(d)) != FLINT_OK) return s;
+    flint::PrefillArgs p = {};
+    p.x = x;
+    p.T = T;
+    p.H = H;
+    p.router_w = router_w;
+    p.E = E;
+    p.bias = bias;
+    p.k = k;
+    p.gu = static_cast<const uint8_t*>(routed->gate_up);
+    p.down = static_cast<const uint8_t*>(routed->down);
+    p.I = I;
+    p.ts = routed->tensor_scale;
+    p.s_gu = shared ? static_cast<const uint8_t*>(shared->gate_up) : nullptr;
+    p.s_down = shared ? static_cast<const uint8_t*>(shared->down) : nullptr;
+    p.Is = Is;
+    p.s_ts = shared ? shared->tensor_scale : nullptr;
+    p.ids = ids;
+    p.weights = weights;
+    p.y = y;
+    p.ws = ws;
+    cudaError_t e = flint::launch_prefill(p, d, as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "prefill launch");
 }
 
 flint_status_t flint_dense_gemv(const flint_bf16* x, int T, const flint_packed* W, int epilogue, flint_bf16* y,

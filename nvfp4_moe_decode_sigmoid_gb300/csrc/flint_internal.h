@@ -29,6 +29,7 @@ enum : uint32_t {
     kStatusTimeoutSelftest = 1u << 3,
     kStatusBadExpertId = 1u << 4,
     kStatusTimeoutLayer = 1u << 5,
+    kStatusTimeoutPrefill = 1u << 6,
 };
 
 constexpr int kThreads = 256;       // router kernel: 8 warps
@@ -173,6 +174,58 @@ struct LayerArgs {
     NormArgs norm;       // norm.r set: x = the norm of the residual stream (x unused)
 };
 
+// One grouped GEMM of the prefill: C[rows of each group] = A B^T on 128 x 128
+// tiles. Groups (experts) are row segments [seg_base[g], + seg_len[g]) of the
+// output; tile_start[g] is the exclusive prefix of their 128-row tile counts
+// (n_groups + 1 entries). Without tile_start there is one group of `rows`.
+struct PrefillGemmArgs {
+    const uint16_t* A;     // bf16 rows, lda elements apart
+    long long lda;
+    const int* a_index;    // A row of output row p: a_index[p] / a_index_div (null: p)
+    int a_index_div;
+    const int* tile_start;
+    const int* seg_base;
+    const int* seg_len;
+    int n_groups, rows, K;
+    const uint8_t* B;      // group g's matrix at B + g * b_group_stride; rows ldb bytes apart
+    long long ldb, b_group_stride;
+    int b_up_row0;         // SwiGLU: first up row (the gate rows start at 0)
+    int n_valid;           // valid B rows (0: all); rows past it read as zero, their columns are not stored
+    const float* ts;       // tensor scales of group g at ts + g * ts_stride (gate, up, down), or null
+    int ts_stride;
+    float* out_f32;        // logits
+    uint16_t* out_bf16;    // h or d
+    long long ldo;         // output row stride (elements)
+    uint32_t* status;
+};
+
+// The MoE layer over T tokens (prefill).
+struct PrefillArgs {
+    const uint16_t* x;      // [T][H]
+    int T, H;
+    const uint16_t* router_w;  // [E][H]
+    int E;
+    const float* bias;
+    int k;
+    const uint8_t* gu;      // routed E x [2I, H] NVFP4
+    const uint8_t* down;    // routed E x [H, I]
+    int I;
+    const float* ts;        // [E][3]
+    const uint8_t* s_gu;    // shared [2Is, H] or null
+    const uint8_t* s_down;
+    int Is;
+    const float* s_ts;
+    int32_t* ids;           // [T][k] out
+    float* weights;         // [T][k] out
+    uint16_t* y;            // [T][H] out
+    void* ws;
+};
+
+struct PrefillWs {
+    size_t logits, counts, seg_base, seg_len, tile_start, perm, inv, h, hs, d, ds, total;
+};
+PrefillWs prefill_ws_layout(int T, int E, int k, int H, int I, int Is);
+
 // ---------------------------------------------------------------------------
 // Launchers (return the CUDA error of the launch)
 // ---------------------------------------------------------------------------
@@ -199,6 +252,9 @@ size_t gate_up_bf16_smem_bytes(const GateUpArgs& a);
 size_t down_bf16_smem_bytes(const DownArgs& a);
 // Standalone residual add + RMSNorm (x_out required), one CTA per token.
 cudaError_t launch_rmsnorm(const NormArgs& a, bool pdl, cudaStream_t s);
+// The prefill: router GEMM, top-k, expert sort, grouped gate/up and down
+// GEMMs on tcgen05, combine (eight launches in stream order).
+cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t* status, uint64_t budget_ns, cudaStream_t s);
 // Cooperative launch of the fused layer kernel, one CTA on every SM (with the
 // programmatic-dependent-launch attribute when `pdl`).

@@ -1,0 +1,576 @@
+// prefill.cu -- the MoE layer over a long batch of tokens (prefill) on the
+// 5th-generation tensor cores.
+//
+// "Day-0 Support for Flint on vLLM", section "Optimizations": the small-batch
+// MoE rewrite (router and expert GEMVs that read only the selected experts'
+// weights) was also the largest gain of the 8K-token prefill; section "Model
+// architecture": weight-only NVFP4 experts with bf16 activations, sigmoid
+// top-6 over 256 experts plus a shared expert. The arithmetic is the decode
+// path's (the same rounding points), on many tokens at once:
+//   1. router logits = x Wr^T (FP32), a tensor-core GEMM;
+//   2. per token: sigmoid, top-k, renormalised weights (one warp per token);
+//   3. the (token, rank) pairs sorted by expert, token order kept within an
+//      expert (counting sort, deterministic);
+//   4. per expert: h = bf16(silu(bf16(ts_g x Wg^T)) bf16(ts_u x Wu^T)) over its
+//      gathered token rows, a grouped GEMM whose NVFP4 B tiles are dequantised
+//      to bf16 in shared memory (exact: a code times its block scale has at
+//      most 6 significant bits); the shared expert over all tokens;
+//   5. per expert: d = bf16(ts_d h Wd^T), grouped the same way;
+//   6. y = bf16(sum_j w_j d_j + d_shared) per token, ranks in order (a gather,
+//      no atomics: deterministic).
+//
+// GEMM tiles are 128 rows x 128 columns, K in steps of 64, accumulated in
+// TMEM by tcgen05.mma (kind::f16, bf16 operands, FP32 accumulator) issued by
+// one thread; the operands stream through a 4-stage ring of shared-memory
+// stages filled with cp.async (A rows, and the raw NVFP4 rows of B, which
+// all threads then dequantise into the stage's B tile).
+#include "router_common.cuh"
+#include "tcgen05.cuh"
+
+namespace flint {
+namespace {
+
+constexpr int kPT = 128;      // threads of a GEMM CTA (4 warps: the 128 TMEM lanes)
+constexpr int kPS = 4;        // pipeline stages
+constexpr int kTileM = 128, kTileN = 128, kStepK = 64;
+constexpr uint32_t kTileBytes = kTileM * kStepK * 2;  // 16 KB
+constexpr uint32_t kRawCodes = kTileN * 32, kRawScales = kTileN * 4;
+
+struct PrefillSmem {
+    static constexpr size_t a = 0;                                   // kPS A tiles
+    static constexpr size_t b = a + (size_t)kPS * kTileBytes;        // kPS B tiles
+    static constexpr size_t rc = b + (size_t)kPS * kTileBytes;       // kPS raw code rows
+    static constexpr size_t rs = rc + (size_t)kPS * kRawCodes;       // kPS raw scale rows
+    static constexpr size_t bar = rs + (size_t)kPS * kRawScales;     // kPS + 1 mbarriers
+    static constexpr size_t tslot = bar + 8 * (kPS + 1);
+    static constexpr size_t total = tslot + 16;
+};
+
+__device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gmem_src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+// 8 codes (one 32-bit word: byte b holds columns 2b, 2b + 1) times their
+// block scale (f16x2, both halves equal) -> 8 bf16 (exact).
+__device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2) {
+    uint32_t h[4];
+    decode_word_h2(w, h);
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&h[i]), *reinterpret_cast<const __half2*>(&s2));
+        const float2 f = __half22float2(p);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+        o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
+
+// The group (expert) of M-tile `mt` and its first row: tile_start is the
+// exclusive prefix of the groups' tile counts (n_groups + 1 entries).
+__device__ __forceinline__ int find_group(const int* tile_start, int n_groups, int mt) {
+    int lo = 0, hi = n_groups - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_start[mid] <= mt) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+enum { kEpiLogits = 0, kEpiSwiglu = 1, kEpiScale = 2 };
+
+// One 128 x 128 output tile of a grouped GEMM (blockIdx.x: M-tile over all
+// groups, blockIdx.y: N-tile). NVFP4: B rows are packed NVFP4 (dequantised in
+// shared memory); otherwise bf16.
+template <bool NVFP4, int EPI>
+__global__ void __launch_bounds__(kPT, 1) prefill_gemm_kernel(const PrefillGemmArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    using L = PrefillSmem;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // ---- which tile ----
+    int g = 0, row0, nrows;
+    const int mt = blockIdx.x;
+    if (a.tile_start) {
+        if (mt >= ld_cg(a.tile_start + a.n_groups)) return;
+        g = find_group(a.tile_start, a.n_groups, mt);
+        const int seg_len = ld_cg(a.seg_len + g);
+        row0 = ld_cg(a.seg_base + g) + (mt - ld_cg(a.tile_start + g)) * kTileM;
+        nrows = min(kTileM, ld_cg(a.seg_base + g) + seg_len - row0);
+    } else {
+        row0 = mt * kTileM;
+        if (row0 >= a.rows) return;
+        nrows = min(kTileM, a.rows - row0);
+    }
+    const int nt = blockIdx.y;
+    const int K = a.K, nk = K / kStepK;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::bar);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::tslot);
+
+    // ---- operand rows of this thread's copies ----
+    // A: chunk q = it * 128 + tid (it < 8) of a stage is row (q >> 6) * 8 + (q & 7), K chunk (q >> 3) & 7.
+    const uint16_t* arow[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int q = it * kPT + tid, r = ((q >> 6) << 3) + (q & 7);
+        arow[it] = nullptr;
+        if (r < nrows) {
+            const int p = row0 + r;
+            const int src = a.a_index ? ld_cg(a.a_index + p) / a.a_index_div : p;
+            arow[it] = a.A + (size_t)src * a.lda + ((q >> 3) & 7) * 8;
+        }
+    }
+    // B row of tile row r: gate/up pairs (rows [0, 64) gate n, [64, 128) up n) or plain rows.
+    auto brow = [&](int r) -> size_t {
+        if (EPI == kEpiSwiglu) return (size_t)(r < 64 ? nt * 64 + r : a.b_up_row0 + nt * 64 + (r - 64));
+        return (size_t)(nt * kTileN + r);
+    };
+    const uint8_t* Bg = a.B + (size_t)g * a.b_group_stride;
+    auto load_stage = [&](int s, int j) {
+        const int k0 = j * kStepK;
+        uint8_t* at = smem + L::a + (size_t)s * kTileBytes;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int q = it * kPT + tid;
+            cp_async16_zfill(at + 16 * q, arow[it] ? arow[it] + k0 : a.A, arow[it] != nullptr);
+        }
+        if constexpr (NVFP4) {
+            uint8_t* rc = smem + L::rc + (size_t)s * kRawCodes;
+            uint8_t* rs = smem + L::rs + (size_t)s * kRawScales;
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int q = it * kPT + tid, r = q >> 1, half = q & 1;
+                cp_async16(rc + 32 * r + 16 * half, Bg + brow(r) * a.ldb + k0 / 2 + 16 * half);
+            }
+            cp_async4(rs + 4 * tid, Bg + brow(tid) * a.ldb + K / 2 + k0 / 16);
+        } else {
+            uint8_t* bt = smem + L::b + (size_t)s * kTileBytes;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int q = it * kPT + tid, r = ((q >> 6) << 3) + (q & 7);
+                const bool v = a.n_valid == 0 || nt * kTileN + r < a.n_valid;
+                cp_async16_zfill(bt + 16 * q, v ? Bg + brow(r) * a.ldb + 2 * (k0 + ((q >> 3) & 7) * 8) : a.B, v);
+            }
+        }
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s <= kPS; ++s) mbar_init(bar + s, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, kTileN);
+        tmem_relinquish();
+    }
+    for (int s = 0; s < kPS - 1; ++s) {
+        if (s < nk) load_stage(s, s);
+        cp_async_commit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t idesc = tc_idesc_bf16(kTileM, kTileN);
+    bool ok = true;
+    for (int i = 0; i < nk && ok; ++i) {
+        const int s = i % kPS;
+        cp_async_wait<kPS - 2>();
+        __syncthreads();  // stage s landed for every thread
+        if constexpr (NVFP4) {
+            const uint8_t* rc = smem + L::rc + (size_t)s * kRawCodes;
+            const uint8_t* rs = smem + L::rs + (size_t)s * kRawScales;
+            uint8_t* bt = smem + L::b + (size_t)s * kTileBytes;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int q = it * kPT + tid, r = ((q >> 6) << 3) + (q & 7), kc = (q >> 3) & 7;
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(rc + 32 * r + 4 * kc);
+                const uint32_t sb = rs[4 * r + (kc >> 1)] & 0x7Fu;
+                uint32_t s2;
+                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"((uint16_t)(sb | (sb << 8))));
+                *reinterpret_cast<uint4*>(bt + 16 * q) = dequant8(w, s2);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();  // the stage's tiles complete in shared memory
+        if (tid == 0) {
+            tc_fence_after_sync();
+            const uint8_t* at = smem + L::a + (size_t)s * kTileBytes;
+            const uint8_t* bt = smem + L::b + (size_t)s * kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kStepK / 16; ++kk)
+                tc_mma_bf16(tmem, tc_smem_desc(at + 256 * kk, kTcCoreK, kTcCoreRow),
+                            tc_smem_desc(bt + 256 * kk, kTcCoreK, kTcCoreRow), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar + s);
+        }
+        // refill the stage of step i - 1 with step i + kPS - 1 once its MMAs are done
+        const int j = i + kPS - 1;
+        if (j < nk) {
+            if (i >= 1) ok = mbar_wait_bounded(bar + (i - 1) % kPS, ((i - 1) / kPS) & 1, a.status, kStatusTimeoutPrefill);
+            if (ok) load_stage(j % kPS, j);
+        }
+        cp_async_commit();
+        ok = __syncthreads_and(ok);
+    }
+    // the last step's MMAs (and so all of them) complete
+    if (ok) ok = mbar_wait_bounded(bar + (nk - 1) % kPS, ((nk - 1) / kPS) & 1, a.status, kStatusTimeoutPrefill);
+    ok = __syncthreads_and(ok);
+    cp_async_wait<0>();
+    tc_fence_after_sync();
+    if (ok) {
+        const int r = 32 * warp + lane;  // the TMEM lane = tile row of this thread
+        const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+        const bool valid = r < nrows;
+        const int p = row0 + r;
+        if (EPI == kEpiSwiglu) {
+            const float tsg = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride) : 1.f;
+            const float tsu = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride + 1) : 1.f;
+            for (int c = 0; c < 64; c += 16) {
+                uint32_t gv[16], uv[16];
+                tmem_ld16(tl + c, gv);
+                tmem_ld16(tl + 64 + c, uv);
+                tmem_ld_wait();
+                uint32_t o[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float h2[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float gg = bf16_round_f32(tsg * __uint_as_float(gv[2 * i + h]));
+                        const float uu = bf16_round_f32(tsu * __uint_as_float(uv[2 * i + h]));
+                        h2[h] = silu_f(gg) * uu;
+                    }
+                    o[i] = (uint32_t)f32_to_bf16_bits(h2[0]) | ((uint32_t)f32_to_bf16_bits(h2[1]) << 16);
+                }
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + (size_t)p * a.ldo + nt * 64 + c);
+                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+        } else {
+            const float ts = (EPI == kEpiScale && a.ts) ? ld_cg(a.ts + (size_t)g * a.ts_stride + 2) : 1.f;
+            for (int c = 0; c < kTileN; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tl + c, v);
+                tmem_ld_wait();
+                if (!valid) continue;
+                if (EPI == kEpiLogits) {
+                    if (a.n_valid && nt * kTileN + c >= a.n_valid) continue;  // n_valid % 16 == 0
+                    float4* dst = reinterpret_cast<float4*>(a.out_f32 + (size_t)p * a.ldo + nt * kTileN + c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                             __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                } else {
+                    uint32_t o[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        o[i] = (uint32_t)f32_to_bf16_bits(ts * __uint_as_float(v[2 * i])) |
+                               ((uint32_t)f32_to_bf16_bits(ts * __uint_as_float(v[2 * i + 1])) << 16);
+                    uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + (size_t)p * a.ldo + nt * kTileN + c);
+                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTileN);
+}
+
+// ---------------------------------------------------------------------------
+// Routing: sigmoid top-k per token (one warp per token, 8 tokens per CTA).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) prefill_topk_kernel(const float* logits, const float* bias, int T, int E,
+                                                           int k, int32_t* ids, float* weights) {
+    extern __shared__ __align__(16) uint32_t sc[];  // [8][E]
+    const int t0 = blockIdx.x * 8, nt = min(8, T - t0);
+    sigmoid_scores(logits + (size_t)t0 * E, bias, nt, E, sc);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < nt) {
+        const int t = t0 + warp;
+        if (E <= 256)
+            topk_warp<8>(sc + (size_t)warp * E, E, k, lane, ids + (size_t)t * k, weights + (size_t)t * k);
+        else
+            topk_warp<FLINT_MAX_EXPERTS / 32>(sc + (size_t)warp * E, E, k, lane, ids + (size_t)t * k,
+                                              weights + (size_t)t * k);
+    }
+}
+
+// Counting sort of the (token, rank) pairs q = t k + j by expert, in q order.
+// count: CTA e counts its pairs. place: CTA e finds its segment start and
+// tile start from the counts of the experts before it, then writes its pairs
+// in order (a block-wide scan per chunk of pairs).
+__global__ void __launch_bounds__(512) prefill_count_kernel(const int32_t* ids, int n, int* counts) {
+    const int e = blockIdx.x;
+    int c = 0;
+    for (int q = threadIdx.x; q < n; q += blockDim.x) c += ids[q] == e;
+    c = __reduce_add_sync(0xffffffffu, c);
+    __shared__ int part[16];
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int s = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += part[w];
+        counts[e] = s;
+    }
+}
+
+__global__ void __launch_bounds__(512) prefill_place_kernel(const int32_t* ids, int n, int E, const int* counts,
+                                                            int* perm, int* inv, int* seg_base, int* seg_len,
+                                                            int* tile_start) {
+    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ int base_s, wsum[16];
+    if (warp == 0) {
+        int b = 0, tb = 0;
+        for (int i = lane; i < E; i += 32) {
+            const int ci = counts[i];
+            if (i < e) {
+                b += ci;
+                tb += (ci + kTileM - 1) / kTileM;
+            }
+        }
+        b = __reduce_add_sync(0xffffffffu, b);
+        tb = __reduce_add_sync(0xffffffffu, tb);
+        if (lane == 0) {
+            base_s = b;
+            seg_base[e] = b;
+            seg_len[e] = counts[e];
+            tile_start[e] = tb;
+            if (e == E - 1) tile_start[E] = tb + (counts[e] + kTileM - 1) / kTileM;
+        }
+    }
+    __syncthreads();
+    int run = base_s;
+    for (int q0 = 0; q0 < n; q0 += blockDim.x) {
+        const int q = q0 + tid;
+        const bool m = q < n && ids[q] == e;
+        const uint32_t bal = __ballot_sync(0xffffffffu, m);
+        if (lane == 0) wsum[warp] = __popc(bal);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            if (w < warp) before += wsum[w];
+            total += wsum[w];
+        }
+        if (m) {
+            const int pos = run + before + __popc(bal & ((1u << lane) - 1u));
+            perm[pos] = q;
+            inv[q] = pos;
+        }
+        run += total;
+        __syncthreads();
+    }
+}
+
+// y[t] = bf16(sum_j w[t][j] d[inv[t k + j]] + d_shared[t]), ranks in order.
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const float* weights, const int* inv, int k,
+                                                              const uint16_t* d, const uint16_t* ds, int H,
+                                                              uint16_t* y) {
+    const int t = blockIdx.x;
+    float w[FLINT_MAX_TOPK];
+    int pj[FLINT_MAX_TOPK];
+    for (int j = 0; j < k; ++j) {
+        w[j] = weights[(size_t)t * k + j];
+        pj[j] = inv[(size_t)t * k + j];
+    }
+    for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < k; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(d + (size_t)pj[j] * H + c);
+            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(w[j], bf16_lo(vw[i]), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(w[j], bf16_hi(vw[i]), acc[2 * i + 1]);
+            }
+        }
+        if (ds) {
+            const uint4 v = *reinterpret_cast<const uint4*>(ds + (size_t)t * H + c);
+            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += bf16_lo(vw[i]);
+                acc[2 * i + 1] += bf16_hi(vw[i]);
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = (uint32_t)f32_to_bf16_bits(acc[2 * i]) | ((uint32_t)f32_to_bf16_bits(acc[2 * i + 1]) << 16);
+        *reinterpret_cast<uint4*>(y + (size_t)t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+template <typename Kern>
+cudaError_t launch_plain(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const PrefillGemmArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+template <bool NVFP4, int EPI>
+cudaError_t launch_gemm(const PrefillGemmArgs& a, const DevInfo& d, int m_tiles, int n_tiles, cudaStream_t s) {
+    static int configured_for = -1;
+    cudaError_t e = configure_smem(prefill_gemm_kernel<NVFP4, EPI>, d, configured_for);
+    if (e != cudaSuccess) return e;
+    if (m_tiles <= 0 || n_tiles <= 0) return cudaSuccess;
+    return launch_plain(prefill_gemm_kernel<NVFP4, EPI>, dim3((unsigned)m_tiles, (unsigned)n_tiles), dim3(kPT),
+                        PrefillSmem::total, s, a);
+}
+
+}  // namespace
+
+PrefillWs prefill_ws_layout(int T, int E, int k, int H, int I, int Is) {
+    PrefillWs w;
+    size_t o = kWsHeader;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    w.logits = take(sizeof(float) * (size_t)T * E);
+    w.counts = take(sizeof(int) * (size_t)E);
+    w.seg_base = take(sizeof(int) * (size_t)E);
+    w.seg_len = take(sizeof(int) * (size_t)E);
+    w.tile_start = take(sizeof(int) * (size_t)(E + 1));
+    w.perm = take(sizeof(int) * (size_t)T * k);
+    w.inv = take(sizeof(int) * (size_t)T * k);
+    w.h = take(2 * (size_t)T * k * I);
+    w.hs = take(2 * (size_t)T * Is);
+    w.d = take(2 * (size_t)T * k * H);
+    w.ds = take(2 * (size_t)T * H);
+    w.total = o;
+    return w;
+}
+
+cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t s) {
+    const PrefillWs W = prefill_ws_layout(p.T, p.E, p.k, p.H, p.I, p.Is);
+    uint8_t* ws = static_cast<uint8_t*>(p.ws);
+    float* logits = reinterpret_cast<float*>(ws + W.logits);
+    int* counts = reinterpret_cast<int*>(ws + W.counts);
+    int* seg_base = reinterpret_cast<int*>(ws + W.seg_base);
+    int* seg_len = reinterpret_cast<int*>(ws + W.seg_len);
+    int* tile_start = reinterpret_cast<int*>(ws + W.tile_start);
+    int* perm = reinterpret_cast<int*>(ws + W.perm);
+    int* inv = reinterpret_cast<int*>(ws + W.inv);
+    uint16_t* h = reinterpret_cast<uint16_t*>(ws + W.h);
+    uint16_t* hs = reinterpret_cast<uint16_t*>(ws + W.hs);
+    uint16_t* dd = reinterpret_cast<uint16_t*>(ws + W.d);
+    uint16_t* ds = reinterpret_cast<uint16_t*>(ws + W.ds);
+    uint32_t* status = reinterpret_cast<uint32_t*>(ws) + 1;
+    const int T = p.T, E = p.E, k = p.k, H = p.H, I = p.I, Is = p.Is;
+    const int mt_all = (T + kTileM - 1) / kTileM;
+    const int mt_routed = (T * k + kTileM - 1) / kTileM + E;  // bound on the grouped M-tiles
+    const long long rs_h = nvfp4_row_stride(H), rs_i = nvfp4_row_stride(I), rs_is = Is ? nvfp4_row_stride(Is) : 0;
+    cudaError_t e;
+
+    // 1. router logits (FP32) = x Wr^T
+    PrefillGemmArgs r = {};
+    r.A = p.x;
+    r.lda = H;
+    r.rows = T;
+    r.K = H;
+    r.B = reinterpret_cast<const uint8_t*>(p.router_w);
+    r.ldb = 2 * (long long)H;
+    r.n_valid = E;
+    r.out_f32 = logits;
+    r.ldo = E;
+    r.status = status;
+    if ((e = launch_gemm<false, kEpiLogits>(r, d, mt_all, (E + kTileN - 1) / kTileN, s)) != cudaSuccess) return e;
+    // 2. top-k per token
+    prefill_topk_kernel<<<(T + 7) / 8, 256, sizeof(uint32_t) * 8 * E, s>>>(logits, p.bias, T, E, k, p.ids, p.weights);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 3. pairs sorted by expert
+    prefill_count_kernel<<<E, 512, 0, s>>>(p.ids, T * k, counts);
+    prefill_place_kernel<<<E, 512, 0, s>>>(p.ids, T * k, E, counts, perm, inv, seg_base, seg_len, tile_start);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 4. gate/up + SiLU: routed experts over their gathered tokens, the shared expert over all
+    PrefillGemmArgs g = {};
+    g.A = p.x;
+    g.lda = H;
+    g.a_index = perm;
+    g.a_index_div = k;
+    g.tile_start = tile_start;
+    g.seg_base = seg_base;
+    g.seg_len = seg_len;
+    g.n_groups = E;
+    g.K = H;
+    g.B = p.gu;
+    g.ldb = rs_h;
+    g.b_group_stride = 2 * (long long)I * rs_h;
+    g.b_up_row0 = I;
+    g.ts = p.ts;
+    g.ts_stride = 3;
+    g.out_bf16 = h;
+    g.ldo = I;
+    g.status = status;
+    if ((e = launch_gemm<true, kEpiSwiglu>(g, d, mt_routed, I / 64, s)) != cudaSuccess) return e;
+    if (p.s_gu) {
+        PrefillGemmArgs gs = {};
+        gs.A = p.x;
+        gs.lda = H;
+        gs.rows = T;
+        gs.K = H;
+        gs.B = p.s_gu;
+        gs.ldb = rs_h;
+        gs.b_up_row0 = Is;
+        gs.ts = p.s_ts;
+        gs.out_bf16 = hs;
+        gs.ldo = Is;
+        gs.status = status;
+        if ((e = launch_gemm<true, kEpiSwiglu>(gs, d, mt_all, Is / 64, s)) != cudaSuccess) return e;
+    }
+    // 5. down
+    PrefillGemmArgs dn = {};
+    dn.A = h;
+    dn.lda = I;
+    dn.tile_start = tile_start;
+    dn.seg_base = seg_base;
+    dn.seg_len = seg_len;
+    dn.n_groups = E;
+    dn.K = I;
+    dn.B = p.down;
+    dn.ldb = rs_i;
+    dn.b_group_stride = (long long)H * rs_i;
+    dn.ts = p.ts;
+    dn.ts_stride = 3;
+    dn.out_bf16 = dd;
+    dn.ldo = H;
+    dn.status = status;
+    if ((e = launch_gemm<true, kEpiScale>(dn, d, mt_routed, H / kTileN, s)) != cudaSuccess) return e;
+    if (p.s_down) {
+        PrefillGemmArgs dsa = {};
+        dsa.A = hs;
+        dsa.lda = Is;
+        dsa.rows = T;
+        dsa.K = Is;
+        dsa.B = p.s_down;
+        dsa.ldb = rs_is;
+        dsa.ts = p.s_ts;
+        dsa.out_bf16 = ds;
+        dsa.ldo = H;
+        dsa.status = status;
+        if ((e = launch_gemm<true, kEpiScale>(dsa, d, mt_all, H / kTileN, s)) != cudaSuccess) return e;
+    }
+    // 6. combine
+    prefill_combine_kernel<<<T, 256, 0, s>>>(p.weights, inv, k, dd, p.s_down ? ds : nullptr, H, p.y);
+    return cudaGetLastError();
+}
+
+}  // namespace flint

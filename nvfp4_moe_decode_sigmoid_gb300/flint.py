@@ -85,6 +85,9 @@ def _load():
         "flint_moe_layer": (i32, [vp, i32, vp, i32, vp, i32, C.POINTER(flint_experts), C.POINTER(flint_experts), vp,
                                   vp, vp, vp, sz, u32, vp]),
         "flint_residual_rmsnorm": (i32, [C.POINTER(flint_norm), i32, i32, u32, vp]),
+        "flint_prefill_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
+        "flint_moe_prefill": (i32, [vp, i32, vp, i32, vp, i32, C.POINTER(flint_experts), C.POINTER(flint_experts),
+                                    vp, vp, vp, vp, sz, u32, vp]),
         "flint_moe_block": (i32, [C.POINTER(flint_norm), i32, vp, i32, vp, i32, C.POINTER(flint_experts),
                                   C.POINTER(flint_experts), vp, vp, vp, vp, sz, u32, vp]),
     }
@@ -313,6 +316,22 @@ def flint_moe_block(residual, router_w, k, routed: Experts, shared: Experts | No
     _check(_lib.flint_moe_block(C.byref(n), T, _ptr(router_w), E, _ptr(bias), k, _ex(routed), _ex(shared),
                                 _ptr(ids), _ptr(weights), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(), flags,
                                 _stream(stream)), "moe_block")
+
+
+def flint_prefill_workspace_bytes(tokens: int, num_experts: int, top_k: int, hidden: int, inter: int,
+                                  inter_shared: int) -> int:
+    return _lib.flint_prefill_workspace_bytes(tokens, num_experts, top_k, hidden, inter, inter_shared)
+
+
+def flint_moe_prefill(x, router_w, k, routed: Experts, shared: Experts | None, ids, weights, y, ws, bias=None,
+                      stream=None):
+    """The MoE layer over T tokens on the tensor cores (router GEMM, top-k,
+    expert sort, grouped gate/up and down GEMMs, combine)."""
+    T = x.shape[0]
+    E = router_w.shape[0]
+    _check(_lib.flint_moe_prefill(_ptr(x), T, _ptr(router_w), E, _ptr(bias), k, _ex(routed), _ex(shared), _ptr(ids),
+                                  _ptr(weights), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(), 0,
+                                  _stream(stream)), "moe_prefill")
 
 
 def flint_dense_gemv(x, W: Packed, y, epilogue=FLINT_EPILOGUE_NONE, ws=None, flags=0, stream=None):
