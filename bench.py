@@ -54,6 +54,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-bf16", action="store_true", help="skip the BF16-expert variant")
     p.add_argument("--no-stack", action="store_true", help="skip the 49-block decode stack")
+    p.add_argument("--no-prefill", action="store_true", help="skip the 8192-token prefill")
     return p.parse_args()
 
 
@@ -419,6 +420,56 @@ def measure_stack(F, args, reps=20):
     return out
 
 
+PREFILL_T = 8192
+
+
+def measure_prefill(F, reps=10):
+    """The MoE layer over 8192 tokens (flint_moe_prefill: router GEMM, top-k,
+    expert sort, grouped gate/up and down GEMMs on tcgen05, combine) on one
+    full-size seeded layer; FLOPs = 2 x (router + 7 experts per token)."""
+    import torch
+    from nvfp4_moe_decode_sigmoid_gb300 import synth
+    L = synth.Layer(1000, H=H, E=E, I=I, I_shared=I_SHARED, device="cuda")
+    s = L.shared
+    routed = F.Experts.from_gguf(L.gate, L.up, L.down, L.ts, E, H, I)
+    shared = F.Experts.from_gguf(s["gate"], s["up"], s["down"], s["ts"].reshape(1, 3), 1, H, I_SHARED)
+    T = PREFILL_T
+    x = synth.activations(4242, T, H, "cuda")
+    ws = torch.empty(F.flint_prefill_workspace_bytes(T, E, TOPK, H, I, I_SHARED), dtype=torch.uint8, device="cuda")
+    F.flint_workspace_init(ws)
+    ids = torch.empty((T, TOPK), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, TOPK), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            F.flint_moe_prefill(x, L.router_w, TOPK, routed, shared, ids, w, y, ws)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            F.flint_moe_prefill(x, L.router_w, TOPK, routed, shared, ids, w, y, ws)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    assert F.flint_workspace_check(ws) == F.FLINT_OK
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    flop = 2 * T * H * E + T * (TOPK + 1) * 2 * 3 * I * H
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        peak = 1900.0
+    tf = flop / (us * 1e-6) / 1e12
+    del L, s, routed, shared, ws
+    torch.cuda.empty_cache()
+    return dict(tokens=T, us=round(us, 1), tflops=round(tf, 1), flop=flop,
+                roofline={"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                          "frac": round(tf / peak, 4), "peak_note": "measured bf16 burst (cuBLAS)"},
+                path="flint_moe_prefill: router GEMM, top-k, expert sort, grouped gate/up + down GEMMs "
+                     "(tcgen05.mma kind::f16, NVFP4 dequantised to bf16 in shared memory), combine")
+
+
 def measure_kernels(F, model, name, reps=8):
     """Average device duration of each kernel: the fused layer kernel and the
     three kernels of the chain. For each, a CUDA graph of back-to-back
@@ -610,11 +661,14 @@ def run_flint(args):
     achieved = kern["layer_bytes"] / (kern["layer_us"] * 1e-6) / 1e9
     traffic = traffic_for(kernel_source_hash())
     e2e = measure_e2e(F, model, args.workload, min(args.steps, 8192), args.graph_steps)
-    stack = {}
-    if not args.no_stack:
+    stack, prefill = {}, {}
+    if not args.no_stack or not args.no_prefill:
         del model
         torch.cuda.empty_cache()
+    if not args.no_stack:
         stack = measure_stack(F, args)
+    if not args.no_prefill:
+        prefill = measure_prefill(F)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload)
@@ -662,6 +716,7 @@ def run_flint(args):
             "extra_workloads": extra,
             "bf16_experts": bf16,
             "decode_stack": stack,
+            "prefill": prefill,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

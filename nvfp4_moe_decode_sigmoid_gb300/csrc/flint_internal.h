@@ -222,7 +222,7 @@ struct PrefillArgs {
 };
 
 struct PrefillWs {
-    size_t logits, counts, seg_base, seg_len, tile_start, perm, inv, h, hs, d, ds, total;
+    size_t logits, chunk_hist, chunk_off, seg_base, seg_len, tile_start, perm, inv, h, hs, d, ds, total;
 };
 PrefillWs prefill_ws_layout(int T, int E, int k, int H, int I, int Is);
 

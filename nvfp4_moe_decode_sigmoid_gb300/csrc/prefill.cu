@@ -30,8 +30,9 @@
 namespace flint {
 namespace {
 
-constexpr int kPT = 128;      // threads of a GEMM CTA (4 warps: the 128 TMEM lanes)
-constexpr int kPS = 4;        // pipeline stages
+constexpr int kPT = 256;      // threads of a GEMM CTA (8 warps; warp w reads TMEM lanes 32 (w % 4))
+constexpr int kPS = 3;        // pipeline stages (two CTAs fit on an SM)
+constexpr int kChunks = 1024 / kPT;  // 16-byte chunks of one 128 x 64 bf16 tile per thread
 constexpr int kTileM = 128, kTileN = 128, kStepK = 64;
 constexpr uint32_t kTileBytes = kTileM * kStepK * 2;  // 16 KB
 constexpr uint32_t kRawCodes = kTileN * 32, kRawScales = kTileN * 4;
@@ -91,7 +92,7 @@ enum { kEpiLogits = 0, kEpiSwiglu = 1, kEpiScale = 2 };
 // groups, blockIdx.y: N-tile). NVFP4: B rows are packed NVFP4 (dequantised in
 // shared memory); otherwise bf16.
 template <bool NVFP4, int EPI>
-__global__ void __launch_bounds__(kPT, 1) prefill_gemm_kernel(const PrefillGemmArgs a) {
+__global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const PrefillGemmArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     using L = PrefillSmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -115,10 +116,10 @@ __global__ void __launch_bounds__(kPT, 1) prefill_gemm_kernel(const PrefillGemmA
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::tslot);
 
     // ---- operand rows of this thread's copies ----
-    // A: chunk q = it * 128 + tid (it < 8) of a stage is row (q >> 6) * 8 + (q & 7), K chunk (q >> 3) & 7.
-    const uint16_t* arow[8];
+    // A: chunk q = it * kPT + tid of a stage is row (q >> 6) * 8 + (q & 7), K chunk (q >> 3) & 7.
+    const uint16_t* arow[kChunks];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
+    for (int it = 0; it < kChunks; ++it) {
         const int q = it * kPT + tid, r = ((q >> 6) << 3) + (q & 7);
         arow[it] = nullptr;
         if (r < nrows) {
@@ -137,23 +138,22 @@ __global__ void __launch_bounds__(kPT, 1) prefill_gemm_kernel(const PrefillGemmA
         const int k0 = j * kStepK;
         uint8_t* at = smem + L::a + (size_t)s * kTileBytes;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
+        for (int it = 0; it < kChunks; ++it) {
             const int q = it * kPT + tid;
             cp_async16_zfill(at + 16 * q, arow[it] ? arow[it] + k0 : a.A, arow[it] != nullptr);
         }
         if constexpr (NVFP4) {
             uint8_t* rc = smem + L::rc + (size_t)s * kRawCodes;
             uint8_t* rs = smem + L::rs + (size_t)s * kRawScales;
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int q = it * kPT + tid, r = q >> 1, half = q & 1;
+            {
+                const int q = tid, r = q >> 1, half = q & 1;  // 256 chunks: 128 rows x 32 code bytes
                 cp_async16(rc + 32 * r + 16 * half, Bg + brow(r) * a.ldb + k0 / 2 + 16 * half);
             }
-            cp_async4(rs + 4 * tid, Bg + brow(tid) * a.ldb + K / 2 + k0 / 16);
+            if (tid < kTileN) cp_async4(rs + 4 * tid, Bg + brow(tid) * a.ldb + K / 2 + k0 / 16);
         } else {
             uint8_t* bt = smem + L::b + (size_t)s * kTileBytes;
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
+            for (int it = 0; it < kChunks; ++it) {
                 const int q = it * kPT + tid, r = ((q >> 6) << 3) + (q & 7);
                 const bool v = a.n_valid == 0 || nt * kTileN + r < a.n_valid;
                 cp_async16_zfill(bt + 16 * q, v ? Bg + brow(r) * a.ldb + 2 * (k0 + ((q >> 3) & 7) * 8) : a.B, v);
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kPT, 1) prefill_gemm_kernel(const PrefillGemmA
             const uint8_t* rs = smem + L::rs + (size_t)s * kRawScales;
             uint8_t* bt = smem + L::b + (size_t)s * kTileBytes;
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
+            for (int it = 0; it < kChunks; ++it) {
                 const int q = it * kPT + tid, r = ((q >> 6) << 3) + (q & 7), kc = (q >> 3) & 7;
                 const uint32_t w = *reinterpret_cast<const uint32_t*>(rc + 32 * r + 4 * kc);
                 const uint32_t sb = rs[4 * r + (kc >> 1)] & 0x7Fu;
@@ -225,14 +225,15 @@ __global__ void __launch_bounds__(kPT, 1) prefill_gemm_kernel(const PrefillGemmA
     cp_async_wait<0>();
     tc_fence_after_sync();
     if (ok) {
-        const int r = 32 * warp + lane;  // the TMEM lane = tile row of this thread
-        const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+        const int wq = warp & 3, half = warp >> 2;  // lane quarter, column half
+        const int r = 32 * wq + lane;  // the TMEM lane = tile row of this thread
+        const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);
         const bool valid = r < nrows;
         const int p = row0 + r;
         if (EPI == kEpiSwiglu) {
             const float tsg = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride) : 1.f;
             const float tsu = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride + 1) : 1.f;
-            for (int c = 0; c < 64; c += 16) {
+            for (int c = 32 * half; c < 32 * half + 32; c += 16) {
                 uint32_t gv[16], uv[16];
                 tmem_ld16(tl + c, gv);
                 tmem_ld16(tl + 64 + c, uv);
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kPT, 1) prefill_gemm_kernel(const PrefillGemmA
             }
         } else {
             const float ts = (EPI == kEpiScale && a.ts) ? ld_cg(a.ts + (size_t)g * a.ts_stride + 2) : 1.f;
-            for (int c = 0; c < kTileN; c += 16) {
+            for (int c = 64 * half; c < 64 * half + 64; c += 16) {
                 uint32_t v[16];
                 tmem_ld16(tl + c, v);
                 tmem_ld_wait();
@@ -307,69 +308,87 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(const float* logits, 
     }
 }
 
-// Counting sort of the (token, rank) pairs q = t k + j by expert, in q order.
-// count: CTA e counts its pairs. place: CTA e finds its segment start and
-// tile start from the counts of the experts before it, then writes its pairs
-// in order (a block-wide scan per chunk of pairs).
-__global__ void __launch_bounds__(512) prefill_count_kernel(const int32_t* ids, int n, int* counts) {
-    const int e = blockIdx.x;
-    int c = 0;
-    for (int q = threadIdx.x; q < n; q += blockDim.x) c += ids[q] == e;
-    c = __reduce_add_sync(0xffffffffu, c);
-    __shared__ int part[16];
-    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
+// Counting sort of the (token, rank) pairs q = t k + j by expert, keeping q
+// order within an expert, in chunks of kSortChunk pairs:
+//   hist:    per chunk, how many of its pairs chose each expert;
+//   scan:    per expert, its segment start and the start of each chunk's run
+//            inside it; the segments' 128-row tile counts and their prefix;
+//   scatter: per chunk, each pair's place = its chunk's run start + the pairs
+//            of the same expert before it in the chunk (earlier warps, then
+//            earlier lanes of its warp).
+constexpr int kSortChunk = 512;
+
+__global__ void __launch_bounds__(kSortChunk) prefill_hist_kernel(const int32_t* ids, int n, int E, int* chunk_hist) {
+    extern __shared__ int hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int s = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += part[w];
-        counts[e] = s;
+    const int q = blockIdx.x * kSortChunk + threadIdx.x;
+    if (q < n) atomicAdd(&hist[ids[q]], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+__global__ void __launch_bounds__(1024) prefill_scan_kernel(const int* chunk_hist, int nch, int E, int* chunk_off,
+                                                            int* seg_base, int* seg_len, int* tile_start) {
+    __shared__ int wsum[32], wtile[32];
+    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+    int total = 0;
+    if (e < E)
+        for (int c = 0; c < nch; ++c) total += chunk_hist[(size_t)c * E + e];
+    const int tiles = (total + kTileM - 1) / kTileM;
+    // exclusive scans of total and tiles over the experts
+    int it = total, tt = tiles;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, it, off), b = __shfl_up_sync(0xffffffffu, tt, off);
+        if (lane >= off) {
+            it += a;
+            tt += b;
+        }
+    }
+    if (lane == 31) {
+        wsum[warp] = it;
+        wtile[warp] = tt;
+    }
+    __syncthreads();
+    int wb = 0, wt = 0;
+    for (int w = 0; w < warp; ++w) {
+        wb += wsum[w];
+        wt += wtile[w];
+    }
+    const int base = wb + it - total, tbase = wt + tt - tiles;
+    if (e < E) {
+        seg_base[e] = base;
+        seg_len[e] = total;
+        tile_start[e] = tbase;
+        if (e == E - 1) tile_start[E] = tbase + tiles;
+        int run = base;
+        for (int c = 0; c < nch; ++c) {
+            chunk_off[(size_t)c * E + e] = run;
+            run += chunk_hist[(size_t)c * E + e];
+        }
     }
 }
 
-__global__ void __launch_bounds__(512) prefill_place_kernel(const int32_t* ids, int n, int E, const int* counts,
-                                                            int* perm, int* inv, int* seg_base, int* seg_len,
-                                                            int* tile_start) {
-    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    __shared__ int base_s, wsum[16];
-    if (warp == 0) {
-        int b = 0, tb = 0;
-        for (int i = lane; i < E; i += 32) {
-            const int ci = counts[i];
-            if (i < e) {
-                b += ci;
-                tb += (ci + kTileM - 1) / kTileM;
-            }
-        }
-        b = __reduce_add_sync(0xffffffffu, b);
-        tb = __reduce_add_sync(0xffffffffu, tb);
-        if (lane == 0) {
-            base_s = b;
-            seg_base[e] = b;
-            seg_len[e] = counts[e];
-            tile_start[e] = tb;
-            if (e == E - 1) tile_start[E] = tb + (counts[e] + kTileM - 1) / kTileM;
-        }
-    }
+__global__ void __launch_bounds__(kSortChunk) prefill_scatter_kernel(const int32_t* ids, int n, int E,
+                                                                     const int* chunk_off, int* perm, int* inv) {
+    extern __shared__ int cnt[];  // [kSortChunk / 32][E]
+    constexpr int NW = kSortChunk / 32;
+    for (int i = threadIdx.x; i < NW * E; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
-    int run = base_s;
-    for (int q0 = 0; q0 < n; q0 += blockDim.x) {
-        const int q = q0 + tid;
-        const bool m = q < n && ids[q] == e;
-        const uint32_t bal = __ballot_sync(0xffffffffu, m);
-        if (lane == 0) wsum[warp] = __popc(bal);
-        __syncthreads();
-        int before = 0, total = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-            if (w < warp) before += wsum[w];
-            total += wsum[w];
-        }
-        if (m) {
-            const int pos = run + before + __popc(bal & ((1u << lane) - 1u));
-            perm[pos] = q;
-            inv[q] = pos;
-        }
-        run += total;
-        __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int q = blockIdx.x * kSortChunk + threadIdx.x;
+    const int e = q < n ? ids[q] : -1;
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) cnt[warp * E + e] = __popc(same);
+    __syncthreads();
+    if (e >= 0) {
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += cnt[w * E + e];
+        const int pos = chunk_off[(size_t)blockIdx.x * E + e] + before + rank;
+        perm[pos] = q;
+        inv[q] = pos;
     }
 }
 
@@ -445,7 +464,9 @@ PrefillWs prefill_ws_layout(int T, int E, int k, int H, int I, int Is) {
         return at;
     };
     w.logits = take(sizeof(float) * (size_t)T * E);
-    w.counts = take(sizeof(int) * (size_t)E);
+    const size_t nch = ((size_t)T * k + kSortChunk - 1) / kSortChunk;
+    w.chunk_hist = take(sizeof(int) * nch * E);
+    w.chunk_off = take(sizeof(int) * nch * E);
     w.seg_base = take(sizeof(int) * (size_t)E);
     w.seg_len = take(sizeof(int) * (size_t)E);
     w.tile_start = take(sizeof(int) * (size_t)(E + 1));
@@ -463,7 +484,8 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     const PrefillWs W = prefill_ws_layout(p.T, p.E, p.k, p.H, p.I, p.Is);
     uint8_t* ws = static_cast<uint8_t*>(p.ws);
     float* logits = reinterpret_cast<float*>(ws + W.logits);
-    int* counts = reinterpret_cast<int*>(ws + W.counts);
+    int* chunk_hist = reinterpret_cast<int*>(ws + W.chunk_hist);
+    int* chunk_off = reinterpret_cast<int*>(ws + W.chunk_off);
     int* seg_base = reinterpret_cast<int*>(ws + W.seg_base);
     int* seg_len = reinterpret_cast<int*>(ws + W.seg_len);
     int* tile_start = reinterpret_cast<int*>(ws + W.tile_start);
@@ -497,8 +519,18 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     prefill_topk_kernel<<<(T + 7) / 8, 256, sizeof(uint32_t) * 8 * E, s>>>(logits, p.bias, T, E, k, p.ids, p.weights);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 3. pairs sorted by expert
-    prefill_count_kernel<<<E, 512, 0, s>>>(p.ids, T * k, counts);
-    prefill_place_kernel<<<E, 512, 0, s>>>(p.ids, T * k, E, counts, perm, inv, seg_base, seg_len, tile_start);
+    const int nch = (T * k + kSortChunk - 1) / kSortChunk;
+    static int scatter_cfg = -1;  // its per-warp tables exceed 48 KB for E > 768
+    if (scatter_cfg != d.device) {
+        if ((e = cudaFuncSetAttribute(prefill_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)(sizeof(int) * (kSortChunk / 32) * FLINT_MAX_EXPERTS))) != cudaSuccess)
+            return e;
+        scatter_cfg = d.device;
+    }
+    prefill_hist_kernel<<<nch, kSortChunk, sizeof(int) * E, s>>>(p.ids, T * k, E, chunk_hist);
+    prefill_scan_kernel<<<1, 1024, 0, s>>>(chunk_hist, nch, E, chunk_off, seg_base, seg_len, tile_start);
+    prefill_scatter_kernel<<<nch, kSortChunk, sizeof(int) * (kSortChunk / 32) * E, s>>>(p.ids, T * k, E, chunk_off,
+                                                                                       perm, inv);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 4. gate/up + SiLU: routed experts over their gathered tokens, the shared expert over all
     PrefillGemmArgs g = {};
