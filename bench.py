@@ -55,6 +55,8 @@ def parse():
     p.add_argument("--no-bf16", action="store_true", help="skip the BF16-expert variant")
     p.add_argument("--no-stack", action="store_true", help="skip the 49-block decode stack")
     p.add_argument("--no-prefill", action="store_true", help="skip the 8192-token prefill")
+    p.add_argument("--prefill-only", action="store_true",
+                   help="only time the 8192-token prefill (one JSON line of its own; for profiling)")
     return p.parse_args()
 
 
@@ -795,6 +797,15 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill_only:
+        import torch
+        from nvfp4_moe_decode_sigmoid_gb300 import _build
+        _build.build()
+        from nvfp4_moe_decode_sigmoid_gb300 import flint as F
+        torch.cuda.set_device(dist_env()[2])
+        r = measure_prefill(F)
+        print(json.dumps({"metric": "MoE-layer prefill TFLOP/s (8192 tokens)", "value": r["tflops"],
+                          "unit": "TFLOP/s", "higher_is_better": True, "prefill": r}), flush=True)
     else:
         run_flint(args)
 
