@@ -175,20 +175,20 @@ struct LayerArgs {
 };
 
 // One grouped GEMM of the prefill: C[rows of each group] = A B^T on 128 x 128
-// tiles. Groups (experts) are row segments [seg_base[g], + seg_len[g]) of the
-// output; tile_start[g] is the exclusive prefix of their 128-row tile counts
-// (n_groups + 1 entries). Without tile_start there is one group of `rows`.
+// tiles, operands loaded by TMA. Groups (experts) are row segments
+// [seg_base[g], + seg_len[g]) of A and of the output; tile_start[g] is the
+// exclusive prefix of their 128-row tile counts (n_groups + 1 entries).
+// Without tile_start there is one group of `rows`.
 struct PrefillGemmArgs {
-    const uint16_t* A;     // bf16 rows, lda elements apart
+    const uint16_t* A;     // bf16 [rows of all groups, K], lda elements apart
     long long lda;
-    const int* a_index;    // A row of output row p: a_index[p] / a_index_div (null: p)
-    int a_index_div;
     const int* tile_start;
     const int* seg_base;
     const int* seg_len;
     int n_groups, rows, K;
-    const uint8_t* B;      // group g's matrix at B + g * b_group_stride; rows ldb bytes apart
-    long long ldb, b_group_stride;
+    const uint8_t* B;      // the groups' B matrices stacked: group g's rows start at row g * b_group_rows
+    long long ldb;         // bytes between B rows
+    int b_group_rows;
     int b_up_row0;         // SwiGLU: first up row (the gate rows start at 0)
     int n_valid;           // valid B rows (0: all); rows past it read as zero, their columns are not stored
     const float* ts;       // tensor scales of group g at ts + g * ts_stride (gate, up, down), or null
@@ -222,7 +222,7 @@ struct PrefillArgs {
 };
 
 struct PrefillWs {
-    size_t logits, chunk_hist, chunk_off, seg_base, seg_len, tile_start, perm, inv, h, hs, d, ds, total;
+    size_t logits, chunk_hist, chunk_off, seg_base, seg_len, tile_start, perm, inv, h, hs, d, x_perm, ds, total;
 };
 PrefillWs prefill_ws_layout(int T, int E, int k, int H, int I, int Is);
 

@@ -24,37 +24,17 @@
 // one thread; the operands stream through a 4-stage ring of shared-memory
 // stages filled with cp.async (A rows, and the raw NVFP4 rows of B, which
 // all threads then dequantise into the stage's B tile).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "router_common.cuh"
 #include "tcgen05.cuh"
 
 namespace flint {
 namespace {
 
-constexpr int kPT = 256;      // threads of a GEMM CTA (8 warps; warp w reads TMEM lanes 32 (w % 4))
-constexpr int kPS = 3;        // pipeline stages (two CTAs fit on an SM)
-constexpr int kChunks = 1024 / kPT;  // 16-byte chunks of one 128 x 64 bf16 tile per thread
 constexpr int kTileM = 128, kTileN = 128, kStepK = 64;
 constexpr uint32_t kTileBytes = kTileM * kStepK * 2;  // 16 KB
-constexpr uint32_t kRawCodes = kTileN * 32, kRawScales = kTileN * 4;
-
-struct PrefillSmem {
-    static constexpr size_t a = 0;                                   // kPS A tiles
-    static constexpr size_t b = a + (size_t)kPS * kTileBytes;        // kPS B tiles
-    static constexpr size_t rc = b + (size_t)kPS * kTileBytes;       // kPS raw code rows
-    static constexpr size_t rs = rc + (size_t)kPS * kRawCodes;       // kPS raw scale rows
-    static constexpr size_t bar = rs + (size_t)kPS * kRawScales;     // kPS + 1 mbarriers
-    static constexpr size_t tslot = bar + 8 * (kPS + 1);
-    static constexpr size_t total = tslot + 16;
-};
-
-__device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gmem_src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
-}
 
 // 8 codes (one 32-bit word: byte b holds columns 2b, 2b + 1) times their
 // block scale (f16x2, both halves equal) -> 8 bf16 (exact).
@@ -89,12 +69,47 @@ __device__ __forceinline__ int find_group(const int* tile_start, int n_groups, i
 enum { kEpiLogits = 0, kEpiSwiglu = 1, kEpiScale = 2 };
 
 // One 128 x 128 output tile of a grouped GEMM (blockIdx.x: M-tile over all
-// groups, blockIdx.y: N-tile). NVFP4: B rows are packed NVFP4 (dequantised in
-// shared memory); otherwise bf16.
+// groups, blockIdx.y: N-tile), fed by TMA:
+//   warp 8 (one thread) issues each K step's tile loads into a stage of the
+//     load ring: the A tile (128 rows x 64 bf16, 128-byte swizzle, exactly the
+//     operand layout of the MMA) and either the raw NVFP4 B rows (codes and the
+//     16-byte window of scales, two 64-row boxes each) or, for a bf16 B, the B
+//     tile itself; completion is counted in bytes on the stage's `full`
+//     barrier;
+//   warps 0-7 (NVFP4 only) dequantise each step's raw B rows into a B tile of
+//     the B ring (each thread half a row: four 8-value chunks, written in the
+//     128-byte swizzled layout) and arrive on its barrier;
+//   warp 9 (one thread) issues the step's four MMAs (K = 16 each) into the
+//     TMEM accumulator and commits them to the `empty` barriers of the load
+//     stage and of the B tile, which releases both for reuse;
+//   warps 0-7 then run the epilogue from TMEM.
+// Every wait is bounded; a timeout is recorded in the status word and the
+// tile is skipped.
+constexpr int kPT = 320;                // 8 dequantise/epilogue warps, the load warp, the MMA warp
+constexpr int kPW = 256;                // dequantise/epilogue threads
+constexpr int kPL = 3;                  // load stages
+constexpr int kPB = 2;                  // B tiles (NVFP4)
+constexpr uint32_t kRawBytes = kTileN * 32 + kTileN * 16;  // codes + scale windows of one step
+
+template <bool NVFP4>
+struct TmaSmem {
+    static constexpr size_t stage = kTileBytes + (NVFP4 ? kRawBytes : kTileBytes);
+    static constexpr size_t load = 0;                                     // kPL x (A tile, B raw or B tile)
+    static constexpr size_t btile = load + kPL * stage;                   // kPB B tiles (NVFP4)
+    static constexpr size_t bar = btile + (NVFP4 ? kPB * (size_t)kTileBytes : 0);
+    static constexpr int nbar = 2 * kPL + 2 * kPB + 1;
+    static constexpr size_t tslot = bar + 8 * nbar;
+    static constexpr size_t total = tslot + 16 + 1024;                    // + alignment slack
+};
+
 template <bool NVFP4, int EPI>
-__global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const PrefillGemmArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    using L = PrefillSmem;
+__global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+                                                              const __grid_constant__ CUtensorMap tma_b,
+                                                              const __grid_constant__ CUtensorMap tma_s,
+                                                              const PrefillGemmArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using L = TmaSmem<NVFP4>;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // ---- which tile ----
     int g = 0, row0, nrows;
@@ -102,9 +117,9 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const PrefillGemmA
     if (a.tile_start) {
         if (mt >= ld_cg(a.tile_start + a.n_groups)) return;
         g = find_group(a.tile_start, a.n_groups, mt);
-        const int seg_len = ld_cg(a.seg_len + g);
-        row0 = ld_cg(a.seg_base + g) + (mt - ld_cg(a.tile_start + g)) * kTileM;
-        nrows = min(kTileM, ld_cg(a.seg_base + g) + seg_len - row0);
+        const int base = ld_cg(a.seg_base + g);
+        row0 = base + (mt - ld_cg(a.tile_start + g)) * kTileM;
+        nrows = min(kTileM, base + ld_cg(a.seg_len + g) - row0);
     } else {
         row0 = mt * kTileM;
         if (row0 >= a.rows) return;
@@ -112,180 +127,169 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const PrefillGemmA
     }
     const int nt = blockIdx.y;
     const int K = a.K, nk = K / kStepK;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::bar);
+    uint64_t* fullL = reinterpret_cast<uint64_t*>(smem + L::bar);
+    uint64_t* emptyL = fullL + kPL;
+    uint64_t* fullB = emptyL + kPL;
+    uint64_t* emptyB = fullB + kPB;
+    uint64_t* done = emptyB + kPB;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::tslot);
-
-    // ---- operand rows of this thread's copies ----
-    // A: chunk q = it * kPT + tid of a stage is row (q >> 6) * 8 + (q & 7), K chunk (q >> 3) & 7.
-    const uint16_t* arow[kChunks];
-#pragma unroll
-    for (int it = 0; it < kChunks; ++it) {
-        const int q = it * kPT + tid, r = ((q >> 6) << 3) + (q & 7);
-        arow[it] = nullptr;
-        if (r < nrows) {
-            const int p = row0 + r;
-            const int src = a.a_index ? ld_cg(a.a_index + p) / a.a_index_div : p;
-            arow[it] = a.A + (size_t)src * a.lda + ((q >> 3) & 7) * 8;
-        }
-    }
-    // B row of tile row r: gate/up pairs (rows [0, 64) gate n, [64, 128) up n) or plain rows.
-    auto brow = [&](int r) -> size_t {
-        if (EPI == kEpiSwiglu) return (size_t)(r < 64 ? nt * 64 + r : a.b_up_row0 + nt * 64 + (r - 64));
-        return (size_t)(nt * kTileN + r);
-    };
-    const uint8_t* Bg = a.B + (size_t)g * a.b_group_stride;
-    auto load_stage = [&](int s, int j) {
-        const int k0 = j * kStepK;
-        uint8_t* at = smem + L::a + (size_t)s * kTileBytes;
-#pragma unroll
-        for (int it = 0; it < kChunks; ++it) {
-            const int q = it * kPT + tid;
-            cp_async16_zfill(at + 16 * q, arow[it] ? arow[it] + k0 : a.A, arow[it] != nullptr);
-        }
-        if constexpr (NVFP4) {
-            uint8_t* rc = smem + L::rc + (size_t)s * kRawCodes;
-            uint8_t* rs = smem + L::rs + (size_t)s * kRawScales;
-            {
-                const int q = tid, r = q >> 1, half = q & 1;  // 256 chunks: 128 rows x 32 code bytes
-                cp_async16(rc + 32 * r + 16 * half, Bg + brow(r) * a.ldb + k0 / 2 + 16 * half);
-            }
-            if (tid < kTileN) cp_async4(rs + 4 * tid, Bg + brow(tid) * a.ldb + K / 2 + k0 / 16);
-        } else {
-            uint8_t* bt = smem + L::b + (size_t)s * kTileBytes;
-#pragma unroll
-            for (int it = 0; it < kChunks; ++it) {
-                const int q = it * kPT + tid, r = ((q >> 6) << 3) + (q & 7);
-                const bool v = a.n_valid == 0 || nt * kTileN + r < a.n_valid;
-                cp_async16_zfill(bt + 16 * q, v ? Bg + brow(r) * a.ldb + 2 * (k0 + ((q >> 3) & 7) * 8) : a.B, v);
-            }
-        }
-    };
+    // B rows of this tile: two 64-row boxes (gate n.., up n.. for SwiGLU; else n0.., n0 + 64..)
+    const int brow_lo = g * a.b_group_rows + (EPI == kEpiSwiglu ? nt * 64 : nt * kTileN);
+    const int brow_hi = g * a.b_group_rows + (EPI == kEpiSwiglu ? a.b_up_row0 + nt * 64 : nt * kTileN + 64);
 
     if (tid == 0) {
-        for (int s = 0; s <= kPS; ++s) mbar_init(bar + s, 1);
+        for (int i = 0; i < L::nbar; ++i) mbar_init(fullL + i, (i >= 2 * kPL && i < 2 * kPL + kPB) ? kPW : 1);
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == 9) {
         tmem_alloc(tslot, kTileN);
         tmem_relinquish();
-    }
-    for (int s = 0; s < kPS - 1; ++s) {
-        if (s < nk) load_stage(s, s);
-        cp_async_commit();
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t idesc = tc_idesc_bf16(kTileM, kTileN);
     bool ok = true;
-    for (int i = 0; i < nk && ok; ++i) {
-        const int s = i % kPS;
-        cp_async_wait<kPS - 2>();
-        __syncthreads();  // stage s landed for every thread
-        if constexpr (NVFP4) {
-            const uint8_t* rc = smem + L::rc + (size_t)s * kRawCodes;
-            const uint8_t* rs = smem + L::rs + (size_t)s * kRawScales;
-            uint8_t* bt = smem + L::b + (size_t)s * kTileBytes;
-#pragma unroll
-            for (int it = 0; it < kChunks; ++it) {
-                const int q = it * kPT + tid, r = ((q >> 6) << 3) + (q & 7), kc = (q >> 3) & 7;
-                const uint32_t w = *reinterpret_cast<const uint32_t*>(rc + 32 * r + 4 * kc);
-                const uint32_t sb = rs[4 * r + (kc >> 1)] & 0x7Fu;
-                uint32_t s2;
-                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"((uint16_t)(sb | (sb << 8))));
-                *reinterpret_cast<uint4*>(bt + 16 * q) = dequant8(w, s2);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();  // the stage's tiles complete in shared memory
-        if (tid == 0) {
-            tc_fence_after_sync();
-            const uint8_t* at = smem + L::a + (size_t)s * kTileBytes;
-            const uint8_t* bt = smem + L::b + (size_t)s * kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < kStepK / 16; ++kk)
-                tc_mma_bf16(tmem, tc_smem_desc(at + 256 * kk, kTcCoreK, kTcCoreRow),
-                            tc_smem_desc(bt + 256 * kk, kTcCoreK, kTcCoreRow), idesc, (i > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(bar + s);
-        }
-        // refill the stage of step i - 1 with step i + kPS - 1 once its MMAs are done
-        const int j = i + kPS - 1;
-        if (j < nk) {
-            if (i >= 1) ok = mbar_wait_bounded(bar + (i - 1) % kPS, ((i - 1) / kPS) & 1, a.status, kStatusTimeoutPrefill);
-            if (ok) load_stage(j % kPS, j);
-        }
-        cp_async_commit();
-        ok = __syncthreads_and(ok);
-    }
-    // the last step's MMAs (and so all of them) complete
-    if (ok) ok = mbar_wait_bounded(bar + (nk - 1) % kPS, ((nk - 1) / kPS) & 1, a.status, kStatusTimeoutPrefill);
-    ok = __syncthreads_and(ok);
-    cp_async_wait<0>();
-    tc_fence_after_sync();
-    if (ok) {
-        const int wq = warp & 3, half = warp >> 2;  // lane quarter, column half
-        const int r = 32 * wq + lane;  // the TMEM lane = tile row of this thread
-        const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);
-        const bool valid = r < nrows;
-        const int p = row0 + r;
-        if (EPI == kEpiSwiglu) {
-            const float tsg = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride) : 1.f;
-            const float tsu = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride + 1) : 1.f;
-            for (int c = 32 * half; c < 32 * half + 32; c += 16) {
-                uint32_t gv[16], uv[16];
-                tmem_ld16(tl + c, gv);
-                tmem_ld16(tl + 64 + c, uv);
-                tmem_ld_wait();
-                uint32_t o[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float h2[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const float gg = bf16_round_f32(tsg * __uint_as_float(gv[2 * i + h]));
-                        const float uu = bf16_round_f32(tsu * __uint_as_float(uv[2 * i + h]));
-                        h2[h] = silu_f(gg) * uu;
-                    }
-                    o[i] = (uint32_t)f32_to_bf16_bits(h2[0]) | ((uint32_t)f32_to_bf16_bits(h2[1]) << 16);
-                }
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + (size_t)p * a.ldo + nt * 64 + c);
-                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                }
-            }
-        } else {
-            const float ts = (EPI == kEpiScale && a.ts) ? ld_cg(a.ts + (size_t)g * a.ts_stride + 2) : 1.f;
-            for (int c = 64 * half; c < 64 * half + 64; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tl + c, v);
-                tmem_ld_wait();
-                if (!valid) continue;
-                if (EPI == kEpiLogits) {
-                    if (a.n_valid && nt * kTileN + c >= a.n_valid) continue;  // n_valid % 16 == 0
-                    float4* dst = reinterpret_cast<float4*>(a.out_f32 + (size_t)p * a.ldo + nt * kTileN + c);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                             __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+
+    if (warp == 8) {
+        // ---------------- loads (one thread) ----------------
+        if (lane == 0) {
+            const uint32_t bytes = (uint32_t)L::stage;
+            for (int j = 0; j < nk && ok; ++j) {
+                const int s = j % kPL, k0 = j * kStepK;
+                if (j >= kPL) ok = mbar_wait_bounded(emptyL + s, ((j / kPL) - 1) & 1, a.status, kStatusTimeoutPrefill);
+                if (!ok) break;
+                uint8_t* st = smem + L::load + (size_t)s * L::stage;
+                mbar_arrive_expect_tx(fullL + s, bytes);
+                tma_load_2d(st, &tma_a, k0, row0, fullL + s);
+                if constexpr (NVFP4) {
+                    uint8_t* codes = st + kTileBytes;
+                    uint8_t* scales = codes + kTileN * 32;
+                    const int sx = K / 2 + ((k0 / 16) & ~15);
+                    tma_load_2d(codes, &tma_b, k0 / 2, brow_lo, fullL + s);
+                    tma_load_2d(codes + 64 * 32, &tma_b, k0 / 2, brow_hi, fullL + s);
+                    tma_load_2d(scales, &tma_s, sx, brow_lo, fullL + s);
+                    tma_load_2d(scales + 64 * 16, &tma_s, sx, brow_hi, fullL + s);
                 } else {
+                    tma_load_2d(st + kTileBytes, &tma_b, k0, nt * kTileN, fullL + s);
+                }
+            }
+        }
+    } else if (warp == 9) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            const uint32_t idesc = tc_idesc_bf16(kTileM, kTileN);
+            for (int i = 0; i < nk && ok; ++i) {
+                const int sl = i % kPL, sb = i % kPB;
+                if constexpr (NVFP4)
+                    ok = mbar_wait_bounded(fullB + sb, (i / kPB) & 1, a.status, kStatusTimeoutPrefill);
+                else
+                    ok = mbar_wait_bounded(fullL + sl, (i / kPL) & 1, a.status, kStatusTimeoutPrefill);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint8_t* at = smem + L::load + (size_t)sl * L::stage;
+                const uint8_t* bt = NVFP4 ? smem + L::btile + (size_t)sb * kTileBytes : at + kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kStepK / 16; ++kk)
+                    tc_mma_bf16(tmem, tc_smem_desc_sw128(at + 32 * kk), tc_smem_desc_sw128(bt + 32 * kk), idesc,
+                                (i > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(emptyL + sl);
+                if constexpr (NVFP4) tc_commit(emptyB + sb);
+            }
+            tc_commit(done);  // completes once every MMA issued above has
+        }
+    } else if constexpr (NVFP4) {
+        // ---------------- dequantise (warps 0-7) ----------------
+        const int r = tid & 127, hb = tid >> 7;  // half row of B owned by this thread
+        for (int i = 0; i < nk && ok; ++i) {
+            const int sl = i % kPL, sb = i % kPB;
+            ok = mbar_wait_bounded(fullL + sl, (i / kPL) & 1, a.status, kStatusTimeoutPrefill);
+            if (ok && i >= kPB) ok = mbar_wait_bounded(emptyB + sb, ((i / kPB) - 1) & 1, a.status, kStatusTimeoutPrefill);
+            if (!ok) break;
+            const uint8_t* st = smem + L::load + (size_t)sl * L::stage + kTileBytes;
+            const uint4 cw = *reinterpret_cast<const uint4*>(st + 32 * r + 16 * hb);
+            const uint32_t sc = *reinterpret_cast<const uint32_t*>(st + kTileN * 32 + 16 * r + (((i * kStepK) / 16) & 15));
+            uint8_t* bt = smem + L::btile + (size_t)sb * kTileBytes;
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int kc = 4 * hb + c;
+                const uint32_t sbyte = (sc >> (8 * (kc >> 1))) & 0x7Fu;
+                uint32_t s2;
+                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"((uint16_t)(sbyte | (sbyte << 8))));
+                *reinterpret_cast<uint4*>(bt + tc_sw128_offset(r, 8 * kc)) = dequant8(words[c], s2);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(fullB + sb);
+        }
+    }
+    // ---------------- epilogue (warps 0-7) ----------------
+    if (warp < 8) {
+        if (ok) ok = mbar_wait_bounded(done, 0, a.status, kStatusTimeoutPrefill);
+        tc_fence_after_sync();
+        if (ok) {
+            const int wq = warp & 3, half = warp >> 2;  // lane quarter, column half
+            const int r = 32 * wq + lane;              // the TMEM lane = tile row of this thread
+            const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);
+            const bool valid = r < nrows;
+            const int p = row0 + r;
+            if (EPI == kEpiSwiglu) {
+                const float tsg = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride) : 1.f;
+                const float tsu = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride + 1) : 1.f;
+                for (int c = 32 * half; c < 32 * half + 32; c += 16) {
+                    uint32_t gv[16], uv[16];
+                    tmem_ld16(tl + c, gv);
+                    tmem_ld16(tl + 64 + c, uv);
+                    tmem_ld_wait();
                     uint32_t o[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        o[i] = (uint32_t)f32_to_bf16_bits(ts * __uint_as_float(v[2 * i])) |
-                               ((uint32_t)f32_to_bf16_bits(ts * __uint_as_float(v[2 * i + 1])) << 16);
-                    uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + (size_t)p * a.ldo + nt * kTileN + c);
-                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    for (int i = 0; i < 8; ++i) {
+                        float h2[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const float gg = bf16_round_f32(tsg * __uint_as_float(gv[2 * i + h]));
+                            const float uu = bf16_round_f32(tsu * __uint_as_float(uv[2 * i + h]));
+                            h2[h] = silu_f(gg) * uu;
+                        }
+                        o[i] = (uint32_t)f32_to_bf16_bits(h2[0]) | ((uint32_t)f32_to_bf16_bits(h2[1]) << 16);
+                    }
+                    if (valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + (size_t)p * a.ldo + nt * 64 + c);
+                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+            } else {
+                const float ts = (EPI == kEpiScale && a.ts) ? ld_cg(a.ts + (size_t)g * a.ts_stride + 2) : 1.f;
+                for (int c = 64 * half; c < 64 * half + 64; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tl + c, v);
+                    tmem_ld_wait();
+                    if (!valid) continue;
+                    if (EPI == kEpiLogits) {
+                        if (a.n_valid && nt * kTileN + c >= a.n_valid) continue;  // n_valid % 16 == 0
+                        float4* dst = reinterpret_cast<float4*>(a.out_f32 + (size_t)p * a.ldo + nt * kTileN + c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                    } else {
+                        uint32_t o[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            o[i] = (uint32_t)f32_to_bf16_bits(ts * __uint_as_float(v[2 * i])) |
+                                   ((uint32_t)f32_to_bf16_bits(ts * __uint_as_float(v[2 * i + 1])) << 16);
+                        uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + (size_t)p * a.ldo + nt * kTileN + c);
+                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
                 }
             }
         }
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTileN);
+    if (warp == 9) tmem_dealloc(tmem, kTileN);
 }
 
 // ---------------------------------------------------------------------------
@@ -431,26 +435,75 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* weigh
     }
 }
 
-template <typename Kern>
-cudaError_t launch_plain(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const PrefillGemmArgs& a) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, kernel, a);
+// x_perm[p] = x[perm[p] / k]: the expert-sorted copy of the token rows (one
+// warp per row), so that the routed gate/up GEMM reads its A tiles as plain
+// 2-D tiles.
+__global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* x, const int* perm, int k, int H, int n,
+                                                             uint16_t* x_perm) {
+    const int p = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (p >= n) return;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(perm[p] / k) * H);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)p * H);
+    for (int i = lane; i < H / 8; i += 32) dst[i] = src[i];
 }
 
+// ---------------------------------------------------------------------------
+// Tensor maps (host): 2-D tiled maps for the TMA loads.
+// ---------------------------------------------------------------------------
+cudaError_t tensor_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t rows, uint64_t inner,
+                       uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || !fn || q != cudaDriverEntryPointSuccess) return e != cudaSuccess ? e : cudaErrorNotSupported;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = encode(m, type, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// A operand: bf16 [rows, K] row-major -> 128 x 64 tiles, 128-byte swizzle.
+cudaError_t map_a(CUtensorMap* m, const uint16_t* A, uint64_t rows, uint64_t K) {
+    return tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, rows, K, 2 * K, kStepK, kTileM, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// One grouped GEMM launch: the A map, the B map(s) and the kernel.
 template <bool NVFP4, int EPI>
-cudaError_t launch_gemm(const PrefillGemmArgs& a, const DevInfo& d, int m_tiles, int n_tiles, cudaStream_t s) {
+cudaError_t launch_gemm(const PrefillGemmArgs& a, uint64_t a_rows, uint64_t b_rows, const DevInfo& d, int m_tiles,
+                        int n_tiles, cudaStream_t s) {
     static int configured_for = -1;
     cudaError_t e = configure_smem(prefill_gemm_kernel<NVFP4, EPI>, d, configured_for);
     if (e != cudaSuccess) return e;
     if (m_tiles <= 0 || n_tiles <= 0) return cudaSuccess;
-    return launch_plain(prefill_gemm_kernel<NVFP4, EPI>, dim3((unsigned)m_tiles, (unsigned)n_tiles), dim3(kPT),
-                        PrefillSmem::total, s, a);
+    CUtensorMap ta, tb, ts;
+    if ((e = map_a(&ta, a.A, a_rows, (uint64_t)a.K)) != cudaSuccess) return e;
+    if (NVFP4) {
+        // packed rows as bytes: 32-byte code windows and 16-byte scale windows of 64 rows
+        if ((e = tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, b_rows, (uint64_t)a.ldb, (uint64_t)a.ldb, 32, 64,
+                            CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+            return e;
+        if ((e = tensor_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, b_rows, (uint64_t)a.ldb, (uint64_t)a.ldb, 16, 64,
+                            CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+            return e;
+    } else {
+        if ((e = tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, b_rows, (uint64_t)a.K, (uint64_t)a.ldb, kStepK,
+                            kTileN, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
+        ts = tb;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)m_tiles, (unsigned)n_tiles);
+    cfg.blockDim = dim3(kPT);
+    cfg.dynamicSmemBytes = TmaSmem<NVFP4>::total;
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<NVFP4, EPI>, ta, tb, ts, a);
 }
 
 }  // namespace
@@ -475,6 +528,7 @@ PrefillWs prefill_ws_layout(int T, int E, int k, int H, int I, int Is) {
     w.h = take(2 * (size_t)T * k * I);
     w.hs = take(2 * (size_t)T * Is);
     w.d = take(2 * (size_t)T * k * H);
+    w.x_perm = take(2 * (size_t)T * k * H);
     w.ds = take(2 * (size_t)T * H);
     w.total = o;
     return w;
@@ -514,7 +568,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     r.out_f32 = logits;
     r.ldo = E;
     r.status = status;
-    if ((e = launch_gemm<false, kEpiLogits>(r, d, mt_all, (E + kTileN - 1) / kTileN, s)) != cudaSuccess) return e;
+    if ((e = launch_gemm<false, kEpiLogits>(r, T, E, d, mt_all, (E + kTileN - 1) / kTileN, s)) != cudaSuccess) return e;
     // 2. top-k per token
     prefill_topk_kernel<<<(T + 7) / 8, 256, sizeof(uint32_t) * 8 * E, s>>>(logits, p.bias, T, E, k, p.ids, p.weights);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -532,12 +586,13 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     prefill_scatter_kernel<<<nch, kSortChunk, sizeof(int) * (kSortChunk / 32) * E, s>>>(p.ids, T * k, E, chunk_off,
                                                                                        perm, inv);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // 4. gate/up + SiLU: routed experts over their gathered tokens, the shared expert over all
+    // 4. gate/up + SiLU: routed experts over their (expert-sorted) token rows, the shared expert over all
+    uint16_t* x_perm = reinterpret_cast<uint16_t*>(ws + W.x_perm);
+    prefill_gather_kernel<<<(T * k + 7) / 8, 256, 0, s>>>(p.x, perm, k, H, T * k, x_perm);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     PrefillGemmArgs g = {};
-    g.A = p.x;
+    g.A = x_perm;
     g.lda = H;
-    g.a_index = perm;
-    g.a_index_div = k;
     g.tile_start = tile_start;
     g.seg_base = seg_base;
     g.seg_len = seg_len;
@@ -545,14 +600,15 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     g.K = H;
     g.B = p.gu;
     g.ldb = rs_h;
-    g.b_group_stride = 2 * (long long)I * rs_h;
+    g.b_group_rows = 2 * I;
     g.b_up_row0 = I;
     g.ts = p.ts;
     g.ts_stride = 3;
     g.out_bf16 = h;
     g.ldo = I;
     g.status = status;
-    if ((e = launch_gemm<true, kEpiSwiglu>(g, d, mt_routed, I / 64, s)) != cudaSuccess) return e;
+    if ((e = launch_gemm<true, kEpiSwiglu>(g, (uint64_t)T * k, (uint64_t)E * 2 * I, d, mt_routed, I / 64, s)) != cudaSuccess)
+        return e;
     if (p.s_gu) {
         PrefillGemmArgs gs = {};
         gs.A = p.x;
@@ -566,7 +622,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
         gs.out_bf16 = hs;
         gs.ldo = Is;
         gs.status = status;
-        if ((e = launch_gemm<true, kEpiSwiglu>(gs, d, mt_all, Is / 64, s)) != cudaSuccess) return e;
+        if ((e = launch_gemm<true, kEpiSwiglu>(gs, T, 2 * (uint64_t)Is, d, mt_all, Is / 64, s)) != cudaSuccess) return e;
     }
     // 5. down
     PrefillGemmArgs dn = {};
@@ -579,13 +635,15 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     dn.K = I;
     dn.B = p.down;
     dn.ldb = rs_i;
-    dn.b_group_stride = (long long)H * rs_i;
+    dn.b_group_rows = H;
     dn.ts = p.ts;
     dn.ts_stride = 3;
     dn.out_bf16 = dd;
     dn.ldo = H;
     dn.status = status;
-    if ((e = launch_gemm<true, kEpiScale>(dn, d, mt_routed, H / kTileN, s)) != cudaSuccess) return e;
+    if ((e = launch_gemm<true, kEpiScale>(dn, (uint64_t)T * k, (uint64_t)E * H, d, mt_routed, H / kTileN, s)) !=
+        cudaSuccess)
+        return e;
     if (p.s_down) {
         PrefillGemmArgs dsa = {};
         dsa.A = hs;
@@ -598,7 +656,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
         dsa.out_bf16 = ds;
         dsa.ldo = H;
         dsa.status = status;
-        if ((e = launch_gemm<true, kEpiScale>(dsa, d, mt_all, H / kTileN, s)) != cudaSuccess) return e;
+        if ((e = launch_gemm<true, kEpiScale>(dsa, T, H, d, mt_all, H / kTileN, s)) != cudaSuccess) return e;
     }
     // 6. combine
     prefill_combine_kernel<<<T, 256, 0, s>>>(p.weights, inv, k, dd, p.s_down ? ds : nullptr, H, p.y);

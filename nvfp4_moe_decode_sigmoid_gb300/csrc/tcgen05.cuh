@@ -33,6 +33,32 @@ __device__ __forceinline__ uint64_t tc_smem_desc(const void* p, uint32_t lead_by
            ((uint64_t)((stride_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
+// Shared-memory matrix descriptor of a K-major tile in the 128-byte swizzled
+// layout that a TMA tile load with 128-byte swizzle writes: rows of 128 bytes
+// (64 bf16 of K), 16-byte chunk c of row r stored at chunk c ^ (r % 8), 8-row
+// groups 1024 bytes apart; the tile starts on a 1024-byte boundary and the
+// k-th MMA of K = 16 starts 32 * k bytes into it.
+__device__ __forceinline__ uint64_t tc_smem_desc_sw128(const void* p) {
+    const uint32_t a = smem_u32(p);
+    return (uint64_t)((a >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+
+// Byte offset of element (r, k) (bf16) in a 128-byte-swizzled K-major tile.
+__host__ __device__ __forceinline__ uint32_t tc_sw128_offset(int r, int k) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k >> 3) ^ r) & 7) << 4) + (k & 7) * 2);
+}
+
+// 2-D TMA tile load global -> shared completing on `bar` (tensor map passed as
+// a __grid_constant__ kernel parameter; c0 = innermost coordinate).
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, FP32 accumulator,
 // both operands K-major, an M x N tile.
 __host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N) {
