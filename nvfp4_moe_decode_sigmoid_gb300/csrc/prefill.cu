@@ -68,8 +68,9 @@ __device__ __forceinline__ int find_group(const int* tile_start, int n_groups, i
 
 enum { kEpiLogits = 0, kEpiSwiglu = 1, kEpiScale = 2 };
 
-// One 128 x 128 output tile of a grouped GEMM (blockIdx.x: M-tile over all
-// groups, blockIdx.y: N-tile), fed by TMA:
+// One 128 x 128 output tile of a grouped GEMM (blockIdx.x: N-tile, blockIdx.y:
+// M-tile over all groups; the N-tiles of one M-tile run together, so its A
+// tile is read from HBM once and from L2 by the others), fed by TMA:
 //   warp 8 (one thread) issues each K step's tile loads into a stage of the
 //     load ring: the A tile (128 rows x 64 bf16, 128-byte swizzle, exactly the
 //     operand layout of the MMA) and either the raw NVFP4 B rows (codes and the
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_const
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // ---- which tile ----
     int g = 0, row0, nrows;
-    const int mt = blockIdx.x;
+    const int mt = blockIdx.y;
     if (a.tile_start) {
         if (mt >= ld_cg(a.tile_start + a.n_groups)) return;
         g = find_group(a.tile_start, a.n_groups, mt);
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_const
         if (row0 >= a.rows) return;
         nrows = min(kTileM, a.rows - row0);
     }
-    const int nt = blockIdx.y;
+    const int nt = blockIdx.x;
     const int K = a.K, nk = K / kStepK;
     uint64_t* fullL = reinterpret_cast<uint64_t*>(smem + L::bar);
     uint64_t* emptyL = fullL + kPL;
@@ -499,7 +500,7 @@ cudaError_t launch_gemm(const PrefillGemmArgs& a, uint64_t a_rows, uint64_t b_ro
         ts = tb;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)m_tiles, (unsigned)n_tiles);
+    cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)m_tiles);
     cfg.blockDim = dim3(kPT);
     cfg.dynamicSmemBytes = TmaSmem<NVFP4>::total;
     cfg.stream = s;
