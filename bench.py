@@ -67,6 +67,24 @@ def dist_env():
     return rank, world, local
 
 
+def replica_max(v: float, world: int, device: str) -> float:
+    """The largest of the ranks' values (the slowest replica's time); every
+    rank gets it. The ranks are independent replicas: this all-reduce of one
+    number is the only exchange between them."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(bytes_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job GB/s: the bytes every replica processed over the slowest time."""
+    return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
+
+
 def expert_bytes():
     from nvfp4_moe_decode_sigmoid_gb300 import flint as F
     gu = 2 * I * F.flint_nvfp4_row_stride(H)
@@ -632,17 +650,13 @@ def run_flint(args):
             dist.barrier()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return replica_max(v, world, "cuda")
 
     model = Model(args.layers, "cuda")
     dev_index = torch.cuda.current_device()
     main = measure_workload(F, model, args.workload, args.steps, args.warmup, args.graph_steps, sync_all, dev_index)
     ms = max_over_ranks(main["ms"])
-    value = main["bytes"] * world / (ms * 1e-3) / 1e9
+    value = replica_value(main["bytes"], world, ms)
     chain = measure_workload(F, model, args.workload, max(1024, args.steps // 4), args.warmup, args.graph_steps,
                              sync_all, dev_index, with_clocks=False, path="chain")
     extra = {}
