@@ -538,6 +538,31 @@ def measure_kernels(F, model, name, reps=8):
     return out
 
 
+def measure_single_flushed(F, model, name, reps=7):
+    """One flint_moe_layer call right after the L2 is flushed (a 512 MB write,
+    four times the 129 MB L2), timed alone with CUDA events; median of `reps`."""
+    import torch
+    T, routing = WORKLOADS[name]
+    bias, inp = make_inputs(model, T, routing, "cuda")
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    times = []
+    with torch.cuda.stream(stream):
+        for r in range(reps + 1):
+            li = r % len(model.layers)
+            flush.fill_(r & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run_step(F, model, inp, li, bias, 0, "fused")
+            e1.record(stream)
+            e1.synchronize()
+            if r > 0:
+                times.append(e0.elapsed_time(e1) * 1e3)
+    del flush
+    torch.cuda.empty_cache()
+    return statistics.median(times)
+
+
 def measure_e2e(F, model, name, steps, graph_steps):
     """Same metric through the C ABI with HOST buffers: every step copies its
     x from pinned host memory to the device and its y back, inside the timed
@@ -669,6 +694,7 @@ def run_flint(args):
             extra[name] = dict(us_per_layer=r["ms"] * 1e3 / r["steps"], gb_s=r["bytes"] / (r["ms"] * 1e-3) / 1e9,
                                mean_distinct_experts=r["mean_distinct"], bytes_per_step=r["bytes_per_step_mean"])
     kern = measure_kernels(F, model, args.workload)
+    kern["single_call_l2_flushed_us"] = measure_single_flushed(F, model, args.workload)
     bf16 = {}
     if not args.no_bf16:
         bf16 = measure_bf16(F, model, args, sync_all, dev_index)
