@@ -33,7 +33,8 @@
 namespace flint {
 namespace {
 
-constexpr int kTileM = 128, kTileN = 128, kStepK = 64;
+constexpr int kTileM = 128, kStepK = 64;
+constexpr int kNTile = 128;  // tile N of the NVFP4 expert GEMMs (256 measured slower: 940 vs 905 us, one CTA per SM)
 constexpr uint32_t kTileBytes = kTileM * kStepK * 2;  // 16 KB
 
 // 8 codes (one 32-bit word: byte b holds columns 2b, 2b + 1) times their
@@ -88,29 +89,34 @@ enum { kEpiLogits = 0, kEpiSwiglu = 1, kEpiScale = 2 };
 // tile is skipped.
 constexpr int kPT = 320;                // 8 dequantise/epilogue warps, the load warp, the MMA warp
 constexpr int kPW = 256;                // dequantise/epilogue threads
-constexpr int kPL = 3;                  // load stages
 constexpr int kPB = 2;                  // B tiles (NVFP4)
-constexpr uint32_t kRawBytes = kTileN * 32 + kTileN * 16;  // codes + scale windows of one step
 
-template <bool NVFP4>
+// Tile N = TN (128: two CTAs per SM, 3 load stages; 256: one CTA per SM, 4
+// load stages, half the A bytes per FLOP).
+template <bool NVFP4, int TN>
 struct TmaSmem {
-    static constexpr size_t stage = kTileBytes + (NVFP4 ? kRawBytes : kTileBytes);
-    static constexpr size_t load = 0;                                     // kPL x (A tile, B raw or B tile)
-    static constexpr size_t btile = load + kPL * stage;                   // kPB B tiles (NVFP4)
-    static constexpr size_t bar = btile + (NVFP4 ? kPB * (size_t)kTileBytes : 0);
-    static constexpr int nbar = 2 * kPL + 2 * kPB + 1;
+    static constexpr int PL = TN == 256 ? 4 : 3;                          // load stages
+    static constexpr size_t raw = (size_t)TN * 48;                        // codes + scale windows of one step
+    static constexpr size_t bt = (size_t)TN * kStepK * 2;                 // one B tile
+    static constexpr size_t stage = kTileBytes + (NVFP4 ? raw : bt);
+    static constexpr size_t load = 0;                                     // PL x (A tile, B raw or B tile)
+    static constexpr size_t btile = load + PL * stage;                    // kPB B tiles (NVFP4)
+    static constexpr size_t bar = btile + (NVFP4 ? kPB * bt : 0);
+    static constexpr int nbar = 2 * PL + 2 * kPB + 1;
     static constexpr size_t tslot = bar + 8 * nbar;
     static constexpr size_t total = tslot + 16 + 1024;                    // + alignment slack
 };
 
-template <bool NVFP4, int EPI>
-__global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+template <bool NVFP4, int EPI, int TN>
+__global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                                                               const __grid_constant__ CUtensorMap tma_b,
                                                               const __grid_constant__ CUtensorMap tma_s,
                                                               const PrefillGemmArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    using L = TmaSmem<NVFP4>;
+    using L = TmaSmem<NVFP4, TN>;
+    constexpr int kPL = L::PL;
+    constexpr int NB = TN / 64;  // 64-row boxes of B per step
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // ---- which tile ----
     int g = 0, row0, nrows;
@@ -134,16 +140,19 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_const
     uint64_t* emptyB = fullB + kPB;
     uint64_t* done = emptyB + kPB;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::tslot);
-    // B rows of this tile: two 64-row boxes (gate n.., up n.. for SwiGLU; else n0.., n0 + 64..)
-    const int brow_lo = g * a.b_group_rows + (EPI == kEpiSwiglu ? nt * 64 : nt * kTileN);
-    const int brow_hi = g * a.b_group_rows + (EPI == kEpiSwiglu ? a.b_up_row0 + nt * 64 : nt * kTileN + 64);
+    // first B row of 64-row box b: gate rows then up rows (SwiGLU), else consecutive rows
+    auto brow = [&](int b) -> int {
+        if (EPI == kEpiSwiglu)
+            return g * a.b_group_rows + (b < NB / 2 ? nt * (TN / 2) + 64 * b : a.b_up_row0 + nt * (TN / 2) + 64 * (b - NB / 2));
+        return g * a.b_group_rows + nt * TN + 64 * b;
+    };
 
     if (tid == 0) {
         for (int i = 0; i < L::nbar; ++i) mbar_init(fullL + i, (i >= 2 * kPL && i < 2 * kPL + kPB) ? kPW : 1);
         fence_mbar_init();
     }
     if (warp == 9) {
-        tmem_alloc(tslot, kTileN);
+        tmem_alloc(tslot, TN);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -165,21 +174,22 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_const
                 tma_load_2d(st, &tma_a, k0, row0, fullL + s);
                 if constexpr (NVFP4) {
                     uint8_t* codes = st + kTileBytes;
-                    uint8_t* scales = codes + kTileN * 32;
+                    uint8_t* scales = codes + TN * 32;
                     const int sx = K / 2 + ((k0 / 16) & ~15);
-                    tma_load_2d(codes, &tma_b, k0 / 2, brow_lo, fullL + s);
-                    tma_load_2d(codes + 64 * 32, &tma_b, k0 / 2, brow_hi, fullL + s);
-                    tma_load_2d(scales, &tma_s, sx, brow_lo, fullL + s);
-                    tma_load_2d(scales + 64 * 16, &tma_s, sx, brow_hi, fullL + s);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        tma_load_2d(codes + 64 * 32 * b, &tma_b, k0 / 2, brow(b), fullL + s);
+                        tma_load_2d(scales + 64 * 16 * b, &tma_s, sx, brow(b), fullL + s);
+                    }
                 } else {
-                    tma_load_2d(st + kTileBytes, &tma_b, k0, nt * kTileN, fullL + s);
+                    tma_load_2d(st + kTileBytes, &tma_b, k0, nt * TN, fullL + s);
                 }
             }
         }
     } else if (warp == 9) {
         // ---------------- MMA issue (one thread) ----------------
         if (lane == 0) {
-            const uint32_t idesc = tc_idesc_bf16(kTileM, kTileN);
+            const uint32_t idesc = tc_idesc_bf16(kTileM, TN);
             for (int i = 0; i < nk && ok; ++i) {
                 const int sl = i % kPL, sb = i % kPB;
                 if constexpr (NVFP4)
@@ -189,7 +199,7 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_const
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint8_t* at = smem + L::load + (size_t)sl * L::stage;
-                const uint8_t* bt = NVFP4 ? smem + L::btile + (size_t)sb * kTileBytes : at + kTileBytes;
+                const uint8_t* bt = NVFP4 ? smem + L::btile + (size_t)sb * L::bt : at + kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kStepK / 16; ++kk)
                     tc_mma_bf16(tmem, tc_smem_desc_sw128(at + 32 * kk), tc_smem_desc_sw128(bt + 32 * kk), idesc,
@@ -201,24 +211,28 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_const
         }
     } else if constexpr (NVFP4) {
         // ---------------- dequantise (warps 0-7) ----------------
-        const int r = tid & 127, hb = tid >> 7;  // half row of B owned by this thread
+        // half rows u = tid, tid + 256, ...: row u % TN, half u / TN
         for (int i = 0; i < nk && ok; ++i) {
             const int sl = i % kPL, sb = i % kPB;
             ok = mbar_wait_bounded(fullL + sl, (i / kPL) & 1, a.status, kStatusTimeoutPrefill);
             if (ok && i >= kPB) ok = mbar_wait_bounded(emptyB + sb, ((i / kPB) - 1) & 1, a.status, kStatusTimeoutPrefill);
             if (!ok) break;
             const uint8_t* st = smem + L::load + (size_t)sl * L::stage + kTileBytes;
-            const uint4 cw = *reinterpret_cast<const uint4*>(st + 32 * r + 16 * hb);
-            const uint32_t sc = *reinterpret_cast<const uint32_t*>(st + kTileN * 32 + 16 * r + (((i * kStepK) / 16) & 15));
-            uint8_t* bt = smem + L::btile + (size_t)sb * kTileBytes;
-            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+            uint8_t* bt = smem + L::btile + (size_t)sb * L::bt;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int kc = 4 * hb + c;
-                const uint32_t sbyte = (sc >> (8 * (kc >> 1))) & 0x7Fu;
-                uint32_t s2;
-                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"((uint16_t)(sbyte | (sbyte << 8))));
-                *reinterpret_cast<uint4*>(bt + tc_sw128_offset(r, 8 * kc)) = dequant8(words[c], s2);
+            for (int u = tid; u < 2 * TN; u += kPW) {
+                const int r = u & (TN - 1), hb = u / TN;
+                const uint4 cw = *reinterpret_cast<const uint4*>(st + 32 * r + 16 * hb);
+                const uint32_t sc = *reinterpret_cast<const uint32_t*>(st + TN * 32 + 16 * r + (((i * kStepK) / 16) & 15));
+                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int kc = 4 * hb + c;
+                    const uint32_t sbyte = (sc >> (8 * (kc >> 1))) & 0x7Fu;
+                    uint32_t s2;
+                    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"((uint16_t)(sbyte | (sbyte << 8))));
+                    *reinterpret_cast<uint4*>(bt + tc_sw128_offset(r, 8 * kc)) = dequant8(words[c], s2);
+                }
             }
             fence_proxy_async_smem();
             mbar_arrive(fullB + sb);
@@ -237,10 +251,10 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_const
             if (EPI == kEpiSwiglu) {
                 const float tsg = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride) : 1.f;
                 const float tsu = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride + 1) : 1.f;
-                for (int c = 32 * half; c < 32 * half + 32; c += 16) {
+                for (int c = half * (TN / 4); c < (half + 1) * (TN / 4); c += 16) {
                     uint32_t gv[16], uv[16];
                     tmem_ld16(tl + c, gv);
-                    tmem_ld16(tl + 64 + c, uv);
+                    tmem_ld16(tl + TN / 2 + c, uv);
                     tmem_ld_wait();
                     uint32_t o[8];
 #pragma unroll
@@ -255,21 +269,21 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_const
                         o[i] = (uint32_t)f32_to_bf16_bits(h2[0]) | ((uint32_t)f32_to_bf16_bits(h2[1]) << 16);
                     }
                     if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + (size_t)p * a.ldo + nt * 64 + c);
+                        uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + (size_t)p * a.ldo + nt * (TN / 2) + c);
                         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
                         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
                     }
                 }
             } else {
                 const float ts = (EPI == kEpiScale && a.ts) ? ld_cg(a.ts + (size_t)g * a.ts_stride + 2) : 1.f;
-                for (int c = 64 * half; c < 64 * half + 64; c += 16) {
+                for (int c = half * (TN / 2); c < (half + 1) * (TN / 2); c += 16) {
                     uint32_t v[16];
                     tmem_ld16(tl + c, v);
                     tmem_ld_wait();
                     if (!valid) continue;
                     if (EPI == kEpiLogits) {
-                        if (a.n_valid && nt * kTileN + c >= a.n_valid) continue;  // n_valid % 16 == 0
-                        float4* dst = reinterpret_cast<float4*>(a.out_f32 + (size_t)p * a.ldo + nt * kTileN + c);
+                        if (a.n_valid && nt * TN + c >= a.n_valid) continue;  // n_valid % 16 == 0
+                        float4* dst = reinterpret_cast<float4*>(a.out_f32 + (size_t)p * a.ldo + nt * TN + c);
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
@@ -280,7 +294,7 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_const
                         for (int i = 0; i < 8; ++i)
                             o[i] = (uint32_t)f32_to_bf16_bits(ts * __uint_as_float(v[2 * i])) |
                                    ((uint32_t)f32_to_bf16_bits(ts * __uint_as_float(v[2 * i + 1])) << 16);
-                        uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + (size_t)p * a.ldo + nt * kTileN + c);
+                        uint4* dst = reinterpret_cast<uint4*>(a.out_bf16 + (size_t)p * a.ldo + nt * TN + c);
                         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
                         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
                     }
@@ -290,7 +304,7 @@ __global__ void __launch_bounds__(kPT, 2) prefill_gemm_kernel(const __grid_const
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 9) tmem_dealloc(tmem, kTileN);
+    if (warp == 9) tmem_dealloc(tmem, TN);
 }
 
 // ---------------------------------------------------------------------------
@@ -476,11 +490,11 @@ cudaError_t map_a(CUtensorMap* m, const uint16_t* A, uint64_t rows, uint64_t K) 
 }
 
 // One grouped GEMM launch: the A map, the B map(s) and the kernel.
-template <bool NVFP4, int EPI>
+template <bool NVFP4, int EPI, int TN>
 cudaError_t launch_gemm(const PrefillGemmArgs& a, uint64_t a_rows, uint64_t b_rows, const DevInfo& d, int m_tiles,
                         int n_tiles, cudaStream_t s) {
     static int configured_for = -1;
-    cudaError_t e = configure_smem(prefill_gemm_kernel<NVFP4, EPI>, d, configured_for);
+    cudaError_t e = configure_smem(prefill_gemm_kernel<NVFP4, EPI, TN>, d, configured_for);
     if (e != cudaSuccess) return e;
     if (m_tiles <= 0 || n_tiles <= 0) return cudaSuccess;
     CUtensorMap ta, tb, ts;
@@ -495,16 +509,16 @@ cudaError_t launch_gemm(const PrefillGemmArgs& a, uint64_t a_rows, uint64_t b_ro
             return e;
     } else {
         if ((e = tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.B, b_rows, (uint64_t)a.K, (uint64_t)a.ldb, kStepK,
-                            kTileN, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+                            TN, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
         ts = tb;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)m_tiles);
     cfg.blockDim = dim3(kPT);
-    cfg.dynamicSmemBytes = TmaSmem<NVFP4>::total;
+    cfg.dynamicSmemBytes = TmaSmem<NVFP4, TN>::total;
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<NVFP4, EPI>, ta, tb, ts, a);
+    return cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<NVFP4, EPI, TN>, ta, tb, ts, a);
 }
 
 }  // namespace
@@ -569,7 +583,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     r.out_f32 = logits;
     r.ldo = E;
     r.status = status;
-    if ((e = launch_gemm<false, kEpiLogits>(r, T, E, d, mt_all, (E + kTileN - 1) / kTileN, s)) != cudaSuccess) return e;
+    if ((e = launch_gemm<false, kEpiLogits, 128>(r, T, E, d, mt_all, (E + 127) / 128, s)) != cudaSuccess) return e;
     // 2. top-k per token
     prefill_topk_kernel<<<(T + 7) / 8, 256, sizeof(uint32_t) * 8 * E, s>>>(logits, p.bias, T, E, k, p.ids, p.weights);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -608,7 +622,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     g.out_bf16 = h;
     g.ldo = I;
     g.status = status;
-    if ((e = launch_gemm<true, kEpiSwiglu>(g, (uint64_t)T * k, (uint64_t)E * 2 * I, d, mt_routed, I / 64, s)) != cudaSuccess)
+    if ((e = launch_gemm<true, kEpiSwiglu, kNTile>(g, (uint64_t)T * k, (uint64_t)E * 2 * I, d, mt_routed, I / (kNTile / 2), s)) != cudaSuccess)
         return e;
     if (p.s_gu) {
         PrefillGemmArgs gs = {};
@@ -623,7 +637,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
         gs.out_bf16 = hs;
         gs.ldo = Is;
         gs.status = status;
-        if ((e = launch_gemm<true, kEpiSwiglu>(gs, T, 2 * (uint64_t)Is, d, mt_all, Is / 64, s)) != cudaSuccess) return e;
+        if ((e = launch_gemm<true, kEpiSwiglu, kNTile>(gs, T, 2 * (uint64_t)Is, d, mt_all, Is / (kNTile / 2), s)) != cudaSuccess) return e;
     }
     // 5. down
     PrefillGemmArgs dn = {};
@@ -642,7 +656,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     dn.out_bf16 = dd;
     dn.ldo = H;
     dn.status = status;
-    if ((e = launch_gemm<true, kEpiScale>(dn, (uint64_t)T * k, (uint64_t)E * H, d, mt_routed, H / kTileN, s)) !=
+    if ((e = launch_gemm<true, kEpiScale, kNTile>(dn, (uint64_t)T * k, (uint64_t)E * H, d, mt_routed, H / kNTile, s)) !=
         cudaSuccess)
         return e;
     if (p.s_down) {
@@ -657,7 +671,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
         dsa.out_bf16 = ds;
         dsa.ldo = H;
         dsa.status = status;
-        if ((e = launch_gemm<true, kEpiScale>(dsa, T, H, d, mt_all, H / kTileN, s)) != cudaSuccess) return e;
+        if ((e = launch_gemm<true, kEpiScale, kNTile>(dsa, T, H, d, mt_all, H / kNTile, s)) != cudaSuccess) return e;
     }
     // 6. combine
     prefill_combine_kernel<<<T, 256, 0, s>>>(p.weights, inv, k, dd, p.s_down ? ds : nullptr, H, p.y);
