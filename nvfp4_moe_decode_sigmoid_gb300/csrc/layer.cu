@@ -237,14 +237,18 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         float* resu = reinterpret_cast<float*>(smem + L.resu);
         const int NSW = a.ns3;
         uint8_t* ring = smem + L.ring3 + (size_t)warp * NSW * 2 * RS;
+        // The routed pairs in list order (pair q = d I + p: row p of expert
+        // dlist[d]) are dealt out round-robin: CTA c takes pairs c, c + G, ...
+        // (its local items 0, 1, ...) and its warp w the local items w, w + kLW,
+        // .... An expert that several tokens chose costs more per pair, and
+        // dealing spreads its rows evenly over the CTAs and warps; contiguous
+        // ranges left a few CTAs ~1.5x the mean work at T = 8, and the grid
+        // barrier after this phase waits for the slowest.
         const int RP = D * I;
-        const int rp0 = (int)((unsigned)c * (unsigned)RP / (unsigned)G);
-        const int nl = (int)((unsigned)(c + 1) * (unsigned)RP / (unsigned)G) - rp0;
-        const int lw0 = (int)((unsigned)warp * (unsigned)nl / (unsigned)kLW);
-        const int lw1 = (int)((unsigned)(warp + 1) * (unsigned)nl / (unsigned)kLW);
-        const int n_items_w = lw1 - lw0;
-        auto issue = [&](int m) {  // routed list item lw0 + m into slot m % NSW
-            const int q = rp0 + lw0 + m, d = q / I, p = q - d * I;
+        const int nl = c < RP ? (RP - c + G - 1) / G : 0;
+        const int n_items_w = nl > warp ? (nl - warp + kLW - 1) / kLW : 0;
+        auto issue = [&](int m) {  // local item warp + m kLW into slot m % NSW
+            const int q = c + (warp + m * kLW) * G, d = q / I, p = q - d * I;
             const uint8_t* g = a.gu + ((size_t)ri.dlist[d] * 2 * I + p) * RS;
             uint8_t* slot = ring + (size_t)(m % NSW) * 2 * RS;
             warp_copy_async(slot, g, RS, lane);
@@ -283,21 +287,12 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                                       resu + i * T);
             }
         }
-        int d = 0, p = 0;
-        if (n_items_w > 0) {
-            d = (rp0 + lw0) / I;
-            p = rp0 + lw0 - d * I;
-        }
         for (int m = 0; m < n_items_w; ++m) {
             cp_async_wait_n(NSW - 1);
             __syncwarp();
             const uint8_t* grow = ring + (size_t)(m % NSW) * 2 * RS;
-            const int item = n_sh + lw0 + m;
+            const int li = warp + m * kLW, item = n_sh + li, d = (c + li * G) / I;
             gate_up_item<true>(grow, grow + RS, H, xh, csc, ri.tmask[d], lane, resg + item * T, resu + item * T);
-            if (++p == I) {
-                p = 0;
-                ++d;
-            }
             __syncwarp();
             if (m + NSW < n_items_w)
                 issue(m + NSW);
@@ -317,7 +312,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 tsg = sm.tss[2 * D];
                 tsu = sm.tss[2 * D + 1];
             } else {
-                const int q = rp0 + i - n_sh, dd = q / I;
+                const int q = c + (i - n_sh) * G, dd = q / I;
                 pp = q - dd * I;
                 ranks = rank_bits(ri.dmask[dd], t);
                 if (!ranks) continue;
