@@ -270,34 +270,41 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         }
         if (tid < 2 * D + 2) sm.tss[tid] = tsv;
         if (tid >= 256 && tid <= 256 + D) sm.tsd[tid - 256] = tdv;
-        // shared-expert pairs (resident), one unit per (pair, two tokens), spread
-        // over the warps from the last one: every token reads every shared row,
-        // so at T = 8 this is four times the work of a routed pair
-        const int ntp = (T + 1) >> 1;
-        for (int q = kLW - 1 - warp; q < n_sh * ntp; q += kLW) {
-            const int i = q / ntp, t0 = 2 * (q - i * ntp);
-            const uint8_t* grow = shgu + (size_t)i * RS;
-            if (t0 + 1 < T) {
-                const int tk[2] = {t0, t0 + 1};
-                gate_up_pass<true, 2>(grow, grow + (size_t)a.shp * RS, H, xh, csc, tk, lane, resg + i * T,
-                                      resu + i * T);
+        // The warp's work, in one loop so that the pass code is inlined once:
+        // first its shared-expert units (resident; one per (pair, two tokens),
+        // spread over the warps from the last one: every token reads every
+        // shared row, so at T = 8 a shared pair is four units), then its routed
+        // items from the ring.
+        const int ntp = (T + 1) >> 1, su0 = kLW - 1 - warp;
+        const int n_su_w = su0 < n_sh * ntp ? (n_sh * ntp - su0 + kLW - 1) / kLW : 0;
+        for (int it = 0; it < n_su_w + n_items_w; ++it) {
+            const int m = it - n_su_w;
+            const uint8_t *grow, *urow;
+            uint32_t tm;
+            int slot;  // row of resg / resu
+            if (m < 0) {
+                const int q = su0 + it * kLW, i = q / ntp, t0 = 2 * (q - i * ntp);
+                grow = shgu + (size_t)i * RS;
+                urow = grow + (size_t)a.shp * RS;
+                tm = (t0 + 1 < T ? 3u : 1u) << t0;  // t0 alone at an odd T
+                slot = i;
             } else {
-                const int tk[1] = {t0};
-                gate_up_pass<true, 1>(grow, grow + (size_t)a.shp * RS, H, xh, csc, tk, lane, resg + i * T,
-                                      resu + i * T);
+                cp_async_wait_n(NSW - 1);
+                __syncwarp();
+                grow = ring + (size_t)(m % NSW) * 2 * RS;
+                urow = grow + RS;
+                const int li = warp + m * kLW;
+                tm = ri.tmask[(c + li * G) / I];
+                slot = n_sh + li;
             }
-        }
-        for (int m = 0; m < n_items_w; ++m) {
-            cp_async_wait_n(NSW - 1);
-            __syncwarp();
-            const uint8_t* grow = ring + (size_t)(m % NSW) * 2 * RS;
-            const int li = warp + m * kLW, item = n_sh + li, d = (c + li * G) / I;
-            gate_up_item<true>(grow, grow + RS, H, xh, csc, ri.tmask[d], lane, resg + item * T, resu + item * T);
-            __syncwarp();
-            if (m + NSW < n_items_w)
-                issue(m + NSW);
-            else
-                cp_async_commit();
+            gate_up_item<true>(grow, urow, H, xh, csc, tm, lane, resg + slot * T, resu + slot * T);
+            if (m >= 0) {
+                __syncwarp();
+                if (m + NSW < n_items_w)
+                    issue(m + NSW);
+                else
+                    cp_async_commit();
+            }
         }
         cp_async_wait<0>();
         __syncthreads();
@@ -363,11 +370,10 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         });
         __syncthreads();
         // One task: rows [r0g, r1g) of unit u (u < D routed, from `rows`; u == D shared).
-        auto task = [&](int u, int r0g, int r1g, const uint8_t* rows) {
+        auto task = [&](int u, int r0g, int r1g, const uint8_t* rows, uint32_t rest) {
             const bool sh = u >= D;
             const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
             const unsigned long long dm = sh ? 0ull : ri.dmask[u];
-            uint32_t rest = sh ? (1u << T) - 1u : ri.tmask[u];
             const float tsd = sm.tsd[u];
             auto vec = [&](int t, const uint4*& h, const float*& cs) {
                 if (sh) {
@@ -420,52 +426,52 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 }
             }
         };
-        // the shared expert's rows (resident), one unit per (8 rows, two tokens),
-        // spread over the warps from the last one
-        if (has_sh) {
-            const int ng8 = (nr + 7) >> 3, ntp = (T + 1) >> 1;
-            for (int q = kLW - 1 - warp; q < ng8 * ntp; q += kLW) {
-                const int g = q / ntp, t0 = 2 * (q - g * ntp), r0g = 8 * g;
-                const uint8_t* rows = shdn + (size_t)r0g * RSs;
-                const float tsd = sm.tsd[D];
-                const uint4* hv[2] = {hs + (size_t)t0 * (Is / 8), hs + (size_t)min(t0 + 1, T - 1) * (Is / 8)};
-                const float* cv[2] = {css + (size_t)t0 * (Is / 32), css + (size_t)min(t0 + 1, T - 1) * (Is / 32)};
-                if (t0 + 1 < T) {
-                    float acc[16];
-                    down_pass<8, 2>(rows, RSs, nr - r0g, Is, hv, cv, lane, acc);
-                    const float v = reduce_scatter<16>(acc, lane);
-                    const int idx = rs_index<16>(lane), r = r0g + (idx & 7);
-                    if ((lane & 1) == 0 && r < nr)
-                        dval[((size_t)(t0 + (idx >> 3)) * (k + 1) + k) * RM + r] = bf16_round_f32(tsd * v);
-                } else {
-                    const uint4* hv1[1] = {hv[0]};
-                    const float* cv1[1] = {cv[0]};
-                    float acc[8];
-                    down_pass<8, 1>(rows, RSs, nr - r0g, Is, hv1, cv1, lane, acc);
-                    const float v = reduce_scatter<8>(acc, lane);
-                    const int r = r0g + rs_index<8>(lane);
-                    if ((lane & 3) == 0 && r < nr) dval[((size_t)t0 * (k + 1) + k) * RM + r] = bf16_round_f32(tsd * v);
-                }
-            }
-        }
         if (a.dpre) {  // every routed group is resident once the prefetch lands
             const bool ok = mbar_wait_bounded(&sm.dbar, 0, tid == 0 ? a.status : nullptr, kStatusTimeoutLayer);
             if (!__syncthreads_and(ok)) return;
-            for (int q = warp; q < n_tasks; q += kLW) {
-                const int u = q / ngr, g = q - u * ngr;
-                task(u, g * RG, min(nr, (g + 1) * RG), dpre + ((size_t)u * nr + (size_t)g * RG) * RSr);
-            }
         }
-        for (int kk = 0; kk < my_tasks; ++kk) {
-            cp_async_wait_n(NSW - 1);
-            __syncwarp();
-            const int q = warp + kk * kLW, u = q / ngr, r0g = (q - u * ngr) * RG;
-            task(u, r0g, min(nr, r0g + RG), ring + (size_t)(kk % NSW) * a.slot4);
-            __syncwarp();
-            if (kk + NSW < my_tasks)
-                issue(kk + NSW);
-            else
-                cp_async_commit();
+        // The warp's work, in one loop so that the task's code is inlined once:
+        // first its units of the shared expert's rows (resident; one per (8
+        // rows, two tokens), spread over the warps from the last one), then its
+        // routed tasks warp, warp + kLW, ... (rows from the prefetch, else from
+        // the ring).
+        const int ng8 = has_sh ? (nr + 7) >> 3 : 0, ntp = (T + 1) >> 1, su0 = kLW - 1 - warp;
+        const int n_su_w = su0 < ng8 * ntp ? (ng8 * ntp - su0 + kLW - 1) / kLW : 0;
+        const int n_mine = n_tasks > warp ? (n_tasks - warp + kLW - 1) / kLW : 0;
+        for (int it = 0; it < n_su_w + n_mine; ++it) {
+            const int kk = it - n_su_w;
+            int u, r0g, r1g;
+            const uint8_t* rows;
+            uint32_t tm;
+            if (kk < 0) {
+                const int q = su0 + it * kLW, g = q / ntp, t0 = 2 * (q - g * ntp);
+                u = D;
+                r0g = 8 * g;
+                r1g = min(nr, r0g + 8);
+                rows = shdn + (size_t)r0g * RSs;
+                tm = (t0 + 1 < T ? 3u : 1u) << t0;
+            } else {
+                const int q = warp + kk * kLW;
+                u = q / ngr;
+                r0g = (q - u * ngr) * RG;
+                r1g = min(nr, r0g + RG);
+                if (a.dpre) {
+                    rows = dpre + ((size_t)u * nr + (size_t)r0g) * RSr;
+                } else {
+                    cp_async_wait_n(NSW - 1);
+                    __syncwarp();
+                    rows = ring + (size_t)(kk % NSW) * a.slot4;
+                }
+                tm = ri.tmask[u];
+            }
+            task(u, r0g, r1g, rows, tm);
+            if (kk >= 0 && !a.dpre) {
+                __syncwarp();
+                if (kk + NSW < n_mine)
+                    issue(kk + NSW);
+                else
+                    cp_async_commit();
+            }
         }
         cp_async_wait<0>();
         __syncthreads();
