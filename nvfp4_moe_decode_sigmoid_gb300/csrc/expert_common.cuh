@@ -141,21 +141,24 @@ struct StageSrc {
     int nvec, K;
 };
 
-// Chunk q of the concatenated sources: its source and offset; false past the end.
+// Chunk q of the concatenated sources: its source (copied out field by field
+// with constant indices, so that the sources stay in registers) and offset;
+// false past the end.
 template <int NS>
-__device__ __forceinline__ bool stage_locate(const StageSrc (&ss)[NS], int q, int& s, int& v, int& c) {
+__device__ __forceinline__ bool stage_locate(const StageSrc (&ss)[NS], int q, StageSrc& src, int& v, int& c) {
+    bool found = false;
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
         const int cpv = ss[i].K / 32, n = ss[i].nvec * cpv;
-        if (q < n) {
-            s = i;
+        if (!found && q < n) {
+            src = ss[i];
             v = q / cpv;
             c = q - v * cpv;
-            return true;
+            found = true;
         }
         q -= n;
     }
-    return false;
+    return found;
 }
 
 __device__ __forceinline__ void stage_load(const StageSrc& ss, int v, int c, uint4 (&w)[4]) {
@@ -204,20 +207,32 @@ __device__ __forceinline__ void stage_store(const StageSrc& ss, int v, int c, co
 template <bool DOWN_ORDER, int NS, typename F>
 __device__ __forceinline__ void stage_f16(const StageSrc (&ss)[NS], F&& between) {
     constexpr int AHEAD = DOWN_ORDER ? 2 : 1;  // chunks loaded ahead of `between` (h: up to two per thread)
-    int s0 = 0, v0 = 0, c0 = 0, s1 = 0, v1 = 0, c1 = 0;
+    const int nt = (int)blockDim.x;
+    StageSrc s0 = ss[0], s1 = ss[0];
+    int v0 = 0, c0 = 0, v1 = 0, c1 = 0;
     uint4 w[4], w1[4];
-    const bool have = stage_locate(ss, threadIdx.x, s0, v0, c0);
-    const bool have1 = AHEAD > 1 && stage_locate(ss, threadIdx.x + (int)blockDim.x, s1, v1, c1);
-    if (have) stage_load(ss[s0], v0, c0, w);
-    if (have1) stage_load(ss[s1], v1, c1, w1);
+    bool have = stage_locate(ss, threadIdx.x, s0, v0, c0);
+    bool have1 = AHEAD > 1 && stage_locate(ss, threadIdx.x + nt, s1, v1, c1);
+    if (have) stage_load(s0, v0, c0, w);
+    if (have1) stage_load(s1, v1, c1, w1);
     between();
-    if (have) stage_store<DOWN_ORDER>(ss[s0], v0, c0, w);
-    if (have1) stage_store<DOWN_ORDER>(ss[s1], v1, c1, w1);
-    for (int q = threadIdx.x + AHEAD * (int)blockDim.x;; q += (int)blockDim.x) {
-        int s, v, c;
-        if (!stage_locate(ss, q, s, v, c)) break;
-        stage_load(ss[s], v, c, w);
-        stage_store<DOWN_ORDER>(ss[s], v, c, w);
+    // one conversion site; the next chunk is loaded while the current one is
+    // converted
+    for (int q = threadIdx.x + AHEAD * nt; have; q += nt) {
+        stage_store<DOWN_ORDER>(s0, v0, c0, w);
+        if (AHEAD > 1) {
+            have = have1;
+            s0 = s1;
+            v0 = v1;
+            c0 = c1;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = w1[i];
+            have1 = stage_locate(ss, q, s1, v1, c1);
+            if (have1) stage_load(s1, v1, c1, w1);
+        } else {
+            have = stage_locate(ss, q, s0, v0, c0);
+            if (have) stage_load(s0, v0, c0, w);
+        }
     }
 }
 

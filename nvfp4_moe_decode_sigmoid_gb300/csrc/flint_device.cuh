@@ -169,13 +169,23 @@ __device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t* p, uint32_t v
     return old;
 }
 
-__device__ __forceinline__ bool grid_sync(uint32_t* ticket, uint32_t* status, uint32_t code) {
-    __shared__ int s_ok;
+// The barrier in two halves, so that a CTA can do work that needs nothing
+// from the other CTAs between its arrival and its wait. grid_arrive returns
+// the ticket target (meaningful in thread 0 only).
+__device__ __forceinline__ uint32_t grid_arrive(uint32_t* ticket) {
     __syncthreads();
+    uint32_t target = 0;
+    if (threadIdx.x == 0) {
+        const uint32_t t = atom_add_release_gpu(ticket, 1u);
+        target = (t / gridDim.x + 1u) * gridDim.x;
+    }
+    return target;
+}
+
+__device__ __forceinline__ bool grid_wait(uint32_t* ticket, uint32_t target, uint32_t* status, uint32_t code) {
+    __shared__ int s_ok;
     if (threadIdx.x == 0) {
         int ok = 1;
-        const uint32_t t = atom_add_release_gpu(ticket, 1u);
-        const uint32_t target = (t / gridDim.x + 1u) * gridDim.x;
         if ((int)(ld_acquire_gpu(ticket) - target) < 0) {
             const uint64_t t0 = globaltimer_ns();
             while ((int)(ld_acquire_gpu(ticket) - target) < 0) {
@@ -190,6 +200,10 @@ __device__ __forceinline__ bool grid_sync(uint32_t* ticket, uint32_t* status, ui
     }
     __syncthreads();
     return s_ok != 0;
+}
+
+__device__ __forceinline__ bool grid_sync(uint32_t* ticket, uint32_t* status, uint32_t code) {
+    return grid_wait(ticket, grid_arrive(ticket), status, code);
 }
 
 // ---------------------------------------------------------------------------

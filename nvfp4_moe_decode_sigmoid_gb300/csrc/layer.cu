@@ -337,10 +337,34 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             }
         }
     }
-    if (!grid_sync(a.bar_ticket, a.status, kStatusTimeoutLayer)) return;
-    pdl_launch_dependents();
-
     // ---- 4: down + combine ---------------------------------------------------------
+    // The down rows depend on the routing only. This CTA's first ring copies
+    // are issued between its arrival at the grid barrier and its wait (the
+    // regions of phases 0-3 are dead once the epilogue is done), so that their
+    // latency overlaps the barrier.
+    const int NSW = a.ns4, RG = a.rg;
+    uint8_t* ring = smem + L.ring4 + (size_t)warp * NSW * a.slot4;
+    const int ngr = (nr + RG - 1) / RG;
+    const int n_tasks = D * ngr;  // routed; the shared expert's groups are resident
+    const int my_tasks = a.dpre ? 0 : (n_tasks > warp ? (n_tasks - warp + kLW - 1) / kLW : 0);
+    auto issue = [&](int kk) {
+        const int q = warp + kk * kLW, u = q / ngr, r0g = (q - u * ngr) * RG, r1g = min(nr, r0g + RG);
+        uint8_t* dst = ring + (size_t)(kk % NSW) * a.slot4;
+        warp_copy_async(dst, a.down + ((size_t)ri.dlist[u] * H + n0 + r0g) * RSr, (r1g - r0g) * RSr, lane);
+        cp_async_commit();
+    };
+    const uint32_t target = grid_arrive(a.bar_ticket);
+    for (int kk = 0; kk < NSW; ++kk) {
+        if (kk < my_tasks)
+            issue(kk);
+        else
+            cp_async_commit();
+    }
+    if (!grid_wait(a.bar_ticket, target, a.status, kStatusTimeoutLayer)) {
+        cp_async_wait<0>();
+        return;
+    }
+    pdl_launch_dependents();
     if (nr == 0) return;
     {
         uint4* hr = reinterpret_cast<uint4*>(smem + L.hr);
@@ -348,26 +372,8 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         float* csr = reinterpret_cast<float*>(smem + L.csr);
         float* css = reinterpret_cast<float*>(smem + L.css);
         float* dval = reinterpret_cast<float*>(smem + L.dval);
-        const int NSW = a.ns4, RG = a.rg;
-        uint8_t* ring = smem + L.ring4 + (size_t)warp * NSW * a.slot4;
-        const int ngr = (nr + RG - 1) / RG;
-        const int n_tasks = D * ngr;  // routed; the shared expert's groups are resident
-        const int my_tasks = a.dpre ? 0 : (n_tasks > warp ? (n_tasks - warp + kLW - 1) / kLW : 0);
-        auto issue = [&](int kk) {
-            const int q = warp + kk * kLW, u = q / ngr, r0g = (q - u * ngr) * RG, r1g = min(nr, r0g + RG);
-            uint8_t* dst = ring + (size_t)(kk % NSW) * a.slot4;
-            warp_copy_async(dst, a.down + ((size_t)ri.dlist[u] * H + n0 + r0g) * RSr, (r1g - r0g) * RSr, lane);
-            cp_async_commit();
-        };
         const StageSrc hsrc[2] = {{a.h_routed, hr, csr, T * k, I}, {a.h_shared, hs, css, has_sh ? T : 0, Is ? Is : 32}};
-        stage_f16<true>(hsrc, [&] {
-            for (int kk = 0; kk < NSW; ++kk) {
-                if (kk < my_tasks)
-                    issue(kk);
-                else
-                    cp_async_commit();
-            }
-        });
+        stage_f16<true>(hsrc, [] {});
         __syncthreads();
         // One task: rows [r0g, r1g) of unit u (u < D routed, from `rows`; u == D shared).
         auto task = [&](int u, int r0g, int r1g, const uint8_t* rows, uint32_t rest) {
