@@ -150,7 +150,7 @@ struct LayerArgs {
     int k;
     int32_t* ids;        // [T][k] out
     float* weights;      // [T][k] out
-    float* logits;       // workspace [8][E]
+    float* logits;       // workspace [8][E]: the sigmoid scores (bits) of the router logits
     uint32_t* bar_ticket; // workspace word 2: grid barrier tickets (a multiple of the grid size between calls)
     uint32_t* status;    // workspace word 1
     const uint8_t* gu;   // routed E x [2I, H]

@@ -18,10 +18,10 @@
 //      every CTA first computes x = rmsnorm(r + y_prev) itself from the
 //      residual stream and writes its share of the new residual out. The
 //      CTA's router logits are computed in FP32 from the staged x and bf16
-//      router rows and written to the workspace. Grid barrier.
-//   2. Every CTA reads all logits and selects the top-k of every token itself
-//      (one warp per token), so no second barrier is needed to share the
-//      routing; CTA 0 also writes ids and weights out.
+//      router rows; their sigmoid scores go to the workspace. Grid barrier.
+//   2. Every CTA reads all scores and selects the top-k of every token itself
+//      (one warp per token, straight from L2), so no second barrier is needed
+//      to share the routing; CTA 0 also writes ids and weights out.
 //   3. gate/up + SiLU as in gate_up_kernel: the CTA's share of the routed
 //      pairs through per-warp cp.async rings, its shared-expert pairs from
 //      shared memory; h goes to the workspace. Grid barrier.
@@ -53,15 +53,15 @@ struct LayerSmall {
 //   persistent: routing view, small arrays, the shared expert's down rows;
 //   phases 0-3 (region U1): staged x and its chunk scales (and the norm's
 //     per-chunk sums of squares when the input is normalised here), the shared
-//     expert's gate/up pairs, then one of: router rows (phases 0-1), sigmoid
-//     scores (phase 2), raw gate/up sums + the gate/up rings (phase 3);
+//     expert's gate/up pairs, then one of: router rows (phases 0-1), raw
+//     gate/up sums + the gate/up rings (phase 3);
 //   phase 4 (region U4, over U1): staged h and its chunk scales, d values,
 //     the down rings;
 //   the prefetched down rows (a.dpre), beside both.
 struct LayerSmem {
     size_t ri, small, shdn, U;
     size_t xs, csc, nred, shgu, V;
-    size_t wrows, scores;
+    size_t wrows;
     size_t resg, resu, ring3;
     size_t hr, hs, csr, css, dval, ring4;
     size_t dpre;
@@ -83,14 +83,12 @@ __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     L.shgu = align_up(L.nred + (a.norm.r ? sizeof(float) * T * (H / 32) : 0), 128);
     L.V = align_up(L.shgu + 2 * (size_t)a.shp * RS, 128);
     L.wrows = L.V;
-    L.scores = L.V;
     L.resg = L.V;
     L.resu = align_up(L.resg + sizeof(float) * (size_t)a.res_items * T, 128);
     L.ring3 = align_up(L.resu + sizeof(float) * (size_t)a.res_items * T, 128);
     size_t end1 = L.ring3 + (size_t)kLW * a.ns3 * 2 * RS;
-    const size_t e_rows = L.wrows + 2 * (size_t)a.rpc * H, e_scores = L.scores + sizeof(uint32_t) * T * a.E;
+    const size_t e_rows = L.wrows + 2 * (size_t)a.rpc * H;
     if (end1 < e_rows) end1 = e_rows;
-    if (end1 < e_scores) end1 = e_scores;
     // U4
     L.hr = L.U;
     L.hs = align_up(L.hr + 2 * T * a.k * a.I, 128);
@@ -160,7 +158,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 
     pdl_wait();  // x comes from the previous kernel
 
-    // ---- 1: stage x (or the norm of the residual stream); this CTA's router logits --
+    // ---- 1: stage x (or the norm of the residual stream); this CTA's router scores --
     const StageSrc xsrc[1] = {{a.x, xh, csc, T, H}};
     if constexpr (NORM)
         stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), sm.ninv, c, G);
@@ -195,22 +193,20 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) a.logits[(size_t)t * E + r0 + r] = v;
+        // the sigmoid score (its bits), once per logit in the grid
+        if (lane == 0) reinterpret_cast<uint32_t*>(a.logits)[(size_t)t * E + r0 + r] = sigmoid_score(v, a.bias, r0 + r);
     }
     if (!grid_sync(a.bar_ticket, a.status, kStatusTimeoutLayer)) return;
 
     // ---- 2: top-k of every token, in every CTA ------------------------------------
     float* wsel = sm.w;
     {
-        uint32_t* scores = reinterpret_cast<uint32_t*>(smem + L.scores);
-        sigmoid_scores(a.logits, a.bias, T, E, scores);
-        __syncthreads();
         if (warp < T) {
-            const uint32_t* sc = scores + (size_t)warp * E;
+            const uint32_t* sc = reinterpret_cast<const uint32_t*>(a.logits) + (size_t)warp * E;
             if (E <= 256)
-                topk_warp<8>(sc, E, k, lane, sm.ids + warp * k, wsel + warp * k);
+                topk_warp<8, true>(sc, E, k, lane, sm.ids + warp * k, wsel + warp * k);
             else
-                topk_warp<FLINT_MAX_EXPERTS / 32>(sc, E, k, lane, sm.ids + warp * k, wsel + warp * k);
+                topk_warp<FLINT_MAX_EXPERTS / 32, true>(sc, E, k, lane, sm.ids + warp * k, wsel + warp * k);
         }
         __syncthreads();
     }

@@ -16,26 +16,31 @@ namespace {
 // time: sigmoid scores are positive floats, so the bits order like the
 // values. Logits come from global memory (written by other CTAs: read past
 // L1). Every thread of the CTA calls this; a __syncthreads must follow.
-__device__ __forceinline__ void sigmoid_scores(const float* logits, const float* bias, int T, int E,
-                                               uint32_t* scores) {
-    for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
-        float z = ld_cg(logits + i);
-        if (bias) z = z + bias[i % E];
-        scores[i] = __float_as_uint(1.f / (1.f + expf(-z)));
-    }
+__device__ __forceinline__ uint32_t sigmoid_score(float z, const float* bias, int e) {
+    if (bias) z = z + bias[e];
+    return __float_as_uint(1.f / (1.f + expf(-z)));
 }
 
-// Top-k of one token's scores (shared memory), one warp: lane holds experts
+__device__ __forceinline__ void sigmoid_scores(const float* logits, const float* bias, int T, int E,
+                                               uint32_t* scores) {
+    for (int i = threadIdx.x; i < T * E; i += blockDim.x) scores[i] = sigmoid_score(ld_cg(logits + i), bias, i % E);
+}
+
+// Top-k of one token's scores (shared memory; global memory written by other
+// CTAs when L2 is set: read past L1), one warp: lane holds experts
 // lane + 32 i. Each lane keeps its best untaken score; a round takes the warp
 // maximum, breaks ties toward the lowest expert index with a warp minimum,
 // and only the owning lane rescans its scores. Weights are the selected
 // scores over their sum.
-template <int SLOTS>
+template <int SLOTS, bool L2 = false>
 __device__ __forceinline__ void topk_warp(const uint32_t* sc, int E, int k, int lane, int32_t* ids,
                                           float* weights) {
     uint32_t s[SLOTS];
 #pragma unroll
-    for (int i = 0; i < SLOTS; ++i) s[i] = lane + 32 * i < E ? sc[lane + 32 * i] : 0u;
+    for (int i = 0; i < SLOTS; ++i) {
+        const int e = lane + 32 * i;
+        s[i] = e >= E ? 0u : L2 ? (uint32_t)ld_cg(reinterpret_cast<const int32_t*>(sc) + e) : sc[e];
+    }
     uint32_t valid = 0;  // bit i: slot i holds an untaken expert
 #pragma unroll
     for (int i = 0; i < SLOTS; ++i)
