@@ -42,6 +42,7 @@ constexpr int kLT = kLayerThreads;
 // of the shared expert; down scales of the units; combine weights; ids.
 struct LayerSmall {
     uint64_t dbar;  // completion of the prefetched down rows
+    uint64_t rbar[kLayerWarps * 4];  // the gate/up ring slots of each warp (up to 4)
     float tss[2 * kMaxDistinct + 2];
     float tsd[kMaxDistinct + 1];
     float w[kMaxDistinct];
@@ -151,10 +152,9 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     }
     cp_async_commit();
     if (tid < 2 * kMaxDistinct + 2) sm.tss[tid] = 0.f;
-    if (tid == 0) {
-        mbar_init(&sm.dbar, 1);
-        fence_mbar_init();
-    }
+    if (tid == 0) mbar_init(&sm.dbar, 1);
+    if (tid < kLW * 4) mbar_init(&sm.rbar[tid], 1);
+    if (tid <= kLW * 4) fence_mbar_init();
 
     pdl_wait();  // x comes from the previous kernel
 
@@ -243,13 +243,22 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         const int RP = D * I;
         const int nl = c < RP ? (RP - c + G - 1) / G : 0;
         const int n_items_w = nl > warp ? (nl - warp + kLW - 1) / kLW : 0;
+        // The ring is fed by bulk copies (the copy engine, one lane per warp):
+        // the gate and up rows of an item land in its slot and complete on the
+        // slot's mbarrier. Per-thread 16-byte copies went through the SM's load
+        // path, which kept the phase near 20 GB/s per SM.
+        uint64_t* rbar = sm.rbar + warp * 4;
         auto issue = [&](int m) {  // local item warp + m kLW into slot m % NSW
-            const int q = c + (warp + m * kLW) * G, d = q / I, p = q - d * I;
-            const uint8_t* g = a.gu + ((size_t)ri.dlist[d] * 2 * I + p) * RS;
-            uint8_t* slot = ring + (size_t)(m % NSW) * 2 * RS;
-            warp_copy_async(slot, g, RS, lane);
-            warp_copy_async(slot + RS, g + (size_t)I * RS, RS, lane);
-            cp_async_commit();
+            if (lane == 0) {
+                const int q = c + (warp + m * kLW) * G, d = q / I, p = q - d * I;
+                const uint8_t* g = a.gu + ((size_t)ri.dlist[d] * 2 * I + p) * RS;
+                uint8_t* slot = ring + (size_t)(m % NSW) * 2 * RS;
+                uint64_t* bar = rbar + m % NSW;
+                fence_proxy_async_smem();  // the slot's earlier reads come first
+                mbar_arrive_expect_tx(bar, 2u * (uint32_t)RS);
+                bulk_g2s(slot, g, (uint32_t)RS, bar);
+                bulk_g2s(slot + RS, g + (size_t)I * RS, (uint32_t)RS, bar);
+            }
         };
         // scales first, then this warp's first copies
         float tsv = 0.f;
@@ -258,12 +267,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         float tdv = 0.f;
         if (tid >= 256 && tid < 256 + D) tdv = ld_cg(a.ts + 3 * ri.dlist[tid - 256] + 2);
         else if (tid == 256 + D && has_sh) tdv = ld_cg(a.s_ts + 2);
-        for (int m = 0; m < NSW; ++m) {
-            if (m < n_items_w)
-                issue(m);
-            else
-                cp_async_commit();
-        }
+        for (int m = 0; m < NSW && m < n_items_w; ++m) issue(m);
         if (tid < 2 * D + 2) sm.tss[tid] = tsv;
         if (tid >= 256 && tid <= 256 + D) sm.tsd[tid - 256] = tdv;
         // The warp's work, in one loop so that the pass code is inlined once:
@@ -273,6 +277,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         // items from the ring.
         const int ntp = (T + 1) >> 1, su0 = kLW - 1 - warp;
         const int n_su_w = su0 < n_sh * ntp ? (n_sh * ntp - su0 + kLW - 1) / kLW : 0;
+        int m_fail = -1;  // the item whose copy never landed
         for (int it = 0; it < n_su_w + n_items_w; ++it) {
             const int m = it - n_su_w;
             const uint8_t *grow, *urow;
@@ -285,8 +290,11 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 tm = (t0 + 1 < T ? 3u : 1u) << t0;  // t0 alone at an odd T
                 slot = i;
             } else {
-                cp_async_wait_n(NSW - 1);
-                __syncwarp();
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(rbar + m % NSW, (uint32_t)(m / NSW) & 1u, a.status,
+                                                               kStatusTimeoutLayer))) {
+                    m_fail = m;
+                    break;
+                }
                 grow = ring + (size_t)(m % NSW) * 2 * RS;
                 urow = grow + RS;
                 const int li = warp + m * kLW;
@@ -294,16 +302,18 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 slot = n_sh + li;
             }
             gate_up_item<true>(grow, urow, H, xh, csc, tm, lane, resg + slot * T, resu + slot * T);
-            if (m >= 0) {
+            if (m >= 0 && m + NSW < n_items_w) {
                 __syncwarp();
-                if (m + NSW < n_items_w)
-                    issue(m + NSW);
-                else
-                    cp_async_commit();
+                issue(m + NSW);
             }
         }
-        cp_async_wait<0>();
-        __syncthreads();
+        if (__syncthreads_or(m_fail >= 0)) {
+            // a copy timed out: let this warp's copies still in flight land
+            // (bounded), then stop
+            for (int mm = max(m_fail, 0); m_fail >= 0 && mm < min(n_items_w, m_fail + NSW); ++mm)
+                mbar_wait_bounded(rbar + mm % NSW, (uint32_t)(mm / NSW) & 1u, nullptr, 0);
+            return;
+        }
         const int n_items = n_sh + nl;
         for (int e = tid; e < n_items * T; e += kLT) {
             const int t = e / n_items, i = e - t * n_items;
