@@ -245,8 +245,8 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         const int n_items_w = nl > warp ? (nl - warp + kLW - 1) / kLW : 0;
         // The ring is fed by bulk copies (the copy engine, one lane per warp):
         // the gate and up rows of an item land in its slot and complete on the
-        // slot's mbarrier. Per-thread 16-byte copies went through the SM's load
-        // path, which kept the phase near 20 GB/s per SM.
+        // slot's mbarrier. Against all 32 lanes issuing 16-byte cp.async this
+        // frees issue slots in a phase bound by instruction latency and issue.
         uint64_t* rbar = sm.rbar + warp * 4;
         auto issue = [&](int m) {  // local item warp + m kLW into slot m % NSW
             if (lane == 0) {
