@@ -1,6 +1,6 @@
 """Build libflint.so in-tree: hand-written CUDA for sm_103a behind the C ABI of
 include/flint.h. Translation units compile in parallel; nvcc links the CUDA
-runtime statically, so the library needs only the driver at run time."""
+runtime statically, so the library needs only the CUDA driver (libcuda) at run time."""
 import os
 import subprocess
 import sys
