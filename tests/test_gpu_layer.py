@@ -90,6 +90,14 @@ def test_full_layer_batch8_uniform(full_layer):
     _check(full_layer, x, 6)
 
 
+@pytest.mark.parametrize("T", [2, 3, 4, 6, 7])
+def test_full_layer_other_batches(full_layer, T):
+    """Batches around the switch from prefetched down rows (T <= 3) to the down
+    ring (T >= 4), with the routed gate/up pairs dealt over all CTAs."""
+    x = margin_x(synth.bits(full_layer.L.router_w), T, 2048, 6, None, seed=40 + T)
+    _check(full_layer, x, 6)
+
+
 def test_full_layer_batch8_zipf(full_layer):
     f = flint()
     bias = synth.zipf_bias(3, 256)
