@@ -26,6 +26,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -39,6 +41,7 @@ WORKLOADS = {
 }
 DEFAULT_WORKLOAD = "moe-layer-b8-uniform"
 METRIC = "NVFP4 MoE-layer decode achieved HBM GB/s (algorithmic bytes / layer time)"
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (context beside the measured copy bandwidth)
 
 
 def parse():
@@ -528,6 +531,7 @@ def measure_kernels(F, model, name, reps=8):
                 g.replay()
             e1.record(stream)
         torch.cuda.synchronize()
+        assert F.flint_workspace_check(model.ws) == F.FLINT_OK, F.flint_last_error()
         out[kname + "_us"] = e0.elapsed_time(e1) * 1e3 / (reps * nl)
     gu_b, dn_b = expert_bytes()
     distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
@@ -558,6 +562,7 @@ def measure_single_flushed(F, model, name, reps=7):
             e1.synchronize()
             if r > 0:
                 times.append(e0.elapsed_time(e1) * 1e3)
+    assert F.flint_workspace_check(model.ws) == F.FLINT_OK, F.flint_last_error()
     del flush
     torch.cuda.empty_cache()
     return statistics.median(times)
@@ -652,16 +657,27 @@ def measure_e2e(F, model, name, steps, graph_steps):
         torch.cuda.synchronize()
         return ev0.elapsed_time(ev1)
 
+    # The graphs run steps 0..R-1, i.e. layers s % nl; only those layers' y
+    # are written by the timed graph of every path (with R < nl the others
+    # keep what an earlier pass left), so only those are compared.
+    covered = sorted({s % nl for s in range(R)})
+
+    def check_ws():
+        assert F.flint_workspace_check(model.ws) == F.FLINT_OK, F.flint_last_error()
+
     ms_copy = timed(copy_step)
+    check_ws()
     ref_y = [h.clone() for h in hy]          # y of every layer through device buffers
-    same = lambda: all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(hy, ref_y))  # noqa: E731
+    same = lambda: all(torch.equal(hy[i].view(torch.int16), ref_y[i].view(torch.int16)) for i in covered)  # noqa: E731
     for h in hy:
         h.zero_()
     ms_zc = timed(zero_copy_step)
+    check_ws()
     zc_ok = same()
     for h in hy:
         h.zero_()
     ms_ov = timed_overlapped()
+    check_ws()
     ov_ok = same()
     distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
     n = reps * R
@@ -678,13 +694,17 @@ def measure_e2e(F, model, name, steps, graph_steps):
     return dict(value=total / (ms * 1e-3) / 1e9, unit="GB/s", h2d_bytes_per_step=T * H * 2,
                 d2h_bytes_per_step=T * H * 2, steps=n, us_per_step=ms * 1e3 / n, path=paths[best][2],
                 us_per_step_by_path={k: round(v[0] * 1e3 / n, 3) for k, v in paths.items()},
-                bit_identical_to_device_path={k: v[1] for k, v in paths.items()})
+                bit_identical_to_device_path={k: v[1] for k, v in paths.items()},
+                layers_compared=len(covered))
 
 
 def cpu_baseline(name, budget_s=20.0):
-    """The oracle, as it stands, single-threaded on this host, on a bounded
-    sample of the same workload: whole layers (router + all selected experts +
-    shared expert + combine) of the same recipe, drawn on the CPU."""
+    """The oracle, as it stands, on this host, on a bounded sample of the same
+    workload: whole layer steps (router + all selected experts + shared
+    expert + combine) of the same recipe on a CPU-drawn layer. Two legs on
+    the same inputs: the plain single-threaded build, and the same source
+    built with OpenMP (output rows split over all host threads; the same
+    bits). `value` is the OpenMP leg (the host's cores), when it exists."""
     import oracle
     from nvfp4_moe_decode_sigmoid_gb300 import synth
     T, routing = WORKLOADS[name]
@@ -693,19 +713,43 @@ def cpu_baseline(name, budget_s=20.0):
     sh = dict(gate=s["gate"].numpy(), up=s["up"].numpy(), down=s["down"].numpy(), ts=s["ts"].numpy(), I=I_SHARED)
     bias = synth.zipf_bias(7, E).numpy() if routing == "zipf" else None
     wr = synth.bits(L.router_w)
-    done, total_bytes, elapsed, rep = 0, 0, 0.0, 0
-    while elapsed < budget_s and done < 64:
-        x = synth.bits(synth.activations(5000 + rep, T, H))
-        t0 = time.perf_counter()
-        ids, _, _ = oracle.moe_layer(x, wr, TOPK, E, I, L.gate.numpy(), L.up.numpy(), L.down.numpy(), L.ts.numpy(),
-                                     shared=sh, bias=bias)
-        elapsed += time.perf_counter() - t0
-        total_bytes += step_bytes(len(set(ids.reshape(-1).tolist())), T, bias is not None)
-        done += 1
-        rep += 1
-    return dict(value=total_bytes / elapsed / 1e9, unit="GB/s", cores=1, kind="oracle",
-                sample=f"{done} whole layer steps of {name} (T={T}) on a CPU-drawn layer, {elapsed:.1f} s, "
-                       f"single thread", seconds=elapsed, steps=done)
+    host_cores = os.cpu_count() or 1
+
+    def leg(budget, max_steps):
+        done, total_bytes, elapsed = 0, 0, 0.0
+        outs = []
+        while elapsed < budget and done < max_steps:
+            x = synth.bits(synth.activations(5000 + done, T, H))
+            t0 = time.perf_counter()
+            ids, _, y = oracle.moe_layer(x, wr, TOPK, E, I, L.gate.numpy(), L.up.numpy(), L.down.numpy(),
+                                         L.ts.numpy(), shared=sh, bias=bias)
+            elapsed += time.perf_counter() - t0
+            total_bytes += step_bytes(len(set(ids.reshape(-1).tolist())), T, bias is not None)
+            outs.append(y)
+            done += 1
+        return total_bytes / elapsed / 1e9, done, elapsed, outs
+
+    st_value, st_steps, st_s, st_out = leg(budget_s / 2, 64)
+    out = dict(unit="GB/s", kind="oracle", host_cores=host_cores,
+               single_thread={"value": st_value, "cores": 1, "steps": st_steps, "seconds": round(st_s, 2)})
+    threads = oracle.use_openmp(0)
+    try:
+        if threads:
+            mt_value, mt_steps, mt_s, mt_out = leg(budget_s / 2, 256)
+            same = all(np.array_equal(a, b) for a, b in zip(st_out, mt_out))
+            out.update(value=mt_value, cores=threads,
+                       openmp={"value": mt_value, "cores": threads, "steps": mt_steps, "seconds": round(mt_s, 2),
+                               "same_bits_as_single_thread": same},
+                       sample=f"whole layer steps of {name} (T={T}) on a CPU-drawn layer: {mt_steps} steps in "
+                              f"{mt_s:.1f} s on {threads} threads (OpenMP over output rows), {st_steps} steps in "
+                              f"{st_s:.1f} s on one thread; host has {host_cores} cores")
+        else:
+            out.update(value=st_value, cores=1,
+                       sample=f"{st_steps} whole layer steps of {name} (T={T}) on a CPU-drawn layer, {st_s:.1f} s, "
+                              f"single thread (no OpenMP build on this host); host has {host_cores} cores")
+    finally:
+        oracle.use_openmp(-1)
+    return out
 
 
 def traffic_for(kernel_src_hash):
@@ -815,6 +859,7 @@ def run_flint(args):
                        "bytes_per_step": main["bytes_per_step_mean"]},
             "roofline": {"bound": "hbm", "kernel": "layer_kernel", "achieved": round(achieved, 1),
                          "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                          "traffic": traffic, "algorithmic_bytes_per_launch": kern["layer_bytes"],
                          "us_per_launch": kern["layer_us"]},
             "kernels_us": {k: round(v, 3) for k, v in kern.items() if k.endswith("_us")},
@@ -842,6 +887,14 @@ def run_flint(args):
 # reference arm: the oracle, on the host cores
 # ---------------------------------------------------------------------------
 def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on this host's cores
+    (the OpenMP build over output rows where the compiler has OpenMP, else
+    the plain build on one thread), on the workload this bench is labelled
+    with. A step is the whole layer for the workload's T tokens (router, the
+    selected experts, the shared expert, combine), with fresh x per step.
+    Where K + W whole steps would not end within the time budget, each step
+    is a bounded sample instead: a slice of gate rows of one selected expert
+    (the GEMVs carry 92% of the layer's bytes), said so in `sample`."""
     rank, world, local = dist_env()
     if rank != 0:
         return
@@ -853,34 +906,32 @@ def run_reference(args):
     sh = dict(gate=s["gate"].numpy(), up=s["up"].numpy(), down=s["down"].numpy(), ts=s["ts"].numpy(), I=I_SHARED)
     bias = synth.zipf_bias(7, E).numpy() if routing == "zipf" else None
     wr = synth.bits(L.router_w)
-    # Each step is a bounded sample of the workload, sized so that the whole
-    # run ends within a few minutes: one token through the whole layer when
-    # that fits the per-step budget, otherwise the oracle's expert GEMV over a
-    # slice of gate/up rows of the experts that token selects (the GEMVs carry
-    # 92% of the layer's bytes). Every step is run and timed.
+    host_cores = os.cpu_count() or 1
+    threads = oracle.use_openmp(0) or 1
     budget = 150.0
     total = args.steps + args.warmup
     per_step = budget / max(total, 1)
     gu_bytes_row = H // 64 * 36  # GGUF and kernel layouts both hold 0.5625 B per weight
-    x1 = synth.bits(synth.activations(9000, 1, H))
-    t0 = time.perf_counter()
-    ids1, _, _ = oracle.moe_layer(x1, wr, TOPK, E, I, L.gate.numpy(), L.up.numpy(), L.down.numpy(), L.ts.numpy(),
-                                  shared=sh, bias=bias)
-    t_token = time.perf_counter() - t0
-    whole = t_token <= per_step
+
+    def whole_step(seed):
+        x = synth.bits(synth.activations(seed, T, H))
+        t0 = time.perf_counter()
+        ids, _, _ = oracle.moe_layer(x, wr, TOPK, E, I, L.gate.numpy(), L.up.numpy(), L.down.numpy(), L.ts.numpy(),
+                                     shared=sh, bias=bias)
+        return time.perf_counter() - t0, step_bytes(len(set(ids.reshape(-1).tolist())), T, bias is not None), ids
+
+    t_step, _, ids1 = whole_step(9000)
+    whole = t_step <= per_step
     gate_np = L.gate.numpy()
-    sel = [int(e) for e in ids1.reshape(-1)]
-    rows_per_step = max(1, int(I * len(sel) * per_step / max(t_token, 1e-9) / 2)) if not whole else 0
-    rows_per_step = min(rows_per_step, I)
+    sel = sorted({int(e) for e in ids1.reshape(-1)})
+    x1 = synth.bits(synth.activations(9000, 1, H))
+    rows_per_step = 0
+    if not whole:
+        rows_per_step = min(I, max(1, int(I * len(sel) * per_step / max(t_step, 1e-9) / 2)))
     timed_s, timed_b, cursor = 0.0, 0, 0
     for i in range(total):
         if whole:
-            x = synth.bits(synth.activations(9001 + i, 1, H))
-            t0 = time.perf_counter()
-            ids, _, _ = oracle.moe_layer(x, wr, TOPK, E, I, L.gate.numpy(), L.up.numpy(), L.down.numpy(),
-                                         L.ts.numpy(), shared=sh, bias=bias)
-            t = time.perf_counter() - t0
-            b = step_bytes(len(set(ids.reshape(-1).tolist())), 1, bias is not None)
+            t, b, _ = whole_step(9001 + i)
         else:
             e = sel[cursor % len(sel)]
             cursor += 1
@@ -892,16 +943,20 @@ def run_reference(args):
         if i >= args.warmup:
             timed_s += t
             timed_b += b
+    oracle.use_openmp(-1)
     value = timed_b / max(timed_s, 1e-12) / 1e9
-    sample = (f"one token per step through the whole layer (router, {TOPK} routed + shared experts, combine)"
-              if whole else f"{rows_per_step} gate rows of one selected expert per step (oracle expert GEMV), "
-                            f"cycling over the {len(sel)} experts one token selects")
+    how = f"{threads} threads (OpenMP over output rows)" if threads > 1 else "one thread"
+    sample = (f"whole layer steps of {args.workload}: {T} tokens per step through the router, the selected "
+              f"experts, the shared expert and the combine, {how}, host has {host_cores} cores"
+              if whole else
+              f"{rows_per_step} gate rows of one selected expert per step (oracle expert GEMV), cycling over the "
+              f"{len(sel)} experts the workload's tokens select, {how}, host has {host_cores} cores")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": timed_s * 1e3 / max(args.steps, 1),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "routing": routing, "whole_token_steps": whole},
-            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample + ", single thread"},
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "tokens": T, "routing": routing, "whole_layer_steps": whole},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": threads, "host_cores": host_cores,
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

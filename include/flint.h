@@ -213,20 +213,25 @@ flint_status_t flint_moe_route(const flint_bf16* x, int T, int H, const flint_bf
  * method); it exists only for such callers.
  *   Arguments as flint_moe_route, without ws/ws_bytes. The results equal those
  *   of flint_moe_route on the same inputs.
- *   Scratch: a 33,024-byte array inside the library (counter, status word,
- *   FP32 logits for at most 8 tokens x 1024 experts), held by every device that
- *   loads the library until the process exits. Larger T x E is rejected with
- *   FLINT_ERR_UNSUPPORTED and a message giving the limit.
+ *   Scratch: a 33,024-byte array inside the library (a 256-byte header with
+ *   the counter and status word, then FP32 logits for T x E <= 8 x 1024),
+ *   held by every device that loads the library until the process exits.
+ *   E above 1024 (the selection's limit, as for flint_moe_route), or T x E
+ *   beyond the scratch, is rejected with FLINT_ERR_UNSUPPORTED and a message
+ *   giving the limit.
  *   The first call on a device looks up the array's device address (with that
  *   device current); make that first call before any stream capture.
- *   Every call clears the counter and status word (an 8-byte memset on
- *   `stream`) and then overwrites the logits. All calls share the one array:
+ *   Every call clears the 256-byte scratch header (one memset on `stream`)
+ *   and then overwrites the logits. All calls share the one array:
  *   calls issued in order on one stream follow each other (the memset waits
  *   for the previous kernel), but calls that can run at the same time on the
  *   GPU (different streams or threads) race on it and must be serialised by
  *   the caller.
  *   A timed-out wait inside the kernel leaves ids/weights unwritten and is not
- *   reported. No memory is allocated or freed.
+ *   reported (the status word lives in the shared scratch, which the next
+ *   call clears): a caller that must detect it fills ids with -1 first and
+ *   checks them after the stream synchronises. No memory is allocated or
+ *   freed.
  */
 flint_status_t flint_moe_route_static(const flint_bf16* x, int T, int H, const flint_bf16* router_w, int E,
                                       const float* bias, int k, int32_t* ids, float* weights, unsigned flags,

@@ -270,12 +270,18 @@ flint_status_t flint_workspace_check(void* ws, size_t ws_bytes, void* stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status");
     if (!st) return FLINT_OK;
-    e = cudaMemsetAsync(ws_status(ws), 0, sizeof st, as_stream(stream));
+    const bool timeout = (st & (flint::kStatusTimeoutRoute | flint::kStatusTimeoutGateUp | flint::kStatusTimeoutDown |
+                                flint::kStatusTimeoutSelftest | flint::kStatusTimeoutLayer |
+                                flint::kStatusTimeoutPrefill)) != 0;
+    // After a timed-out wait the counters the kernels synchronise on (the
+    // router's arrival counter, the grid barrier's ticket) may be left
+    // mid-round: the whole workspace is re-initialised, as flint_workspace_init
+    // does. Otherwise only the status word is cleared.
+    e = cudaMemsetAsync(timeout ? ws : static_cast<void*>(ws_status(ws)), 0, timeout ? ws_bytes : sizeof st,
+                        as_stream(stream));
     if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status");
-    if (st & (flint::kStatusTimeoutRoute | flint::kStatusTimeoutGateUp | flint::kStatusTimeoutDown |
-              flint::kStatusTimeoutSelftest | flint::kStatusTimeoutLayer | flint::kStatusTimeoutPrefill))
-        return fail(FLINT_ERR_TIMEOUT, "device wait timed out (status 0x%x)", st);
+    if (timeout) return fail(FLINT_ERR_TIMEOUT, "device wait timed out (status 0x%x); workspace re-initialised", st);
     return fail(FLINT_ERR_INVALID_ARG, "an expert id was outside [0, num_experts) (status 0x%x)", st);
 }
 
@@ -566,7 +572,7 @@ static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, cons
     a.weights = weights;
     a.logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + W.logits_off);
     a.status = ws_status(ws);
-    a.bar_ticket = reinterpret_cast<uint32_t*>(ws) + 2;
+    a.bar_ticket = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + 8);
     a.gu = static_cast<const uint8_t*>(routed->gate_up);
     a.down = static_cast<const uint8_t*>(routed->down);
     a.I = routed->inter;
@@ -757,12 +763,19 @@ extern "C" flint_status_t flint_moe_route_static(const flint_bf16* x, int T, int
         return fail(FLINT_ERR_UNSUPPORTED, "route_static: T=%d outside 1..%d", T, FLINT_MAX_TOKENS);
     if (H <= 0 || H % 256) return fail(FLINT_ERR_UNSUPPORTED, "route_static: H=%d must be a positive multiple of 256", H);
     if (E < 1) return fail(FLINT_ERR_INVALID_ARG, "route_static: E=%d", E);
-    if (flint::kWsHeader + sizeof(float) * (size_t)T * (size_t)E > kRouteStaticScratchBytes)
+    // The selection keeps at most FLINT_MAX_EXPERTS scores per token, whatever
+    // the scratch could hold.
+    if (E > FLINT_MAX_EXPERTS)
+        return fail(FLINT_ERR_UNSUPPORTED, "route_static: E=%d above the router's limit of %d experts", E,
+                    FLINT_MAX_EXPERTS);
+    if (flint::kWsHeader + sizeof(float) * (size_t)T * (size_t)E > kRouteStaticScratchBytes) {
+        const int by_scratch = (int)((kRouteStaticScratchBytes - flint::kWsHeader) / sizeof(float) / T);
         return fail(FLINT_ERR_UNSUPPORTED,
                     "route_static: %d tokens x %d experts need %zu bytes of scratch; the static scratch holds %zu "
                     "(at most %d experts for %d tokens)",
                     T, E, flint::kWsHeader + sizeof(float) * (size_t)T * (size_t)E, kRouteStaticScratchBytes,
-                    (int)((kRouteStaticScratchBytes - flint::kWsHeader) / sizeof(float) / T), T);
+                    by_scratch < FLINT_MAX_EXPERTS ? by_scratch : FLINT_MAX_EXPERTS, T);
+    }
     if (k < 1 || k > FLINT_MAX_TOPK || k > E)
         return fail(FLINT_ERR_UNSUPPORTED, "route_static: k=%d outside 1..min(%d, E)", k, FLINT_MAX_TOPK);
     if (!x || !router_w || !ids || !weights || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) ||

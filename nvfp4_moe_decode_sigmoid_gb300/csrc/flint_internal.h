@@ -40,7 +40,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kGemvWarps = 24;
 constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kMaxSlotsPerWarp = 4;
-constexpr size_t kWsHeader = 256;   // router counter (word 0), status (word 1), grid barrier tickets (word 2)
+constexpr size_t kWsHeader = 256;   // router counter (word 0), status (word 1), 64-bit grid barrier ticket (bytes 8..15)
 // Expert GEMV kernels for BF16 weights: 16 warps (a BF16 row is 4x the bytes
 // of an NVFP4 row, so fewer, larger ring slots per SM).
 constexpr int kBf16Warps = 16;
@@ -151,7 +151,7 @@ struct LayerArgs {
     int32_t* ids;        // [T][k] out
     float* weights;      // [T][k] out
     float* logits;       // workspace [8][E]: the sigmoid scores (bits) of the router logits
-    uint32_t* bar_ticket; // workspace word 2: grid barrier tickets (a multiple of the grid size between calls)
+    unsigned long long* bar_ticket; // workspace bytes 8..15: grid barrier tickets (a multiple of the grid size between calls)
     uint32_t* status;    // workspace word 1
     const uint8_t* gu;   // routed E x [2I, H]
     const uint8_t* down; // routed E x [H, I]

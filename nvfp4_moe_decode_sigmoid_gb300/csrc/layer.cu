@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         warp_copy_async(dst, a.down + ((size_t)ri.dlist[u] * H + n0 + r0g) * RSr, (r1g - r0g) * RSr, lane);
         cp_async_commit();
     };
-    const uint32_t target = grid_arrive(a.bar_ticket);
+    const unsigned long long target = grid_arrive(a.bar_ticket);
     for (int kk = 0; kk < NSW; ++kk) {
         if (kk < my_tasks)
             issue(kk);

@@ -1,6 +1,6 @@
 """CPU oracle for the Flint-style NVFP4 MoE decode step -- TEST INFRASTRUCTURE.
 
-A ctypes front end over ``libflint_oracle.so`` (plain C, double accumulation,
+A ctypes front end over ``libflint_oracle.so`` (plain C, FP32 accumulation,
 bf16 rounding at the method's stated points; see ``flint_oracle.c`` for the
 definitions it follows and the readings it takes). Only the test suite, the
 smoke check and the CPU-baseline leg of the benchmark may use it; the product
@@ -14,6 +14,8 @@ import numpy as np
 from . import build as _build
 
 _lib = None
+_lib_omp = None
+_active = None  # the library the functions below call (the plain build unless use_openmp)
 
 W_NVFP4 = 0
 W_BF16 = 1
@@ -21,55 +23,80 @@ EPI_NONE = 0
 EPI_SWIGLU = 1
 
 
+def _setup(L):
+    L.fo_e2m1_value.restype = C.c_double
+    L.fo_e2m1_value.argtypes = [C.c_int]
+    L.fo_ue4m3_value.restype = C.c_double
+    L.fo_ue4m3_value.argtypes = [C.c_int]
+    L.fo_bf16_value.restype = C.c_double
+    L.fo_bf16_value.argtypes = [C.c_uint16]
+    L.fo_bf16_round.restype = C.c_uint16
+    L.fo_bf16_round.argtypes = [C.c_double]
+    L.fo_gguf_matrix_bytes.restype = C.c_int64
+    L.fo_gguf_matrix_bytes.argtypes = [C.c_int64, C.c_int64]
+    L.fo_packed_row_stride.restype = C.c_int64
+    L.fo_packed_row_stride.argtypes = [C.c_int64]
+    for name in ("fo_gguf_decode", "fo_packed_decode"):
+        f = getattr(L, name)
+        f.restype = C.c_int
+        f.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p]
+    L.fo_repack.restype = C.c_int
+    L.fo_repack.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_void_p, C.c_int64]
+    L.fo_unrepack.restype = C.c_int
+    L.fo_unrepack.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_int64, C.c_void_p]
+    L.fo_router.restype = C.c_int
+    L.fo_router.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_int,
+                            C.c_void_p, C.c_void_p, C.c_void_p]
+    L.fo_expert.restype = C.c_int
+    L.fo_expert.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
+                            C.c_double, C.c_double, C.c_double, C.c_void_p, C.c_void_p, C.c_void_p,
+                            C.c_void_p]
+    L.fo_moe_experts.restype = C.c_int
+    L.fo_moe_experts.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
+                                 C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                 C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+    L.fo_moe_layer.restype = C.c_int
+    L.fo_moe_layer.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_int,
+                               C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                               C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                               C.c_void_p, C.c_void_p, C.c_void_p]
+    L.fo_dense_gemv.restype = C.c_int
+    L.fo_dense_gemv.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
+                                C.c_int, C.c_void_p]
+    L.fo_residual_rmsnorm.restype = C.c_int
+    L.fo_residual_rmsnorm.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_double,
+                                      C.c_void_p, C.c_void_p]
+    L.fo_set_threads.restype = C.c_int
+    L.fo_set_threads.argtypes = [C.c_int]
+    return L
+
+
 def lib():
-    global _lib
+    global _lib, _active
     if _lib is None:
-        path = _build.build()
-        L = C.CDLL(path)
-        L.fo_e2m1_value.restype = C.c_double
-        L.fo_e2m1_value.argtypes = [C.c_int]
-        L.fo_ue4m3_value.restype = C.c_double
-        L.fo_ue4m3_value.argtypes = [C.c_int]
-        L.fo_bf16_value.restype = C.c_double
-        L.fo_bf16_value.argtypes = [C.c_uint16]
-        L.fo_bf16_round.restype = C.c_uint16
-        L.fo_bf16_round.argtypes = [C.c_double]
-        L.fo_gguf_matrix_bytes.restype = C.c_int64
-        L.fo_gguf_matrix_bytes.argtypes = [C.c_int64, C.c_int64]
-        L.fo_packed_row_stride.restype = C.c_int64
-        L.fo_packed_row_stride.argtypes = [C.c_int64]
-        for name in ("fo_gguf_decode", "fo_packed_decode"):
-            f = getattr(L, name)
-            f.restype = C.c_int
-            f.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p]
-        L.fo_repack.restype = C.c_int
-        L.fo_repack.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_void_p, C.c_int64]
-        L.fo_unrepack.restype = C.c_int
-        L.fo_unrepack.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_int64, C.c_void_p]
-        L.fo_router.restype = C.c_int
-        L.fo_router.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_int,
-                                C.c_void_p, C.c_void_p, C.c_void_p]
-        L.fo_expert.restype = C.c_int
-        L.fo_expert.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
-                                C.c_double, C.c_double, C.c_double, C.c_void_p, C.c_void_p, C.c_void_p,
-                                C.c_void_p]
-        L.fo_moe_experts.restype = C.c_int
-        L.fo_moe_experts.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
-                                     C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
-                                     C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
-        L.fo_moe_layer.restype = C.c_int
-        L.fo_moe_layer.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_int,
-                                   C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
-                                   C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
-                                   C.c_void_p, C.c_void_p, C.c_void_p]
-        L.fo_dense_gemv.restype = C.c_int
-        L.fo_dense_gemv.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
-                                    C.c_int, C.c_void_p]
-        L.fo_residual_rmsnorm.restype = C.c_int
-        L.fo_residual_rmsnorm.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_double,
-                                          C.c_void_p, C.c_void_p]
-        _lib = L
-    return _lib
+        _lib = _setup(C.CDLL(_build.build()))
+    if _active is None:
+        _active = _lib
+    return _active
+
+
+def use_openmp(threads: int = 0) -> int:
+    """Route the calls below to the OpenMP build with `threads` threads (0:
+    all host threads); returns the thread count, or 0 (and keeps the plain
+    build) where no OpenMP build exists. use_openmp(-1) returns to the plain
+    build. Results are the same bits either way."""
+    global _lib_omp, _active
+    lib()
+    if threads < 0:
+        _active = _lib
+        return 1
+    if _lib_omp is None:
+        path = _build.build_omp()
+        if path is None:
+            return 0
+        _lib_omp = _setup(C.CDLL(path))
+    _active = _lib_omp
+    return _lib_omp.fo_set_threads(threads if threads > 0 else (os.cpu_count() or 1))
 
 
 def _p(a):

@@ -21,14 +21,19 @@
  *          "Flint 是什么" (256 routed experts, sigmoid top-6, one always-on
  *          shared expert, hidden size 2048).
  *
- * Precision: every dot product and every combine is accumulated in double
- * (the pages fix no accumulation precision). Values are rounded to bf16, round
- * to nearest even, exactly at the rounding points the method states: after
- * each GEMV (g, u, d), after silu(g)*u (h), and for the layer output y.
- * Router logits are not rounded to bf16. Where a float decides an integer
- * (the top-k selection), the decision is taken in FP32 like the kernels: the
- * logit is rounded to float, the bias added in float, and the sigmoid score
- * rounded to float before ranking.
+ * Precision ([Blog] "Model architecture": every kernel follows the
+ * reference's rounding points; the reference accumulates in FP32): every dot
+ * product is accumulated in FP32 in index order, one rounding per step (each
+ * product of a weight and a bf16 activation is exact in FP32, so a fused
+ * multiply-add and a multiply followed by an add give the same bits). The
+ * per-tensor FP32 scale multiplies the FP32 sum once, in FP32. Values are
+ * rounded to bf16, round to nearest even, exactly at the rounding points the
+ * method states: after each GEMV (g, u, d), after silu(g)*u (h, with silu and
+ * the product in FP32), and for the layer output y, whose combine is an FP32
+ * multiply-add per routed expert in rank order, then the shared expert's d
+ * added in FP32. Router logits stay FP32 (FP32 sum, FP32 bias add, FP32
+ * sigmoid), and the top-k weights are the selected FP32 scores over their
+ * FP32 sum in rank order.
  *
  * Readings of points the pages leave open (each listed in the design notes):
  *  - GGUF superblock byte order (36 bytes per 64 values): bytes 0..3 are the
@@ -50,6 +55,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define FO_OK 0
 #define FO_BAD_ARG 1
@@ -59,6 +67,18 @@
 
 #define FO_EPI_NONE 0
 #define FO_EPI_SWIGLU 1
+
+/* Threads of the OpenMP build (the same source compiled with -fopenmp, for
+ * timing the oracle on all host cores); the plain build ignores them. */
+int fo_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------------ */
 /* Number formats                                                            */
@@ -246,14 +266,16 @@ static int64_t weight_matrix_bytes(int wdtype, int64_t rows, int64_t cols) {
     return rows * cols * 2;
 }
 
-/* acc = sum_k W[row, k] * x[k], in double, in index order. */
-static double dot_row(int wdtype, const void* w, int64_t cols, int64_t row, const double* x) {
-    double acc = 0.0;
-    for (int64_t c = 0; c < cols; ++c) acc += weight_elem(wdtype, w, cols, row, c) * x[c];
+/* acc = sum_k W[row, k] * x[k], in FP32, in index order: one rounding per
+ * step (the product of a weight and a bf16 value is exact in FP32). */
+static float dot_row(int wdtype, const void* w, int64_t cols, int64_t row, const float* x) {
+    float acc = 0.0f;
+    for (int64_t c = 0; c < cols; ++c) acc = fmaf((float)weight_elem(wdtype, w, cols, row, c), x[c], acc);
     return acc;
 }
 
-static double silu(double g) { return g / (1.0 + exp(-g)); }
+/* silu(g) = g / (1 + exp(-g)), in FP32. */
+static float silu(float g) { return g / (1.0f + expf(-g)); }
 
 /* ------------------------------------------------------------------------ */
 /* Router: logits, sigmoid scores, top-k, renormalised weights               */
@@ -270,17 +292,18 @@ int fo_router(const uint16_t* x, int T, int H, const uint16_t* wr, int E, const 
     char* taken = (char*)malloc((size_t)E);
     if (!s || !taken) { free(s); free(taken); return FO_BAD_ARG; }
     for (int t = 0; t < T; ++t) {
+        /* expert rows are independent (the OpenMP build splits them over threads) */
+#pragma omp parallel for schedule(static)
         for (int e = 0; e < E; ++e) {
-            double acc = 0.0;
+            float z = 0.0f;
             for (int h = 0; h < H; ++h)
-                acc += fo_bf16_value(x[(int64_t)t * H + h]) * fo_bf16_value(wr[(int64_t)e * H + h]);
-            float z = (float)acc;
+                z = fmaf((float)fo_bf16_value(x[(int64_t)t * H + h]), (float)fo_bf16_value(wr[(int64_t)e * H + h]), z);
             if (bias) z = z + bias[e];
-            s[e] = (float)(1.0 / (1.0 + exp(-(double)z)));
+            s[e] = 1.0f / (1.0f + expf(-z));
             if (scores) scores[(int64_t)t * E + e] = s[e];
         }
         memset(taken, 0, (size_t)E);
-        double sum = 0.0;
+        float sum = 0.0f;
         for (int j = 0; j < k; ++j) {
             int best = -1;
             for (int e = 0; e < E; ++e) {
@@ -289,9 +312,9 @@ int fo_router(const uint16_t* x, int T, int H, const uint16_t* wr, int E, const 
             }
             taken[best] = 1;
             ids[t * k + j] = best;
-            sum += (double)s[best];
+            sum += s[best];
         }
-        for (int j = 0; j < k; ++j) weights[t * k + j] = (double)s[ids[t * k + j]] / sum;
+        for (int j = 0; j < k; ++j) weights[t * k + j] = (double)(s[ids[t * k + j]] / sum);
     }
     free(s);
     free(taken);
@@ -305,25 +328,31 @@ int fo_router(const uint16_t* x, int T, int H, const uint16_t* wr, int E, const 
 /* g[i] = bf16(ts_g * sum_h Wg[i,h] x[h]);  u[i] = bf16(ts_u * sum_h Wu[i,h] x[h])
  * h[i] = bf16(silu(g[i]) * u[i])
  * d[n] = bf16(ts_d * sum_i Wd[n,i] h[i])
- * Any of g, u, hh may be NULL. */
+ * (sums, scale products, silu and its product in FP32). Any of g, u, hh may
+ * be NULL. */
 int fo_expert(const uint16_t* x, int H, int I, int wdtype, const void* gate, const void* up,
               const void* down, double ts_g, double ts_u, double ts_d,
               uint16_t* g, uint16_t* u, uint16_t* hh, uint16_t* d) {
     if (!x || !gate || !up || !down || !d || H <= 0 || I <= 0) return FO_BAD_ARG;
-    double* xd = (double*)malloc(sizeof(double) * (size_t)H);
-    double* hd = (double*)malloc(sizeof(double) * (size_t)I);
+    float* xd = (float*)malloc(sizeof(float) * (size_t)H);
+    float* hd = (float*)malloc(sizeof(float) * (size_t)I);
     if (!xd || !hd) { free(xd); free(hd); return FO_BAD_ARG; }
-    for (int c = 0; c < H; ++c) xd[c] = fo_bf16_value(x[c]);
+    const float sg = (float)ts_g, su = (float)ts_u, sd = (float)ts_d;
+    for (int c = 0; c < H; ++c) xd[c] = (float)fo_bf16_value(x[c]);
+    /* Output rows are independent, and each is summed in index order by one
+     * thread: the OpenMP build (rows split over threads) gives the same bits. */
+#pragma omp parallel for schedule(static)
     for (int i = 0; i < I; ++i) {
-        uint16_t gb = fo_bf16_round(ts_g * dot_row(wdtype, gate, H, i, xd));
-        uint16_t ub = fo_bf16_round(ts_u * dot_row(wdtype, up, H, i, xd));
-        uint16_t hb = fo_bf16_round(silu(fo_bf16_value(gb)) * fo_bf16_value(ub));
+        uint16_t gb = fo_bf16_round(sg * dot_row(wdtype, gate, H, i, xd));
+        uint16_t ub = fo_bf16_round(su * dot_row(wdtype, up, H, i, xd));
+        uint16_t hb = fo_bf16_round(silu((float)fo_bf16_value(gb)) * (float)fo_bf16_value(ub));
         if (g) g[i] = gb;
         if (u) u[i] = ub;
         if (hh) hh[i] = hb;
-        hd[i] = fo_bf16_value(hb);
+        hd[i] = (float)fo_bf16_value(hb);
     }
-    for (int n = 0; n < H; ++n) d[n] = fo_bf16_round(ts_d * dot_row(wdtype, down, I, n, hd));
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < H; ++n) d[n] = fo_bf16_round(sd * dot_row(wdtype, down, I, n, hd));
     free(xd);
     free(hd);
     return FO_OK;
@@ -341,7 +370,8 @@ int fo_expert(const uint16_t* x, int H, int I, int wdtype, const void* gate, con
  *
  * For each token t:
  *   y[t] = bf16( sum_{j<k} w[t,j] * d_{ids[t,j]}(x[t])  +  d_shared(x[t]) )
- * accumulated in double, routed experts in rank order, then the shared one. */
+ * accumulated in FP32: a multiply-add per routed expert in rank order (one
+ * rounding each), then the shared expert's d added. */
 int fo_moe_experts(const uint16_t* x, int T, int H, const int32_t* ids, const float* w, int k,
                    int E, int I, int wdtype, const void* gate, const void* up, const void* down,
                    const float* ts, int Is, const void* sgate, const void* sup, const void* sdown,
@@ -350,12 +380,12 @@ int fo_moe_experts(const uint16_t* x, int T, int H, const int32_t* ids, const fl
     int64_t gb = weight_matrix_bytes(wdtype, I, H);
     int64_t db = weight_matrix_bytes(wdtype, H, I);
     uint16_t* d = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)H);
-    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    float* acc = (float*)malloc(sizeof(float) * (size_t)H);
     if (!d || !acc) { free(d); free(acc); return FO_BAD_ARG; }
     int rc = FO_OK;
     for (int t = 0; t < T && rc == FO_OK; ++t) {
         const uint16_t* xt = x + (int64_t)t * H;
-        for (int n = 0; n < H; ++n) acc[n] = 0.0;
+        for (int n = 0; n < H; ++n) acc[n] = 0.0f;
         for (int j = 0; j < k; ++j) {
             int e = ids[t * k + j];
             if (e < 0 || e >= E) { rc = FO_BAD_ARG; break; }
@@ -363,12 +393,12 @@ int fo_moe_experts(const uint16_t* x, int T, int H, const int32_t* ids, const fl
             rc = fo_expert(xt, H, I, wdtype, (const uint8_t*)gate + e * gb, (const uint8_t*)up + e * gb,
                            (const uint8_t*)down + e * db, tg, tu, td, NULL, NULL, NULL, d);
             if (rc != FO_OK) break;
-            for (int n = 0; n < H; ++n) acc[n] += (double)w[t * k + j] * fo_bf16_value(d[n]);
+            for (int n = 0; n < H; ++n) acc[n] = fmaf(w[t * k + j], (float)fo_bf16_value(d[n]), acc[n]);
         }
         if (rc == FO_OK && sgate) {
             double tg = sts ? sts[0] : 1.0, tu = sts ? sts[1] : 1.0, td = sts ? sts[2] : 1.0;
             rc = fo_expert(xt, H, Is, wdtype, sgate, sup, sdown, tg, tu, td, NULL, NULL, NULL, d);
-            for (int n = 0; n < H && rc == FO_OK; ++n) acc[n] += fo_bf16_value(d[n]);
+            for (int n = 0; n < H && rc == FO_OK; ++n) acc[n] += (float)fo_bf16_value(d[n]);
         }
         for (int n = 0; n < H; ++n) y[(int64_t)t * H + n] = fo_bf16_round(acc[n]);
     }
@@ -403,24 +433,25 @@ int fo_moe_layer(const uint16_t* x, int T, int H, const uint16_t* wr, int E, con
  * epilogue SWIGLU: W is [N, K] with rows [0, N/2) the gate projection
  *                  (tensor scale ts[0]) and rows [N/2, N) the up projection
  *                  (ts[1]); y[t, i] = bf16(silu(g) * u), g and u rounded to
- *                  bf16 first, i < N/2. */
+ *                  bf16 first, i < N/2.
+ * Sums, scale products, silu and its product in FP32, as in fo_expert. */
 int fo_dense_gemv(const uint16_t* x, int T, int K, int wdtype, const void* W, int N,
                   const float* ts, int epilogue, uint16_t* y) {
     if (!x || !W || !y || T < 0 || K <= 0 || N <= 0) return FO_BAD_ARG;
     if (epilogue == FO_EPI_SWIGLU && N % 2) return FO_BAD_ARG;
-    double* xd = (double*)malloc(sizeof(double) * (size_t)K);
+    float* xd = (float*)malloc(sizeof(float) * (size_t)K);
     if (!xd) return FO_BAD_ARG;
     for (int t = 0; t < T; ++t) {
-        for (int c = 0; c < K; ++c) xd[c] = fo_bf16_value(x[(int64_t)t * K + c]);
+        for (int c = 0; c < K; ++c) xd[c] = (float)fo_bf16_value(x[(int64_t)t * K + c]);
         if (epilogue == FO_EPI_NONE) {
-            double s = ts ? ts[0] : 1.0;
+            float s = ts ? ts[0] : 1.0f;
             for (int n = 0; n < N; ++n) y[(int64_t)t * N + n] = fo_bf16_round(s * dot_row(wdtype, W, K, n, xd));
         } else {
             int half = N / 2;
-            double sg = ts ? ts[0] : 1.0, su = ts ? ts[1] : 1.0;
+            float sg = ts ? ts[0] : 1.0f, su = ts ? ts[1] : 1.0f;
             for (int i = 0; i < half; ++i) {
-                double g = fo_bf16_value(fo_bf16_round(sg * dot_row(wdtype, W, K, i, xd)));
-                double u = fo_bf16_value(fo_bf16_round(su * dot_row(wdtype, W, K, half + i, xd)));
+                float g = (float)fo_bf16_value(fo_bf16_round(sg * dot_row(wdtype, W, K, i, xd)));
+                float u = (float)fo_bf16_value(fo_bf16_round(su * dot_row(wdtype, W, K, half + i, xd)));
                 y[(int64_t)t * half + i] = fo_bf16_round(silu(g) * u);
             }
         }
@@ -441,26 +472,28 @@ int fo_dense_gemv(const uint16_t* x, int T, int K, int wdtype, const void* W, in
  * Per token t:
  *   r'[h] = bf16(r[h] + y[h])                  (r' = r when y is NULL)
  *   x[h]  = bf16(r'[h] / sqrt(mean_h(r'^2) + eps) * gamma[h])   (gamma = 1 when NULL)
- * with the sum, the mean, the square root and the products in double.
+ * in FP32 like every other step: the residual add, the sum of squares in
+ * index order, the mean, the square root, its reciprocal and the products.
  * r_out (may be NULL) receives r'; x_out receives x. */
 int fo_residual_rmsnorm(const uint16_t* r, const uint16_t* y, int T, int H, const uint16_t* gamma, double eps,
                         uint16_t* r_out, uint16_t* x_out) {
     if (!r || !x_out || T < 0 || H <= 0 || eps < 0.0) return FO_BAD_ARG;
-    double* rr = (double*)malloc(sizeof(double) * (size_t)H);
+    float* rr = (float*)malloc(sizeof(float) * (size_t)H);
     if (!rr) return FO_BAD_ARG;
+    const float epsf = (float)eps;
     for (int t = 0; t < T; ++t) {
-        double ss = 0.0;
+        float ss = 0.0f;
         for (int h = 0; h < H; ++h) {
             int64_t i = (int64_t)t * H + h;
-            double v = fo_bf16_value(r[i]);
-            if (y) v = fo_bf16_value(fo_bf16_round(v + fo_bf16_value(y[i])));
+            float v = (float)fo_bf16_value(r[i]);
+            if (y) v = (float)fo_bf16_value(fo_bf16_round(v + (float)fo_bf16_value(y[i])));
             rr[h] = v;
-            ss += v * v;
+            ss = fmaf(v, v, ss);
             if (r_out) r_out[i] = fo_bf16_round(v);
         }
-        double inv = 1.0 / sqrt(ss / (double)H + eps);
+        float inv = 1.0f / sqrtf(ss / (float)H + epsf);
         for (int h = 0; h < H; ++h) {
-            double g = gamma ? fo_bf16_value(gamma[h]) : 1.0;
+            float g = gamma ? (float)fo_bf16_value(gamma[h]) : 1.0f;
             x_out[(int64_t)t * H + h] = fo_bf16_round(rr[h] * inv * g);
         }
     }

@@ -36,12 +36,14 @@ def assert_close(y_gpu_bits, y_ref_bits, what="", terms=None):
     |gpu - ref| <= ELEM_A (|ref| + ELEM_B).
 
     terms (optional, [T, H]): sum_j |w_j d_j| + |d_shared| per output element
-    (from the oracle). y is a sum of bf16-rounded terms; a term whose FP32 and
-    double sums straddle a bf16 rounding boundary rounds one ulp apart, which
-    moves y by up to w_j ulp(d_j). Where the terms cancel (|y| much smaller
-    than the terms) that exceeds the relative bound without being an error.
+    (from the oracle). y is a sum of bf16-rounded terms. Both sides sum in
+    FP32, in different orders, so a term's two FP32 sums can straddle a bf16
+    rounding boundary and round one ulp apart, which moves y by up to
+    w_j ulp(d_j). Where the terms cancel (|y| much smaller than the terms)
+    that exceeds the relative bound without being an error on either side.
     With `terms`, an element outside the per-element bound still passes if
-    its error is within 2 ulp(terms), and such elements must be rare (<= 0.1 %)."""
+    its error is within 2 ulp(terms) (one flipped rounding per term), and
+    such elements must be rare (<= 0.1 %)."""
     a, r = bf16_to_f64(y_gpu_bits), bf16_to_f64(y_ref_bits)
     assert np.all(np.isfinite(a)), f"{what}: non-finite GPU output"
     rel = np.linalg.norm(a - r) / max(np.linalg.norm(r), 1e-30)

@@ -127,3 +127,15 @@ def test_norm_validation_without_a_gpu(flint):
     assert L.flint_moe_block(None, 1, p, 256, None, 6, C.byref(ex), None, p, p, o, p, 1 << 24, 0, None) == \
         flint.FLINT_ERR_INVALID_ARG
     del q
+
+
+@pytest.mark.parametrize("T,E", [(1, 1025), (4, 2048), (8, 1025)])
+def test_static_router_rejects_more_experts_than_the_selection_keeps(flint, T, E):
+    """flint_moe_route_static keeps at most 1024 scores per token, like
+    flint_moe_route, even where its scratch would hold more (T = 1): larger E
+    is rejected on the host."""
+    L = _raw(flint)
+    p = C.c_void_p(0x1000)
+    st = L.flint_moe_route_static(p, T, 2048, p, E, None, 6, p, p, 0, None)
+    assert st == flint.FLINT_ERR_UNSUPPORTED
+    assert "limit of 1024" in flint.flint_last_error()

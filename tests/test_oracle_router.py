@@ -1,8 +1,11 @@
 """Oracle self-tests: sigmoid top-k routing (CPU only).
 
-Pins: logits against a library matmul, scores against scipy's expit,
+Pins: logits against an FP32 running sum written out in numpy (each step one
+float32 rounding; the products of two bf16 values are exact in float32) and
+against a library matmul, scores against scipy's expit of those logits,
 selection against a brute-force full sort, planted ties, the all-equal
-special case and the renormalisation invariant.
+special case and the renormalisation invariant (weights are FP32: they sum to
+1 within the rounding of k float32 steps).
 """
 import numpy as np
 import pytest
@@ -31,7 +34,13 @@ def test_selection_matches_brute_force(E, k):
     ids, w, s = oracle.router(x, wr, k)
     for t in range(5):
         assert list(ids[t]) == _brute_topk(s[t], k)
-        assert abs(w[t].sum() - 1.0) < 1e-12
+        assert abs(w[t].sum() - 1.0) < 4 * k * 2.0 ** -24
+        # weight j belongs to the expert of rank j: its score over the FP32 sum of the selected scores
+        sel = s[t][ids[t]]
+        tot = np.float32(0)
+        for v in sel:
+            tot = np.float32(tot + v)
+        assert np.array_equal(w[t].astype(np.float32), (sel / tot).astype(np.float32))
 
 
 def test_scores_match_library_matmul_and_expit():
@@ -42,9 +51,17 @@ def test_scores_match_library_matmul_and_expit():
     _, _, s = oracle.router(x, wr, 6, bias=bias)
     xf = oracle.bf16_value(x)
     wf = oracle.bf16_value(wr)
-    logits = (xf @ wf.T).astype(np.float32) + bias          # FP32 decision precision
-    ref = expit(logits.astype(np.float64)).astype(np.float32)
-    assert np.array_equal(s, ref)
+    # FP32 running sums in index order: products exact in float32, one rounding per add
+    acc = np.zeros((T, E), np.float32)
+    for h in range(H):
+        acc = (acc + np.outer(xf[:, h], wf[:, h]).astype(np.float32)).astype(np.float32)
+    exact = xf @ wf.T
+    assert np.all(np.abs(acc - exact) <= H * 2.0 ** -24 * (np.abs(xf) @ np.abs(wf).T))
+    logits = (acc + bias).astype(np.float32)
+    ref = expit(logits.astype(np.float64))
+    # the FP32 sigmoid is within 2 float32 ulps of the exact value of the FP32 logit
+    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(s.astype(np.float64) - ref) <= 2 * ulp)
 
 
 def test_ties_go_to_lower_index():
@@ -75,7 +92,7 @@ def test_all_equal_scores():
     ids, w, s = oracle.router(x, wr, k)
     assert np.all(s == 0.5)
     assert np.array_equal(ids, np.tile(np.arange(k, dtype=np.int32), (2, 1)))
-    assert np.allclose(w, 1.0 / k, rtol=0, atol=1e-15)
+    assert np.allclose(w, 1.0 / k, rtol=0, atol=2.0 ** -24)
 
 
 def test_bias_steers_selection():

@@ -59,16 +59,32 @@ def test_static_scratch_router_matches_workspace_router_twice():
         assert np.array_equal(a_ids, r_ids)
 
 
-def test_static_scratch_router_rejects_shapes_beyond_its_scratch():
+@pytest.mark.parametrize("T,E,why", [
+    (8, 1025, "limit of 1024"),   # beyond both the selection and the 33,024-byte scratch
+    (1, 1025, "limit of 1024"),   # fits the scratch, but the selection keeps 1024 scores per token
+    (4, 2048, "limit of 1024"),
+    (8, 1024, None),              # the largest accepted shape is not rejected by the size checks
+])
+def test_static_scratch_router_rejects_shapes_beyond_its_limits(T, E, why):
     F = flint()
     lib = F.raw_library()
-    p = torch.empty(16, dtype=torch.int32, device="cuda")
     f = lib.flint_moe_route_static
     f.restype = C.c_int
     f.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
                   C.c_uint, C.c_void_p]
+    if why is None:
+        # a valid call: its inputs are real buffers of the right sizes
+        H, k = 256, 6
+        wr = synth.bf16_normal(90, (E, H), 0.02).cuda()
+        x = synth.activations(91, T, H).cuda()
+        ids = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+        w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+        assert _static_route(lib, x, wr, k, ids, w, None, torch.cuda.current_stream()) == F.FLINT_OK
+        torch.cuda.synchronize()
+        assert bool((ids >= 0).all()) and bool((ids < E).all())
+        return
+    p = torch.empty(16, dtype=torch.int32, device="cuda")
     ptr = C.c_void_p(p.data_ptr())
-    # 8 tokens x 1025 experts would need more than the 33,024-byte scratch
-    st = f(ptr, 8, 2048, ptr, 1025, None, 6, ptr, ptr, 0, None)
+    st = f(ptr, T, 2048, ptr, E, None, 6, ptr, ptr, 0, None)
     assert st == F.FLINT_ERR_UNSUPPORTED
-    assert "static scratch" in F.flint_last_error()
+    assert why in F.flint_last_error()
