@@ -191,7 +191,7 @@ class Model:
             self.layers.append(dict(router_w=L.router_w, routed=routed, shared=shared, seed=1000 + li))
             del L, s
             torch.cuda.synchronize()
-        self.ws = torch.empty(F.flint_workspace_bytes(E, TOPK, I, I_SHARED), dtype=torch.uint8, device=device)
+        self.ws = torch.empty(F.flint_workspace_bytes(E, TOPK, H, I, I_SHARED), dtype=torch.uint8, device=device)
         F.flint_workspace_init(self.ws)
 
     def step_bytes(self, n_distinct: int, T: int, with_bias: bool) -> int:
@@ -352,7 +352,7 @@ class Stack:
                                                             H, I_SHARED)))
             del L, s
             torch.cuda.synchronize()
-        self.ws = torch.empty(F.flint_workspace_bytes(E, TOPK, I, I_SHARED), dtype=torch.uint8, device=device)
+        self.ws = torch.empty(F.flint_workspace_bytes(E, TOPK, H, I, I_SHARED), dtype=torch.uint8, device=device)
         F.flint_workspace_init(self.ws)
 
     def dense_bytes(self):

@@ -143,21 +143,44 @@ flint_status_t flint_nvfp4_dequant(const uint8_t* packed, int64_t rows, int64_t 
 /* ------------------------------------------------------------------------ */
 /*
  * One workspace serves flint_moe_route, flint_moe_gate_up,
- * flint_moe_down_combine and flint_moe_decode for one layer shape; layers of
- * the same shape may share it when their calls are issued in order on one
- * stream. It holds a control header (router arrival counter, status word),
- * the router's FP32 logits [8, E] and the SwiGLU activations h of the routed
- * [8, k, I] and shared [8, I_shared] experts (bf16).
+ * flint_moe_down_combine, flint_moe_decode, flint_moe_layer and
+ * flint_moe_block for one layer shape; layers of the same shape may share it
+ * when their calls are issued in order on one stream. It holds a control
+ * header (router arrival counter, status word, the fused layer's call counter
+ * and finished-CTA count, the wait budget, a test hook), the router's FP32
+ * logits [8, E] and the bf16 SwiGLU activations h of the routed [8, k, I] and
+ * shared [8, I_shared] experts (flint_moe_route / flint_moe_decode), then the
+ * fused layer's tagged router scores and h, its per-expert outputs d
+ * [8, k, hidden] and [8, hidden], and one arrival counter per 16 output rows.
  *   - Must be 256-byte aligned and zero-filled before first use
- *     (flint_workspace_init). Every call leaves the counter at 0 again.
+ *     (flint_workspace_init). Every completed call leaves the counters ready
+ *     for the next.
  *   - Calls that use one workspace must not overlap on the GPU except as the
- *     PDL chain route -> gate_up -> down_combine -> next route allows.
+ *     PDL chain route -> gate_up -> down_combine -> next route allows (and
+ *     fused-layer calls chained with FLINT_PDL, which wait for the previous
+ *     kernel before touching the workspace).
+ *   - flint_moe_route and flint_moe_decode need only the regions up to the
+ *     routed experts' h; any `hidden` (0 included) sizes a workspace for them.
  */
-size_t flint_workspace_bytes(int num_experts, int top_k, int inter, int inter_shared);
+size_t flint_workspace_bytes(int num_experts, int top_k, int hidden, int inter, int inter_shared);
 flint_status_t flint_workspace_init(void* ws, size_t ws_bytes, void* stream);
-/* Synchronises `stream`, reads the status word, clears it, and returns
- * FLINT_ERR_TIMEOUT if a kernel recorded a timed-out wait, else FLINT_OK. */
+/* Synchronises `stream`, reads the status word and returns:
+ *   FLINT_ERR_TIMEOUT if a kernel recorded a timed-out wait: the whole
+ *     workspace is then re-initialised (zero-filled, as flint_workspace_init),
+ *     because the counters the kernels synchronise on may have been left
+ *     mid-call. Until this check runs, every later fused-layer call on the
+ *     workspace returns at once without writing its outputs;
+ *   FLINT_ERR_INVALID_ARG if flint_moe_decode was given an expert id outside
+ *     [0, num_experts) (the status word is cleared);
+ *   FLINT_ERR_UNSUPPORTED if a fused-layer CTA's work exceeded its shared-memory
+ *     plan (not expected; the workspace is re-initialised as after a timeout);
+ *   FLINT_OK otherwise. */
 flint_status_t flint_workspace_check(void* ws, size_t ws_bytes, void* stream);
+/* Sets the budget of every bounded device-side wait of the kernels that use
+ * this workspace to budget_us microseconds (0 restores the default of 2 s).
+ * A wait that runs out records FLINT_ERR_TIMEOUT (see flint_workspace_check).
+ * Synchronises `stream`. */
+flint_status_t flint_workspace_set_wait_budget(void* ws, size_t ws_bytes, uint32_t budget_us, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* MoE layer                                                                 */
@@ -274,20 +297,25 @@ flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, 
  * router GEMV + sigmoid top-k + renormalisation (as flint_moe_route), the
  * gate/up GEMVs + SiLU and the down GEMVs + combine (as flint_moe_decode).
  * ("Optimizations": the small-batch MoE path fuses the routing and the
- * combine into the neighbouring expert GEMVs and chains them with PDL; here
- * the three steps meet at two grid-wide barriers inside one launch, one CTA
- * per SM, all CTAs resident by a cooperative launch.)
- *   x [T, H] bf16 (H = routed->hidden), router_w [E, H] bf16 with E =
- *   routed->num_experts, bias [E] FP32 or NULL, 1 <= k <= min(8, E).
- *   ids [T, k] int32 and weights [T, k] FP32 are written (as flint_moe_route
- *   would); y [T, H] bf16 out. shared may be NULL.
- *   ws: the layer's workspace (flint_workspace_bytes(E, k, inter, inter_shared)),
- *   initialised once; its header also holds the grid barrier's counters, which
- *   a completed call leaves ready for the next. A grid barrier that waits too
- *   long records FLINT_ERR_TIMEOUT in the status word (flint_workspace_check)
- *   instead of hanging; re-initialise the workspace after such an error.
+ * combine into the neighbouring expert GEMVs and chains them with PDL so that
+ * each kernel loads its weights while the previous one runs.) One CTA per SM,
+ * all resident (cooperative launch). A group of CTAs runs the shared expert,
+ * whose weights they start loading before the PDL wait; the rest split the
+ * selected experts' gate/up pairs and down rows by cost. CTAs exchange the
+ * router scores and h through tagged words in the workspace (no grid-wide
+ * barrier), and the combine of each 16-row block of y is done by the CTA that
+ * delivers its last expert output.
+ *   x [T, H] bf16 (H = routed->hidden, H % 1024 == 0, H <= 8192), router_w
+ *   [E, H] bf16 with E = routed->num_experts, bias [E] FP32 or NULL,
+ *   1 <= k <= min(8, E). ids [T, k] int32 and weights [T, k] FP32 are written
+ *   (as flint_moe_route would); y [T, H] bf16 out. shared may be NULL.
+ *   ws: the layer's workspace (flint_workspace_bytes(E, k, H, inter,
+ *   inter_shared)), initialised once. A wait that runs out (the budget of
+ *   flint_workspace_set_wait_budget, 2 s by default) records FLINT_ERR_TIMEOUT
+ *   in the status word instead of hanging; flint_workspace_check reports it
+ *   and re-initialises the workspace.
  *   flags: FLINT_PDL lets the launch overlap the previous kernel of the stream
- *   (this kernel waits for it before reading x).
+ *   (this kernel waits for it before reading x or the workspace).
  *   Errors: FLINT_ERR_UNSUPPORTED when one CTA's shared memory cannot hold
  *   the layer's working set, the device cannot co-schedule one CTA per SM, or
  *   the experts are not NVFP4.
@@ -413,6 +441,18 @@ const char* flint_status_string(flint_status_t status);
  * records a timeout in the workspace status word, which flint_workspace_check
  * then reports as FLINT_ERR_TIMEOUT. Faults nothing; the context stays usable. */
 flint_status_t flint_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t budget_ns, void* stream);
+
+/*
+ * flint_selftest_lose_cta -- test hook for the fused layer's failure path
+ * (no counterpart in the method). On the next flint_moe_layer /
+ * flint_moe_block call with this workspace, CTA `cta` publishes no router
+ * scores, as if it had been lost: the other CTAs' bounded waits for those
+ * scores run out (after the budget of flint_workspace_set_wait_budget), the
+ * kernel records FLINT_ERR_TIMEOUT and every CTA returns. Nothing faults or
+ * hangs. flint_workspace_check then reports the timeout and re-initialises the
+ * workspace, which also clears the hook. Synchronises `stream`.
+ */
+flint_status_t flint_selftest_lose_cta(void* ws, size_t ws_bytes, int cta, void* stream);
 
 #ifdef __cplusplus
 }

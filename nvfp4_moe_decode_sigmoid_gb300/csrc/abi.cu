@@ -188,41 +188,40 @@ bool down_bf16_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
     return found;
 }
 
-// Shapes of the fused layer kernel: gate/up ring slots (up to 4 per warp),
-// down tasks of 16 or 8 rows with up to 4 slots, shrunk until the CTA fits.
+// Shapes of the fused layer kernel. The shared expert gets the CTAs
+// [0, Gs), in proportion to its cost among all the layer's experts: a row of
+// an expert costs ~ 2 + the tokens that use it (decoding the codes once,
+// then a multiply-add per token), with the routed experts' token count at
+// its expected T k / min(E, T k). The ring takes as many slots of
+// 2 x kLayerWarps gate/up rows (up to 4) as shared memory allows, at least 2.
 bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     const int G = sm_count;
-    const long long units = a.T * a.k < a.E ? a.T * a.k : a.E;
-    a.rpc = ceil_div(a.E, G);
-    a.shp = a.Is > 0 ? ceil_div(a.Is, G) : 0;
-    a.rows_max = ceil_div(a.H, G);
-    const int routed_items = ceil_div(units * a.I, G);
-    a.res_items = a.shp + routed_items;
-    const int per_warp3 = ceil_div(routed_items, flint::kLayerWarps);
-    const long long rs_r = flint::nvfp4_row_stride(a.I);
-    // Small batches: prefetch every routed down row right after routing, in
-    // groups of 8 rows when 16-row groups would leave warps idle.
-    for (int ns3 = per_warp3 < 1 ? 1 : (per_warp3 > 4 ? 4 : per_warp3); ns3 >= 1; --ns3) {
-        a.ns3 = ns3;
-        a.rg = units * ceil_div(a.rows_max, 16) < flint::kLayerWarps ? 8 : 16;
-        a.ns4 = 0;
-        a.slot4 = 0;
-        a.dpre = 1;
-        if (flint::layer_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin && ns3 >= (per_warp3 < 2 ? per_warp3 : 2))
-            return true;
+    const int T = a.T, H = a.H;
+    const int units = a.T * a.k < a.E ? a.T * a.k : a.E;
+    if (a.s_gu) {
+        const double n_routed = (double)T * a.k / units;
+        const double cs = (2.0 + T) * a.Is, cr = units * (2.0 + n_routed) * a.I;
+        int gs = (int)(G * cs / (cs + cr) + 0.5);
+        a.Gs = gs < 1 ? 1 : (gs > G / 2 ? G / 2 : gs);
+    } else {
+        a.Gs = 0;
     }
-    a.dpre = 0;
-    for (int rg : {16, 8}) {
-        const int per_warp4 = ceil_div(units * ceil_div(a.rows_max, rg), flint::kLayerWarps);
-        for (int ns3 = per_warp3 < 1 ? 1 : (per_warp3 > 4 ? 4 : per_warp3); ns3 >= 1; --ns3) {
-            for (int ns4 = per_warp4 < 1 ? 1 : (per_warp4 > 4 ? 4 : per_warp4); ns4 >= 1; --ns4) {
-                a.ns3 = ns3;
-                a.rg = rg;
-                a.ns4 = ns4;
-                a.slot4 = (int)(rg * rs_r);
-                if (flint::layer_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin) return true;
-            }
-        }
+    a.rpc = ceil_div(a.E, G);
+    const int RS = (int)flint::nvfp4_row_stride(H);
+    a.slot = 2 * flint::kLayerWarps * RS;
+    // a down chunk takes whole 16-row blocks
+    const int kmax = a.I > a.Is ? a.I : a.Is;
+    if (a.slot / flint::nvfp4_row_stride(kmax) < 16) return false;
+    // staging: x, later the h of at most two routed experts (all tokens) or of the shared expert
+    const size_t x_vals = 2 * (size_t)T * H, x_sc = 4 * (size_t)T * (H / 32);
+    const size_t h_r = 2 * (2 * (size_t)T * a.I), h_s = 2 * (size_t)T * a.Is;  // two routed experts, or the shared one
+    const size_t h_vals = h_r > h_s ? h_r : h_s;
+    const size_t h_sc = 4 * (size_t)T * ((2 * a.I > a.Is ? 2 * a.I : a.Is) / 32);
+    a.stage_vals = (int)(x_vals > h_vals ? x_vals : h_vals);
+    a.stage_scales = (int)(x_sc > h_sc ? x_sc : h_sc);
+    for (int ns = flint::kLayerMaxSlots; ns >= 2; --ns) {
+        a.ns = ns;
+        if (flint::layer_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin) return true;
     }
     return false;
 }
@@ -252,9 +251,9 @@ int64_t flint_nvfp4_packed_bytes(int64_t n_mats, int64_t rows, int64_t cols) {
 
 int64_t flint_gguf_nvfp4_bytes(int64_t n_mats, int64_t rows, int64_t cols) { return n_mats * rows * (cols / 64) * 36; }
 
-size_t flint_workspace_bytes(int num_experts, int top_k, int inter, int inter_shared) {
-    if (num_experts < 0 || top_k < 0 || inter < 0 || inter_shared < 0) return 0;
-    return flint::ws_layout(num_experts, top_k, inter, inter_shared).total;
+size_t flint_workspace_bytes(int num_experts, int top_k, int hidden, int inter, int inter_shared) {
+    if (num_experts < 0 || top_k < 0 || hidden < 0 || inter < 0 || inter_shared < 0) return 0;
+    return flint::ws_layout(num_experts, top_k, hidden, inter, inter_shared).total;
 }
 
 flint_status_t flint_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -273,15 +272,21 @@ flint_status_t flint_workspace_check(void* ws, size_t ws_bytes, void* stream) {
     const bool timeout = (st & (flint::kStatusTimeoutRoute | flint::kStatusTimeoutGateUp | flint::kStatusTimeoutDown |
                                 flint::kStatusTimeoutSelftest | flint::kStatusTimeoutLayer |
                                 flint::kStatusTimeoutPrefill)) != 0;
-    // After a timed-out wait the counters the kernels synchronise on (the
-    // router's arrival counter, the grid barrier's ticket) may be left
-    // mid-round: the whole workspace is re-initialised, as flint_workspace_init
-    // does. Otherwise only the status word is cleared.
-    e = cudaMemsetAsync(timeout ? ws : static_cast<void*>(ws_status(ws)), 0, timeout ? ws_bytes : sizeof st,
+    // After a timed-out wait (or a fused-layer CTA that stopped) the counters
+    // the kernels synchronise on (the router's arrival counter, the fused
+    // layer's call counter and arrival counters) may be left mid-call: the
+    // whole workspace is re-initialised, as flint_workspace_init does.
+    // Otherwise only the status word is cleared.
+    const bool reinit = timeout || (st & flint::kStatusLayerPlan) != 0;
+    e = cudaMemsetAsync(reinit ? ws : static_cast<void*>(ws_status(ws)), 0, reinit ? ws_bytes : sizeof st,
                         as_stream(stream));
     if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status");
     if (timeout) return fail(FLINT_ERR_TIMEOUT, "device wait timed out (status 0x%x); workspace re-initialised", st);
+    if (st & flint::kStatusLayerPlan)
+        return fail(FLINT_ERR_UNSUPPORTED,
+                    "a fused-layer CTA's work exceeded its shared-memory plan (status 0x%x); workspace re-initialised",
+                    st);
     return fail(FLINT_ERR_INVALID_ARG, "an expert id was outside [0, num_experts) (status 0x%x)", st);
 }
 
@@ -345,7 +350,7 @@ flint_status_t flint_moe_route(const flint_bf16* x, int T, int H, const flint_bf
     if (!x || !router_w || !ids || !weights || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) ||
         !aligned(weights, 4) || (bias && !aligned(bias, 4)))
         return fail(FLINT_ERR_INVALID_ARG, "route: null or misaligned pointer");
-    flint_status_t s = check_ws(ws, ws_bytes, flint::ws_layout(E, 0, 0, 0).h_routed_off);
+    flint_status_t s = check_ws(ws, ws_bytes, flint::ws_layout(E, 0, 0, 0, 0).h_routed_off);
     if (s != FLINT_OK) return s;
     DevInfo d;
     if ((s = device_info(d)) != FLINT_OK) return s;
@@ -395,8 +400,8 @@ flint_status_t flint_moe_gate_up(const flint_bf16* x, int T, const int32_t* ids,
     if (!x || !ids || !aligned(x, 16) || !aligned(ids, 4))
         return fail(FLINT_ERR_INVALID_ARG, "gate_up: null or misaligned x/ids");
     const int Is = shared ? shared->inter : 0;
-    const flint::WsLayout L = flint::ws_layout(routed->num_experts, k, routed->inter, Is);
-    if ((s = check_ws(ws, ws_bytes, L.total)) != FLINT_OK) return s;
+    const flint::WsLayout L = flint::ws_layout(routed->num_experts, k, 0, routed->inter, Is);
+    if ((s = check_ws(ws, ws_bytes, L.scores_off)) != FLINT_OK) return s;
     DevInfo d;
     if ((s = device_info(d)) != FLINT_OK) return s;
     flint::GateUpArgs a = {};
@@ -440,8 +445,8 @@ flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* we
     if (!ids || !weights || !y || !aligned(ids, 4) || !aligned(weights, 4) || !aligned(y, 16))
         return fail(FLINT_ERR_INVALID_ARG, "down_combine: null or misaligned ids/weights/y");
     const int Is = shared ? shared->inter : 0;
-    const flint::WsLayout L = flint::ws_layout(routed->num_experts, k, routed->inter, Is);
-    if ((s = check_ws(ws, ws_bytes, L.total)) != FLINT_OK) return s;
+    const flint::WsLayout L = flint::ws_layout(routed->num_experts, k, 0, routed->inter, Is);
+    if ((s = check_ws(ws, ws_bytes, L.scores_off)) != FLINT_OK) return s;
     DevInfo d;
     if ((s = device_info(d)) != FLINT_OK) return s;
     flint::DownArgs a = {};
@@ -556,23 +561,32 @@ static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, cons
         !aligned(weights, 4) || !aligned(y, 16) || (bias && !aligned(bias, 4)))
         return fail(FLINT_ERR_INVALID_ARG, "%s: null or misaligned pointer", what);
     const int Is = shared ? shared->inter : 0;
-    const flint::WsLayout W = flint::ws_layout(E, k, routed->inter, Is);
+    const int H = routed->hidden;
+    if (H > flint::kLayerMaxHidden)
+        return fail(FLINT_ERR_UNSUPPORTED, "%s: hidden %d above %d", what, H, flint::kLayerMaxHidden);
+    const flint::WsLayout W = flint::ws_layout(E, k, H, routed->inter, Is);
     if ((s = check_ws(ws, ws_bytes, W.total)) != FLINT_OK) return s;
     DevInfo d;
     if ((s = device_info(d)) != FLINT_OK) return s;
+    uint8_t* wb = static_cast<uint8_t*>(ws);
     flint::LayerArgs a = {};
     a.x = x;
     a.T = T;
-    a.H = routed->hidden;
+    a.H = H;
     a.wr = router_w;
     a.E = E;
     a.bias = bias;
     a.k = k;
     a.ids = ids;
     a.weights = weights;
-    a.logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + W.logits_off);
+    a.hdr = reinterpret_cast<uint32_t*>(ws);
     a.status = ws_status(ws);
-    a.bar_ticket = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + 8);
+    a.scores = reinterpret_cast<uint64_t*>(wb + W.scores_off);
+    a.h_routed = reinterpret_cast<uint64_t*>(wb + W.th_routed_off);
+    a.h_shared = reinterpret_cast<uint64_t*>(wb + W.th_shared_off);
+    a.d_routed = reinterpret_cast<uint16_t*>(wb + W.d_routed_off);
+    a.d_shared = reinterpret_cast<uint16_t*>(wb + W.d_shared_off);
+    a.counters = reinterpret_cast<uint32_t*>(wb + W.counters_off);
     a.gu = static_cast<const uint8_t*>(routed->gate_up);
     a.down = static_cast<const uint8_t*>(routed->down);
     a.I = routed->inter;
@@ -581,8 +595,6 @@ static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, cons
     a.s_down = shared ? static_cast<const uint8_t*>(shared->down) : nullptr;
     a.Is = Is;
     a.s_ts = shared ? shared->tensor_scale : nullptr;
-    a.h_routed = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + W.h_routed_off);
-    a.h_shared = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + W.h_shared_off);
     a.y = y;
     a.norm = na;
     if (!layer_shape(a, d.sm_count, d.smem_optin))
@@ -718,6 +730,27 @@ flint_status_t flint_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t b
     if ((s = device_info(d)) != FLINT_OK) return s;
     cudaError_t e = flint::launch_selftest_wait(ws_status(ws), budget_ns, as_stream(stream));
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "selftest launch");
+}
+
+// Writes one header word of the workspace (stream-ordered; the source is
+// copied before the call returns).
+static flint_status_t set_header_word(void* ws, size_t ws_bytes, int word, uint32_t v, void* stream,
+                                      const char* what) {
+    flint_status_t s = check_ws(ws, ws_bytes, flint::kWsHeader);
+    if (s != FLINT_OK) return s;
+    cudaError_t e = cudaMemcpyAsync(static_cast<uint32_t*>(ws) + word, &v, sizeof v, cudaMemcpyHostToDevice,
+                                    as_stream(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+    return e == cudaSuccess ? FLINT_OK : cuda_fail(e, what);
+}
+
+flint_status_t flint_workspace_set_wait_budget(void* ws, size_t ws_bytes, uint32_t budget_us, void* stream) {
+    return set_header_word(ws, ws_bytes, flint::kHdrBudget, budget_us, stream, "setting the wait budget");
+}
+
+flint_status_t flint_selftest_lose_cta(void* ws, size_t ws_bytes, int cta, void* stream) {
+    if (cta < 0) return fail(FLINT_ERR_INVALID_ARG, "selftest_lose_cta: cta %d", cta);
+    return set_header_word(ws, ws_bytes, flint::kHdrLoseCta, (uint32_t)cta + 1u, stream, "setting the test hook");
 }
 
 }  // extern "C"

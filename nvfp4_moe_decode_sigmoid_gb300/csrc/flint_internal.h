@@ -30,6 +30,7 @@ enum : uint32_t {
     kStatusBadExpertId = 1u << 4,
     kStatusTimeoutLayer = 1u << 5,
     kStatusTimeoutPrefill = 1u << 6,
+    kStatusLayerPlan = 1u << 7,  // a fused-layer CTA's work exceeded the shared-memory plan (not expected)
 };
 
 constexpr int kThreads = 256;       // router kernel: 8 warps
@@ -40,7 +41,13 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kGemvWarps = 24;
 constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kMaxSlotsPerWarp = 4;
-constexpr size_t kWsHeader = 256;   // router counter (word 0), status (word 1), 64-bit grid barrier ticket (bytes 8..15)
+constexpr size_t kWsHeader = 256;   // control words, below
+// Workspace header words (uint32): the router's arrival counter, the status
+// word, the fused layer's call counter (the tag of its published values is
+// the counter + 1) and its count of finished CTAs, the bounded waits' budget
+// in microseconds (0: kWaitBudgetNs), and a test hook (c + 1: CTA c of the
+// next fused-layer call publishes no router scores).
+enum : int { kHdrRouteCounter = 0, kHdrStatus = 1, kHdrEpoch = 4, kHdrDone = 5, kHdrBudget = 6, kHdrLoseCta = 7 };
 // Expert GEMV kernels for BF16 weights: 16 warps (a BF16 row is 4x the bytes
 // of an NVFP4 row, so fewer, larger ring slots per SM).
 constexpr int kBf16Warps = 16;
@@ -48,19 +55,34 @@ constexpr int kBf16Threads = kBf16Warps * 32;
 // Fused layer kernel: one cooperative CTA per SM.
 constexpr int kLayerWarps = 24;
 constexpr int kLayerThreads = kLayerWarps * 32;
+constexpr int kLayerMaxSlots = 4;        // ring slots of one CTA
+constexpr int kLayerMaxHidden = 8192;    // largest hidden size of the fused layer
 
 FLINT_HD constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Workspace regions, from the layer shape.
+// Workspace regions, from the layer shape: the router's FP32 logits and the
+// bf16 h of the routed / shared experts (flint_moe_route, flint_moe_decode);
+// then the fused layer's tagged router scores [8][E] and tagged h (64-bit
+// words: tag, value), its bf16 per-expert outputs d of the routed ranks
+// [8][k][H] and of the shared expert [8][H], and its per-16-row-block
+// arrival counters [H / 16].
 struct WsLayout {
-    size_t logits_off, h_routed_off, h_shared_off, total;
+    size_t logits_off, h_routed_off, h_shared_off, scores_off, th_routed_off, th_shared_off, d_routed_off,
+        d_shared_off, counters_off, total;
 };
-inline WsLayout ws_layout(int E, int k, int I, int Is) {
+inline WsLayout ws_layout(int E, int k, int H, int I, int Is) {
     WsLayout L;
+    const size_t Tm = FLINT_MAX_TOKENS;
     L.logits_off = kWsHeader;
-    L.h_routed_off = align_up(L.logits_off + sizeof(float) * FLINT_MAX_TOKENS * (size_t)E, 256);
-    L.h_shared_off = align_up(L.h_routed_off + 2 * (size_t)FLINT_MAX_TOKENS * k * I, 256);
-    L.total = align_up(L.h_shared_off + 2 * (size_t)FLINT_MAX_TOKENS * (size_t)Is, 256);
+    L.h_routed_off = align_up(L.logits_off + sizeof(float) * Tm * (size_t)E, 256);
+    L.h_shared_off = align_up(L.h_routed_off + 2 * Tm * k * (size_t)I, 256);
+    L.scores_off = align_up(L.h_shared_off + 2 * Tm * (size_t)Is, 256);
+    L.th_routed_off = align_up(L.scores_off + 8 * Tm * (size_t)E, 256);
+    L.th_shared_off = align_up(L.th_routed_off + 8 * Tm * k * (size_t)I, 256);
+    L.d_routed_off = align_up(L.th_shared_off + 8 * Tm * (size_t)Is, 256);
+    L.d_shared_off = align_up(L.d_routed_off + 2 * Tm * k * (size_t)H, 256);
+    L.counters_off = align_up(L.d_shared_off + 2 * Tm * (size_t)H, 256);
+    L.total = align_up(L.counters_off + 4 * (size_t)(H / 16), 256);
     return L;
 }
 
@@ -150,9 +172,14 @@ struct LayerArgs {
     int k;
     int32_t* ids;        // [T][k] out
     float* weights;      // [T][k] out
-    float* logits;       // workspace [8][E]: the sigmoid scores (bits) of the router logits
-    unsigned long long* bar_ticket; // workspace bytes 8..15: grid barrier tickets (a multiple of the grid size between calls)
-    uint32_t* status;    // workspace word 1
+    uint32_t* hdr;       // workspace header (kHdr* words)
+    uint32_t* status;    // hdr + kHdrStatus
+    uint64_t* scores;    // workspace [8][E]: tagged sigmoid scores
+    uint64_t* h_routed;  // workspace [8][k][I]: tagged h
+    uint64_t* h_shared;  // workspace [8][Is]
+    uint16_t* d_routed;  // workspace [8][k][H]: bf16 d of each rank
+    uint16_t* d_shared;  // workspace [8][H]
+    uint32_t* counters;  // workspace [H / 16]: arrivals per row block (0 between calls)
     const uint8_t* gu;   // routed E x [2I, H]
     const uint8_t* down; // routed E x [H, I]
     int I;
@@ -161,16 +188,11 @@ struct LayerArgs {
     const uint8_t* s_down;
     int Is;
     const float* s_ts;
-    uint16_t* h_routed;  // workspace [8][k][I]
-    uint16_t* h_shared;  // workspace [8][Is]
     uint16_t* y;         // [T][H] out
+    int Gs;              // CTAs [0, Gs) run the shared expert
     int rpc;             // router rows per CTA
-    int shp;             // shared-expert pairs per CTA (bound)
-    int rows_max;        // output rows per CTA (bound)
-    int res_items;       // gate/up items per CTA (bound)
-    int ns3;             // gate/up ring slots per warp
-    int rg, ns4, slot4;  // down: rows per task, ring slots per warp, bytes per slot
-    int dpre;            // 1: all of the CTA's routed down rows are prefetched after routing
+    int ns, slot;        // ring slots per CTA and bytes per slot
+    int stage_vals, stage_scales;  // bytes of the staging region (x, later h) and of its chunk scales
     NormArgs norm;       // norm.r set: x = the norm of the residual stream (x unused)
 };
 

@@ -5,30 +5,35 @@
 // "Day-0 Support for Flint on vLLM", section "Optimizations": the small-batch
 // MoE path is a short chain of kernels whose expert GEMVs read only the
 // selected experts' weights, with routing and the combine fused into the
-// neighbouring GEMVs. Here the chain is one launch: at batch 1 to 8 the
-// layer moves 13-80 MB, a few microseconds of HBM time, so the fixed cost of
-// each kernel boundary (launch, prologue, drain) is a large share; inside one
-// kernel the three steps meet at two grid-wide barriers instead.
+// neighbouring GEMVs, each kernel launched with programmatic dependent launch
+// so that it loads its weights while the previous kernel still runs. Here the
+// chain is one launch, one CTA per SM, all CTAs resident (cooperative launch),
+// and no CTA ever waits for the whole grid:
 //
-// One CTA per SM, all resident (cooperative launch):
-//   0. Before the PDL wait: this CTA's router rows, its slice of the shared
-//      expert's gate/up pairs and its slice of the shared expert's down rows
-//      are copied into shared memory (static weights).
-//   1. x is staged (chunk-scaled f16, for gate/up); for a pre-norm block
-//      every CTA first computes x = rmsnorm(r + y_prev) itself from the
-//      residual stream and writes its share of the new residual out. The
-//      CTA's router logits are computed in FP32 from the staged x and bf16
-//      router rows; their sigmoid scores go to the workspace. Grid barrier.
-//   2. Every CTA reads all scores and selects the top-k of every token itself
-//      (one warp per token, straight from L2), so no second barrier is needed
-//      to share the routing; CTA 0 also writes ids and weights out.
-//   3. gate/up + SiLU as in gate_up_kernel: the CTA's share of the routed
-//      pairs through per-warp cp.async rings, its shared-expert pairs from
-//      shared memory; h goes to the workspace. Grid barrier.
-//   4. down + combine as in down_kernel: h is staged, the CTA's output rows of
-//      every selected expert stream through per-warp rings (the shared
-//      expert's rows are already resident), then y = bf16(sum_j w_j d_j +
-//      d_shared) in rank order.
+//   * The CTAs are split by expert. CTAs [0, Gs) run the shared expert (it
+//     needs no routing); CTAs [Gs, G) run the routed experts the tokens
+//     selected. Each CTA owns one contiguous, cost-balanced range of gate/up
+//     pairs and one of down-row blocks in the concatenation of its group's
+//     experts (cost of an expert's row ~ 2 + the tokens that chose it), so a
+//     CTA touches one or two experts and streams their rows as a few large
+//     bulk copies (TMA) into a CTA-wide ring of shared-memory slots.
+//   * Before the PDL wait each CTA starts the copies of its static weights:
+//     its router rows, and in the shared group all of its shared-expert rows.
+//   * Router scores and h are published as 64-bit words that carry the call's
+//     tag beside the value, so a reader polls the data itself (no counter, no
+//     barrier, no separate flag read): every CTA reads all scores and selects
+//     the top-k itself; a CTA that computes down rows of an expert reads that
+//     expert's h (only that expert's) once every value carries the tag.
+//   * The combine y = bf16(sum_j w_j d_j + d_shared) runs per 16-row block:
+//     each expert's down CTA writes its d rows and counts its arrival on the
+//     block's counter; the CTA that arrives last (all experts' d present)
+//     combines the block in rank order and resets the counter. Nothing waits.
+//
+// The tag is the workspace's call counter plus one; the last CTA to finish
+// advances the counter. After a timed-out wait (or any other failure that
+// stops a CTA) the workspace must be re-initialised (flint_workspace_check
+// does it); until then every call returns at once, leaving its outputs
+// unwritten, and the status stays set.
 #include "expert_common.cuh"
 #include "router_common.cuh"
 
@@ -37,465 +42,630 @@ namespace {
 
 constexpr int kLW = kLayerWarps;
 constexpr int kLT = kLayerThreads;
+constexpr int kMaxChunks = 96;
+constexpr int kMaxDownUnits = 4;
+constexpr int kMaxVec = kMaxDownUnits * FLINT_MAX_TOKENS;
+constexpr int kRowBlock = 16;                 // output rows per combine block
+constexpr int kSharedUnit = -1;
+constexpr int kShIdx = kMaxDistinct;          // index of the shared expert in the per-unit arrays
+// Status bits after which a call must not run: its tags could repeat an
+// unfinished call's (the call counter did not advance).
+constexpr uint32_t kStatusPoisonMask = kStatusTimeoutRoute | kStatusTimeoutGateUp | kStatusTimeoutDown |
+                                       kStatusTimeoutSelftest | kStatusTimeoutLayer | kStatusTimeoutPrefill |
+                                       kStatusLayerPlan;
 
-// Small per-CTA arrays: tensor scales (gate, up) of the distinct experts then
-// of the shared expert; down scales of the units; combine weights; ids.
-struct LayerSmall {
-    uint64_t dbar;  // completion of the prefetched down rows
-    uint64_t rbar[kLayerWarps * 4];  // the gate/up ring slots of each warp (up to 4)
-    float tss[2 * kMaxDistinct + 2];
-    float tsd[kMaxDistinct + 1];
-    float w[kMaxDistinct];
-    int32_t ids[kMaxDistinct];
-    float ninv[FLINT_MAX_TOKENS];  // per-token 1 / rms of the normalised input
+enum : int8_t { kChunkGateUp = 0, kChunkDown = 1 };
+
+// One ring chunk: `count` gate/up pairs (gate rows then up rows, two bulk
+// copies) or `count` down rows (one bulk copy) of one expert.
+struct Chunk {
+    int8_t kind;
+    int8_t q;       // down chunks: index of the expert among the CTA's down experts
+    int16_t unit;   // index into the distinct-expert list, or kSharedUnit
+    int32_t start, count;
 };
 
-// Shared memory, by lifetime:
-//   persistent: routing view, small arrays, the shared expert's down rows;
-//   phases 0-3 (region U1): staged x and its chunk scales (and the norm's
-//     per-chunk sums of squares when the input is normalised here), the shared
-//     expert's gate/up pairs, then one of: router rows (phases 0-1), raw
-//     gate/up sums + the gate/up rings (phase 3);
-//   phase 4 (region U4, over U1): staged h and its chunk scales, d values,
-//     the down rings;
-//   the prefetched down rows (a.dpre), beside both.
+struct LayerSmall {
+    uint64_t full[kLayerMaxSlots];   // ring slot s holds its chunk's bytes
+    uint64_t rbar;                   // the router rows are in
+    uint32_t rel[kLayerMaxSlots];    // warps done with the slot's current chunk
+    int32_t last_issued[kLayerMaxSlots];
+    uint32_t hdr[8];                 // workspace header at the start of the call
+    int n_chunks, n_gu, fail, n_last;
+    int b0, b1;                      // this CTA's down range, in (expert, row block) items
+    Chunk chunk[kMaxChunks];
+    int n_dn;                        // experts among the down chunks
+    int16_t dn_unit[kMaxDownUnits];
+    int16_t vec[kMaxDownUnits][FLINT_MAX_TOKENS];  // staged h vector of (down expert, token), or -1
+    int n_vec;
+    int32_t v_item0[kMaxVec + 1];    // first 32-value staging item of each vector
+    int32_t v_off[kMaxVec];          // byte offset of its f16 values in the staging region
+    int32_t v_coff[kMaxVec];         // byte offset of its chunk scales
+    int16_t v_q[kMaxVec], v_t[kMaxVec];
+    float tsg[kMaxDistinct + 1], tsu[kMaxDistinct + 1], tsd[kMaxDistinct + 1];
+    float w[kMaxDistinct];
+    int32_t ids[kMaxDistinct];
+    int32_t cumw[2 * 32];            // inclusive prefix of the experts' cost weights
+    float res[kLW][2][FLINT_MAX_TOKENS];  // a warp's raw gate / up sums per token
+    float ninv[FLINT_MAX_TOKENS];
+    int16_t last[kLayerMaxHidden / kRowBlock];  // row blocks this CTA combines
+};
+
+// Shared memory: small arrays, the routing view, the staging region (x, then
+// h of the CTA's down experts) and its chunk scales, the norm's partial sums,
+// the router rows (later: all sigmoid scores for the top-k), the ring.
 struct LayerSmem {
-    size_t ri, small, shdn, U;
-    size_t xs, csc, nred, shgu, V;
-    size_t wrows;
-    size_t resg, resu, ring3;
-    size_t hr, hs, csr, css, dval, ring4;
-    size_t dpre;
-    size_t total;
+    size_t small, ri, xs, csc, nred, rows, ring, total;
 };
 
 __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     LayerSmem L;
-    const size_t RS = (size_t)nvfp4_row_stride(a.H), RSs = a.Is ? (size_t)nvfp4_row_stride(a.Is) : 0;
     const size_t T = a.T, H = a.H;
-    L.ri = 0;
-    L.small = align_up(sizeof(RouteInfo), 128);
-    L.shdn = align_up(L.small + sizeof(LayerSmall), 128);
-    L.U = align_up(L.shdn + (size_t)a.rows_max * RSs, 128);
-    // U1
-    L.xs = L.U;
-    L.csc = align_up(L.xs + 2 * T * H, 128);
-    L.nred = align_up(L.csc + sizeof(float) * T * (H / 32), 128);
-    L.shgu = align_up(L.nred + (a.norm.r ? sizeof(float) * T * (H / 32) : 0), 128);
-    L.V = align_up(L.shgu + 2 * (size_t)a.shp * RS, 128);
-    L.wrows = L.V;
-    L.resg = L.V;
-    L.resu = align_up(L.resg + sizeof(float) * (size_t)a.res_items * T, 128);
-    L.ring3 = align_up(L.resu + sizeof(float) * (size_t)a.res_items * T, 128);
-    size_t end1 = L.ring3 + (size_t)kLW * a.ns3 * 2 * RS;
-    const size_t e_rows = L.wrows + 2 * (size_t)a.rpc * H;
-    if (end1 < e_rows) end1 = e_rows;
-    // U4
-    L.hr = L.U;
-    L.hs = align_up(L.hr + 2 * T * a.k * a.I, 128);
-    L.csr = align_up(L.hs + 2 * T * a.Is, 128);
-    L.css = align_up(L.csr + sizeof(float) * T * a.k * (a.I / 32), 128);
-    L.dval = align_up(L.css + sizeof(float) * T * (a.Is / 32), 128);
-    L.ring4 = align_up(L.dval + sizeof(float) * T * (a.k + 1) * a.rows_max, 128);
-    const size_t end4 = L.ring4 + (size_t)kLW * a.ns4 * a.slot4;
-    L.total = end1 > end4 ? end1 : end4;
-    L.dpre = align_up(L.total, 128);
-    if (a.dpre) {
-        const size_t units = (size_t)(a.T * a.k < a.E ? a.T * a.k : a.E);
-        L.total = L.dpre + units * a.rows_max * (size_t)nvfp4_row_stride(a.I);
-    }
+    L.small = 0;
+    L.ri = align_up(sizeof(LayerSmall), 128);
+    L.xs = align_up(L.ri + sizeof(RouteInfo), 128);
+    L.csc = align_up(L.xs + (size_t)a.stage_vals, 128);
+    L.nred = align_up(L.csc + (size_t)a.stage_scales, 128);
+    L.rows = align_up(L.nred + (a.norm.r ? sizeof(float) * T * (H / 32) : 0), 128);
+    const size_t rows_b = 2 * (size_t)a.rpc * H, sc_b = sizeof(uint32_t) * T * a.E;
+    L.ring = align_up(L.rows + (rows_b > sc_b ? rows_b : sc_b), 128);
+    L.total = L.ring + (size_t)a.ns * a.slot;
     return L;
 }
 
-// All threads of the CTA copy `bytes` (a multiple of 16) from src to dst with
-// 16-byte cp.async (no commit).
-__device__ __forceinline__ void block_copy_async(void* dst, const void* src, size_t bytes) {
-    uint8_t* d = static_cast<uint8_t*>(dst);
-    const uint8_t* s = static_cast<const uint8_t*>(src);
-    for (size_t o = 16 * (size_t)threadIdx.x; o < bytes; o += 16 * (size_t)kLT) cp_async16(d + o, s + o);
+// Tagged 64-bit words: the tag in the high half, the value in the low half,
+// one single-copy-atomic store / load at GPU scope.
+__device__ __forceinline__ void st_tagged(uint64_t* p, uint32_t tag, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(((uint64_t)tag << 32) | v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void ld_tagged2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cta_smem(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.cta.shared::cta.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// Position, in the concatenation of D experts of `per` items each, of the
+// cost target tau, where an item of expert u costs w_u and cum[u] is the
+// inclusive prefix of the w_u: the experts before the one that holds tau,
+// plus the items of that expert whose cost lies below tau (rounded up).
+// Monotone in tau, pos(0) = 0, pos(per * cum[D - 1]) = D * per, so the ranges
+// [pos(c total / G'), pos((c + 1) total / G')) tile the items exactly.
+__device__ __forceinline__ int cost_pos(long long tau, const int32_t* cum, int D, int per) {
+    int lo = 0, hi = D;  // first expert u with per * cum[u] > tau
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((long long)per * cum[mid] > tau) hi = mid;
+        else lo = mid + 1;
+    }
+    if (lo >= D) return D * per;
+    const long long before = lo ? (long long)per * cum[lo - 1] : 0;
+    const int wu = cum[lo] - (lo ? cum[lo - 1] : 0);
+    const long long p = (tau - before + wu - 1) / wu;
+    return lo * per + (int)(p < per ? p : per);
+}
+
+// Appends the chunks of the pair range [p0, p1) and the down block range
+// [b0, b1) (items of a concatenation of experts of I_u pairs / NB blocks;
+// unit(i) maps an item's expert position to its unit id). One thread.
+template <typename UnitOf, typename RsOf>
+__device__ void build_chunks(LayerSmall& sm, int p0, int p1, int per_gu, int b0, int b1, int NB, uint32_t* status,
+                             UnitOf unit_of, RsOf rows_per_chunk) {
+    int n = 0;
+    for (int P = p0; P < p1; ) {
+        if (n == kMaxChunks) {
+            sm.fail = 1;  // the host sizes the grid so that this cannot happen
+            atomicOr(status, kStatusLayerPlan);
+            break;
+        }
+        const int u = P / per_gu, p = P - u * per_gu;
+        const int m = min(kLW, min(p1 - P, per_gu - p));
+        sm.chunk[n++] = Chunk{kChunkGateUp, 0, (int16_t)unit_of(u), p, m};
+        P += m;
+    }
+    sm.n_gu = n;
+    int nd = 0;
+    for (int B = b0; B < b1;) {
+        const int u = B / NB, b = B - u * NB;
+        const int unit = unit_of(u);
+        const int take = min(b1 - B, min(NB - b, max(1, rows_per_chunk(unit) / kRowBlock)));
+        if (n == kMaxChunks || (nd == kMaxDownUnits && sm.dn_unit[nd - 1] != unit)) {
+            sm.fail = 1;  // the host sizes the grid so that this cannot happen
+            atomicOr(status, kStatusLayerPlan);
+            break;
+        }
+        if (nd == 0 || sm.dn_unit[nd - 1] != unit) sm.dn_unit[nd++] = (int16_t)unit;
+        sm.chunk[n++] = Chunk{kChunkDown, (int8_t)(nd - 1), (int16_t)unit, b * kRowBlock, take * kRowBlock};
+        B += take;
+    }
+    sm.n_chunks = n;
+    sm.n_dn = nd;
+    sm.b0 = b0;
+    sm.b1 = b1;
 }
 
 // NORM: the input is rmsnorm(r + y_prev) of the residual stream (a.norm), not
 // a.x. Two instantiations, so that the plain layer carries none of the norm's
-// code (measured: the never-taken branch alone cost 3-4 us at T = 8).
+// code (measured: a never-taken norm branch cost 3-4 us at T = 8).
 template <bool NORM>
 __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const LayerSmem L = layer_layout(a);
-    const int T = a.T, H = a.H, E = a.E, k = a.k, I = a.I, Is = a.Is, RM = a.rows_max;
+    const int T = a.T, H = a.H, E = a.E, k = a.k, I = a.I, Is = a.Is;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = blockIdx.x, G = gridDim.x;
-    RouteInfo& ri = *reinterpret_cast<RouteInfo*>(smem + L.ri);
+    const int c = blockIdx.x, G = gridDim.x, Gs = a.Gs, NS = a.ns;
+    const bool sh_cta = c < Gs;
+    const bool has_sh = a.s_gu != nullptr;
     LayerSmall& sm = *reinterpret_cast<LayerSmall*>(smem + L.small);
+    RouteInfo& ri = *reinterpret_cast<RouteInfo*>(smem + L.ri);
     uint4* xh = reinterpret_cast<uint4*>(smem + L.xs);
     float* csc = reinterpret_cast<float*>(smem + L.csc);
-    const uint16_t* wrows = reinterpret_cast<const uint16_t*>(smem + L.wrows);
-    uint8_t* shgu = smem + L.shgu;
-    uint8_t* shdn = smem + L.shdn;
+    uint8_t* ring = smem + L.ring;
     const int RS = (int)nvfp4_row_stride(H), RSr = (int)nvfp4_row_stride(I);
     const int RSs = Is ? (int)nvfp4_row_stride(Is) : 0;
-    const bool has_sh = a.s_gu != nullptr;
-
-    // This CTA's router rows, shared-expert pairs and output rows.
+    const int NB = H / kRowBlock;
     const int r0 = c * a.rpc, nrr = max(0, min(a.rpc, E - r0));
-    const int sp0 = (int)((unsigned)c * (unsigned)Is / (unsigned)G);
-    const int n_sh = has_sh ? (int)((unsigned)(c + 1) * (unsigned)Is / (unsigned)G) - sp0 : 0;
-    const int n0 = (int)((unsigned)c * (unsigned)H / (unsigned)G);
-    const int nr = (int)((unsigned)(c + 1) * (unsigned)H / (unsigned)G) - n0;
+    const uint32_t full_mask = 0xffffffffu;
 
-    // ---- 0: static weights, before the PDL wait ------------------------------------
-    block_copy_async(smem + L.wrows, a.wr + (size_t)r0 * H, (size_t)nrr * H * 2);
-    if (n_sh > 0) {
-        block_copy_async(shgu, a.s_gu + (size_t)sp0 * RS, (size_t)n_sh * RS);
-        block_copy_async(shgu + (size_t)a.shp * RS, a.s_gu + (size_t)(Is + sp0) * RS, (size_t)n_sh * RS);
-        block_copy_async(shdn, a.s_down + (size_t)n0 * RSs, (size_t)nr * RSs);
+    // Issues chunk i into its ring slot (one thread).
+    auto issue = [&](int i) {
+        if (i >= sm.n_chunks) return;
+        const Chunk ch = sm.chunk[i];
+        const int s = i % NS;
+        uint8_t* slot = ring + (size_t)s * a.slot;
+        const bool sh = ch.unit == kSharedUnit;
+        fence_proxy_async_smem();  // the slot's earlier generic reads come first
+        if (ch.kind == kChunkGateUp) {
+            const uint8_t* base = sh ? a.s_gu : a.gu + (size_t)ri.dlist[ch.unit] * 2 * I * RS;
+            const uint32_t bytes = (uint32_t)ch.count * RS;
+            mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
+            bulk_g2s(slot, base + (size_t)ch.start * RS, bytes, &sm.full[s]);
+            bulk_g2s(slot + (size_t)kLW * RS, base + (size_t)((sh ? Is : I) + ch.start) * RS, bytes, &sm.full[s]);
+        } else {
+            const int RSu = sh ? RSs : RSr;
+            const uint8_t* base = sh ? a.s_down : a.down + (size_t)ri.dlist[ch.unit] * H * RSr;
+            const uint32_t bytes = (uint32_t)ch.count * RSu;
+            mbar_arrive_expect_tx(&sm.full[s], bytes);
+            bulk_g2s(slot, base + (size_t)ch.start * RSu, bytes, &sm.full[s]);
+        }
+        sm.last_issued[s] = i;
+    };
+    // Before an early exit: the bulk copies still in flight into this CTA's
+    // shared memory land first (bounded; thread 0).
+    auto drain = [&](uint64_t budget_ns) {
+        if (tid != 0) return;
+        if (nrr > 0) mbar_wait_bounded(&sm.rbar, 0, nullptr, 0, budget_ns);
+        for (int s = 0; s < NS; ++s) {
+            const int j = sm.last_issued[s];
+            if (j >= 0) mbar_wait_bounded(&sm.full[s], (uint32_t)(j / NS) & 1u, nullptr, 0, budget_ns);
+        }
+    };
+    auto rows_per_chunk = [&](int unit) {
+        const int RSu = unit == kSharedUnit ? RSs : RSr;
+        return min(8 * kLW, a.slot / RSu);
+    };
+
+    // ---- 0: before the PDL wait: barriers, static weight copies ----------------------
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&sm.full[s], 1);
+            sm.rel[s] = 0;
+            sm.last_issued[s] = -1;
+        }
+        mbar_init(&sm.rbar, 1);
+        fence_mbar_init();
+        sm.fail = 0;
+        sm.n_last = 0;
+        sm.n_chunks = sm.n_gu = sm.n_dn = 0;
+        if (nrr > 0) {
+            mbar_arrive_expect_tx(&sm.rbar, (uint32_t)(nrr * H * 2));
+            bulk_g2s(smem + L.rows, a.wr + (size_t)r0 * H, (uint32_t)(nrr * H * 2), &sm.rbar);
+        }
+        if (sh_cta) {
+            // the shared expert: an even split of its pairs and row blocks
+            const int p0 = (int)((long long)c * Is / Gs), p1 = (int)((long long)(c + 1) * Is / Gs);
+            const int b0 = (int)((long long)c * NB / Gs), b1 = (int)((long long)(c + 1) * NB / Gs);
+            build_chunks(sm, p0, p1, Is, b0, b1, NB, a.status, [](int) { return kSharedUnit; }, rows_per_chunk);
+            for (int i = 0; i < NS; ++i) issue(i);
+        }
     }
-    cp_async_commit();
-    if (tid < 2 * kMaxDistinct + 2) sm.tss[tid] = 0.f;
-    if (tid == 0) mbar_init(&sm.dbar, 1);
-    if (tid < kLW * 4) mbar_init(&sm.rbar[tid], 1);
-    if (tid <= kLW * 4) fence_mbar_init();
+    // Dependents may launch now: their CTAs take SMs as ours exit, and only
+    // read static weights before their own wait.
+    pdl_launch_dependents();
+    pdl_wait();  // x (or the residual stream) comes from the previous kernel
 
-    pdl_wait();  // x comes from the previous kernel
-
-    // ---- 1: stage x (or the norm of the residual stream); this CTA's router scores --
+    // ---- 1: the call's header, x; this CTA's router scores ---------------------------
+    if (tid == 0) {
+        const uint4 h0 = ld_cg(reinterpret_cast<const uint4*>(a.hdr));
+        const uint4 h1 = ld_cg(reinterpret_cast<const uint4*>(a.hdr) + 1);
+        sm.hdr[0] = h0.x; sm.hdr[1] = h0.y; sm.hdr[2] = h0.z; sm.hdr[3] = h0.w;
+        sm.hdr[4] = h1.x; sm.hdr[5] = h1.y; sm.hdr[6] = h1.z; sm.hdr[7] = h1.w;
+    }
     const StageSrc xsrc[1] = {{a.x, xh, csc, T, H}};
     if constexpr (NORM)
         stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), sm.ninv, c, G);
     else
         stage_f16<false>(xsrc, [] {});
-    cp_async_wait<0>();
     __syncthreads();
-    // logits from the staged (exact, chunk-scaled f16) x: lane l takes the
-    // 32-value chunks l, l + 32, ...; each chunk's FP32 partial sum is
-    // multiplied back by its power-of-two scale
-    for (int q = warp; q < nrr * T; q += kLW) {
-        const int r = q / T, t = q - r * T;
-        const uint4* xb = xh + (size_t)t * (H / 8) + lane;
-        const float* cb = csc + (size_t)t * (H / 32) + lane;
-        const uint4* wv = reinterpret_cast<const uint4*>(wrows + (size_t)r * H);
-        float v = 0.f;
-        for (int m = 0; m < H / 1024; ++m) {
-            const int ch = lane + 32 * m;
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint4 xv = xb[(m * 4 + w) * 32], wq = wv[4 * ch + w];
-                const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xa[i]));
-                    s0 = fmaf(bf16_lo(wa[i]), xf.x, s0);
-                    s1 = fmaf(bf16_hi(wa[i]), xf.y, s1);
-                }
-            }
-            v = fmaf(cb[32 * m], s0 + s1, v);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        // the sigmoid score (its bits), once per logit in the grid
-        if (lane == 0) reinterpret_cast<uint32_t*>(a.logits)[(size_t)t * E + r0 + r] = sigmoid_score(v, a.bias, r0 + r);
-    }
-    if (!grid_sync(a.bar_ticket, a.status, kStatusTimeoutLayer)) return;
-
-    // ---- 2: top-k of every token, in every CTA ------------------------------------
-    float* wsel = sm.w;
-    {
-        if (warp < T) {
-            const uint32_t* sc = reinterpret_cast<const uint32_t*>(a.logits) + (size_t)warp * E;
-            if (E <= 256)
-                topk_warp<8, true>(sc, E, k, lane, sm.ids + warp * k, wsel + warp * k);
-            else
-                topk_warp<FLINT_MAX_EXPERTS / 32, true>(sc, E, k, lane, sm.ids + warp * k, wsel + warp * k);
-        }
-        __syncthreads();
-    }
-    if (c == 0 && tid < T * k) {
-        a.ids[tid] = sm.ids[tid];
-        a.weights[tid] = wsel[tid];
-    }
-    build_route_info<true>(ri, sm.ids, T, k, E, a.status);
-    const int D = ri.D;
-    // The routing is known: this CTA's down rows of every selected expert can
-    // stream in now, behind gate/up, when they fit (one bulk copy per expert).
-    uint8_t* dpre = smem + L.dpre;
-    if (a.dpre && nr > 0 && warp == 0) {
-        if (lane == 0) mbar_arrive_expect_tx(&sm.dbar, (uint32_t)(D * nr * RSr));
-        __syncwarp();
-        for (int u = lane; u < D; u += 32)
-            bulk_g2s(dpre + (size_t)u * nr * RSr, a.down + ((size_t)ri.dlist[u] * H + n0) * RSr,
-                     (uint32_t)(nr * RSr), &sm.dbar);
-    }
-
-    // ---- 3: gate/up + SiLU ---------------------------------------------------------
-    {
-        float* resg = reinterpret_cast<float*>(smem + L.resg);
-        float* resu = reinterpret_cast<float*>(smem + L.resu);
-        const int NSW = a.ns3;
-        uint8_t* ring = smem + L.ring3 + (size_t)warp * NSW * 2 * RS;
-        // The routed pairs in list order (pair q = d I + p: row p of expert
-        // dlist[d]) are dealt out round-robin: CTA c takes pairs c, c + G, ...
-        // (its local items 0, 1, ...) and its warp w the local items w, w + kLW,
-        // .... An expert that several tokens chose costs more per pair, and
-        // dealing spreads its rows evenly over the CTAs and warps; contiguous
-        // ranges left a few CTAs ~1.5x the mean work at T = 8, and the grid
-        // barrier after this phase waits for the slowest.
-        const int RP = D * I;
-        const int nl = c < RP ? (RP - c + G - 1) / G : 0;
-        const int n_items_w = nl > warp ? (nl - warp + kLW - 1) / kLW : 0;
-        // The ring is fed by bulk copies (the copy engine, one lane per warp):
-        // the gate and up rows of an item land in its slot and complete on the
-        // slot's mbarrier. Against all 32 lanes issuing 16-byte cp.async this
-        // frees issue slots in a phase bound by instruction latency and issue.
-        uint64_t* rbar = sm.rbar + warp * 4;
-        auto issue = [&](int m) {  // local item warp + m kLW into slot m % NSW
-            if (lane == 0) {
-                const int q = c + (warp + m * kLW) * G, d = q / I, p = q - d * I;
-                const uint8_t* g = a.gu + ((size_t)ri.dlist[d] * 2 * I + p) * RS;
-                uint8_t* slot = ring + (size_t)(m % NSW) * 2 * RS;
-                uint64_t* bar = rbar + m % NSW;
-                fence_proxy_async_smem();  // the slot's earlier reads come first
-                mbar_arrive_expect_tx(bar, 2u * (uint32_t)RS);
-                bulk_g2s(slot, g, (uint32_t)RS, bar);
-                bulk_g2s(slot + RS, g + (size_t)I * RS, (uint32_t)RS, bar);
-            }
-        };
-        // scales first, then this warp's first copies
-        float tsv = 0.f;
-        if (tid < 2 * D) tsv = ld_cg(a.ts + 3 * ri.dlist[tid >> 1] + (tid & 1));
-        else if (tid < 2 * D + 2 && has_sh) tsv = ld_cg(a.s_ts + tid - 2 * D);
-        float tdv = 0.f;
-        if (tid >= 256 && tid < 256 + D) tdv = ld_cg(a.ts + 3 * ri.dlist[tid - 256] + 2);
-        else if (tid == 256 + D && has_sh) tdv = ld_cg(a.s_ts + 2);
-        for (int m = 0; m < NSW && m < n_items_w; ++m) issue(m);
-        if (tid < 2 * D + 2) sm.tss[tid] = tsv;
-        if (tid >= 256 && tid <= 256 + D) sm.tsd[tid - 256] = tdv;
-        // The warp's work, in one loop so that the pass code is inlined once:
-        // first its shared-expert units (resident; one per (pair, two tokens),
-        // spread over the warps from the last one: every token reads every
-        // shared row, so at T = 8 a shared pair is four units), then its routed
-        // items from the ring.
-        const int ntp = (T + 1) >> 1, su0 = kLW - 1 - warp;
-        const int n_su_w = su0 < n_sh * ntp ? (n_sh * ntp - su0 + kLW - 1) / kLW : 0;
-        int m_fail = -1;  // the item whose copy never landed
-        for (int it = 0; it < n_su_w + n_items_w; ++it) {
-            const int m = it - n_su_w;
-            const uint8_t *grow, *urow;
-            uint32_t tm;
-            int slot;  // row of resg / resu
-            if (m < 0) {
-                const int q = su0 + it * kLW, i = q / ntp, t0 = 2 * (q - i * ntp);
-                grow = shgu + (size_t)i * RS;
-                urow = grow + (size_t)a.shp * RS;
-                tm = (t0 + 1 < T ? 3u : 1u) << t0;  // t0 alone at an odd T
-                slot = i;
-            } else {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(rbar + m % NSW, (uint32_t)(m / NSW) & 1u, a.status,
-                                                               kStatusTimeoutLayer))) {
-                    m_fail = m;
-                    break;
-                }
-                grow = ring + (size_t)(m % NSW) * 2 * RS;
-                urow = grow + RS;
-                const int li = warp + m * kLW;
-                tm = ri.tmask[(c + li * G) / I];
-                slot = n_sh + li;
-            }
-            gate_up_item<true>(grow, urow, H, xh, csc, tm, lane, resg + slot * T, resu + slot * T);
-            if (m >= 0 && m + NSW < n_items_w) {
-                __syncwarp();
-                issue(m + NSW);
-            }
-        }
-        if (__syncthreads_or(m_fail >= 0)) {
-            // a copy timed out: let this warp's copies still in flight land
-            // (bounded), then stop
-            for (int mm = max(m_fail, 0); m_fail >= 0 && mm < min(n_items_w, m_fail + NSW); ++mm)
-                mbar_wait_bounded(rbar + mm % NSW, (uint32_t)(mm / NSW) & 1u, nullptr, 0);
-            return;
-        }
-        const int n_items = n_sh + nl;
-        for (int e = tid; e < n_items * T; e += kLT) {
-            const int t = e / n_items, i = e - t * n_items;
-            float tsg, tsu;
-            int pp;
-            uint32_t ranks = 0;
-            if (i < n_sh) {
-                pp = sp0 + i;
-                tsg = sm.tss[2 * D];
-                tsu = sm.tss[2 * D + 1];
-            } else {
-                const int q = c + (i - n_sh) * G, dd = q / I;
-                pp = q - dd * I;
-                ranks = rank_bits(ri.dmask[dd], t);
-                if (!ranks) continue;
-                tsg = sm.tss[2 * dd];
-                tsu = sm.tss[2 * dd + 1];
-            }
-            const float g = bf16_round_f32(tsg * resg[i * T + t]);
-            const float u = bf16_round_f32(tsu * resu[i * T + t]);
-            const uint16_t out = f32_to_bf16_bits(silu_f32(g) * u);
-            if (i < n_sh) {
-                a.h_shared[(size_t)t * Is + pp] = out;
-            } else {
-                for (int j = 0; j < k; ++j)
-                    if ((ranks >> j) & 1u) a.h_routed[((size_t)t * k + j) * I + pp] = out;
-            }
-        }
-    }
-    // ---- 4: down + combine ---------------------------------------------------------
-    // The down rows depend on the routing only. This CTA's first ring copies
-    // are issued between its arrival at the grid barrier and its wait (the
-    // regions of phases 0-3 are dead once the epilogue is done), so that their
-    // latency overlaps the barrier.
-    const int NSW = a.ns4, RG = a.rg;
-    uint8_t* ring = smem + L.ring4 + (size_t)warp * NSW * a.slot4;
-    const int ngr = (nr + RG - 1) / RG;
-    const int n_tasks = D * ngr;  // routed; the shared expert's groups are resident
-    const int my_tasks = a.dpre ? 0 : (n_tasks > warp ? (n_tasks - warp + kLW - 1) / kLW : 0);
-    auto issue = [&](int kk) {
-        const int q = warp + kk * kLW, u = q / ngr, r0g = (q - u * ngr) * RG, r1g = min(nr, r0g + RG);
-        uint8_t* dst = ring + (size_t)(kk % NSW) * a.slot4;
-        warp_copy_async(dst, a.down + ((size_t)ri.dlist[u] * H + n0 + r0g) * RSr, (r1g - r0g) * RSr, lane);
-        cp_async_commit();
-    };
-    const unsigned long long target = grid_arrive(a.bar_ticket);
-    for (int kk = 0; kk < NSW; ++kk) {
-        if (kk < my_tasks)
-            issue(kk);
-        else
-            cp_async_commit();
-    }
-    if (!grid_wait(a.bar_ticket, target, a.status, kStatusTimeoutLayer)) {
-        cp_async_wait<0>();
+    const uint64_t budget = sm.hdr[kHdrBudget] ? (uint64_t)sm.hdr[kHdrBudget] * 1000ull : kWaitBudgetNs;
+    if (sm.hdr[kHdrStatus] & kStatusPoisonMask) {  // an earlier call failed: re-initialise first
+        drain(budget);
         return;
     }
-    pdl_launch_dependents();
-    if (nr == 0) return;
-    {
-        uint4* hr = reinterpret_cast<uint4*>(smem + L.hr);
-        uint4* hs = reinterpret_cast<uint4*>(smem + L.hs);
-        float* csr = reinterpret_cast<float*>(smem + L.csr);
-        float* css = reinterpret_cast<float*>(smem + L.css);
-        float* dval = reinterpret_cast<float*>(smem + L.dval);
-        const StageSrc hsrc[2] = {{a.h_routed, hr, csr, T * k, I}, {a.h_shared, hs, css, has_sh ? T : 0, Is ? Is : 32}};
-        stage_f16<true>(hsrc, [] {});
-        __syncthreads();
-        // One task: rows [r0g, r1g) of unit u (u < D routed, from `rows`; u == D shared).
-        auto task = [&](int u, int r0g, int r1g, const uint8_t* rows, uint32_t rest) {
-            const bool sh = u >= D;
-            const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
-            const unsigned long long dm = sh ? 0ull : ri.dmask[u];
-            const float tsd = sm.tsd[u];
-            auto vec = [&](int t, const uint4*& h, const float*& cs) {
-                if (sh) {
-                    h = hs + (size_t)t * (Is / 8);
-                    cs = css + (size_t)t * (Is / 32);
-                } else {
-                    const int j = __ffs(rank_bits(dm, t)) - 1;
-                    h = hr + ((size_t)t * k + j) * (I / 8);
-                    cs = csr + ((size_t)t * k + j) * (I / 32);
-                }
-            };
-            auto put = [&](float v, int r, int t) {
-                const float dv = bf16_round_f32(tsd * v);
-                if (sh) {
-                    dval[((size_t)t * (k + 1) + k) * RM + r] = dv;
-                } else {
-                    const uint32_t ranks = rank_bits(dm, t);
-                    for (int jj = 0; jj < k; ++jj)
-                        if ((ranks >> jj) & 1u) dval[((size_t)t * (k + 1) + jj) * RM + r] = dv;
-                }
-            };
-            while (rest) {
-                const int t0 = __ffs(rest) - 1;
-                rest &= rest - 1u;
-                if (rest) {  // two tokens, rows in groups of 8
-                    const int t1 = __ffs(rest) - 1;
-                    rest &= rest - 1u;
-                    const uint4* hv[2];
-                    const float* cv[2];
-                    vec(t0, hv[0], cv[0]);
-                    vec(t1, hv[1], cv[1]);
-                    for (int hb = 0; hb < RG && r0g + hb < r1g; hb += 8) {
-                        float acc[16];
-                        down_pass<8, 2>(rows + (size_t)hb * RSu, RSu, r1g - r0g - hb, K, hv, cv, lane, acc);
-                        const float v = reduce_scatter<16>(acc, lane);
-                        const int idx = rs_index<16>(lane), r = r0g + hb + (idx & 7);
-                        if ((lane & 1) == 0 && r < r1g) put(v, r, (idx >> 3) ? t1 : t0);
+    const uint32_t tag = sm.hdr[kHdrEpoch] + 1u;
+    const bool withhold = sm.hdr[kHdrLoseCta] == (uint32_t)c + 1u;  // test hook: this CTA publishes no scores
+    if (nrr > 0) {
+        const bool ok = mbar_wait_bounded(&sm.rbar, 0, a.status, kStatusTimeoutLayer, budget);
+        if (!ok) sm.fail = 1;
+        const uint16_t* wrows = reinterpret_cast<const uint16_t*>(smem + L.rows);
+        // logits from the staged (exact, chunk-scaled f16) x: lane l takes the
+        // 32-value chunks l, l + 32, ...; each chunk's FP32 partial sum is
+        // multiplied back by its power-of-two scale
+        for (int q = warp; ok && q < nrr * T; q += kLW) {
+            const int r = q / T, t = q - r * T;
+            const uint4* xb = xh + (size_t)t * (H / 8) + lane;
+            const float* cb = csc + (size_t)t * (H / 32) + lane;
+            const uint4* wv = reinterpret_cast<const uint4*>(wrows + (size_t)r * H);
+            float v = 0.f;
+            for (int m = 0; m < H / 1024; ++m) {
+                const int ch = lane + 32 * m;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint4 xv = xb[(m * 4 + w) * 32], wq = wv[4 * ch + w];
+                    const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xa[i]));
+                        s0 = fmaf(bf16_lo(wa[i]), xf.x, s0);
+                        s1 = fmaf(bf16_hi(wa[i]), xf.y, s1);
                     }
-                } else {
-                    const uint4* hv[1];
-                    const float* cv[1];
-                    vec(t0, hv[0], cv[0]);
-                    for (int hb = 0; hb < RG && r0g + hb < r1g; hb += 8) {
-                        float acc[8];
-                        down_pass<8, 1>(rows + (size_t)hb * RSu, RSu, r1g - r0g - hb, K, hv, cv, lane, acc);
-                        const float v = reduce_scatter<8>(acc, lane);
-                        const int r = r0g + hb + rs_index<8>(lane);
-                        if ((lane & 3) == 0 && r < r1g) put(v, r, t0);
+                }
+                v = fmaf(cb[32 * m], s0 + s1, v);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(full_mask, v, off);
+            if (lane == 0 && !withhold)
+                st_tagged(a.scores + (size_t)t * E + r0 + r, tag, sigmoid_score(v, a.bias, r0 + r));
+        }
+    }
+
+    // Routing in this CTA: all T x E tagged scores (polled until every one
+    // carries this call's tag) into shared memory over the router rows, the
+    // top-k of each token (one warp per token), the routing view. Every
+    // thread calls it; false (in every thread) if a score never came.
+    auto route = [&]() -> bool {
+        __syncthreads();  // the router rows are dead
+        uint32_t* sc = reinterpret_cast<uint32_t*>(smem + L.rows);
+        bool ok = !sm.fail;
+        for (int i = tid; ok && i < T * E; i += kLT) {
+            uint64_t v = ld_tagged(a.scores + i);
+            if ((uint32_t)(v >> 32) != tag) {
+                const uint64_t t0 = globaltimer_ns();
+                while ((uint32_t)((v = ld_tagged(a.scores + i)) >> 32) != tag) {
+                    if (globaltimer_ns() - t0 > budget) {
+                        atomicOr(a.status, kStatusTimeoutLayer);
+                        ok = false;
+                        break;
                     }
                 }
             }
-        };
-        if (a.dpre) {  // every routed group is resident once the prefetch lands
-            const bool ok = mbar_wait_bounded(&sm.dbar, 0, tid == 0 ? a.status : nullptr, kStatusTimeoutLayer);
-            if (!__syncthreads_and(ok)) return;
+            sc[i] = (uint32_t)v;
         }
-        // The warp's work, in one loop so that the task's code is inlined once:
-        // first its units of the shared expert's rows (resident; one per (8
-        // rows, two tokens), spread over the warps from the last one), then its
-        // routed tasks warp, warp + kLW, ... (rows from the prefetch, else from
-        // the ring).
-        const int ng8 = has_sh ? (nr + 7) >> 3 : 0, ntp = (T + 1) >> 1, su0 = kLW - 1 - warp;
-        const int n_su_w = su0 < ng8 * ntp ? (ng8 * ntp - su0 + kLW - 1) / kLW : 0;
-        const int n_mine = n_tasks > warp ? (n_tasks - warp + kLW - 1) / kLW : 0;
-        for (int it = 0; it < n_su_w + n_mine; ++it) {
-            const int kk = it - n_su_w;
-            int u, r0g, r1g;
-            const uint8_t* rows;
-            uint32_t tm;
-            if (kk < 0) {
-                const int q = su0 + it * kLW, g = q / ntp, t0 = 2 * (q - g * ntp);
-                u = D;
-                r0g = 8 * g;
-                r1g = min(nr, r0g + 8);
-                rows = shdn + (size_t)r0g * RSs;
-                tm = (t0 + 1 < T ? 3u : 1u) << t0;
-            } else {
-                const int q = warp + kk * kLW;
-                u = q / ngr;
-                r0g = (q - u * ngr) * RG;
-                r1g = min(nr, r0g + RG);
-                if (a.dpre) {
-                    rows = dpre + ((size_t)u * nr + (size_t)r0g) * RSr;
-                } else {
-                    cp_async_wait_n(NSW - 1);
+        if (!__syncthreads_and(ok)) return false;
+        if (warp < T) {
+            if (E <= 256)
+                topk_warp<8>(sc + (size_t)warp * E, E, k, lane, sm.ids + warp * k, sm.w + warp * k);
+            else
+                topk_warp<FLINT_MAX_EXPERTS / 32>(sc + (size_t)warp * E, E, k, lane, sm.ids + warp * k,
+                                                  sm.w + warp * k);
+        }
+        __syncthreads();
+        build_route_info<true>(ri, sm.ids, T, k, E, nullptr);
+        return true;
+    };
+
+    bool failed = false;
+    if (!sh_cta) {
+        // ---- 2: routing, this CTA's share of the selected experts ---------------
+        if (!route()) {
+            failed = true;
+        } else {
+            const int D = ri.D;
+            if (c == G - 1 && tid < T * k) {
+                a.ids[tid] = sm.ids[tid];
+                a.weights[tid] = sm.w[tid];
+            }
+            if (warp == 0) {
+                // cost weight of an expert: 2 + the tokens that chose it
+                // (its decode, once, and a multiply-add per token)
+                for (int base = 0; base < D; base += 32) {
+                    const int u = base + lane;
+                    int v = u < D ? 2 + __popc(ri.tmask[u]) : 0;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const int n = __shfl_up_sync(full_mask, v, off);
+                        if (lane >= off) v += n;
+                    }
+                    if (base) v += sm.cumw[base - 1];
+                    if (u < D) sm.cumw[u] = v;
                     __syncwarp();
-                    rows = ring + (size_t)(kk % NSW) * a.slot4;
                 }
-                tm = ri.tmask[u];
+                const int Gr = G - Gs, cr = c - Gs;
+                const long long Wt = sm.cumw[D - 1];
+                int pos = 0;
+                if (lane < 4) {  // gate/up lo, hi; down lo, hi
+                    const int per = lane < 2 ? I : NB;
+                    const long long tot = Wt * per;
+                    const long long tau = (long long)(cr + (lane & 1)) * tot / Gr;
+                    pos = cost_pos(tau, sm.cumw, D, per);
+                }
+                const int p0 = __shfl_sync(full_mask, pos, 0), p1 = __shfl_sync(full_mask, pos, 1);
+                const int b0 = __shfl_sync(full_mask, pos, 2), b1 = __shfl_sync(full_mask, pos, 3);
+                if (lane == 0) {
+                    build_chunks(sm, p0, p1, I, b0, b1, NB, a.status, [](int u) { return u; }, rows_per_chunk);
+                    if (!sm.fail)
+                        for (int i = 0; i < NS; ++i) issue(i);
+                }
             }
-            task(u, r0g, r1g, rows, tm);
-            if (kk >= 0 && !a.dpre) {
+            // the tensor scales of the selected experts (their copies are in flight)
+            if (tid < D) {
+                const float* ts = a.ts + 3 * ri.dlist[tid];
+                sm.tsg[tid] = __ldg(ts);
+                sm.tsu[tid] = __ldg(ts + 1);
+                sm.tsd[tid] = __ldg(ts + 2);
+            }
+        }
+    } else if (tid == 0 && has_sh) {
+        sm.tsg[kShIdx] = __ldg(a.s_ts);
+        sm.tsu[kShIdx] = __ldg(a.s_ts + 1);
+        sm.tsd[kShIdx] = __ldg(a.s_ts + 2);
+    }
+    failed = __syncthreads_or(failed || sm.fail);
+
+    // ---- 3-4: the ring: gate/up chunks, then (h of the down experts staged) down chunks --
+    const int n_chunks = failed ? 0 : sm.n_chunks, n_gu = sm.n_gu;
+    bool wfail = false;  // this warp gave up on a copy
+    for (int i = 0; i < n_chunks; ++i) {
+        if (i == n_gu) {
+            // Stage h of this CTA's down experts: every value must carry the
+            // tag (written by the CTAs that computed that expert's gate/up).
+            __syncthreads();  // x is dead; the CTA's own h stores are issued
+            if (tid == 0) {
+                int nv = 0, item = 0, off = 0, coff = 0;
+                for (int q = 0; q < sm.n_dn; ++q) {
+                    const int unit = sm.dn_unit[q];
+                    const int K = unit == kSharedUnit ? Is : I;
+                    const uint32_t tm = unit == kSharedUnit ? (1u << T) - 1u : ri.tmask[unit];
+                    for (int t = 0; t < FLINT_MAX_TOKENS; ++t) {
+                        sm.vec[q][t] = -1;
+                        if (t < T && ((tm >> t) & 1u)) {
+                            sm.vec[q][t] = (int16_t)nv;
+                            sm.v_item0[nv] = item;
+                            sm.v_off[nv] = off;
+                            sm.v_coff[nv] = coff;
+                            sm.v_q[nv] = (int16_t)q;
+                            sm.v_t[nv] = (int16_t)t;
+                            item += K / 32;
+                            off += 2 * K;
+                            coff += 4 * (K / 32);
+                            ++nv;
+                        }
+                    }
+                }
+                if (off > a.stage_vals || coff > a.stage_scales) {  // the host plans for this not to happen
+                    atomicOr(a.status, kStatusLayerPlan);
+                    sm.fail = 1;
+                    nv = 0;
+                    item = 0;
+                }
+                sm.n_vec = nv;
+                sm.v_item0[nv] = item;
+            }
+            __syncthreads();
+            bool ok = true;
+            const int n_items = sm.v_item0[sm.n_vec];
+            for (int it = tid; ok && it < n_items; it += kLT) {
+                int v = 0;
+                while (sm.v_item0[v + 1] <= it) ++v;
+                const int cc = it - sm.v_item0[v], q = sm.v_q[v], t = sm.v_t[v];
+                const int unit = sm.dn_unit[q];
+                const bool sh = unit == kSharedUnit;
+                const int K = sh ? Is : I;
+                const uint64_t* src;
+                if (sh) {
+                    src = a.h_shared + (size_t)t * Is;
+                } else {
+                    const int j = __ffs(rank_bits(ri.dmask[unit], t)) - 1;
+                    src = a.h_routed + ((size_t)t * k + j) * I;
+                }
+                src += 32 * cc;
+                // the 32 values as bf16 pairs, once every word carries the tag
+                uint4 w4[4];
+                uint64_t t0 = 0;
+                while (true) {
+                    bool all = true;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint64_t e[8];
+#pragma unroll
+                        for (int i2 = 0; i2 < 4; ++i2) ld_tagged2(src + 8 * g + 2 * i2, e[2 * i2], e[2 * i2 + 1]);
+#pragma unroll
+                        for (int i2 = 0; i2 < 8; ++i2) all = all && (uint32_t)(e[i2] >> 32) == tag;
+                        w4[g] = make_uint4((uint32_t)(e[0] & 0xFFFFu) | ((uint32_t)e[1] << 16),
+                                           (uint32_t)(e[2] & 0xFFFFu) | ((uint32_t)e[3] << 16),
+                                           (uint32_t)(e[4] & 0xFFFFu) | ((uint32_t)e[5] << 16),
+                                           (uint32_t)(e[6] & 0xFFFFu) | ((uint32_t)e[7] << 16));
+                    }
+                    if (all) break;
+                    if (!t0) {
+                        t0 = globaltimer_ns();
+                    } else if (globaltimer_ns() - t0 > budget) {
+                        atomicOr(a.status, kStatusTimeoutLayer);
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!ok) break;
+                const StageSrc ss = {nullptr, reinterpret_cast<uint4*>(smem + L.xs + sm.v_off[v]),
+                                     reinterpret_cast<float*>(smem + L.csc + sm.v_coff[v]), 1, K};
+                stage_store<true>(ss, 0, cc, w4);
+            }
+            if (!__syncthreads_and(ok)) {
+                wfail = true;
+                if (tid == 0) sm.fail = 1;
+            }
+        }
+        const int s = i % NS;
+        if (!wfail && !sm.fail) {
+            if (!__all_sync(full_mask,
+                            mbar_wait_bounded(&sm.full[s], (uint32_t)(i / NS) & 1u, a.status, kStatusTimeoutLayer,
+                                              budget))) {
+                wfail = true;
+                if (lane == 0) sm.fail = 1;
+            }
+        } else {
+            wfail = true;
+        }
+        if (wfail) continue;
+        const Chunk ch = sm.chunk[i];
+        const uint8_t* slot = ring + (size_t)s * a.slot;
+        const bool sh = ch.unit == kSharedUnit;
+        const int ui = sh ? kShIdx : ch.unit;
+        const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[ch.unit];
+        if (ch.kind == kChunkGateUp) {
+            if (warp < ch.count) {
+                const uint8_t* grow = slot + (size_t)warp * RS;
+                const uint8_t* urow = slot + (size_t)(kLW + warp) * RS;
+                float* rg = sm.res[warp][0];
+                float* ru = sm.res[warp][1];
+                gate_up_item<true>(grow, urow, H, xh, csc, tm, lane, rg, ru);
                 __syncwarp();
-                if (kk + NSW < n_mine)
-                    issue(kk + NSW);
-                else
-                    cp_async_commit();
+                if (lane < T && ((tm >> lane) & 1u)) {
+                    const int p = ch.start + warp;
+                    const float g = bf16_round_f32(sm.tsg[ui] * rg[lane]);
+                    const float u = bf16_round_f32(sm.tsu[ui] * ru[lane]);
+                    const uint32_t hv = f32_to_bf16_bits(silu_f32(g) * u);
+                    uint64_t* dst;
+                    if (sh) {
+                        dst = a.h_shared + (size_t)lane * Is + p;
+                    } else {
+                        const int j = __ffs(rank_bits(ri.dmask[ch.unit], lane)) - 1;
+                        dst = a.h_routed + ((size_t)lane * k + j) * I + p;
+                    }
+                    st_tagged(dst, tag, hv);
+                }
+            }
+        } else {
+            const int rw0 = 8 * warp;
+            if (rw0 < ch.count) {
+                const int nrw = min(8, ch.count - rw0);
+                const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
+                const uint8_t* rows = slot + (size_t)rw0 * RSu;
+                const int row0 = ch.start + rw0;
+                const float tsd = sm.tsd[ui];
+                const unsigned long long dm = sh ? 0ull : ri.dmask[ch.unit];
+                auto vec = [&](int t, const uint4*& hv, const float*& cv) {
+                    const int v = sm.vec[ch.q][t];
+                    hv = reinterpret_cast<const uint4*>(smem + L.xs + sm.v_off[v]);
+                    cv = reinterpret_cast<const float*>(smem + L.csc + sm.v_coff[v]);
+                };
+                auto put = [&](float v, int r, int t) {
+                    const uint16_t d = f32_to_bf16_bits(tsd * v);
+                    if (sh) {
+                        a.d_shared[(size_t)t * H + row0 + r] = d;
+                    } else {
+                        const int j = __ffs(rank_bits(dm, t)) - 1;
+                        a.d_routed[((size_t)t * k + j) * H + row0 + r] = d;
+                    }
+                };
+                uint32_t rest = tm;
+                while (rest) {
+                    const int t0 = __ffs(rest) - 1;
+                    rest &= rest - 1u;
+                    if (rest) {  // two tokens
+                        const int t1 = __ffs(rest) - 1;
+                        rest &= rest - 1u;
+                        const uint4* hv[2];
+                        const float* cv[2];
+                        vec(t0, hv[0], cv[0]);
+                        vec(t1, hv[1], cv[1]);
+                        float acc[16];
+                        down_pass<8, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                        const float v = reduce_scatter<16>(acc, lane);
+                        const int idx = rs_index<16>(lane), r = idx & 7;
+                        if ((lane & 1) == 0 && r < nrw) put(v, r, (idx >> 3) ? t1 : t0);
+                    } else {
+                        const uint4* hv[1];
+                        const float* cv[1];
+                        vec(t0, hv[0], cv[0]);
+                        float acc[8];
+                        down_pass<8, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                        const float v = reduce_scatter<8>(acc, lane);
+                        const int r = rs_index<8>(lane);
+                        if ((lane & 3) == 0 && r < nrw) put(v, r, t0);
+                    }
+                }
             }
         }
-        cp_async_wait<0>();
-        __syncthreads();
-        // combine, in rank order then the shared expert
-        for (int i = tid; i < T * nr; i += kLT) {
-            const int t = i / nr, r = i - t * nr;
-            float acc = 0.f;
-            for (int j = 0; j < k; ++j)
-                if (ri.ids[t * k + j] >= 0) acc = fmaf(wsel[t * k + j], dval[((size_t)t * (k + 1) + j) * RM + r], acc);
-            if (has_sh) acc += dval[((size_t)t * (k + 1) + k) * RM + r];
-            a.y[(size_t)t * H + n0 + r] = f32_to_bf16_bits(acc);
+        // The last warp done with the chunk refills its slot.
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t old = atom_add_acq_rel_cta_smem(&sm.rel[s], 1u);
+            if (old == kLW - 1) {
+                sm.rel[s] = 0;
+                if (!sm.fail) issue(i + NS);
+            }
         }
+    }
+
+    // ---- 5: arrivals on the row blocks; the last arriver of a block combines it ------
+    if (!__syncthreads_or(failed || wfail || sm.fail) && sh_cta) {
+        // the shared group learns the routing now (weights, number of experts)
+        failed = !route();
+    }
+    __threadfence();  // this thread's d (and h) stores are visible before any arrival
+    if (__syncthreads_or(failed || wfail || sm.fail)) {
+        drain(budget);
+        return;
+    }
+    const uint32_t U = (uint32_t)ri.D + (has_sh ? 1u : 0u);
+    for (int j = sm.b0 + tid; j < sm.b1; j += kLT) {
+        const int blk = j % NB;
+        if (atom_add_acq_rel_gpu(a.counters + blk, 1u) == U - 1u) sm.last[atomicAdd(&sm.n_last, 1)] = (int16_t)blk;
+    }
+    __syncthreads();
+    const int n_last = sm.n_last;
+    for (int e = tid; e < n_last * T * kRowBlock; e += kLT) {
+        const int qb = e / (T * kRowBlock), rem = e - qb * (T * kRowBlock);
+        const int t = rem / kRowBlock, r = sm.last[qb] * kRowBlock + (rem - t * kRowBlock);
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const float d = __uint_as_float((uint32_t)__ldcg(a.d_routed + ((size_t)t * k + j) * H + r) << 16);
+            acc = fmaf(sm.w[t * k + j], d, acc);
+        }
+        if (has_sh) acc += __uint_as_float((uint32_t)__ldcg(a.d_shared + (size_t)t * H + r) << 16);
+        a.y[(size_t)t * H + r] = f32_to_bf16_bits(acc);
+    }
+    for (int q = tid; q < n_last; q += kLT) a.counters[sm.last[q]] = 0;
+    __syncthreads();
+    // the last CTA to finish advances the call counter (the next call's tag)
+    if (tid == 0 && atomicAdd(a.hdr + kHdrDone, 1u) == (uint32_t)G - 1u) {
+        a.hdr[kHdrDone] = 0;
+        a.hdr[kHdrEpoch] = tag;
     }
 }
 

@@ -66,7 +66,9 @@ def _load():
         "flint_nvfp4_row_stride": (i64, [i64]),
         "flint_nvfp4_packed_bytes": (i64, [i64, i64, i64]),
         "flint_gguf_nvfp4_bytes": (i64, [i64, i64, i64]),
-        "flint_workspace_bytes": (sz, [i32, i32, i32, i32]),
+        "flint_workspace_bytes": (sz, [i32, i32, i32, i32, i32]),
+        "flint_workspace_set_wait_budget": (i32, [vp, sz, u32, vp]),
+        "flint_selftest_lose_cta": (i32, [vp, sz, i32, vp]),
         "flint_workspace_init": (i32, [vp, sz, vp]),
         "flint_workspace_check": (i32, [vp, sz, vp]),
         "flint_nvfp4_repack": (i32, [vp, i64, i64, i64, vp, i64, vp]),
@@ -136,8 +138,8 @@ def flint_gguf_nvfp4_bytes(n_mats: int, rows: int, cols: int) -> int:
     return _lib.flint_gguf_nvfp4_bytes(n_mats, rows, cols)
 
 
-def flint_workspace_bytes(num_experts: int, top_k: int, inter: int, inter_shared: int) -> int:
-    return _lib.flint_workspace_bytes(num_experts, top_k, inter, inter_shared)
+def flint_workspace_bytes(num_experts: int, top_k: int, hidden: int, inter: int, inter_shared: int) -> int:
+    return _lib.flint_workspace_bytes(num_experts, top_k, hidden, inter, inter_shared)
 
 
 def flint_last_error() -> str:
@@ -353,6 +355,16 @@ def flint_moe_route_static(x, router_w, k, ids, weights, bias=None, flags=0, str
 def flint_selftest_wait_timeout(ws, budget_ns: int, stream=None):
     _check(_lib.flint_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), budget_ns, _stream(stream)),
            "selftest_wait_timeout")
+
+
+def flint_workspace_set_wait_budget(ws, budget_us: int, stream=None):
+    _check(_lib.flint_workspace_set_wait_budget(_ptr(ws), ws.numel() * ws.element_size(), budget_us,
+                                                _stream(stream)), "workspace_set_wait_budget")
+
+
+def flint_selftest_lose_cta(ws, cta: int, stream=None):
+    _check(_lib.flint_selftest_lose_cta(_ptr(ws), ws.numel() * ws.element_size(), cta, _stream(stream)),
+           "selftest_lose_cta")
 
 
 def raw_library():

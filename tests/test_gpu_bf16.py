@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from flint_testlib import DeviceLayer, assert_close, flint, margin_x
+from flint_testlib import DeviceLayer, assert_close, flint, layer_flips, margin_x
 from nvfp4_moe_decode_sigmoid_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -28,13 +28,14 @@ def _run(dl, x, k, flags=0, bias=None):
 
 def _check(dl, x, k, flags=0, bias=None):
     ids, w, y = _run(dl, x, k, flags, bias)
-    rids, _, ry = oracle.moe_layer(synth.bits(x), synth.bits(dl.L.router_w), k,
+    rids, rw, ry = oracle.moe_layer(synth.bits(x), synth.bits(dl.L.router_w), k,
                                    bias=None if bias is None else bias.numpy(), **dl.oracle_args())
     for t in range(x.shape[0]):
         assert set(ids[t]) == set(rids[t])
     ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
-    assert_close(y, ref, "bf16 layer (gpu routing)")
-    assert_close(y, ry, "bf16 layer (oracle routing)")
+    flips = layer_flips(synth.bits(x), rids, rw, dl)
+    assert_close(y, ref, "bf16 layer (gpu routing)", flips=flips)
+    assert_close(y, ry, "bf16 layer (oracle routing)", flips=flips)
     return y
 
 

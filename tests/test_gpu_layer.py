@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from flint_testlib import DeviceLayer, assert_close, flint, margin_x
+from flint_testlib import DeviceLayer, assert_close, flint, layer_flips, margin_x
 from nvfp4_moe_decode_sigmoid_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -32,8 +32,9 @@ def _check(dl, x, k, bias=None, flags=0):
     assert np.array_equal(ids, rids), f"selection differs: {ids} vs {rids}"
     assert np.allclose(w, rw, rtol=2e-6, atol=1e-7), f"weights differ: {w} vs {rw}"
     ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
-    assert_close(y, ref, "fused layer (gpu routing)")
-    assert_close(y, ry, "fused layer (oracle routing)")
+    flips = layer_flips(synth.bits(x), rids, rw, dl)
+    assert_close(y, ref, "fused layer (gpu routing)", flips=flips)
+    assert_close(y, ry, "fused layer (oracle routing)", flips=flips)
     return ids, w, y
 
 
@@ -128,4 +129,48 @@ def test_matches_the_three_kernel_path(full_layer):
     f.flint_moe_decode(xc, ids2, w2, full_layer.routed, full_layer.shared, y2, ws)
     assert np.array_equal(ids, ids2.cpu().numpy())
     assert np.allclose(w, w2.cpu().numpy(), rtol=2e-6, atol=1e-7)
-    assert_close(y, synth.bits(y2), "fused vs three kernels")
+    assert_close(y, synth.bits(y2), "fused vs three kernels", flips=2 * layer_flips(synth.bits(x), ids, w, full_layer))
+
+
+def test_pdl_chained_layers_in_a_graph_match_single_calls(full_layer):
+    """Several layer calls PDL-chained on one stream and on one workspace,
+    captured in a CUDA graph and replayed (each call may start while the
+    previous one finishes; the call counter gives each its own tag), give the
+    same bits as the same calls made one at a time with a synchronisation in
+    between."""
+    f = flint()
+    k, T = 6, 8
+    xs = [margin_x(synth.bits(full_layer.L.router_w), T, 2048, k, None, seed=80 + i).cuda() for i in range(3)]
+    ws = full_layer.workspace(k)
+    outs = [(torch.empty((T, k), dtype=torch.int32, device="cuda"), torch.empty((T, k), dtype=torch.float32,
+                                                                                  device="cuda"),
+             torch.empty((T, 2048), dtype=torch.bfloat16, device="cuda")) for _ in range(6)]
+    steps = [(xs[i % 3], (T if i % 2 == 0 else 1)) for i in range(6)]
+
+    def run(flags):
+        for (x, t), (ids, w, y) in zip(steps, outs):
+            f.flint_moe_layer(x[:t], full_layer.router_w, k, full_layer.routed, full_layer.shared, ids[:t], w[:t],
+                              y[:t], ws, flags=flags)
+
+    ref = []
+    for (x, t), (ids, w, y) in zip(steps, outs):
+        f.flint_moe_layer(x[:t], full_layer.router_w, k, full_layer.routed, full_layer.shared, ids[:t], w[:t], y[:t],
+                          ws)
+        torch.cuda.synchronize()
+        ref.append((ids[:t].clone(), w[:t].clone(), y[:t].clone()))
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        run(f.FLINT_PDL)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run(f.FLINT_PDL)
+        for (_, _, y) in outs:
+            y.zero_()
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    assert f.flint_workspace_check(ws) == f.FLINT_OK
+    for (x, t), (ids, w, y), (ri, rw, ry) in zip(steps, outs, ref):
+        assert torch.equal(ids[:t], ri) and torch.equal(w[:t], rw)
+        assert torch.equal(y[:t].view(torch.int16), ry.view(torch.int16))

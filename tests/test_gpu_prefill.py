@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from flint_testlib import DeviceLayer, MARGIN, assert_close, bf16_to_f64, combine_terms, flint
+from flint_testlib import DeviceLayer, MARGIN, assert_close, bf16_to_f64, layer_flips, flint
 from nvfp4_moe_decode_sigmoid_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -48,8 +48,8 @@ def check_prefill(dl, x, k, n_sample, bias=None, seed=0):
     cand = np.nonzero(margin_ok)[0]
     pick = np.sort(rng.choice(cand, size=min(n_sample, cand.size), replace=False))
     ref = oracle.moe_experts(xb[pick], rids[pick], rw[pick].astype(np.float32), **dl.oracle_args())
-    terms = combine_terms(xb[pick], rids[pick], rw[pick], dl)
-    assert_close(y[pick], ref, "prefill", terms=terms)
+    flips = layer_flips(xb[pick], rids[pick], rw[pick], dl)
+    assert_close(y[pick], ref, "prefill", flips=flips)
     return ids, w, y
 
 
@@ -108,8 +108,8 @@ def test_full_prefill_8k_tokens(full_layer):
         assert set(ids[pick[i]]) == set(rids[i])
     sub = np.nonzero(ok)[0][:16]
     ref = oracle.moe_experts(xb[sub], rids[sub], rw[sub].astype(np.float32), **full_layer.oracle_args())
-    terms = combine_terms(xb[sub], rids[sub], rw[sub], full_layer)
-    assert_close(y[pick[sub]], ref, "prefill 8k", terms=terms)
+    flips = layer_flips(xb[sub], rids[sub], rw[sub], full_layer)
+    assert_close(y[pick[sub]], ref, "prefill 8k", flips=flips)
     assert np.all(np.isfinite(bf16_to_f64(y)))
     assert np.all((ids >= 0) & (ids < 256))
     del f

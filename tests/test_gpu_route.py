@@ -16,7 +16,7 @@ def _run(x, wr, k, bias=None, flags=0):
     f = flint()
     T = x.shape[0]
     E = wr.shape[0]
-    ws = torch.empty(f.flint_workspace_bytes(E, k, 0, 0), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(f.flint_workspace_bytes(E, k, 0, 0, 0), dtype=torch.uint8, device="cuda")
     f.flint_workspace_init(ws)
     ids = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
     w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
@@ -80,7 +80,7 @@ def test_route_repeated_calls_reuse_the_workspace():
     E, k, H, T = 64, 4, 512, 4
     wr = synth.bf16_normal(8, (E, H), 0.02)
     x = margin_x(synth.bits(wr), T, H, k, None, seed=8)
-    ws = torch.empty(f.flint_workspace_bytes(E, k, 0, 0), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(f.flint_workspace_bytes(E, k, 0, 0, 0), dtype=torch.uint8, device="cuda")
     f.flint_workspace_init(ws)
     ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, k), dtype=torch.float32, device="cuda")

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from flint_testlib import DeviceLayer, MARGIN, assert_close, bf16_to_f64, combine_terms, flint
+from flint_testlib import DeviceLayer, MARGIN, assert_close, bf16_to_f64, layer_flips, flint
 from nvfp4_moe_decode_sigmoid_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -101,7 +101,7 @@ def check_block(dl, r, y_prev, k, flags=0):
     rids, rw, ry = oracle.moe_layer(rx, synth.bits(dl.L.router_w), k, **dl.oracle_args())
     for t in range(r.shape[0]):
         assert set(ids[t]) == set(rids[t])
-    assert_close(y, ry, "block", terms=combine_terms(rx, rids, rw, dl))
+    assert_close(y, ry, "block", flips=layer_flips(rx, rids, rw, dl))
     return ids, y
 
 
@@ -213,7 +213,7 @@ def run_stack(f, blocks, x0, k, flags):
     ybuf = [torch.empty((T, H_S), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     x = torch.empty((T, H_S), dtype=torch.bfloat16, device=dev)
     h = torch.empty((T, F_S), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(f.flint_workspace_bytes(E_S, k, I_S, I_S), dtype=torch.uint8, device=dev)
+    ws = torch.empty(f.flint_workspace_bytes(E_S, k, H_S, I_S, I_S), dtype=torch.uint8, device=dev)
     f.flint_workspace_init(ws)
     ids_all = []
     cur, y_prev = 0, None

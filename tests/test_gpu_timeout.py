@@ -21,3 +21,43 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     dst = torch.empty(f.flint_nvfp4_packed_bytes(1, 4, 64), dtype=torch.uint8, device="cuda")
     f.flint_nvfp4_repack(src, 1, 4, 64, dst)
     torch.cuda.synchronize()
+
+
+def test_fused_layer_lost_cta_times_out_and_the_workspace_recovers():
+    """The fused layer with one CTA that publishes no router scores (the test
+    hook): the others' bounded waits run out after the short budget, the call
+    records FLINT_ERR_TIMEOUT, and flint_workspace_check re-initialises the
+    workspace. A later call on the same workspace is correct again (oracle),
+    and one made before the check does nothing and keeps the error."""
+    import numpy as np
+
+    import oracle
+    from flint_testlib import DeviceLayer, assert_close, layer_flips, margin_x
+
+    f = flint()
+    dl = DeviceLayer(synth.Layer(17, H=1024, E=16, I=256, I_shared=256))
+    T, k, H = 2, 6, 1024
+    x = margin_x(synth.bits(dl.L.router_w), T, H, k, None, seed=3)
+    ws = dl.workspace(k)
+    ids = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    y = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
+    xc = x.cuda()
+
+    def call():
+        f.flint_moe_layer(xc, dl.router_w, k, dl.routed, dl.shared, ids, w, y, ws)
+
+    f.flint_workspace_set_wait_budget(ws, 2000)  # 2 ms
+    f.flint_selftest_lose_cta(ws, 0)             # CTA 0 holds router rows
+    call()
+    torch.cuda.synchronize()
+    call()                                       # before the check: returns at once
+    torch.cuda.synchronize()
+    assert f.flint_workspace_check(ws) == f.FLINT_ERR_TIMEOUT
+    assert f.flint_workspace_check(ws) == f.FLINT_OK  # re-initialised: hook and status gone
+    y.zero_()
+    call()
+    assert f.flint_workspace_check(ws) == f.FLINT_OK
+    rids, rw, ry = oracle.moe_layer(synth.bits(x), synth.bits(dl.L.router_w), k, **dl.oracle_args())
+    assert np.array_equal(ids.cpu().numpy(), rids)
+    assert_close(synth.bits(y), ry, "after recovery", flips=layer_flips(synth.bits(x), rids, rw, dl))

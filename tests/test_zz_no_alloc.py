@@ -42,7 +42,7 @@ def test_static_scratch_router_matches_workspace_router_twice():
         b = None if bias is None else bias.cuda()
         ref_ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
         ref_w = torch.empty((T, k), dtype=torch.float32, device="cuda")
-        ws = torch.empty(F.flint_workspace_bytes(E, k, 0, 0), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(F.flint_workspace_bytes(E, k, 0, 0, 0), dtype=torch.uint8, device="cuda")
         F.flint_workspace_init(ws)
         F.flint_moe_route(x, wr, k, ref_ids, ref_w, ws, bias=b)
         ids = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
