@@ -12,6 +12,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libflint.so")
+# The phase-trace build (FLINT_PHASE_TRACE: the fused layer kernel stamps its
+# phase boundaries; used by phase_trace.py), in its own build folder.
+BUILD_TRACE = os.path.join(PKG, "_build_trace")
+LIB_TRACE = os.path.join(PKG, "libflint_trace.so")
 SOURCES = ["abi.cu", "repack.cu", "route.cu", "gemv.cu", "layer.cu", "bf16.cu", "norm.cu", "prefill.cu"]
 HEADERS = ["flint_device.cuh", "flint_internal.h", "expert_common.cuh", "router_common.cuh", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -25,14 +29,16 @@ def _newest_input():
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    lib, bdir = (LIB_TRACE, BUILD_TRACE) if trace else (LIB, BUILD)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
+    os.makedirs(bdir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [NVCC, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(bdir, os.path.splitext(src)[0] + ".o")
+        cmd = [NVCC, *ARCH, *FLAGS, *(["-DFLINT_PHASE_TRACE"] if trace else []), "-c", os.path.join(CSRC, src),
+               "-o", obj]
         if os.environ.get("FLINT_PTXAS_VERBOSE"):
             cmd[1:1] = ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -44,10 +50,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -40,6 +40,24 @@
 namespace flint {
 namespace {
 
+// Phase trace (a separate build of the library, with FLINT_PHASE_TRACE
+// defined, for the phase_trace tool): thread 0 of every CTA stamps %clock64 at
+// the phase boundaries into shared memory and, at the end of the call, copies
+// the stamps to a ring of the last kTraceCalls calls, indexed by the call's
+// tag. The plain build has none of this code.
+#ifdef FLINT_PHASE_TRACE
+constexpr int kTraceStamps = 16, kTraceCalls = 64, kTraceCtas = 256;
+__device__ unsigned long long g_phase_trace[kTraceCalls][kTraceCtas][kTraceStamps];
+#define FLINT_PHASE(i)                                     \
+    do {                                                   \
+        if (threadIdx.x == 0) sm.trace[(i)] = clock64();   \
+    } while (0)
+#else
+#define FLINT_PHASE(i) \
+    do {               \
+    } while (0)
+#endif
+
 constexpr int kLW = kLayerWarps;
 constexpr int kLT = kLayerThreads;
 constexpr int kMaxChunks = 96;
@@ -89,6 +107,9 @@ struct LayerSmall {
     float res[kLW][2][FLINT_MAX_TOKENS];  // a warp's raw gate / up sums per token
     float ninv[FLINT_MAX_TOKENS];
     int16_t last[kLayerMaxHidden / kRowBlock];  // row blocks this CTA combines
+#ifdef FLINT_PHASE_TRACE
+    unsigned long long trace[kTraceStamps];
+#endif
 };
 
 // Shared memory: small arrays, the routing view, the staging region (x, then
@@ -259,6 +280,10 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     };
 
     // ---- 0: before the PDL wait: barriers, static weight copies ----------------------
+#ifdef FLINT_PHASE_TRACE
+    const uint64_t trace_t0 = globaltimer_ns();
+#endif
+    FLINT_PHASE(0);
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&sm.full[s], 1);
@@ -286,6 +311,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     // read static weights before their own wait.
     pdl_launch_dependents();
     pdl_wait();  // x (or the residual stream) comes from the previous kernel
+    FLINT_PHASE(1);
 
     // ---- 1: the call's header, x; this CTA's router scores ---------------------------
     if (tid == 0) {
@@ -300,6 +326,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     else
         stage_f16<false>(xsrc, [] {});
     __syncthreads();
+    FLINT_PHASE(2);
     const uint64_t budget = sm.hdr[kHdrBudget] ? (uint64_t)sm.hdr[kHdrBudget] * 1000ull : kWaitBudgetNs;
     if (sm.hdr[kHdrStatus] & kStatusPoisonMask) {  // an earlier call failed: re-initialise first
         drain(budget);
@@ -343,6 +370,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         }
     }
 
+    FLINT_PHASE(3);
     // Routing in this CTA: all T x E tagged scores (polled until every one
     // carries this call's tag) into shared memory over the router rows, the
     // top-k of each token (one warp per token), the routing view. Every
@@ -435,6 +463,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         sm.tsd[kShIdx] = __ldg(a.s_ts + 2);
     }
     failed = __syncthreads_or(failed || sm.fail);
+    FLINT_PHASE(4);
 
     // ---- 3-4: the ring: gate/up chunks, then (h of the down experts staged) down chunks --
     const int n_chunks = failed ? 0 : sm.n_chunks, n_gu = sm.n_gu;
@@ -444,6 +473,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             // Stage h of this CTA's down experts: every value must carry the
             // tag (written by the CTAs that computed that expert's gate/up).
             __syncthreads();  // x is dead; the CTA's own h stores are issued
+            FLINT_PHASE(6);
             if (tid == 0) {
                 int nv = 0, item = 0, off = 0, coff = 0;
                 for (int q = 0; q < sm.n_dn; ++q) {
@@ -528,6 +558,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 wfail = true;
                 if (tid == 0) sm.fail = 1;
             }
+            FLINT_PHASE(7);
         }
         const int s = i % NS;
         if (!wfail && !sm.fail) {
@@ -541,6 +572,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             wfail = true;
         }
         if (wfail) continue;
+        if (i == 0) FLINT_PHASE(5);
         const Chunk ch = sm.chunk[i];
         const uint8_t* slot = ring + (size_t)s * a.slot;
         const bool sh = ch.unit == kSharedUnit;
@@ -633,6 +665,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     }
 
     // ---- 5: arrivals on the row blocks; the last arriver of a block combines it ------
+    FLINT_PHASE(8);
     if (!__syncthreads_or(failed || wfail || sm.fail) && sh_cta) {
         // the shared group learns the routing now (weights, number of experts)
         failed = !route();
@@ -648,6 +681,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         if (atom_add_acq_rel_gpu(a.counters + blk, 1u) == U - 1u) sm.last[atomicAdd(&sm.n_last, 1)] = (int16_t)blk;
     }
     __syncthreads();
+    FLINT_PHASE(9);
     const int n_last = sm.n_last;
     for (int e = tid; e < n_last * T * kRowBlock; e += kLT) {
         const int qb = e / (T * kRowBlock), rem = e - qb * (T * kRowBlock);
@@ -662,6 +696,20 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     }
     for (int q = tid; q < n_last; q += kLT) a.counters[sm.last[q]] = 0;
     __syncthreads();
+#ifdef FLINT_PHASE_TRACE
+    if (tid == 0 && c < kTraceCtas) {
+        unsigned long long* dst = g_phase_trace[tag % kTraceCalls][c];
+        for (int i = 0; i < 11; ++i) dst[i] = sm.trace[i];
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        dst[11] = smid;
+        dst[12] = (unsigned long long)sh_cta | ((unsigned long long)sm.n_chunks << 8) |
+                  ((unsigned long long)n_last << 16) | ((unsigned long long)sm.n_gu << 32);
+        dst[13] = trace_t0;
+        dst[14] = globaltimer_ns();
+        dst[15] = tag;
+    }
+#endif
     // the last CTA to finish advances the call counter (the next call's tag)
     if (tid == 0 && atomicAdd(a.hdr + kHdrDone, 1u) == (uint32_t)G - 1u) {
         a.hdr[kHdrDone] = 0;
@@ -705,3 +753,15 @@ cudaError_t launch_layer(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStr
 }
 
 }  // namespace flint
+
+#ifdef FLINT_PHASE_TRACE
+// The trace build's reader: copies the ring of phase stamps ([calls][CTAs]
+// [stamps] unsigned 64-bit) to host memory `out` of `n` entries; returns the
+// entries copied, or -1 on a CUDA error.
+extern "C" long long flint_phase_trace_read(unsigned long long* out, size_t n) {
+    const size_t total = sizeof(flint::g_phase_trace) / sizeof(unsigned long long);
+    if (n > total) n = total;
+    if (cudaMemcpyFromSymbol(out, flint::g_phase_trace, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
+    return (long long)n;
+}
+#endif

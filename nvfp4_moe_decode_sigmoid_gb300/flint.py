@@ -17,7 +17,9 @@ import torch
 
 from . import _build
 
-_LIB_PATH = _build.LIB
+# FLINT_LIBRARY selects another build of the same C ABI (the phase-trace
+# build of phase_trace.py); unset, the library built in this package.
+_LIB_PATH = os.environ.get("FLINT_LIBRARY") or _build.LIB
 
 FLINT_OK = 0
 FLINT_ERR_INVALID_ARG = 1
