@@ -146,12 +146,13 @@ flint_status_t flint_nvfp4_dequant(const uint8_t* packed, int64_t rows, int64_t 
  * flint_moe_down_combine, flint_moe_decode, flint_moe_layer and
  * flint_moe_block for one layer shape; layers of the same shape may share it
  * when their calls are issued in order on one stream. It holds a control
- * header (router arrival counter, status word, the fused layer's call counter
- * and finished-CTA count, the wait budget, a test hook), the router's FP32
- * logits [8, E] and the bf16 SwiGLU activations h of the routed [8, k, I] and
- * shared [8, I_shared] experts (flint_moe_route / flint_moe_decode), then the
- * fused layer's tagged router scores and h, its per-expert outputs d
- * [8, k, hidden] and [8, hidden], and one arrival counter per 16 output rows.
+ * header (router arrival counter, status word, the fused layer's call and
+ * finished-CTA counts and published-router-rows count, the wait budget, a
+ * test hook), the router's FP32 logits [8, E] and the bf16 SwiGLU activations
+ * h of the routed [8, k, I] and shared [8, I_shared] experts (used by
+ * flint_moe_route / flint_moe_decode and by the fused layer), then the fused
+ * layer's per-expert outputs d [8, k, hidden] and [8, hidden], one arrival
+ * counter per 16 output rows and one published-h counter per expert.
  *   - Must be 256-byte aligned and zero-filled before first use
  *     (flint_workspace_init). Every completed call leaves the counters ready
  *     for the next.
@@ -302,9 +303,10 @@ flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, 
  * all resident (cooperative launch). A group of CTAs runs the shared expert,
  * whose weights they start loading before the PDL wait; the rest split the
  * selected experts' gate/up pairs and down rows by cost. CTAs exchange the
- * router scores and h through tagged words in the workspace (no grid-wide
- * barrier), and the combine of each 16-row block of y is done by the CTA that
- * delivers its last expert output.
+ * router scores and h through the workspace under release / acquire counters
+ * (a CTA waits only for the scores and for the h of the experts it uses; no
+ * grid-wide barrier), and the combine of each 16-row block of y is done by
+ * the CTA that delivers its last expert output.
  *   x [T, H] bf16 (H = routed->hidden, H % 1024 == 0, H <= 8192), router_w
  *   [E, H] bf16 with E = routed->num_experts, bias [E] FP32 or NULL,
  *   1 <= k <= min(8, E). ids [T, k] int32 and weights [T, k] FP32 are written

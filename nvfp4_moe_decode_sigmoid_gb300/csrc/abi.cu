@@ -190,9 +190,9 @@ bool down_bf16_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
 
 // Shapes of the fused layer kernel. The shared expert gets the CTAs
 // [0, Gs), in proportion to its cost among all the layer's experts: a row of
-// an expert costs ~ 2 + the tokens that use it (decoding the codes once,
-// then a multiply-add per token), with the routed experts' token count at
-// its expected T k / min(E, T k). The ring takes as many slots of
+// an expert costs ~ 4 + 3 x the tokens that use it (decoding the codes once,
+// then a multiply-add per token; measured per-pair times at 1 and 8 tokens),
+// with the routed experts' token count at its expected T k / min(E, T k). The ring takes as many slots of
 // 2 x kLayerWarps gate/up rows (up to 4) as shared memory allows, at least 2.
 bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     const int G = sm_count;
@@ -200,7 +200,7 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     const int units = a.T * a.k < a.E ? a.T * a.k : a.E;
     if (a.s_gu) {
         const double n_routed = (double)T * a.k / units;
-        const double cs = (2.0 + T) * a.Is, cr = units * (2.0 + n_routed) * a.I;
+        const double cs = (4.0 + 3.0 * T) * a.Is, cr = units * (4.0 + 3.0 * n_routed) * a.I;
         int gs = (int)(G * cs / (cs + cr) + 0.5);
         a.Gs = gs < 1 ? 1 : (gs > G / 2 ? G / 2 : gs);
     } else {
@@ -401,7 +401,7 @@ flint_status_t flint_moe_gate_up(const flint_bf16* x, int T, const int32_t* ids,
         return fail(FLINT_ERR_INVALID_ARG, "gate_up: null or misaligned x/ids");
     const int Is = shared ? shared->inter : 0;
     const flint::WsLayout L = flint::ws_layout(routed->num_experts, k, 0, routed->inter, Is);
-    if ((s = check_ws(ws, ws_bytes, L.scores_off)) != FLINT_OK) return s;
+    if ((s = check_ws(ws, ws_bytes, L.d_routed_off)) != FLINT_OK) return s;
     DevInfo d;
     if ((s = device_info(d)) != FLINT_OK) return s;
     flint::GateUpArgs a = {};
@@ -446,7 +446,7 @@ flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* we
         return fail(FLINT_ERR_INVALID_ARG, "down_combine: null or misaligned ids/weights/y");
     const int Is = shared ? shared->inter : 0;
     const flint::WsLayout L = flint::ws_layout(routed->num_experts, k, 0, routed->inter, Is);
-    if ((s = check_ws(ws, ws_bytes, L.scores_off)) != FLINT_OK) return s;
+    if ((s = check_ws(ws, ws_bytes, L.d_routed_off)) != FLINT_OK) return s;
     DevInfo d;
     if ((s = device_info(d)) != FLINT_OK) return s;
     flint::DownArgs a = {};
@@ -581,12 +581,13 @@ static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, cons
     a.weights = weights;
     a.hdr = reinterpret_cast<uint32_t*>(ws);
     a.status = ws_status(ws);
-    a.scores = reinterpret_cast<uint64_t*>(wb + W.scores_off);
-    a.h_routed = reinterpret_cast<uint64_t*>(wb + W.th_routed_off);
-    a.h_shared = reinterpret_cast<uint64_t*>(wb + W.th_shared_off);
+    a.scores = reinterpret_cast<uint32_t*>(wb + W.logits_off);
+    a.h_routed = reinterpret_cast<uint16_t*>(wb + W.h_routed_off);
+    a.h_shared = reinterpret_cast<uint16_t*>(wb + W.h_shared_off);
     a.d_routed = reinterpret_cast<uint16_t*>(wb + W.d_routed_off);
     a.d_shared = reinterpret_cast<uint16_t*>(wb + W.d_shared_off);
     a.counters = reinterpret_cast<uint32_t*>(wb + W.counters_off);
+    a.unit_counters = reinterpret_cast<uint32_t*>(wb + W.unit_counters_off);
     a.gu = static_cast<const uint8_t*>(routed->gate_up);
     a.down = static_cast<const uint8_t*>(routed->down);
     a.I = routed->inter;

@@ -43,11 +43,19 @@ constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kMaxSlotsPerWarp = 4;
 constexpr size_t kWsHeader = 256;   // control words, below
 // Workspace header words (uint32): the router's arrival counter, the status
-// word, the fused layer's call counter (the tag of its published values is
-// the counter + 1) and its count of finished CTAs, the bounded waits' budget
-// in microseconds (0: kWaitBudgetNs), and a test hook (c + 1: CTA c of the
-// next fused-layer call publishes no router scores).
-enum : int { kHdrRouteCounter = 0, kHdrStatus = 1, kHdrEpoch = 4, kHdrDone = 5, kHdrBudget = 6, kHdrLoseCta = 7 };
+// word, the fused layer's count of completed calls and of finished CTAs, the
+// bounded waits' budget in microseconds (0: kWaitBudgetNs), a test hook
+// (c + 1: CTA c of the next fused-layer call publishes no router scores), and
+// the fused layer's count of published router rows.
+enum : int {
+    kHdrRouteCounter = 0,
+    kHdrStatus = 1,
+    kHdrCalls = 4,
+    kHdrDone = 5,
+    kHdrBudget = 6,
+    kHdrLoseCta = 7,
+    kHdrScoresIn = 8,
+};
 // Expert GEMV kernels for BF16 weights: 16 warps (a BF16 row is 4x the bytes
 // of an NVFP4 row, so fewer, larger ring slots per SM).
 constexpr int kBf16Warps = 16;
@@ -60,15 +68,15 @@ constexpr int kLayerMaxHidden = 8192;    // largest hidden size of the fused lay
 
 FLINT_HD constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Workspace regions, from the layer shape: the router's FP32 logits and the
-// bf16 h of the routed / shared experts (flint_moe_route, flint_moe_decode);
-// then the fused layer's tagged router scores [8][E] and tagged h (64-bit
-// words: tag, value), its bf16 per-expert outputs d of the routed ranks
-// [8][k][H] and of the shared expert [8][H], and its per-16-row-block
-// arrival counters [H / 16].
+// Workspace regions, from the layer shape: the router's FP32 logits [8][E]
+// (the fused layer: the sigmoid scores' bits) and the bf16 h of the routed
+// [8][k][I] and shared [8][Is] experts; then the fused layer's bf16
+// per-expert outputs d of the routed ranks [8][k][H] and of the shared expert
+// [8][H], its per-16-row-block arrival counters [H / 16] and its per-expert
+// counts of published h pairs [kMaxDistinct + 1] (the shared expert last).
 struct WsLayout {
-    size_t logits_off, h_routed_off, h_shared_off, scores_off, th_routed_off, th_shared_off, d_routed_off,
-        d_shared_off, counters_off, total;
+    size_t logits_off, h_routed_off, h_shared_off, d_routed_off, d_shared_off, counters_off, unit_counters_off,
+        total;
 };
 inline WsLayout ws_layout(int E, int k, int H, int I, int Is) {
     WsLayout L;
@@ -76,13 +84,11 @@ inline WsLayout ws_layout(int E, int k, int H, int I, int Is) {
     L.logits_off = kWsHeader;
     L.h_routed_off = align_up(L.logits_off + sizeof(float) * Tm * (size_t)E, 256);
     L.h_shared_off = align_up(L.h_routed_off + 2 * Tm * k * (size_t)I, 256);
-    L.scores_off = align_up(L.h_shared_off + 2 * Tm * (size_t)Is, 256);
-    L.th_routed_off = align_up(L.scores_off + 8 * Tm * (size_t)E, 256);
-    L.th_shared_off = align_up(L.th_routed_off + 8 * Tm * k * (size_t)I, 256);
-    L.d_routed_off = align_up(L.th_shared_off + 8 * Tm * (size_t)Is, 256);
+    L.d_routed_off = align_up(L.h_shared_off + 2 * Tm * (size_t)Is, 256);
     L.d_shared_off = align_up(L.d_routed_off + 2 * Tm * k * (size_t)H, 256);
     L.counters_off = align_up(L.d_shared_off + 2 * Tm * (size_t)H, 256);
-    L.total = align_up(L.counters_off + 4 * (size_t)(H / 16), 256);
+    L.unit_counters_off = align_up(L.counters_off + 4 * (size_t)(H / 16), 256);
+    L.total = align_up(L.unit_counters_off + 4 * (size_t)(FLINT_MAX_TOKENS * FLINT_MAX_TOPK + 1), 256);
     return L;
 }
 
@@ -174,12 +180,13 @@ struct LayerArgs {
     float* weights;      // [T][k] out
     uint32_t* hdr;       // workspace header (kHdr* words)
     uint32_t* status;    // hdr + kHdrStatus
-    uint64_t* scores;    // workspace [8][E]: tagged sigmoid scores
-    uint64_t* h_routed;  // workspace [8][k][I]: tagged h
-    uint64_t* h_shared;  // workspace [8][Is]
+    uint32_t* scores;    // workspace [8][E]: the bits of the sigmoid scores
+    uint16_t* h_routed;  // workspace [8][k][I]: bf16 h
+    uint16_t* h_shared;  // workspace [8][Is]
     uint16_t* d_routed;  // workspace [8][k][H]: bf16 d of each rank
     uint16_t* d_shared;  // workspace [8][H]
     uint32_t* counters;  // workspace [H / 16]: arrivals per row block (0 between calls)
+    uint32_t* unit_counters;  // workspace [kMaxDistinct + 1]: published h pairs per expert (0 between calls)
     const uint8_t* gu;   // routed E x [2I, H]
     const uint8_t* down; // routed E x [H, I]
     int I;

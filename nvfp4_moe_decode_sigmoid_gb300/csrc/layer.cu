@@ -8,32 +8,33 @@
 // neighbouring GEMVs, each kernel launched with programmatic dependent launch
 // so that it loads its weights while the previous kernel still runs. Here the
 // chain is one launch, one CTA per SM, all CTAs resident (cooperative launch),
-// and no CTA ever waits for the whole grid:
+// and no CTA waits for the whole grid to reach a point:
 //
 //   * The CTAs are split by expert. CTAs [0, Gs) run the shared expert (it
 //     needs no routing); CTAs [Gs, G) run the routed experts the tokens
 //     selected. Each CTA owns one contiguous, cost-balanced range of gate/up
 //     pairs and one of down-row blocks in the concatenation of its group's
-//     experts (cost of an expert's row ~ 2 + the tokens that chose it), so a
-//     CTA touches one or two experts and streams their rows as a few large
-//     bulk copies (TMA) into a CTA-wide ring of shared-memory slots.
+//     experts (an expert's row costs ~ 4 + 3 x the tokens that chose it: its
+//     decode once, a multiply-add per token), so a CTA touches one or two
+//     experts and streams their rows as a few large bulk copies (TMA) into a
+//     CTA-wide ring of shared-memory slots.
 //   * Before the PDL wait each CTA starts the copies of its static weights:
 //     its router rows, and in the shared group all of its shared-expert rows.
-//   * Router scores and h are published as 64-bit words that carry the call's
-//     tag beside the value, so a reader polls the data itself (no counter, no
-//     barrier, no separate flag read): every CTA reads all scores and selects
-//     the top-k itself; a CTA that computes down rows of an expert reads that
-//     expert's h (only that expert's) once every value carries the tag.
+//   * Exchanges go through the workspace with release / acquire counters,
+//     each polled by one thread per CTA: the router rows published (every CTA
+//     then reads all scores and selects the top-k itself), and per expert the
+//     gate/up pairs whose h is written (a CTA waits only for the experts whose
+//     down rows it computes).
 //   * The combine y = bf16(sum_j w_j d_j + d_shared) runs per 16-row block:
 //     each expert's down CTA writes its d rows and counts its arrival on the
 //     block's counter; the CTA that arrives last (all experts' d present)
 //     combines the block in rank order and resets the counter. Nothing waits.
+//   * The last CTA to finish resets the exchange counters for the next call.
 //
-// The tag is the workspace's call counter plus one; the last CTA to finish
-// advances the counter. After a timed-out wait (or any other failure that
-// stops a CTA) the workspace must be re-initialised (flint_workspace_check
-// does it); until then every call returns at once, leaving its outputs
-// unwritten, and the status stays set.
+// After a timed-out wait (or any other failure that stops a CTA) the counters
+// are left mid-call and the workspace must be re-initialised
+// (flint_workspace_check does it); until then every call returns at once,
+// leaving its outputs unwritten, and the status stays set.
 #include "expert_common.cuh"
 #include "router_common.cuh"
 
@@ -43,8 +44,8 @@ namespace {
 // Phase trace (a separate build of the library, with FLINT_PHASE_TRACE
 // defined, for the phase_trace tool): thread 0 of every CTA stamps %clock64 at
 // the phase boundaries into shared memory and, at the end of the call, copies
-// the stamps to a ring of the last kTraceCalls calls, indexed by the call's
-// tag. The plain build has none of this code.
+// the stamps to a ring of the last kTraceCalls calls, indexed by the
+// workspace's call count. The plain build has none of this code.
 #ifdef FLINT_PHASE_TRACE
 constexpr int kTraceStamps = 16, kTraceCalls = 64, kTraceCtas = 256;
 __device__ unsigned long long g_phase_trace[kTraceCalls][kTraceCtas][kTraceStamps];
@@ -65,9 +66,9 @@ constexpr int kMaxDownUnits = 4;
 constexpr int kMaxVec = kMaxDownUnits * FLINT_MAX_TOKENS;
 constexpr int kRowBlock = 16;                 // output rows per combine block
 constexpr int kSharedUnit = -1;
-constexpr int kShIdx = kMaxDistinct;          // index of the shared expert in the per-unit arrays
-// Status bits after which a call must not run: its tags could repeat an
-// unfinished call's (the call counter did not advance).
+constexpr int kShIdx = kMaxDistinct;          // index of the shared expert in the per-expert arrays
+// Status bits after which a call must not run (the exchange counters may
+// have been left mid-call).
 constexpr uint32_t kStatusPoisonMask = kStatusTimeoutRoute | kStatusTimeoutGateUp | kStatusTimeoutDown |
                                        kStatusTimeoutSelftest | kStatusTimeoutLayer | kStatusTimeoutPrefill |
                                        kStatusLayerPlan;
@@ -89,7 +90,7 @@ struct LayerSmall {
     uint32_t rel[kLayerMaxSlots];    // warps done with the slot's current chunk
     int32_t last_issued[kLayerMaxSlots];
     uint32_t hdr[8];                 // workspace header at the start of the call
-    int n_chunks, n_gu, fail, n_last;
+    int n_chunks, n_gu, fail, n_last, ok;
     int b0, b1;                      // this CTA's down range, in (expert, row block) items
     Chunk chunk[kMaxChunks];
     int n_dn;                        // experts among the down chunks
@@ -134,19 +135,6 @@ __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     return L;
 }
 
-// Tagged 64-bit words: the tag in the high half, the value in the low half,
-// one single-copy-atomic store / load at GPU scope.
-__device__ __forceinline__ void st_tagged(uint64_t* p, uint32_t tag, uint32_t v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(((uint64_t)tag << 32) | v) : "memory");
-}
-__device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void ld_tagged2(const uint64_t* p, uint64_t& a, uint64_t& b) {
-    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -157,6 +145,32 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_cta_smem(uint32_t* p, uint3
     asm volatile("atom.add.acq_rel.cta.shared::cta.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v)
                  : "memory");
     return old;
+}
+// Publishes the CTA's earlier writes (ordered before this thread by a
+// __syncthreads) and adds v to a counter at GPU scope.
+__device__ __forceinline__ void release_add_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("fence.acq_rel.gpu;\n red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Thread 0 waits until *p >= target (acquire), for at most budget_ns; the
+// result reaches every thread of the CTA. `code` goes to *status on expiry.
+__device__ __forceinline__ bool cta_wait_count(const uint32_t* p, uint32_t target, uint32_t* status, uint32_t code,
+                                               uint64_t budget_ns, int* s_ok) {
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        if (ld_acquire_gpu(p) < target) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(p) < target) {
+                if (globaltimer_ns() - t0 > budget_ns) {
+                    atomicOr(status, code);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        *s_ok = ok;
+    }
+    __syncthreads();
+    return *s_ok != 0;
 }
 
 // Position, in the concatenation of D experts of `per` items each, of the
@@ -180,13 +194,13 @@ __device__ __forceinline__ int cost_pos(long long tau, const int32_t* cum, int D
 }
 
 // Appends the chunks of the pair range [p0, p1) and the down block range
-// [b0, b1) (items of a concatenation of experts of I_u pairs / NB blocks;
-// unit(i) maps an item's expert position to its unit id). One thread.
-template <typename UnitOf, typename RsOf>
+// [b0, b1) (items of a concatenation of experts of per_gu pairs / NB blocks;
+// unit_of(i) maps an item's expert position to its unit id). One thread.
+template <typename UnitOf, typename RowsOf>
 __device__ void build_chunks(LayerSmall& sm, int p0, int p1, int per_gu, int b0, int b1, int NB, uint32_t* status,
-                             UnitOf unit_of, RsOf rows_per_chunk) {
+                             UnitOf unit_of, RowsOf rows_per_chunk) {
     int n = 0;
-    for (int P = p0; P < p1; ) {
+    for (int P = p0; P < p1;) {
         if (n == kMaxChunks) {
             sm.fail = 1;  // the host sizes the grid so that this cannot happen
             atomicOr(status, kStatusLayerPlan);
@@ -332,7 +346,6 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         drain(budget);
         return;
     }
-    const uint32_t tag = sm.hdr[kHdrEpoch] + 1u;
     const bool withhold = sm.hdr[kHdrLoseCta] == (uint32_t)c + 1u;  // test hook: this CTA publishes no scores
     if (nrr > 0) {
         const bool ok = mbar_wait_bounded(&sm.rbar, 0, a.status, kStatusTimeoutLayer, budget);
@@ -365,35 +378,24 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(full_mask, v, off);
-            if (lane == 0 && !withhold)
-                st_tagged(a.scores + (size_t)t * E + r0 + r, tag, sigmoid_score(v, a.bias, r0 + r));
+            if (lane == 0) a.scores[(size_t)t * E + r0 + r] = sigmoid_score(v, a.bias, r0 + r);
         }
+        __syncthreads();
+        if (tid == 0 && ok && !withhold) release_add_gpu(a.hdr + kHdrScoresIn, (uint32_t)nrr);
     }
-
     FLINT_PHASE(3);
-    // Routing in this CTA: all T x E tagged scores (polled until every one
-    // carries this call's tag) into shared memory over the router rows, the
-    // top-k of each token (one warp per token), the routing view. Every
-    // thread calls it; false (in every thread) if a score never came.
+
+    // Routing in this CTA: once all E router rows are published, all T x E
+    // scores into shared memory over the router rows, the top-k of each token
+    // (one warp per token), the routing view. Every thread calls it; false
+    // (in every thread) if the scores never came.
     auto route = [&]() -> bool {
-        __syncthreads();  // the router rows are dead
-        uint32_t* sc = reinterpret_cast<uint32_t*>(smem + L.rows);
-        bool ok = !sm.fail;
-        for (int i = tid; ok && i < T * E; i += kLT) {
-            uint64_t v = ld_tagged(a.scores + i);
-            if ((uint32_t)(v >> 32) != tag) {
-                const uint64_t t0 = globaltimer_ns();
-                while ((uint32_t)((v = ld_tagged(a.scores + i)) >> 32) != tag) {
-                    if (globaltimer_ns() - t0 > budget) {
-                        atomicOr(a.status, kStatusTimeoutLayer);
-                        ok = false;
-                        break;
-                    }
-                }
-            }
-            sc[i] = (uint32_t)v;
-        }
-        if (!__syncthreads_and(ok)) return false;
+        if (!cta_wait_count(a.hdr + kHdrScoresIn, (uint32_t)E, a.status, kStatusTimeoutLayer, budget, &sm.ok) ||
+            sm.fail)
+            return false;
+        uint32_t* sc = reinterpret_cast<uint32_t*>(smem + L.rows);  // the router rows are dead
+        for (int i = tid; i < T * E; i += kLT) sc[i] = (uint32_t)ld_cg(reinterpret_cast<const int32_t*>(a.scores) + i);
+        __syncthreads();
         if (warp < T) {
             if (E <= 256)
                 topk_warp<8>(sc + (size_t)warp * E, E, k, lane, sm.ids + warp * k, sm.w + warp * k);
@@ -418,11 +420,10 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 a.weights[tid] = sm.w[tid];
             }
             if (warp == 0) {
-                // cost weight of an expert: 2 + the tokens that chose it
-                // (its decode, once, and a multiply-add per token)
+                // cost weight of an expert: 4 + 3 x the tokens that chose it
                 for (int base = 0; base < D; base += 32) {
                     const int u = base + lane;
-                    int v = u < D ? 2 + __popc(ri.tmask[u]) : 0;
+                    int v = u < D ? 4 + 3 * __popc(ri.tmask[u]) : 0;
 #pragma unroll
                     for (int off = 1; off < 32; off <<= 1) {
                         const int n = __shfl_up_sync(full_mask, v, off);
@@ -466,202 +467,198 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     FLINT_PHASE(4);
 
     // ---- 3-4: the ring: gate/up chunks, then (h of the down experts staged) down chunks --
-    const int n_chunks = failed ? 0 : sm.n_chunks, n_gu = sm.n_gu;
+    const int n_chunks = failed ? 0 : sm.n_chunks, n_gu = failed ? 0 : sm.n_gu;
     bool wfail = false;  // this warp gave up on a copy
-    for (int i = 0; i < n_chunks; ++i) {
-        if (i == n_gu) {
-            // Stage h of this CTA's down experts: every value must carry the
-            // tag (written by the CTAs that computed that expert's gate/up).
-            __syncthreads();  // x is dead; the CTA's own h stores are issued
-            FLINT_PHASE(6);
-            if (tid == 0) {
-                int nv = 0, item = 0, off = 0, coff = 0;
-                for (int q = 0; q < sm.n_dn; ++q) {
-                    const int unit = sm.dn_unit[q];
-                    const int K = unit == kSharedUnit ? Is : I;
-                    const uint32_t tm = unit == kSharedUnit ? (1u << T) - 1u : ri.tmask[unit];
-                    for (int t = 0; t < FLINT_MAX_TOKENS; ++t) {
-                        sm.vec[q][t] = -1;
-                        if (t < T && ((tm >> t) & 1u)) {
-                            sm.vec[q][t] = (int16_t)nv;
-                            sm.v_item0[nv] = item;
-                            sm.v_off[nv] = off;
-                            sm.v_coff[nv] = coff;
-                            sm.v_q[nv] = (int16_t)q;
-                            sm.v_t[nv] = (int16_t)t;
-                            item += K / 32;
-                            off += 2 * K;
-                            coff += 4 * (K / 32);
-                            ++nv;
-                        }
-                    }
-                }
-                if (off > a.stage_vals || coff > a.stage_scales) {  // the host plans for this not to happen
-                    atomicOr(a.status, kStatusLayerPlan);
-                    sm.fail = 1;
-                    nv = 0;
-                    item = 0;
-                }
-                sm.n_vec = nv;
-                sm.v_item0[nv] = item;
-            }
-            __syncthreads();
-            bool ok = true;
-            const int n_items = sm.v_item0[sm.n_vec];
-            for (int it = tid; ok && it < n_items; it += kLT) {
-                int v = 0;
-                while (sm.v_item0[v + 1] <= it) ++v;
-                const int cc = it - sm.v_item0[v], q = sm.v_q[v], t = sm.v_t[v];
-                const int unit = sm.dn_unit[q];
-                const bool sh = unit == kSharedUnit;
-                const int K = sh ? Is : I;
-                const uint64_t* src;
-                if (sh) {
-                    src = a.h_shared + (size_t)t * Is;
-                } else {
-                    const int j = __ffs(rank_bits(ri.dmask[unit], t)) - 1;
-                    src = a.h_routed + ((size_t)t * k + j) * I;
-                }
-                src += 32 * cc;
-                // the 32 values as bf16 pairs, once every word carries the tag
-                uint4 w4[4];
-                uint64_t t0 = 0;
-                while (true) {
-                    bool all = true;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        uint64_t e[8];
-#pragma unroll
-                        for (int i2 = 0; i2 < 4; ++i2) ld_tagged2(src + 8 * g + 2 * i2, e[2 * i2], e[2 * i2 + 1]);
-#pragma unroll
-                        for (int i2 = 0; i2 < 8; ++i2) all = all && (uint32_t)(e[i2] >> 32) == tag;
-                        w4[g] = make_uint4((uint32_t)(e[0] & 0xFFFFu) | ((uint32_t)e[1] << 16),
-                                           (uint32_t)(e[2] & 0xFFFFu) | ((uint32_t)e[3] << 16),
-                                           (uint32_t)(e[4] & 0xFFFFu) | ((uint32_t)e[5] << 16),
-                                           (uint32_t)(e[6] & 0xFFFFu) | ((uint32_t)e[7] << 16));
-                    }
-                    if (all) break;
-                    if (!t0) {
-                        t0 = globaltimer_ns();
-                    } else if (globaltimer_ns() - t0 > budget) {
-                        atomicOr(a.status, kStatusTimeoutLayer);
-                        ok = false;
-                        break;
-                    }
-                }
-                if (!ok) break;
-                const StageSrc ss = {nullptr, reinterpret_cast<uint4*>(smem + L.xs + sm.v_off[v]),
-                                     reinterpret_cast<float*>(smem + L.csc + sm.v_coff[v]), 1, K};
-                stage_store<true>(ss, 0, cc, w4);
-            }
-            if (!__syncthreads_and(ok)) {
-                wfail = true;
-                if (tid == 0) sm.fail = 1;
-            }
-            FLINT_PHASE(7);
-        }
-        const int s = i % NS;
+    // Waits for chunk i's bytes (all lanes; false once anything failed).
+    auto chunk_in = [&](int i) {
         if (!wfail && !sm.fail) {
-            if (!__all_sync(full_mask,
-                            mbar_wait_bounded(&sm.full[s], (uint32_t)(i / NS) & 1u, a.status, kStatusTimeoutLayer,
-                                              budget))) {
-                wfail = true;
-                if (lane == 0) sm.fail = 1;
-            }
-        } else {
-            wfail = true;
+            if (__all_sync(full_mask, mbar_wait_bounded(&sm.full[i % NS], (uint32_t)(i / NS) & 1u, a.status,
+                                                        kStatusTimeoutLayer, budget)))
+                return true;
+            if (lane == 0) sm.fail = 1;
         }
-        if (wfail) continue;
-        if (i == 0) FLINT_PHASE(5);
-        const Chunk ch = sm.chunk[i];
-        const uint8_t* slot = ring + (size_t)s * a.slot;
-        const bool sh = ch.unit == kSharedUnit;
-        const int ui = sh ? kShIdx : ch.unit;
-        const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[ch.unit];
-        if (ch.kind == kChunkGateUp) {
-            if (warp < ch.count) {
-                const uint8_t* grow = slot + (size_t)warp * RS;
-                const uint8_t* urow = slot + (size_t)(kLW + warp) * RS;
-                float* rg = sm.res[warp][0];
-                float* ru = sm.res[warp][1];
-                gate_up_item<true>(grow, urow, H, xh, csc, tm, lane, rg, ru);
-                __syncwarp();
-                if (lane < T && ((tm >> lane) & 1u)) {
-                    const int p = ch.start + warp;
-                    const float g = bf16_round_f32(sm.tsg[ui] * rg[lane]);
-                    const float u = bf16_round_f32(sm.tsu[ui] * ru[lane]);
-                    const uint32_t hv = f32_to_bf16_bits(silu_f32(g) * u);
-                    uint64_t* dst;
-                    if (sh) {
-                        dst = a.h_shared + (size_t)lane * Is + p;
-                    } else {
-                        const int j = __ffs(rank_bits(ri.dmask[ch.unit], lane)) - 1;
-                        dst = a.h_routed + ((size_t)lane * k + j) * I + p;
-                    }
-                    st_tagged(dst, tag, hv);
-                }
-            }
-        } else {
-            const int rw0 = 8 * warp;
-            if (rw0 < ch.count) {
-                const int nrw = min(8, ch.count - rw0);
-                const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
-                const uint8_t* rows = slot + (size_t)rw0 * RSu;
-                const int row0 = ch.start + rw0;
-                const float tsd = sm.tsd[ui];
-                const unsigned long long dm = sh ? 0ull : ri.dmask[ch.unit];
-                auto vec = [&](int t, const uint4*& hv, const float*& cv) {
-                    const int v = sm.vec[ch.q][t];
-                    hv = reinterpret_cast<const uint4*>(smem + L.xs + sm.v_off[v]);
-                    cv = reinterpret_cast<const float*>(smem + L.csc + sm.v_coff[v]);
-                };
-                auto put = [&](float v, int r, int t) {
-                    const uint16_t d = f32_to_bf16_bits(tsd * v);
-                    if (sh) {
-                        a.d_shared[(size_t)t * H + row0 + r] = d;
-                    } else {
-                        const int j = __ffs(rank_bits(dm, t)) - 1;
-                        a.d_routed[((size_t)t * k + j) * H + row0 + r] = d;
-                    }
-                };
-                uint32_t rest = tm;
-                while (rest) {
-                    const int t0 = __ffs(rest) - 1;
-                    rest &= rest - 1u;
-                    if (rest) {  // two tokens
-                        const int t1 = __ffs(rest) - 1;
-                        rest &= rest - 1u;
-                        const uint4* hv[2];
-                        const float* cv[2];
-                        vec(t0, hv[0], cv[0]);
-                        vec(t1, hv[1], cv[1]);
-                        float acc[16];
-                        down_pass<8, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
-                        const float v = reduce_scatter<16>(acc, lane);
-                        const int idx = rs_index<16>(lane), r = idx & 7;
-                        if ((lane & 1) == 0 && r < nrw) put(v, r, (idx >> 3) ? t1 : t0);
-                    } else {
-                        const uint4* hv[1];
-                        const float* cv[1];
-                        vec(t0, hv[0], cv[0]);
-                        float acc[8];
-                        down_pass<8, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
-                        const float v = reduce_scatter<8>(acc, lane);
-                        const int r = rs_index<8>(lane);
-                        if ((lane & 3) == 0 && r < nrw) put(v, r, t0);
-                    }
-                }
-            }
-        }
-        // The last warp done with the chunk refills its slot.
+        wfail = true;
+        return false;
+    };
+    // The last warp done with chunk i refills its slot with chunk i + NS.
+    auto chunk_done = [&](int i) {
         __syncwarp();
         if (lane == 0) {
-            const uint32_t old = atom_add_acq_rel_cta_smem(&sm.rel[s], 1u);
-            if (old == kLW - 1) {
+            const int s = i % NS;
+            if (atom_add_acq_rel_cta_smem(&sm.rel[s], 1u) == kLW - 1) {
                 sm.rel[s] = 0;
                 if (!sm.fail) issue(i + NS);
             }
         }
+    };
+    for (int i = 0; i < n_gu; ++i) {
+        if (!chunk_in(i)) continue;
+        if (i == 0) FLINT_PHASE(5);
+        const Chunk ch = sm.chunk[i];
+        if (warp < ch.count) {
+            const uint8_t* slot = ring + (size_t)(i % NS) * a.slot;
+            const bool sh = ch.unit == kSharedUnit;
+            const int ui = sh ? kShIdx : ch.unit;
+            const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[ch.unit];
+            const uint8_t* grow = slot + (size_t)warp * RS;
+            const uint8_t* urow = slot + (size_t)(kLW + warp) * RS;
+            float* rg = sm.res[warp][0];
+            float* ru = sm.res[warp][1];
+            gate_up_item<true>(grow, urow, H, xh, csc, tm, lane, rg, ru);
+            __syncwarp();
+            if (lane < T && ((tm >> lane) & 1u)) {
+                const int p = ch.start + warp;
+                const float g = bf16_round_f32(sm.tsg[ui] * rg[lane]);
+                const float u = bf16_round_f32(sm.tsu[ui] * ru[lane]);
+                const uint16_t hv = f32_to_bf16_bits(silu_f32(g) * u);
+                if (sh) {
+                    a.h_shared[(size_t)lane * Is + p] = hv;
+                } else {
+                    const int j = __ffs(rank_bits(ri.dmask[ch.unit], lane)) - 1;
+                    a.h_routed[((size_t)lane * k + j) * I + p] = hv;
+                }
+            }
+        }
+        chunk_done(i);
+    }
+    // Publish this CTA's h: per expert, the number of its pairs done here.
+    if (__syncthreads_or(wfail) && tid == 0) sm.fail = 1;
+    if (tid == 0 && !sm.fail) {
+        int unit = -2, cnt = 0;
+        for (int i = 0; i <= n_gu; ++i) {
+            const int u = i < n_gu ? sm.chunk[i].unit : -3;
+            if (u != unit && cnt) release_add_gpu(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit), cnt);
+            if (u != unit) {
+                unit = u;
+                cnt = 0;
+            }
+            if (i < n_gu) cnt += sm.chunk[i].count;
+        }
+    }
+    FLINT_PHASE(6);
+    if (n_chunks > n_gu) {
+        // Stage h of this CTA's down experts once every pair of each is published.
+        if (tid == 0) {
+            int nv = 0, item = 0, off = 0, coff = 0;
+            for (int q = 0; q < sm.n_dn; ++q) {
+                const int unit = sm.dn_unit[q];
+                const int K = unit == kSharedUnit ? Is : I;
+                const uint32_t tm = unit == kSharedUnit ? (1u << T) - 1u : ri.tmask[unit];
+                for (int t = 0; t < FLINT_MAX_TOKENS; ++t) {
+                    sm.vec[q][t] = -1;
+                    if (t < T && ((tm >> t) & 1u)) {
+                        sm.vec[q][t] = (int16_t)nv;
+                        sm.v_item0[nv] = item;
+                        sm.v_off[nv] = off;
+                        sm.v_coff[nv] = coff;
+                        sm.v_q[nv] = (int16_t)q;
+                        sm.v_t[nv] = (int16_t)t;
+                        item += K / 32;
+                        off += 2 * K;
+                        coff += 4 * (K / 32);
+                        ++nv;
+                    }
+                }
+            }
+            if (off > a.stage_vals || coff > a.stage_scales) {  // the host plans for this not to happen
+                atomicOr(a.status, kStatusLayerPlan);
+                sm.fail = 1;
+                nv = 0;
+                item = 0;
+            }
+            sm.n_vec = nv;
+            sm.v_item0[nv] = item;
+        }
+        bool ok = true;
+        for (int q = 0; q < sm.n_dn && ok; ++q) {  // sm.n_dn: written before the earlier barriers
+            const int unit = sm.dn_unit[q];
+            ok = cta_wait_count(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit),
+                                (uint32_t)(unit == kSharedUnit ? Is : I), a.status, kStatusTimeoutLayer, budget,
+                                &sm.ok);
+        }
+        ok = ok && !sm.fail;
+        const int n_items = ok ? sm.v_item0[sm.n_vec] : 0;
+        for (int it = tid; it < n_items; it += kLT) {
+            int v = 0;
+            while (sm.v_item0[v + 1] <= it) ++v;
+            const int cc = it - sm.v_item0[v], t = sm.v_t[v];
+            const int unit = sm.dn_unit[sm.v_q[v]];
+            const bool sh = unit == kSharedUnit;
+            const int K = sh ? Is : I;
+            const uint16_t* src;
+            if (sh) {
+                src = a.h_shared + (size_t)t * Is;
+            } else {
+                const int j = __ffs(rank_bits(ri.dmask[unit], t)) - 1;
+                src = a.h_routed + ((size_t)t * k + j) * I;
+            }
+            const StageSrc ss = {src, reinterpret_cast<uint4*>(smem + L.xs + sm.v_off[v]),
+                                 reinterpret_cast<float*>(smem + L.csc + sm.v_coff[v]), 1, K};
+            uint4 w4[4];
+            stage_load(ss, 0, cc, w4);
+            stage_store<true>(ss, 0, cc, w4);
+        }
+        if (!__syncthreads_and(ok)) wfail = true;
+    }
+    FLINT_PHASE(7);
+    for (int i = n_gu; i < n_chunks; ++i) {
+        if (!chunk_in(i)) continue;
+        const Chunk ch = sm.chunk[i];
+        const int rw0 = 8 * warp;
+        if (rw0 < ch.count) {
+            const uint8_t* slot = ring + (size_t)(i % NS) * a.slot;
+            const bool sh = ch.unit == kSharedUnit;
+            const int ui = sh ? kShIdx : ch.unit;
+            const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[ch.unit];
+            const int nrw = min(8, ch.count - rw0);
+            const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
+            const uint8_t* rows = slot + (size_t)rw0 * RSu;
+            const int row0 = ch.start + rw0;
+            const float tsd = sm.tsd[ui];
+            const unsigned long long dm = sh ? 0ull : ri.dmask[ch.unit];
+            auto vec = [&](int t, const uint4*& hv, const float*& cv) {
+                const int v = sm.vec[ch.q][t];
+                hv = reinterpret_cast<const uint4*>(smem + L.xs + sm.v_off[v]);
+                cv = reinterpret_cast<const float*>(smem + L.csc + sm.v_coff[v]);
+            };
+            auto put = [&](float v, int r, int t) {
+                const uint16_t d = f32_to_bf16_bits(tsd * v);
+                if (sh) {
+                    a.d_shared[(size_t)t * H + row0 + r] = d;
+                } else {
+                    const int j = __ffs(rank_bits(dm, t)) - 1;
+                    a.d_routed[((size_t)t * k + j) * H + row0 + r] = d;
+                }
+            };
+            uint32_t rest = tm;
+            while (rest) {
+                const int t0 = __ffs(rest) - 1;
+                rest &= rest - 1u;
+                if (rest) {  // two tokens
+                    const int t1 = __ffs(rest) - 1;
+                    rest &= rest - 1u;
+                    const uint4* hv[2];
+                    const float* cv[2];
+                    vec(t0, hv[0], cv[0]);
+                    vec(t1, hv[1], cv[1]);
+                    float acc[16];
+                    down_pass<8, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                    const float v = reduce_scatter<16>(acc, lane);
+                    const int idx = rs_index<16>(lane), r = idx & 7;
+                    if ((lane & 1) == 0 && r < nrw) put(v, r, (idx >> 3) ? t1 : t0);
+                } else {
+                    const uint4* hv[1];
+                    const float* cv[1];
+                    vec(t0, hv[0], cv[0]);
+                    float acc[8];
+                    down_pass<8, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                    const float v = reduce_scatter<8>(acc, lane);
+                    const int r = rs_index<8>(lane);
+                    if ((lane & 3) == 0 && r < nrw) put(v, r, t0);
+                }
+            }
+        }
+        chunk_done(i);
     }
 
     // ---- 5: arrivals on the row blocks; the last arriver of a block combines it ------
@@ -670,13 +667,14 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         // the shared group learns the routing now (weights, number of experts)
         failed = !route();
     }
-    __threadfence();  // this thread's d (and h) stores are visible before any arrival
     if (__syncthreads_or(failed || wfail || sm.fail)) {
         drain(budget);
         return;
     }
     const uint32_t U = (uint32_t)ri.D + (has_sh ? 1u : 0u);
     for (int j = sm.b0 + tid; j < sm.b1; j += kLT) {
+        // the release half of the add publishes the CTA's d, ordered before
+        // this thread by the barriers above
         const int blk = j % NB;
         if (atom_add_acq_rel_gpu(a.counters + blk, 1u) == U - 1u) sm.last[atomicAdd(&sm.n_last, 1)] = (int16_t)blk;
     }
@@ -696,9 +694,10 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     }
     for (int q = tid; q < n_last; q += kLT) a.counters[sm.last[q]] = 0;
     __syncthreads();
+    FLINT_PHASE(10);
 #ifdef FLINT_PHASE_TRACE
     if (tid == 0 && c < kTraceCtas) {
-        unsigned long long* dst = g_phase_trace[tag % kTraceCalls][c];
+        unsigned long long* dst = g_phase_trace[sm.hdr[kHdrCalls] % kTraceCalls][c];
         for (int i = 0; i < 11; ++i) dst[i] = sm.trace[i];
         uint32_t smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -707,13 +706,17 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                   ((unsigned long long)n_last << 16) | ((unsigned long long)sm.n_gu << 32);
         dst[13] = trace_t0;
         dst[14] = globaltimer_ns();
-        dst[15] = tag;
+        dst[15] = sm.hdr[kHdrCalls] + 1ull;
     }
 #endif
-    // the last CTA to finish advances the call counter (the next call's tag)
+    // The last CTA to finish resets the exchange counters for the next call
+    // (every other CTA is past all of its waits) and counts the call.
     if (tid == 0 && atomicAdd(a.hdr + kHdrDone, 1u) == (uint32_t)G - 1u) {
+        a.hdr[kHdrScoresIn] = 0;
+        for (int u = 0; u < ri.D; ++u) a.unit_counters[u] = 0;
+        a.unit_counters[kShIdx] = 0;
+        a.hdr[kHdrCalls] = sm.hdr[kHdrCalls] + 1u;
         a.hdr[kHdrDone] = 0;
-        a.hdr[kHdrEpoch] = tag;
     }
 }
 

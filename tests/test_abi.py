@@ -44,9 +44,9 @@ def test_size_helpers(flint):
     assert flint.flint_nvfp4_packed_bytes(256, 1024, 2048) == 256 * 1024 * 1152
     assert flint.flint_gguf_nvfp4_bytes(1, 2048, 512) == 2048 * 8 * 36
     ws = flint.flint_workspace_bytes(256, 6, 2048, 512, 512)
-    # header, logits, h (routed, shared), tagged scores and h, d (routed, shared), row-block counters
-    need = (256 + 8 * 256 * 4 + 2 * 8 * 6 * 512 + 2 * 8 * 512 + 8 * 8 * 256 + 8 * 8 * 6 * 512 + 8 * 8 * 512
-            + 2 * 8 * 6 * 2048 + 2 * 8 * 2048 + 4 * 2048 // 16)
+    # header, logits, h (routed, shared), d (routed, shared), row-block counters, per-expert counters
+    need = (256 + 8 * 256 * 4 + 2 * 8 * 6 * 512 + 2 * 8 * 512 + 2 * 8 * 6 * 2048 + 2 * 8 * 2048 + 4 * 2048 // 16
+            + 4 * (8 * 8 + 1))
     assert ws % 256 == 0 and ws >= need
     assert flint.flint_status_string(4) == "device wait timed out"
 
