@@ -47,7 +47,7 @@ namespace {
 // the stamps to a ring of the last kTraceCalls calls, indexed by the
 // workspace's call count. The plain build has none of this code.
 #ifdef FLINT_PHASE_TRACE
-constexpr int kTraceStamps = 16, kTraceCalls = 64, kTraceCtas = 256;
+constexpr int kTraceStamps = 32, kTraceCalls = 64, kTraceCtas = 256;
 __device__ unsigned long long g_phase_trace[kTraceCalls][kTraceCtas][kTraceStamps];
 #define FLINT_PHASE(i)                                     \
     do {                                                   \
@@ -297,6 +297,10 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 #ifdef FLINT_PHASE_TRACE
     const uint64_t trace_t0 = globaltimer_ns();
 #endif
+#ifdef FLINT_PHASE_TRACE
+    if (tid < kTraceStamps) sm.trace[tid] = 0;
+    __syncthreads();
+#endif
     FLINT_PHASE(0);
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -382,6 +386,9 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         }
         __syncthreads();
         if (tid == 0 && ok && !withhold) release_add_gpu(a.hdr + kHdrScoresIn, (uint32_t)nrr);
+#ifdef FLINT_PHASE_TRACE
+        if (tid == 0) sm.trace[26] = globaltimer_ns();
+#endif
     }
     FLINT_PHASE(3);
 
@@ -389,13 +396,16 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     // scores into shared memory over the router rows, the top-k of each token
     // (one warp per token), the routing view. Every thread calls it; false
     // (in every thread) if the scores never came.
-    auto route = [&]() -> bool {
+    auto route = [&](int stamp) -> bool {
+        (void)stamp;
         if (!cta_wait_count(a.hdr + kHdrScoresIn, (uint32_t)E, a.status, kStatusTimeoutLayer, budget, &sm.ok) ||
             sm.fail)
             return false;
+        FLINT_PHASE(stamp);
         uint32_t* sc = reinterpret_cast<uint32_t*>(smem + L.rows);  // the router rows are dead
         for (int i = tid; i < T * E; i += kLT) sc[i] = (uint32_t)ld_cg(reinterpret_cast<const int32_t*>(a.scores) + i);
         __syncthreads();
+        FLINT_PHASE(stamp + 1);
         if (warp < T) {
             if (E <= 256)
                 topk_warp<8>(sc + (size_t)warp * E, E, k, lane, sm.ids + warp * k, sm.w + warp * k);
@@ -404,14 +414,16 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                                                   sm.w + warp * k);
         }
         __syncthreads();
+        FLINT_PHASE(stamp + 2);
         build_route_info<true>(ri, sm.ids, T, k, E, nullptr);
+        FLINT_PHASE(stamp + 3);
         return true;
     };
 
     bool failed = false;
     if (!sh_cta) {
         // ---- 2: routing, this CTA's share of the selected experts ---------------
-        if (!route()) {
+        if (!route(11)) {
             failed = true;
         } else {
             const int D = ri.D;
@@ -449,6 +461,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                     if (!sm.fail)
                         for (int i = 0; i < NS; ++i) issue(i);
                 }
+                FLINT_PHASE(19);
             }
             // the tensor scales of the selected experts (their copies are in flight)
             if (tid < D) {
@@ -665,7 +678,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     FLINT_PHASE(8);
     if (!__syncthreads_or(failed || wfail || sm.fail) && sh_cta) {
         // the shared group learns the routing now (weights, number of experts)
-        failed = !route();
+        failed = !route(15);
     }
     if (__syncthreads_or(failed || wfail || sm.fail)) {
         drain(budget);
@@ -698,15 +711,15 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 #ifdef FLINT_PHASE_TRACE
     if (tid == 0 && c < kTraceCtas) {
         unsigned long long* dst = g_phase_trace[sm.hdr[kHdrCalls] % kTraceCalls][c];
-        for (int i = 0; i < 11; ++i) dst[i] = sm.trace[i];
+        for (int i = 0; i < 27; ++i) dst[i] = sm.trace[i];
         uint32_t smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        dst[11] = smid;
-        dst[12] = (unsigned long long)sh_cta | ((unsigned long long)sm.n_chunks << 8) |
+        dst[27] = smid;
+        dst[28] = (unsigned long long)sh_cta | ((unsigned long long)sm.n_chunks << 8) |
                   ((unsigned long long)n_last << 16) | ((unsigned long long)sm.n_gu << 32);
-        dst[13] = trace_t0;
-        dst[14] = globaltimer_ns();
-        dst[15] = sm.hdr[kHdrCalls] + 1ull;
+        dst[29] = trace_t0;
+        dst[30] = globaltimer_ns();
+        dst[31] = sm.hdr[kHdrCalls] + 1ull;
     }
 #endif
     // The last CTA to finish resets the exchange counters for the next call

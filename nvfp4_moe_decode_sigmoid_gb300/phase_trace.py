@@ -10,17 +10,23 @@ cycles.
 
     python -m nvfp4_moe_decode_sigmoid_gb300.phase_trace --tokens 1
 
-Phases (stamp i to stamp i + 1):
-  0 entry -> PDL wait passed      the static copies issued; waiting for the previous call
-  1 -> x staged                   x read and converted (or the norm of the residual)
-  2 -> router scores published    this CTA's router rows (bulk copy) times x
-  3 -> routing known              all scores read, top-k, the work split, the first copies issued
-  4 -> first chunk in             the first ring chunk's bytes landed
-  5 -> gate/up done               the CTA's gate/up pairs, h published
-  6 -> h staged                   the h of its down experts read (waits for the other CTAs)
-  7 -> down done                  its down rows, d written
-  8 -> arrivals                   the counts on its row blocks
-  9 -> end                        the combine of the blocks it completed
+Intervals (between the kernel's stamps; "-" where a group of CTAs has none):
+  wait for the previous call      entry to the PDL wait's return (static copies issued)
+  x staged                        x read and converted (or the norm of the residual)
+  router scores published         this CTA's router rows (bulk copy) times x, the count raised
+  all scores in                   waiting until every router row is published
+  scores read                     all T x E scores into shared memory
+  top-k                           one warp per token
+  routing view                    the distinct experts and their tokens
+  split, first copies             this CTA's ranges and its first ring copies issued
+  tensor scales                   the selected experts' tensor scales
+  first chunk in                  the first ring chunk's bytes landed
+  gate/up                         the CTA's gate/up pairs, h written and counted
+  h of the down experts staged    waits for the other CTAs' h of those experts
+  down                            its down rows, d written
+  routing (shared group, at end)  the same four routing steps, for the combine weights
+  arrivals                        the counts on its row blocks
+  combine                         the blocks it completed
 """
 from __future__ import annotations
 
@@ -32,9 +38,18 @@ import sys
 
 import numpy as np
 
-PHASES = ["wait for the previous call", "x staged", "router scores published", "routing, split, first copies",
-          "first chunk in", "gate/up", "h of the down experts staged", "down", "arrivals", "combine"]
-N_STAMPS, N_CALLS, N_CTAS = 16, 64, 256
+# (name, from stamp, to stamp); the stamps the kernel takes (see layer.cu)
+INTERVALS = [("wait for the previous call", 0, 1, "all"), ("x staged", 1, 2, "all"),
+             ("router scores published", 2, 3, "all"), ("all scores in", 3, 11, "routed"),
+             ("scores read", 11, 12, "routed"), ("top-k", 12, 13, "routed"), ("routing view", 13, 14, "routed"),
+             ("split, first copies", 14, 19, "routed"), ("tensor scales", 19, 4, "routed"),
+             ("tensor scales", 3, 4, "shared"), ("first chunk in", 4, 5, "all"), ("gate/up", 5, 6, "all"),
+             ("h of the down experts staged", 6, 7, "all"), ("down", 7, 8, "all"),
+             ("at the end: all scores in", 8, 15, "shared"), ("at the end: scores read", 15, 16, "shared"),
+             ("at the end: top-k", 16, 17, "shared"), ("at the end: routing view", 17, 18, "shared"),
+             ("arrivals", 18, 9, "shared"), ("arrivals", 8, 9, "routed"), ("combine", 9, 10, "all"),
+             ("after the wait, to the end", 1, 10, "all")]
+N_STAMPS, N_CALLS, N_CTAS = 32, 64, 256
 
 
 def main(argv=None):
@@ -101,36 +116,38 @@ def main(argv=None):
     tr = buf.reshape(N_CALLS, N_CTAS, N_STAMPS).astype(np.int64)
     G = torch.cuda.get_device_properties(0).multi_processor_count
     tr = tr[:, :G]
-    calls = [c for c in range(N_CALLS) if np.all(tr[c, :, 15] == tr[c, 0, 15]) and tr[c, 0, 15] > 0]
-    shared_role = (tr[:, :, 12] & 0xFF) == 1
-    durations = {}  # (role, phase) -> list of cycles
+    calls = [c for c in range(N_CALLS) if np.all(tr[c, :, 31] == tr[c, 0, 31]) and tr[c, 0, 31] > 0]
+    shared_role = (tr[:, :, 28] & 0xFF) == 1
+    cells = {}  # (role, interval) -> list of cycles
     for c in calls:
         for cta in range(G):
             role = "shared" if shared_role[c, cta] else "routed"
-            st = tr[c, cta, :11]
-            for ph in range(10):
-                durations.setdefault((role, ph), []).append(int(st[ph + 1] - st[ph]))
-    # kernel span from the coarse global timer: first entry to last end of each call
-    spans = [(tr[c, :, 14].max() - tr[c, :, 13].min()) / 1e3 for c in calls]
+            st = tr[c, cta]
+            for n, (_, a, b, who) in enumerate(INTERVALS):
+                if who in ("all", role) and st[a] and st[b]:
+                    cells.setdefault((role, n), []).append(int(st[b] - st[a]))
+    spans = [(tr[c, :, 30].max() - tr[c, :, 29].min()) / 1e3 for c in calls]
+    # spread over the CTAs of one call (global timer, coarse): entries, score publications
+    entry_spread = [(tr[c, :, 29].max() - tr[c, :, 29].min()) / 1e3 for c in calls]
+    pub = [tr[c, tr[c, :, 26] > 0, 26] for c in calls]
+    pub_spread = [(p.max() - p.min()) / 1e3 for p in pub if p.size]
     print(f"## Fused layer phases: T = {T}, {args.routing} routing, {len(calls)} calls traced "
           f"({args.layers} resident layers, PDL-chained in one CUDA graph)\n")
     print("kcycles of the SM clock, median / max over the CTAs of all traced calls\n")
-    print("| phase | shared-expert CTAs | routed-expert CTAs |")
+    print("| interval | shared-expert CTAs | routed-expert CTAs |")
     print("|---|---|---|")
-    for ph in range(10):
-        cells = []
+    for n, (name, _, _, _) in enumerate(INTERVALS):
+        row = []
         for role in ("shared", "routed"):
-            v = durations.get((role, ph), [])
-            cells.append(f"{statistics.median(v) / 1e3:.2f} / {max(v) / 1e3:.2f}" if v else "-")
-        print(f"| {ph} {PHASES[ph]} | {cells[0]} | {cells[1]} |")
-    tot = {role: [int(tr[c, cta, 10] - tr[c, cta, 1]) for c in calls for cta in range(G)
-                  if (role == "shared") == bool(shared_role[c, cta])] for role in ("shared", "routed")}
-    print(f"| after the wait, to the end | {statistics.median(tot['shared']) / 1e3:.2f} / "
-          f"{max(tot['shared']) / 1e3:.2f} | {statistics.median(tot['routed']) / 1e3:.2f} / "
-          f"{max(tot['routed']) / 1e3:.2f} |")
-    print(f"\nCTAs: {int(shared_role[calls[0]].sum())} shared, {G - int(shared_role[calls[0]].sum())} routed; "
-          f"call span on the global timer (first entry to last end, includes the wait for the previous call): "
-          f"median {statistics.median(spans):.2f} us")
+            v = cells.get((role, n), [])
+            row.append(f"{statistics.median(v) / 1e3:.2f} / {max(v) / 1e3:.2f}" if v else "-")
+        if row != ["-", "-"]:
+            print(f"| {name} | {row[0]} | {row[1]} |")
+    n_sh = int(shared_role[calls[0]].sum())
+    print(f"\nCTAs: {n_sh} shared, {G - n_sh} routed. On the global timer (coarse), median over the calls: "
+          f"call span (first entry to last end, with the wait for the previous call) "
+          f"{statistics.median(spans):.2f} us; spread of the CTAs' entries {statistics.median(entry_spread):.2f} us; "
+          f"spread of their router-score publications {statistics.median(pub_spread):.2f} us")
 
 
 if __name__ == "__main__":
