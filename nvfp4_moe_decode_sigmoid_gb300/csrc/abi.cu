@@ -207,6 +207,13 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
         a.Gs = 0;
     }
     a.rpc = ceil_div(a.E, G);
+    // the kernel splits by cost in 32-bit arithmetic: the total cost of the
+    // routed pairs (or blocks) times the group's CTA count must stay below 2^32
+    // (an expert's weight is at most 4 + 3 T and the weights sum to at most
+    // 4 min(E, T k) + 3 T k)
+    const unsigned long long wmax = 4ull * units + 3ull * T * a.k;
+    const unsigned long long per = (unsigned long long)(a.I > H / 16 ? a.I : H / 16);
+    if (wmax * per * (unsigned long long)(G + 1) >= (1ull << 32)) return false;
     const int RS = (int)flint::nvfp4_row_stride(H);
     a.slot = 2 * flint::kLayerWarps * RS;
     // a down chunk takes whole 16-row blocks

@@ -35,6 +35,8 @@
 // are left mid-call and the workspace must be re-initialised
 // (flint_workspace_check does it); until then every call returns at once,
 // leaving its outputs unwritten, and the status stays set.
+#include <type_traits>
+
 #include "expert_common.cuh"
 #include "router_common.cuh"
 
@@ -113,11 +115,12 @@ struct LayerSmall {
 #endif
 };
 
-// Shared memory: small arrays, the routing view, the staging region (x, then
+// Shared memory: small arrays, the routing view, the tensor scales of all
+// routed experts, the router logits' partial sums, the staging region (x, then
 // h of the CTA's down experts) and its chunk scales, the norm's partial sums,
 // the router rows (later: all sigmoid scores for the top-k), the ring.
 struct LayerSmem {
-    size_t small, ri, xs, csc, nred, rows, ring, total;
+    size_t small, ri, tsall, part, xs, csc, nred, rows, ring, total;
 };
 
 __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
@@ -125,7 +128,9 @@ __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     const size_t T = a.T, H = a.H;
     L.small = 0;
     L.ri = align_up(sizeof(LayerSmall), 128);
-    L.xs = align_up(L.ri + sizeof(RouteInfo), 128);
+    L.tsall = align_up(L.ri + sizeof(RouteInfo), 128);
+    L.part = align_up(L.tsall + 12 * (size_t)a.E, 128);
+    L.xs = align_up(L.part + sizeof(float) * (size_t)a.rpc * T * (H / 256), 128);
     L.csc = align_up(L.xs + (size_t)a.stage_vals, 128);
     L.nred = align_up(L.csc + (size_t)a.stage_scales, 128);
     L.rows = align_up(L.nred + (a.norm.r ? sizeof(float) * T * (H / 32) : 0), 128);
@@ -173,24 +178,69 @@ __device__ __forceinline__ bool cta_wait_count(const uint32_t* p, uint32_t targe
     return *s_ok != 0;
 }
 
+// The routing view (the distinct selected experts in ascending order, and
+// per expert which ranks of which tokens chose it) built by one warp from the
+// T x k ids in shared memory (every id valid, distinct within a token, E <=
+// 1024): lane l owns the bitmap word of experts 32 l .. 32 l + 31.
+__device__ void route_view_warp(RouteInfo& ri, const int32_t* ids, int T, int k, int lane) {
+    const uint32_t full = 0xffffffffu;
+    const int n = T * k;
+    uint32_t word = 0;
+    for (int i = 0; i < n; ++i) {
+        const int e = ids[i];
+        if ((e >> 5) == lane) word |= 1u << (e & 31);
+    }
+    const uint32_t cnt = __popc(word);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_up_sync(full, incl, off);
+        if (lane >= off) incl += v;
+    }
+    const uint32_t base = incl - cnt;
+    const int D = (int)__shfl_sync(full, incl, 31);
+    for (uint32_t w = word, d = base; w; w &= w - 1u, ++d) ri.dlist[d] = 32 * lane + __ffs(w) - 1;
+    for (int d = lane; d < D; d += 32) {
+        ri.dmask[d] = 0ull;
+        ri.tmask[d] = 0u;
+    }
+    __syncwarp();
+    for (int i0 = 0; i0 < n; i0 += 32) {
+        const int i = i0 + lane;
+        const int e = i < n ? ids[i] : 0;
+        const uint32_t bw = __shfl_sync(full, word, e >> 5), bb = __shfl_sync(full, base, e >> 5);
+        if (i < n) {
+            const int d = (int)(bb + __popc(bw & ((1u << (e & 31)) - 1u)));
+            const int t = i / k, j = i - t * k;
+            atomicOr(&ri.dmask[d], 1ull << (8 * t + j));
+            atomicOr(&ri.tmask[d], 1u << t);
+            ri.ids[i] = e;
+        }
+    }
+    if (lane == 0) ri.D = D;
+    __syncwarp();
+}
+
 // Position, in the concatenation of D experts of `per` items each, of the
 // cost target tau, where an item of expert u costs w_u and cum[u] is the
 // inclusive prefix of the w_u: the experts before the one that holds tau,
 // plus the items of that expert whose cost lies below tau (rounded up).
 // Monotone in tau, pos(0) = 0, pos(per * cum[D - 1]) = D * per, so the ranges
 // [pos(c total / G'), pos((c + 1) total / G')) tile the items exactly.
-__device__ __forceinline__ int cost_pos(long long tau, const int32_t* cum, int D, int per) {
+// (32-bit arithmetic: per * cum[D - 1] * (G' + 1) < 2^32 for the shapes the
+// host accepts.)
+__device__ __forceinline__ int cost_pos(uint32_t tau, const int32_t* cum, int D, int per) {
     int lo = 0, hi = D;  // first expert u with per * cum[u] > tau
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if ((long long)per * cum[mid] > tau) hi = mid;
+        if ((uint32_t)per * (uint32_t)cum[mid] > tau) hi = mid;
         else lo = mid + 1;
     }
     if (lo >= D) return D * per;
-    const long long before = lo ? (long long)per * cum[lo - 1] : 0;
-    const int wu = cum[lo] - (lo ? cum[lo - 1] : 0);
-    const long long p = (tau - before + wu - 1) / wu;
-    return lo * per + (int)(p < per ? p : per);
+    const uint32_t before = lo ? (uint32_t)per * (uint32_t)cum[lo - 1] : 0u;
+    const uint32_t wu = (uint32_t)(cum[lo] - (lo ? cum[lo - 1] : 0));
+    const uint32_t p = (tau - before + wu - 1u) / wu;
+    return lo * per + (int)(p < (uint32_t)per ? p : (uint32_t)per);
 }
 
 // Appends the chunks of the pair range [p0, p1) and the down block range
@@ -254,6 +304,11 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     const int NB = H / kRowBlock;
     const int r0 = c * a.rpc, nrr = max(0, min(a.rpc, E - r0));
     const uint32_t full_mask = 0xffffffffu;
+    // The routed group copies the tensor scales of all routed experts before
+    // the PDL wait (static; one bulk copy when their bytes allow it).
+    const bool ts_bulk = !sh_cta && (reinterpret_cast<uintptr_t>(a.ts) % 16 == 0) && ((12 * E) % 16 == 0);
+    const uint32_t rbar_bytes = (uint32_t)(nrr * H * 2) + (ts_bulk ? 12u * (uint32_t)E : 0u);
+    const float* tsall = reinterpret_cast<const float*>(smem + L.tsall);
 
     // Issues chunk i into its ring slot (one thread).
     auto issue = [&](int i) {
@@ -282,7 +337,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     // shared memory land first (bounded; thread 0).
     auto drain = [&](uint64_t budget_ns) {
         if (tid != 0) return;
-        if (nrr > 0) mbar_wait_bounded(&sm.rbar, 0, nullptr, 0, budget_ns);
+        if (rbar_bytes) mbar_wait_bounded(&sm.rbar, 0, nullptr, 0, budget_ns);
         for (int s = 0; s < NS; ++s) {
             const int j = sm.last_issued[s];
             if (j >= 0) mbar_wait_bounded(&sm.full[s], (uint32_t)(j / NS) & 1u, nullptr, 0, budget_ns);
@@ -313,10 +368,9 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         sm.fail = 0;
         sm.n_last = 0;
         sm.n_chunks = sm.n_gu = sm.n_dn = 0;
-        if (nrr > 0) {
-            mbar_arrive_expect_tx(&sm.rbar, (uint32_t)(nrr * H * 2));
-            bulk_g2s(smem + L.rows, a.wr + (size_t)r0 * H, (uint32_t)(nrr * H * 2), &sm.rbar);
-        }
+        if (rbar_bytes) mbar_arrive_expect_tx(&sm.rbar, rbar_bytes);
+        if (nrr > 0) bulk_g2s(smem + L.rows, a.wr + (size_t)r0 * H, (uint32_t)(nrr * H * 2), &sm.rbar);
+        if (ts_bulk) bulk_g2s(smem + L.tsall, a.ts, 12u * (uint32_t)E, &sm.rbar);
         if (sh_cta) {
             // the shared expert: an even split of its pairs and row blocks
             const int p0 = (int)((long long)c * Is / Gs), p1 = (int)((long long)(c + 1) * Is / Gs);
@@ -355,34 +409,40 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         const bool ok = mbar_wait_bounded(&sm.rbar, 0, a.status, kStatusTimeoutLayer, budget);
         if (!ok) sm.fail = 1;
         const uint16_t* wrows = reinterpret_cast<const uint16_t*>(smem + L.rows);
-        // logits from the staged (exact, chunk-scaled f16) x: lane l takes the
-        // 32-value chunks l, l + 32, ...; each chunk's FP32 partial sum is
-        // multiplied back by its power-of-two scale
-        for (int q = warp; ok && q < nrr * T; q += kLW) {
-            const int r = q / T, t = q - r * T;
-            const uint4* xb = xh + (size_t)t * (H / 8) + lane;
-            const float* cb = csc + (size_t)t * (H / 32) + lane;
-            const uint4* wv = reinterpret_cast<const uint4*>(wrows + (size_t)r * H);
-            float v = 0.f;
-            for (int m = 0; m < H / 1024; ++m) {
-                const int ch = lane + 32 * m;
-                float s0 = 0.f, s1 = 0.f;
+        // Logits from the staged (exact, chunk-scaled f16) x, spread over all
+        // warps: an item is (row, token, 256-column slice); lane l takes word
+        // l % 4 (8 values) of the slice's 32-value chunk l / 4, whose FP32
+        // partial sum is multiplied back by the chunk's power-of-two scale. The
+        // slices' sums are added in slice order.
+        float* part = reinterpret_cast<float*>(smem + L.part);
+        const int nsl = H / 256, n_it = nrr * T * nsl;
+        for (int q = warp; ok && q < n_it; q += kLW) {
+            const int rt = q / nsl, sl = q - rt * nsl, r = rt / T, t = rt - r * T;
+            const int cch = 8 * sl + (lane >> 2), wd = lane & 3;  // 32-value chunk, word
+            const uint4 xv = xh[(size_t)t * (H / 8) + (cch >> 5) * 128 + wd * 32 + (cch & 31)];
+            const uint4 wq = reinterpret_cast<const uint4*>(wrows + (size_t)r * H)[4 * cch + wd];
+            const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wq.x, wq.y, wq.z, wq.w};
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint4 xv = xb[(m * 4 + w) * 32], wq = wv[4 * ch + w];
-                    const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xa[i]));
-                        s0 = fmaf(bf16_lo(wa[i]), xf.x, s0);
-                        s1 = fmaf(bf16_hi(wa[i]), xf.y, s1);
-                    }
-                }
-                v = fmaf(cb[32 * m], s0 + s1, v);
+            for (int i = 0; i < 4; ++i) {
+                const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xa[i]));
+                s0 = fmaf(bf16_lo(wa[i]), xf.x, s0);
+                s1 = fmaf(bf16_hi(wa[i]), xf.y, s1);
             }
+            float v = s0 + s1;
+            v += __shfl_xor_sync(full_mask, v, 1);
+            v += __shfl_xor_sync(full_mask, v, 2);
+            v *= csc[(size_t)t * (H / 32) + cch];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(full_mask, v, off);
-            if (lane == 0) a.scores[(size_t)t * E + r0 + r] = sigmoid_score(v, a.bias, r0 + r);
+            for (int off = 4; off < 32; off <<= 1) v += __shfl_xor_sync(full_mask, v, off);
+            if (lane == 0) part[q] = v;
+        }
+        __syncthreads();
+        for (int rt = tid; ok && rt < nrr * T; rt += kLT) {
+            const int r = rt / T, t = rt - r * T;
+            float v = 0.f;
+            for (int sl = 0; sl < nsl; ++sl) v += part[rt * nsl + sl];
+            a.scores[(size_t)t * E + r0 + r] = sigmoid_score(v, a.bias, r0 + r);
         }
         __syncthreads();
         if (tid == 0 && ok && !withhold) release_add_gpu(a.hdr + kHdrScoresIn, (uint32_t)nrr);
@@ -393,9 +453,10 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     FLINT_PHASE(3);
 
     // Routing in this CTA: once all E router rows are published, all T x E
-    // scores into shared memory over the router rows, the top-k of each token
-    // (one warp per token), the routing view. Every thread calls it; false
-    // (in every thread) if the scores never came.
+    // scores into shared memory over the router rows and the top-k of each
+    // token (one warp per token); warp 0 then builds the routing view
+    // (route_view_warp). Every thread calls it; false (in every thread) if
+    // the scores never came.
     auto route = [&](int stamp) -> bool {
         (void)stamp;
         if (!cta_wait_count(a.hdr + kHdrScoresIn, (uint32_t)E, a.status, kStatusTimeoutLayer, budget, &sm.ok) ||
@@ -415,8 +476,6 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         }
         __syncthreads();
         FLINT_PHASE(stamp + 2);
-        build_route_info<true>(ri, sm.ids, T, k, E, nullptr);
-        FLINT_PHASE(stamp + 3);
         return true;
     };
 
@@ -426,12 +485,14 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         if (!route(11)) {
             failed = true;
         } else {
-            const int D = ri.D;
             if (c == G - 1 && tid < T * k) {
                 a.ids[tid] = sm.ids[tid];
                 a.weights[tid] = sm.w[tid];
             }
             if (warp == 0) {
+                route_view_warp(ri, sm.ids, T, k, lane);
+                FLINT_PHASE(14);
+                const int D = ri.D;
                 // cost weight of an expert: 4 + 3 x the tokens that chose it
                 for (int base = 0; base < D; base += 32) {
                     const int u = base + lane;
@@ -445,13 +506,13 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                     if (u < D) sm.cumw[u] = v;
                     __syncwarp();
                 }
-                const int Gr = G - Gs, cr = c - Gs;
-                const long long Wt = sm.cumw[D - 1];
+                const uint32_t Gr = (uint32_t)(G - Gs), cr = (uint32_t)(c - Gs);
+                const uint32_t Wt = (uint32_t)sm.cumw[D - 1];
                 int pos = 0;
                 if (lane < 4) {  // gate/up lo, hi; down lo, hi
                     const int per = lane < 2 ? I : NB;
-                    const long long tot = Wt * per;
-                    const long long tau = (long long)(cr + (lane & 1)) * tot / Gr;
+                    const uint32_t tot = Wt * (uint32_t)per;
+                    const uint32_t tau = (cr + (uint32_t)(lane & 1)) * tot / Gr;
                     pos = cost_pos(tau, sm.cumw, D, per);
                 }
                 const int p0 = __shfl_sync(full_mask, pos, 0), p1 = __shfl_sync(full_mask, pos, 1);
@@ -463,12 +524,18 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 }
                 FLINT_PHASE(19);
             }
-            // the tensor scales of the selected experts (their copies are in flight)
+            __syncthreads();
+            // the tensor scales of the selected experts (copied before the wait,
+            // or read now while the weight copies are in flight)
+            const int D = ri.D;
             if (tid < D) {
-                const float* ts = a.ts + 3 * ri.dlist[tid];
-                sm.tsg[tid] = __ldg(ts);
-                sm.tsu[tid] = __ldg(ts + 1);
-                sm.tsd[tid] = __ldg(ts + 2);
+                bool ok = true;
+                if (ts_bulk && nrr == 0) ok = mbar_wait_bounded(&sm.rbar, 0, a.status, kStatusTimeoutLayer, budget);
+                if (!ok) sm.fail = 1;
+                const int e = ri.dlist[tid];
+                sm.tsg[tid] = ts_bulk ? tsall[3 * e] : __ldg(a.ts + 3 * e);
+                sm.tsu[tid] = ts_bulk ? tsall[3 * e + 1] : __ldg(a.ts + 3 * e + 1);
+                sm.tsd[tid] = ts_bulk ? tsall[3 * e + 2] : __ldg(a.ts + 3 * e + 2);
             }
         }
     } else if (tid == 0 && has_sh) {
@@ -617,13 +684,16 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     for (int i = n_gu; i < n_chunks; ++i) {
         if (!chunk_in(i)) continue;
         const Chunk ch = sm.chunk[i];
-        const int rw0 = 8 * warp;
+        // 8 rows per warp, or 4 when the chunk is small enough that every
+        // warp then has rows
+        const int rpw = ch.count <= 4 * kLW ? 4 : 8;
+        const int rw0 = rpw * warp;
         if (rw0 < ch.count) {
             const uint8_t* slot = ring + (size_t)(i % NS) * a.slot;
             const bool sh = ch.unit == kSharedUnit;
             const int ui = sh ? kShIdx : ch.unit;
             const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[ch.unit];
-            const int nrw = min(8, ch.count - rw0);
+            const int nrw = min(rpw, ch.count - rw0);
             const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
             const uint8_t* rows = slot + (size_t)rw0 * RSu;
             const int row0 = ch.start + rw0;
@@ -643,32 +713,43 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                     a.d_routed[((size_t)t * k + j) * H + row0 + r] = d;
                 }
             };
-            uint32_t rest = tm;
-            while (rest) {
-                const int t0 = __ffs(rest) - 1;
-                rest &= rest - 1u;
-                if (rest) {  // two tokens
-                    const int t1 = __ffs(rest) - 1;
-                    rest &= rest - 1u;
+            // rows [0, nrw) of the warp's RP-row group against one or two tokens
+            auto rows_pass = [&](auto rp_tag, int t0, int t1) {
+                constexpr int RP = decltype(rp_tag)::value;
+                if (t1 >= 0) {
                     const uint4* hv[2];
                     const float* cv[2];
                     vec(t0, hv[0], cv[0]);
                     vec(t1, hv[1], cv[1]);
-                    float acc[16];
-                    down_pass<8, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
-                    const float v = reduce_scatter<16>(acc, lane);
-                    const int idx = rs_index<16>(lane), r = idx & 7;
-                    if ((lane & 1) == 0 && r < nrw) put(v, r, (idx >> 3) ? t1 : t0);
+                    float acc[2 * RP];
+                    down_pass<RP, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                    const float v = reduce_scatter<2 * RP>(acc, lane);
+                    const int idx = rs_index<2 * RP>(lane), r = idx % RP;
+                    if (lane % (16 / RP) == 0 && r < nrw) put(v, r, idx >= RP ? t1 : t0);
                 } else {
                     const uint4* hv[1];
                     const float* cv[1];
                     vec(t0, hv[0], cv[0]);
-                    float acc[8];
-                    down_pass<8, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
-                    const float v = reduce_scatter<8>(acc, lane);
-                    const int r = rs_index<8>(lane);
-                    if ((lane & 3) == 0 && r < nrw) put(v, r, t0);
+                    float acc[RP];
+                    down_pass<RP, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                    const float v = reduce_scatter<RP>(acc, lane);
+                    const int r = rs_index<RP>(lane);
+                    if (lane % (32 / RP) == 0 && r < nrw) put(v, r, t0);
                 }
+            };
+            uint32_t rest = tm;
+            while (rest) {
+                const int t0 = __ffs(rest) - 1;
+                rest &= rest - 1u;
+                int t1 = -1;
+                if (rest) {
+                    t1 = __ffs(rest) - 1;
+                    rest &= rest - 1u;
+                }
+                if (rpw == 4)
+                    rows_pass(std::integral_constant<int, 4>(), t0, t1);
+                else
+                    rows_pass(std::integral_constant<int, 8>(), t0, t1);
             }
         }
         chunk_done(i);
@@ -679,6 +760,8 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     if (!__syncthreads_or(failed || wfail || sm.fail) && sh_cta) {
         // the shared group learns the routing now (weights, number of experts)
         failed = !route(15);
+        if (!failed && warp == 0) route_view_warp(ri, sm.ids, T, k, lane);
+        FLINT_PHASE(18);
     }
     if (__syncthreads_or(failed || wfail || sm.fail)) {
         drain(budget);
@@ -693,17 +776,44 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     }
     __syncthreads();
     FLINT_PHASE(9);
+    // the blocks this CTA completed: one thread per 8 rows of one token, the
+    // k + 1 expert outputs read as 16-byte words, summed in rank order
     const int n_last = sm.n_last;
-    for (int e = tid; e < n_last * T * kRowBlock; e += kLT) {
-        const int qb = e / (T * kRowBlock), rem = e - qb * (T * kRowBlock);
-        const int t = rem / kRowBlock, r = sm.last[qb] * kRowBlock + (rem - t * kRowBlock);
-        float acc = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const float d = __uint_as_float((uint32_t)__ldcg(a.d_routed + ((size_t)t * k + j) * H + r) << 16);
-            acc = fmaf(sm.w[t * k + j], d, acc);
+    for (int e = tid; e < n_last * T * (kRowBlock / 8); e += kLT) {
+        const int qb = e / (T * (kRowBlock / 8)), rem = e - qb * (T * (kRowBlock / 8));
+        const int t = rem / (kRowBlock / 8), r = sm.last[qb] * kRowBlock + 8 * (rem - t * (kRowBlock / 8));
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        auto add = [&](float wj, const uint4 dj) {
+            const uint32_t dw[4] = {dj.x, dj.y, dj.z, dj.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(wj, bf16_lo(dw[i]), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wj, bf16_hi(dw[i]), acc[2 * i + 1]);
+            }
+        };
+        const uint4* dr = reinterpret_cast<const uint4*>(a.d_routed + (size_t)t * k * H + r);
+        for (int j = 0; j < k; j += 2) {  // two loads in flight
+            const uint4 d0 = __ldcg(dr + (size_t)j * (H / 8));
+            const uint4 d1 = j + 1 < k ? __ldcg(dr + (size_t)(j + 1) * (H / 8)) : make_uint4(0u, 0u, 0u, 0u);
+            add(sm.w[t * k + j], d0);
+            if (j + 1 < k) add(sm.w[t * k + j + 1], d1);
         }
-        if (has_sh) acc += __uint_as_float((uint32_t)__ldcg(a.d_shared + (size_t)t * H + r) << 16);
-        a.y[(size_t)t * H + r] = f32_to_bf16_bits(acc);
+        if (has_sh) {
+            const uint4 ds = __ldcg(reinterpret_cast<const uint4*>(a.d_shared + (size_t)t * H + r));
+            const uint32_t dw[4] = {ds.x, ds.y, ds.z, ds.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += bf16_lo(dw[i]);
+                acc[2 * i + 1] += bf16_hi(dw[i]);
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = (uint32_t)f32_to_bf16_bits(acc[2 * i]) | ((uint32_t)f32_to_bf16_bits(acc[2 * i + 1]) << 16);
+        *reinterpret_cast<uint4*>(a.y + (size_t)t * H + r) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     for (int q = tid; q < n_last; q += kLT) a.counters[sm.last[q]] = 0;
     __syncthreads();
