@@ -86,15 +86,7 @@ struct Chunk {
     int32_t start, count;
 };
 
-// What the one-thread copy issuer needs (set once per call by thread 0).
-struct RingCfg {
-    uint8_t* ring;
-    const uint8_t *gu, *down, *s_gu, *s_down;
-    int slot, ns, I, Is, H, RS, RSr, RSs;
-};
-
 struct LayerSmall {
-    RingCfg cfg;
     uint64_t full[kLayerMaxSlots];   // ring slot s holds its chunk's bytes
     uint64_t rbar;                   // the router rows are in
     uint32_t rel[kLayerMaxSlots];    // warps done with the slot's current chunk
@@ -124,11 +116,11 @@ struct LayerSmall {
 };
 
 // Shared memory: small arrays, the routing view, the tensor scales of all
-// routed experts, the staging region (x, then
+// routed experts, the router logits' partial sums, the staging region (x, then
 // h of the CTA's down experts) and its chunk scales, the norm's partial sums,
 // the router rows (later: all sigmoid scores for the top-k), the ring.
 struct LayerSmem {
-    size_t small, ri, tsall, xs, csc, nred, rows, ring, total;
+    size_t small, ri, tsall, part, xs, csc, nred, rows, ring, total;
 };
 
 __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
@@ -137,7 +129,8 @@ __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     L.small = 0;
     L.ri = align_up(sizeof(LayerSmall), 128);
     L.tsall = align_up(L.ri + sizeof(RouteInfo), 128);
-    L.xs = align_up(L.tsall + 12 * (size_t)a.E, 128);
+    L.part = align_up(L.tsall + 12 * (size_t)a.E, 128);
+    L.xs = align_up(L.part + sizeof(float) * (size_t)a.rpc * T * (H / 256), 128);
     L.csc = align_up(L.xs + (size_t)a.stage_vals, 128);
     L.nred = align_up(L.csc + (size_t)a.stage_scales, 128);
     L.rows = align_up(L.nred + (a.norm.r ? sizeof(float) * T * (H / 32) : 0), 128);
@@ -189,7 +182,7 @@ __device__ __forceinline__ bool cta_wait_count(const uint32_t* p, uint32_t targe
 // per expert which ranks of which tokens chose it) built by one warp from the
 // T x k ids in shared memory (every id valid, distinct within a token, E <=
 // 1024): lane l owns the bitmap word of experts 32 l .. 32 l + 31.
-__device__ __noinline__ void route_view_warp(RouteInfo& ri, const int32_t* ids, int T, int k, int lane) {
+__device__ void route_view_warp(RouteInfo& ri, const int32_t* ids, int T, int k, int lane) {
     const uint32_t full = 0xffffffffu;
     const int n = T * k;
     uint32_t word = 0;
@@ -250,14 +243,12 @@ __device__ __forceinline__ int cost_pos(uint32_t tau, const int32_t* cum, int D,
     return lo * per + (int)(p < (uint32_t)per ? p : (uint32_t)per);
 }
 
-// The chunks of the pair range [p0, p1) and the down block range [b0, b1)
-// (items of a concatenation of experts of per_gu pairs / NB blocks: the
-// routed experts in list order, or the shared expert alone); a down chunk
-// takes at most rows_chunk rows. One thread. (The one-time steps of a call
-// are separate functions, each in the code once: the kernel's size was
-// costing instruction-fetch stalls on every step run once per call.)
-__device__ __noinline__ void build_chunks(LayerSmall& sm, int p0, int p1, int per_gu, int b0, int b1, int NB,
-                                          uint32_t* status, bool shared, int rows_chunk) {
+// Appends the chunks of the pair range [p0, p1) and the down block range
+// [b0, b1) (items of a concatenation of experts of per_gu pairs / NB blocks;
+// unit_of(i) maps an item's expert position to its unit id). One thread.
+template <typename UnitOf, typename RowsOf>
+__device__ void build_chunks(LayerSmall& sm, int p0, int p1, int per_gu, int b0, int b1, int NB, uint32_t* status,
+                             UnitOf unit_of, RowsOf rows_per_chunk) {
     int n = 0;
     for (int P = p0; P < p1;) {
         if (n == kMaxChunks) {
@@ -267,16 +258,15 @@ __device__ __noinline__ void build_chunks(LayerSmall& sm, int p0, int p1, int pe
         }
         const int u = P / per_gu, p = P - u * per_gu;
         const int m = min(kLW, min(p1 - P, per_gu - p));
-        sm.chunk[n++] = Chunk{kChunkGateUp, 0, (int16_t)(shared ? kSharedUnit : u), p, m};
+        sm.chunk[n++] = Chunk{kChunkGateUp, 0, (int16_t)unit_of(u), p, m};
         P += m;
     }
     sm.n_gu = n;
     int nd = 0;
-    const int blocks_chunk = max(1, rows_chunk / kRowBlock);
     for (int B = b0; B < b1;) {
         const int u = B / NB, b = B - u * NB;
-        const int unit = shared ? kSharedUnit : u;
-        const int take = min(b1 - B, min(NB - b, blocks_chunk));
+        const int unit = unit_of(u);
+        const int take = min(b1 - B, min(NB - b, max(1, rows_per_chunk(unit) / kRowBlock)));
         if (n == kMaxChunks || (nd == kMaxDownUnits && sm.dn_unit[nd - 1] != unit)) {
             sm.fail = 1;  // the host sizes the grid so that this cannot happen
             atomicOr(status, kStatusLayerPlan);
@@ -290,209 +280,6 @@ __device__ __noinline__ void build_chunks(LayerSmall& sm, int p0, int p1, int pe
     sm.n_dn = nd;
     sm.b0 = b0;
     sm.b1 = b1;
-}
-
-// Issues chunk i into its ring slot (one thread).
-__device__ __noinline__ void issue_chunk(LayerSmall& sm, const RouteInfo& ri, int i) {
-    if (i >= sm.n_chunks) return;
-    const RingCfg& g = sm.cfg;
-    const Chunk ch = sm.chunk[i];
-    const int s = i % g.ns;
-    uint8_t* slot = g.ring + (size_t)s * g.slot;
-    const bool sh = ch.unit == kSharedUnit;
-    fence_proxy_async_smem();  // the slot's earlier generic reads come first
-    if (ch.kind == kChunkGateUp) {
-        const uint8_t* base = sh ? g.s_gu : g.gu + (size_t)ri.dlist[ch.unit] * 2 * g.I * g.RS;
-        const uint32_t bytes = (uint32_t)ch.count * g.RS;
-        mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
-        bulk_g2s(slot, base + (size_t)ch.start * g.RS, bytes, &sm.full[s]);
-        bulk_g2s(slot + (size_t)kLW * g.RS, base + (size_t)((sh ? g.Is : g.I) + ch.start) * g.RS, bytes, &sm.full[s]);
-    } else {
-        const int RSu = sh ? g.RSs : g.RSr;
-        const uint8_t* base = sh ? g.s_down : g.down + (size_t)ri.dlist[ch.unit] * g.H * g.RSr;
-        const uint32_t bytes = (uint32_t)ch.count * RSu;
-        mbar_arrive_expect_tx(&sm.full[s], bytes);
-        bulk_g2s(slot, base + (size_t)ch.start * RSu, bytes, &sm.full[s]);
-    }
-    sm.last_issued[s] = i;
-}
-
-// Routing in a CTA: once all E router rows are published, all T x E scores
-// into shared memory (sc, over the dead router rows) and the top-k of each
-// token (one warp per token) into sm.ids / sm.w. Every thread calls it; false
-// (in every thread) if the scores never came. Stamps stamp .. stamp + 2.
-__device__ __noinline__ bool route_topk(LayerSmall& sm, const uint32_t* counter, const uint32_t* scores, int T,
-                                        int E, int k, uint32_t* status, uint64_t budget, uint32_t* sc, int stamp) {
-    (void)stamp;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (!cta_wait_count(counter, (uint32_t)E, status, kStatusTimeoutLayer, budget, &sm.ok) || sm.fail) return false;
-    FLINT_PHASE(stamp);
-    for (int i = tid; i < T * E; i += kLT) sc[i] = (uint32_t)ld_cg(reinterpret_cast<const int32_t*>(scores) + i);
-    __syncthreads();
-    FLINT_PHASE(stamp + 1);
-    if (warp < T) {
-        if (E <= 256)
-            topk_warp<8>(sc + (size_t)warp * E, E, k, lane, sm.ids + warp * k, sm.w + warp * k);
-        else
-            topk_warp<FLINT_MAX_EXPERTS / 32>(sc + (size_t)warp * E, E, k, lane, sm.ids + warp * k, sm.w + warp * k);
-    }
-    __syncthreads();
-    FLINT_PHASE(stamp + 2);
-    return true;
-}
-
-// Warp 0 of a routed CTA: its cost-balanced ranges of the selected experts'
-// gate/up pairs and down row blocks (cost weight of an expert: 4 + 3 x the
-// tokens that chose it), its chunk list, its first NS ring copies.
-__device__ __noinline__ void plan_routed(LayerSmall& sm, const RouteInfo& ri, int G, int Gs, int c, int I, int NB,
-                                         uint32_t* status, int rows_chunk) {
-    const uint32_t full = 0xffffffffu;
-    const int lane = threadIdx.x & 31;
-    const int D = ri.D;
-    for (int base = 0; base < D; base += 32) {
-        const int u = base + lane;
-        int v = u < D ? 4 + 3 * __popc(ri.tmask[u]) : 0;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int n = __shfl_up_sync(full, v, off);
-            if (lane >= off) v += n;
-        }
-        if (base) v += sm.cumw[base - 1];
-        if (u < D) sm.cumw[u] = v;
-        __syncwarp();
-    }
-    const uint32_t Gr = (uint32_t)(G - Gs), cr = (uint32_t)(c - Gs);
-    const uint32_t Wt = (uint32_t)sm.cumw[D - 1];
-    int pos = 0;
-    if (lane < 4) {  // gate/up lo, hi; down lo, hi
-        const int per = lane < 2 ? I : NB;
-        const uint32_t tot = Wt * (uint32_t)per;
-        const uint32_t tau = (cr + (uint32_t)(lane & 1)) * tot / Gr;
-        pos = cost_pos(tau, sm.cumw, D, per);
-    }
-    const int p0 = __shfl_sync(full, pos, 0), p1 = __shfl_sync(full, pos, 1);
-    const int b0 = __shfl_sync(full, pos, 2), b1 = __shfl_sync(full, pos, 3);
-    if (lane == 0) {
-        build_chunks(sm, p0, p1, I, b0, b1, NB, status, false, rows_chunk);
-        if (!sm.fail)
-            for (int i = 0; i < sm.cfg.ns; ++i) issue_chunk(sm, ri, i);
-    }
-    __syncwarp();
-}
-
-// The h of this CTA's down experts, staged once every pair of each is
-// published: per (expert, token) one vector of K values as chunk-scaled f16
-// in DOWN order at xs + v_off, its chunk scales at csc + v_coff. Every thread
-// calls it; false (in every thread) on a timed-out wait or a failed plan.
-__device__ __noinline__ bool stage_down_h(LayerSmall& sm, const RouteInfo& ri, int T, int k, int I, int Is,
-                                          const uint16_t* h_routed, const uint16_t* h_shared,
-                                          const uint32_t* unit_counters, uint32_t* status, uint64_t budget,
-                                          uint8_t* xs, uint8_t* csc, int stage_vals, int stage_scales) {
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        int nv = 0, item = 0, off = 0, coff = 0;
-        for (int q = 0; q < sm.n_dn; ++q) {
-            const int unit = sm.dn_unit[q];
-            const int K = unit == kSharedUnit ? Is : I;
-            const uint32_t tm = unit == kSharedUnit ? (1u << T) - 1u : ri.tmask[unit];
-            for (int t = 0; t < FLINT_MAX_TOKENS; ++t) {
-                sm.vec[q][t] = -1;
-                if (t < T && ((tm >> t) & 1u)) {
-                    sm.vec[q][t] = (int16_t)nv;
-                    sm.v_item0[nv] = item;
-                    sm.v_off[nv] = off;
-                    sm.v_coff[nv] = coff;
-                    sm.v_q[nv] = (int16_t)q;
-                    sm.v_t[nv] = (int16_t)t;
-                    item += K / 32;
-                    off += 2 * K;
-                    coff += 4 * (K / 32);
-                    ++nv;
-                }
-            }
-        }
-        if (off > stage_vals || coff > stage_scales) {  // the host plans for this not to happen
-            atomicOr(status, kStatusLayerPlan);
-            sm.fail = 1;
-            nv = 0;
-            item = 0;
-        }
-        sm.n_vec = nv;
-        sm.v_item0[nv] = item;
-    }
-    bool ok = true;
-    for (int q = 0; q < sm.n_dn && ok; ++q) {  // sm.n_dn: written before the earlier barriers
-        const int unit = sm.dn_unit[q];
-        ok = cta_wait_count(unit_counters + (unit == kSharedUnit ? kShIdx : unit),
-                            (uint32_t)(unit == kSharedUnit ? Is : I), status, kStatusTimeoutLayer, budget, &sm.ok);
-    }
-    ok = ok && !sm.fail;
-    const int n_items = ok ? sm.v_item0[sm.n_vec] : 0;
-    for (int it = tid; it < n_items; it += kLT) {
-        int v = 0;
-        while (sm.v_item0[v + 1] <= it) ++v;
-        const int cc = it - sm.v_item0[v], t = sm.v_t[v];
-        const int unit = sm.dn_unit[sm.v_q[v]];
-        const bool sh = unit == kSharedUnit;
-        const int K = sh ? Is : I;
-        const uint16_t* src;
-        if (sh) {
-            src = h_shared + (size_t)t * Is;
-        } else {
-            const int j = __ffs(rank_bits(ri.dmask[unit], t)) - 1;
-            src = h_routed + ((size_t)t * k + j) * I;
-        }
-        const StageSrc ss = {src, reinterpret_cast<uint4*>(xs + sm.v_off[v]), reinterpret_cast<float*>(csc + sm.v_coff[v]),
-                             1, K};
-        uint4 w4[4];
-        stage_load(ss, 0, cc, w4);
-        stage_store<true>(ss, 0, cc, w4);
-    }
-    return __syncthreads_and(ok) != 0;
-}
-
-// The row blocks this CTA completed (sm.last): y = bf16(sum_j w_j d_j +
-// d_shared) in rank order, one thread per 8 rows of one token, the k + 1
-// expert outputs read as 16-byte words (two in flight).
-__device__ __noinline__ void combine_blocks(const LayerSmall& sm, int T, int k, int H, const uint16_t* d_routed,
-                                            const uint16_t* d_shared, uint16_t* y) {
-    const int n_last = sm.n_last;
-    for (int e = threadIdx.x; e < n_last * T * (kRowBlock / 8); e += kLT) {
-        const int qb = e / (T * (kRowBlock / 8)), rem = e - qb * (T * (kRowBlock / 8));
-        const int t = rem / (kRowBlock / 8), r = sm.last[qb] * kRowBlock + 8 * (rem - t * (kRowBlock / 8));
-        float acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        auto add = [&](float wj, const uint4 dj) {
-            const uint32_t dw[4] = {dj.x, dj.y, dj.z, dj.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = fmaf(wj, bf16_lo(dw[i]), acc[2 * i]);
-                acc[2 * i + 1] = fmaf(wj, bf16_hi(dw[i]), acc[2 * i + 1]);
-            }
-        };
-        const uint4* dr = reinterpret_cast<const uint4*>(d_routed + (size_t)t * k * H + r);
-        for (int j = 0; j < k; j += 2) {
-            const uint4 d0 = __ldcg(dr + (size_t)j * (H / 8));
-            const uint4 d1 = j + 1 < k ? __ldcg(dr + (size_t)(j + 1) * (H / 8)) : make_uint4(0u, 0u, 0u, 0u);
-            add(sm.w[t * k + j], d0);
-            if (j + 1 < k) add(sm.w[t * k + j + 1], d1);
-        }
-        if (d_shared) {
-            const uint4 ds = __ldcg(reinterpret_cast<const uint4*>(d_shared + (size_t)t * H + r));
-            const uint32_t dw[4] = {ds.x, ds.y, ds.z, ds.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] += bf16_lo(dw[i]);
-                acc[2 * i + 1] += bf16_hi(dw[i]);
-            }
-        }
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            o[i] = (uint32_t)f32_to_bf16_bits(acc[2 * i]) | ((uint32_t)f32_to_bf16_bits(acc[2 * i + 1]) << 16);
-        *reinterpret_cast<uint4*>(y + (size_t)t * H + r) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
 }
 
 // NORM: the input is rmsnorm(r + y_prev) of the residual stream (a.norm), not
@@ -523,6 +310,29 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     const uint32_t rbar_bytes = (uint32_t)(nrr * H * 2) + (ts_bulk ? 12u * (uint32_t)E : 0u);
     const float* tsall = reinterpret_cast<const float*>(smem + L.tsall);
 
+    // Issues chunk i into its ring slot (one thread).
+    auto issue = [&](int i) {
+        if (i >= sm.n_chunks) return;
+        const Chunk ch = sm.chunk[i];
+        const int s = i % NS;
+        uint8_t* slot = ring + (size_t)s * a.slot;
+        const bool sh = ch.unit == kSharedUnit;
+        fence_proxy_async_smem();  // the slot's earlier generic reads come first
+        if (ch.kind == kChunkGateUp) {
+            const uint8_t* base = sh ? a.s_gu : a.gu + (size_t)ri.dlist[ch.unit] * 2 * I * RS;
+            const uint32_t bytes = (uint32_t)ch.count * RS;
+            mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
+            bulk_g2s(slot, base + (size_t)ch.start * RS, bytes, &sm.full[s]);
+            bulk_g2s(slot + (size_t)kLW * RS, base + (size_t)((sh ? Is : I) + ch.start) * RS, bytes, &sm.full[s]);
+        } else {
+            const int RSu = sh ? RSs : RSr;
+            const uint8_t* base = sh ? a.s_down : a.down + (size_t)ri.dlist[ch.unit] * H * RSr;
+            const uint32_t bytes = (uint32_t)ch.count * RSu;
+            mbar_arrive_expect_tx(&sm.full[s], bytes);
+            bulk_g2s(slot, base + (size_t)ch.start * RSu, bytes, &sm.full[s]);
+        }
+        sm.last_issued[s] = i;
+    };
     // Before an early exit: the bulk copies still in flight into this CTA's
     // shared memory land first (bounded; thread 0).
     auto drain = [&](uint64_t budget_ns) {
@@ -533,7 +343,10 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             if (j >= 0) mbar_wait_bounded(&sm.full[s], (uint32_t)(j / NS) & 1u, nullptr, 0, budget_ns);
         }
     };
-    const int rows_chunk_r = min(8 * kLW, a.slot / RSr), rows_chunk_s = RSs ? min(8 * kLW, a.slot / RSs) : 0;
+    auto rows_per_chunk = [&](int unit) {
+        const int RSu = unit == kSharedUnit ? RSs : RSr;
+        return min(8 * kLW, a.slot / RSu);
+    };
 
     // ---- 0: before the PDL wait: barriers, static weight copies ----------------------
 #ifdef FLINT_PHASE_TRACE
@@ -555,7 +368,6 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         sm.fail = 0;
         sm.n_last = 0;
         sm.n_chunks = sm.n_gu = sm.n_dn = 0;
-        sm.cfg = RingCfg{ring, a.gu, a.down, a.s_gu, a.s_down, a.slot, NS, I, Is, H, RS, RSr, RSs};
         if (rbar_bytes) mbar_arrive_expect_tx(&sm.rbar, rbar_bytes);
         if (nrr > 0) bulk_g2s(smem + L.rows, a.wr + (size_t)r0 * H, (uint32_t)(nrr * H * 2), &sm.rbar);
         if (ts_bulk) bulk_g2s(smem + L.tsall, a.ts, 12u * (uint32_t)E, &sm.rbar);
@@ -563,8 +375,8 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             // the shared expert: an even split of its pairs and row blocks
             const int p0 = (int)((long long)c * Is / Gs), p1 = (int)((long long)(c + 1) * Is / Gs);
             const int b0 = (int)((long long)c * NB / Gs), b1 = (int)((long long)(c + 1) * NB / Gs);
-            build_chunks(sm, p0, p1, Is, b0, b1, NB, a.status, true, rows_chunk_s);
-            for (int i = 0; i < NS; ++i) issue_chunk(sm, ri, i);
+            build_chunks(sm, p0, p1, Is, b0, b1, NB, a.status, [](int) { return kSharedUnit; }, rows_per_chunk);
+            for (int i = 0; i < NS; ++i) issue(i);
         }
     }
     // Dependents may launch now: their CTAs take SMs as ours exit, and only
@@ -597,34 +409,40 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         const bool ok = mbar_wait_bounded(&sm.rbar, 0, a.status, kStatusTimeoutLayer, budget);
         if (!ok) sm.fail = 1;
         const uint16_t* wrows = reinterpret_cast<const uint16_t*>(smem + L.rows);
-        // logits from the staged (exact, chunk-scaled f16) x, one warp per
-        // (row, token): lane l takes the 32-value chunks l, l + 32, ...; each
-        // chunk's FP32 partial sum is multiplied back by its power-of-two scale
-        for (int q = warp; ok && q < nrr * T; q += kLW) {
-            const int r = q / T, t = q - r * T;
-            const uint4* xb = xh + (size_t)t * (H / 8) + lane;
-            const float* cb = csc + (size_t)t * (H / 32) + lane;
-            const uint4* wv = reinterpret_cast<const uint4*>(wrows + (size_t)r * H);
-            float v = 0.f;
-            for (int m = 0; m < H / 1024; ++m) {
-                const int ch = lane + 32 * m;
-                float s0 = 0.f, s1 = 0.f;
+        // Logits from the staged (exact, chunk-scaled f16) x, spread over all
+        // warps: an item is (row, token, 256-column slice); lane l takes word
+        // l % 4 (8 values) of the slice's 32-value chunk l / 4, whose FP32
+        // partial sum is multiplied back by the chunk's power-of-two scale. The
+        // slices' sums are added in slice order.
+        float* part = reinterpret_cast<float*>(smem + L.part);
+        const int nsl = H / 256, n_it = nrr * T * nsl;
+        for (int q = warp; ok && q < n_it; q += kLW) {
+            const int rt = q / nsl, sl = q - rt * nsl, r = rt / T, t = rt - r * T;
+            const int cch = 8 * sl + (lane >> 2), wd = lane & 3;  // 32-value chunk, word
+            const uint4 xv = xh[(size_t)t * (H / 8) + (cch >> 5) * 128 + wd * 32 + (cch & 31)];
+            const uint4 wq = reinterpret_cast<const uint4*>(wrows + (size_t)r * H)[4 * cch + wd];
+            const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wq.x, wq.y, wq.z, wq.w};
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint4 xv = xb[(m * 4 + w) * 32], wq = wv[4 * ch + w];
-                    const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xa[i]));
-                        s0 = fmaf(bf16_lo(wa[i]), xf.x, s0);
-                        s1 = fmaf(bf16_hi(wa[i]), xf.y, s1);
-                    }
-                }
-                v = fmaf(cb[32 * m], s0 + s1, v);
+            for (int i = 0; i < 4; ++i) {
+                const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xa[i]));
+                s0 = fmaf(bf16_lo(wa[i]), xf.x, s0);
+                s1 = fmaf(bf16_hi(wa[i]), xf.y, s1);
             }
+            float v = s0 + s1;
+            v += __shfl_xor_sync(full_mask, v, 1);
+            v += __shfl_xor_sync(full_mask, v, 2);
+            v *= csc[(size_t)t * (H / 32) + cch];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(full_mask, v, off);
-            if (lane == 0) a.scores[(size_t)t * E + r0 + r] = sigmoid_score(v, a.bias, r0 + r);
+            for (int off = 4; off < 32; off <<= 1) v += __shfl_xor_sync(full_mask, v, off);
+            if (lane == 0) part[q] = v;
+        }
+        __syncthreads();
+        for (int rt = tid; ok && rt < nrr * T; rt += kLT) {
+            const int r = rt / T, t = rt - r * T;
+            float v = 0.f;
+            for (int sl = 0; sl < nsl; ++sl) v += part[rt * nsl + sl];
+            a.scores[(size_t)t * E + r0 + r] = sigmoid_score(v, a.bias, r0 + r);
         }
         __syncthreads();
         if (tid == 0 && ok && !withhold) release_add_gpu(a.hdr + kHdrScoresIn, (uint32_t)nrr);
@@ -634,11 +452,37 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     }
     FLINT_PHASE(3);
 
+    // Routing in this CTA: once all E router rows are published, all T x E
+    // scores into shared memory over the router rows and the top-k of each
+    // token (one warp per token); warp 0 then builds the routing view
+    // (route_view_warp). Every thread calls it; false (in every thread) if
+    // the scores never came.
+    auto route = [&](int stamp) -> bool {
+        (void)stamp;
+        if (!cta_wait_count(a.hdr + kHdrScoresIn, (uint32_t)E, a.status, kStatusTimeoutLayer, budget, &sm.ok) ||
+            sm.fail)
+            return false;
+        FLINT_PHASE(stamp);
+        uint32_t* sc = reinterpret_cast<uint32_t*>(smem + L.rows);  // the router rows are dead
+        for (int i = tid; i < T * E; i += kLT) sc[i] = (uint32_t)ld_cg(reinterpret_cast<const int32_t*>(a.scores) + i);
+        __syncthreads();
+        FLINT_PHASE(stamp + 1);
+        if (warp < T) {
+            if (E <= 256)
+                topk_warp<8>(sc + (size_t)warp * E, E, k, lane, sm.ids + warp * k, sm.w + warp * k);
+            else
+                topk_warp<FLINT_MAX_EXPERTS / 32>(sc + (size_t)warp * E, E, k, lane, sm.ids + warp * k,
+                                                  sm.w + warp * k);
+        }
+        __syncthreads();
+        FLINT_PHASE(stamp + 2);
+        return true;
+    };
+
     bool failed = false;
     if (!sh_cta) {
         // ---- 2: routing, this CTA's share of the selected experts ---------------
-        uint32_t* sc = reinterpret_cast<uint32_t*>(smem + L.rows);  // the router rows are dead
-        if (!route_topk(sm, a.hdr + kHdrScoresIn, a.scores, T, E, k, a.status, budget, sc, 11)) {
+        if (!route(11)) {
             failed = true;
         } else {
             if (c == G - 1 && tid < T * k) {
@@ -648,7 +492,36 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             if (warp == 0) {
                 route_view_warp(ri, sm.ids, T, k, lane);
                 FLINT_PHASE(14);
-                plan_routed(sm, ri, G, Gs, c, I, NB, a.status, rows_chunk_r);
+                const int D = ri.D;
+                // cost weight of an expert: 4 + 3 x the tokens that chose it
+                for (int base = 0; base < D; base += 32) {
+                    const int u = base + lane;
+                    int v = u < D ? 4 + 3 * __popc(ri.tmask[u]) : 0;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const int n = __shfl_up_sync(full_mask, v, off);
+                        if (lane >= off) v += n;
+                    }
+                    if (base) v += sm.cumw[base - 1];
+                    if (u < D) sm.cumw[u] = v;
+                    __syncwarp();
+                }
+                const uint32_t Gr = (uint32_t)(G - Gs), cr = (uint32_t)(c - Gs);
+                const uint32_t Wt = (uint32_t)sm.cumw[D - 1];
+                int pos = 0;
+                if (lane < 4) {  // gate/up lo, hi; down lo, hi
+                    const int per = lane < 2 ? I : NB;
+                    const uint32_t tot = Wt * (uint32_t)per;
+                    const uint32_t tau = (cr + (uint32_t)(lane & 1)) * tot / Gr;
+                    pos = cost_pos(tau, sm.cumw, D, per);
+                }
+                const int p0 = __shfl_sync(full_mask, pos, 0), p1 = __shfl_sync(full_mask, pos, 1);
+                const int b0 = __shfl_sync(full_mask, pos, 2), b1 = __shfl_sync(full_mask, pos, 3);
+                if (lane == 0) {
+                    build_chunks(sm, p0, p1, I, b0, b1, NB, a.status, [](int u) { return u; }, rows_per_chunk);
+                    if (!sm.fail)
+                        for (int i = 0; i < NS; ++i) issue(i);
+                }
                 FLINT_PHASE(19);
             }
             __syncthreads();
@@ -694,7 +567,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             const int s = i % NS;
             if (atom_add_acq_rel_cta_smem(&sm.rel[s], 1u) == kLW - 1) {
                 sm.rel[s] = 0;
-                if (!sm.fail) issue_chunk(sm, ri, i + NS);
+                if (!sm.fail) issue(i + NS);
             }
         }
     };
@@ -743,9 +616,70 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         }
     }
     FLINT_PHASE(6);
-    if (n_chunks > n_gu && !stage_down_h(sm, ri, T, k, I, Is, a.h_routed, a.h_shared, a.unit_counters, a.status,
-                                         budget, smem + L.xs, smem + L.csc, a.stage_vals, a.stage_scales))
-        wfail = true;
+    if (n_chunks > n_gu) {
+        // Stage h of this CTA's down experts once every pair of each is published.
+        if (tid == 0) {
+            int nv = 0, item = 0, off = 0, coff = 0;
+            for (int q = 0; q < sm.n_dn; ++q) {
+                const int unit = sm.dn_unit[q];
+                const int K = unit == kSharedUnit ? Is : I;
+                const uint32_t tm = unit == kSharedUnit ? (1u << T) - 1u : ri.tmask[unit];
+                for (int t = 0; t < FLINT_MAX_TOKENS; ++t) {
+                    sm.vec[q][t] = -1;
+                    if (t < T && ((tm >> t) & 1u)) {
+                        sm.vec[q][t] = (int16_t)nv;
+                        sm.v_item0[nv] = item;
+                        sm.v_off[nv] = off;
+                        sm.v_coff[nv] = coff;
+                        sm.v_q[nv] = (int16_t)q;
+                        sm.v_t[nv] = (int16_t)t;
+                        item += K / 32;
+                        off += 2 * K;
+                        coff += 4 * (K / 32);
+                        ++nv;
+                    }
+                }
+            }
+            if (off > a.stage_vals || coff > a.stage_scales) {  // the host plans for this not to happen
+                atomicOr(a.status, kStatusLayerPlan);
+                sm.fail = 1;
+                nv = 0;
+                item = 0;
+            }
+            sm.n_vec = nv;
+            sm.v_item0[nv] = item;
+        }
+        bool ok = true;
+        for (int q = 0; q < sm.n_dn && ok; ++q) {  // sm.n_dn: written before the earlier barriers
+            const int unit = sm.dn_unit[q];
+            ok = cta_wait_count(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit),
+                                (uint32_t)(unit == kSharedUnit ? Is : I), a.status, kStatusTimeoutLayer, budget,
+                                &sm.ok);
+        }
+        ok = ok && !sm.fail;
+        const int n_items = ok ? sm.v_item0[sm.n_vec] : 0;
+        for (int it = tid; it < n_items; it += kLT) {
+            int v = 0;
+            while (sm.v_item0[v + 1] <= it) ++v;
+            const int cc = it - sm.v_item0[v], t = sm.v_t[v];
+            const int unit = sm.dn_unit[sm.v_q[v]];
+            const bool sh = unit == kSharedUnit;
+            const int K = sh ? Is : I;
+            const uint16_t* src;
+            if (sh) {
+                src = a.h_shared + (size_t)t * Is;
+            } else {
+                const int j = __ffs(rank_bits(ri.dmask[unit], t)) - 1;
+                src = a.h_routed + ((size_t)t * k + j) * I;
+            }
+            const StageSrc ss = {src, reinterpret_cast<uint4*>(smem + L.xs + sm.v_off[v]),
+                                 reinterpret_cast<float*>(smem + L.csc + sm.v_coff[v]), 1, K};
+            uint4 w4[4];
+            stage_load(ss, 0, cc, w4);
+            stage_store<true>(ss, 0, cc, w4);
+        }
+        if (!__syncthreads_and(ok)) wfail = true;
+    }
     FLINT_PHASE(7);
     for (int i = n_gu; i < n_chunks; ++i) {
         if (!chunk_in(i)) continue;
@@ -825,8 +759,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     FLINT_PHASE(8);
     if (!__syncthreads_or(failed || wfail || sm.fail) && sh_cta) {
         // the shared group learns the routing now (weights, number of experts)
-        failed = !route_topk(sm, a.hdr + kHdrScoresIn, a.scores, T, E, k, a.status, budget,
-                             reinterpret_cast<uint32_t*>(smem + L.rows), 15);
+        failed = !route(15);
         if (!failed && warp == 0) route_view_warp(ri, sm.ids, T, k, lane);
         FLINT_PHASE(18);
     }
@@ -843,8 +776,45 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     }
     __syncthreads();
     FLINT_PHASE(9);
-    combine_blocks(sm, T, k, H, a.d_routed, has_sh ? a.d_shared : nullptr, a.y);
+    // the blocks this CTA completed: one thread per 8 rows of one token, the
+    // k + 1 expert outputs read as 16-byte words, summed in rank order
     const int n_last = sm.n_last;
+    for (int e = tid; e < n_last * T * (kRowBlock / 8); e += kLT) {
+        const int qb = e / (T * (kRowBlock / 8)), rem = e - qb * (T * (kRowBlock / 8));
+        const int t = rem / (kRowBlock / 8), r = sm.last[qb] * kRowBlock + 8 * (rem - t * (kRowBlock / 8));
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        auto add = [&](float wj, const uint4 dj) {
+            const uint32_t dw[4] = {dj.x, dj.y, dj.z, dj.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(wj, bf16_lo(dw[i]), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wj, bf16_hi(dw[i]), acc[2 * i + 1]);
+            }
+        };
+        const uint4* dr = reinterpret_cast<const uint4*>(a.d_routed + (size_t)t * k * H + r);
+        for (int j = 0; j < k; j += 2) {  // two loads in flight
+            const uint4 d0 = __ldcg(dr + (size_t)j * (H / 8));
+            const uint4 d1 = j + 1 < k ? __ldcg(dr + (size_t)(j + 1) * (H / 8)) : make_uint4(0u, 0u, 0u, 0u);
+            add(sm.w[t * k + j], d0);
+            if (j + 1 < k) add(sm.w[t * k + j + 1], d1);
+        }
+        if (has_sh) {
+            const uint4 ds = __ldcg(reinterpret_cast<const uint4*>(a.d_shared + (size_t)t * H + r));
+            const uint32_t dw[4] = {ds.x, ds.y, ds.z, ds.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += bf16_lo(dw[i]);
+                acc[2 * i + 1] += bf16_hi(dw[i]);
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = (uint32_t)f32_to_bf16_bits(acc[2 * i]) | ((uint32_t)f32_to_bf16_bits(acc[2 * i + 1]) << 16);
+        *reinterpret_cast<uint4*>(a.y + (size_t)t * H + r) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
     for (int q = tid; q < n_last; q += kLT) a.counters[sm.last[q]] = 0;
     __syncthreads();
     FLINT_PHASE(10);
