@@ -116,11 +116,11 @@ struct LayerSmall {
 };
 
 // Shared memory: small arrays, the routing view, the tensor scales of all
-// routed experts, the router logits' partial sums, the staging region (x, then
+// routed experts, the staging region (x, then
 // h of the CTA's down experts) and its chunk scales, the norm's partial sums,
 // the router rows (later: all sigmoid scores for the top-k), the ring.
 struct LayerSmem {
-    size_t small, ri, tsall, part, xs, csc, nred, rows, ring, total;
+    size_t small, ri, tsall, xs, csc, nred, rows, ring, total;
 };
 
 __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
@@ -129,8 +129,7 @@ __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     L.small = 0;
     L.ri = align_up(sizeof(LayerSmall), 128);
     L.tsall = align_up(L.ri + sizeof(RouteInfo), 128);
-    L.part = align_up(L.tsall + 12 * (size_t)a.E, 128);
-    L.xs = align_up(L.part + sizeof(float) * (size_t)a.rpc * T * (H / 256), 128);
+    L.xs = align_up(L.tsall + 12 * (size_t)a.E, 128);
     L.csc = align_up(L.xs + (size_t)a.stage_vals, 128);
     L.nred = align_up(L.csc + (size_t)a.stage_scales, 128);
     L.rows = align_up(L.nred + (a.norm.r ? sizeof(float) * T * (H / 32) : 0), 128);
@@ -409,40 +408,34 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         const bool ok = mbar_wait_bounded(&sm.rbar, 0, a.status, kStatusTimeoutLayer, budget);
         if (!ok) sm.fail = 1;
         const uint16_t* wrows = reinterpret_cast<const uint16_t*>(smem + L.rows);
-        // Logits from the staged (exact, chunk-scaled f16) x, spread over all
-        // warps: an item is (row, token, 256-column slice); lane l takes word
-        // l % 4 (8 values) of the slice's 32-value chunk l / 4, whose FP32
-        // partial sum is multiplied back by the chunk's power-of-two scale. The
-        // slices' sums are added in slice order.
-        float* part = reinterpret_cast<float*>(smem + L.part);
-        const int nsl = H / 256, n_it = nrr * T * nsl;
-        for (int q = warp; ok && q < n_it; q += kLW) {
-            const int rt = q / nsl, sl = q - rt * nsl, r = rt / T, t = rt - r * T;
-            const int cch = 8 * sl + (lane >> 2), wd = lane & 3;  // 32-value chunk, word
-            const uint4 xv = xh[(size_t)t * (H / 8) + (cch >> 5) * 128 + wd * 32 + (cch & 31)];
-            const uint4 wq = reinterpret_cast<const uint4*>(wrows + (size_t)r * H)[4 * cch + wd];
-            const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wq.x, wq.y, wq.z, wq.w};
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xa[i]));
-                s0 = fmaf(bf16_lo(wa[i]), xf.x, s0);
-                s1 = fmaf(bf16_hi(wa[i]), xf.y, s1);
-            }
-            float v = s0 + s1;
-            v += __shfl_xor_sync(full_mask, v, 1);
-            v += __shfl_xor_sync(full_mask, v, 2);
-            v *= csc[(size_t)t * (H / 32) + cch];
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) v += __shfl_xor_sync(full_mask, v, off);
-            if (lane == 0) part[q] = v;
-        }
-        __syncthreads();
-        for (int rt = tid; ok && rt < nrr * T; rt += kLT) {
-            const int r = rt / T, t = rt - r * T;
+        // logits from the staged (exact, chunk-scaled f16) x, one warp per
+        // (row, token): lane l takes the 32-value chunks l, l + 32, ...; each
+        // chunk's FP32 partial sum is multiplied back by its power-of-two scale
+        for (int q = warp; ok && q < nrr * T; q += kLW) {
+            const int r = q / T, t = q - r * T;
+            const uint4* xb = xh + (size_t)t * (H / 8) + lane;
+            const float* cb = csc + (size_t)t * (H / 32) + lane;
+            const uint4* wv = reinterpret_cast<const uint4*>(wrows + (size_t)r * H);
             float v = 0.f;
-            for (int sl = 0; sl < nsl; ++sl) v += part[rt * nsl + sl];
-            a.scores[(size_t)t * E + r0 + r] = sigmoid_score(v, a.bias, r0 + r);
+            for (int m = 0; m < H / 1024; ++m) {
+                const int ch = lane + 32 * m;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint4 xv = xb[(m * 4 + w) * 32], wq = wv[4 * ch + w];
+                    const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xa[i]));
+                        s0 = fmaf(bf16_lo(wa[i]), xf.x, s0);
+                        s1 = fmaf(bf16_hi(wa[i]), xf.y, s1);
+                    }
+                }
+                v = fmaf(cb[32 * m], s0 + s1, v);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(full_mask, v, off);
+            if (lane == 0) a.scores[(size_t)t * E + r0 + r] = sigmoid_score(v, a.bias, r0 + r);
         }
         __syncthreads();
         if (tid == 0 && ok && !withhold) release_add_gpu(a.hdr + kHdrScoresIn, (uint32_t)nrr);

@@ -65,12 +65,13 @@ def main(argv=None):
     args = p.parse_args(argv)
 
     from . import _build
-    os.environ["FLINT_LIBRARY"] = _build.build(trace=True)
+    if "trace" not in os.path.basename(os.environ.get("FLINT_LIBRARY", "")):  # a trace build chosen by the caller
+        os.environ["FLINT_LIBRARY"] = _build.build(trace=True)
     import torch
 
     from . import flint as F
     from . import synth
-    if "libflint_trace" not in F.LIBRARY_PATH:
+    if "trace" not in os.path.basename(F.LIBRARY_PATH):
         sys.exit("the binding was imported before the trace build was selected")
     read = F.raw_library().flint_phase_trace_read
     read.restype = C.c_longlong
