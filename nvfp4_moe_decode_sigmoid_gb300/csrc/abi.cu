@@ -192,8 +192,7 @@ bool down_bf16_shape(flint::DownArgs& a, int sm_count, int smem_optin) {
 // [0, Gs), in proportion to its cost among all the layer's experts: a row of
 // an expert costs ~ 4 + 3 x the tokens that use it (decoding the codes once,
 // then a multiply-add per token; measured per-pair times at 1 and 8 tokens),
-// with the routed experts' token count at its expected T k / min(E, T k). The ring takes as many slots of
-// 2 x kLayerWarps gate/up rows (up to 4) as shared memory allows, at least 2.
+// with the routed experts' token count at its expected T k / min(E, T k).
 bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     const int G = sm_count;
     const int T = a.T, H = a.H;
@@ -214,11 +213,11 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     const unsigned long long wmax = 4ull * units + 3ull * T * a.k;
     const unsigned long long per = (unsigned long long)(a.I > H / 16 ? a.I : H / 16);
     if (wmax * per * (unsigned long long)(G + 1) >= (1ull << 32)) return false;
+    // a ring slot holds one gate/up pair (two rows of H) or a group of down rows
     const int RS = (int)flint::nvfp4_row_stride(H);
-    a.slot = 2 * flint::kLayerWarps * RS;
-    // a down chunk takes whole 16-row blocks
+    a.slot = 2 * RS;
     const int kmax = a.I > a.Is ? a.I : a.Is;
-    if (a.slot / flint::nvfp4_row_stride(kmax) < 16) return false;
+    if (a.slot < flint::nvfp4_row_stride(kmax)) return false;
     // staging: x, later the h of at most two routed experts (all tokens) or of the shared expert
     const size_t x_vals = 2 * (size_t)T * H, x_sc = 4 * (size_t)T * (H / 32);
     const size_t h_r = 2 * (2 * (size_t)T * a.I), h_s = 2 * (size_t)T * a.Is;  // two routed experts, or the shared one
@@ -226,6 +225,7 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     const size_t h_sc = 4 * (size_t)T * ((2 * a.I > a.Is ? 2 * a.I : a.Is) / 32);
     a.stage_vals = (int)(x_vals > h_vals ? x_vals : h_vals);
     a.stage_scales = (int)(x_sc > h_sc ? x_sc : h_sc);
+    // ring slots per warp: as many as fit, up to 4, at least 2
     for (int ns = flint::kLayerMaxSlots; ns >= 2; --ns) {
         a.ns = ns;
         if (flint::layer_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin) return true;

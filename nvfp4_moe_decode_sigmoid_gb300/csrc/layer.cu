@@ -16,10 +16,14 @@
 //     pairs and one of down-row blocks in the concatenation of its group's
 //     experts (an expert's row costs ~ 4 + 3 x the tokens that chose it: its
 //     decode once, a multiply-add per token), so a CTA touches one or two
-//     experts and streams their rows as a few large bulk copies (TMA) into a
-//     CTA-wide ring of shared-memory slots.
+//     experts.
+//   * The CTA's items (a gate/up pair; a group of up to 8 down rows) are dealt
+//     to its warps round-robin; each warp streams its own items through a
+//     private ring of shared-memory slots fed by bulk copies (TMA) that its
+//     lane 0 issues, so a slot is refilled as soon as its warp is done with it.
 //   * Before the PDL wait each CTA starts the copies of its static weights:
-//     its router rows, and in the shared group all of its shared-expert rows.
+//     its router rows, the routed experts' tensor scales, and in the shared
+//     group the first items of every warp's ring.
 //   * Exchanges go through the workspace with release / acquire counters,
 //     each polled by one thread per CTA: the router rows published (every CTA
 //     then reads all scores and selects the top-k itself), and per expert the
@@ -63,7 +67,7 @@ __device__ unsigned long long g_phase_trace[kTraceCalls][kTraceCtas][kTraceStamp
 
 constexpr int kLW = kLayerWarps;
 constexpr int kLT = kLayerThreads;
-constexpr int kMaxChunks = 96;
+constexpr int kMaxSegs = 4;
 constexpr int kMaxDownUnits = 4;
 constexpr int kMaxVec = kMaxDownUnits * FLINT_MAX_TOKENS;
 constexpr int kRowBlock = 16;                 // output rows per combine block
@@ -75,28 +79,26 @@ constexpr uint32_t kStatusPoisonMask = kStatusTimeoutRoute | kStatusTimeoutGateU
                                        kStatusTimeoutSelftest | kStatusTimeoutLayer | kStatusTimeoutPrefill |
                                        kStatusLayerPlan;
 
-enum : int8_t { kChunkGateUp = 0, kChunkDown = 1 };
-
-// One ring chunk: `count` gate/up pairs (gate rows then up rows, two bulk
-// copies) or `count` down rows (one bulk copy) of one expert.
-struct Chunk {
-    int8_t kind;
-    int8_t q;       // down chunks: index of the expert among the CTA's down experts
+// A run of a CTA's items from one expert: gate/up pairs [start, start +
+// count) (one item each), or down rows [start, start + count) in items of rg
+// rows.
+struct Seg {
     int16_t unit;   // index into the distinct-expert list, or kSharedUnit
+    int8_t q;       // down runs: index of the expert among the CTA's down experts
+    int8_t rg;      // down runs: rows per item
+    int32_t item0;  // the run's first item (CTA-local index)
     int32_t start, count;
 };
 
 struct LayerSmall {
-    uint64_t full[kLayerMaxSlots];   // ring slot s holds its chunk's bytes
-    uint64_t rbar;                   // the router rows are in
-    uint32_t rel[kLayerMaxSlots];    // warps done with the slot's current chunk
-    int32_t last_issued[kLayerMaxSlots];
+    uint64_t wbar[kLW][kLayerMaxSlots];  // warp w's ring slot s holds its item's bytes
+    uint64_t rbar;                   // the router rows (and tensor scales) are in
+    int32_t issued[kLW];             // items a warp has issued (for the drain on failure)
     uint32_t hdr[8];                 // workspace header at the start of the call
-    int n_chunks, n_gu, fail, n_last, ok;
+    int fail, n_last, ok;
+    int n_gseg, n_dseg, n_gi, n_di;  // runs and items of this CTA
     int b0, b1;                      // this CTA's down range, in (expert, row block) items
-    Chunk chunk[kMaxChunks];
-    int n_dn;                        // experts among the down chunks
-    int16_t dn_unit[kMaxDownUnits];
+    Seg gseg[kMaxSegs], dseg[kMaxDownUnits];
     int16_t vec[kMaxDownUnits][FLINT_MAX_TOKENS];  // staged h vector of (down expert, token), or -1
     int n_vec;
     int32_t v_item0[kMaxVec + 1];    // first 32-value staging item of each vector
@@ -116,9 +118,9 @@ struct LayerSmall {
 };
 
 // Shared memory: small arrays, the routing view, the tensor scales of all
-// routed experts, the staging region (x, then
-// h of the CTA's down experts) and its chunk scales, the norm's partial sums,
-// the router rows (later: all sigmoid scores for the top-k), the ring.
+// routed experts, the staging region (x, then h of the CTA's down experts)
+// and its chunk scales, the norm's partial sums, the router rows (later: all
+// sigmoid scores for the top-k), the warps' rings.
 struct LayerSmem {
     size_t small, ri, tsall, xs, csc, nred, rows, ring, total;
 };
@@ -135,19 +137,13 @@ __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     L.rows = align_up(L.nred + (a.norm.r ? sizeof(float) * T * (H / 32) : 0), 128);
     const size_t rows_b = 2 * (size_t)a.rpc * H, sc_b = sizeof(uint32_t) * T * a.E;
     L.ring = align_up(L.rows + (rows_b > sc_b ? rows_b : sc_b), 128);
-    L.total = L.ring + (size_t)a.ns * a.slot;
+    L.total = L.ring + (size_t)kLW * a.ns * a.slot;
     return L;
 }
 
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-__device__ __forceinline__ uint32_t atom_add_acq_rel_cta_smem(uint32_t* p, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.add.acq_rel.cta.shared::cta.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v)
-                 : "memory");
     return old;
 }
 // Publishes the CTA's earlier writes (ordered before this thread by a
@@ -242,41 +238,43 @@ __device__ __forceinline__ int cost_pos(uint32_t tau, const int32_t* cum, int D,
     return lo * per + (int)(p < (uint32_t)per ? p : (uint32_t)per);
 }
 
-// Appends the chunks of the pair range [p0, p1) and the down block range
-// [b0, b1) (items of a concatenation of experts of per_gu pairs / NB blocks;
-// unit_of(i) maps an item's expert position to its unit id). One thread.
-template <typename UnitOf, typename RowsOf>
-__device__ void build_chunks(LayerSmall& sm, int p0, int p1, int per_gu, int b0, int b1, int NB, uint32_t* status,
-                             UnitOf unit_of, RowsOf rows_per_chunk) {
+// The runs of the pair range [p0, p1) and of the down block range [b0, b1)
+// (items of a concatenation of experts of per_gu pairs / NB blocks: the
+// routed experts in list order, or the shared expert alone); a down item
+// takes rg rows. One thread.
+__device__ void build_segs(LayerSmall& sm, int p0, int p1, int per_gu, int b0, int b1, int NB, uint32_t* status,
+                           bool shared, int rg) {
     int n = 0;
     for (int P = p0; P < p1;) {
-        if (n == kMaxChunks) {
+        const int u = P / per_gu, p = P - u * per_gu;
+        const int m = min(p1 - P, per_gu - p);
+        if (n == kMaxSegs) {
             sm.fail = 1;  // the host sizes the grid so that this cannot happen
             atomicOr(status, kStatusLayerPlan);
             break;
         }
-        const int u = P / per_gu, p = P - u * per_gu;
-        const int m = min(kLW, min(p1 - P, per_gu - p));
-        sm.chunk[n++] = Chunk{kChunkGateUp, 0, (int16_t)unit_of(u), p, m};
+        sm.gseg[n++] = Seg{(int16_t)(shared ? kSharedUnit : u), 0, 0, P - p0, p, m};
         P += m;
     }
-    sm.n_gu = n;
-    int nd = 0;
+    sm.n_gseg = n;
+    sm.n_gi = p1 > p0 ? p1 - p0 : 0;
+    int nd = 0, items = 0;
     for (int B = b0; B < b1;) {
         const int u = B / NB, b = B - u * NB;
-        const int unit = unit_of(u);
-        const int take = min(b1 - B, min(NB - b, max(1, rows_per_chunk(unit) / kRowBlock)));
-        if (n == kMaxChunks || (nd == kMaxDownUnits && sm.dn_unit[nd - 1] != unit)) {
-            sm.fail = 1;  // the host sizes the grid so that this cannot happen
+        const int take = min(b1 - B, NB - b);
+        if (nd == kMaxDownUnits) {
+            sm.fail = 1;
             atomicOr(status, kStatusLayerPlan);
             break;
         }
-        if (nd == 0 || sm.dn_unit[nd - 1] != unit) sm.dn_unit[nd++] = (int16_t)unit;
-        sm.chunk[n++] = Chunk{kChunkDown, (int8_t)(nd - 1), (int16_t)unit, b * kRowBlock, take * kRowBlock};
+        const int rows = take * kRowBlock;
+        sm.dseg[nd] = Seg{(int16_t)(shared ? kSharedUnit : u), (int8_t)nd, (int8_t)rg, items, b * kRowBlock, rows};
+        items += (rows + rg - 1) / rg;
+        ++nd;
         B += take;
     }
-    sm.n_chunks = n;
-    sm.n_dn = nd;
+    sm.n_dseg = nd;
+    sm.n_di = items;
     sm.b0 = b0;
     sm.b1 = b1;
 }
@@ -290,14 +288,15 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     const LayerSmem L = layer_layout(a);
     const int T = a.T, H = a.H, E = a.E, k = a.k, I = a.I, Is = a.Is;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = blockIdx.x, G = gridDim.x, Gs = a.Gs, NS = a.ns;
+    const int c = blockIdx.x, G = gridDim.x, Gs = a.Gs, NSW = a.ns;
     const bool sh_cta = c < Gs;
     const bool has_sh = a.s_gu != nullptr;
     LayerSmall& sm = *reinterpret_cast<LayerSmall*>(smem + L.small);
     RouteInfo& ri = *reinterpret_cast<RouteInfo*>(smem + L.ri);
     uint4* xh = reinterpret_cast<uint4*>(smem + L.xs);
     float* csc = reinterpret_cast<float*>(smem + L.csc);
-    uint8_t* ring = smem + L.ring;
+    uint8_t* wring = smem + L.ring + (size_t)warp * NSW * a.slot;  // this warp's ring
+    uint64_t* wbar = sm.wbar[warp];
     const int RS = (int)nvfp4_row_stride(H), RSr = (int)nvfp4_row_stride(I);
     const int RSs = Is ? (int)nvfp4_row_stride(Is) : 0;
     const int NB = H / kRowBlock;
@@ -308,75 +307,96 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     const bool ts_bulk = !sh_cta && (reinterpret_cast<uintptr_t>(a.ts) % 16 == 0) && ((12 * E) % 16 == 0);
     const uint32_t rbar_bytes = (uint32_t)(nrr * H * 2) + (ts_bulk ? 12u * (uint32_t)E : 0u);
     const float* tsall = reinterpret_cast<const float*>(smem + L.tsall);
+    // rows per down item: up to 8 (4 when the CTA has at most 4 per warp), as
+    // many as one slot holds
+    auto rows_per_item = [&](int RSu, int rows) {
+        int rg = rows <= 4 * kLW ? 4 : 8;
+        while (rg > 1 && rg * RSu > a.slot) rg >>= 1;
+        return rg;
+    };
 
-    // Issues chunk i into its ring slot (one thread).
-    auto issue = [&](int i) {
-        if (i >= sm.n_chunks) return;
-        const Chunk ch = sm.chunk[i];
-        const int s = i % NS;
-        uint8_t* slot = ring + (size_t)s * a.slot;
-        const bool sh = ch.unit == kSharedUnit;
-        fence_proxy_async_smem();  // the slot's earlier generic reads come first
-        if (ch.kind == kChunkGateUp) {
-            const uint8_t* base = sh ? a.s_gu : a.gu + (size_t)ri.dlist[ch.unit] * 2 * I * RS;
-            const uint32_t bytes = (uint32_t)ch.count * RS;
-            mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
-            bulk_g2s(slot, base + (size_t)ch.start * RS, bytes, &sm.full[s]);
-            bulk_g2s(slot + (size_t)kLW * RS, base + (size_t)((sh ? Is : I) + ch.start) * RS, bytes, &sm.full[s]);
+    // This warp's items: the CTA's gate/up items warp, warp + kLW, ... then
+    // its down items warp, warp + kLW, ... (sequence index it).
+    int my_g = 0, my_d = 0;
+    auto count_mine = [&]() {
+        my_g = sm.n_gi > warp ? (sm.n_gi - warp + kLW - 1) / kLW : 0;
+        my_d = sm.n_di > warp ? (sm.n_di - warp + kLW - 1) / kLW : 0;
+    };
+    // Issues item `it` of this warp's sequence into its slot (lane 0).
+    auto issue = [&](int it) {
+        const int slot = it % NSW;
+        uint8_t* dst = wring + (size_t)slot * a.slot;
+        uint64_t* bar = wbar + slot;
+        fence_proxy_async_smem();  // the slot's earlier reads come first
+        if (it < my_g) {
+            const int m = warp + it * kLW;
+            int s = 0;
+            while (s + 1 < sm.n_gseg && sm.gseg[s + 1].item0 <= m) ++s;
+            const Seg sg = sm.gseg[s];
+            const bool sh = sg.unit == kSharedUnit;
+            const int p = sg.start + (m - sg.item0);
+            const uint8_t* g = sh ? a.s_gu : a.gu + (size_t)ri.dlist[sg.unit] * 2 * I * RS;
+            mbar_arrive_expect_tx(bar, 2u * (uint32_t)RS);
+            bulk_g2s(dst, g + (size_t)p * RS, (uint32_t)RS, bar);
+            bulk_g2s(dst + RS, g + (size_t)((sh ? Is : I) + p) * RS, (uint32_t)RS, bar);
         } else {
+            const int m = warp + (it - my_g) * kLW;
+            int s = 0;
+            while (s + 1 < sm.n_dseg && sm.dseg[s + 1].item0 <= m) ++s;
+            const Seg sg = sm.dseg[s];
+            const bool sh = sg.unit == kSharedUnit;
             const int RSu = sh ? RSs : RSr;
-            const uint8_t* base = sh ? a.s_down : a.down + (size_t)ri.dlist[ch.unit] * H * RSr;
-            const uint32_t bytes = (uint32_t)ch.count * RSu;
-            mbar_arrive_expect_tx(&sm.full[s], bytes);
-            bulk_g2s(slot, base + (size_t)ch.start * RSu, bytes, &sm.full[s]);
+            const int r = sg.start + (m - sg.item0) * sg.rg, nr = min((int)sg.rg, sg.start + sg.count - r);
+            const uint8_t* d = sh ? a.s_down : a.down + (size_t)ri.dlist[sg.unit] * H * RSr;
+            mbar_arrive_expect_tx(bar, (uint32_t)(nr * RSu));
+            bulk_g2s(dst, d + (size_t)r * RSu, (uint32_t)(nr * RSu), bar);
         }
-        sm.last_issued[s] = i;
+        sm.issued[warp] = it + 1;
     };
     // Before an early exit: the bulk copies still in flight into this CTA's
-    // shared memory land first (bounded; thread 0).
+    // shared memory land first (bounded; thread 0 for the router rows, lane 0
+    // of each warp for its ring).
     auto drain = [&](uint64_t budget_ns) {
-        if (tid != 0) return;
-        if (rbar_bytes) mbar_wait_bounded(&sm.rbar, 0, nullptr, 0, budget_ns);
-        for (int s = 0; s < NS; ++s) {
-            const int j = sm.last_issued[s];
-            if (j >= 0) mbar_wait_bounded(&sm.full[s], (uint32_t)(j / NS) & 1u, nullptr, 0, budget_ns);
+        if (tid == 0 && rbar_bytes) mbar_wait_bounded(&sm.rbar, 0, nullptr, 0, budget_ns);
+        if (lane == 0) {
+            const int n = sm.issued[warp];
+            for (int it = max(0, n - NSW); it < n; ++it)
+                mbar_wait_bounded(wbar + it % NSW, (uint32_t)(it / NSW) & 1u, nullptr, 0, budget_ns);
         }
-    };
-    auto rows_per_chunk = [&](int unit) {
-        const int RSu = unit == kSharedUnit ? RSs : RSr;
-        return min(8 * kLW, a.slot / RSu);
     };
 
     // ---- 0: before the PDL wait: barriers, static weight copies ----------------------
 #ifdef FLINT_PHASE_TRACE
+    if (tid < kTraceStamps) sm.trace[tid] = 0;
     const uint64_t trace_t0 = globaltimer_ns();
 #endif
-#ifdef FLINT_PHASE_TRACE
-    if (tid < kTraceStamps) sm.trace[tid] = 0;
-    __syncthreads();
-#endif
     FLINT_PHASE(0);
+    if (tid < kLW * NSW) mbar_init(&sm.wbar[tid / NSW][tid % NSW], 1);
+    if (tid < kLW) sm.issued[tid] = 0;
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&sm.full[s], 1);
-            sm.rel[s] = 0;
-            sm.last_issued[s] = -1;
-        }
         mbar_init(&sm.rbar, 1);
-        fence_mbar_init();
         sm.fail = 0;
         sm.n_last = 0;
-        sm.n_chunks = sm.n_gu = sm.n_dn = 0;
-        if (rbar_bytes) mbar_arrive_expect_tx(&sm.rbar, rbar_bytes);
-        if (nrr > 0) bulk_g2s(smem + L.rows, a.wr + (size_t)r0 * H, (uint32_t)(nrr * H * 2), &sm.rbar);
-        if (ts_bulk) bulk_g2s(smem + L.tsall, a.ts, 12u * (uint32_t)E, &sm.rbar);
+        sm.n_gi = sm.n_di = sm.n_gseg = sm.n_dseg = 0;
+        sm.b0 = sm.b1 = 0;
         if (sh_cta) {
             // the shared expert: an even split of its pairs and row blocks
             const int p0 = (int)((long long)c * Is / Gs), p1 = (int)((long long)(c + 1) * Is / Gs);
             const int b0 = (int)((long long)c * NB / Gs), b1 = (int)((long long)(c + 1) * NB / Gs);
-            build_chunks(sm, p0, p1, Is, b0, b1, NB, a.status, [](int) { return kSharedUnit; }, rows_per_chunk);
-            for (int i = 0; i < NS; ++i) issue(i);
+            build_segs(sm, p0, p1, Is, b0, b1, NB, a.status, true, rows_per_item(RSs, (b1 - b0) * kRowBlock));
         }
+    }
+    if (tid <= kLW * NSW) fence_mbar_init();
+    __syncthreads();
+    if (tid == 0) {
+        if (rbar_bytes) mbar_arrive_expect_tx(&sm.rbar, rbar_bytes);
+        if (nrr > 0) bulk_g2s(smem + L.rows, a.wr + (size_t)r0 * H, (uint32_t)(nrr * H * 2), &sm.rbar);
+        if (ts_bulk) bulk_g2s(smem + L.tsall, a.ts, 12u * (uint32_t)E, &sm.rbar);
+    }
+    if (sh_cta) {
+        count_mine();
+        if (lane == 0 && !sm.fail)
+            for (int it = 0; it < NSW && it < my_g + my_d; ++it) issue(it);
     }
     // Dependents may launch now: their CTAs take SMs as ours exit, and only
     // read static weights before their own wait.
@@ -447,9 +467,8 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 
     // Routing in this CTA: once all E router rows are published, all T x E
     // scores into shared memory over the router rows and the top-k of each
-    // token (one warp per token); warp 0 then builds the routing view
-    // (route_view_warp). Every thread calls it; false (in every thread) if
-    // the scores never came.
+    // token (one warp per token). Every thread calls it; false (in every
+    // thread) if the scores never came.
     auto route = [&](int stamp) -> bool {
         (void)stamp;
         if (!cta_wait_count(a.hdr + kHdrScoresIn, (uint32_t)E, a.status, kStatusTimeoutLayer, budget, &sm.ok) ||
@@ -510,14 +529,14 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 }
                 const int p0 = __shfl_sync(full_mask, pos, 0), p1 = __shfl_sync(full_mask, pos, 1);
                 const int b0 = __shfl_sync(full_mask, pos, 2), b1 = __shfl_sync(full_mask, pos, 3);
-                if (lane == 0) {
-                    build_chunks(sm, p0, p1, I, b0, b1, NB, a.status, [](int u) { return u; }, rows_per_chunk);
-                    if (!sm.fail)
-                        for (int i = 0; i < NS; ++i) issue(i);
-                }
+                if (lane == 0)
+                    build_segs(sm, p0, p1, I, b0, b1, NB, a.status, false, rows_per_item(RSr, (b1 - b0) * kRowBlock));
                 FLINT_PHASE(19);
             }
             __syncthreads();
+            count_mine();
+            if (lane == 0 && !sm.fail)
+                for (int it = 0; it < NSW && it < my_g + my_d; ++it) issue(it);
             // the tensor scales of the selected experts (copied before the wait,
             // or read now while the weight copies are in flight)
             const int D = ri.D;
@@ -539,13 +558,13 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     failed = __syncthreads_or(failed || sm.fail);
     FLINT_PHASE(4);
 
-    // ---- 3-4: the ring: gate/up chunks, then (h of the down experts staged) down chunks --
-    const int n_chunks = failed ? 0 : sm.n_chunks, n_gu = failed ? 0 : sm.n_gu;
+    // ---- 3-4: this warp's ring: gate/up items, then (h of the down experts staged) down items --
+    if (failed) my_g = my_d = 0;
     bool wfail = false;  // this warp gave up on a copy
-    // Waits for chunk i's bytes (all lanes; false once anything failed).
-    auto chunk_in = [&](int i) {
+    // Waits for item it's bytes (all lanes; false once anything failed).
+    auto item_in = [&](int it) {
         if (!wfail && !sm.fail) {
-            if (__all_sync(full_mask, mbar_wait_bounded(&sm.full[i % NS], (uint32_t)(i / NS) & 1u, a.status,
+            if (__all_sync(full_mask, mbar_wait_bounded(wbar + it % NSW, (uint32_t)(it / NSW) & 1u, a.status,
                                                         kStatusTimeoutLayer, budget)))
                 return true;
             if (lane == 0) sm.fail = 1;
@@ -553,68 +572,54 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         wfail = true;
         return false;
     };
-    // The last warp done with chunk i refills its slot with chunk i + NS.
-    auto chunk_done = [&](int i) {
+    // Done with item it: lane 0 refills its slot with item it + NSW.
+    auto item_done = [&](int it) {
         __syncwarp();
-        if (lane == 0) {
-            const int s = i % NS;
-            if (atom_add_acq_rel_cta_smem(&sm.rel[s], 1u) == kLW - 1) {
-                sm.rel[s] = 0;
-                if (!sm.fail) issue(i + NS);
-            }
-        }
+        if (lane == 0 && it + NSW < my_g + my_d && !sm.fail) issue(it + NSW);
     };
-    for (int i = 0; i < n_gu; ++i) {
-        if (!chunk_in(i)) continue;
-        if (i == 0) FLINT_PHASE(5);
-        const Chunk ch = sm.chunk[i];
-        if (warp < ch.count) {
-            const uint8_t* slot = ring + (size_t)(i % NS) * a.slot;
-            const bool sh = ch.unit == kSharedUnit;
-            const int ui = sh ? kShIdx : ch.unit;
-            const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[ch.unit];
-            const uint8_t* grow = slot + (size_t)warp * RS;
-            const uint8_t* urow = slot + (size_t)(kLW + warp) * RS;
-            float* rg = sm.res[warp][0];
-            float* ru = sm.res[warp][1];
-            gate_up_item<true>(grow, urow, H, xh, csc, tm, lane, rg, ru);
-            __syncwarp();
-            if (lane < T && ((tm >> lane) & 1u)) {
-                const int p = ch.start + warp;
-                const float g = bf16_round_f32(sm.tsg[ui] * rg[lane]);
-                const float u = bf16_round_f32(sm.tsu[ui] * ru[lane]);
-                const uint16_t hv = f32_to_bf16_bits(silu_f32(g) * u);
-                if (sh) {
-                    a.h_shared[(size_t)lane * Is + p] = hv;
-                } else {
-                    const int j = __ffs(rank_bits(ri.dmask[ch.unit], lane)) - 1;
-                    a.h_routed[((size_t)lane * k + j) * I + p] = hv;
-                }
+    for (int it = 0; it < my_g; ++it) {
+        if (!item_in(it)) break;
+        if (it == 0) FLINT_PHASE(5);
+        const int m = warp + it * kLW;
+        int s = 0;
+        while (s + 1 < sm.n_gseg && sm.gseg[s + 1].item0 <= m) ++s;
+        const Seg sg = sm.gseg[s];
+        const bool sh = sg.unit == kSharedUnit;
+        const int ui = sh ? kShIdx : sg.unit;
+        const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[sg.unit];
+        const uint8_t* grow = wring + (size_t)(it % NSW) * a.slot;
+        float* rg = sm.res[warp][0];
+        float* ru = sm.res[warp][1];
+        gate_up_item<true>(grow, grow + RS, H, xh, csc, tm, lane, rg, ru);
+        __syncwarp();
+        if (lane < T && ((tm >> lane) & 1u)) {
+            const int p = sg.start + (m - sg.item0);
+            const float g = bf16_round_f32(sm.tsg[ui] * rg[lane]);
+            const float u = bf16_round_f32(sm.tsu[ui] * ru[lane]);
+            const uint16_t hv = f32_to_bf16_bits(silu_f32(g) * u);
+            if (sh) {
+                a.h_shared[(size_t)lane * Is + p] = hv;
+            } else {
+                const int j = __ffs(rank_bits(ri.dmask[sg.unit], lane)) - 1;
+                a.h_routed[((size_t)lane * k + j) * I + p] = hv;
             }
         }
-        chunk_done(i);
+        item_done(it);
     }
     // Publish this CTA's h: per expert, the number of its pairs done here.
     if (__syncthreads_or(wfail) && tid == 0) sm.fail = 1;
-    if (tid == 0 && !sm.fail) {
-        int unit = -2, cnt = 0;
-        for (int i = 0; i <= n_gu; ++i) {
-            const int u = i < n_gu ? sm.chunk[i].unit : -3;
-            if (u != unit && cnt) release_add_gpu(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit), cnt);
-            if (u != unit) {
-                unit = u;
-                cnt = 0;
-            }
-            if (i < n_gu) cnt += sm.chunk[i].count;
+    if (tid == 0 && !sm.fail && !failed)
+        for (int s = 0; s < sm.n_gseg; ++s) {
+            const int unit = sm.gseg[s].unit;
+            release_add_gpu(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit), (uint32_t)sm.gseg[s].count);
         }
-    }
     FLINT_PHASE(6);
-    if (n_chunks > n_gu) {
+    if (!failed && sm.n_di > 0) {
         // Stage h of this CTA's down experts once every pair of each is published.
         if (tid == 0) {
             int nv = 0, item = 0, off = 0, coff = 0;
-            for (int q = 0; q < sm.n_dn; ++q) {
-                const int unit = sm.dn_unit[q];
+            for (int q = 0; q < sm.n_dseg; ++q) {
+                const int unit = sm.dseg[q].unit;
                 const int K = unit == kSharedUnit ? Is : I;
                 const uint32_t tm = unit == kSharedUnit ? (1u << T) - 1u : ri.tmask[unit];
                 for (int t = 0; t < FLINT_MAX_TOKENS; ++t) {
@@ -643,19 +648,19 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             sm.v_item0[nv] = item;
         }
         bool ok = true;
-        for (int q = 0; q < sm.n_dn && ok; ++q) {  // sm.n_dn: written before the earlier barriers
-            const int unit = sm.dn_unit[q];
+        for (int q = 0; q < sm.n_dseg && ok; ++q) {  // sm.n_dseg: written before the earlier barriers
+            const int unit = sm.dseg[q].unit;
             ok = cta_wait_count(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit),
                                 (uint32_t)(unit == kSharedUnit ? Is : I), a.status, kStatusTimeoutLayer, budget,
                                 &sm.ok);
         }
         ok = ok && !sm.fail;
         const int n_items = ok ? sm.v_item0[sm.n_vec] : 0;
-        for (int it = tid; it < n_items; it += kLT) {
+        for (int q = tid; q < n_items; q += kLT) {
             int v = 0;
-            while (sm.v_item0[v + 1] <= it) ++v;
-            const int cc = it - sm.v_item0[v], t = sm.v_t[v];
-            const int unit = sm.dn_unit[sm.v_q[v]];
+            while (sm.v_item0[v + 1] <= q) ++v;
+            const int cc = q - sm.v_item0[v], t = sm.v_t[v];
+            const int unit = sm.dseg[sm.v_q[v]].unit;
             const bool sh = unit == kSharedUnit;
             const int K = sh ? Is : I;
             const uint16_t* src;
@@ -674,78 +679,74 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         if (!__syncthreads_and(ok)) wfail = true;
     }
     FLINT_PHASE(7);
-    for (int i = n_gu; i < n_chunks; ++i) {
-        if (!chunk_in(i)) continue;
-        const Chunk ch = sm.chunk[i];
-        // 8 rows per warp, or 4 when the chunk is small enough that every
-        // warp then has rows
-        const int rpw = ch.count <= 4 * kLW ? 4 : 8;
-        const int rw0 = rpw * warp;
-        if (rw0 < ch.count) {
-            const uint8_t* slot = ring + (size_t)(i % NS) * a.slot;
-            const bool sh = ch.unit == kSharedUnit;
-            const int ui = sh ? kShIdx : ch.unit;
-            const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[ch.unit];
-            const int nrw = min(rpw, ch.count - rw0);
-            const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
-            const uint8_t* rows = slot + (size_t)rw0 * RSu;
-            const int row0 = ch.start + rw0;
-            const float tsd = sm.tsd[ui];
-            const unsigned long long dm = sh ? 0ull : ri.dmask[ch.unit];
-            auto vec = [&](int t, const uint4*& hv, const float*& cv) {
-                const int v = sm.vec[ch.q][t];
-                hv = reinterpret_cast<const uint4*>(smem + L.xs + sm.v_off[v]);
-                cv = reinterpret_cast<const float*>(smem + L.csc + sm.v_coff[v]);
-            };
-            auto put = [&](float v, int r, int t) {
-                const uint16_t d = f32_to_bf16_bits(tsd * v);
-                if (sh) {
-                    a.d_shared[(size_t)t * H + row0 + r] = d;
-                } else {
-                    const int j = __ffs(rank_bits(dm, t)) - 1;
-                    a.d_routed[((size_t)t * k + j) * H + row0 + r] = d;
-                }
-            };
-            // rows [0, nrw) of the warp's RP-row group against one or two tokens
-            auto rows_pass = [&](auto rp_tag, int t0, int t1) {
-                constexpr int RP = decltype(rp_tag)::value;
-                if (t1 >= 0) {
-                    const uint4* hv[2];
-                    const float* cv[2];
-                    vec(t0, hv[0], cv[0]);
-                    vec(t1, hv[1], cv[1]);
-                    float acc[2 * RP];
-                    down_pass<RP, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
-                    const float v = reduce_scatter<2 * RP>(acc, lane);
-                    const int idx = rs_index<2 * RP>(lane), r = idx % RP;
-                    if (lane % (16 / RP) == 0 && r < nrw) put(v, r, idx >= RP ? t1 : t0);
-                } else {
-                    const uint4* hv[1];
-                    const float* cv[1];
-                    vec(t0, hv[0], cv[0]);
-                    float acc[RP];
-                    down_pass<RP, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
-                    const float v = reduce_scatter<RP>(acc, lane);
-                    const int r = rs_index<RP>(lane);
-                    if (lane % (32 / RP) == 0 && r < nrw) put(v, r, t0);
-                }
-            };
-            uint32_t rest = tm;
-            while (rest) {
-                const int t0 = __ffs(rest) - 1;
-                rest &= rest - 1u;
-                int t1 = -1;
-                if (rest) {
-                    t1 = __ffs(rest) - 1;
-                    rest &= rest - 1u;
-                }
-                if (rpw == 4)
-                    rows_pass(std::integral_constant<int, 4>(), t0, t1);
-                else
-                    rows_pass(std::integral_constant<int, 8>(), t0, t1);
+    for (int it = my_g; it < my_g + my_d; ++it) {
+        if (!item_in(it)) break;
+        const int m = warp + (it - my_g) * kLW;
+        int s = 0;
+        while (s + 1 < sm.n_dseg && sm.dseg[s + 1].item0 <= m) ++s;
+        const Seg sg = sm.dseg[s];
+        const bool sh = sg.unit == kSharedUnit;
+        const int ui = sh ? kShIdx : sg.unit;
+        const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[sg.unit];
+        const int row0 = sg.start + (m - sg.item0) * sg.rg;
+        const int nrw = min((int)sg.rg, sg.start + sg.count - row0);
+        const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
+        const uint8_t* rows = wring + (size_t)(it % NSW) * a.slot;
+        const float tsd = sm.tsd[ui];
+        const unsigned long long dm = sh ? 0ull : ri.dmask[sg.unit];
+        auto vec = [&](int t, const uint4*& hv, const float*& cv) {
+            const int v = sm.vec[sg.q][t];
+            hv = reinterpret_cast<const uint4*>(smem + L.xs + sm.v_off[v]);
+            cv = reinterpret_cast<const float*>(smem + L.csc + sm.v_coff[v]);
+        };
+        auto put = [&](float v, int r, int t) {
+            const uint16_t d = f32_to_bf16_bits(tsd * v);
+            if (sh) {
+                a.d_shared[(size_t)t * H + row0 + r] = d;
+            } else {
+                const int j = __ffs(rank_bits(dm, t)) - 1;
+                a.d_routed[((size_t)t * k + j) * H + row0 + r] = d;
             }
+        };
+        // rows [0, nrw) of the item against one or two tokens
+        auto rows_pass = [&](auto rp_tag, int t0, int t1) {
+            constexpr int RP = decltype(rp_tag)::value;
+            if (t1 >= 0) {
+                const uint4* hv[2];
+                const float* cv[2];
+                vec(t0, hv[0], cv[0]);
+                vec(t1, hv[1], cv[1]);
+                float acc[2 * RP];
+                down_pass<RP, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                const float v = reduce_scatter<2 * RP>(acc, lane);
+                const int idx = rs_index<2 * RP>(lane), r = idx % RP;
+                if (lane % (16 / RP) == 0 && r < nrw) put(v, r, idx >= RP ? t1 : t0);
+            } else {
+                const uint4* hv[1];
+                const float* cv[1];
+                vec(t0, hv[0], cv[0]);
+                float acc[RP];
+                down_pass<RP, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                const float v = reduce_scatter<RP>(acc, lane);
+                const int r = rs_index<RP>(lane);
+                if (lane % (32 / RP) == 0 && r < nrw) put(v, r, t0);
+            }
+        };
+        uint32_t rest = tm;
+        while (rest) {
+            const int t0 = __ffs(rest) - 1;
+            rest &= rest - 1u;
+            int t1 = -1;
+            if (rest) {
+                t1 = __ffs(rest) - 1;
+                rest &= rest - 1u;
+            }
+            if (sg.rg <= 4)
+                rows_pass(std::integral_constant<int, 4>(), t0, t1);
+            else
+                rows_pass(std::integral_constant<int, 8>(), t0, t1);
         }
-        chunk_done(i);
+        item_done(it);
     }
 
     // ---- 5: arrivals on the row blocks; the last arriver of a block combines it ------
@@ -818,8 +819,8 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         uint32_t smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
         dst[27] = smid;
-        dst[28] = (unsigned long long)sh_cta | ((unsigned long long)sm.n_chunks << 8) |
-                  ((unsigned long long)n_last << 16) | ((unsigned long long)sm.n_gu << 32);
+        dst[28] = (unsigned long long)sh_cta | ((unsigned long long)(sm.n_gi + sm.n_di) << 8) |
+                  ((unsigned long long)n_last << 16) | ((unsigned long long)sm.n_gi << 32);
         dst[29] = trace_t0;
         dst[30] = globaltimer_ns();
         dst[31] = sm.hdr[kHdrCalls] + 1ull;
