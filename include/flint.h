@@ -447,9 +447,10 @@ flint_status_t flint_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t b
 /*
  * flint_selftest_lose_cta -- test hook for the fused layer's failure path
  * (no counterpart in the method). On the next flint_moe_layer /
- * flint_moe_block call with this workspace, CTA `cta` publishes no router
- * scores, as if it had been lost: the other CTAs' bounded waits for those
- * scores run out (after the budget of flint_workspace_set_wait_budget), the
+ * flint_moe_block call with this workspace, CTA `cta` publishes neither its
+ * router scores nor its count of finished gate/up rows, as if it had been
+ * lost: the bounded waits for them (in the other CTAs, and in itself) run out
+ * (after the budget of flint_workspace_set_wait_budget), the
  * kernel records FLINT_ERR_TIMEOUT and every CTA returns. Nothing faults or
  * hangs. flint_workspace_check then reports the timeout and re-initialises the
  * workspace, which also clears the hook. Synchronises `stream`.

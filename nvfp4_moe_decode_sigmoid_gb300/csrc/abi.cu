@@ -205,7 +205,7 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     } else {
         a.Gs = 0;
     }
-    a.rpc = ceil_div(a.E, G);
+    a.rpc = ceil_div(a.E, G - a.Gs);  // router rows per routed CTA
     // the kernel splits by cost in 32-bit arithmetic: the total cost of the
     // routed pairs (or blocks) times the group's CTA count must stay below 2^32
     // (an expert's weight is at most 4 + 3 T and the weights sum to at most
@@ -225,12 +225,10 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     const size_t h_sc = 4 * (size_t)T * ((2 * a.I > a.Is ? 2 * a.I : a.Is) / 32);
     a.stage_vals = (int)(x_vals > h_vals ? x_vals : h_vals);
     a.stage_scales = (int)(x_sc > h_sc ? x_sc : h_sc);
-    // ring slots per warp: as many as fit, up to 4, at least 2
-    for (int ns = flint::kLayerMaxSlots; ns >= 2; --ns) {
-        a.ns = ns;
-        if (flint::layer_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin) return true;
-    }
-    return false;
+    // two ring slots per warp (three, where they fit, measured slower at 8
+    // tokens: more copies in flight slowed the weight stream)
+    a.ns = flint::kLayerSlots;
+    return flint::layer_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin;
 }
 
 }  // namespace

@@ -45,7 +45,8 @@ constexpr size_t kWsHeader = 256;   // control words, below
 // Workspace header words (uint32): the router's arrival counter, the status
 // word, the fused layer's count of completed calls and of finished CTAs, the
 // bounded waits' budget in microseconds (0: kWaitBudgetNs), a test hook
-// (c + 1: CTA c of the next fused-layer call publishes no router scores), and
+// (c + 1: CTA c of the next fused-layer call publishes neither router scores
+// nor h counts), and
 // the fused layer's count of published router rows.
 enum : int {
     kHdrRouteCounter = 0,
@@ -63,7 +64,7 @@ constexpr int kBf16Threads = kBf16Warps * 32;
 // Fused layer kernel: one cooperative CTA per SM.
 constexpr int kLayerWarps = 24;
 constexpr int kLayerThreads = kLayerWarps * 32;
-constexpr int kLayerMaxSlots = 4;        // ring slots of one CTA
+constexpr int kLayerSlots = 2;           // ring slots of each warp of the fused layer
 constexpr int kLayerMaxHidden = 8192;    // largest hidden size of the fused layer
 
 FLINT_HD constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -198,7 +199,7 @@ struct LayerArgs {
     uint16_t* y;         // [T][H] out
     int Gs;              // CTAs [0, Gs) run the shared expert
     int rpc;             // router rows per CTA
-    int ns, slot;        // ring slots per CTA and bytes per slot
+    int ns, slot;        // ring slots per warp (kLayerSlots) and bytes per slot
     int stage_vals, stage_scales;  // bytes of the staging region (x, later h) and of its chunk scales
     NormArgs norm;       // norm.r set: x = the norm of the residual stream (x unused)
 };

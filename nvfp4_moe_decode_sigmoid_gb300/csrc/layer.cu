@@ -22,8 +22,8 @@
 //     private ring of shared-memory slots fed by bulk copies (TMA) that its
 //     lane 0 issues, so a slot is refilled as soon as its warp is done with it.
 //   * Before the PDL wait each CTA starts the copies of its static weights:
-//     its router rows, the routed experts' tensor scales, and in the shared
-//     group the first items of every warp's ring.
+//     in the routed group its router rows and the routed experts' tensor
+//     scales, in the shared group the first items of every warp's ring.
 //   * Exchanges go through the workspace with release / acquire counters,
 //     each polled by one thread per CTA: the router rows published (every CTA
 //     then reads all scores and selects the top-k itself), and per expert the
@@ -53,7 +53,7 @@ namespace {
 // the stamps to a ring of the last kTraceCalls calls, indexed by the
 // workspace's call count. The plain build has none of this code.
 #ifdef FLINT_PHASE_TRACE
-constexpr int kTraceStamps = 32, kTraceCalls = 64, kTraceCtas = 256;
+constexpr int kTraceStamps = 40, kTraceCalls = 64, kTraceCtas = 256;
 __device__ unsigned long long g_phase_trace[kTraceCalls][kTraceCtas][kTraceStamps];
 #define FLINT_PHASE(i)                                     \
     do {                                                   \
@@ -91,7 +91,7 @@ struct Seg {
 };
 
 struct LayerSmall {
-    uint64_t wbar[kLW][kLayerMaxSlots];  // warp w's ring slot s holds its item's bytes
+    uint64_t wbar[kLW][kLayerSlots];  // warp w's ring slot s holds its item's bytes
     uint64_t rbar;                   // the router rows (and tensor scales) are in
     int32_t issued[kLW];             // items a warp has issued (for the drain on failure)
     uint32_t hdr[8];                 // workspace header at the start of the call
@@ -105,7 +105,6 @@ struct LayerSmall {
     int32_t v_off[kMaxVec];          // byte offset of its f16 values in the staging region
     int32_t v_coff[kMaxVec];         // byte offset of its chunk scales
     int16_t v_q[kMaxVec], v_t[kMaxVec];
-    float tsg[kMaxDistinct + 1], tsu[kMaxDistinct + 1], tsd[kMaxDistinct + 1];
     float w[kMaxDistinct];
     int32_t ids[kMaxDistinct];
     int32_t cumw[2 * 32];            // inclusive prefix of the experts' cost weights
@@ -114,13 +113,14 @@ struct LayerSmall {
     int16_t last[kLayerMaxHidden / kRowBlock];  // row blocks this CTA combines
 #ifdef FLINT_PHASE_TRACE
     unsigned long long trace[kTraceStamps];
+    unsigned long long wend[kLW];  // when each warp left its gate/up loop
 #endif
 };
 
 // Shared memory: small arrays, the routing view, the tensor scales of all
 // routed experts, the staging region (x, then h of the CTA's down experts)
-// and its chunk scales, the norm's partial sums, the router rows (later: all
-// sigmoid scores for the top-k), the warps' rings.
+// and its chunk scales, the norm's partial sums, the router rows, the warps'
+// rings.
 struct LayerSmem {
     size_t small, ri, tsall, xs, csc, nred, rows, ring, total;
 };
@@ -135,8 +135,7 @@ __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     L.csc = align_up(L.xs + (size_t)a.stage_vals, 128);
     L.nred = align_up(L.csc + (size_t)a.stage_scales, 128);
     L.rows = align_up(L.nred + (a.norm.r ? sizeof(float) * T * (H / 32) : 0), 128);
-    const size_t rows_b = 2 * (size_t)a.rpc * H, sc_b = sizeof(uint32_t) * T * a.E;
-    L.ring = align_up(L.rows + (rows_b > sc_b ? rows_b : sc_b), 128);
+    L.ring = align_up(L.rows + 2 * (size_t)a.rpc * H, 128);
     L.total = L.ring + (size_t)kLW * a.ns * a.slot;
     return L;
 }
@@ -288,7 +287,8 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     const LayerSmem L = layer_layout(a);
     const int T = a.T, H = a.H, E = a.E, k = a.k, I = a.I, Is = a.Is;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = blockIdx.x, G = gridDim.x, Gs = a.Gs, NSW = a.ns;
+    const int c = blockIdx.x, G = gridDim.x, Gs = a.Gs;
+    constexpr int NSW = kLayerSlots;
     const bool sh_cta = c < Gs;
     const bool has_sh = a.s_gu != nullptr;
     LayerSmall& sm = *reinterpret_cast<LayerSmall*>(smem + L.small);
@@ -300,13 +300,22 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     const int RS = (int)nvfp4_row_stride(H), RSr = (int)nvfp4_row_stride(I);
     const int RSs = Is ? (int)nvfp4_row_stride(Is) : 0;
     const int NB = H / kRowBlock;
-    const int r0 = c * a.rpc, nrr = max(0, min(a.rpc, E - r0));
+    // router rows: rpc each on the routed CTAs (the shared CTAs queue their
+    // expert's copies before the PDL wait and would publish late)
+    const int r0 = (c - Gs) * a.rpc, nrr = sh_cta ? 0 : max(0, min(a.rpc, E - r0));
     const uint32_t full_mask = 0xffffffffu;
     // The routed group copies the tensor scales of all routed experts before
     // the PDL wait (static; one bulk copy when their bytes allow it).
     const bool ts_bulk = !sh_cta && (reinterpret_cast<uintptr_t>(a.ts) % 16 == 0) && ((12 * E) % 16 == 0);
     const uint32_t rbar_bytes = (uint32_t)(nrr * H * 2) + (ts_bulk ? 12u * (uint32_t)E : 0u);
     const float* tsall = reinterpret_cast<const float*>(smem + L.tsall);
+    // tensor scale j (gate, up, down) of unit u: the shared expert, or routed
+    // expert ri.dlist[u] (from the copy of all of them when there is one)
+    auto tscale = [&](bool sh, int u, int j) -> float {
+        if (sh) return __ldg(a.s_ts + j);
+        const int e = ri.dlist[u];
+        return ts_bulk ? tsall[3 * e + j] : __ldg(a.ts + 3 * e + j);
+    };
     // rows per down item: up to 8 (4 when the CTA has at most 4 per warp), as
     // many as one slot holds
     auto rows_per_item = [&](int RSu, int rows) {
@@ -423,10 +432,12 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         drain(budget);
         return;
     }
-    const bool withhold = sm.hdr[kHdrLoseCta] == (uint32_t)c + 1u;  // test hook: this CTA publishes no scores
+    // test hook: this CTA publishes nothing (no router scores, no h counts)
+    const bool withhold = sm.hdr[kHdrLoseCta] == (uint32_t)c + 1u;
     if (nrr > 0) {
         const bool ok = mbar_wait_bounded(&sm.rbar, 0, a.status, kStatusTimeoutLayer, budget);
         if (!ok) sm.fail = 1;
+        FLINT_PHASE(35);
         const uint16_t* wrows = reinterpret_cast<const uint16_t*>(smem + L.rows);
         // logits from the staged (exact, chunk-scaled f16) x, one warp per
         // (row, token): lane l takes the 32-value chunks l, l + 32, ...; each
@@ -441,7 +452,10 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 const int ch = lane + 32 * m;
                 float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
+                for (int w0 = 0; w0 < 4; ++w0) {
+                    // lanes 2i, 2i + 1 start at word i % 4 of their 64-byte chunk,
+                    // so that a wavefront's eight 16-byte reads hit distinct banks
+                    const int w = (w0 + (lane >> 1)) & 3;
                     const uint4 xv = xb[(m * 4 + w) * 32], wq = wv[4 * ch + w];
                     const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
@@ -458,7 +472,9 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             if (lane == 0) a.scores[(size_t)t * E + r0 + r] = sigmoid_score(v, a.bias, r0 + r);
         }
         __syncthreads();
+        FLINT_PHASE(36);
         if (tid == 0 && ok && !withhold) release_add_gpu(a.hdr + kHdrScoresIn, (uint32_t)nrr);
+        FLINT_PHASE(37);
 #ifdef FLINT_PHASE_TRACE
         if (tid == 0) sm.trace[26] = globaltimer_ns();
 #endif
@@ -475,16 +491,13 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             sm.fail)
             return false;
         FLINT_PHASE(stamp);
-        uint32_t* sc = reinterpret_cast<uint32_t*>(smem + L.rows);  // the router rows are dead
-        for (int i = tid; i < T * E; i += kLT) sc[i] = (uint32_t)ld_cg(reinterpret_cast<const int32_t*>(a.scores) + i);
-        __syncthreads();
         FLINT_PHASE(stamp + 1);
-        if (warp < T) {
+        if (warp < T) {  // each token's scores read from L2 by its warp
+            const uint32_t* sc = a.scores + (size_t)warp * E;
             if (E <= 256)
-                topk_warp<8>(sc + (size_t)warp * E, E, k, lane, sm.ids + warp * k, sm.w + warp * k);
+                topk_warp<8, true>(sc, E, k, lane, sm.ids + warp * k, sm.w + warp * k);
             else
-                topk_warp<FLINT_MAX_EXPERTS / 32>(sc + (size_t)warp * E, E, k, lane, sm.ids + warp * k,
-                                                  sm.w + warp * k);
+                topk_warp<FLINT_MAX_EXPERTS / 32, true>(sc, E, k, lane, sm.ids + warp * k, sm.w + warp * k);
         }
         __syncthreads();
         FLINT_PHASE(stamp + 2);
@@ -533,40 +546,44 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                     build_segs(sm, p0, p1, I, b0, b1, NB, a.status, false, rows_per_item(RSr, (b1 - b0) * kRowBlock));
                 FLINT_PHASE(19);
             }
+            // the segments are in; the tensor scales of all routed experts too
+            // (copied before the PDL wait; the CTAs with router rows waited for
+            // them already)
+            if (ts_bulk && nrr == 0 && !mbar_wait_bounded(&sm.rbar, 0, a.status, kStatusTimeoutLayer, budget))
+                sm.fail = 1;
             __syncthreads();
+            FLINT_PHASE(38);
             count_mine();
             if (lane == 0 && !sm.fail)
                 for (int it = 0; it < NSW && it < my_g + my_d; ++it) issue(it);
-            // the tensor scales of the selected experts (copied before the wait,
-            // or read now while the weight copies are in flight)
-            const int D = ri.D;
-            if (tid < D) {
-                bool ok = true;
-                if (ts_bulk && nrr == 0) ok = mbar_wait_bounded(&sm.rbar, 0, a.status, kStatusTimeoutLayer, budget);
-                if (!ok) sm.fail = 1;
-                const int e = ri.dlist[tid];
-                sm.tsg[tid] = ts_bulk ? tsall[3 * e] : __ldg(a.ts + 3 * e);
-                sm.tsu[tid] = ts_bulk ? tsall[3 * e + 1] : __ldg(a.ts + 3 * e + 1);
-                sm.tsd[tid] = ts_bulk ? tsall[3 * e + 2] : __ldg(a.ts + 3 * e + 2);
-            }
+            FLINT_PHASE(39);
         }
-    } else if (tid == 0 && has_sh) {
-        sm.tsg[kShIdx] = __ldg(a.s_ts);
-        sm.tsu[kShIdx] = __ldg(a.s_ts + 1);
-        sm.tsd[kShIdx] = __ldg(a.s_ts + 2);
     }
-    failed = __syncthreads_or(failed || sm.fail);
+    // (no CTA barrier here: each warp goes on to its own items; `failed` is
+    // the same in every thread, and sm.fail was last set before the barrier
+    // above or is checked per item)
     FLINT_PHASE(4);
 
     // ---- 3-4: this warp's ring: gate/up items, then (h of the down experts staged) down items --
     if (failed) my_g = my_d = 0;
     bool wfail = false;  // this warp gave up on a copy
+#ifdef FLINT_PHASE_TRACE
+    unsigned long long wait_gu = 0, wait_dn = 0;  // warp 0: cycles spent waiting for item bytes
+    unsigned long long t_math = 0, t_epi = 0;      // warp 0: gate/up arithmetic; epilogue and refill
+#endif
     // Waits for item it's bytes (all lanes; false once anything failed).
     auto item_in = [&](int it) {
+#ifdef FLINT_PHASE_TRACE
+        const unsigned long long tw = clock64();
+#endif
         if (!wfail && !sm.fail) {
             if (__all_sync(full_mask, mbar_wait_bounded(wbar + it % NSW, (uint32_t)(it / NSW) & 1u, a.status,
-                                                        kStatusTimeoutLayer, budget)))
+                                                        kStatusTimeoutLayer, budget))) {
+#ifdef FLINT_PHASE_TRACE
+                (it < my_g ? wait_gu : wait_dn) += clock64() - tw;
+#endif
                 return true;
+            }
             if (lane == 0) sm.fail = 1;
         }
         wfail = true;
@@ -585,30 +602,47 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         while (s + 1 < sm.n_gseg && sm.gseg[s + 1].item0 <= m) ++s;
         const Seg sg = sm.gseg[s];
         const bool sh = sg.unit == kSharedUnit;
-        const int ui = sh ? kShIdx : sg.unit;
         const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[sg.unit];
         const uint8_t* grow = wring + (size_t)(it % NSW) * a.slot;
         float* rg = sm.res[warp][0];
         float* ru = sm.res[warp][1];
+#ifdef FLINT_PHASE_TRACE
+        const unsigned long long tm0 = clock64();
+#endif
         gate_up_item<true>(grow, grow + RS, H, xh, csc, tm, lane, rg, ru);
         __syncwarp();
-        if (lane < T && ((tm >> lane) & 1u)) {
+#ifdef FLINT_PHASE_TRACE
+        const unsigned long long tm1 = clock64();
+        t_math += tm1 - tm0;
+#endif
+        // The slot is free once the sums are out: refill it before the epilogue,
+        // whose h stores come from the top lanes (token t in lane 31 - t), so
+        // that the refilling lane 0 has no global store of its own to order
+        // behind its proxy fence.
+        item_done(it);
+        const int t = 31 - lane;
+        if (t < T && ((tm >> t) & 1u)) {
             const int p = sg.start + (m - sg.item0);
-            const float g = bf16_round_f32(sm.tsg[ui] * rg[lane]);
-            const float u = bf16_round_f32(sm.tsu[ui] * ru[lane]);
+            const float g = bf16_round_f32(tscale(sh, sg.unit, 0) * rg[t]);
+            const float u = bf16_round_f32(tscale(sh, sg.unit, 1) * ru[t]);
             const uint16_t hv = f32_to_bf16_bits(silu_f32(g) * u);
             if (sh) {
-                a.h_shared[(size_t)lane * Is + p] = hv;
+                a.h_shared[(size_t)t * Is + p] = hv;
             } else {
-                const int j = __ffs(rank_bits(ri.dmask[sg.unit], lane)) - 1;
-                a.h_routed[((size_t)lane * k + j) * I + p] = hv;
+                const int j = __ffs(rank_bits(ri.dmask[sg.unit], t)) - 1;
+                a.h_routed[((size_t)t * k + j) * I + p] = hv;
             }
         }
-        item_done(it);
+#ifdef FLINT_PHASE_TRACE
+        t_epi += clock64() - tm1;
+#endif
     }
+#ifdef FLINT_PHASE_TRACE
+    if (lane == 0) sm.wend[warp] = clock64();
+#endif
     // Publish this CTA's h: per expert, the number of its pairs done here.
     if (__syncthreads_or(wfail) && tid == 0) sm.fail = 1;
-    if (tid == 0 && !sm.fail && !failed)
+    if (tid == 0 && !sm.fail && !failed && !withhold)
         for (int s = 0; s < sm.n_gseg; ++s) {
             const int unit = sm.gseg[s].unit;
             release_add_gpu(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit), (uint32_t)sm.gseg[s].count);
@@ -686,13 +720,12 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         while (s + 1 < sm.n_dseg && sm.dseg[s + 1].item0 <= m) ++s;
         const Seg sg = sm.dseg[s];
         const bool sh = sg.unit == kSharedUnit;
-        const int ui = sh ? kShIdx : sg.unit;
         const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[sg.unit];
         const int row0 = sg.start + (m - sg.item0) * sg.rg;
         const int nrw = min((int)sg.rg, sg.start + sg.count - row0);
         const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
         const uint8_t* rows = wring + (size_t)(it % NSW) * a.slot;
-        const float tsd = sm.tsd[ui];
+        const float tsd = tscale(sh, sg.unit, 2);
         const unsigned long long dm = sh ? 0ull : ri.dmask[sg.unit];
         auto vec = [&](int t, const uint4*& hv, const float*& cv) {
             const int v = sm.vec[sg.q][t];
@@ -720,7 +753,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 down_pass<RP, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
                 const float v = reduce_scatter<2 * RP>(acc, lane);
                 const int idx = rs_index<2 * RP>(lane), r = idx % RP;
-                if (lane % (16 / RP) == 0 && r < nrw) put(v, r, idx >= RP ? t1 : t0);
+                if (lane % (16 / RP) == 16 / RP - 1 && r < nrw) put(v, r, idx >= RP ? t1 : t0);
             } else {
                 const uint4* hv[1];
                 const float* cv[1];
@@ -729,7 +762,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 down_pass<RP, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
                 const float v = reduce_scatter<RP>(acc, lane);
                 const int r = rs_index<RP>(lane);
-                if (lane % (32 / RP) == 0 && r < nrw) put(v, r, t0);
+                if (lane % (32 / RP) == 32 / RP - 1 && r < nrw) put(v, r, t0);
             }
         };
         uint32_t rest = tm;
@@ -741,10 +774,9 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 t1 = __ffs(rest) - 1;
                 rest &= rest - 1u;
             }
-            if (sg.rg <= 4)
-                rows_pass(std::integral_constant<int, 4>(), t0, t1);
-            else
-                rows_pass(std::integral_constant<int, 8>(), t0, t1);
+            // one instantiation (rows past nrw are skipped inside); a second,
+            // 4-row one measured slower (register spills)
+            rows_pass(std::integral_constant<int, 8>(), t0, t1);
         }
         item_done(it);
     }
@@ -813,9 +845,23 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     __syncthreads();
     FLINT_PHASE(10);
 #ifdef FLINT_PHASE_TRACE
+    if (tid == 0) {
+        sm.trace[20] = wait_gu;
+        sm.trace[21] = t_math;
+        sm.trace[22] = t_epi;
+        sm.trace[23] = (unsigned long long)my_g | ((unsigned long long)my_d << 16) | (wait_dn << 32);
+        unsigned long long lo = ~0ull, hi = 0;
+        for (int w = 0; w < kLW; ++w) {
+            lo = min(lo, sm.wend[w]);
+            hi = max(hi, sm.wend[w]);
+        }
+        sm.trace[24] = lo;
+        sm.trace[25] = hi;
+    }
     if (tid == 0 && c < kTraceCtas) {
         unsigned long long* dst = g_phase_trace[sm.hdr[kHdrCalls] % kTraceCalls][c];
         for (int i = 0; i < 27; ++i) dst[i] = sm.trace[i];
+        for (int i = 32; i < kTraceStamps; ++i) dst[i] = sm.trace[i];
         uint32_t smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
         dst[27] = smid;

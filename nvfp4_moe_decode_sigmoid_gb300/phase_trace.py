@@ -49,7 +49,7 @@ INTERVALS = [("wait for the previous call", 0, 1, "all"), ("x staged", 1, 2, "al
              ("at the end: top-k", 16, 17, "shared"), ("at the end: routing view", 17, 18, "shared"),
              ("arrivals", 18, 9, "shared"), ("arrivals", 8, 9, "routed"), ("combine", 9, 10, "all"),
              ("after the wait, to the end", 1, 10, "all")]
-N_STAMPS, N_CALLS, N_CTAS = 32, 64, 256
+N_STAMPS, N_CALLS, N_CTAS = 40, 64, 256
 
 
 def main(argv=None):
@@ -62,6 +62,7 @@ def main(argv=None):
     p.add_argument("--experts", type=int, default=256)
     p.add_argument("--inter", type=int, default=512)
     p.add_argument("--top-k", type=int, default=6)
+    p.add_argument("--dump", default=None, help="also save the raw stamps ([calls][CTAs][stamps]) to this .npy file")
     args = p.parse_args(argv)
 
     from . import _build
@@ -117,6 +118,8 @@ def main(argv=None):
     tr = buf.reshape(N_CALLS, N_CTAS, N_STAMPS).astype(np.int64)
     G = torch.cuda.get_device_properties(0).multi_processor_count
     tr = tr[:, :G]
+    if args.dump:
+        np.save(args.dump, tr)
     calls = [c for c in range(N_CALLS) if np.all(tr[c, :, 31] == tr[c, 0, 31]) and tr[c, 0, 31] > 0]
     shared_role = (tr[:, :, 28] & 0xFF) == 1
     cells = {}  # (role, interval) -> list of cycles
@@ -144,6 +147,20 @@ def main(argv=None):
             row.append(f"{statistics.median(v) / 1e3:.2f} / {max(v) / 1e3:.2f}" if v else "-")
         if row != ["-", "-"]:
             print(f"| {name} | {row[0]} | {row[1]} |")
+    # warp 0 of each CTA: its gate/up items' waits for bytes, arithmetic, epilogue and refill; the
+    # spread of the warps' ends of the gate/up loop
+    med = lambda v: statistics.median(v) / 1e3
+    for role in ("shared", "routed"):
+        sel = [tr[c, cta] for c in calls for cta in range(G) if (role == "shared") == bool(shared_role[c, cta])]
+        if not sel:
+            continue
+        print(f"\n{role}, warp 0 over its {statistics.median([int(st[23]) & 0xFFFF for st in sel]):.0f} gate/up "
+              f"items (median kcycles): waits {med([int(st[20]) for st in sel]):.2f}, arithmetic "
+              f"{med([int(st[21]) for st in sel]):.2f}, epilogue and refill {med([int(st[22]) for st in sel]):.2f}; "
+              f"over its {statistics.median([(int(st[23]) >> 16) & 0xFFFF for st in sel]):.0f} down items waits "
+              f"{med([int(st[23]) >> 32 for st in sel]):.2f}; warps' gate/up ends: last - first "
+              f"{med([int(st[25] - st[24]) for st in sel]):.2f}, last - stamp 5 "
+              f"{med([int(st[25] - st[5]) for st in sel if st[5]]):.2f}")
     n_sh = int(shared_role[calls[0]].sum())
     print(f"\nCTAs: {n_sh} shared, {G - n_sh} routed. On the global timer (coarse), median over the calls: "
           f"call span (first entry to last end, with the wait for the previous call) "

@@ -48,7 +48,7 @@ def test_fused_layer_lost_cta_times_out_and_the_workspace_recovers():
         f.flint_moe_layer(xc, dl.router_w, k, dl.routed, dl.shared, ids, w, y, ws)
 
     f.flint_workspace_set_wait_budget(ws, 2000)  # 2 ms
-    f.flint_selftest_lose_cta(ws, 0)             # CTA 0 holds router rows
+    f.flint_selftest_lose_cta(ws, 0)             # CTA 0 (a shared-expert CTA) publishes nothing
     call()
     torch.cuda.synchronize()
     call()                                       # before the check: returns at once
