@@ -107,7 +107,6 @@ struct LayerSmall {
     int16_t v_q[kMaxVec], v_t[kMaxVec];
     float w[kMaxDistinct];
     int32_t ids[kMaxDistinct];
-    int32_t cumw[2 * 32];            // inclusive prefix of the experts' cost weights
     float res[kLW][2][FLINT_MAX_TOKENS];  // a warp's raw gate / up sums per token
     float ninv[FLINT_MAX_TOKENS];
     int16_t last[kLayerMaxHidden / kRowBlock];  // row blocks this CTA combines
@@ -172,19 +171,22 @@ __device__ __forceinline__ bool cta_wait_count(const uint32_t* p, uint32_t targe
     return *s_ok != 0;
 }
 
-// The routing view (the distinct selected experts in ascending order, and
+// The routing view (the distinct selected experts in ascending id order, and
 // per expert which ranks of which tokens chose it) built by one warp from the
 // T x k ids in shared memory (every id valid, distinct within a token, E <=
-// 1024): lane l owns the bitmap word of experts 32 l .. 32 l + 31.
+// 1024, T k <= 64): lane l holds ids l and l + 32 and marks them in a bitmap
+// of 32 words (word w: experts 32 w .. 32 w + 31); the prefix popcounts of the
+// words give each selected expert its dense index.
 __device__ void route_view_warp(RouteInfo& ri, const int32_t* ids, int T, int k, int lane) {
     const uint32_t full = 0xffffffffu;
     const int n = T * k;
-    uint32_t word = 0;
-    for (int i = 0; i < n; ++i) {
-        const int e = ids[i];
-        if ((e >> 5) == lane) word |= 1u << (e & 31);
-    }
-    const uint32_t cnt = __popc(word);
+    const int e0 = lane < n ? ids[lane] : -1, e1 = lane + 32 < n ? ids[lane + 32] : -1;
+    ri.bitmap[lane] = 0u;
+    __syncwarp();
+    if (e0 >= 0) atomicOr(&ri.bitmap[e0 >> 5], 1u << (e0 & 31));
+    if (e1 >= 0) atomicOr(&ri.bitmap[e1 >> 5], 1u << (e1 & 31));
+    __syncwarp();
+    const uint32_t word = ri.bitmap[lane], cnt = __popc(word);
     uint32_t incl = cnt;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -193,48 +195,90 @@ __device__ void route_view_warp(RouteInfo& ri, const int32_t* ids, int T, int k,
     }
     const uint32_t base = incl - cnt;
     const int D = (int)__shfl_sync(full, incl, 31);
-    for (uint32_t w = word, d = base; w; w &= w - 1u, ++d) ri.dlist[d] = 32 * lane + __ffs(w) - 1;
-    for (int d = lane; d < D; d += 32) {
-        ri.dmask[d] = 0ull;
-        ri.tmask[d] = 0u;
+    auto dense = [&](int e) {  // every lane calls it (shuffles)
+        const int src = e >= 0 ? e >> 5 : 0;
+        const uint32_t bw = __shfl_sync(full, word, src), bb = __shfl_sync(full, base, src);
+        return e >= 0 ? (int)(bb + __popc(bw & ((1u << (e & 31)) - 1u))) : -1;
+    };
+    const int d0 = dense(e0), d1 = dense(e1);
+    if (lane < D) {
+        ri.dmask[lane] = 0ull;
+        ri.tmask[lane] = 0u;
+    }
+    if (lane + 32 < D) {
+        ri.dmask[lane + 32] = 0ull;
+        ri.tmask[lane + 32] = 0u;
     }
     __syncwarp();
-    for (int i0 = 0; i0 < n; i0 += 32) {
-        const int i = i0 + lane;
-        const int e = i < n ? ids[i] : 0;
-        const uint32_t bw = __shfl_sync(full, word, e >> 5), bb = __shfl_sync(full, base, e >> 5);
-        if (i < n) {
-            const int d = (int)(bb + __popc(bw & ((1u << (e & 31)) - 1u)));
-            const int t = i / k, j = i - t * k;
-            atomicOr(&ri.dmask[d], 1ull << (8 * t + j));
-            atomicOr(&ri.tmask[d], 1u << t);
-            ri.ids[i] = e;
-        }
-    }
+    auto mark = [&](int i, int e, int d) {
+        if (e < 0) return;
+        const int t = i / k, j = i - t * k;
+        ri.dlist[d] = e;  // (every lane holding e writes the same value)
+        atomicOr(&ri.dmask[d], 1ull << (8 * t + j));
+        atomicOr(&ri.tmask[d], 1u << t);
+        ri.ids[i] = e;
+    };
+    mark(lane, e0, d0);
+    mark(lane + 32, e1, d1);
     if (lane == 0) ri.D = D;
     __syncwarp();
 }
 
-// Position, in the concatenation of D experts of `per` items each, of the
-// cost target tau, where an item of expert u costs w_u and cum[u] is the
-// inclusive prefix of the w_u: the experts before the one that holds tau,
-// plus the items of that expert whose cost lies below tau (rounded up).
-// Monotone in tau, pos(0) = 0, pos(per * cum[D - 1]) = D * per, so the ranges
-// [pos(c total / G'), pos((c + 1) total / G')) tile the items exactly.
-// (32-bit arithmetic: per * cum[D - 1] * (G' + 1) < 2^32 for the shapes the
-// host accepts.)
-__device__ __forceinline__ int cost_pos(uint32_t tau, const int32_t* cum, int D, int per) {
-    int lo = 0, hi = D;  // first expert u with per * cum[u] > tau
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if ((uint32_t)per * (uint32_t)cum[mid] > tau) hi = mid;
-        else lo = mid + 1;
+// This routed CTA's share of the D selected experts (one warp, after
+// route_view_warp): the concatenation of the experts' items (per of each) is
+// cut where the cumulative cost reaches the CTA's equal shares, an item of
+// expert u costing w_u = 4 + 3 x its tokens (its decode once, a multiply-add
+// per token). pos(tau) is the number of items whose cost starts below tau:
+// the experts u with per cum[u] <= tau (cum: inclusive prefix of w) and the
+// first ceil((tau - per cum[u - 1]) / w_u) items of the next one. Monotone in
+// tau, pos(0) = 0, pos(per cum[D - 1]) = D per, so the CTAs' ranges tile the
+// items exactly. Lane u holds cum[u] and cum[u + 32]; the search is two
+// ballots. Returns (lo, hi) of share `cr` of `Gr` in lanes 0 and 1.
+// (32-bit arithmetic: per cum[D - 1] (Gr + 1) < 2^32 for the shapes the host
+// accepts.)
+__device__ __forceinline__ void cost_split_warp(const RouteInfo& ri, int per_a, int per_b, uint32_t cr, uint32_t Gr,
+                                                int lane, int& a0, int& a1, int& b0, int& b1) {
+    const uint32_t full = 0xffffffffu;
+    const int D = ri.D;
+    uint32_t ca = lane < D ? 4u + 3u * __popc(ri.tmask[lane]) : 0u;
+    uint32_t cb = lane + 32 < D ? 4u + 3u * __popc(ri.tmask[lane + 32]) : 0u;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t va = __shfl_up_sync(full, ca, off), vb = __shfl_up_sync(full, cb, off);
+        if (lane >= off) {
+            ca += va;
+            cb += vb;
+        }
     }
-    if (lo >= D) return D * per;
-    const uint32_t before = lo ? (uint32_t)per * (uint32_t)cum[lo - 1] : 0u;
-    const uint32_t wu = (uint32_t)(cum[lo] - (lo ? cum[lo - 1] : 0));
-    const uint32_t p = (tau - before + wu - 1u) / wu;
-    return lo * per + (int)(p < (uint32_t)per ? p : (uint32_t)per);
+    cb += __shfl_sync(full, ca, 31);
+    const uint32_t Wt = __shfl_sync(full, cb, 31);
+    // lane q < 4 takes cut q: gate/up lo, hi; down lo, hi (the divisions in
+    // parallel, the searches one after the other)
+    const int q = lane & 3;
+    const uint32_t per = (uint32_t)(q < 2 ? per_a : per_b);
+    const uint32_t tau = (cr + (uint32_t)(q & 1)) * (Wt * per) / Gr;
+    int lo = D;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t ti = __shfl_sync(full, tau, i), pi = (uint32_t)(i < 2 ? per_a : per_b);
+        const uint32_t ma = __ballot_sync(full, lane < D && pi * ca > ti);
+        const uint32_t mb = __ballot_sync(full, lane + 32 < D && pi * cb > ti);
+        if (q == i) lo = ma ? __ffs(ma) - 1 : (mb ? 31 + __ffs(mb) : D);
+    }
+    // cum[lo] and cum[lo - 1] (each lane its own source)
+    const int s1 = lo < D ? lo : 0, s0 = lo > 0 && lo < D ? lo - 1 : 0;
+    const uint32_t x1 = __shfl_sync(full, ca, s1 & 31), y1 = __shfl_sync(full, cb, s1 & 31);
+    const uint32_t x0 = __shfl_sync(full, ca, s0 & 31), y0 = __shfl_sync(full, cb, s0 & 31);
+    int r = D * (int)per;
+    if (lo < D) {
+        const uint32_t cl = s1 < 32 ? x1 : y1, cp = lo ? (s0 < 32 ? x0 : y0) : 0u;
+        const uint32_t wu = cl - cp, n = (tau - per * cp + wu - 1u) / wu;
+        r = lo * (int)per + (int)(n < per ? n : per);
+    }
+    a0 = __shfl_sync(full, r, 0);
+    a1 = __shfl_sync(full, r, 1);
+    b0 = __shfl_sync(full, r, 2);
+    b1 = __shfl_sync(full, r, 3);
 }
 
 // The runs of the pair range [p0, p1) and of the down block range [b0, b1)
@@ -244,8 +288,7 @@ __device__ __forceinline__ int cost_pos(uint32_t tau, const int32_t* cum, int D,
 __device__ void build_segs(LayerSmall& sm, int p0, int p1, int per_gu, int b0, int b1, int NB, uint32_t* status,
                            bool shared, int rg) {
     int n = 0;
-    for (int P = p0; P < p1;) {
-        const int u = P / per_gu, p = P - u * per_gu;
+    for (int P = p0, u = p0 / per_gu, p = p0 - u * per_gu; P < p1; ++u, p = 0) {
         const int m = min(p1 - P, per_gu - p);
         if (n == kMaxSegs) {
             sm.fail = 1;  // the host sizes the grid so that this cannot happen
@@ -258,8 +301,7 @@ __device__ void build_segs(LayerSmall& sm, int p0, int p1, int per_gu, int b0, i
     sm.n_gseg = n;
     sm.n_gi = p1 > p0 ? p1 - p0 : 0;
     int nd = 0, items = 0;
-    for (int B = b0; B < b1;) {
-        const int u = B / NB, b = B - u * NB;
+    for (int B = b0, u = b0 / NB, b = b0 - u * NB; B < b1; ++u, b = 0) {
         const int take = min(b1 - B, NB - b);
         if (nd == kMaxDownUnits) {
             sm.fail = 1;
@@ -517,31 +559,8 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             if (warp == 0) {
                 route_view_warp(ri, sm.ids, T, k, lane);
                 FLINT_PHASE(14);
-                const int D = ri.D;
-                // cost weight of an expert: 4 + 3 x the tokens that chose it
-                for (int base = 0; base < D; base += 32) {
-                    const int u = base + lane;
-                    int v = u < D ? 4 + 3 * __popc(ri.tmask[u]) : 0;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const int n = __shfl_up_sync(full_mask, v, off);
-                        if (lane >= off) v += n;
-                    }
-                    if (base) v += sm.cumw[base - 1];
-                    if (u < D) sm.cumw[u] = v;
-                    __syncwarp();
-                }
-                const uint32_t Gr = (uint32_t)(G - Gs), cr = (uint32_t)(c - Gs);
-                const uint32_t Wt = (uint32_t)sm.cumw[D - 1];
-                int pos = 0;
-                if (lane < 4) {  // gate/up lo, hi; down lo, hi
-                    const int per = lane < 2 ? I : NB;
-                    const uint32_t tot = Wt * (uint32_t)per;
-                    const uint32_t tau = (cr + (uint32_t)(lane & 1)) * tot / Gr;
-                    pos = cost_pos(tau, sm.cumw, D, per);
-                }
-                const int p0 = __shfl_sync(full_mask, pos, 0), p1 = __shfl_sync(full_mask, pos, 1);
-                const int b0 = __shfl_sync(full_mask, pos, 2), b1 = __shfl_sync(full_mask, pos, 3);
+                int p0, p1, b0, b1;
+                cost_split_warp(ri, I, NB, (uint32_t)(c - Gs), (uint32_t)(G - Gs), lane, p0, p1, b0, b1);
                 if (lane == 0)
                     build_segs(sm, p0, p1, I, b0, b1, NB, a.status, false, rows_per_item(RSr, (b1 - b0) * kRowBlock));
                 FLINT_PHASE(19);
