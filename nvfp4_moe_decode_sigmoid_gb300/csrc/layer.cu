@@ -145,9 +145,15 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v
     return old;
 }
 // Publishes the CTA's earlier writes (ordered before this thread by a
-// __syncthreads) and adds v to a counter at GPU scope.
+// __syncthreads) and adds v to a counter at GPU scope: the fence, then the
+// relaxed add (several adds may follow one fence).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void red_add_relaxed_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ void release_add_gpu(uint32_t* p, uint32_t v) {
-    asm volatile("fence.acq_rel.gpu;\n red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    fence_acq_rel_gpu();
+    red_add_relaxed_gpu(p, v);
 }
 // Thread 0 waits until *p >= target (acquire), for at most budget_ns; the
 // result reaches every thread of the CTA. `code` goes to *status on expiry.
@@ -237,7 +243,7 @@ __device__ void route_view_warp(RouteInfo& ri, const int32_t* ids, int T, int k,
 // (32-bit arithmetic: per cum[D - 1] (Gr + 1) < 2^32 for the shapes the host
 // accepts.)
 __device__ __forceinline__ void cost_split_warp(const RouteInfo& ri, int per_a, int per_b, uint32_t cr, uint32_t Gr,
-                                                int lane, int& a0, int& a1, int& b0, int& b1) {
+                                                int lane, int& a0, int& a1, int& b0, int& b1, int& ua0, int& ub0) {
     const uint32_t full = 0xffffffffu;
     const int D = ri.D;
     uint32_t ca = lane < D ? 4u + 3u * __popc(ri.tmask[lane]) : 0u;
@@ -269,12 +275,15 @@ __device__ __forceinline__ void cost_split_warp(const RouteInfo& ri, int per_a, 
     const int s1 = lo < D ? lo : 0, s0 = lo > 0 && lo < D ? lo - 1 : 0;
     const uint32_t x1 = __shfl_sync(full, ca, s1 & 31), y1 = __shfl_sync(full, cb, s1 & 31);
     const uint32_t x0 = __shfl_sync(full, ca, s0 & 31), y0 = __shfl_sync(full, cb, s0 & 31);
-    int r = D * (int)per;
+    int r = D * (int)per, u = D;  // the cut, and the expert it falls in
     if (lo < D) {
         const uint32_t cl = s1 < 32 ? x1 : y1, cp = lo ? (s0 < 32 ? x0 : y0) : 0u;
         const uint32_t wu = cl - cp, n = (tau - per * cp + wu - 1u) / wu;
         r = lo * (int)per + (int)(n < per ? n : per);
+        u = n < per ? lo : lo + 1;
     }
+    ua0 = __shfl_sync(full, u, 0);
+    ub0 = __shfl_sync(full, u, 2);
     a0 = __shfl_sync(full, r, 0);
     a1 = __shfl_sync(full, r, 1);
     b0 = __shfl_sync(full, r, 2);
@@ -285,10 +294,11 @@ __device__ __forceinline__ void cost_split_warp(const RouteInfo& ri, int per_a, 
 // (items of a concatenation of experts of per_gu pairs / NB blocks: the
 // routed experts in list order, or the shared expert alone); a down item
 // takes rg rows. One thread.
-__device__ void build_segs(LayerSmall& sm, int p0, int p1, int per_gu, int b0, int b1, int NB, uint32_t* status,
-                           bool shared, int rg) {
+__device__ void build_segs(LayerSmall& sm, int p0, int up0, int p1, int per_gu, int b0, int ub0, int b1, int NB,
+                           uint32_t* status, bool shared, int rg) {
+    // up0, ub0: the experts that p0 and b0 fall in (p0 / per_gu, b0 / NB)
     int n = 0;
-    for (int P = p0, u = p0 / per_gu, p = p0 - u * per_gu; P < p1; ++u, p = 0) {
+    for (int P = p0, u = up0, p = p0 - u * per_gu; P < p1; ++u, p = 0) {
         const int m = min(p1 - P, per_gu - p);
         if (n == kMaxSegs) {
             sm.fail = 1;  // the host sizes the grid so that this cannot happen
@@ -301,7 +311,8 @@ __device__ void build_segs(LayerSmall& sm, int p0, int p1, int per_gu, int b0, i
     sm.n_gseg = n;
     sm.n_gi = p1 > p0 ? p1 - p0 : 0;
     int nd = 0, items = 0;
-    for (int B = b0, u = b0 / NB, b = b0 - u * NB; B < b1; ++u, b = 0) {
+    const int rg_log2 = __ffs(rg) - 1;  // rg is a power of two
+    for (int B = b0, u = ub0, b = b0 - u * NB; B < b1; ++u, b = 0) {
         const int take = min(b1 - B, NB - b);
         if (nd == kMaxDownUnits) {
             sm.fail = 1;
@@ -310,7 +321,7 @@ __device__ void build_segs(LayerSmall& sm, int p0, int p1, int per_gu, int b0, i
         }
         const int rows = take * kRowBlock;
         sm.dseg[nd] = Seg{(int16_t)(shared ? kSharedUnit : u), (int8_t)nd, (int8_t)rg, items, b * kRowBlock, rows};
-        items += (rows + rg - 1) / rg;
+        items += (rows + rg - 1) >> rg_log2;
         ++nd;
         B += take;
     }
@@ -434,7 +445,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             // the shared expert: an even split of its pairs and row blocks
             const int p0 = (int)((long long)c * Is / Gs), p1 = (int)((long long)(c + 1) * Is / Gs);
             const int b0 = (int)((long long)c * NB / Gs), b1 = (int)((long long)(c + 1) * NB / Gs);
-            build_segs(sm, p0, p1, Is, b0, b1, NB, a.status, true, rows_per_item(RSs, (b1 - b0) * kRowBlock));
+            build_segs(sm, p0, 0, p1, Is, b0, 0, b1, NB, a.status, true, rows_per_item(RSs, (b1 - b0) * kRowBlock));
         }
     }
     if (tid <= kLW * NSW) fence_mbar_init();
@@ -559,10 +570,11 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             if (warp == 0) {
                 route_view_warp(ri, sm.ids, T, k, lane);
                 FLINT_PHASE(14);
-                int p0, p1, b0, b1;
-                cost_split_warp(ri, I, NB, (uint32_t)(c - Gs), (uint32_t)(G - Gs), lane, p0, p1, b0, b1);
+                int p0, p1, b0, b1, up0, ub0;
+                cost_split_warp(ri, I, NB, (uint32_t)(c - Gs), (uint32_t)(G - Gs), lane, p0, p1, b0, b1, up0, ub0);
                 if (lane == 0)
-                    build_segs(sm, p0, p1, I, b0, b1, NB, a.status, false, rows_per_item(RSr, (b1 - b0) * kRowBlock));
+                    build_segs(sm, p0, up0, p1, I, b0, ub0, b1, NB, a.status, false,
+                               rows_per_item(RSr, (b1 - b0) * kRowBlock));
                 FLINT_PHASE(19);
             }
             // the segments are in; the tensor scales of all routed experts too
@@ -661,11 +673,13 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 #endif
     // Publish this CTA's h: per expert, the number of its pairs done here.
     if (__syncthreads_or(wfail) && tid == 0) sm.fail = 1;
-    if (tid == 0 && !sm.fail && !failed && !withhold)
+    if (tid == 0 && !sm.fail && !failed && !withhold && sm.n_gseg > 0) {
+        fence_acq_rel_gpu();  // one fence for all of them
         for (int s = 0; s < sm.n_gseg; ++s) {
             const int unit = sm.gseg[s].unit;
-            release_add_gpu(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit), (uint32_t)sm.gseg[s].count);
+            red_add_relaxed_gpu(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit), (uint32_t)sm.gseg[s].count);
         }
+    }
     FLINT_PHASE(6);
     if (!failed && sm.n_di > 0) {
         // Stage h of this CTA's down experts once every pair of each is published.
