@@ -39,6 +39,7 @@
 // are left mid-call and the workspace must be re-initialised
 // (flint_workspace_check does it); until then every call returns at once,
 // leaving its outputs unwritten, and the status stays set.
+#include <climits>
 #include <type_traits>
 
 #include "expert_common.cuh"
@@ -68,6 +69,7 @@ __device__ unsigned long long g_phase_trace[kTraceCalls][kTraceCtas][kTraceStamp
 constexpr int kLW = kLayerWarps;
 constexpr int kLT = kLayerThreads;
 constexpr int kMaxSegs = 4;
+constexpr int kEpiBatch = 8;  // gate/up items per epilogue pass of a warp
 constexpr int kMaxDownUnits = 4;
 constexpr int kMaxVec = kMaxDownUnits * FLINT_MAX_TOKENS;
 constexpr int kRowBlock = 16;                 // output rows per combine block
@@ -107,7 +109,11 @@ struct LayerSmall {
     int16_t v_q[kMaxVec], v_t[kMaxVec];
     float w[kMaxDistinct];
     int32_t ids[kMaxDistinct];
-    float res[kLW][2][FLINT_MAX_TOKENS];  // a warp's raw gate / up sums per token
+    // a warp's raw gate / up sums of its last items (per token), and per item
+    // its pair (below 2^16: a slot holds a down row of I values, so I < 2 H <=
+    // 16384), unit (kShIdx: the shared expert) and token mask
+    float gres[kLW][kEpiBatch][2][FLINT_MAX_TOKENS];
+    uint32_t gkey[kLW][kEpiBatch];
     float ninv[FLINT_MAX_TOKENS];
     int16_t last[kLayerMaxHidden / kRowBlock];  // row blocks this CTA combines
 #ifdef FLINT_PHASE_TRACE
@@ -625,49 +631,65 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         __syncwarp();
         if (lane == 0 && it + NSW < my_g + my_d && !sm.fail) issue(it + NSW);
     };
-    for (int it = 0; it < my_g; ++it) {
-        if (!item_in(it)) break;
-        if (it == 0) FLINT_PHASE(5);
-        const int m = warp + it * kLW;
-        int s = 0;
-        while (s + 1 < sm.n_gseg && sm.gseg[s + 1].item0 <= m) ++s;
-        const Seg sg = sm.gseg[s];
-        const bool sh = sg.unit == kSharedUnit;
-        const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[sg.unit];
-        const uint8_t* grow = wring + (size_t)(it % NSW) * a.slot;
-        float* rg = sm.res[warp][0];
-        float* ru = sm.res[warp][1];
-#ifdef FLINT_PHASE_TRACE
-        const unsigned long long tm0 = clock64();
-#endif
-        gate_up_item<true>(grow, grow + RS, H, xh, csc, tm, lane, rg, ru);
+    // The epilogue of a warp's buffered items, one (item, token) per lane:
+    // h = bf16(silu(bf16(ts_g g)) bf16(ts_u u)).
+    int nb = 0;
+    auto epilogue = [&]() {
         __syncwarp();
-#ifdef FLINT_PHASE_TRACE
-        const unsigned long long tm1 = clock64();
-        t_math += tm1 - tm0;
-#endif
-        // The slot is free once the sums are out: refill it before the epilogue,
-        // whose h stores come from the top lanes (token t in lane 31 - t), so
-        // that the refilling lane 0 has no global store of its own to order
-        // behind its proxy fence.
-        item_done(it);
-        const int t = 31 - lane;
-        if (t < T && ((tm >> t) & 1u)) {
-            const int p = sg.start + (m - sg.item0);
-            const float g = bf16_round_f32(tscale(sh, sg.unit, 0) * rg[t]);
-            const float u = bf16_round_f32(tscale(sh, sg.unit, 1) * ru[t]);
+        for (int e = lane; e < nb * FLINT_MAX_TOKENS; e += 32) {
+            const int b = e / FLINT_MAX_TOKENS, t = e % FLINT_MAX_TOKENS;
+            const uint32_t key = sm.gkey[warp][b];
+            if (!((key >> (24 + t)) & 1u)) continue;
+            const int p = (int)(key & 0xFFFFu), ui = (int)((key >> 16) & 0xFFu);
+            const bool sh = ui == kShIdx;
+            const float g = bf16_round_f32(tscale(sh, ui, 0) * sm.gres[warp][b][0][t]);
+            const float u = bf16_round_f32(tscale(sh, ui, 1) * sm.gres[warp][b][1][t]);
             const uint16_t hv = f32_to_bf16_bits(silu_f32(g) * u);
             if (sh) {
                 a.h_shared[(size_t)t * Is + p] = hv;
             } else {
-                const int j = __ffs(rank_bits(ri.dmask[sg.unit], t)) - 1;
+                const int j = __ffs(rank_bits(ri.dmask[ui], t)) - 1;
                 a.h_routed[((size_t)t * k + j) * I + p] = hv;
             }
         }
+        __syncwarp();
+        nb = 0;
+    };
+    // the run the current item falls in, kept from one item to the next
+    int cg_s = -1, cg_next = 0, cg_start = 0, cg_item0 = 0, cg_ui = 0;
+    uint32_t cg_tm = 0;
+    for (int it = 0; it < my_g; ++it) {
+        if (!item_in(it)) break;
+        if (it == 0) FLINT_PHASE(5);
+        const int m = warp + it * kLW;
+        while (m >= cg_next) {
+            const Seg sg = sm.gseg[++cg_s];
+            cg_next = cg_s + 1 < sm.n_gseg ? sm.gseg[cg_s + 1].item0 : INT_MAX;
+            cg_start = sg.start;
+            cg_item0 = sg.item0;
+            const bool sh = sg.unit == kSharedUnit;
+            cg_ui = sh ? kShIdx : sg.unit;
+            cg_tm = sh ? (1u << T) - 1u : ri.tmask[sg.unit];
+        }
+        const uint8_t* grow = wring + (size_t)(it % NSW) * a.slot;
+#ifdef FLINT_PHASE_TRACE
+        const unsigned long long tm0 = clock64();
+#endif
+        gate_up_item<true>(grow, grow + RS, H, xh, csc, cg_tm, lane, sm.gres[warp][nb][0], sm.gres[warp][nb][1]);
+        if (lane == 0)
+            sm.gkey[warp][nb] = (uint32_t)(cg_start + (m - cg_item0)) | ((uint32_t)cg_ui << 16) | (cg_tm << 24);
+        ++nb;
+#ifdef FLINT_PHASE_TRACE
+        const unsigned long long tm1 = clock64();
+        t_math += tm1 - tm0;
+#endif
+        item_done(it);  // the slot is free once the sums are out
+        if (nb == kEpiBatch) epilogue();
 #ifdef FLINT_PHASE_TRACE
         t_epi += clock64() - tm1;
 #endif
     }
+    if (nb > 0) epilogue();
 #ifdef FLINT_PHASE_TRACE
     if (lane == 0) sm.wend[warp] = clock64();
 #endif
