@@ -69,7 +69,7 @@ __device__ unsigned long long g_phase_trace[kTraceCalls][kTraceCtas][kTraceStamp
 constexpr int kLW = kLayerWarps;
 constexpr int kLT = kLayerThreads;
 constexpr int kMaxSegs = 4;
-constexpr int kEpiBatch = 8;  // gate/up items per epilogue pass of a warp
+constexpr int kEpiBatch = 4;  // gate/up items per epilogue pass of a warp (8 measured slower)
 constexpr int kMaxDownUnits = 4;
 constexpr int kMaxVec = kMaxDownUnits * FLINT_MAX_TOKENS;
 constexpr int kRowBlock = 16;                 // output rows per combine block
@@ -768,20 +768,29 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         if (!__syncthreads_and(ok)) wfail = true;
     }
     FLINT_PHASE(7);
+    // the run of the current down item and what it needs, kept from one item
+    // to the next
+    int cd_s = -1, cd_next = 0;
+    Seg sg = {};
+    bool sh = false;
+    uint32_t tm = 0;
+    float tsd = 0.f;
+    unsigned long long dm = 0ull;
     for (int it = my_g; it < my_g + my_d; ++it) {
         if (!item_in(it)) break;
         const int m = warp + (it - my_g) * kLW;
-        int s = 0;
-        while (s + 1 < sm.n_dseg && sm.dseg[s + 1].item0 <= m) ++s;
-        const Seg sg = sm.dseg[s];
-        const bool sh = sg.unit == kSharedUnit;
-        const uint32_t tm = sh ? (1u << T) - 1u : ri.tmask[sg.unit];
+        while (m >= cd_next) {
+            sg = sm.dseg[++cd_s];
+            cd_next = cd_s + 1 < sm.n_dseg ? sm.dseg[cd_s + 1].item0 : INT_MAX;
+            sh = sg.unit == kSharedUnit;
+            tm = sh ? (1u << T) - 1u : ri.tmask[sg.unit];
+            tsd = tscale(sh, sg.unit, 2);
+            dm = sh ? 0ull : ri.dmask[sg.unit];
+        }
         const int row0 = sg.start + (m - sg.item0) * sg.rg;
         const int nrw = min((int)sg.rg, sg.start + sg.count - row0);
         const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
         const uint8_t* rows = wring + (size_t)(it % NSW) * a.slot;
-        const float tsd = tscale(sh, sg.unit, 2);
-        const unsigned long long dm = sh ? 0ull : ri.dmask[sg.unit];
         auto vec = [&](int t, const uint4*& hv, const float*& cv) {
             const int v = sm.vec[sg.q][t];
             hv = reinterpret_cast<const uint4*>(smem + L.xs + sm.v_off[v]);
