@@ -218,11 +218,23 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     a.slot = 2 * RS;
     const int kmax = a.I > a.Is ? a.I : a.Is;
     if (a.slot < flint::nvfp4_row_stride(kmax)) return false;
-    // staging: x, later the h of at most two routed experts (all tokens) or of the shared expert
+    // up to kLayerRowsMaxTokens tokens down is split by output rows: rg rows
+    // (a power of two up to 8) of I or Is values per ring slot
+    a.rows = T <= flint::kLayerRowsMaxTokens ? 1 : 0;
+    a.rows_max = ceil_div(H, G);
+    const int RSk = (int)flint::nvfp4_row_stride(kmax);
+    a.rg = 8;
+    while (a.rg > 1 && a.rg * RSk > a.slot) a.rg >>= 1;
+    // staging: x, later the h of at most two routed experts (all tokens) or of
+    // the shared expert; split by rows, all of h
     const size_t x_vals = 2 * (size_t)T * H, x_sc = 4 * (size_t)T * (H / 32);
     const size_t h_r = 2 * (2 * (size_t)T * a.I), h_s = 2 * (size_t)T * a.Is;  // two routed experts, or the shared one
-    const size_t h_vals = h_r > h_s ? h_r : h_s;
-    const size_t h_sc = 4 * (size_t)T * ((2 * a.I > a.Is ? 2 * a.I : a.Is) / 32);
+    size_t h_vals = h_r > h_s ? h_r : h_s;
+    size_t h_sc = 4 * (size_t)T * ((2 * a.I > a.Is ? 2 * a.I : a.Is) / 32);
+    if (a.rows) {
+        h_vals = 2 * (size_t)T * ((size_t)a.k * a.I + a.Is);
+        h_sc = 4 * (size_t)T * ((size_t)a.k * (a.I / 32) + a.Is / 32);
+    }
     a.stage_vals = (int)(x_vals > h_vals ? x_vals : h_vals);
     a.stage_scales = (int)(x_sc > h_sc ? x_sc : h_sc);
     // two ring slots per warp (three, where they fit, measured slower at 8

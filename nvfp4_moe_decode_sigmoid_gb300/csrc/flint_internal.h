@@ -46,8 +46,8 @@ constexpr size_t kWsHeader = 256;   // control words, below
 // word, the fused layer's count of completed calls and of finished CTAs, the
 // bounded waits' budget in microseconds (0: kWaitBudgetNs), a test hook
 // (c + 1: CTA c of the next fused-layer call publishes neither router scores
-// nor h counts), and
-// the fused layer's count of published router rows.
+// nor h counts), and the fused layer's counts of published router rows and
+// (one token) of gate/up pairs whose h is written (both 0 between calls).
 enum : int {
     kHdrRouteCounter = 0,
     kHdrStatus = 1,
@@ -56,6 +56,7 @@ enum : int {
     kHdrBudget = 6,
     kHdrLoseCta = 7,
     kHdrScoresIn = 8,
+    kHdrPairsIn = 9,
 };
 // Expert GEMV kernels for BF16 weights: 16 warps (a BF16 row is 4x the bytes
 // of an NVFP4 row, so fewer, larger ring slots per SM).
@@ -66,6 +67,7 @@ constexpr int kLayerWarps = 24;
 constexpr int kLayerThreads = kLayerWarps * 32;
 constexpr int kLayerSlots = 2;           // ring slots of each warp of the fused layer
 constexpr int kLayerMaxHidden = 8192;    // largest hidden size of the fused layer
+constexpr int kLayerRowsMaxTokens = 1;   // fused layer: down split by output rows up to this many tokens
 
 FLINT_HD constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -201,6 +203,9 @@ struct LayerArgs {
     int rpc;             // router rows per CTA
     int ns, slot;        // ring slots per warp (kLayerSlots) and bytes per slot
     int stage_vals, stage_scales;  // bytes of the staging region (x, later h) and of its chunk scales
+    int rows;            // down split by output rows (the ROWS instantiation)
+    int rows_max;        // ROWS: most output rows of a CTA (ceil(H / G))
+    int rg;              // ROWS: rows per down item (a power of two, at most 8)
     NormArgs norm;       // norm.r set: x = the norm of the residual stream (x unused)
 };
 

@@ -33,6 +33,13 @@
 //     each expert's down CTA writes its d rows and counts its arrival on the
 //     block's counter; the CTA that arrives last (all experts' d present)
 //     combines the block in rank order and resets the counter. Nothing waits.
+//   * One token (the ROWS instantiation): the combine's last arrivers make the
+//     call's tail, so down and the combine are split by output rows instead.
+//     CTA c owns rows [c H / G, (c + 1) H / G) of y, computes them for every
+//     selected expert and the shared one from all of h (once every pair is
+//     published: one count) and sums them in rank order in shared memory; no
+//     d leaves the CTA. (From two tokens on this measured slower: every CTA
+//     then walks the rows of every selected expert.)
 //   * The last CTA to finish resets the exchange counters for the next call.
 //
 // After a timed-out wait (or any other failure that stops a CTA) the counters
@@ -54,7 +61,7 @@ namespace {
 // the stamps to a ring of the last kTraceCalls calls, indexed by the
 // workspace's call count. The plain build has none of this code.
 #ifdef FLINT_PHASE_TRACE
-constexpr int kTraceStamps = 40, kTraceCalls = 64, kTraceCtas = 256;
+constexpr int kTraceStamps = 48, kTraceCalls = 64, kTraceCtas = 256;
 __device__ unsigned long long g_phase_trace[kTraceCalls][kTraceCtas][kTraceStamps];
 #define FLINT_PHASE(i)                                     \
     do {                                                   \
@@ -127,7 +134,7 @@ struct LayerSmall {
 // and its chunk scales, the norm's partial sums, the router rows, the warps'
 // rings.
 struct LayerSmem {
-    size_t small, ri, tsall, xs, csc, nred, rows, ring, total;
+    size_t small, ri, tsall, xs, csc, nred, rows, dres, ring, total;
 };
 
 __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
@@ -140,7 +147,10 @@ __host__ __device__ inline LayerSmem layer_layout(const LayerArgs& a) {
     L.csc = align_up(L.xs + (size_t)a.stage_vals, 128);
     L.nred = align_up(L.csc + (size_t)a.stage_scales, 128);
     L.rows = align_up(L.nred + (a.norm.r ? sizeof(float) * T * (H / 32) : 0), 128);
-    L.ring = align_up(L.rows + 2 * (size_t)a.rpc * H, 128);
+    // ROWS: the CTA's expert outputs d[t][rank, or k: shared][row] (FP32
+    // holding the bf16 values)
+    L.dres = align_up(L.rows + 2 * (size_t)a.rpc * H, 128);
+    L.ring = align_up(L.dres + (a.rows ? sizeof(float) * T * (a.k + 1) * (size_t)a.rows_max : 0), 128);
     L.total = L.ring + (size_t)kLW * a.ns * a.slot;
     return L;
 }
@@ -340,7 +350,7 @@ __device__ void build_segs(LayerSmall& sm, int p0, int up0, int p1, int per_gu, 
 // NORM: the input is rmsnorm(r + y_prev) of the residual stream (a.norm), not
 // a.x. Two instantiations, so that the plain layer carries none of the norm's
 // code (measured: a never-taken norm branch cost 3-4 us at T = 8).
-template <bool NORM>
+template <bool NORM, bool ROWS>
 __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const LayerSmem L = layer_layout(a);
@@ -359,6 +369,10 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     const int RS = (int)nvfp4_row_stride(H), RSr = (int)nvfp4_row_stride(I);
     const int RSs = Is ? (int)nvfp4_row_stride(Is) : 0;
     const int NB = H / kRowBlock;
+    // ROWS: this CTA's output rows [R0, R1), in down items of rg rows (ng per
+    // expert)
+    const int R0 = c * H / G, R1 = (c + 1) * H / G, nrows = R1 - R0;
+    const int ng = (nrows + a.rg - 1) / a.rg;
     // router rows: rpc each on the routed CTAs (the shared CTAs queue their
     // expert's copies before the PDL wait and would publish late)
     const int r0 = (c - Gs) * a.rpc, nrr = sh_cta ? 0 : max(0, min(a.rpc, E - r0));
@@ -407,6 +421,16 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
             mbar_arrive_expect_tx(bar, 2u * (uint32_t)RS);
             bulk_g2s(dst, g + (size_t)p * RS, (uint32_t)RS, bar);
             bulk_g2s(dst + RS, g + (size_t)((sh ? Is : I) + p) * RS, (uint32_t)RS, bar);
+        } else if constexpr (ROWS) {
+            // down item m: rows [R0 + rg (m % ng), + rg) of unit m / ng (the
+            // routed experts in list order, then the shared expert)
+            const int m = warp + (it - my_g) * kLW;
+            const int u = m / ng, r = R0 + (m - u * ng) * a.rg, nr = min(a.rg, R1 - r);
+            const bool sh = u == ri.D;
+            const int RSu = sh ? RSs : RSr;
+            const uint8_t* d = sh ? a.s_down : a.down + (size_t)ri.dlist[u] * H * RSr;
+            mbar_arrive_expect_tx(bar, (uint32_t)(nr * RSu));
+            bulk_g2s(dst, d + (size_t)r * RSu, (uint32_t)(nr * RSu), bar);
         } else {
             const int m = warp + (it - my_g) * kLW;
             int s = 0;
@@ -449,8 +473,9 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         sm.b0 = sm.b1 = 0;
         if (sh_cta) {
             // the shared expert: an even split of its pairs and row blocks
+            // (ROWS: no row blocks; its down items come with the routing)
             const int p0 = (int)((long long)c * Is / Gs), p1 = (int)((long long)(c + 1) * Is / Gs);
-            const int b0 = (int)((long long)c * NB / Gs), b1 = (int)((long long)(c + 1) * NB / Gs);
+            const int b0 = ROWS ? 0 : (int)((long long)c * NB / Gs), b1 = ROWS ? 0 : (int)((long long)(c + 1) * NB / Gs);
             build_segs(sm, p0, 0, p1, Is, b0, 0, b1, NB, a.status, true, rows_per_item(RSs, (b1 - b0) * kRowBlock));
         }
     }
@@ -578,9 +603,15 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 FLINT_PHASE(14);
                 int p0, p1, b0, b1, up0, ub0;
                 cost_split_warp(ri, I, NB, (uint32_t)(c - Gs), (uint32_t)(G - Gs), lane, p0, p1, b0, b1, up0, ub0);
-                if (lane == 0)
-                    build_segs(sm, p0, up0, p1, I, b0, ub0, b1, NB, a.status, false,
-                               rows_per_item(RSr, (b1 - b0) * kRowBlock));
+                if (lane == 0) {
+                    if constexpr (ROWS) {
+                        build_segs(sm, p0, up0, p1, I, 0, 0, 0, NB, a.status, false, 1);
+                        sm.n_di = (ri.D + (has_sh ? 1 : 0)) * ng;
+                    } else {
+                        build_segs(sm, p0, up0, p1, I, b0, ub0, b1, NB, a.status, false,
+                                   rows_per_item(RSr, (b1 - b0) * kRowBlock));
+                    }
+                }
                 FLINT_PHASE(19);
             }
             // the segments are in; the tensor scales of all routed experts too
@@ -695,219 +726,344 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 #endif
     // Publish this CTA's h: per expert, the number of its pairs done here.
     if (__syncthreads_or(wfail) && tid == 0) sm.fail = 1;
-    if (tid == 0 && !sm.fail && !failed && !withhold && sm.n_gseg > 0) {
-        fence_acq_rel_gpu();  // one fence for all of them
-        for (int s = 0; s < sm.n_gseg; ++s) {
-            const int unit = sm.gseg[s].unit;
-            red_add_relaxed_gpu(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit), (uint32_t)sm.gseg[s].count);
+    if constexpr (ROWS) {
+        // ROWS: publish the number of this CTA's pairs done; the shared group
+        // learns the routing, and with it its down items; every CTA stages all of
+        // h once every pair is published, then computes its rows of every
+        // expert's down GEMV and of y.
+        if (tid == 0 && !sm.fail && !failed && !withhold && sm.n_gi > 0)
+            release_add_gpu(a.hdr + kHdrPairsIn, (uint32_t)sm.n_gi);
+        FLINT_PHASE(6);
+        if (!__syncthreads_or(failed || sm.fail) && sh_cta) {
+            failed = !route(40);
+            if (!failed && warp == 0) {
+                route_view_warp(ri, sm.ids, T, k, lane);
+                if (lane == 0) sm.n_di = (ri.D + (has_sh ? 1 : 0)) * ng;
+            }
+            __syncthreads();
+            FLINT_PHASE(43);
+            if (!failed) {
+                count_mine();
+                if (lane == 0 && !sm.fail)
+                    for (int it = my_g; it < my_g + NSW && it < my_g + my_d; ++it) issue(it);
+            }
         }
-    }
-    FLINT_PHASE(6);
-    if (!failed && sm.n_di > 0) {
-        // Stage h of this CTA's down experts once every pair of each is published.
-        if (tid == 0) {
-            int nv = 0, item = 0, off = 0, coff = 0;
-            for (int q = 0; q < sm.n_dseg; ++q) {
-                const int unit = sm.dseg[q].unit;
-                const int K = unit == kSharedUnit ? Is : I;
-                const uint32_t tm = unit == kSharedUnit ? (1u << T) - 1u : ri.tmask[unit];
-                for (int t = 0; t < FLINT_MAX_TOKENS; ++t) {
-                    sm.vec[q][t] = -1;
-                    if (t < T && ((tm >> t) & 1u)) {
-                        sm.vec[q][t] = (int16_t)nv;
-                        sm.v_item0[nv] = item;
-                        sm.v_off[nv] = off;
-                        sm.v_coff[nv] = coff;
-                        sm.v_q[nv] = (int16_t)q;
-                        sm.v_t[nv] = (int16_t)t;
-                        item += K / 32;
-                        off += 2 * K;
-                        coff += 4 * (K / 32);
-                        ++nv;
+        const int D = ri.D;
+        const uint32_t pairs = (uint32_t)D * (uint32_t)I + (has_sh ? (uint32_t)Is : 0u);
+        if (failed || sm.fail ||
+            !cta_wait_count(a.hdr + kHdrPairsIn, pairs, a.status, kStatusTimeoutLayer, budget, &sm.ok) || sm.fail) {
+            drain(budget);
+            return;
+        }
+        // the routed h [T][k][I] (vector t k + j), then the shared h [T][Is]
+        const StageSrc hsrc[2] = {{a.h_routed, xh, csc, T * k, I},
+                                  {a.h_shared, xh + (size_t)T * k * (I / 8), csc + (size_t)T * k * (I / 32),
+                                   has_sh ? T : 0, has_sh ? Is : 32}};
+        stage_f16<true>(hsrc, [] {});
+        __syncthreads();
+        FLINT_PHASE(7);
+        float* dres = reinterpret_cast<float*>(smem + L.dres);
+        auto dslot = [&](int t, int j, int r) -> float& { return dres[((size_t)t * (k + 1) + j) * a.rows_max + r]; };
+        // the unit of the current down item and what it needs, kept from one item
+        // to the next
+        int cu = -1;
+        bool sh = false;
+        uint32_t tm = 0;
+        float tsd = 0.f;
+        unsigned long long dm = 0ull;
+        for (int it = my_g; it < my_g + my_d; ++it) {
+            if (!item_in(it)) break;
+            const int m = warp + (it - my_g) * kLW;
+            const int u = m / ng;
+            if (u != cu) {
+                cu = u;
+                sh = u == D;
+                tm = sh ? (1u << T) - 1u : ri.tmask[u];
+                tsd = tscale(sh, u, 2);
+                dm = sh ? 0ull : ri.dmask[u];
+            }
+            const int rl = (m - u * ng) * a.rg, nrw = min(a.rg, nrows - rl);  // local rows [rl, rl + nrw)
+            const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
+            const uint8_t* rows = wring + (size_t)(it % NSW) * a.slot;
+            // token t's rank of this expert (k: the shared expert) and its staged h
+            auto rank = [&](int t) { return sh ? k : __ffs(rank_bits(dm, t)) - 1; };
+            auto vec = [&](int t, int j, const uint4*& hv, const float*& cv) {
+                if (sh) {
+                    hv = hsrc[1].dst + (size_t)t * (Is / 8);
+                    cv = hsrc[1].csc + (size_t)t * (Is / 32);
+                } else {
+                    hv = xh + (size_t)(t * k + j) * (I / 8);
+                    cv = csc + (size_t)(t * k + j) * (I / 32);
+                }
+            };
+            auto put = [&](float v, int r, int t, int j) { dslot(t, j, rl + r) = bf16_round_f32(tsd * v); };
+            // rows [0, nrw) against one or two tokens (rows past nrw are skipped inside)
+            constexpr int RP = 8;
+            uint32_t rest = tm;
+            while (rest) {
+                const int t0 = __ffs(rest) - 1;
+                rest &= rest - 1u;
+                const int j0 = rank(t0);
+                if (rest) {
+                    const int t1 = __ffs(rest) - 1;
+                    rest &= rest - 1u;
+                    const int j1 = rank(t1);
+                    const uint4* hv[2];
+                    const float* cv[2];
+                    vec(t0, j0, hv[0], cv[0]);
+                    vec(t1, j1, hv[1], cv[1]);
+                    float acc[2 * RP];
+                    down_pass<RP, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                    const float v = reduce_scatter<2 * RP>(acc, lane);
+                    const int idx = rs_index<2 * RP>(lane), r = idx % RP;
+                    if (lane % (16 / RP) == 16 / RP - 1 && r < nrw) {
+                        if (idx >= RP) put(v, r, t1, j1);
+                        else put(v, r, t0, j0);
                     }
+                } else {
+                    const uint4* hv[1];
+                    const float* cv[1];
+                    vec(t0, j0, hv[0], cv[0]);
+                    float acc[RP];
+                    down_pass<RP, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                    const float v = reduce_scatter<RP>(acc, lane);
+                    const int r = rs_index<RP>(lane);
+                    if (lane % (32 / RP) == 32 / RP - 1 && r < nrw) put(v, r, t0, j0);
                 }
             }
-            if (off > a.stage_vals || coff > a.stage_scales) {  // the host plans for this not to happen
-                atomicOr(a.status, kStatusLayerPlan);
-                sm.fail = 1;
-                nv = 0;
-                item = 0;
-            }
-            sm.n_vec = nv;
-            sm.v_item0[nv] = item;
+            item_done(it);
         }
-        bool ok = true;
-        for (int q = 0; q < sm.n_dseg && ok; ++q) {  // sm.n_dseg: written before the earlier barriers
-            const int unit = sm.dseg[q].unit;
-            ok = cta_wait_count(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit),
-                                (uint32_t)(unit == kSharedUnit ? Is : I), a.status, kStatusTimeoutLayer, budget,
-                                &sm.ok);
+        if (__syncthreads_or(wfail || sm.fail)) {
+            drain(budget);
+            return;
         }
-        ok = ok && !sm.fail;
-        const int n_items = ok ? sm.v_item0[sm.n_vec] : 0;
-        for (int q = tid; q < n_items; q += kLT) {
-            int v = 0;
-            while (sm.v_item0[v + 1] <= q) ++v;
-            const int cc = q - sm.v_item0[v], t = sm.v_t[v];
-            const int unit = sm.dseg[sm.v_q[v]].unit;
-            const bool sh = unit == kSharedUnit;
-            const int K = sh ? Is : I;
-            const uint16_t* src;
-            if (sh) {
-                src = a.h_shared + (size_t)t * Is;
-            } else {
-                const int j = __ffs(rank_bits(ri.dmask[unit], t)) - 1;
-                src = a.h_routed + ((size_t)t * k + j) * I;
-            }
-            const StageSrc ss = {src, reinterpret_cast<uint4*>(smem + L.xs + sm.v_off[v]),
-                                 reinterpret_cast<float*>(smem + L.csc + sm.v_coff[v]), 1, K};
-            uint4 w4[4];
-            stage_load(ss, 0, cc, w4);
-            stage_store<true>(ss, 0, cc, w4);
+        FLINT_PHASE(8);
+        // y = bf16(sum_j w_j d_j + d_shared), ranks in order, one (token, row) per thread
+        for (int e = tid; e < T * nrows; e += kLT) {
+            const int t = e / nrows, r = e - t * nrows;
+            float acc = 0.f;
+            for (int j = 0; j < k; ++j) acc = fmaf(sm.w[t * k + j], dslot(t, j, r), acc);
+            if (has_sh) acc += dslot(t, k, r);
+            a.y[(size_t)t * H + R0 + r] = f32_to_bf16_bits(acc);
         }
-        if (!__syncthreads_and(ok)) wfail = true;
-    }
-    FLINT_PHASE(7);
-    // the run of the current down item and what it needs, kept from one item
-    // to the next
-    int cd_s = -1, cd_next = 0;
-    Seg sg = {};
-    bool sh = false;
-    uint32_t tm = 0;
-    float tsd = 0.f;
-    unsigned long long dm = 0ull;
-    for (int it = my_g; it < my_g + my_d; ++it) {
-        if (!item_in(it)) break;
-        const int m = warp + (it - my_g) * kLW;
-        while (m >= cd_next) {
-            sg = sm.dseg[++cd_s];
-            cd_next = cd_s + 1 < sm.n_dseg ? sm.dseg[cd_s + 1].item0 : INT_MAX;
-            sh = sg.unit == kSharedUnit;
-            tm = sh ? (1u << T) - 1u : ri.tmask[sg.unit];
-            tsd = tscale(sh, sg.unit, 2);
-            dm = sh ? 0ull : ri.dmask[sg.unit];
-        }
-        const int row0 = sg.start + (m - sg.item0) * sg.rg;
-        const int nrw = min((int)sg.rg, sg.start + sg.count - row0);
-        const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
-        const uint8_t* rows = wring + (size_t)(it % NSW) * a.slot;
-        auto vec = [&](int t, const uint4*& hv, const float*& cv) {
-            const int v = sm.vec[sg.q][t];
-            hv = reinterpret_cast<const uint4*>(smem + L.xs + sm.v_off[v]);
-            cv = reinterpret_cast<const float*>(smem + L.csc + sm.v_coff[v]);
-        };
-        auto put = [&](float v, int r, int t) {
-            const uint16_t d = f32_to_bf16_bits(tsd * v);
-            if (sh) {
-                a.d_shared[(size_t)t * H + row0 + r] = d;
-            } else {
-                const int j = __ffs(rank_bits(dm, t)) - 1;
-                a.d_routed[((size_t)t * k + j) * H + row0 + r] = d;
-            }
-        };
-        // rows [0, nrw) of the item against one or two tokens
-        auto rows_pass = [&](auto rp_tag, int t0, int t1) {
-            constexpr int RP = decltype(rp_tag)::value;
-            if (t1 >= 0) {
-                const uint4* hv[2];
-                const float* cv[2];
-                vec(t0, hv[0], cv[0]);
-                vec(t1, hv[1], cv[1]);
-                float acc[2 * RP];
-                down_pass<RP, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
-                const float v = reduce_scatter<2 * RP>(acc, lane);
-                const int idx = rs_index<2 * RP>(lane), r = idx % RP;
-                if (lane % (16 / RP) == 16 / RP - 1 && r < nrw) put(v, r, idx >= RP ? t1 : t0);
-            } else {
-                const uint4* hv[1];
-                const float* cv[1];
-                vec(t0, hv[0], cv[0]);
-                float acc[RP];
-                down_pass<RP, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
-                const float v = reduce_scatter<RP>(acc, lane);
-                const int r = rs_index<RP>(lane);
-                if (lane % (32 / RP) == 32 / RP - 1 && r < nrw) put(v, r, t0);
-            }
-        };
-        uint32_t rest = tm;
-        while (rest) {
-            const int t0 = __ffs(rest) - 1;
-            rest &= rest - 1u;
-            int t1 = -1;
-            if (rest) {
-                t1 = __ffs(rest) - 1;
-                rest &= rest - 1u;
-            }
-            // one instantiation (rows past nrw are skipped inside); a second,
-            // 4-row one measured slower (register spills)
-            rows_pass(std::integral_constant<int, 8>(), t0, t1);
-        }
-        item_done(it);
-    }
+        FLINT_PHASE(10);
 
-    // ---- 5: arrivals on the row blocks; the last arriver of a block combines it ------
-    FLINT_PHASE(8);
-    if (!__syncthreads_or(failed || wfail || sm.fail) && sh_cta) {
-        // the shared group learns the routing now (weights, number of experts)
-        failed = !route(15);
-        if (!failed && warp == 0) route_view_warp(ri, sm.ids, T, k, lane);
-        FLINT_PHASE(18);
-    }
-    if (__syncthreads_or(failed || wfail || sm.fail)) {
-        drain(budget);
-        return;
-    }
-    const uint32_t U = (uint32_t)ri.D + (has_sh ? 1u : 0u);
-    for (int j = sm.b0 + tid; j < sm.b1; j += kLT) {
-        // the release half of the add publishes the CTA's d, ordered before
-        // this thread by the barriers above
-        const int blk = j % NB;
-        if (atom_add_acq_rel_gpu(a.counters + blk, 1u) == U - 1u) sm.last[atomicAdd(&sm.n_last, 1)] = (int16_t)blk;
-    }
-    __syncthreads();
-    FLINT_PHASE(9);
-    // the blocks this CTA completed: one thread per 8 rows of one token, the
-    // k + 1 expert outputs read as 16-byte words, summed in rank order
-    const int n_last = sm.n_last;
-    for (int e = tid; e < n_last * T * (kRowBlock / 8); e += kLT) {
-        const int qb = e / (T * (kRowBlock / 8)), rem = e - qb * (T * (kRowBlock / 8));
-        const int t = rem / (kRowBlock / 8), r = sm.last[qb] * kRowBlock + 8 * (rem - t * (kRowBlock / 8));
-        float acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        auto add = [&](float wj, const uint4 dj) {
-            const uint32_t dw[4] = {dj.x, dj.y, dj.z, dj.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = fmaf(wj, bf16_lo(dw[i]), acc[2 * i]);
-                acc[2 * i + 1] = fmaf(wj, bf16_hi(dw[i]), acc[2 * i + 1]);
-            }
-        };
-        const uint4* dr = reinterpret_cast<const uint4*>(a.d_routed + (size_t)t * k * H + r);
-        for (int j = 0; j < k; j += 2) {  // two loads in flight
-            const uint4 d0 = __ldcg(dr + (size_t)j * (H / 8));
-            const uint4 d1 = j + 1 < k ? __ldcg(dr + (size_t)(j + 1) * (H / 8)) : make_uint4(0u, 0u, 0u, 0u);
-            add(sm.w[t * k + j], d0);
-            if (j + 1 < k) add(sm.w[t * k + j + 1], d1);
-        }
-        if (has_sh) {
-            const uint4 ds = __ldcg(reinterpret_cast<const uint4*>(a.d_shared + (size_t)t * H + r));
-            const uint32_t dw[4] = {ds.x, ds.y, ds.z, ds.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] += bf16_lo(dw[i]);
-                acc[2 * i + 1] += bf16_hi(dw[i]);
+    } else {
+        if (tid == 0 && !sm.fail && !failed && !withhold && sm.n_gseg > 0) {
+            fence_acq_rel_gpu();  // one fence for all of them
+            for (int s = 0; s < sm.n_gseg; ++s) {
+                const int unit = sm.gseg[s].unit;
+                red_add_relaxed_gpu(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit), (uint32_t)sm.gseg[s].count);
             }
         }
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            o[i] = (uint32_t)f32_to_bf16_bits(acc[2 * i]) | ((uint32_t)f32_to_bf16_bits(acc[2 * i + 1]) << 16);
-        *reinterpret_cast<uint4*>(a.y + (size_t)t * H + r) = make_uint4(o[0], o[1], o[2], o[3]);
+        FLINT_PHASE(6);
+        if (!failed && sm.n_di > 0) {
+            // Stage h of this CTA's down experts once every pair of each is published.
+            if (tid == 0) {
+                int nv = 0, item = 0, off = 0, coff = 0;
+                for (int q = 0; q < sm.n_dseg; ++q) {
+                    const int unit = sm.dseg[q].unit;
+                    const int K = unit == kSharedUnit ? Is : I;
+                    const uint32_t tm = unit == kSharedUnit ? (1u << T) - 1u : ri.tmask[unit];
+                    for (int t = 0; t < FLINT_MAX_TOKENS; ++t) {
+                        sm.vec[q][t] = -1;
+                        if (t < T && ((tm >> t) & 1u)) {
+                            sm.vec[q][t] = (int16_t)nv;
+                            sm.v_item0[nv] = item;
+                            sm.v_off[nv] = off;
+                            sm.v_coff[nv] = coff;
+                            sm.v_q[nv] = (int16_t)q;
+                            sm.v_t[nv] = (int16_t)t;
+                            item += K / 32;
+                            off += 2 * K;
+                            coff += 4 * (K / 32);
+                            ++nv;
+                        }
+                    }
+                }
+                if (off > a.stage_vals || coff > a.stage_scales) {  // the host plans for this not to happen
+                    atomicOr(a.status, kStatusLayerPlan);
+                    sm.fail = 1;
+                    nv = 0;
+                    item = 0;
+                }
+                sm.n_vec = nv;
+                sm.v_item0[nv] = item;
+            }
+            bool ok = true;
+            for (int q = 0; q < sm.n_dseg && ok; ++q) {  // sm.n_dseg: written before the earlier barriers
+                const int unit = sm.dseg[q].unit;
+                ok = cta_wait_count(a.unit_counters + (unit == kSharedUnit ? kShIdx : unit),
+                                    (uint32_t)(unit == kSharedUnit ? Is : I), a.status, kStatusTimeoutLayer, budget,
+                                    &sm.ok);
+            }
+            ok = ok && !sm.fail;
+            const int n_items = ok ? sm.v_item0[sm.n_vec] : 0;
+            for (int q = tid; q < n_items; q += kLT) {
+                int v = 0;
+                while (sm.v_item0[v + 1] <= q) ++v;
+                const int cc = q - sm.v_item0[v], t = sm.v_t[v];
+                const int unit = sm.dseg[sm.v_q[v]].unit;
+                const bool sh = unit == kSharedUnit;
+                const int K = sh ? Is : I;
+                const uint16_t* src;
+                if (sh) {
+                    src = a.h_shared + (size_t)t * Is;
+                } else {
+                    const int j = __ffs(rank_bits(ri.dmask[unit], t)) - 1;
+                    src = a.h_routed + ((size_t)t * k + j) * I;
+                }
+                const StageSrc ss = {src, reinterpret_cast<uint4*>(smem + L.xs + sm.v_off[v]),
+                                     reinterpret_cast<float*>(smem + L.csc + sm.v_coff[v]), 1, K};
+                uint4 w4[4];
+                stage_load(ss, 0, cc, w4);
+                stage_store<true>(ss, 0, cc, w4);
+            }
+            if (!__syncthreads_and(ok)) wfail = true;
+        }
+        FLINT_PHASE(7);
+        // the run of the current down item and what it needs, kept from one item
+        // to the next
+        int cd_s = -1, cd_next = 0;
+        Seg sg = {};
+        bool sh = false;
+        uint32_t tm = 0;
+        float tsd = 0.f;
+        unsigned long long dm = 0ull;
+        for (int it = my_g; it < my_g + my_d; ++it) {
+            if (!item_in(it)) break;
+            const int m = warp + (it - my_g) * kLW;
+            while (m >= cd_next) {
+                sg = sm.dseg[++cd_s];
+                cd_next = cd_s + 1 < sm.n_dseg ? sm.dseg[cd_s + 1].item0 : INT_MAX;
+                sh = sg.unit == kSharedUnit;
+                tm = sh ? (1u << T) - 1u : ri.tmask[sg.unit];
+                tsd = tscale(sh, sg.unit, 2);
+                dm = sh ? 0ull : ri.dmask[sg.unit];
+            }
+            const int row0 = sg.start + (m - sg.item0) * sg.rg;
+            const int nrw = min((int)sg.rg, sg.start + sg.count - row0);
+            const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
+            const uint8_t* rows = wring + (size_t)(it % NSW) * a.slot;
+            auto vec = [&](int t, const uint4*& hv, const float*& cv) {
+                const int v = sm.vec[sg.q][t];
+                hv = reinterpret_cast<const uint4*>(smem + L.xs + sm.v_off[v]);
+                cv = reinterpret_cast<const float*>(smem + L.csc + sm.v_coff[v]);
+            };
+            auto put = [&](float v, int r, int t) {
+                const uint16_t d = f32_to_bf16_bits(tsd * v);
+                if (sh) {
+                    a.d_shared[(size_t)t * H + row0 + r] = d;
+                } else {
+                    const int j = __ffs(rank_bits(dm, t)) - 1;
+                    a.d_routed[((size_t)t * k + j) * H + row0 + r] = d;
+                }
+            };
+            // rows [0, nrw) of the item against one or two tokens
+            auto rows_pass = [&](auto rp_tag, int t0, int t1) {
+                constexpr int RP = decltype(rp_tag)::value;
+                if (t1 >= 0) {
+                    const uint4* hv[2];
+                    const float* cv[2];
+                    vec(t0, hv[0], cv[0]);
+                    vec(t1, hv[1], cv[1]);
+                    float acc[2 * RP];
+                    down_pass<RP, 2>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                    const float v = reduce_scatter<2 * RP>(acc, lane);
+                    const int idx = rs_index<2 * RP>(lane), r = idx % RP;
+                    if (lane % (16 / RP) == 16 / RP - 1 && r < nrw) put(v, r, idx >= RP ? t1 : t0);
+                } else {
+                    const uint4* hv[1];
+                    const float* cv[1];
+                    vec(t0, hv[0], cv[0]);
+                    float acc[RP];
+                    down_pass<RP, 1>(rows, RSu, nrw, K, hv, cv, lane, acc);
+                    const float v = reduce_scatter<RP>(acc, lane);
+                    const int r = rs_index<RP>(lane);
+                    if (lane % (32 / RP) == 32 / RP - 1 && r < nrw) put(v, r, t0);
+                }
+            };
+            uint32_t rest = tm;
+            while (rest) {
+                const int t0 = __ffs(rest) - 1;
+                rest &= rest - 1u;
+                int t1 = -1;
+                if (rest) {
+                    t1 = __ffs(rest) - 1;
+                    rest &= rest - 1u;
+                }
+                // one instantiation (rows past nrw are skipped inside); a second,
+                // 4-row one measured slower (register spills)
+                rows_pass(std::integral_constant<int, 8>(), t0, t1);
+            }
+            item_done(it);
+        }
+
+        // ---- 5: arrivals on the row blocks; the last arriver of a block combines it ------
+        FLINT_PHASE(8);
+        if (!__syncthreads_or(failed || wfail || sm.fail) && sh_cta) {
+            // the shared group learns the routing now (weights, number of experts)
+            failed = !route(15);
+            if (!failed && warp == 0) route_view_warp(ri, sm.ids, T, k, lane);
+            FLINT_PHASE(18);
+        }
+        if (__syncthreads_or(failed || wfail || sm.fail)) {
+            drain(budget);
+            return;
+        }
+        const uint32_t U = (uint32_t)ri.D + (has_sh ? 1u : 0u);
+        for (int j = sm.b0 + tid; j < sm.b1; j += kLT) {
+            // the release half of the add publishes the CTA's d, ordered before
+            // this thread by the barriers above
+            const int blk = j % NB;
+            if (atom_add_acq_rel_gpu(a.counters + blk, 1u) == U - 1u) sm.last[atomicAdd(&sm.n_last, 1)] = (int16_t)blk;
+        }
+        __syncthreads();
+        FLINT_PHASE(9);
+        // the blocks this CTA completed: one thread per 8 rows of one token, the
+        // k + 1 expert outputs read as 16-byte words, summed in rank order
+        const int n_last = sm.n_last;
+        for (int e = tid; e < n_last * T * (kRowBlock / 8); e += kLT) {
+            const int qb = e / (T * (kRowBlock / 8)), rem = e - qb * (T * (kRowBlock / 8));
+            const int t = rem / (kRowBlock / 8), r = sm.last[qb] * kRowBlock + 8 * (rem - t * (kRowBlock / 8));
+            float acc[8];
+    #pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+            auto add = [&](float wj, const uint4 dj) {
+                const uint32_t dw[4] = {dj.x, dj.y, dj.z, dj.w};
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = fmaf(wj, bf16_lo(dw[i]), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(wj, bf16_hi(dw[i]), acc[2 * i + 1]);
+                }
+            };
+            const uint4* dr = reinterpret_cast<const uint4*>(a.d_routed + (size_t)t * k * H + r);
+            for (int j = 0; j < k; j += 2) {  // two loads in flight
+                const uint4 d0 = __ldcg(dr + (size_t)j * (H / 8));
+                const uint4 d1 = j + 1 < k ? __ldcg(dr + (size_t)(j + 1) * (H / 8)) : make_uint4(0u, 0u, 0u, 0u);
+                add(sm.w[t * k + j], d0);
+                if (j + 1 < k) add(sm.w[t * k + j + 1], d1);
+            }
+            if (has_sh) {
+                const uint4 ds = __ldcg(reinterpret_cast<const uint4*>(a.d_shared + (size_t)t * H + r));
+                const uint32_t dw[4] = {ds.x, ds.y, ds.z, ds.w};
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] += bf16_lo(dw[i]);
+                    acc[2 * i + 1] += bf16_hi(dw[i]);
+                }
+            }
+            uint32_t o[4];
+    #pragma unroll
+            for (int i = 0; i < 4; ++i)
+                o[i] = (uint32_t)f32_to_bf16_bits(acc[2 * i]) | ((uint32_t)f32_to_bf16_bits(acc[2 * i + 1]) << 16);
+            *reinterpret_cast<uint4*>(a.y + (size_t)t * H + r) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        for (int q = tid; q < n_last; q += kLT) a.counters[sm.last[q]] = 0;
+        __syncthreads();
+        FLINT_PHASE(10);
+
     }
-    for (int q = tid; q < n_last; q += kLT) a.counters[sm.last[q]] = 0;
-    __syncthreads();
-    FLINT_PHASE(10);
 #ifdef FLINT_PHASE_TRACE
     if (tid == 0) {
         sm.trace[20] = wait_gu;
@@ -930,7 +1086,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
         dst[27] = smid;
         dst[28] = (unsigned long long)sh_cta | ((unsigned long long)(sm.n_gi + sm.n_di) << 8) |
-                  ((unsigned long long)n_last << 16) | ((unsigned long long)sm.n_gi << 32);
+                  ((unsigned long long)sm.n_last << 16) | ((unsigned long long)sm.n_gi << 32);
         dst[29] = trace_t0;
         dst[30] = globaltimer_ns();
         dst[31] = sm.hdr[kHdrCalls] + 1ull;
@@ -940,6 +1096,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     // (every other CTA is past all of its waits) and counts the call.
     if (tid == 0 && atomicAdd(a.hdr + kHdrDone, 1u) == (uint32_t)G - 1u) {
         a.hdr[kHdrScoresIn] = 0;
+        a.hdr[kHdrPairsIn] = 0;
         for (int u = 0; u < ri.D; ++u) a.unit_counters[u] = 0;
         a.unit_counters[kShIdx] = 0;
         a.hdr[kHdrCalls] = sm.hdr[kHdrCalls] + 1u;
@@ -952,14 +1109,14 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 size_t layer_smem_bytes(const LayerArgs& a) { return layer_layout(a).total; }
 
 namespace {
-template <bool NORM>
+template <bool NORM, bool ROWS>
 cudaError_t launch_layer_t(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
     static int configured_for = -1;
-    cudaError_t e = configure_smem(layer_kernel<NORM>, d, configured_for);
+    cudaError_t e = configure_smem(layer_kernel<NORM, ROWS>, d, configured_for);
     if (e != cudaSuccess) return e;
     const size_t smem = layer_smem_bytes(a);
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_kernel<NORM>, kLT, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_kernel<NORM, ROWS>, kLT, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     cudaLaunchConfig_t cfg = {};
@@ -974,12 +1131,13 @@ cudaError_t launch_layer_t(const LayerArgs& a, const DevInfo& d, bool pdl, cudaS
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, layer_kernel<NORM>, a);
+    return cudaLaunchKernelEx(&cfg, layer_kernel<NORM, ROWS>, a);
 }
 }  // namespace
 
 cudaError_t launch_layer(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
-    return a.norm.r ? launch_layer_t<true>(a, d, pdl, s) : launch_layer_t<false>(a, d, pdl, s);
+    if (a.rows) return a.norm.r ? launch_layer_t<true, true>(a, d, pdl, s) : launch_layer_t<false, true>(a, d, pdl, s);
+    return a.norm.r ? launch_layer_t<true, false>(a, d, pdl, s) : launch_layer_t<false, false>(a, d, pdl, s);
 }
 
 }  // namespace flint

@@ -27,6 +27,11 @@ Intervals (between the kernel's stamps; "-" where a group of CTAs has none):
   routing (shared group, at end)  the same four routing steps, for the combine weights
   arrivals                        the counts on its row blocks
   combine                         the blocks it completed
+One token (down split by output rows):
+  routing (shared group)          the shared group's routing, after its gate/up
+  h of the down experts staged    here: every pair published, all of h staged
+  down                            the CTA's rows of every expert's down GEMV
+  after the down items            its rows of y (with more tokens: arrivals and combine)
 """
 from __future__ import annotations
 
@@ -48,8 +53,10 @@ INTERVALS = [("wait for the previous call", 0, 1, "all"), ("x staged", 1, 2, "al
              ("at the end: all scores in", 8, 15, "shared"), ("at the end: scores read", 15, 16, "shared"),
              ("at the end: top-k", 16, 17, "shared"), ("at the end: routing view", 17, 18, "shared"),
              ("arrivals", 18, 9, "shared"), ("arrivals", 8, 9, "routed"), ("combine", 9, 10, "all"),
+             ("one token: routing (shared group, after its gate/up)", 6, 43, "shared"),
+             ("after the down items, to the end", 8, 10, "all"),
              ("after the wait, to the end", 1, 10, "all")]
-N_STAMPS, N_CALLS, N_CTAS = 40, 64, 256
+N_STAMPS, N_CALLS, N_CTAS = 48, 64, 256
 
 
 def main(argv=None):
