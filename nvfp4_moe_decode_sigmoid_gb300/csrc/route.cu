@@ -13,13 +13,13 @@
 // one warp per token, and leaves the ticket counter at zero.
 #include <cfloat>
 
+#include "expert_common.cuh"
 #include "router_common.cuh"
 
 namespace flint {
 namespace {
 
-// Shared memory: mbarrier, per-warp partial logits, the CTA's router rows,
-// then (last CTA) the sigmoid scores of all tokens.
+// Shared memory: mbarrier, per-warp partial logits, the CTA's router rows.
 __host__ __device__ inline size_t route_scores_offset(const RouteArgs& a) {
     return 128 + align_up(sizeof(float) * kWarps * FLINT_MAX_TOKENS * a.rows_per_cta, 128) +
            align_up((size_t)a.rows_per_cta * a.H * 2, 128);
@@ -91,20 +91,18 @@ __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
                 }
             }
         }
-        // reduce over the block: warp shuffle, then fixed-order sum over warps
+        // reduce over the block: the 2 x 8 sums reduce-scattered over the warp
+        // (two lanes end with each), then a fixed-order sum over the warps
+        float v16[2 * FLINT_MAX_TOKENS];
 #pragma unroll
         for (int t = 0; t < FLINT_MAX_TOKENS; ++t) {
-            if (t < T) {
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    float v = acc[t][q];
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                    if (lane == 0 && rb + q < nrows) partial[(warp * FLINT_MAX_TOKENS + t) * rpc + rb + q] = v;
-                    acc[t][q] = 0.f;
-                }
-            }
+            v16[2 * t] = acc[t][0];
+            v16[2 * t + 1] = acc[t][1];
+            acc[t][0] = acc[t][1] = 0.f;
         }
+        const float v = reduce_scatter<2 * FLINT_MAX_TOKENS>(v16, lane);
+        const int idx = rs_index<2 * FLINT_MAX_TOKENS>(lane), t = idx >> 1, q = idx & 1;
+        if ((lane & 1) == 0 && t < T && rb + q < nrows) partial[(warp * FLINT_MAX_TOKENS + t) * rpc + rb + q] = v;
     }
     __syncthreads();
     for (int i = tid; i < T * nrows; i += kThreads) {
@@ -123,15 +121,14 @@ __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
     __syncthreads();
     if (!is_last) return;
 
-    uint32_t* scores = reinterpret_cast<uint32_t*>(smem + route_scores_offset(a));
-    sigmoid_scores(a.logits, a.bias, T, a.E, scores);
-    __syncthreads();
+    // one warp per token: its logits straight from L2, the sigmoid on load
     if (warp < T) {
-        const uint32_t* sc = scores + (size_t)warp * a.E;
+        const float* lg = a.logits + (size_t)warp * a.E;
         if (a.E <= 256)
-            topk_warp<8>(sc, a.E, a.k, lane, a.ids + warp * a.k, a.weights + warp * a.k);
+            topk_warp_logits<8>(lg, a.bias, a.E, a.k, lane, a.ids + warp * a.k, a.weights + warp * a.k);
         else
-            topk_warp<FLINT_MAX_EXPERTS / 32>(sc, a.E, a.k, lane, a.ids + warp * a.k, a.weights + warp * a.k);
+            topk_warp_logits<FLINT_MAX_EXPERTS / 32>(lg, a.bias, a.E, a.k, lane, a.ids + warp * a.k,
+                                                     a.weights + warp * a.k);
     }
     __syncthreads();
     if (tid == 0) atomicExch(a.counter, 0u);
@@ -139,9 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1) route_kernel(const RouteArgs a) {
 
 }  // namespace
 
-size_t route_smem_bytes(const RouteArgs& a) {
-    return route_scores_offset(a) + sizeof(uint32_t) * (size_t)a.T * a.E;
-}
+size_t route_smem_bytes(const RouteArgs& a) { return route_scores_offset(a); }
 
 cudaError_t launch_route(const RouteArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
     const size_t smem = route_smem_bytes(a);

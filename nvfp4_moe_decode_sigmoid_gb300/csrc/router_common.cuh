@@ -26,9 +26,8 @@ __device__ __forceinline__ void sigmoid_scores(const float* logits, const float*
     for (int i = threadIdx.x; i < T * E; i += blockDim.x) scores[i] = sigmoid_score(ld_cg(logits + i), bias, i % E);
 }
 
-// Top-k of one token's scores (shared memory; global memory written by other
-// CTAs when L2 is set: read past L1), one warp: lane holds experts
-// lane + 32 i. Weights are the selected scores over their sum. Each round
+// Top-k of one token's scores, one warp: lane holds the scores of experts
+// lane + 32 i in s[i] (0 past E). Weights are the selected scores over their sum. Each round
 // takes the warp maximum of the lanes' best untaken scores and breaks ties
 // toward the lowest expert index with a warp minimum.
 //   SLOTS == 8 (E <= 256): each lane first sorts its keys (score bits above,
@@ -36,16 +35,10 @@ __device__ __forceinline__ void sigmoid_scores(const float* logits, const float*
 //   no expert) with Batcher's 19-comparator network, so that its best
 //   untaken key is always key[0] and the owning lane of a round just shifts.
 //   Otherwise the owning lane rescans its slots.
-template <int SLOTS, bool L2 = false>
-__device__ __forceinline__ void topk_warp(const uint32_t* sc, int E, int k, int lane, int32_t* ids,
-                                          float* weights) {
+template <int SLOTS>
+__device__ __forceinline__ void topk_warp_regs(const uint32_t (&s)[SLOTS], int E, int k, int lane, int32_t* ids,
+                                               float* weights) {
     const uint32_t full = 0xffffffffu;
-    uint32_t s[SLOTS];
-#pragma unroll
-    for (int i = 0; i < SLOTS; ++i) {
-        const int e = lane + 32 * i;
-        s[i] = e >= E ? 0u : L2 ? (uint32_t)ld_cg(reinterpret_cast<const int32_t*>(sc) + e) : sc[e];
-    }
     float sel_s = 0.f, sum = 0.f;
     int sel_e = 0;
     if constexpr (SLOTS == 8) {
@@ -121,6 +114,33 @@ __device__ __forceinline__ void topk_warp(const uint32_t* sc, int E, int k, int 
         ids[lane] = sel_e;
         weights[lane] = sel_s / sum;
     }
+}
+
+// The same over scores in memory (lane l: experts l + 32 i).
+template <int SLOTS, bool L2 = false>
+__device__ __forceinline__ void topk_warp(const uint32_t* sc, int E, int k, int lane, int32_t* ids,
+                                          float* weights) {
+    uint32_t s[SLOTS];
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i) {
+        const int e = lane + 32 * i;
+        s[i] = e >= E ? 0u : L2 ? (uint32_t)ld_cg(reinterpret_cast<const int32_t*>(sc) + e) : sc[e];
+    }
+    topk_warp_regs<SLOTS>(s, E, k, lane, ids, weights);
+}
+
+// The same from one token's FP32 logits in global memory (written by other
+// CTAs: read past L1), the sigmoid (and bias) applied on load.
+template <int SLOTS>
+__device__ __forceinline__ void topk_warp_logits(const float* logits, const float* bias, int E, int k, int lane,
+                                                 int32_t* ids, float* weights) {
+    uint32_t s[SLOTS];
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i) {
+        const int e = lane + 32 * i;
+        s[i] = e >= E ? 0u : sigmoid_score(ld_cg(logits + e), bias, e);
+    }
+    topk_warp_regs<SLOTS>(s, E, k, lane, ids, weights);
 }
 
 }  // namespace
