@@ -15,16 +15,15 @@ Intervals (between the kernel's stamps; "-" where a group of CTAs has none):
   x staged                        x read and converted (or the norm of the residual)
   router scores published         this CTA's router rows (bulk copy) times x, the count raised
   all scores in                   waiting until every router row is published
-  scores read                     all T x E scores into shared memory
-  top-k                           one warp per token
+  top-k                           one warp per token, its scores read from L2
   routing view                    the distinct experts and their tokens
-  split, first copies             this CTA's ranges and its first ring copies issued
-  tensor scales                   the selected experts' tensor scales
-  first chunk in                  the first ring chunk's bytes landed
+  split                           this CTA's ranges (cost split) and runs
+  first copies                    the plan shared, each warp's first ring copies issued
+  first chunk in                  the first ring item's bytes landed
   gate/up                         the CTA's gate/up pairs, h written and counted
   h of the down experts staged    waits for the other CTAs' h of those experts
   down                            its down rows, d written
-  routing (shared group, at end)  the same four routing steps, for the combine weights
+  at the end: ...                 the shared group's routing steps, for the combine weights
   arrivals                        the counts on its row blocks
   combine                         the blocks it completed
 One token (down split by output rows):
@@ -45,14 +44,13 @@ import numpy as np
 
 # (name, from stamp, to stamp); the stamps the kernel takes (see layer.cu)
 INTERVALS = [("wait for the previous call", 0, 1, "all"), ("x staged", 1, 2, "all"),
-             ("router scores published", 2, 3, "all"), ("all scores in", 3, 11, "routed"),
-             ("scores read", 11, 12, "routed"), ("top-k", 12, 13, "routed"), ("routing view", 13, 14, "routed"),
-             ("split, first copies", 14, 19, "routed"), ("tensor scales", 19, 4, "routed"),
-             ("tensor scales", 3, 4, "shared"), ("first chunk in", 4, 5, "all"), ("gate/up", 5, 6, "all"),
+             ("router scores published", 2, 3, "routed"), ("all scores in", 3, 11, "routed"),
+             ("top-k", 12, 13, "routed"), ("routing view", 13, 14, "routed"), ("split", 14, 19, "routed"),
+             ("first copies", 19, 4, "routed"), ("first chunk in", 4, 5, "all"), ("gate/up", 5, 6, "all"),
              ("h of the down experts staged", 6, 7, "all"), ("down", 7, 8, "all"),
-             ("at the end: all scores in", 8, 15, "shared"), ("at the end: scores read", 15, 16, "shared"),
-             ("at the end: top-k", 16, 17, "shared"), ("at the end: routing view", 17, 18, "shared"),
-             ("arrivals", 18, 9, "shared"), ("arrivals", 8, 9, "routed"), ("combine", 9, 10, "all"),
+             ("at the end: all scores in", 8, 15, "shared"), ("at the end: top-k", 16, 17, "shared"),
+             ("at the end: routing view", 17, 18, "shared"), ("arrivals", 18, 9, "shared"),
+             ("arrivals", 8, 9, "routed"), ("combine", 9, 10, "all"),
              ("one token: routing (shared group, after its gate/up)", 6, 43, "shared"),
              ("after the down items, to the end", 8, 10, "all"),
              ("after the wait, to the end", 1, 10, "all")]
