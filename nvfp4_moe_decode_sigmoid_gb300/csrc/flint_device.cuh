@@ -154,67 +154,6 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     return v;
 }
 
-// Grid-wide barrier for a grid whose CTAs are all resident at once (a
-// cooperative launch), on a 64-bit ticket counter that only ever grows:
-// thread 0 of each CTA takes a ticket with a release add (publishing the
-// CTA's writes, which the __syncthreads before it ordered) and waits with
-// acquire loads until all gridDim.x tickets of its round are taken. One
-// atomic round trip and no reset (measured about half the cost of a count +
-// generation pair). The counter must start at a multiple of gridDim.x and
-// only this barrier may touch it; at 64 bits it does not wrap in practice
-// (a 32-bit counter would wrap after 2^32 / gridDim.x rounds, and 2^32 is
-// not a multiple of a grid of 152 CTAs). The wait gives up after
-// kWaitBudgetNs: `code` is set in *status, false is returned and the CTA
-// stops instead of hanging.
-__device__ __forceinline__ unsigned long long atom_add_release_gpu(unsigned long long* p, unsigned long long v) {
-    unsigned long long old;
-    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// The barrier in two halves, so that a CTA can do work that needs nothing
-// from the other CTAs between its arrival and its wait. grid_arrive returns
-// the ticket target (meaningful in thread 0 only).
-__device__ __forceinline__ unsigned long long grid_arrive(unsigned long long* ticket) {
-    __syncthreads();
-    unsigned long long target = 0;
-    if (threadIdx.x == 0) {
-        const unsigned long long t = atom_add_release_gpu(ticket, 1ull);
-        target = (t / gridDim.x + 1ull) * gridDim.x;
-    }
-    return target;
-}
-
-__device__ __forceinline__ bool grid_wait(unsigned long long* ticket, unsigned long long target, uint32_t* status,
-                                          uint32_t code) {
-    __shared__ int s_ok;
-    if (threadIdx.x == 0) {
-        int ok = 1;
-        if (ld_acquire_gpu(ticket) < target) {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(ticket) < target) {
-                if (globaltimer_ns() - t0 > kWaitBudgetNs) {
-                    atomicOr(status, code);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-        s_ok = ok;
-    }
-    __syncthreads();
-    return s_ok != 0;
-}
-
-__device__ __forceinline__ bool grid_sync(unsigned long long* ticket, uint32_t* status, uint32_t code) {
-    return grid_wait(ticket, grid_arrive(ticket), status, code);
-}
 
 // ---------------------------------------------------------------------------
 // bf16 helpers

@@ -107,7 +107,7 @@ def test_full_layer_batch8_zipf(full_layer):
 
 
 def test_repeated_calls_on_one_workspace_are_deterministic(full_layer):
-    # the grid barrier's counters are left ready for the next call
+    # the exchange counts are back at zero after every call
     x = margin_x(synth.bits(full_layer.L.router_w), 8, 2048, 6, None, seed=10)
     ws = full_layer.workspace(6)
     outs = [_run(full_layer, x, 6, ws=ws) for _ in range(4)]
