@@ -31,39 +31,52 @@ def bf16_ulp(v):
     return 2.0 ** (np.floor(np.log2(mag)) - 7)
 
 
-def assert_close(y_gpu_bits, y_ref_bits, what="", flips=None):
+def assert_close(y_gpu_bits, y_ref_bits, what="", terms=None):
     """The layer tolerance: relative L2 error <= REL_L2 and per element
     |gpu - ref| <= ELEM_A (|ref| + ELEM_B).
 
-    flips (optional, [T, H], from layer_flips): per output element, the
-    change that one flipped bf16 rounding of each term of the combine can
-    make. The GPU and the oracle both sum in FP32, in different orders; where
-    an exact sum lies near a bf16 rounding boundary their two FP32 sums can
-    fall on either side of it, so that d_j (or d_shared) rounds one ulp apart
-    and y moves by w_j ulp(d_j) (or ulp(d_shared)). Where the terms cancel
-    (|y| much smaller than the terms) that exceeds the relative bound without
-    an error on either side. With `flips`, an element outside the per-element
-    bound still passes if its error is within flips, and such elements must be
-    rare (at most 0.1 %, at least one allowed); relative L2 still holds for all."""
+    terms (optional, [T, H], from combine_terms): per output element the
+    magnitude sum_j |w_j d_j| + |d_shared| of the terms the combine adds. The
+    GPU and the oracle both compute in FP32 with bf16 at the stated rounding
+    points, in different summation orders; near a bf16 rounding boundary
+    their g, u, h or d then round one ulp apart, and a few such steps can move
+    y by a few bf16 ulps of the terms. Where the terms cancel (|y| much
+    smaller than them) that exceeds the bound relative to |y| without an
+    error on either side: an evaluation of the oracle's own definition in
+    another FP32 order (tests/test_oracle_tolerance.py) does so. With
+    `terms`, an element outside the per-element bound still passes if its
+    error is within the same bound relative to the terms, ELEM_A (terms +
+    ELEM_B), and such elements must be rare (at most 0.1 %, at least one
+    allowed); relative L2 still holds for all."""
     a, r = bf16_to_f64(y_gpu_bits), bf16_to_f64(y_ref_bits)
     assert np.all(np.isfinite(a)), f"{what}: non-finite GPU output"
     rel = np.linalg.norm(a - r) / max(np.linalg.norm(r), 1e-30)
     assert rel <= REL_L2, f"{what}: relative L2 error {rel:.3e} > {REL_L2}"
     err = np.abs(a - r)
     bad = err > ELEM_A * (np.abs(r) + ELEM_B)
-    if flips is not None and bad.any():
-        flip = bad & (err <= np.asarray(flips, np.float64))
-        assert flip.sum() <= max(1, 1e-3 * bad.size), f"{what}: {int(flip.sum())} rounding-flip outliers"
-        bad = bad & ~flip
+    if terms is not None and bad.any():
+        cancel = bad & (err <= ELEM_A * (np.asarray(terms, np.float64) + ELEM_B))
+        assert cancel.sum() <= max(1, 1e-3 * bad.size), f"{what}: {int(cancel.sum())} cancellation outliers"
+        bad = bad & ~cancel
     assert not bad.any(), f"{what}: {int(bad.sum())} elements outside tolerance, e.g. gpu {a[bad][:4]} ref {r[bad][:4]}"
     return rel
 
 
-def layer_flips(x_bits, ids, weights, dl):
-    """Per token and output row: sum_j |w_j| ulp(d_j) + ulp(d_shared) + ulp(y),
-    the change of y that one flipped bf16 rounding of each combined term (and
-    of y itself) can make, from the oracle's per-expert outputs (for
-    assert_close)."""
+def terms_where_needed(y_gpu_bits, y_ref_bits, terms_of_rows):
+    """The `terms` argument of assert_close, computed (by terms_of_rows(rows))
+    only for the rows (tokens) that have an element outside the per-element
+    bound; 0 elsewhere, where no element needs it."""
+    a, r = bf16_to_f64(y_gpu_bits), bf16_to_f64(y_ref_bits)
+    rows = np.nonzero((np.abs(a - r) > ELEM_A * (np.abs(r) + ELEM_B)).any(axis=1))[0]
+    terms = np.zeros(r.shape)
+    if rows.size:
+        terms[rows] = terms_of_rows(rows)
+    return terms
+
+
+def combine_terms(x_bits, ids, weights, dl):
+    """Per token and output row: sum_j |w_j d_j| + |d_shared|, the magnitude of
+    the terms the combine adds, from the oracle's per-expert outputs."""
     args = dl.oracle_args()
     L = dl.L
     H, I = L.H, L.I
@@ -72,25 +85,21 @@ def layer_flips(x_bits, ids, weights, dl):
     per = lambda a, e: np.ascontiguousarray(a.reshape(L.E, -1)[e])  # noqa: E731
     out = np.zeros((T, H))
     for t in range(T):
-        total = np.zeros(H)
         for j in range(k):
             e = int(ids[t, j])
             ts = args["ts"][e] if args["ts"] is not None else (1.0, 1.0, 1.0)
             _, _, _, d = oracle.expert(x_bits[t], per(args["gate"], e), per(args["up"], e),
                                        per(args["down"], e), H, I, ts=ts, wdtype=args["wdtype"])
-            dv = bf16_to_f64(d)
-            out[t] += abs(float(weights[t, j])) * bf16_ulp(dv)
-            total += float(weights[t, j]) * dv
+            out[t] += np.abs(float(weights[t, j]) * bf16_to_f64(d))
         sh = args["shared"]
         if sh is not None:
             ts = sh["ts"] if sh["ts"] is not None else (1.0, 1.0, 1.0)
             _, _, _, d = oracle.expert(x_bits[t], sh["gate"].reshape(-1), sh["up"].reshape(-1),
                                        sh["down"].reshape(-1), H, sh["I"], ts=ts, wdtype=args["wdtype"])
-            dv = bf16_to_f64(d)
-            out[t] += bf16_ulp(dv)
-            total += dv
-        out[t] += bf16_ulp(total)
+            out[t] += np.abs(bf16_to_f64(d))
     return out
+
+
 
 
 def margin_x(router_bits, T, H, k, bias, seed, margin=MARGIN):

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from flint_testlib import DeviceLayer, assert_close, flint, layer_flips, margin_x
+from flint_testlib import DeviceLayer, assert_close, flint, combine_terms, margin_x
 from nvfp4_moe_decode_sigmoid_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -33,9 +33,9 @@ def _check(dl, x, k, flags=0, bias=None):
     for t in range(x.shape[0]):
         assert set(ids[t]) == set(rids[t])
     ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
-    flips = layer_flips(synth.bits(x), rids, rw, dl)
-    assert_close(y, ref, "bf16 layer (gpu routing)", flips=flips)
-    assert_close(y, ry, "bf16 layer (oracle routing)", flips=flips)
+    terms = combine_terms(synth.bits(x), rids, rw, dl)
+    assert_close(y, ref, "bf16 layer (gpu routing)", terms=terms)
+    assert_close(y, ry, "bf16 layer (oracle routing)", terms=terms)
     return y
 
 

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from flint_testlib import DeviceLayer, assert_close, flint, layer_flips, margin_x
+from flint_testlib import DeviceLayer, assert_close, flint, combine_terms, margin_x
 from nvfp4_moe_decode_sigmoid_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -34,9 +34,9 @@ def _check_layer(dl, x, k, bias=None, flags=0):
         assert set(ids[t]) == set(rids[t])
     # the experts' outputs given the GPU's own routing (same ids, its weights)
     ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
-    flips = layer_flips(synth.bits(x), rids, rw, dl)
-    assert_close(y, ref, "layer (gpu routing)", flips=flips)
-    assert_close(y, ry, "layer (oracle routing)", flips=flips)
+    terms = combine_terms(synth.bits(x), rids, rw, dl)
+    assert_close(y, ref, "layer (gpu routing)", terms=terms)
+    assert_close(y, ry, "layer (oracle routing)", terms=terms)
     return y
 
 
@@ -87,7 +87,7 @@ def test_decode_with_repeated_and_shared_ids(small_layer):
                        ws)
     assert f.flint_workspace_check(ws) == f.FLINT_OK
     ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
-    assert_close(synth.bits(y), ref, "repeated ids", flips=layer_flips(synth.bits(x), ids, w, dl))
+    assert_close(synth.bits(y), ref, "repeated ids", terms=combine_terms(synth.bits(x), ids, w, dl))
 
 
 def test_out_of_range_id_is_reported_not_read(small_layer):
@@ -120,7 +120,7 @@ def test_full_layer_batch1_after_route(full_layer):
     x = margin_x(synth.bits(full_layer.L.router_w), 1, 2048, 6, None, seed=17)
     ids, w, y = _layer_run(full_layer, x, 6, flags=f.FLINT_PDL | f.FLINT_PDL_AFTER_ROUTE, route_flags=f.FLINT_PDL)
     ref = oracle.moe_experts(synth.bits(x), ids, w, **full_layer.oracle_args())
-    assert_close(y, ref, "layer (x staged before the wait)", flips=layer_flips(synth.bits(x), ids, w, full_layer))
+    assert_close(y, ref, "layer (x staged before the wait)", terms=combine_terms(synth.bits(x), ids, w, full_layer))
 
 
 def test_full_layer_batch8_uniform(full_layer):

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from flint_testlib import DeviceLayer, assert_close, flint, layer_flips, margin_x
+from flint_testlib import DeviceLayer, assert_close, flint, combine_terms, margin_x
 from nvfp4_moe_decode_sigmoid_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -32,9 +32,9 @@ def _check(dl, x, k, bias=None, flags=0):
     assert np.array_equal(ids, rids), f"selection differs: {ids} vs {rids}"
     assert np.allclose(w, rw, rtol=2e-6, atol=1e-7), f"weights differ: {w} vs {rw}"
     ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
-    flips = layer_flips(synth.bits(x), rids, rw, dl)
-    assert_close(y, ref, "fused layer (gpu routing)", flips=flips)
-    assert_close(y, ry, "fused layer (oracle routing)", flips=flips)
+    terms = combine_terms(synth.bits(x), rids, rw, dl)
+    assert_close(y, ref, "fused layer (gpu routing)", terms=terms)
+    assert_close(y, ry, "fused layer (oracle routing)", terms=terms)
     return ids, w, y
 
 
@@ -129,7 +129,7 @@ def test_matches_the_three_kernel_path(full_layer):
     f.flint_moe_decode(xc, ids2, w2, full_layer.routed, full_layer.shared, y2, ws)
     assert np.array_equal(ids, ids2.cpu().numpy())
     assert np.allclose(w, w2.cpu().numpy(), rtol=2e-6, atol=1e-7)
-    assert_close(y, synth.bits(y2), "fused vs three kernels", flips=2 * layer_flips(synth.bits(x), ids, w, full_layer))
+    assert_close(y, synth.bits(y2), "fused vs three kernels", terms=combine_terms(synth.bits(x), ids, w, full_layer))
 
 
 def test_pdl_chained_layers_in_a_graph_match_single_calls(full_layer):

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from flint_testlib import DeviceLayer, MARGIN, assert_close, bf16_to_f64, layer_flips, flint
+from flint_testlib import DeviceLayer, MARGIN, assert_close, bf16_to_f64, combine_terms, flint
 from nvfp4_moe_decode_sigmoid_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -106,7 +106,7 @@ def check_block(dl, r, y_prev, k, flags=0):
     # the oracle's norm to one ulp): the same inputs on both sides
     gids, gw, gy = oracle.moe_layer(x_out, synth.bits(dl.L.router_w), k, **dl.oracle_args())
     assert np.array_equal(ids, gids)
-    assert_close(y, gy, "block", flips=layer_flips(x_out, gids, gw, dl))
+    assert_close(y, gy, "block", terms=combine_terms(x_out, gids, gw, dl))
     return ids, y
 
 
@@ -292,7 +292,7 @@ def test_short_stack_matches_oracle(stack):
         else:
             args = {kk: v for kk, v in b.items() if kk not in ("kind", "wr", "k")}
             gids, gw, gy = oracle.moe_layer(x, b["wr"], k, **args)
-            assert_close(y_out, gy, "moe block", flips=layer_flips(x, gids, gw, blk["_dl"]))
+            assert_close(y_out, gy, "moe block", terms=combine_terms(x, gids, gw, blk["_dl"]))
     rr, _, rids = oracle.decode_stack(synth.bits(x0), ob, EPS)
     for a, b in zip(ids, rids):
         for t in range(a.shape[0]):

@@ -32,7 +32,7 @@ def test_fused_layer_lost_cta_times_out_and_the_workspace_recovers():
     import numpy as np
 
     import oracle
-    from flint_testlib import DeviceLayer, assert_close, layer_flips, margin_x
+    from flint_testlib import DeviceLayer, assert_close, combine_terms, margin_x
 
     f = flint()
     dl = DeviceLayer(synth.Layer(17, H=1024, E=16, I=256, I_shared=256))
@@ -60,4 +60,4 @@ def test_fused_layer_lost_cta_times_out_and_the_workspace_recovers():
     assert f.flint_workspace_check(ws) == f.FLINT_OK
     rids, rw, ry = oracle.moe_layer(synth.bits(x), synth.bits(dl.L.router_w), k, **dl.oracle_args())
     assert np.array_equal(ids.cpu().numpy(), rids)
-    assert_close(synth.bits(y), ry, "after recovery", flips=layer_flips(synth.bits(x), rids, rw, dl))
+    assert_close(synth.bits(y), ry, "after recovery", terms=combine_terms(synth.bits(x), rids, rw, dl))
