@@ -191,6 +191,11 @@ class Model:
             self.layers.append(dict(router_w=L.router_w, routed=routed, shared=shared, seed=1000 + li))
             del L, s
             torch.cuda.synchronize()
+        # each layer pulls the next one's router and shared expert into L2
+        # before its PDL wait (static weights, as in a model's layer chain)
+        for li, lay in enumerate(self.layers):
+            nx = self.layers[(li + 1) % n_layers]
+            lay["next_pf"] = F.l2_prefetch(nx["router_w"], nx["shared"].gate_up, nx["shared"].down)
         self.ws = torch.empty(F.flint_workspace_bytes(E, TOPK, H, I, I_SHARED), dtype=torch.uint8, device=device)
         F.flint_workspace_init(self.ws)
 
@@ -219,7 +224,7 @@ def run_step(F, model, inp, li, bias, flags, path="fused"):
     lay, io = model.layers[li], inp[li]
     if path == "fused":
         F.flint_moe_layer(io["x"], lay["router_w"], TOPK, lay["routed"], lay["shared"], io["ids"], io["w"], io["y"],
-                          model.ws, bias=bias, flags=flags)
+                          model.ws, bias=bias, flags=flags, next=lay["next_pf"])
         return
     F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], model.ws, bias=bias, flags=flags)
     dflags = flags | (F.FLINT_PDL_AFTER_ROUTE if flags & F.FLINT_PDL else 0)
@@ -352,6 +357,9 @@ class Stack:
                                                             H, I_SHARED)))
             del L, s
             torch.cuda.synchronize()
+        for i, lay in enumerate(self.moe):  # each block pulls the next one's static weights into L2
+            nx = self.moe[i + 1] if i + 1 < len(self.moe) else None
+            lay["next_pf"] = F.l2_prefetch(nx["router_w"], nx["shared"].gate_up, nx["shared"].down) if nx else None
         self.ws = torch.empty(F.flint_workspace_bytes(E, TOPK, H, I, I_SHARED), dtype=torch.uint8, device=device)
         F.flint_workspace_init(self.ws)
 
@@ -376,7 +384,7 @@ class Stack:
         for i, lay in enumerate(self.moe):
             yo = y[(N_DENSE + i) % 2]
             F.flint_moe_block(src, lay["router_w"], TOPK, lay["routed"], lay["shared"], ids[i], w[i], yo, self.ws,
-                              y_prev=y_prev, residual_out=r[nxt], flags=flags)
+                              y_prev=y_prev, residual_out=r[nxt], flags=flags, next=lay["next_pf"])
             src, nxt = r[nxt], 1 - nxt
             y_prev = yo
         F.flint_residual_rmsnorm(src, io["xf"], y_prev=y_prev, residual_out=io["r_final"], flags=flags)
@@ -509,7 +517,8 @@ def measure_kernels(F, model, name, reps=8):
     stream = torch.cuda.Stream()
     calls = {
         "layer": lambda lay, io: F.flint_moe_layer(io["x"], lay["router_w"], TOPK, lay["routed"], lay["shared"],
-                                                   io["ids"], io["w"], io["y"], model.ws, bias=bias),
+                                                   io["ids"], io["w"], io["y"], model.ws, bias=bias,
+                                                   next=lay["next_pf"]),
         "route": lambda lay, io: F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], model.ws,
                                                    bias=bias),
         "gate_up": lambda lay, io: F.flint_moe_gate_up(io["x"], io["ids"], lay["routed"], lay["shared"], model.ws),
@@ -594,7 +603,7 @@ def measure_e2e(F, model, name, steps, graph_steps):
         lay, io = model.layers[li], inp[li]
         io["x"].copy_(hx[li], non_blocking=True)
         F.flint_moe_layer(io["x"], lay["router_w"], TOPK, lay["routed"], lay["shared"], io["ids"], io["w"], hy[li],
-                          model.ws, bias=bias, flags=flags)
+                          model.ws, bias=bias, flags=flags, next=lay["next_pf"])
 
     def copy_step(li, flags):
         inp[li]["x"].copy_(hx[li], non_blocking=True)
@@ -642,7 +651,7 @@ def measure_e2e(F, model, name, steps, graph_steps):
                 stream.wait_event(evs[s])
                 lay, io = model.layers[li], inp[li]
                 F.flint_moe_layer(io["x"], lay["router_w"], TOPK, lay["routed"], lay["shared"], io["ids"], io["w"],
-                                  hy[li], model.ws, bias=bias, flags=F.FLINT_PDL)
+                                  hy[li], model.ws, bias=bias, flags=F.FLINT_PDL, next=lay["next_pf"])
         with torch.cuda.stream(stream):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -850,6 +859,8 @@ def run_flint(args):
             "config": {"workload": args.workload, "tokens": T, "routing": routing, "hidden": H, "experts": E,
                        "top_k": TOPK, "inter": I, "shared_inter": I_SHARED, "weights": "nvfp4 (e2m1 + ue4m3/16 + fp32)",
                        "activations": "bf16", "layers_rotated": args.layers, "pdl": True,
+                       "prefetch": "each layer pulls the next one's router and shared expert into L2 before its "
+                                   "PDL wait",
                        "path": "flint_moe_layer: one cooperative kernel per layer",
                        "graph_steps": args.graph_steps,
                        "l2": f"inputs larger than L2: {args.layers} resident layers cycled, reuse distance "

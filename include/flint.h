@@ -294,6 +294,20 @@ flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, 
                                 void* ws, size_t ws_bytes, unsigned flags, void* stream);
 
 /*
+ * Byte ranges of the NEXT layer's static weights (its router rows, its shared
+ * expert) that flint_moe_layer / flint_moe_block pull into L2 while this
+ * layer routes (its HBM traffic is low then): those addresses do not depend
+ * on data ("Optimizations": each kernel loads its weights while the previous
+ * one runs). Up to four ranges; a range has a
+ * 16-byte aligned start and a size that is a multiple of 16 (0: unused); the
+ * sizes sum to less than 4 GiB. Pass NULL for none.
+ */
+typedef struct flint_l2_prefetch {
+    const void* ptr[4];
+    size_t bytes[4];
+} flint_l2_prefetch;
+
+/*
  * flint_moe_layer -- the whole decode step of one MoE layer in ONE kernel:
  * router GEMV + sigmoid top-k + renormalisation (as flint_moe_route), the
  * gate/up GEMVs + SiLU and the down GEMVs + combine (as flint_moe_decode).
@@ -302,11 +316,13 @@ flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, 
  * each kernel loads its weights while the previous one runs.) One CTA per SM,
  * all resident (cooperative launch). A group of CTAs runs the shared expert,
  * whose weights they start loading before the PDL wait; the rest split the
- * selected experts' gate/up pairs and down rows by cost. CTAs exchange the
- * router scores and h through the workspace under release / acquire counters
- * (a CTA waits only for the scores and for the h of the experts it uses; no
- * grid-wide barrier), and the combine of each 16-row block of y is done by
- * the CTA that delivers its last expert output.
+ * selected experts' gate/up pairs (and, from two tokens, their down rows) by
+ * cost. CTAs exchange the router scores and h through the workspace under
+ * release / acquire counts (a CTA waits only for the scores and for the h of
+ * the experts it uses; no grid-wide barrier); the combine of each 16-row
+ * block of y is done by the CTA that delivers its last expert output. At one
+ * token down and the combine are split by output rows instead: every CTA
+ * computes its rows of y from all of h, with no exchange of d.
  *   x [T, H] bf16 (H = routed->hidden, H % 1024 == 0, H <= 8192), router_w
  *   [E, H] bf16 with E = routed->num_experts, bias [E] FP32 or NULL,
  *   1 <= k <= min(8, E). ids [T, k] int32 and weights [T, k] FP32 are written
@@ -318,14 +334,16 @@ flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, 
  *   and re-initialises the workspace.
  *   flags: FLINT_PDL lets the launch overlap the previous kernel of the stream
  *   (this kernel waits for it before reading x or the workspace).
- *   Errors: FLINT_ERR_UNSUPPORTED when one CTA's shared memory cannot hold
+ *   next: the next layer's ranges to pull into L2 (above), or NULL.
+ *   Errors: FLINT_ERR_INVALID_ARG for a misaligned or oversized prefetch
+ *   range; FLINT_ERR_UNSUPPORTED when one CTA's shared memory cannot hold
  *   the layer's working set, the device cannot co-schedule one CTA per SM, or
  *   the experts are not NVFP4.
  */
 flint_status_t flint_moe_layer(const flint_bf16* x, int T, const flint_bf16* router_w, int E, const float* bias,
                                int k, const flint_experts* routed, const flint_experts* shared, int32_t* ids,
-                               float* weights, flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
-                               void* stream);
+                               float* weights, flint_bf16* y, void* ws, size_t ws_bytes,
+                               const flint_l2_prefetch* next, unsigned flags, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Residual stream of the decode stack                                       */
@@ -369,8 +387,8 @@ flint_status_t flint_residual_rmsnorm(const flint_norm* norm, int T, int H, unsi
  */
 flint_status_t flint_moe_block(const flint_norm* norm, int T, const flint_bf16* router_w, int E, const float* bias,
                                int k, const flint_experts* routed, const flint_experts* shared, int32_t* ids,
-                               float* weights, flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
-                               void* stream);
+                               float* weights, flint_bf16* y, void* ws, size_t ws_bytes,
+                               const flint_l2_prefetch* next, unsigned flags, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Prefill: the MoE layer over many tokens, on the tensor cores               */

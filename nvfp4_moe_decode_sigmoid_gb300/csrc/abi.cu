@@ -552,10 +552,21 @@ flint_status_t flint_residual_rmsnorm(const flint_norm* norm, int T, int H, unsi
 static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, const flint_norm* norm, int T,
                                      const flint_bf16* router_w, int E, const float* bias, int k,
                                      const flint_experts* routed, const flint_experts* shared, int32_t* ids,
-                                     float* weights, flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
-                                     void* stream) {
+                                     float* weights, flint_bf16* y, void* ws, size_t ws_bytes,
+                                     const flint_l2_prefetch* next, unsigned flags, void* stream) {
     flint_status_t s = moe_common(what, T, k, routed, shared, true);
     if (s != FLINT_OK) return s;
+    unsigned long long pf_granules = 0;
+    if (next) {
+        for (int r = 0; r < 4; ++r) {
+            if (next->bytes[r] == 0) continue;
+            if (!next->ptr[r] || !aligned(next->ptr[r], 16) || next->bytes[r] % 16)
+                return fail(FLINT_ERR_INVALID_ARG, "%s: prefetch range %d misaligned (16-byte start and size)", what, r);
+            pf_granules += next->bytes[r] / 16;
+        }
+        if (pf_granules >= (1ull << 28))
+            return fail(FLINT_ERR_INVALID_ARG, "%s: prefetch ranges sum to 4 GiB or more", what);
+    }
     flint::NormArgs na = {};
     if (norm) {
         if ((s = norm_args(what, norm, T, routed->hidden, false, na)) != FLINT_OK) return s;
@@ -615,6 +626,11 @@ static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, cons
     a.s_ts = shared ? shared->tensor_scale : nullptr;
     a.y = y;
     a.norm = na;
+    for (int r = 0; r < 4; ++r) {
+        a.pf_ptr[r] = next && next->bytes[r] ? static_cast<const uint8_t*>(next->ptr[r]) : nullptr;
+        a.pf_bytes[r] = next && next->bytes[r] ? (unsigned long long)next->bytes[r] : 0ull;
+    }
+    a.pf_granules = pf_granules;
     if (!layer_shape(a, d.sm_count, d.smem_optin))
         return fail(FLINT_ERR_UNSUPPORTED, "%s: shapes exceed one CTA's shared memory", what);
     cudaError_t e = flint::launch_layer(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
@@ -623,18 +639,19 @@ static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, cons
 
 flint_status_t flint_moe_layer(const flint_bf16* x, int T, const flint_bf16* router_w, int E, const float* bias, int k,
                                const flint_experts* routed, const flint_experts* shared, int32_t* ids, float* weights,
-                               flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags, void* stream) {
+                               flint_bf16* y, void* ws, size_t ws_bytes, const flint_l2_prefetch* next,
+                               unsigned flags, void* stream) {
     return moe_layer_impl("layer", x, nullptr, T, router_w, E, bias, k, routed, shared, ids, weights, y, ws, ws_bytes,
-                          flags, stream);
+                          next, flags, stream);
 }
 
 flint_status_t flint_moe_block(const flint_norm* norm, int T, const flint_bf16* router_w, int E, const float* bias,
                                int k, const flint_experts* routed, const flint_experts* shared, int32_t* ids,
-                               float* weights, flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
-                               void* stream) {
+                               float* weights, flint_bf16* y, void* ws, size_t ws_bytes,
+                               const flint_l2_prefetch* next, unsigned flags, void* stream) {
     if (!norm) return fail(FLINT_ERR_INVALID_ARG, "block: norm is null");
     return moe_layer_impl("block", nullptr, norm, T, router_w, E, bias, k, routed, shared, ids, weights, y, ws,
-                          ws_bytes, flags, stream);
+                          ws_bytes, next, flags, stream);
 }
 
 size_t flint_prefill_workspace_bytes(int tokens, int num_experts, int top_k, int hidden, int inter, int inter_shared) {

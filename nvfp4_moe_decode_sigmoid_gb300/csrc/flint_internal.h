@@ -204,6 +204,9 @@ struct LayerArgs {
     int ns, slot;        // ring slots per warp (kLayerSlots) and bytes per slot
     int stage_vals, stage_scales;  // bytes of the staging region (x, later h) and of its chunk scales
     int rows;            // down split by output rows (the ROWS instantiation)
+    const uint8_t* pf_ptr[4];      // the next layer's ranges to pull into L2 before the PDL wait
+    unsigned long long pf_bytes[4];
+    unsigned long long pf_granules;  // their total in 16-byte granules
     int rows_max;        // ROWS: most output rows of a CTA (ceil(H / G))
     int rg;              // ROWS: rows per down item (a power of two, at most 8)
     NormArgs norm;       // norm.r set: x = the norm of the residual stream (x unused)

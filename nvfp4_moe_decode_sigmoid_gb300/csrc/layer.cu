@@ -564,6 +564,26 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 #endif
     }
     FLINT_PHASE(3);
+    // The next layer's static weights into L2, issued once this CTA's router
+    // scores are out (HBM is otherwise idle while the routing runs; issued
+    // before the PDL wait it measured slower, competing with the previous
+    // kernel's stream): CTA c takes granules [c n / G, (c + 1) n / G) of the
+    // ranges' concatenation (16-byte granules), in bulk L2 prefetches of up
+    // to 32 KB.
+    if (tid == kLT - 1 && a.pf_granules) {
+        const unsigned long long g0 = a.pf_granules * c / G, g1 = a.pf_granules * (c + 1) / G;
+        unsigned long long base = 0;
+        for (int r = 0; r < 4; ++r) {
+            const unsigned long long n = a.pf_bytes[r] / 16;
+            const unsigned long long lo = max(g0, base), hi = min(g1, base + n);
+            for (unsigned long long q = lo; q < hi;) {
+                const unsigned long long m = min(hi - q, 2048ull);
+                bulk_prefetch_l2(a.pf_ptr[r] + (q - base) * 16, (uint32_t)(m * 16));
+                q += m;
+            }
+            base += n;
+        }
+    }
 
     // Routing in this CTA: once all E router rows are published, all T x E
     // scores into shared memory over the router rows and the top-k of each

@@ -57,6 +57,22 @@ class flint_norm(C.Structure):
                 ("reserved", C.c_float), ("residual_out", C.c_void_p), ("x_out", C.c_void_p)]
 
 
+class flint_l2_prefetch(C.Structure):
+    _fields_ = [("ptr", C.c_void_p * 4), ("bytes", C.c_size_t * 4)]
+
+
+def l2_prefetch(*tensors):
+    """The next layer's weights (up to four device tensors, each 16-byte
+    aligned with a size that is a multiple of 16) for flint_moe_layer /
+    flint_moe_block to pull into L2 before their PDL wait."""
+    assert len(tensors) <= 4
+    p = flint_l2_prefetch()
+    for i, t in enumerate(tensors):
+        p.ptr[i] = t.data_ptr()
+        p.bytes[i] = t.numel() * t.element_size()
+    return p
+
+
 def _load():
     if not os.path.exists(_LIB_PATH):
         raise ImportError(f"libflint.so is not built ({_LIB_PATH}); run __graft_entry__.build() first")
@@ -87,13 +103,14 @@ def _load():
         "flint_selftest_wait_timeout": (i32, [vp, sz, C.c_uint64, vp]),
         "flint_moe_route_static": (i32, [vp, i32, i32, vp, i32, vp, i32, vp, vp, u32, vp]),
         "flint_moe_layer": (i32, [vp, i32, vp, i32, vp, i32, C.POINTER(flint_experts), C.POINTER(flint_experts), vp,
-                                  vp, vp, vp, sz, u32, vp]),
+                                  vp, vp, vp, sz, C.POINTER(flint_l2_prefetch), u32, vp]),
         "flint_residual_rmsnorm": (i32, [C.POINTER(flint_norm), i32, i32, u32, vp]),
         "flint_prefill_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "flint_moe_prefill": (i32, [vp, i32, vp, i32, vp, i32, C.POINTER(flint_experts), C.POINTER(flint_experts),
                                     vp, vp, vp, vp, sz, u32, vp]),
         "flint_moe_block": (i32, [C.POINTER(flint_norm), i32, vp, i32, vp, i32, C.POINTER(flint_experts),
-                                  C.POINTER(flint_experts), vp, vp, vp, vp, sz, u32, vp]),
+                                  C.POINTER(flint_experts), vp, vp, vp, vp, sz, C.POINTER(flint_l2_prefetch), u32,
+                                  vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -284,13 +301,14 @@ def flint_moe_decode(x, ids, weights, routed: Experts, shared: Experts | None, y
 
 
 def flint_moe_layer(x, router_w, k, routed: Experts, shared: Experts | None, ids, weights, y, ws, bias=None, flags=0,
-                    stream=None):
-    """The whole layer in one launch: routing (ids, weights written) and y."""
+                    stream=None, next=None):
+    """The whole layer in one launch: routing (ids, weights written) and y.
+    next: l2_prefetch(...) of the next layer's weights, or None."""
     T = x.shape[0]
     E = router_w.shape[0]
     _check(_lib.flint_moe_layer(_ptr(x), T, _ptr(router_w), E, _ptr(bias), k, _ex(routed), _ex(shared), _ptr(ids),
-                                _ptr(weights), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(), flags,
-                                _stream(stream)), "moe_layer")
+                                _ptr(weights), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(),
+                                C.byref(next) if next is not None else None, flags, _stream(stream)), "moe_layer")
 
 
 def _norm(residual, y_prev, gamma, eps, residual_out, x_out):
@@ -311,15 +329,16 @@ def flint_residual_rmsnorm(residual, x_out, y_prev=None, residual_out=None, gamm
 
 def flint_moe_block(residual, router_w, k, routed: Experts, shared: Experts | None, ids, weights, y, ws,
                     y_prev=None, residual_out=None, x_out=None, gamma=None, eps=1e-6, bias=None, flags=0,
-                    stream=None):
+                    stream=None, next=None):
     """One pre-norm MoE block in one launch: x = rmsnorm(residual + y_prev)
-    (residual_out receives the sum), then the MoE layer on x into y."""
+    (residual_out receives the sum), then the MoE layer on x into y.
+    next: l2_prefetch(...) of the next block's weights, or None."""
     T = residual.shape[0]
     E = router_w.shape[0]
     n = _norm(residual, y_prev, gamma, eps, residual_out, x_out)
     _check(_lib.flint_moe_block(C.byref(n), T, _ptr(router_w), E, _ptr(bias), k, _ex(routed), _ex(shared),
-                                _ptr(ids), _ptr(weights), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(), flags,
-                                _stream(stream)), "moe_block")
+                                _ptr(ids), _ptr(weights), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(),
+                                C.byref(next) if next is not None else None, flags, _stream(stream)), "moe_block")
 
 
 def flint_prefill_workspace_bytes(tokens: int, num_experts: int, top_k: int, hidden: int, inter: int,

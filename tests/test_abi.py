@@ -86,9 +86,17 @@ def test_host_validation_without_a_gpu(flint):
     assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(bf), C.byref(bf_sh), p, p, 1 << 24, 0, None) == \
         flint.FLINT_ERR_UNSUPPORTED
     assert "same dtype" in flint.flint_last_error()
-    assert L.flint_moe_layer(p, 1, p, 256, None, 6, C.byref(bf), None, p, p, p, p, 1 << 24, 0, None) == \
+    assert L.flint_moe_layer(p, 1, p, 256, None, 6, C.byref(bf), None, p, p, p, p, 1 << 24, None, 0, None) == \
         flint.FLINT_ERR_UNSUPPORTED
     assert "NVFP4" in flint.flint_last_error()
+    # the next layer's L2 prefetch ranges: 16-byte start and size, under 4 GiB in all
+    ex4 = flint.flint_experts(0, 256, 2048, 512, 0x1000, 0x1000, 0x1000)
+    for ptr, n in ((0x1008, 4096), (0x1000, 100), (0x1000, 1 << 32)):
+        pf = flint.flint_l2_prefetch()
+        pf.ptr[1], pf.bytes[1] = ptr, n
+        assert L.flint_moe_layer(p, 1, p, 256, None, 6, C.byref(ex4), None, p, p, p, p, 1 << 24, C.byref(pf), 0,
+                                 None) == flint.FLINT_ERR_INVALID_ARG
+        assert "prefetch" in flint.flint_last_error()
     # NVFP4 experts need their tensor scales
     nots = flint.flint_experts(0, 256, 2048, 512, 0x1000, 0x1000, None)
     assert L.flint_moe_decode(p, 1, p, p, 6, C.byref(nots), None, p, p, 1 << 24, 0, None) == \
@@ -126,8 +134,8 @@ def test_norm_validation_without_a_gpu(flint):
     # block: y may not overlap the norm's buffers
     ex = flint.flint_experts(0, 256, 2048, 512, 0x1000, 0x1000, 0x1000)
     assert L.flint_moe_block(C.byref(n), 1, p, 256, None, 6, C.byref(ex), None, p, p, C.c_void_p(0x20000), p,
-                             1 << 24, 0, None) == flint.FLINT_ERR_INVALID_ARG
-    assert L.flint_moe_block(None, 1, p, 256, None, 6, C.byref(ex), None, p, p, o, p, 1 << 24, 0, None) == \
+                             1 << 24, None, 0, None) == flint.FLINT_ERR_INVALID_ARG
+    assert L.flint_moe_block(None, 1, p, 256, None, 6, C.byref(ex), None, p, p, o, p, 1 << 24, None, 0, None) == \
         flint.FLINT_ERR_INVALID_ARG
     del q
 

@@ -174,3 +174,24 @@ def test_pdl_chained_layers_in_a_graph_match_single_calls(full_layer):
     for (x, t), (ids, w, y), (ri, rw, ry) in zip(steps, outs, ref):
         assert torch.equal(ids[:t], ri) and torch.equal(w[:t], rw)
         assert torch.equal(y[:t].view(torch.int16), ry.view(torch.int16))
+
+
+def test_next_layer_prefetch_changes_nothing(full_layer):
+    """flint_moe_layer with the next layer's ranges to pull into L2 (here
+    another layer's router and shared expert, and the ranges at any offset of
+    16 bytes) gives the same bits as without."""
+    f = flint()
+    other = DeviceLayer(synth.Layer(1008))
+    x = margin_x(synth.bits(full_layer.L.router_w), 3, 2048, 6, None, seed=21)
+    base = _run(full_layer, x, 6)
+    nxt = f.l2_prefetch(other.router_w, other.shared.gate_up[16:], other.shared.down[: 4096 * 16])
+    ids = torch.empty((3, 6), dtype=torch.int32, device="cuda")
+    w = torch.empty((3, 6), dtype=torch.float32, device="cuda")
+    y = torch.empty((3, 2048), dtype=torch.bfloat16, device="cuda")
+    ws = full_layer.workspace(6)
+    f.flint_moe_layer(x.cuda(), full_layer.router_w, 6, full_layer.routed, full_layer.shared, ids, w, y, ws,
+                      flags=f.FLINT_PDL, next=nxt)
+    assert f.flint_workspace_check(ws) == f.FLINT_OK
+    for u, v in zip((ids.cpu().numpy(), w.cpu().numpy(), synth.bits(y)), base):
+        assert np.array_equal(u, v)
+
