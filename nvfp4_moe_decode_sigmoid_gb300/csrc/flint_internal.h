@@ -221,6 +221,7 @@ struct PrefillGemmArgs {
     const uint16_t* A;     // bf16 [rows of all groups, K], lda elements apart
     long long lda;
     const int* tile_start;
+    const int* pair_start;   // exclusive prefix of the groups' counts of M-tile pairs (two tiles per CTA)
     const int* seg_base;
     const int* seg_len;
     int n_groups, rows, K;
@@ -260,7 +261,8 @@ struct PrefillArgs {
 };
 
 struct PrefillWs {
-    size_t logits, chunk_hist, chunk_off, seg_base, seg_len, tile_start, perm, inv, h, hs, d, x_perm, ds, total;
+    size_t logits, chunk_hist, chunk_off, seg_base, seg_len, tile_start, pair_start, perm, inv, h, hs, d, x_perm, ds,
+        total;
 };
 PrefillWs prefill_ws_layout(int T, int E, int k, int H, int I, int Is);
 

@@ -40,6 +40,7 @@ namespace {
 
 constexpr int kTileM = 128, kStepK = 64;
 constexpr int kNTile = 128;  // tile N of the NVFP4 expert GEMMs (256 measured slower: 940 vs 905 us, one CTA per SM)
+constexpr int kMT = 2;       // M-tiles per CTA of the expert GEMMs (one dequantised B tile serves both)
 constexpr uint32_t kTileBytes = kTileM * kStepK * 2;  // 16 KB
 
 // 8 codes (one 32-bit word: byte b holds columns 2b, 2b + 1) times their
@@ -97,13 +98,16 @@ constexpr int kPW = 256;                // dequantise/epilogue threads
 constexpr int kPB = 2;                  // B tiles (NVFP4)
 
 // Tile N = TN (128: two CTAs per SM, 3 load stages; 256: one CTA per SM, 4
-// load stages, half the A bytes per FLOP).
-template <bool NVFP4, int TN>
+// load stages, half the A bytes per FLOP); MT M-tiles of 128 rows per CTA (2:
+// one dequantised B tile serves both; 2 load stages, so that two CTAs still
+// fit an SM: 776 us for the 8192-token layer against 922 with one M-tile,
+// and 985 with 3 stages and one CTA per SM).
+template <bool NVFP4, int TN, int MT = 1>
 struct TmaSmem {
-    static constexpr int PL = TN == 256 ? 4 : 3;                          // load stages
+    static constexpr int PL = TN == 256 ? 4 : (MT == 2 ? 2 : 3);         // load stages
     static constexpr size_t raw = (size_t)TN * 48;                        // codes + scale windows of one step
     static constexpr size_t bt = (size_t)TN * kStepK * 2;                 // one B tile
-    static constexpr size_t stage = kTileBytes + (NVFP4 ? raw : bt);
+    static constexpr size_t stage = MT * kTileBytes + (NVFP4 ? raw : bt);
     static constexpr size_t load = 0;                                     // PL x (A tile, B raw or B tile)
     static constexpr size_t btile = load + PL * stage;                    // kPB B tiles (NVFP4)
     static constexpr size_t bar = btile + (NVFP4 ? kPB * bt : 0);
@@ -112,31 +116,32 @@ struct TmaSmem {
     static constexpr size_t total = tslot + 16 + 1024;                    // + alignment slack
 };
 
-template <bool NVFP4, int EPI, int TN>
-__global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
-                                                              const __grid_constant__ CUtensorMap tma_b,
-                                                              const __grid_constant__ CUtensorMap tma_s,
-                                                              const PrefillGemmArgs a) {
+template <bool NVFP4, int EPI, int TN, int MT = 1>
+__global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(
+    const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+    const __grid_constant__ CUtensorMap tma_s, const PrefillGemmArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    using L = TmaSmem<NVFP4, TN>;
+    using L = TmaSmem<NVFP4, TN, MT>;
     constexpr int kPL = L::PL;
     constexpr int NB = TN / 64;  // 64-row boxes of B per step
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // ---- which tile ----
+    // ---- which tiles: MT consecutive M-tiles of one group (fewer at its end) ----
     int g = 0, row0, nrows;
     const int mt = blockIdx.y;
     if (a.tile_start) {
-        if (mt >= ld_cg(a.tile_start + a.n_groups)) return;
-        g = find_group(a.tile_start, a.n_groups, mt);
+        const int* starts = MT == 2 ? a.pair_start : a.tile_start;
+        if (mt >= ld_cg(starts + a.n_groups)) return;
+        g = find_group(starts, a.n_groups, mt);
         const int base = ld_cg(a.seg_base + g);
-        row0 = base + (mt - ld_cg(a.tile_start + g)) * kTileM;
-        nrows = min(kTileM, base + ld_cg(a.seg_len + g) - row0);
+        row0 = base + (mt - ld_cg(starts + g)) * (MT * kTileM);
+        nrows = min(MT * kTileM, base + ld_cg(a.seg_len + g) - row0);
     } else {
-        row0 = mt * kTileM;
+        row0 = mt * (MT * kTileM);
         if (row0 >= a.rows) return;
-        nrows = min(kTileM, a.rows - row0);
+        nrows = min(MT * kTileM, a.rows - row0);
     }
+    const int ntile = (nrows + kTileM - 1) / kTileM;  // 1 or MT
     const int nt = blockIdx.x;
     const int K = a.K, nk = K / kStepK;
     uint64_t* fullL = reinterpret_cast<uint64_t*>(smem + L::bar);
@@ -157,7 +162,7 @@ __global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(co
         fence_mbar_init();
     }
     if (warp == 9) {
-        tmem_alloc(tslot, TN);
+        tmem_alloc(tslot, MT * TN);  // accumulator of tile t at columns [t TN, (t + 1) TN)
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -169,16 +174,16 @@ __global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(co
     if (warp == 8) {
         // ---------------- loads (one thread) ----------------
         if (lane == 0) {
-            const uint32_t bytes = (uint32_t)L::stage;
+            const uint32_t bytes = (uint32_t)(L::stage - (size_t)(MT - ntile) * kTileBytes);
             for (int j = 0; j < nk && ok; ++j) {
                 const int s = j % kPL, k0 = j * kStepK;
                 if (j >= kPL) ok = mbar_wait_bounded(emptyL + s, ((j / kPL) - 1) & 1, a.status, kStatusTimeoutPrefill);
                 if (!ok) break;
                 uint8_t* st = smem + L::load + (size_t)s * L::stage;
                 mbar_arrive_expect_tx(fullL + s, bytes);
-                tma_load_2d(st, &tma_a, k0, row0, fullL + s);
+                for (int t = 0; t < ntile; ++t) tma_load_2d(st + (size_t)t * kTileBytes, &tma_a, k0, row0 + t * kTileM, fullL + s);
                 if constexpr (NVFP4) {
-                    uint8_t* codes = st + kTileBytes;
+                    uint8_t* codes = st + MT * kTileBytes;
                     uint8_t* scales = codes + TN * 32;
                     const int sx = K / 2 + ((k0 / 16) & ~15);
 #pragma unroll
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(co
                         tma_load_2d(scales + 64 * 16 * b, &tma_s, sx, brow(b), fullL + s);
                     }
                 } else {
-                    tma_load_2d(st + kTileBytes, &tma_b, k0, nt * TN, fullL + s);
+                    tma_load_2d(st + MT * kTileBytes, &tma_b, k0, nt * TN, fullL + s);
                 }
             }
         }
@@ -204,11 +209,12 @@ __global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(co
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint8_t* at = smem + L::load + (size_t)sl * L::stage;
-                const uint8_t* bt = NVFP4 ? smem + L::btile + (size_t)sb * L::bt : at + kTileBytes;
+                const uint8_t* bt = NVFP4 ? smem + L::btile + (size_t)sb * L::bt : at + MT * kTileBytes;
+                for (int t = 0; t < ntile; ++t)
 #pragma unroll
-                for (int kk = 0; kk < kStepK / 16; ++kk)
-                    tc_mma_bf16(tmem, tc_smem_desc_sw128(at + 32 * kk), tc_smem_desc_sw128(bt + 32 * kk), idesc,
-                                (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kStepK / 16; ++kk)
+                        tc_mma_bf16(tmem + (uint32_t)(t * TN), tc_smem_desc_sw128(at + (size_t)t * kTileBytes + 32 * kk),
+                                    tc_smem_desc_sw128(bt + 32 * kk), idesc, (i > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(emptyL + sl);
                 if constexpr (NVFP4) tc_commit(emptyB + sb);
             }
@@ -222,7 +228,7 @@ __global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(co
             ok = mbar_wait_bounded(fullL + sl, (i / kPL) & 1, a.status, kStatusTimeoutPrefill);
             if (ok && i >= kPB) ok = mbar_wait_bounded(emptyB + sb, ((i / kPB) - 1) & 1, a.status, kStatusTimeoutPrefill);
             if (!ok) break;
-            const uint8_t* st = smem + L::load + (size_t)sl * L::stage + kTileBytes;
+            const uint8_t* st = smem + L::load + (size_t)sl * L::stage + MT * kTileBytes;
             uint8_t* bt = smem + L::btile + (size_t)sb * L::bt;
 #pragma unroll
             for (int u = tid; u < 2 * TN; u += kPW) {
@@ -247,12 +253,12 @@ __global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(co
     if (warp < 8) {
         if (ok) ok = mbar_wait_bounded(done, 0, a.status, kStatusTimeoutPrefill);
         tc_fence_after_sync();
-        if (ok) {
+        for (int t = 0; ok && t < ntile; ++t) {
             const int wq = warp & 3, half = warp >> 2;  // lane quarter, column half
             const int r = 32 * wq + lane;              // the TMEM lane = tile row of this thread
-            const uint32_t tl = tmem + ((uint32_t)(32 * wq) << 16);
-            const bool valid = r < nrows;
-            const int p = row0 + r;
+            const uint32_t tl = tmem + (uint32_t)(t * TN) + ((uint32_t)(32 * wq) << 16);
+            const bool valid = t * kTileM + r < nrows;
+            const int p = row0 + t * kTileM + r;
             if (EPI == kEpiSwiglu) {
                 const float tsg = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride) : 1.f;
                 const float tsu = a.ts ? ld_cg(a.ts + (size_t)g * a.ts_stride + 1) : 1.f;
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(co
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 9) tmem_dealloc(tmem, TN);
+    if (warp == 9) tmem_dealloc(tmem, MT * TN);
 }
 
 // ---------------------------------------------------------------------------
@@ -353,39 +359,48 @@ __global__ void __launch_bounds__(kSortChunk) prefill_hist_kernel(const int32_t*
 }
 
 __global__ void __launch_bounds__(1024) prefill_scan_kernel(const int* chunk_hist, int nch, int E, int* chunk_off,
-                                                            int* seg_base, int* seg_len, int* tile_start) {
-    __shared__ int wsum[32], wtile[32];
+                                                            int* seg_base, int* seg_len, int* tile_start,
+                                                            int* pair_start) {
+    __shared__ int wsum[32], wtile[32], wpair[32];
     const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
     int total = 0;
     if (e < E)
         for (int c = 0; c < nch; ++c) total += chunk_hist[(size_t)c * E + e];
-    const int tiles = (total + kTileM - 1) / kTileM;
-    // exclusive scans of total and tiles over the experts
-    int it = total, tt = tiles;
+    const int tiles = (total + kTileM - 1) / kTileM, pairs = (tiles + 1) / 2;
+    // exclusive scans of total, tiles and tile pairs over the experts
+    int it = total, tt = tiles, pt = pairs;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, it, off), b = __shfl_up_sync(0xffffffffu, tt, off);
+        const int a = __shfl_up_sync(0xffffffffu, it, off), b = __shfl_up_sync(0xffffffffu, tt, off),
+                  c2 = __shfl_up_sync(0xffffffffu, pt, off);
         if (lane >= off) {
             it += a;
             tt += b;
+            pt += c2;
         }
     }
     if (lane == 31) {
         wsum[warp] = it;
         wtile[warp] = tt;
+        wpair[warp] = pt;
     }
     __syncthreads();
-    int wb = 0, wt = 0;
+    int wb = 0, wt = 0, wp = 0;
     for (int w = 0; w < warp; ++w) {
         wb += wsum[w];
         wt += wtile[w];
+        wp += wpair[w];
     }
-    const int base = wb + it - total, tbase = wt + tt - tiles;
+    const int base = wb + it - total, tbase = wt + tt - tiles, pbase = wp + pt - pairs;
     if (e < E) {
         seg_base[e] = base;
         seg_len[e] = total;
         tile_start[e] = tbase;
-        if (e == E - 1) tile_start[E] = tbase + tiles;
+        pair_start[e] = pbase;
+        if (e == E - 1) {
+            tile_start[E] = tbase + tiles;
+            pair_start[E] = pbase + pairs;
+        }
         int run = base;
         for (int c = 0; c < nch; ++c) {
             chunk_off[(size_t)c * E + e] = run;
@@ -495,11 +510,11 @@ cudaError_t map_a(CUtensorMap* m, const uint16_t* A, uint64_t rows, uint64_t K) 
 }
 
 // One grouped GEMM launch: the A map, the B map(s) and the kernel.
-template <bool NVFP4, int EPI, int TN>
+template <bool NVFP4, int EPI, int TN, int MT = 1>
 cudaError_t launch_gemm(const PrefillGemmArgs& a, uint64_t a_rows, uint64_t b_rows, const DevInfo& d, int m_tiles,
                         int n_tiles, cudaStream_t s) {
     static int configured_for = -1;
-    cudaError_t e = configure_smem(prefill_gemm_kernel<NVFP4, EPI, TN>, d, configured_for);
+    cudaError_t e = configure_smem(prefill_gemm_kernel<NVFP4, EPI, TN, MT>, d, configured_for);
     if (e != cudaSuccess) return e;
     if (m_tiles <= 0 || n_tiles <= 0) return cudaSuccess;
     CUtensorMap ta, tb, ts;
@@ -521,9 +536,9 @@ cudaError_t launch_gemm(const PrefillGemmArgs& a, uint64_t a_rows, uint64_t b_ro
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)m_tiles);
     cfg.blockDim = dim3(kPT);
-    cfg.dynamicSmemBytes = TmaSmem<NVFP4, TN>::total;
+    cfg.dynamicSmemBytes = TmaSmem<NVFP4, TN, MT>::total;
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<NVFP4, EPI, TN>, ta, tb, ts, a);
+    return cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<NVFP4, EPI, TN, MT>, ta, tb, ts, a);
 }
 
 }  // namespace
@@ -543,6 +558,7 @@ PrefillWs prefill_ws_layout(int T, int E, int k, int H, int I, int Is) {
     w.seg_base = take(sizeof(int) * (size_t)E);
     w.seg_len = take(sizeof(int) * (size_t)E);
     w.tile_start = take(sizeof(int) * (size_t)(E + 1));
+    w.pair_start = take(sizeof(int) * (size_t)(E + 1));
     w.perm = take(sizeof(int) * (size_t)T * k);
     w.inv = take(sizeof(int) * (size_t)T * k);
     w.h = take(2 * (size_t)T * k * I);
@@ -563,6 +579,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     int* seg_base = reinterpret_cast<int*>(ws + W.seg_base);
     int* seg_len = reinterpret_cast<int*>(ws + W.seg_len);
     int* tile_start = reinterpret_cast<int*>(ws + W.tile_start);
+    int* pair_start = reinterpret_cast<int*>(ws + W.pair_start);
     int* perm = reinterpret_cast<int*>(ws + W.perm);
     int* inv = reinterpret_cast<int*>(ws + W.inv);
     uint16_t* h = reinterpret_cast<uint16_t*>(ws + W.h);
@@ -572,7 +589,9 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     uint32_t* status = reinterpret_cast<uint32_t*>(ws) + 1;
     const int T = p.T, E = p.E, k = p.k, H = p.H, I = p.I, Is = p.Is;
     const int mt_all = (T + kTileM - 1) / kTileM;
-    const int mt_routed = (T * k + kTileM - 1) / kTileM + E;  // bound on the grouped M-tiles
+    // the expert GEMMs' CTAs: kMT M-tiles each (bounds for the grouped ones)
+    const int mx_all = (T + kMT * kTileM - 1) / (kMT * kTileM);
+    const int mx_routed = (T * k + kMT * kTileM - 1) / (kMT * kTileM) + E;
     const long long rs_h = nvfp4_row_stride(H), rs_i = nvfp4_row_stride(I), rs_is = Is ? nvfp4_row_stride(Is) : 0;
     cudaError_t e;
 
@@ -602,7 +621,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
         scatter_cfg = d.device;
     }
     prefill_hist_kernel<<<nch, kSortChunk, sizeof(int) * E, s>>>(p.ids, T * k, E, chunk_hist);
-    prefill_scan_kernel<<<1, 1024, 0, s>>>(chunk_hist, nch, E, chunk_off, seg_base, seg_len, tile_start);
+    prefill_scan_kernel<<<1, 1024, 0, s>>>(chunk_hist, nch, E, chunk_off, seg_base, seg_len, tile_start, pair_start);
     prefill_scatter_kernel<<<nch, kSortChunk, sizeof(int) * (kSortChunk / 32) * E, s>>>(p.ids, T * k, E, chunk_off,
                                                                                        perm, inv);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -614,6 +633,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     g.A = x_perm;
     g.lda = H;
     g.tile_start = tile_start;
+    g.pair_start = pair_start;
     g.seg_base = seg_base;
     g.seg_len = seg_len;
     g.n_groups = E;
@@ -627,7 +647,8 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     g.out_bf16 = h;
     g.ldo = I;
     g.status = status;
-    if ((e = launch_gemm<true, kEpiSwiglu, kNTile>(g, (uint64_t)T * k, (uint64_t)E * 2 * I, d, mt_routed, I / (kNTile / 2), s)) != cudaSuccess)
+    if ((e = launch_gemm<true, kEpiSwiglu, kNTile, kMT>(g, (uint64_t)T * k, (uint64_t)E * 2 * I, d, mx_routed,
+                                                         I / (kNTile / 2), s)) != cudaSuccess)
         return e;
     if (p.s_gu) {
         PrefillGemmArgs gs = {};
@@ -642,13 +663,16 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
         gs.out_bf16 = hs;
         gs.ldo = Is;
         gs.status = status;
-        if ((e = launch_gemm<true, kEpiSwiglu, kNTile>(gs, T, 2 * (uint64_t)Is, d, mt_all, Is / (kNTile / 2), s)) != cudaSuccess) return e;
+        if ((e = launch_gemm<true, kEpiSwiglu, kNTile, kMT>(gs, T, 2 * (uint64_t)Is, d, mx_all, Is / (kNTile / 2),
+                                                             s)) != cudaSuccess)
+            return e;
     }
     // 5. down
     PrefillGemmArgs dn = {};
     dn.A = h;
     dn.lda = I;
     dn.tile_start = tile_start;
+    dn.pair_start = pair_start;
     dn.seg_base = seg_base;
     dn.seg_len = seg_len;
     dn.n_groups = E;
@@ -661,8 +685,8 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     dn.out_bf16 = dd;
     dn.ldo = H;
     dn.status = status;
-    if ((e = launch_gemm<true, kEpiScale, kNTile>(dn, (uint64_t)T * k, (uint64_t)E * H, d, mt_routed, H / kNTile, s)) !=
-        cudaSuccess)
+    if ((e = launch_gemm<true, kEpiScale, kNTile, kMT>(dn, (uint64_t)T * k, (uint64_t)E * H, d, mx_routed, H / kNTile,
+                                                        s)) != cudaSuccess)
         return e;
     if (p.s_down) {
         PrefillGemmArgs dsa = {};
@@ -676,7 +700,8 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
         dsa.out_bf16 = ds;
         dsa.ldo = H;
         dsa.status = status;
-        if ((e = launch_gemm<true, kEpiScale, kNTile>(dsa, T, H, d, mt_all, H / kNTile, s)) != cudaSuccess) return e;
+        if ((e = launch_gemm<true, kEpiScale, kNTile, kMT>(dsa, T, H, d, mx_all, H / kNTile, s)) != cudaSuccess)
+            return e;
     }
     // 6. combine
     prefill_combine_kernel<<<T, 256, 0, s>>>(p.weights, inv, k, dd, p.s_down ? ds : nullptr, H, p.y);
