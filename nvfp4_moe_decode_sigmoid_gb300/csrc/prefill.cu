@@ -323,19 +323,15 @@ __global__ void __launch_bounds__(kPT, TN == 128 ? 2 : 1) prefill_gemm_kernel(
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) prefill_topk_kernel(const float* logits, const float* bias, int T, int E,
                                                            int k, int32_t* ids, float* weights) {
-    extern __shared__ __align__(16) uint32_t sc[];  // [8][E]
-    const int t0 = blockIdx.x * 8, nt = min(8, T - t0);
-    sigmoid_scores(logits + (size_t)t0 * E, bias, nt, E, sc);
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp < nt) {
-        const int t = t0 + warp;
-        if (E <= 256)
-            topk_warp<8>(sc + (size_t)warp * E, E, k, lane, ids + (size_t)t * k, weights + (size_t)t * k);
-        else
-            topk_warp<FLINT_MAX_EXPERTS / 32>(sc + (size_t)warp * E, E, k, lane, ids + (size_t)t * k,
-                                              weights + (size_t)t * k);
-    }
+    // one warp per token: its logits straight from memory into registers, the
+    // sigmoid (and bias) applied on load
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const float* lg = logits + (size_t)t * E;
+    if (E <= 256)
+        topk_warp_logits<8>(lg, bias, E, k, lane, ids + (size_t)t * k, weights + (size_t)t * k);
+    else
+        topk_warp_logits<FLINT_MAX_EXPERTS / 32>(lg, bias, E, k, lane, ids + (size_t)t * k, weights + (size_t)t * k);
 }
 
 // Counting sort of the (token, rank) pairs q = t k + j by expert, keeping q
@@ -364,8 +360,10 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(const int* chunk_his
     __shared__ int wsum[32], wtile[32], wpair[32];
     const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
     int total = 0;
-    if (e < E)
-        for (int c = 0; c < nch; ++c) total += chunk_hist[(size_t)c * E + e];
+    if (e < E) {
+#pragma unroll 8
+        for (int c = 0; c < nch; ++c) total += ld_cg(chunk_hist + (size_t)c * E + e);  // independent loads in flight
+    }
     const int tiles = (total + kTileM - 1) / kTileM, pairs = (tiles + 1) / 2;
     // exclusive scans of total, tiles and tile pairs over the experts
     int it = total, tt = tiles, pt = pairs;
@@ -402,9 +400,10 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(const int* chunk_his
             pair_start[E] = pbase + pairs;
         }
         int run = base;
+#pragma unroll 8
         for (int c = 0; c < nch; ++c) {
             chunk_off[(size_t)c * E + e] = run;
-            run += chunk_hist[(size_t)c * E + e];
+            run += ld_cg(chunk_hist + (size_t)c * E + e);
         }
     }
 }
@@ -609,7 +608,7 @@ cudaError_t launch_prefill(const PrefillArgs& p, const DevInfo& d, cudaStream_t 
     r.status = status;
     if ((e = launch_gemm<false, kEpiLogits, 128>(r, T, E, d, mt_all, (E + 127) / 128, s)) != cudaSuccess) return e;
     // 2. top-k per token
-    prefill_topk_kernel<<<(T + 7) / 8, 256, sizeof(uint32_t) * 8 * E, s>>>(logits, p.bias, T, E, k, p.ids, p.weights);
+    prefill_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, p.bias, T, E, k, p.ids, p.weights);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 3. pairs sorted by expert
     const int nch = (T * k + kSortChunk - 1) / kSortChunk;
