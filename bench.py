@@ -198,6 +198,10 @@ class Model:
             lay["next_pf"] = F.l2_prefetch(nx["router_w"], nx["shared"].gate_up, nx["shared"].down)
         self.ws = torch.empty(F.flint_workspace_bytes(E, TOPK, H, I, I_SHARED), dtype=torch.uint8, device=device)
         F.flint_workspace_init(self.ws)
+        # sized without the hidden size: flint_moe_decode runs as two kernels on it
+        self.ws_small = torch.empty(F.flint_workspace_bytes(E, TOPK, 0, I, I_SHARED), dtype=torch.uint8,
+                                    device=device)
+        F.flint_workspace_init(self.ws_small)
 
     def step_bytes(self, n_distinct: int, T: int, with_bias: bool) -> int:
         if self.wdtype == "nvfp4":
@@ -220,15 +224,18 @@ def make_inputs(model, T, routing, device):
 
 
 def run_step(F, model, inp, li, bias, flags, path="fused"):
-    """One layer step: the fused kernel, or the router + decode chain."""
+    """One layer step: the fused kernel ("fused"), or the router then
+    flint_moe_decode: one cooperative kernel on the full workspace ("chain"),
+    gate/up and down kernels on one sized without the hidden size ("chain3")."""
     lay, io = model.layers[li], inp[li]
     if path == "fused":
         F.flint_moe_layer(io["x"], lay["router_w"], TOPK, lay["routed"], lay["shared"], io["ids"], io["w"], io["y"],
                           model.ws, bias=bias, flags=flags, next=lay["next_pf"])
         return
-    F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], model.ws, bias=bias, flags=flags)
+    ws = model.ws_small if path == "chain3" else model.ws
+    F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], ws, bias=bias, flags=flags)
     dflags = flags | (F.FLINT_PDL_AFTER_ROUTE if flags & F.FLINT_PDL else 0)
-    F.flint_moe_decode(io["x"], io["ids"], io["w"], lay["routed"], lay["shared"], io["y"], model.ws, flags=dflags)
+    F.flint_moe_decode(io["x"], io["ids"], io["w"], lay["routed"], lay["shared"], io["y"], ws, flags=dflags)
 
 
 def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, device_index, with_clocks=True,
@@ -242,6 +249,7 @@ def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, devic
         run_step(F, model, inp, s % nl, bias, flags, path)
     torch.cuda.synchronize()
     assert F.flint_workspace_check(model.ws) == F.FLINT_OK
+    assert F.flint_workspace_check(model.ws_small) == F.FLINT_OK
     # distinct experts each layer's routing selects -> algorithmic bytes per step
     distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
     bytes_per_layer = [model.step_bytes(d, T, bias is not None) for d in distinct]
@@ -300,8 +308,9 @@ def measure_workload(F, model, name, steps, warmup, graph_steps, sync_all, devic
 
 def measure_bf16(F, nvfp4_model, args, sync_all, dev_index, n_layers=6):
     """The BF16-weight variant of the same layer (router -> gate/up -> down,
-    three PDL-chained kernels; the one-kernel layer is NVFP4-only), at T = 1
-    and T = 8, beside the NVFP4 three-kernel chain on the same workloads.
+    three PDL-chained kernels; the one-kernel layer and decode are NVFP4-only),
+    at T = 1 and T = 8, beside the NVFP4 three-kernel chain on the same
+    workloads.
     `n_layers` BF16 layers (1.5 GB each) rotate, so every step reads HBM."""
     import torch
     bmodel = Model(n_layers, "cuda", "bf16")
@@ -312,7 +321,7 @@ def measure_bf16(F, nvfp4_model, args, sync_all, dev_index, n_layers=6):
         r = measure_workload(F, bmodel, name, steps, args.warmup, args.graph_steps, sync_all, dev_index,
                              with_clocks=False, path="chain")
         q = measure_workload(F, nvfp4_model, name, steps, args.warmup, args.graph_steps, sync_all, dev_index,
-                             with_clocks=False, path="chain")
+                             with_clocks=False, path="chain3")
         gbs = r["bytes"] / (r["ms"] * 1e-3) / 1e9
         out[name] = dict(us_per_layer=round(r["ms"] * 1e3 / r["steps"], 3), gb_s=round(gbs, 1),
                          frac_of_peak=round(gbs / peak, 4), bytes_per_step=r["bytes_per_step_mean"],
@@ -502,8 +511,9 @@ def measure_prefill(F, reps=10):
 
 
 def measure_kernels(F, model, name, reps=8):
-    """Average device duration of each kernel: the fused layer kernel and the
-    three kernels of the chain. For each, a CUDA graph of back-to-back
+    """Average device duration of each kernel: the fused layer kernel, the
+    router, flint_moe_decode as one kernel, and its gate/up and down kernels
+    (the two-kernel path). For each, a CUDA graph of back-to-back
     launches (one per resident layer, no PDL) is replayed `reps` times between
     two CUDA events on the replay stream. The routing comes from a warm-up
     pass, so the gate/up and down launches see each layer's real selection."""
@@ -521,6 +531,8 @@ def measure_kernels(F, model, name, reps=8):
                                                    next=lay["next_pf"]),
         "route": lambda lay, io: F.flint_moe_route(io["x"], lay["router_w"], TOPK, io["ids"], io["w"], model.ws,
                                                    bias=bias),
+        "decode": lambda lay, io: F.flint_moe_decode(io["x"], io["ids"], io["w"], lay["routed"], lay["shared"],
+                                                     io["y"], model.ws),
         "gate_up": lambda lay, io: F.flint_moe_gate_up(io["x"], io["ids"], lay["routed"], lay["shared"], model.ws),
         "down": lambda lay, io: F.flint_moe_down_combine(io["ids"], io["w"], lay["routed"], lay["shared"], io["y"],
                                                          model.ws),
@@ -546,6 +558,7 @@ def measure_kernels(F, model, name, reps=8):
     distinct = [len(set(io["ids"].cpu().numpy().reshape(-1).tolist())) for io in inp]
     out["gate_up_bytes"] = statistics.mean((d + 1) * (gu_b + 8) + T * H * 2 for d in distinct)
     out["down_bytes"] = statistics.mean((d + 1) * (dn_b + 4) + T * H * 2 for d in distinct)
+    out["decode_bytes"] = out["gate_up_bytes"] + out["down_bytes"]
     out["route_bytes"] = ROUTER_BYTES + T * H * 2
     out["layer_bytes"] = statistics.mean(step_bytes(d, T, bias is not None) for d in distinct)
     return out
@@ -810,6 +823,8 @@ def run_flint(args):
     value = replica_value(main["bytes"], world, ms)
     chain = measure_workload(F, model, args.workload, max(1024, args.steps // 4), args.warmup, args.graph_steps,
                              sync_all, dev_index, with_clocks=False, path="chain")
+    chain3 = measure_workload(F, model, args.workload, max(1024, args.steps // 4), args.warmup, args.graph_steps,
+                              sync_all, dev_index, with_clocks=False, path="chain3")
     extra = {}
     if not args.no_extra:
         for name in WORKLOADS:
@@ -875,10 +890,15 @@ def run_flint(args):
                          "us_per_launch": kern["layer_us"]},
             "kernels_us": {k: round(v, 3) for k, v in kern.items() if k.endswith("_us")},
             "kernels_gb_s": {k: round(kern[k + "_bytes"] / (kern[k + "_us"] * 1e-6) / 1e9, 1)
-                             for k in ("layer", "route", "gate_up", "down")},
-            "three_kernel_chain": {"us_per_layer": round(chain["ms"] * 1e3 / chain["steps"], 3),
+                             for k in ("layer", "route", "decode", "gate_up", "down")},
+            "route_decode_chain": {"us_per_layer": round(chain["ms"] * 1e3 / chain["steps"], 3),
                                    "gb_s": round(chain["bytes"] / (chain["ms"] * 1e-3) / 1e9, 1),
-                                   "path": "flint_moe_route -> flint_moe_decode (gate/up, down), PDL"},
+                                   "path": "flint_moe_route -> flint_moe_decode (one cooperative kernel, routing "
+                                           "given), PDL"},
+            "three_kernel_chain": {"us_per_layer": round(chain3["ms"] * 1e3 / chain3["steps"], 3),
+                                   "gb_s": round(chain3["bytes"] / (chain3["ms"] * 1e-3) / 1e9, 1),
+                                   "path": "flint_moe_route -> flint_moe_decode on a workspace sized without the "
+                                           "hidden size (gate/up, down), PDL"},
             "layer_frac_of_peak": round(value / world / peak, 4),
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -160,8 +160,10 @@ flint_status_t flint_nvfp4_dequant(const uint8_t* packed, int64_t rows, int64_t 
  *     PDL chain route -> gate_up -> down_combine -> next route allows (and
  *     fused-layer calls chained with FLINT_PDL, which wait for the previous
  *     kernel before touching the workspace).
- *   - flint_moe_route and flint_moe_decode need only the regions up to the
- *     routed experts' h; any `hidden` (0 included) sizes a workspace for them.
+ *   - flint_moe_route needs only the regions up to the routed experts' h;
+ *     any `hidden` (0 included) sizes a workspace for it. So does
+ *     flint_moe_decode, which then runs as two kernels; on a workspace sized
+ *     with the experts' hidden size it runs as one (see there).
  */
 size_t flint_workspace_bytes(int num_experts, int top_k, int hidden, int inter, int inter_shared);
 flint_status_t flint_workspace_init(void* ws, size_t ws_bytes, void* stream);
@@ -287,8 +289,30 @@ flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* we
                                       flint_bf16* y, void* ws, size_t ws_bytes, unsigned flags,
                                       void* stream);
 
-/* flint_moe_decode -- flint_moe_gate_up then flint_moe_down_combine (two
- * kernels; the second PDL-chained to the first when flags has FLINT_PDL). */
+/*
+ * flint_moe_decode -- the experts of one MoE layer for a given routing:
+ * y = bf16(sum_j weights[j] * d_j + d_shared) with h and d as in
+ * flint_moe_gate_up and flint_moe_down_combine ("Optimizations": the expert
+ * GEMVs read only the selected experts, the combine fused into the down GEMV).
+ *   x [T, H] bf16; ids [T, k] int32 and weights [T, k] FP32 (as from
+ *   flint_moe_route; an id may repeat within a token, and an id outside
+ *   [0, E) is reported by flint_workspace_check and its rank adds nothing);
+ *   y out [T, H] bf16.
+ *   - NVFP4 experts and a workspace of at least
+ *     flint_workspace_bytes(E, k, hidden, inter, inter_shared) (hidden = the
+ *     experts' H): one cooperative kernel, one CTA per SM (the fused layer of
+ *     flint_moe_layer with its router left out; ids and weights read after its
+ *     PDL wait). With FLINT_PDL | FLINT_PDL_AFTER_ROUTE it stages x before
+ *     that wait. Like flint_moe_layer, it needs every CTA resident (shapes
+ *     that do not fit run as below) and a workspace used by one such call at a
+ *     time.
+ *   - Otherwise (BF16 experts, a smaller workspace, or shapes the one kernel
+ *     cannot hold): flint_moe_gate_up then flint_moe_down_combine, two kernels,
+ *     the second PDL-chained to the first when flags has FLINT_PDL.
+ * Both give the same rounding points and rank order of the combine; the FP32
+ * summation order inside the GEMVs differs, so their y may differ in the last
+ * bf16 place.
+ */
 flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, const float* weights, int k,
                                 const flint_experts* routed, const flint_experts* shared, flint_bf16* y,
                                 void* ws, size_t ws_bytes, unsigned flags, void* stream);
@@ -465,7 +489,8 @@ flint_status_t flint_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t b
 /*
  * flint_selftest_lose_cta -- test hook for the fused layer's failure path
  * (no counterpart in the method). On the next flint_moe_layer /
- * flint_moe_block call with this workspace, CTA `cta` publishes neither its
+ * flint_moe_block call with this workspace (or flint_moe_decode where it runs
+ * as one kernel), CTA `cta` publishes neither its
  * router scores nor its count of finished gate/up rows, as if it had been
  * lost: the bounded waits for them (in the other CTAs, and in itself) run out
  * (after the budget of flint_workspace_set_wait_budget), the

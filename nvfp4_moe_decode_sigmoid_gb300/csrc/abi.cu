@@ -205,7 +205,7 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     } else {
         a.Gs = 0;
     }
-    a.rpc = ceil_div(a.E, G - a.Gs);  // router rows per routed CTA
+    a.rpc = a.given ? 0 : ceil_div(a.E, G - a.Gs);  // router rows per routed CTA
     // the kernel splits by cost in 32-bit arithmetic: the total cost of the
     // routed pairs (or blocks) times the group's CTA count must stay below 2^32
     // (an expert's weight is at most 4 + 3 T and the weights sum to at most
@@ -495,6 +495,13 @@ flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* we
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "down_combine launch");
 }
 
+static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, const flint_norm* norm, int T,
+                                     const flint_bf16* router_w, int E, const float* bias, int k,
+                                     const flint_experts* routed, const flint_experts* shared, int32_t* ids,
+                                     float* weights, flint_bf16* y, void* ws, size_t ws_bytes,
+                                     const flint_l2_prefetch* next, unsigned flags, void* stream,
+                                     bool given = false, bool* no_fit = nullptr);
+
 flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, const float* weights, int k,
                                 const flint_experts* routed, const flint_experts* shared, flint_bf16* y, void* ws,
                                 size_t ws_bytes, unsigned flags, void* stream) {
@@ -502,6 +509,19 @@ flint_status_t flint_moe_decode(const flint_bf16* x, int T, const int32_t* ids, 
     if (s != FLINT_OK) return s;
     if (!weights || !y || !aligned(weights, 4) || !aligned(y, 16))
         return fail(FLINT_ERR_INVALID_ARG, "decode: null or misaligned weights/y");
+    if (routed->dtype == FLINT_DTYPE_NVFP4) {
+        // one cooperative launch (the fused layer with the routing given) when
+        // the workspace holds the fused layer's regions and the shapes fit
+        const int Is = shared ? shared->inter : 0;
+        const flint::WsLayout W = flint::ws_layout(routed->num_experts, k, routed->hidden, routed->inter, Is);
+        if (ws && ws_bytes >= W.total) {
+            bool no_fit = false;
+            s = moe_layer_impl("decode", x, nullptr, T, nullptr, routed->num_experts, nullptr, k, routed, shared,
+                               const_cast<int32_t*>(ids), const_cast<float*>(weights), y, ws, ws_bytes, nullptr, flags,
+                               stream, true, &no_fit);
+            if (!no_fit) return s;
+        }
+    }
     s = flint_moe_gate_up(x, T, ids, k, routed, shared, ws, ws_bytes, flags, stream);
     if (s != FLINT_OK) return s;
     return flint_moe_down_combine(T, ids, weights, k, routed, shared, y, ws, ws_bytes, flags, stream);
@@ -549,11 +569,16 @@ flint_status_t flint_residual_rmsnorm(const flint_norm* norm, int T, int H, unsi
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "rmsnorm launch");
 }
 
+// The fused layer launch. given: ids and weights are the caller's routing
+// (flint_moe_decode; no router, norm or prefetch); *no_fit (when not null) is
+// set where the shapes exceed one CTA's shared memory, before anything runs.
 static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, const flint_norm* norm, int T,
                                      const flint_bf16* router_w, int E, const float* bias, int k,
                                      const flint_experts* routed, const flint_experts* shared, int32_t* ids,
                                      float* weights, flint_bf16* y, void* ws, size_t ws_bytes,
-                                     const flint_l2_prefetch* next, unsigned flags, void* stream) {
+                                     const flint_l2_prefetch* next, unsigned flags, void* stream,
+                                     bool given, bool* no_fit) {
+    if (no_fit) *no_fit = false;
     flint_status_t s = moe_common(what, T, k, routed, shared, true);
     if (s != FLINT_OK) return s;
     unsigned long long pf_granules = 0;
@@ -585,13 +610,15 @@ static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, cons
         return fail(FLINT_ERR_UNSUPPORTED,
                     "%s: the one-kernel layer takes NVFP4 experts; run BF16 experts with flint_moe_route + "
                     "flint_moe_decode", what);
-    if (!x || !router_w || !ids || !weights || !y || !aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) ||
-        !aligned(weights, 4) || !aligned(y, 16) || (bias && !aligned(bias, 4)))
+    if (!x || (!given && !router_w) || !ids || !weights || !y || !aligned(x, 16) || !aligned(router_w, 16) ||
+        !aligned(ids, 4) || !aligned(weights, 4) || !aligned(y, 16) || (bias && !aligned(bias, 4)))
         return fail(FLINT_ERR_INVALID_ARG, "%s: null or misaligned pointer", what);
     const int Is = shared ? shared->inter : 0;
     const int H = routed->hidden;
-    if (H > flint::kLayerMaxHidden)
+    if (H > flint::kLayerMaxHidden) {
+        if (no_fit) *no_fit = true;
         return fail(FLINT_ERR_UNSUPPORTED, "%s: hidden %d above %d", what, H, flint::kLayerMaxHidden);
+    }
     const flint::WsLayout W = flint::ws_layout(E, k, H, routed->inter, Is);
     if ((s = check_ws(ws, ws_bytes, W.total)) != FLINT_OK) return s;
     DevInfo d;
@@ -631,8 +658,12 @@ static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, cons
         a.pf_bytes[r] = next && next->bytes[r] ? (unsigned long long)next->bytes[r] : 0ull;
     }
     a.pf_granules = pf_granules;
-    if (!layer_shape(a, d.sm_count, d.smem_optin))
+    a.given = given ? 1 : 0;
+    a.x_early = given && (flags & FLINT_PDL) && (flags & FLINT_PDL_AFTER_ROUTE) ? 1 : 0;
+    if (!layer_shape(a, d.sm_count, d.smem_optin)) {
+        if (no_fit) *no_fit = true;
         return fail(FLINT_ERR_UNSUPPORTED, "%s: shapes exceed one CTA's shared memory", what);
+    }
     cudaError_t e = flint::launch_layer(a, d, (flags & FLINT_PDL) != 0, as_stream(stream));
     return e == cudaSuccess ? FLINT_OK : cuda_fail(e, "layer launch");
 }

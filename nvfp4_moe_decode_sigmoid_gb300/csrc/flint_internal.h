@@ -179,8 +179,8 @@ struct LayerArgs {
     int E;
     const float* bias;   // [E] or null
     int k;
-    int32_t* ids;        // [T][k] out
-    float* weights;      // [T][k] out
+    int32_t* ids;        // [T][k] out (given: in)
+    float* weights;      // [T][k] out (given: in)
     uint32_t* hdr;       // workspace header (kHdr* words)
     uint32_t* status;    // hdr + kHdrStatus
     uint32_t* scores;    // workspace [8][E]: the bits of the sigmoid scores
@@ -210,6 +210,8 @@ struct LayerArgs {
     int rows_max;        // ROWS: most output rows of a CTA (ceil(H / G))
     int rg;              // ROWS: rows per down item (a power of two, at most 8)
     NormArgs norm;       // norm.r set: x = the norm of the residual stream (x unused)
+    int given;           // ids and weights are inputs (flint_moe_decode): no router
+    int x_early;         // given: x is complete before the PDL wait (the router ran on it)
 };
 
 // One grouped GEMM of the prefill: C[rows of each group] = A B^T on 128 x 128

@@ -41,6 +41,12 @@
 //     d leaves the CTA. (From two tokens on this measured slower: every CTA
 //     then walks the rows of every selected expert.)
 //   * The last CTA to finish resets the exchange counters for the next call.
+//   * Given routing (the GIVEN instantiation, behind flint_moe_decode): the
+//     router rows, the score exchange and the top-k are left out; every CTA
+//     reads the caller's ids and weights after its PDL wait. Those may repeat
+//     an expert within a token (its h and d are computed once and d is written
+//     for each of its ranks) or hold an id outside [0, E) (reported in the
+//     status word; the rank adds nothing to y).
 //
 // After a timed-out wait (or any other failure that stops a CTA) the counters
 // are left mid-call and the workspace must be re-initialised
@@ -233,12 +239,12 @@ __device__ void route_view_warp(RouteInfo& ri, const int32_t* ids, int T, int k,
     }
     __syncwarp();
     auto mark = [&](int i, int e, int d) {
+        ri.ids[i] = e;  // -1: no expert (past T k, or an invalid given id)
         if (e < 0) return;
         const int t = i / k, j = i - t * k;
         ri.dlist[d] = e;  // (every lane holding e writes the same value)
         atomicOr(&ri.dmask[d], 1ull << (8 * t + j));
         atomicOr(&ri.tmask[d], 1u << t);
-        ri.ids[i] = e;
     };
     mark(lane, e0, d0);
     mark(lane + 32, e1, d1);
@@ -350,7 +356,7 @@ __device__ void build_segs(LayerSmall& sm, int p0, int up0, int p1, int per_gu, 
 // NORM: the input is rmsnorm(r + y_prev) of the residual stream (a.norm), not
 // a.x. Two instantiations, so that the plain layer carries none of the norm's
 // code (measured: a never-taken norm branch cost 3-4 us at T = 8).
-template <bool NORM, bool ROWS>
+template <bool NORM, bool ROWS, bool GIVEN>
 __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const LayerSmem L = layer_layout(a);
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     const int ng = (nrows + a.rg - 1) / a.rg;
     // router rows: rpc each on the routed CTAs (the shared CTAs queue their
     // expert's copies before the PDL wait and would publish late)
-    const int r0 = (c - Gs) * a.rpc, nrr = sh_cta ? 0 : max(0, min(a.rpc, E - r0));
+    const int r0 = (c - Gs) * a.rpc, nrr = (GIVEN || sh_cta) ? 0 : max(0, min(a.rpc, E - r0));
     const uint32_t full_mask = 0xffffffffu;
     // The routed group copies the tensor scales of all routed experts before
     // the PDL wait (static; one bulk copy when their bytes allow it).
@@ -491,6 +497,18 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         if (lane == 0 && !sm.fail)
             for (int it = 0; it < NSW && it < my_g + my_d; ++it) issue(it);
     }
+    const StageSrc xsrc[1] = {{a.x, xh, csc, T, H}};
+    auto stage_x = [&]() {
+        if constexpr (NORM)
+            stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), sm.ninv, c, G);
+        else
+            stage_f16<false>(xsrc, [] {});
+    };
+    // Given routing right after the router on the same x: the router lets its
+    // dependents launch only once its own wait has returned, so x is complete
+    // and is staged before this kernel's wait (the ids and weights are not).
+    const bool x_early = GIVEN && a.x_early;
+    if (x_early) stage_x();
     // Dependents may launch now: their CTAs take SMs as ours exit, and only
     // read static weights before their own wait.
     pdl_launch_dependents();
@@ -504,11 +522,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         sm.hdr[0] = h0.x; sm.hdr[1] = h0.y; sm.hdr[2] = h0.z; sm.hdr[3] = h0.w;
         sm.hdr[4] = h1.x; sm.hdr[5] = h1.y; sm.hdr[6] = h1.z; sm.hdr[7] = h1.w;
     }
-    const StageSrc xsrc[1] = {{a.x, xh, csc, T, H}};
-    if constexpr (NORM)
-        stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), sm.ninv, c, G);
-    else
-        stage_f16<false>(xsrc, [] {});
+    if (!x_early) stage_x();
     __syncthreads();
     FLINT_PHASE(2);
     const uint64_t budget = sm.hdr[kHdrBudget] ? (uint64_t)sm.hdr[kHdrBudget] * 1000ull : kWaitBudgetNs;
@@ -591,6 +605,22 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     // thread) if the scores never came.
     auto route = [&](int stamp) -> bool {
         (void)stamp;
+        if constexpr (GIVEN) {
+            // the caller's ids and weights (written by an earlier kernel: read
+            // through L2); an id outside [0, E) is reported and becomes -1
+            if (tid < T * k) {
+                int e = ld_cg(a.ids + tid);
+                if (e < 0 || e >= E) {
+                    atomicOr(a.status, kStatusBadExpertId);
+                    e = -1;
+                }
+                sm.ids[tid] = e;
+                sm.w[tid] = ld_cg(a.weights + tid);
+            }
+            __syncthreads();
+            FLINT_PHASE(stamp + 2);
+            return !sm.fail;
+        }
         if (!cta_wait_count(a.hdr + kHdrScoresIn, (uint32_t)E, a.status, kStatusTimeoutLayer, budget, &sm.ok) ||
             sm.fail)
             return false;
@@ -614,7 +644,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         if (!route(11)) {
             failed = true;
         } else {
-            if (c == G - 1 && tid < T * k) {
+            if (!GIVEN && c == G - 1 && tid < T * k) {
                 a.ids[tid] = sm.ids[tid];
                 a.weights[tid] = sm.w[tid];
             }
@@ -816,7 +846,14 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                     cv = csc + (size_t)(t * k + j) * (I / 32);
                 }
             };
-            auto put = [&](float v, int r, int t, int j) { dslot(t, j, rl + r) = bf16_round_f32(tsd * v); };
+            auto put = [&](float v, int r, int t, int j) {
+                const float d = bf16_round_f32(tsd * v);
+                if (GIVEN && !sh) {  // every rank of the token that chose this expert
+                    for (uint32_t b = rank_bits(dm, t); b; b &= b - 1u) dslot(t, __ffs(b) - 1, rl + r) = d;
+                } else {
+                    dslot(t, j, rl + r) = d;
+                }
+            };
             // rows [0, nrw) against one or two tokens (rows past nrw are skipped inside)
             constexpr int RP = 8;
             uint32_t rest = tm;
@@ -862,7 +899,8 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         for (int e = tid; e < T * nrows; e += kLT) {
             const int t = e / nrows, r = e - t * nrows;
             float acc = 0.f;
-            for (int j = 0; j < k; ++j) acc = fmaf(sm.w[t * k + j], dslot(t, j, r), acc);
+            for (int j = 0; j < k; ++j)
+                if (!GIVEN || ri.ids[t * k + j] >= 0) acc = fmaf(sm.w[t * k + j], dslot(t, j, r), acc);
             if (has_sh) acc += dslot(t, k, r);
             a.y[(size_t)t * H + R0 + r] = f32_to_bf16_bits(acc);
         }
@@ -974,6 +1012,9 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 const uint16_t d = f32_to_bf16_bits(tsd * v);
                 if (sh) {
                     a.d_shared[(size_t)t * H + row0 + r] = d;
+                } else if constexpr (GIVEN) {  // every rank of the token that chose this expert
+                    for (uint32_t b = rank_bits(dm, t); b; b &= b - 1u)
+                        a.d_routed[((size_t)t * k + __ffs(b) - 1) * H + row0 + r] = d;
                 } else {
                     const int j = __ffs(rank_bits(dm, t)) - 1;
                     a.d_routed[((size_t)t * k + j) * H + row0 + r] = d;
@@ -1058,11 +1099,16 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
                 }
             };
             const uint4* dr = reinterpret_cast<const uint4*>(a.d_routed + (size_t)t * k * H + r);
-            for (int j = 0; j < k; j += 2) {  // two loads in flight
-                const uint4 d0 = __ldcg(dr + (size_t)j * (H / 8));
-                const uint4 d1 = j + 1 < k ? __ldcg(dr + (size_t)(j + 1) * (H / 8)) : make_uint4(0u, 0u, 0u, 0u);
-                add(sm.w[t * k + j], d0);
-                if (j + 1 < k) add(sm.w[t * k + j + 1], d1);
+            if constexpr (GIVEN) {  // ranks without an expert add nothing
+                for (int j = 0; j < k; ++j)
+                    if (ri.ids[t * k + j] >= 0) add(sm.w[t * k + j], __ldcg(dr + (size_t)j * (H / 8)));
+            } else {
+                for (int j = 0; j < k; j += 2) {  // two loads in flight
+                    const uint4 d0 = __ldcg(dr + (size_t)j * (H / 8));
+                    const uint4 d1 = j + 1 < k ? __ldcg(dr + (size_t)(j + 1) * (H / 8)) : make_uint4(0u, 0u, 0u, 0u);
+                    add(sm.w[t * k + j], d0);
+                    if (j + 1 < k) add(sm.w[t * k + j + 1], d1);
+                }
             }
             if (has_sh) {
                 const uint4 ds = __ldcg(reinterpret_cast<const uint4*>(a.d_shared + (size_t)t * H + r));
@@ -1129,14 +1175,14 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
 size_t layer_smem_bytes(const LayerArgs& a) { return layer_layout(a).total; }
 
 namespace {
-template <bool NORM, bool ROWS>
+template <bool NORM, bool ROWS, bool GIVEN>
 cudaError_t launch_layer_t(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
     static int configured_for = -1;
-    cudaError_t e = configure_smem(layer_kernel<NORM, ROWS>, d, configured_for);
+    cudaError_t e = configure_smem(layer_kernel<NORM, ROWS, GIVEN>, d, configured_for);
     if (e != cudaSuccess) return e;
     const size_t smem = layer_smem_bytes(a);
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_kernel<NORM, ROWS>, kLT, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_kernel<NORM, ROWS, GIVEN>, kLT, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     cudaLaunchConfig_t cfg = {};
@@ -1151,13 +1197,15 @@ cudaError_t launch_layer_t(const LayerArgs& a, const DevInfo& d, bool pdl, cudaS
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, layer_kernel<NORM, ROWS>, a);
+    return cudaLaunchKernelEx(&cfg, layer_kernel<NORM, ROWS, GIVEN>, a);
 }
 }  // namespace
 
 cudaError_t launch_layer(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
-    if (a.rows) return a.norm.r ? launch_layer_t<true, true>(a, d, pdl, s) : launch_layer_t<false, true>(a, d, pdl, s);
-    return a.norm.r ? launch_layer_t<true, false>(a, d, pdl, s) : launch_layer_t<false, false>(a, d, pdl, s);
+    if (a.given) return a.rows ? launch_layer_t<false, true, true>(a, d, pdl, s) : launch_layer_t<false, false, true>(a, d, pdl, s);
+    if (a.rows)
+        return a.norm.r ? launch_layer_t<true, true, false>(a, d, pdl, s) : launch_layer_t<false, true, false>(a, d, pdl, s);
+    return a.norm.r ? launch_layer_t<true, false, false>(a, d, pdl, s) : launch_layer_t<false, false, false>(a, d, pdl, s);
 }
 
 }  // namespace flint

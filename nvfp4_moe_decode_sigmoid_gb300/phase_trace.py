@@ -9,6 +9,12 @@ shared-expert CTAs and the routed-expert CTAs separately, in thousands of SM
 cycles.
 
     python -m nvfp4_moe_decode_sigmoid_gb300.phase_trace --tokens 1
+    python -m nvfp4_moe_decode_sigmoid_gb300.phase_trace --tokens 8 --path decode
+
+--path decode traces flint_moe_decode as one kernel (the routing given: each
+call follows flint_moe_route on the same x, PDL-chained) instead of
+flint_moe_layer; its routed CTAs have no router rows or score exchange, and
+"ids read" replaces those intervals.
 
 Intervals (between the kernel's stamps; "-" where a group of CTAs has none):
   wait for the previous call      entry to the PDL wait's return (static copies issued)
@@ -44,6 +50,7 @@ import numpy as np
 
 # (name, from stamp, to stamp); the stamps the kernel takes (see layer.cu)
 INTERVALS = [("wait for the previous call", 0, 1, "all"), ("x staged", 1, 2, "all"),
+             ("ids read (decode)", 3, 13, "decode"),
              ("router scores published", 2, 3, "routed"), ("all scores in", 3, 11, "routed"),
              ("top-k", 12, 13, "routed"), ("routing view", 13, 14, "routed"), ("split", 14, 19, "routed"),
              ("first copies", 19, 4, "routed"), ("first chunk in", 4, 5, "all"), ("gate/up", 5, 6, "all"),
@@ -67,6 +74,7 @@ def main(argv=None):
     p.add_argument("--experts", type=int, default=256)
     p.add_argument("--inter", type=int, default=512)
     p.add_argument("--top-k", type=int, default=6)
+    p.add_argument("--path", choices=["layer", "decode"], default="layer")
     p.add_argument("--dump", default=None, help="also save the raw stamps ([calls][CTAs][stamps]) to this .npy file")
     args = p.parse_args(argv)
 
@@ -101,6 +109,11 @@ def main(argv=None):
 
     def step(i):
         lay = layers[i % len(layers)]
+        if args.path == "decode":
+            F.flint_moe_route(lay["x"], lay["router_w"], k, lay["ids"], lay["w"], ws, bias=bias, flags=F.FLINT_PDL)
+            F.flint_moe_decode(lay["x"], lay["ids"], lay["w"], lay["routed"], lay["shared"], lay["y"], ws,
+                               flags=F.FLINT_PDL | F.FLINT_PDL_AFTER_ROUTE)
+            return
         F.flint_moe_layer(lay["x"], lay["router_w"], k, lay["routed"], lay["shared"], lay["ids"], lay["w"], lay["y"],
                           ws, bias=bias, flags=F.FLINT_PDL)
 
@@ -133,6 +146,8 @@ def main(argv=None):
             role = "shared" if shared_role[c, cta] else "routed"
             st = tr[c, cta]
             for n, (_, a, b, who) in enumerate(INTERVALS):
+                if who == "decode":
+                    who = "routed" if args.path == "decode" else None
                 if who in ("all", role) and st[a] and st[b]:
                     cells.setdefault((role, n), []).append(int(st[b] - st[a]))
     spans = [(tr[c, :, 30].max() - tr[c, :, 29].min()) / 1e3 for c in calls]
@@ -140,7 +155,8 @@ def main(argv=None):
     entry_spread = [(tr[c, :, 29].max() - tr[c, :, 29].min()) / 1e3 for c in calls]
     pub = [tr[c, tr[c, :, 26] > 0, 26] for c in calls]
     pub_spread = [(p.max() - p.min()) / 1e3 for p in pub if p.size]
-    print(f"## Fused layer phases: T = {T}, {args.routing} routing, {len(calls)} calls traced "
+    what = "Fused layer" if args.path == "layer" else "One-kernel decode (routing given, after the router)"
+    print(f"## {what} phases: T = {T}, {args.routing} routing, {len(calls)} calls traced "
           f"({args.layers} resident layers, PDL-chained in one CUDA graph)\n")
     print("kcycles of the SM clock, median / max over the CTAs of all traced calls\n")
     print("| interval | shared-expert CTAs | routed-expert CTAs |")
@@ -170,7 +186,8 @@ def main(argv=None):
     print(f"\nCTAs: {n_sh} shared, {G - n_sh} routed. On the global timer (coarse), median over the calls: "
           f"call span (first entry to last end, with the wait for the previous call) "
           f"{statistics.median(spans):.2f} us; spread of the CTAs' entries {statistics.median(entry_spread):.2f} us; "
-          f"spread of their router-score publications {statistics.median(pub_spread):.2f} us")
+          + (f"spread of their router-score publications {statistics.median(pub_spread):.2f} us" if pub_spread
+             else "no router-score publications"))
 
 
 if __name__ == "__main__":

@@ -73,40 +73,114 @@ def test_shared_expert_wider_than_routed():
     _check_layer(dl, x, 6)
 
 
-def test_decode_with_repeated_and_shared_ids(small_layer):
-    # hand-made routing: token 0 picks expert 3 twice, tokens share experts
+def _decode_ws(dl, k, path):
+    """A workspace for flint_moe_decode: sized with the experts' hidden size
+    (one cooperative kernel) or with hidden 0 (the two-kernel path)."""
+    if path == "one kernel":
+        return dl.workspace(k)
+    f = flint()
+    Is = dl.L.Is if dl.L.shared is not None else 0
+    ws = torch.empty(f.flint_workspace_bytes(dl.L.E, k, 0, dl.L.I, Is), dtype=torch.uint8, device="cuda")
+    f.flint_workspace_init(ws)
+    return ws
+
+
+PATHS = ["one kernel", "two kernels"]
+
+# hand-made routings: an expert picked twice by one token, experts shared
+# between tokens; one token (the one-kernel path splits down by output rows)
+# and several (split by expert)
+REPEATED = {
+    1: ([[3, 3, 7, 0]], [[0.4, 0.3, 0.2, 0.1]]),
+    3: ([[3, 3, 7, 0], [7, 0, 15, 3], [15, 14, 13, 12]],
+        [[0.4, 0.3, 0.2, 0.1], [0.25, 0.25, 0.25, 0.25], [0.7, 0.1, 0.1, 0.1]]),
+    8: ([[5, 5, 5, 5]] + [[(3 * t + j) % 16 for j in range(4)] for t in range(1, 8)],
+        [[0.1, 0.2, 0.3, 0.4]] * 8),
+}
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("T", sorted(REPEATED))
+def test_decode_with_repeated_and_shared_ids(small_layer, T, path):
     f = flint()
     dl = small_layer
-    T, k, H = 3, 4, 1024
-    x = synth.activations(21, T, H)
-    ids = np.array([[3, 3, 7, 0], [7, 0, 15, 3], [15, 14, 13, 12]], np.int32)
-    w = np.array([[0.4, 0.3, 0.2, 0.1], [0.25, 0.25, 0.25, 0.25], [0.7, 0.1, 0.1, 0.1]], np.float32)
-    ws = dl.workspace(k)
-    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    k, H = 4, 1024
+    x = synth.activations(21 + T, T, H)
+    ids = np.array(REPEATED[T][0], np.int32)
+    w = np.array(REPEATED[T][1], np.float32)
+    ws = _decode_ws(dl, k, path)
+    y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
     f.flint_moe_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), dl.routed, dl.shared, y,
                        ws)
     assert f.flint_workspace_check(ws) == f.FLINT_OK
     ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
-    assert_close(synth.bits(y), ref, "repeated ids", terms=combine_terms(synth.bits(x), ids, w, dl))
+    assert_close(synth.bits(y), ref, f"repeated ids ({path})", terms=combine_terms(synth.bits(x), ids, w, dl))
 
 
-def test_out_of_range_id_is_reported_not_read(small_layer):
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("T", [1, 3])
+def test_out_of_range_id_is_reported_and_adds_nothing(small_layer, T, path):
+    """An id outside [0, E) is reported (FLINT_ERR_INVALID_ARG from the check,
+    which clears it), its weights are never read against any expert, and y is
+    the combine of the other ranks: the oracle with that rank's weight 0."""
     f = flint()
     dl = small_layer
-    T, k, H = 1, 2, 1024
-    ids = torch.tensor([[1, 999]], dtype=torch.int32, device="cuda")
-    w = torch.tensor([[0.5, 0.5]], dtype=torch.float32, device="cuda")
-    ws = dl.workspace(k)
-    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-    f.flint_moe_decode(synth.activations(2, T, H).cuda(), ids, w, dl.routed, dl.shared, y, ws)
+    k, H = 2, 1024
+    ids = np.array([[1, 999], [-4, 2], [6, 5]][:T], np.int32)
+    w = np.array([[0.5, 0.5], [0.5, 0.5], [0.6, 0.4]][:T], np.float32)
+    x = synth.activations(2 + T, T, H)
+    ws = _decode_ws(dl, k, path)
+    y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    f.flint_moe_decode(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), dl.routed, dl.shared, y,
+                       ws)
     assert f.flint_workspace_check(ws) == f.FLINT_ERR_INVALID_ARG
     assert f.flint_workspace_check(ws) == f.FLINT_OK  # cleared
+    bad = (ids < 0) | (ids >= dl.L.E)
+    ids_ref, w_ref = np.where(bad, 0, ids).astype(np.int32), np.where(bad, 0.0, w).astype(np.float32)
+    ref = oracle.moe_experts(synth.bits(x), ids_ref, w_ref, **dl.oracle_args())
+    assert_close(synth.bits(y), ref, f"invalid id ({path})", terms=combine_terms(synth.bits(x), ids_ref, w_ref, dl))
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_decode_paths_agree_with_the_oracle_on_router_output(T):
+    """The one-kernel and the two-kernel decode on the router's own ids and
+    weights (full Flint shape): each within the tolerance of the oracle, and
+    each deterministic."""
+    f = flint()
+    dl = _full()
+    k, H = 6, 2048
+    x = margin_x(synth.bits(dl.L.router_w), T, H, k, None, seed=40 + T)
+    xc = x.cuda()
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    f.flint_moe_route(xc, dl.router_w, k, ids, w, dl.workspace(k))
+    ref = oracle.moe_experts(synth.bits(x), ids.cpu().numpy(), w.cpu().numpy(), **dl.oracle_args())
+    terms = combine_terms(synth.bits(x), ids.cpu().numpy(), w.cpu().numpy(), dl)
+    for path in PATHS:
+        ws = _decode_ws(dl, k, path)
+        outs = []
+        for _ in range(2):
+            y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+            f.flint_moe_decode(xc, ids, w, dl.routed, dl.shared, y, ws, flags=f.FLINT_PDL)
+            assert f.flint_workspace_check(ws) == f.FLINT_OK
+            outs.append(synth.bits(y))
+        assert np.array_equal(outs[0], outs[1]), path
+        assert_close(outs[0], ref, f"decode ({path})", terms=terms)
+
+
+_FULL = {}
+
+
+def _full():
+    # one Flint-shaped layer: H 2048, 256 routed + 1 shared expert, I 512
+    if "dl" not in _FULL:
+        _FULL["dl"] = DeviceLayer(synth.Layer(1000, H=2048, E=256, I=512, I_shared=512))
+    return _FULL["dl"]
 
 
 @pytest.fixture(scope="module")
 def full_layer():
-    # one Flint-shaped layer: H 2048, 256 routed + 1 shared expert, I 512
-    return DeviceLayer(synth.Layer(1000, H=2048, E=256, I=512, I_shared=512))
+    return _full()
 
 
 def test_full_layer_batch1(full_layer):

@@ -61,3 +61,39 @@ def test_fused_layer_lost_cta_times_out_and_the_workspace_recovers():
     rids, rw, ry = oracle.moe_layer(synth.bits(x), synth.bits(dl.L.router_w), k, **dl.oracle_args())
     assert np.array_equal(ids.cpu().numpy(), rids)
     assert_close(synth.bits(y), ry, "after recovery", terms=combine_terms(synth.bits(x), rids, rw, dl))
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_decode_one_kernel_lost_cta_times_out_and_the_workspace_recovers(T):
+    """flint_moe_decode on a workspace sized for one kernel, with CTA 0 (a
+    shared-expert CTA) publishing no h counts: the CTAs that wait for them give
+    up after the short budget, the check reports FLINT_ERR_TIMEOUT and
+    re-initialises the workspace, and the next call is correct (oracle)."""
+    import numpy as np
+
+    import oracle
+    from flint_testlib import DeviceLayer, assert_close, combine_terms
+
+    f = flint()
+    dl = DeviceLayer(synth.Layer(19, H=1024, E=16, I=256, I_shared=256))
+    k, H = 4, 1024
+    ids = np.array([[2, 9, 4, 11], [0, 9, 15, 6]][:T], np.int32)
+    w = np.array([[0.4, 0.3, 0.2, 0.1], [0.1, 0.2, 0.3, 0.4]][:T], np.float32)
+    x = synth.activations(5 + T, T, H)
+    ws = dl.workspace(k)
+    y = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
+    xc, ic, wc = x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
+
+    def call():
+        f.flint_moe_decode(xc, ic, wc, dl.routed, dl.shared, y, ws)
+
+    f.flint_workspace_set_wait_budget(ws, 2000)  # 2 ms
+    f.flint_selftest_lose_cta(ws, 0)
+    call()
+    torch.cuda.synchronize()
+    assert f.flint_workspace_check(ws) == f.FLINT_ERR_TIMEOUT
+    assert f.flint_workspace_check(ws) == f.FLINT_OK
+    call()
+    assert f.flint_workspace_check(ws) == f.FLINT_OK
+    ref = oracle.moe_experts(synth.bits(x), ids, w, **dl.oracle_args())
+    assert_close(synth.bits(y), ref, "after recovery", terms=combine_terms(synth.bits(x), ids, w, dl))
