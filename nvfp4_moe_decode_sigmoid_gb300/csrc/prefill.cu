@@ -354,16 +354,29 @@ __global__ void __launch_bounds__(kSortChunk) prefill_hist_kernel(const int32_t*
     for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[(size_t)blockIdx.x * E + e] = hist[e];
 }
 
+// One CTA of 1024 threads; E <= 1024. Q = 1024 / E threads per expert
+// (thread q E + e), each over a contiguous range of the chunks, so that an
+// expert's counts are read Q ranges at a time; the ranges' sums meet in
+// shared memory.
 __global__ void __launch_bounds__(1024) prefill_scan_kernel(const int* chunk_hist, int nch, int E, int* chunk_off,
                                                             int* seg_base, int* seg_len, int* tile_start,
                                                             int* pair_start) {
+    __shared__ int part[1024];  // per thread: its range's sum, then the range's first offset
     __shared__ int wsum[32], wtile[32], wpair[32];
-    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-    int total = 0;
-    if (e < E) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int Q = max(1, 1024 / E), q = tid / E, ex = tid - q * E;
+    const bool act = q < Q;
+    const int c0 = act ? (int)((long long)q * nch / Q) : 0, c1 = act ? (int)((long long)(q + 1) * nch / Q) : 0;
+    int s = 0;
 #pragma unroll 8
-        for (int c = 0; c < nch; ++c) total += ld_cg(chunk_hist + (size_t)c * E + e);  // independent loads in flight
-    }
+    for (int c = c0; c < c1; ++c) s += ld_cg(chunk_hist + (size_t)c * E + ex);  // independent loads in flight
+    part[tid] = s;
+    __syncthreads();
+    // threads [0, E): expert e = tid, its total over the Q ranges
+    const int e = tid;
+    int total = 0;
+    if (e < E)
+        for (int j = 0; j < Q; ++j) total += part[j * E + e];
     const int tiles = (total + kTileM - 1) / kTileM, pairs = (tiles + 1) / 2;
     // exclusive scans of total, tiles and tile pairs over the experts
     int it = total, tt = tiles, pt = pairs;
@@ -399,11 +412,20 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(const int* chunk_his
             tile_start[E] = tbase + tiles;
             pair_start[E] = pbase + pairs;
         }
-        int run = base;
+        int run = base;  // each range's first offset, in chunk order
+        for (int j = 0; j < Q; ++j) {
+            const int v = part[j * E + e];
+            part[j * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    if (act) {
+        int run = part[tid];
 #pragma unroll 8
-        for (int c = 0; c < nch; ++c) {
-            chunk_off[(size_t)c * E + e] = run;
-            run += ld_cg(chunk_hist + (size_t)c * E + e);
+        for (int c = c0; c < c1; ++c) {
+            chunk_off[(size_t)c * E + ex] = run;
+            run += ld_cg(chunk_hist + (size_t)c * E + ex);
         }
     }
 }

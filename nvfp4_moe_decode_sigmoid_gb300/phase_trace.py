@@ -148,6 +148,8 @@ def main(argv=None):
             for n, (_, a, b, who) in enumerate(INTERVALS):
                 if who == "decode":
                     who = "routed" if args.path == "decode" else None
+                elif args.path == "decode" and a in (2, 35) and b in (3, 36, 37):
+                    who = None  # no router rows on this path
                 if who in ("all", role) and st[a] and st[b]:
                     cells.setdefault((role, n), []).append(int(st[b] - st[a]))
     spans = [(tr[c, :, 30].max() - tr[c, :, 29].min()) / 1e3 for c in calls]
