@@ -17,7 +17,8 @@ LIB = os.path.join(PKG, "libflint.so")
 BUILD_TRACE = os.path.join(PKG, "_build_trace")
 LIB_TRACE = os.path.join(PKG, "libflint_trace.so")
 SOURCES = ["abi.cu", "repack.cu", "route.cu", "gemv.cu", "layer.cu", "bf16.cu", "norm.cu", "prefill.cu"]
-HEADERS = ["flint_device.cuh", "flint_internal.h", "expert_common.cuh", "router_common.cuh", "tcgen05.cuh"]
+HEADERS = ["flint_device.cuh", "flint_internal.h", "expert_common.cuh", "router_common.cuh", "tcgen05.cuh",
+           "layer_one.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "--expt-relaxed-constexpr",

@@ -243,6 +243,34 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     return flint::layer_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin;
 }
 
+// Shapes of the one-token kernel (layer_one_kernel): CTA c of G takes router
+// rows, shared pairs, routed pairs and output rows in equal shares; every
+// share of a CTA must fit its shared memory at once (no rings). False where
+// it does not (the fused layer kernel then runs the token). Blocks (the norm
+// fused in) stay on the fused layer kernel: chained block after block, the
+// one-token kernel measured slower (935-940 against 907 us for the 49-block
+// stack on one GPU), the plain layer within noise of it or faster.
+bool one_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
+    const int G = sm_count;
+    if (a.T != 1 || a.given || a.norm.r) return false;
+    a.rpc = ceil_div(a.E, G);
+    if (a.rpc > flint::kOneWarps - 1) return false;  // one router row per warp, the last warp selects
+    const int ns_max = a.s_gu ? ceil_div(a.Is, G) : 0;
+    a.one_items = ns_max + ceil_div((long long)a.k * a.I, G);
+    if (a.one_items > 32) return false;  // one mbarrier bit per pair
+    const int RS = (int)flint::nvfp4_row_stride(a.H), RSr = (int)flint::nvfp4_row_stride(a.I);
+    const int RSs = a.s_gu ? (int)flint::nvfp4_row_stride(a.Is) : 0;
+    a.slot = 2 * RS;
+    a.rows_max = ceil_div(a.H, G);
+    a.one_rsd = RSr > RSs ? RSr : RSs;
+    a.Gs = 0;
+    a.rows = 0;
+    a.one = 1;
+    if (flint::layer_smem_bytes(a) + kSmemSlack <= (size_t)smem_optin) return true;
+    a.one = 0;
+    return false;
+}
+
 }  // namespace
 
 extern "C" {
@@ -660,7 +688,7 @@ static flint_status_t moe_layer_impl(const char* what, const flint_bf16* x, cons
     a.pf_granules = pf_granules;
     a.given = given ? 1 : 0;
     a.x_early = given && (flags & FLINT_PDL) && (flags & FLINT_PDL_AFTER_ROUTE) ? 1 : 0;
-    if (!layer_shape(a, d.sm_count, d.smem_optin)) {
+    if (!one_shape(a, d.sm_count, d.smem_optin) && !layer_shape(a, d.sm_count, d.smem_optin)) {
         if (no_fit) *no_fit = true;
         return fail(FLINT_ERR_UNSUPPORTED, "%s: shapes exceed one CTA's shared memory", what);
     }

@@ -68,6 +68,10 @@ constexpr int kLayerThreads = kLayerWarps * 32;
 constexpr int kLayerSlots = 2;           // ring slots of each warp of the fused layer
 constexpr int kLayerMaxHidden = 8192;    // largest hidden size of the fused layer
 constexpr int kLayerRowsMaxTokens = 1;   // fused layer: down split by output rows up to this many tokens
+// One-token layer kernel: 12 warps, so that two CTAs fit on an SM (registers)
+// and the next layer's CTA starts its static copies while this one finishes.
+constexpr int kOneWarps = 12;
+constexpr int kOneThreads = kOneWarps * 32;
 
 FLINT_HD constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -212,6 +216,9 @@ struct LayerArgs {
     NormArgs norm;       // norm.r set: x = the norm of the residual stream (x unused)
     int given;           // ids and weights are inputs (flint_moe_decode): no router
     int x_early;         // given: x is complete before the PDL wait (the router ran on it)
+    int one;             // one token: the latency-laid-out kernel (layer_one_kernel)
+    int one_items;       // one: most gate/up pairs of a CTA (shared + routed)
+    int one_rsd;         // one: bytes of a down-row slot (the larger row stride of I and Is)
 };
 
 // One grouped GEMM of the prefill: C[rows of each group] = A B^T on 128 x 128

@@ -1170,9 +1170,11 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     }
 }
 
+#include "layer_one.cuh"
+
 }  // namespace
 
-size_t layer_smem_bytes(const LayerArgs& a) { return layer_layout(a).total; }
+size_t layer_smem_bytes(const LayerArgs& a) { return a.one ? one_layout(a).total : layer_layout(a).total; }
 
 namespace {
 template <bool NORM, bool ROWS, bool GIVEN>
@@ -1199,9 +1201,35 @@ cudaError_t launch_layer_t(const LayerArgs& a, const DevInfo& d, bool pdl, cudaS
     cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, layer_kernel<NORM, ROWS, GIVEN>, a);
 }
+
+template <bool NORM>
+cudaError_t launch_one_t(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
+    static int configured_for = -1;
+    cudaError_t e = configure_smem(layer_one_kernel<NORM>, d, configured_for);
+    if (e != cudaSuccess) return e;
+    const size_t smem = layer_smem_bytes(a);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_one_kernel<NORM>, kOneThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)d.sm_count);
+    cfg.blockDim = dim3(kOneThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, layer_one_kernel<NORM>, a);
+}
 }  // namespace
 
 cudaError_t launch_layer(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
+    if (a.one) return a.norm.r ? launch_one_t<true>(a, d, pdl, s) : launch_one_t<false>(a, d, pdl, s);
     if (a.given) return a.rows ? launch_layer_t<false, true, true>(a, d, pdl, s) : launch_layer_t<false, false, true>(a, d, pdl, s);
     if (a.rows)
         return a.norm.r ? launch_layer_t<true, true, false>(a, d, pdl, s) : launch_layer_t<false, true, false>(a, d, pdl, s);

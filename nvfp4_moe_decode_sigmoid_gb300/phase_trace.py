@@ -61,6 +61,16 @@ INTERVALS = [("wait for the previous call", 0, 1, "all"), ("x staged", 1, 2, "al
              ("one token: routing (shared group, after its gate/up)", 6, 43, "shared"),
              ("after the down items, to the end", 8, 10, "all"),
              ("after the wait, to the end", 1, 10, "all")]
+# The one-token kernel (layer_one_kernel, marked 2 in the low byte of stamp
+# 28): every CTA holds a share of every step, so one column.
+INTERVALS_ONE = [("wait for the previous call", 0, 1), ("x staged", 1, 2),
+                 ("router row published (fence, count)", 2, 3), ("x staged to all scores in", 2, 5),
+                 ("top-k warp: waiting for the scores", 4, 5), ("top-k", 5, 6),
+                 ("routing shared with the CTA", 6, 7), ("routed copies issued", 7, 8),
+                 ("first routed pair done", 8, 9), ("routing to every pair done, h written", 7, 10),
+                 ("all pairs published (h exchange)", 10, 11), ("all of h staged", 11, 12),
+                 ("down rows of every expert", 12, 13), ("rows of y", 13, 14),
+                 ("after the wait, to the end", 1, 14)]
 N_STAMPS, N_CALLS, N_CTAS = 48, 64, 256
 
 
@@ -139,6 +149,8 @@ def main(argv=None):
     if args.dump:
         np.save(args.dump, tr)
     calls = [c for c in range(N_CALLS) if np.all(tr[c, :, 31] == tr[c, 0, 31]) and tr[c, 0, 31] > 0]
+    if calls and np.all((tr[calls, :, 28] & 0xFF) == 2):
+        return report_one(args, tr, calls, G)
     shared_role = (tr[:, :, 28] & 0xFF) == 1
     cells = {}  # (role, interval) -> list of cycles
     for c in calls:
@@ -190,6 +202,40 @@ def main(argv=None):
           f"{statistics.median(spans):.2f} us; spread of the CTAs' entries {statistics.median(entry_spread):.2f} us; "
           + (f"spread of their router-score publications {statistics.median(pub_spread):.2f} us" if pub_spread
              else "no router-score publications"))
+
+
+def report_one(args, tr, calls, G):
+    """The one-token kernel's intervals, median / max over all CTAs of the calls."""
+    print(f"## One-token layer kernel phases: {args.routing} routing, {len(calls)} calls traced "
+          f"({args.layers} resident layers, PDL-chained in one CUDA graph)\n")
+    print("kcycles of the SM clock, median / max over the CTAs of all traced calls\n")
+    print("| interval | all CTAs |")
+    print("|---|---|")
+    for name, a, b in INTERVALS_ONE:
+        v = [int(tr[c, cta, b] - tr[c, cta, a]) for c in calls for cta in range(G) if tr[c, cta, a] and tr[c, cta, b]]
+        if v:
+            print(f"| {name} | {statistics.median(v) / 1e3:.2f} / {max(v) / 1e3:.2f} |")
+    spans = [(tr[c, :, 30].max() - tr[c, :, 29].min()) / 1e3 for c in calls]
+    entry = [(tr[c, :, 29].max() - tr[c, :, 29].min()) / 1e3 for c in calls]
+    pub = [tr[c, tr[c, :, 26] > 0, 26] for c in calls]
+    pub_spread = [(p.max() - p.min()) / 1e3 for p in pub if p.size]
+    # consecutive calls n, n + 1: the first entry of n + 1 against the last end of n, and the last entry of
+    # n + 1 against the last end of n (negative: overlap)
+    by_no = {int(tr[c, 0, 31]): c for c in calls}
+    first_gap, last_gap = [], []
+    for n, c in by_no.items():
+        if n + 1 in by_no:
+            c1 = by_no[n + 1]
+            first_gap.append((tr[c1, :, 29].min() - tr[c, :, 30].max()) / 1e3)
+            last_gap.append((tr[c1, :, 29].max() - tr[c, :, 30].max()) / 1e3)
+    print(f"\nOn the global timer (coarse), median over the calls: call span (first entry to last end, with the "
+          f"wait for the previous call) {statistics.median(spans):.2f} us; spread of the CTAs' entries "
+          f"{statistics.median(entry):.2f} us; spread of their first router-row publications "
+          f"{statistics.median(pub_spread) if pub_spread else float('nan'):.2f} us")
+    if first_gap:
+        print(f"Between consecutive calls: first entry of the next call minus last end of this one "
+              f"{statistics.median(first_gap):.2f} us, last entry of the next minus last end of this one "
+              f"{statistics.median(last_gap):.2f} us ({len(first_gap)} pairs)")
 
 
 if __name__ == "__main__":

@@ -75,6 +75,28 @@ def test_many_experts_wide_topk():
     _check(dl, x, 8)
 
 
+@pytest.mark.parametrize("case", ["no_shared", "wide_shared", "many_experts_k8", "bias"])
+def test_one_token_shapes(case):
+    """One token runs the one-token kernel (equal shares of every step per
+    CTA): without a shared expert, with a shared expert wider than the routed
+    ones, with E = 600 (fewer than one router row per CTA on some, top-k over
+    32 scores per lane) and k = 8, and with a router bias."""
+    f = flint()
+    k, bias = 6, None
+    if case == "no_shared":
+        dl = DeviceLayer(synth.Layer(12, H=1024, E=16, I=256, I_shared=0, shared=False))
+    elif case == "wide_shared":
+        dl = DeviceLayer(synth.Layer(13, H=1024, E=16, I=256, I_shared=1024))
+    elif case == "many_experts_k8":
+        dl, k = DeviceLayer(synth.Layer(14, H=1024, E=600, I=256, I_shared=256)), 8
+    else:
+        dl = DeviceLayer(synth.Layer(15, H=2048, E=256, I=512, I_shared=512))
+        bias = synth.zipf_bias(5, 256)
+    H = dl.L.router_w.shape[1]
+    x = margin_x(synth.bits(dl.L.router_w), 1, H, k, None if bias is None else bias.numpy(), seed=50)
+    _check(dl, x, k, bias=bias, flags=f.FLINT_PDL)
+
+
 @pytest.fixture(scope="module")
 def full_layer():
     return DeviceLayer(synth.Layer(1000, H=2048, E=256, I=512, I_shared=512))
@@ -106,9 +128,10 @@ def test_full_layer_batch8_zipf(full_layer):
     _check(full_layer, x, 6, bias=bias, flags=f.FLINT_PDL)
 
 
-def test_repeated_calls_on_one_workspace_are_deterministic(full_layer):
+@pytest.mark.parametrize("T", [1, 8])
+def test_repeated_calls_on_one_workspace_are_deterministic(full_layer, T):
     # the exchange counts are back at zero after every call
-    x = margin_x(synth.bits(full_layer.L.router_w), 8, 2048, 6, None, seed=10)
+    x = margin_x(synth.bits(full_layer.L.router_w), T, 2048, 6, None, seed=10)
     ws = full_layer.workspace(6)
     outs = [_run(full_layer, x, 6, ws=ws) for _ in range(4)]
     for o in outs[1:]:
@@ -176,18 +199,19 @@ def test_pdl_chained_layers_in_a_graph_match_single_calls(full_layer):
         assert torch.equal(y[:t].view(torch.int16), ry.view(torch.int16))
 
 
-def test_next_layer_prefetch_changes_nothing(full_layer):
+@pytest.mark.parametrize("T", [1, 3])
+def test_next_layer_prefetch_changes_nothing(full_layer, T):
     """flint_moe_layer with the next layer's ranges to pull into L2 (here
     another layer's router and shared expert, and the ranges at any offset of
     16 bytes) gives the same bits as without."""
     f = flint()
     other = DeviceLayer(synth.Layer(1008))
-    x = margin_x(synth.bits(full_layer.L.router_w), 3, 2048, 6, None, seed=21)
+    x = margin_x(synth.bits(full_layer.L.router_w), T, 2048, 6, None, seed=21)
     base = _run(full_layer, x, 6)
     nxt = f.l2_prefetch(other.router_w, other.shared.gate_up[16:], other.shared.down[: 4096 * 16])
-    ids = torch.empty((3, 6), dtype=torch.int32, device="cuda")
-    w = torch.empty((3, 6), dtype=torch.float32, device="cuda")
-    y = torch.empty((3, 2048), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((T, 6), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, 6), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, 2048), dtype=torch.bfloat16, device="cuda")
     ws = full_layer.workspace(6)
     f.flint_moe_layer(x.cuda(), full_layer.router_w, 6, full_layer.routed, full_layer.shared, ids, w, y, ws,
                       flags=f.FLINT_PDL, next=nxt)

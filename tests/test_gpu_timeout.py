@@ -23,12 +23,16 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     torch.cuda.synchronize()
 
 
-def test_fused_layer_lost_cta_times_out_and_the_workspace_recovers():
+@pytest.mark.parametrize("T,lost", [(2, "cta0"), (1, "cta0"), (1, "router_row")])
+def test_fused_layer_lost_cta_times_out_and_the_workspace_recovers(T, lost):
     """The fused layer with one CTA that publishes no router scores (the test
     hook): the others' bounded waits run out after the short budget, the call
     records FLINT_ERR_TIMEOUT, and flint_workspace_check re-initialises the
     workspace. A later call on the same workspace is correct again (oracle),
-    and one made before the check does nothing and keeps the error."""
+    and one made before the check does nothing and keeps the error. At one
+    token (the one-token kernel: E = 16 router rows spread over all CTAs) the
+    lost CTA is CTA 0, which holds no router row and withholds its h count,
+    or the first CTA that holds a router row."""
     import numpy as np
 
     import oracle
@@ -36,7 +40,7 @@ def test_fused_layer_lost_cta_times_out_and_the_workspace_recovers():
 
     f = flint()
     dl = DeviceLayer(synth.Layer(17, H=1024, E=16, I=256, I_shared=256))
-    T, k, H = 2, 6, 1024
+    k, H = 6, 1024
     x = margin_x(synth.bits(dl.L.router_w), T, H, k, None, seed=3)
     ws = dl.workspace(k)
     ids = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
@@ -48,7 +52,9 @@ def test_fused_layer_lost_cta_times_out_and_the_workspace_recovers():
         f.flint_moe_layer(xc, dl.router_w, k, dl.routed, dl.shared, ids, w, y, ws)
 
     f.flint_workspace_set_wait_budget(ws, 2000)  # 2 ms
-    f.flint_selftest_lose_cta(ws, 0)             # CTA 0 (a shared-expert CTA) publishes nothing
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    cta = 0 if lost == "cta0" else next(c for c in range(G) if (c + 1) * 16 // G > c * 16 // G)
+    f.flint_selftest_lose_cta(ws, cta)           # this CTA publishes nothing
     call()
     torch.cuda.synchronize()
     call()                                       # before the check: returns at once
