@@ -252,8 +252,8 @@ bool layer_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
 // stack on one GPU), the plain layer within noise of it or faster.
 bool one_shape(flint::LayerArgs& a, int sm_count, int smem_optin) {
     const int G = sm_count;
-    if (a.T != 1 || a.given || a.norm.r) return false;
-    a.rpc = ceil_div(a.E, G);
+    if (a.T != 1 || a.norm.r) return false;
+    a.rpc = a.given ? 0 : ceil_div(a.E, G);
     if (a.rpc > flint::kOneWarps - 1) return false;  // one router row per warp, the last warp selects
     const int ns_max = a.s_gu ? ceil_div(a.Is, G) : 0;
     a.one_items = ns_max + ceil_div((long long)a.k * a.I, G);

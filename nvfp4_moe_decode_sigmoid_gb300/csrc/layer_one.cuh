@@ -38,6 +38,12 @@
 //     k + 1 down GEMVs (their weights arrived long before) and sums them in
 //     rank order into its rows of y. The last CTA to finish resets the counts.
 //
+// Given routing (GIVEN, behind flint_moe_decode): no router rows, scores or
+// top-k; the caller's ids and weights are read after the PDL wait. An id
+// outside [0, E) is reported in the status word and its rank adds nothing
+// (its pairs and down rows are neither copied nor computed); an expert given
+// at two ranks is simply computed for each.
+//
 // Every wait is bounded by the workspace's budget; on expiry the CTA records
 // FLINT_ERR_TIMEOUT, lets its copies in flight land and returns, and the
 // workspace must be re-initialised (flint_workspace_check does it).
@@ -114,7 +120,7 @@ __device__ __forceinline__ bool warp_wait_count(const uint32_t* p, uint32_t targ
     } while (0)
 #endif
 
-template <bool NORM>
+template <bool NORM, bool GIVEN>
 __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_one_kernel(const LayerArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const OneSmem L = one_layout(a);
@@ -132,7 +138,7 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     float* dres = reinterpret_cast<float*>(smem + L.dres);
     const float* tsall = reinterpret_cast<const float*>(smem + L.tsall);
     // this CTA's shares
-    const int r0 = (int)((long long)c * E / G), nrr = (int)((long long)(c + 1) * E / G) - r0;
+    const int r0 = (int)((long long)c * E / G), nrr = GIVEN ? 0 : (int)((long long)(c + 1) * E / G) - r0;
     const int s0 = has_sh ? (int)((long long)c * Is / G) : 0;
     const int ns = has_sh ? (int)((long long)(c + 1) * Is / G) - s0 : 0;
     const long long kI = (long long)k * I;
@@ -184,6 +190,9 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
         if (i < n1) return cs0 + i / CH;
         return cs0 + cs1 + (i - n1) / CH;
     };
+    // rank r (k: the shared expert) has an expert to compute
+    auto live = [&](int r) { return !GIVEN || r == k || sm.ids[r] >= 0; };
+    auto chunk_rank = [&](int ch) { return ch < cs0 ? k : (ch < cs0 + cs1 ? j0 : j0 + 1); };
     // chunk ch: its first pair, pair count, rank (k: shared) and first row
     auto chunk_span = [&](int ch, int& i0, int& n, int& r, int& p0) {
         if (ch < cs0) {
@@ -220,6 +229,7 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     };
     // the CTA's rows of unit u's down matrix (u = k: the shared expert)
     auto issue_down = [&](int u) {
+        if (!live(u)) return;
         const bool sh = u == k;
         const int RSu = sh ? RSs : RSr;
         const uint8_t* d = sh ? a.s_down : a.down + (size_t)sm.ids[u] * H * RSr;
@@ -229,6 +239,7 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     };
     // chunk ch's two copies (one thread)
     auto issue_chunk = [&](int ch) {
+        if (!live(chunk_rank(ch))) return;
         mbar_arrive_expect_tx(&sm.ibar[ch], chunk_bytes(ch));
         copy_half(ch, 0);
         copy_half(ch, 1);
@@ -276,7 +287,8 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     // x (or the norm's inputs) and the header into L2: the previous kernel may
     // still be writing them (L2 is where its writes land), so only the
     // address translation and a first copy are warmed, no data is read
-    if (warp == TOPW - 1) {
+    const bool x_early = GIVEN && a.x_early;
+    if (warp == TOPW - 1 && !x_early) {
         const size_t xb = (size_t)H * 2;
         for (size_t o = (size_t)lane * 128; o < xb; o += 32 * 128) {
             if constexpr (NORM) {
@@ -288,6 +300,10 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
         }
         if (lane == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.hdr));
     }
+    const StageSrc xsrc[1] = {{a.x, xh, csc, 1, H}};
+    // given routing right after the router on the same x: the router lets its
+    // dependents launch only once its own wait has returned, so x is complete
+    if (x_early) stage_f16<false>(xsrc, [] {});
     pdl_launch_dependents();
     pdl_wait();  // x (or the residual stream) comes from the previous kernel
     FLINT_PHASE(1);
@@ -299,13 +315,10 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
         sm.hdr[0] = h0.x; sm.hdr[1] = h0.y; sm.hdr[2] = h0.z; sm.hdr[3] = h0.w;
         sm.hdr[4] = h1.x; sm.hdr[5] = h1.y; sm.hdr[6] = h1.z; sm.hdr[7] = h1.w;
     }
-    {
-        const StageSrc xsrc[1] = {{a.x, xh, csc, 1, H}};
-        if constexpr (NORM)
-            stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), &sm.ninv, c, G);
-        else
-            stage_f16<false>(xsrc, [] {});
-    }
+    if constexpr (NORM)
+        stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), &sm.ninv, c, G);
+    else if (!x_early)
+        stage_f16<false>(xsrc, [] {});
     __syncthreads();
     FLINT_PHASE(2);
     const uint64_t budget = sm.hdr[kHdrBudget] ? (uint64_t)sm.hdr[kHdrBudget] * 1000ull : kWaitBudgetNs;
@@ -376,6 +389,7 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
 
     // ---- one pair: gate/up sums, then h = bf16(silu(bf16(ts_g g)) bf16(ts_u u)) ----------
     auto compute_item = [&](int i) -> bool {
+        if (!live(chunk_rank(chunk_of(i)))) return true;  // an invalid given id: nothing to compute
         if (!__all_sync(full, mbar_wait_bounded(&sm.ibar[chunk_of(i)], 0, a.status, kStatusTimeoutLayer, budget)))
             return false;
         const int tk[1] = {0};
@@ -397,7 +411,25 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
         if (!compute_item(i)) wfail = true;
 
     // ---- routing: the last warp waits for all E scores and selects the top k -------------
-    if (warp == TOPW && !wfail) {
+    if (GIVEN && warp == TOPW && !wfail) {
+        // the caller's ids and weights (written by an earlier kernel: read
+        // through L2); an id outside [0, E) is reported and becomes -1
+        ONE_STAMP(4);
+        if (lane < k) {
+            int e = ld_cg(a.ids + lane);
+            if (e < 0 || e >= E) {
+                atomicOr(a.status, kStatusBadExpertId);
+                e = -1;
+            }
+            sm.ids[lane] = e;
+            sm.w[lane] = ld_cg(a.weights + lane);
+        }
+        ONE_STAMP(5);
+        if (ts_bulk && !__all_sync(full, mbar_wait_bounded(&sm.rbar, 0, a.status, kStatusTimeoutLayer, budget)))
+            wfail = true;
+        ONE_STAMP(6);
+    }
+    if (!GIVEN && warp == TOPW && !wfail) {
         ONE_STAMP(4);
         if (!warp_wait_count(a.hdr + kHdrScoresIn, (uint32_t)E, a.status, kStatusTimeoutLayer, budget)) {
             wfail = true;
@@ -466,6 +498,7 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     // ---- down: item m is unit m / ngrp's rows [DR (m % ngrp), + DR) of this CTA's rows -----
     for (int m = warp; m < n_units * ngrp && !wfail; m += W) {
         const int u = m / ngrp, rl = DR * (m - u * ngrp), nr = min(DR, nrows - rl);
+        if (!live(u)) continue;
         if (!__all_sync(full, mbar_wait_bounded(&sm.dbar[u], 0, a.status, kStatusTimeoutLayer, budget))) {
             wfail = true;
             break;
@@ -488,7 +521,8 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     // y = bf16(sum_j w_j d_j + d_shared), ranks in order
     for (int r = tid; r < nrows; r += kOneThreads) {
         float acc = 0.f;
-        for (int j = 0; j < k; ++j) acc = fmaf(sm.w[j], dres[j * a.rows_max + r], acc);
+        for (int j = 0; j < k; ++j)
+            if (live(j)) acc = fmaf(sm.w[j], dres[j * a.rows_max + r], acc);
         if (has_sh) acc += dres[k * a.rows_max + r];
         a.y[R0 + r] = f32_to_bf16_bits(acc);
     }
