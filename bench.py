@@ -774,9 +774,10 @@ def cpu_baseline(name, budget_s=20.0):
     return out
 
 
-def traffic_for(kernel_src_hash):
-    """DRAM bytes per launch of the fused layer kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+def traffic_for(kernel_src_hash, tokens):
+    """DRAM bytes per launch of the layer kernel that runs `tokens` tokens
+    (the one-token kernel at one token, else the fused layer kernel) from the
+    committed ncu summary, if it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "layer_traffic.json")
     try:
         with open(path) as f:
@@ -785,13 +786,14 @@ def traffic_for(kernel_src_hash):
         return None
     if d.get("source_sha256") != kernel_src_hash:
         return None
-    return d.get("dram_bytes_per_launch")
+    return (d.get("one_token") or {}).get("dram_bytes_per_launch") if tokens == 1 else d.get("dram_bytes_per_launch")
 
 
 def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
-    for fn in ("layer.cu", "expert_common.cuh", "router_common.cuh", "flint_device.cuh", "flint_internal.h"):
+    for fn in ("layer.cu", "layer_one.cuh", "expert_common.cuh", "router_common.cuh", "flint_device.cuh",
+               "flint_internal.h"):
         with open(os.path.join(ROOT, "nvfp4_moe_decode_sigmoid_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -842,7 +844,7 @@ def run_flint(args):
 
     peak, peak_src = load_peaks()
     achieved = kern["layer_bytes"] / (kern["layer_us"] * 1e-6) / 1e9
-    traffic = traffic_for(kernel_source_hash())
+    traffic = traffic_for(kernel_source_hash(), WORKLOADS[args.workload][0])
     e2e = measure_e2e(F, model, args.workload, min(args.steps, 8192), args.graph_steps)
     stack, prefill = {}, {}
     if not args.no_stack or not args.no_prefill:
@@ -883,7 +885,8 @@ def run_flint(args):
                        "parallelism": f"replicas x{world}",
                        "mean_distinct_experts": main["mean_distinct"],
                        "bytes_per_step": main["bytes_per_step_mean"]},
-            "roofline": {"bound": "hbm", "kernel": "layer_kernel", "achieved": round(achieved, 1),
+            "roofline": {"bound": "hbm", "kernel": "layer_one_kernel" if T == 1 else "layer_kernel",
+                         "achieved": round(achieved, 1),
                          "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                          "traffic": traffic, "algorithmic_bytes_per_launch": kern["layer_bytes"],

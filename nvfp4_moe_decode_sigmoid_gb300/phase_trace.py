@@ -206,12 +206,17 @@ def main(argv=None):
 
 def report_one(args, tr, calls, G):
     """The one-token kernel's intervals, median / max over all CTAs of the calls."""
-    print(f"## One-token layer kernel phases: {args.routing} routing, {len(calls)} calls traced "
+    what = "One-token layer kernel" if args.path == "layer" else "One-token kernel, routing given (after the router)"
+    print(f"## {what} phases: {args.routing} routing, {len(calls)} calls traced "
           f"({args.layers} resident layers, PDL-chained in one CUDA graph)\n")
     print("kcycles of the SM clock, median / max over the CTAs of all traced calls\n")
     print("| interval | all CTAs |")
     print("|---|---|")
     for name, a, b in INTERVALS_ONE:
+        if args.path == "decode":  # the routing given: no router rows, scores or top-k
+            if (a, b) in ((2, 3), (4, 5), (5, 6)):
+                continue
+            name = {"x staged to all scores in": "ids and weights read"}.get(name, name)
         v = [int(tr[c, cta, b] - tr[c, cta, a]) for c in calls for cta in range(G) if tr[c, cta, a] and tr[c, cta, b]]
         if v:
             print(f"| {name} | {statistics.median(v) / 1e3:.2f} / {max(v) / 1e3:.2f} |")
