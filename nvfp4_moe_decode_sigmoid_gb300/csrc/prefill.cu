@@ -21,12 +21,13 @@
 //
 // GEMM tiles are 128 rows x 128 columns, K in steps of 64, accumulated in
 // TMEM by tcgen05.mma (kind::f16, bf16 operands, FP32 accumulator) issued by
-// one thread. The operands stream through a 3-stage ring of shared-memory
-// stages filled by TMA (one thread issues cp.async.bulk.tensor 2-D tile
-// copies completing on the stage's full mbarrier): the A tile with 128-byte
-// swizzle, already in the MMA operand layout, and raw NVFP4 B windows (code
-// and scale bytes), which eight dequantising warps expand into one of two
-// swizzled bf16 B tiles. Empty mbarriers, committed by the MMA thread, hand
+// one thread. The operands stream through a ring of shared-memory stages
+// filled by TMA (one thread issues cp.async.bulk.tensor 2-D tile copies
+// completing on the stage's full mbarrier; 2 stages for the expert GEMMs,
+// which take two M-tiles per CTA, 3 for the router's): the A tiles with
+// 128-byte swizzle, already in the MMA operand layout, and raw NVFP4 B
+// windows (code and scale bytes), which eight dequantising warps expand into
+// one of two swizzled bf16 B tiles. Empty mbarriers, committed by the MMA thread, hand
 // each stage and B tile back. The expert GEMMs' A rows are the expert-sorted
 // copy of the tokens, so every A tile is a plain 2-D tile.
 #include <cuda.h>
