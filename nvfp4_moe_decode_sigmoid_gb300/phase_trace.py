@@ -84,7 +84,7 @@ def main(argv=None):
     p.add_argument("--experts", type=int, default=256)
     p.add_argument("--inter", type=int, default=512)
     p.add_argument("--top-k", type=int, default=6)
-    p.add_argument("--path", choices=["layer", "decode"], default="layer")
+    p.add_argument("--path", choices=["layer", "decode", "block"], default="layer")
     p.add_argument("--dump", default=None, help="also save the raw stamps ([calls][CTAs][stamps]) to this .npy file")
     args = p.parse_args(argv)
 
@@ -117,8 +117,18 @@ def main(argv=None):
     ws = torch.empty(F.flint_workspace_bytes(E, k, H, I, I), dtype=torch.uint8, device="cuda")
     F.flint_workspace_init(ws)
 
+    # block: pre-norm blocks chained as in a decode stack (each block's y is the
+    # next one's y_prev; the residual stream ping-pongs between two buffers)
+    res = [synth.activations(5, T, H, "cuda"), torch.empty((T, H), dtype=torch.bfloat16, device="cuda")]
+    ys = [torch.zeros((T, H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+
     def step(i):
         lay = layers[i % len(layers)]
+        if args.path == "block":
+            F.flint_moe_block(res[i % 2], lay["router_w"], k, lay["routed"], lay["shared"], lay["ids"], lay["w"],
+                              ys[i % 2], ws, y_prev=ys[(i + 1) % 2] if i else None, residual_out=res[(i + 1) % 2],
+                              bias=bias, flags=F.FLINT_PDL)
+            return
         if args.path == "decode":
             F.flint_moe_route(lay["x"], lay["router_w"], k, lay["ids"], lay["w"], ws, bias=bias, flags=F.FLINT_PDL)
             F.flint_moe_decode(lay["x"], lay["ids"], lay["w"], lay["routed"], lay["shared"], lay["y"], ws,
@@ -169,7 +179,8 @@ def main(argv=None):
     entry_spread = [(tr[c, :, 29].max() - tr[c, :, 29].min()) / 1e3 for c in calls]
     pub = [tr[c, tr[c, :, 26] > 0, 26] for c in calls]
     pub_spread = [(p.max() - p.min()) / 1e3 for p in pub if p.size]
-    what = "Fused layer" if args.path == "layer" else "One-kernel decode (routing given, after the router)"
+    what = {"layer": "Fused layer", "block": "Fused pre-norm blocks chained",
+            "decode": "One-kernel decode (routing given, after the router)"}[args.path]
     print(f"## {what} phases: T = {T}, {args.routing} routing, {len(calls)} calls traced "
           f"({args.layers} resident layers, PDL-chained in one CUDA graph)\n")
     print("kcycles of the SM clock, median / max over the CTAs of all traced calls\n")
@@ -206,7 +217,8 @@ def main(argv=None):
 
 def report_one(args, tr, calls, G):
     """The one-token kernel's intervals, median / max over all CTAs of the calls."""
-    what = "One-token layer kernel" if args.path == "layer" else "One-token kernel, routing given (after the router)"
+    what = {"layer": "One-token layer kernel", "block": "One-token kernel, pre-norm blocks chained",
+            "decode": "One-token kernel, routing given (after the router)"}[args.path]
     print(f"## {what} phases: {args.routing} routing, {len(calls)} calls traced "
           f"({args.layers} resident layers, PDL-chained in one CUDA graph)\n")
     print("kcycles of the SM clock, median / max over the CTAs of all traced calls\n")
