@@ -301,9 +301,9 @@ flint_status_t flint_moe_down_combine(int T, const int32_t* ids, const float* we
  *   - NVFP4 experts and a workspace of at least
  *     flint_workspace_bytes(E, k, hidden, inter, inter_shared) (hidden = the
  *     experts' H): one cooperative kernel, one CTA per SM (the fused layer of
- *     flint_moe_layer with its router left out; ids and weights read after its
- *     PDL wait). With FLINT_PDL | FLINT_PDL_AFTER_ROUTE it stages x before
- *     that wait. Like flint_moe_layer, it needs every CTA resident (shapes
+ *     flint_moe_layer with its router left out, its one-token kernel at
+ *     T == 1; ids and weights read after its PDL wait). With FLINT_PDL |
+ *     FLINT_PDL_AFTER_ROUTE it stages x before that wait. Like flint_moe_layer, it needs every CTA resident (shapes
  *     that do not fit run as below) and a workspace used by one such call at a
  *     time.
  *   - Otherwise (BF16 experts, a smaller workspace, or shapes the one kernel
@@ -345,8 +345,13 @@ typedef struct flint_l2_prefetch {
  * release / acquire counts (a CTA waits only for the scores and for the h of
  * the experts it uses; no grid-wide barrier); the combine of each 16-row
  * block of y is done by the CTA that delivers its last expert output. At one
- * token down and the combine are split by output rows instead: every CTA
- * computes its rows of y from all of h, with no exchange of d.
+ * token (T == 1) a kernel laid out for latency runs instead: every CTA takes
+ * equal fixed shares of the router rows, the shared expert's pairs, the
+ * selected experts' pairs (in rank order) and the output rows, and issues its
+ * whole share of the weights at once; its CTAs are small enough (12 warps)
+ * for two to fit on an SM, so with FLINT_PDL the next layer's CTAs become
+ * resident while this one runs. Every CTA then computes its rows of y from
+ * all of h, with no exchange of d. Same rounding points either way.
  *   x [T, H] bf16 (H = routed->hidden, H % 1024 == 0, H <= 8192), router_w
  *   [E, H] bf16 with E = routed->num_experts, bias [E] FP32 or NULL,
  *   1 <= k <= min(8, E). ids [T, k] int32 and weights [T, k] FP32 are written
