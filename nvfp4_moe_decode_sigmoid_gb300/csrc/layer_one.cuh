@@ -49,9 +49,10 @@
 // workspace must be re-initialised (flint_workspace_check does it).
 
 constexpr int kOneMaxItems = 32;  // gate/up pairs of one CTA (shared + routed)
-// pairs per copy of gate rows (and of up rows): one (four measured slower:
-// a pair's compute then waits for the whole chunk)
-constexpr int kOneChunk = 1;
+// pairs per copy of gate rows (and of up rows): two (14.37 against 14.51 us
+// per layer with one: half the copies for the SM to take in; four measured
+// slower in a 24-warp build, a pair's compute then waiting for its chunk)
+constexpr int kOneChunk = 2;
 
 struct OneSmall {
     uint64_t rbar;                        // router rows and tensor scales in
@@ -153,8 +154,6 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     constexpr int CH = kOneChunk;
     const int cs0 = (ns + CH - 1) / CH, cs1 = (n1 + CH - 1) / CH, cs2 = (n2 + CH - 1) / CH;
     const int R0 = c * H / G, nrows = (c + 1) * H / G - R0;
-    constexpr int DR = 8;  // rows per down item (4 measured slower)
-    const int ngrp = (nrows + DR - 1) / DR;
     const int n_units = k + (has_sh ? 1 : 0);
     constexpr int W = kOneWarps;
     constexpr int TOPW = W - 1;  // waits for the scores and selects
@@ -495,23 +494,30 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     __syncthreads();
     FLINT_PHASE(12);
 
-    // ---- down: item m is unit m / ngrp's rows [DR (m % ngrp), + DR) of this CTA's rows -----
-    for (int m = warp; m < n_units * ngrp && !wfail; m += W) {
-        const int u = m / ngrp, rl = DR * (m - u * ngrp), nr = min(DR, nrows - rl);
-        if (!live(u)) continue;
-        if (!__all_sync(full, mbar_wait_bounded(&sm.dbar[u], 0, a.status, kStatusTimeoutLayer, budget))) {
-            wfail = true;
-            break;
+    // ---- down: the CTA's rows of every unit (unit u's rows are u nrows .. u nrows +
+    // nrows - 1 of one list) cut evenly over the warps, in passes of up to 8 rows of
+    // one unit (a warp's cut spans at most two units at the Flint shape) -----------
+    {
+        const int total = n_units * nrows;
+        const int w1 = (warp + 1) * total / W;
+        for (int q = warp * total / W; q < w1 && !wfail;) {
+            const int u = q / nrows, rl = q - u * nrows, nr = min(min(8, nrows - rl), w1 - q);
+            q += nr;
+            if (!live(u)) continue;
+            if (!__all_sync(full, mbar_wait_bounded(&sm.dbar[u], 0, a.status, kStatusTimeoutLayer, budget))) {
+                wfail = true;
+                break;
+            }
+            const bool sh = u == k;
+            const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
+            const uint4* hv[1] = {hh + (size_t)u * (I / 8)};
+            const float* cv[1] = {hsc + (size_t)u * (I / 32)};
+            float acc[8];
+            down_pass<8, 1>(down_dst(u) + (size_t)rl * RSu, RSu, nr, K, hv, cv, lane, acc);
+            const float v = reduce_scatter<8>(acc, lane);
+            const int r = rs_index<8>(lane);
+            if (lane % 4 == 3 && r < nr) dres[u * a.rows_max + rl + r] = bf16_round_f32(tscale(u, 2) * v);
         }
-        const bool sh = u == k;
-        const int K = sh ? Is : I, RSu = sh ? RSs : RSr;
-        const uint4* hv[1] = {hh + (size_t)u * (I / 8)};
-        const float* cv[1] = {hsc + (size_t)u * (I / 32)};
-        float acc[DR];
-        down_pass<DR, 1>(down_dst(u) + (size_t)rl * RSu, RSu, nr, K, hv, cv, lane, acc);
-        const float v = reduce_scatter<DR>(acc, lane);
-        const int r = rs_index<DR>(lane);
-        if (lane % (32 / DR) == 32 / DR - 1 && r < nr) dres[u * a.rows_max + rl + r] = bf16_round_f32(tscale(u, 2) * v);
     }
     if (__syncthreads_or(wfail)) {
         drain(budget);
