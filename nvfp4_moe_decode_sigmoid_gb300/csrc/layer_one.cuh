@@ -110,6 +110,61 @@ __device__ __forceinline__ bool warp_wait_count(const uint32_t* p, uint32_t targ
     return __all_sync(0xffffffffu, ok);
 }
 
+// One token's x (H bf16 values, H % 256 == 0) staged as chunk-scaled f16 in
+// the GATE order of stage_f16, four threads per 32-value chunk: thread q takes
+// the 16-byte word q % 4 of chunk q / 4, the chunk's largest magnitude comes
+// from two shuffles, and each value is converted on its own (the same bits as
+// one thread per chunk, with a quarter of the dependent steps).
+__device__ __forceinline__ void stage_x_quarters(const uint16_t* x, int H, uint4* xh, float* csc) {
+    for (int q = threadIdx.x; q < H / 8; q += blockDim.x) {  // H / 8 is a multiple of 32: whole warps
+        const uint4 w = ld_cg(reinterpret_cast<const uint4*>(x) + q);
+        uint32_t m2 = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                               __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+        m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, 1));
+        m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, 2));
+        // bf16 exponent field of the largest magnitude -> s with max * 2^-s in [2^14, 2^15)
+        const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+        const int sh = min(126, max(-126, (int)(m >> 7) - 141));
+        const float down = __int_as_float((127 - sh) << 23);
+        const int c = q >> 2, i = q & 3;
+        if (i == 0) csc[c] = __int_as_float((127 + sh) << 23);
+        xh[(c / 32) * 128 + i * 32 + c % 32] =
+            make_uint4(f32x2_to_f16x2(bf16_lo(w.x) * down, bf16_hi(w.x) * down),
+                       f32x2_to_f16x2(bf16_lo(w.y) * down, bf16_hi(w.y) * down),
+                       f32x2_to_f16x2(bf16_lo(w.z) * down, bf16_hi(w.z) * down),
+                       f32x2_to_f16x2(bf16_lo(w.w) * down, bf16_hi(w.w) * down));
+    }
+}
+
+// All of h (the routed ranks' [k][I], then the shared expert's [Is]; bf16,
+// written by other CTAs: read through L2) staged in the DOWN order of
+// stage_f16, four threads per 32-value chunk as above (the same bits).
+__device__ __forceinline__ void stage_h_quarters(const uint16_t* hr, const uint16_t* hs, int k, int I, int Is,
+                                                 uint4* hh, float* hsc) {
+    const int nr = k * I / 8, n = nr + Is / 8;  // 16-byte words; a multiple of 32 (I, Is % 256 == 0)
+    for (int q = threadIdx.x; q < n; q += blockDim.x) {
+        const bool sh = q >= nr;
+        const int K = sh ? Is : I, wq = sh ? q - nr : q % (I / 8), v = sh ? 0 : q / (I / 8);
+        const uint4 w = ld_cg(reinterpret_cast<const uint4*>(sh ? hs : hr) + (sh ? wq : q));
+        uint32_t m2 = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                               __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+        m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, 1));
+        m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, 2));
+        const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+        const int s = min(126, max(-126, (int)(m >> 7) - 141));
+        const float down = __int_as_float((127 - s) << 23);
+        const int c = wq >> 2, i = wq & 3;
+        uint4* d = hh + (sh ? (size_t)k * (I / 8) : (size_t)v * (I / 8));
+        float* cs = hsc + (sh ? (size_t)k * (I / 32) : (size_t)v * (I / 32));
+        if (i == 0) cs[c] = __int_as_float((127 + s) << 23);
+        d[(i & 1) * (K / 16) + 2 * c + (i >> 1)] =
+            make_uint4(f32x2_to_f16x2(bf16_lo(w.x) * down, bf16_hi(w.x) * down),
+                       f32x2_to_f16x2(bf16_lo(w.y) * down, bf16_hi(w.y) * down),
+                       f32x2_to_f16x2(bf16_lo(w.z) * down, bf16_hi(w.z) * down),
+                       f32x2_to_f16x2(bf16_lo(w.w) * down, bf16_hi(w.w) * down));
+    }
+}
+
 #ifdef FLINT_PHASE_TRACE
 #define ONE_STAMP(i)                                   \
     do {                                               \
@@ -302,7 +357,7 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     const StageSrc xsrc[1] = {{a.x, xh, csc, 1, H}};
     // given routing right after the router on the same x: the router lets its
     // dependents launch only once its own wait has returned, so x is complete
-    if (x_early) stage_f16<false>(xsrc, [] {});
+    if (x_early) stage_x_quarters(a.x, H, xh, csc);
     pdl_launch_dependents();
     pdl_wait();  // x (or the residual stream) comes from the previous kernel
     FLINT_PHASE(1);
@@ -317,7 +372,7 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     if constexpr (NORM)
         stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), &sm.ninv, c, G);
     else if (!x_early)
-        stage_f16<false>(xsrc, [] {});
+        stage_x_quarters(a.x, H, xh, csc);
     __syncthreads();
     FLINT_PHASE(2);
     const uint64_t budget = sm.hdr[kHdrBudget] ? (uint64_t)sm.hdr[kHdrBudget] * 1000ull : kWaitBudgetNs;
@@ -485,12 +540,7 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     }
     FLINT_PHASE(11);
     // all of h: the routed ranks' [k][I], then the shared expert's [Is]
-    {
-        const StageSrc hsrc[2] = {{a.h_routed, hh, hsc, k, I},
-                                  {a.h_shared, hh + (size_t)k * (I / 8), hsc + (size_t)k * (I / 32),
-                                   has_sh ? 1 : 0, has_sh ? Is : 32}};
-        stage_f16<true>(hsrc, [] {});
-    }
+    stage_h_quarters(a.h_routed, a.h_shared, k, I, has_sh ? Is : 0, hh, hsc);
     __syncthreads();
     FLINT_PHASE(12);
 
