@@ -236,6 +236,62 @@ __device__ __forceinline__ void stage_f16(const StageSrc (&ss)[NS], F&& between)
     }
 }
 
+// One 16-byte word (8 values) of a chunk, staged by the thread that holds it
+// when the four words of every chunk are held by four consecutive lanes (word
+// i = lane % 4): the chunk's largest magnitude comes from two shuffles, then
+// each value is converted on its own. The same bits as stage_store, with a
+// quarter of the dependent steps per thread. Every lane of the warp calls it.
+template <bool DOWN_ORDER>
+__device__ __forceinline__ void stage_store_word(const StageSrc& ss, int v, int c, int i, const uint4 w) {
+    uint32_t m2 = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                           __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+    m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, 1));
+    m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, 2));
+    // bf16 exponent field of the largest magnitude -> s with max * 2^-s in [2^14, 2^15)
+    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    const int sh = min(126, max(-126, (int)(m >> 7) - 141));
+    const float down = __int_as_float((127 - sh) << 23);
+    const int K = ss.K;
+    if (i == 0) ss.csc[v * (K / 32) + c] = __int_as_float((127 + sh) << 23);
+    const int idx = DOWN_ORDER ? (i & 1) * (K / 16) + 2 * c + (i >> 1) : (c / 32) * 128 + i * 32 + c % 32;
+    ss.dst[(size_t)v * (K / 8) + idx] = make_uint4(f32x2_to_f16x2(bf16_lo(w.x) * down, bf16_hi(w.x) * down),
+                                                   f32x2_to_f16x2(bf16_lo(w.y) * down, bf16_hi(w.y) * down),
+                                                   f32x2_to_f16x2(bf16_lo(w.z) * down, bf16_hi(w.z) * down),
+                                                   f32x2_to_f16x2(bf16_lo(w.w) * down, bf16_hi(w.w) * down));
+}
+
+// stage_f16 with four threads per 32-value chunk (thread q of the sources'
+// 16-byte words takes word q % 4 of chunk q / 4), every thread's words loaded
+// at once (up to four per thread per round). The same bits as stage_f16. It
+// pays where the chunks are few against the threads (all of h at one token:
+// the 49-block stack 907 -> 892 us per token step) and measured slower where
+// every thread already has a chunk (eight tokens). Every source holds a
+// multiple of 32 words (K % 256 == 0), so whole warps take part.
+template <bool DOWN_ORDER, int NS>
+__device__ __forceinline__ void stage_f16_quarters(const StageSrc (&ss)[NS]) {
+    constexpr int MW = 4;  // words per thread per round
+    const int nt = (int)blockDim.x;
+    int total = 0;
+#pragma unroll
+    for (int i = 0; i < NS; ++i) total += ss[i].nvec * (ss[i].K / 8);
+    for (int base = 0; base < total; base += MW * nt) {
+        uint4 w[MW];
+        StageSrc sw[MW];
+        int vw[MW], cw[MW];
+#pragma unroll
+        for (int r = 0; r < MW; ++r) {
+            const int q = base + (int)threadIdx.x + r * nt;
+            if (q < total && stage_locate(ss, q >> 2, sw[r], vw[r], cw[r]))
+                w[r] = ld_cg(reinterpret_cast<const uint4*>(sw[r].src + (size_t)vw[r] * sw[r].K + 32 * cw[r]) + (q & 3));
+        }
+#pragma unroll
+        for (int r = 0; r < MW; ++r) {
+            const int q = base + (int)threadIdx.x + r * nt;  // q < total is the same in all lanes of a warp
+            if (q < total) stage_store_word<DOWN_ORDER>(sw[r], vw[r], cw[r], q & 3, w[r]);
+        }
+    }
+}
+
 // ===========================================================================
 // Residual add + RMSNorm ahead of a block, fused into the activation staging
 // ("Flint 是什么": pre-norm blocks; "Optimizations": norm kernels that follow

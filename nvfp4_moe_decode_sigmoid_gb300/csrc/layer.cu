@@ -809,7 +809,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
         const StageSrc hsrc[2] = {{a.h_routed, xh, csc, T * k, I},
                                   {a.h_shared, xh + (size_t)T * k * (I / 8), csc + (size_t)T * k * (I / 32),
                                    has_sh ? T : 0, has_sh ? Is : 32}};
-        stage_f16<true>(hsrc, [] {});
+        stage_f16_quarters<true>(hsrc);
         __syncthreads();
         FLINT_PHASE(7);
         float* dres = reinterpret_cast<float*>(smem + L.dres);
