@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kLT, 1) layer_kernel(const LayerArgs a) {
     const StageSrc xsrc[1] = {{a.x, xh, csc, T, H}};
     auto stage_x = [&]() {
         if constexpr (NORM)
-            stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), sm.ninv, c, G);
+            stage_norm_f16<ROWS>(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), sm.ninv, c, G);
         else
             stage_f16<false>(xsrc, [] {});
     };

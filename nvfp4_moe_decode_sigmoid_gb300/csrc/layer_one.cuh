@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
         sm.hdr[4] = h1.x; sm.hdr[5] = h1.y; sm.hdr[6] = h1.z; sm.hdr[7] = h1.w;
     }
     if constexpr (NORM)
-        stage_norm_f16(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), &sm.ninv, c, G);
+        stage_norm_f16<true>(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), &sm.ninv, c, G);
     else if (!x_early)
         stage_x_quarters(a.x, H, xh, csc);
     __syncthreads();
