@@ -1202,14 +1202,14 @@ cudaError_t launch_layer_t(const LayerArgs& a, const DevInfo& d, bool pdl, cudaS
     return cudaLaunchKernelEx(&cfg, layer_kernel<NORM, ROWS, GIVEN>, a);
 }
 
-template <bool NORM, bool GIVEN>
+template <bool GIVEN>
 cudaError_t launch_one_t(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
     static int configured_for = -1;
-    cudaError_t e = configure_smem(layer_one_kernel<NORM, GIVEN>, d, configured_for);
+    cudaError_t e = configure_smem(layer_one_kernel<GIVEN>, d, configured_for);
     if (e != cudaSuccess) return e;
     const size_t smem = layer_smem_bytes(a);
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_one_kernel<NORM, GIVEN>, kOneThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layer_one_kernel<GIVEN>, kOneThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     cudaLaunchConfig_t cfg = {};
@@ -1224,15 +1224,12 @@ cudaError_t launch_one_t(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStr
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, layer_one_kernel<NORM, GIVEN>, a);
+    return cudaLaunchKernelEx(&cfg, layer_one_kernel<GIVEN>, a);
 }
 }  // namespace
 
 cudaError_t launch_layer(const LayerArgs& a, const DevInfo& d, bool pdl, cudaStream_t s) {
-    if (a.one) {
-        if (a.given) return launch_one_t<false, true>(a, d, pdl, s);
-        return a.norm.r ? launch_one_t<true, false>(a, d, pdl, s) : launch_one_t<false, false>(a, d, pdl, s);
-    }
+    if (a.one) return a.given ? launch_one_t<true>(a, d, pdl, s) : launch_one_t<false>(a, d, pdl, s);
     if (a.given) return a.rows ? launch_layer_t<false, true, true>(a, d, pdl, s) : launch_layer_t<false, false, true>(a, d, pdl, s);
     if (a.rows)
         return a.norm.r ? launch_layer_t<true, true, false>(a, d, pdl, s) : launch_layer_t<false, true, false>(a, d, pdl, s);

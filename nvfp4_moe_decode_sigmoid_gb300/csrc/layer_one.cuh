@@ -26,9 +26,9 @@
 //     experts' tensor scales, the CTA's shared pairs and its shared down rows
 //     are copied (1-D bulk copies, one mbarrier per pair, each used once),
 //     and x is pulled into L2.
-//   * After it: x is staged (chunk-scaled f16, or the block's residual +
-//     RMSNorm), the router warps compute their rows' scores and publish each
-//     with a GPU-scope fence and a count; the warps holding shared pairs
+//   * After it: x is staged (chunk-scaled f16), the router warps compute
+//     their rows' scores and publish each with a GPU-scope fence and a count;
+//     the warps holding shared pairs
 //     compute them meanwhile; the last warp waits for all E scores and selects
 //     the top k. Then the warps issue the CTA's routed pairs' copies (and one
 //     expert's down rows per rank), all at once: the CTA's whole share of the
@@ -62,7 +62,6 @@ struct OneSmall {
     int32_t ids[FLINT_MAX_TOPK];
     float w[FLINT_MAX_TOPK];
     float ts_sh[3];
-    float ninv;
     float res[kOneMaxItems][2];           // raw gate / up sums of pair i
     uint32_t issued_chunks, issued_down;  // copies issued (for the drain on failure)
     int fail, ok;
@@ -72,7 +71,7 @@ struct OneSmall {
 };
 
 struct OneSmem {
-    size_t tsall, xs, csc, nred, hs, hsc, rows, items, down, dres, total;
+    size_t tsall, xs, csc, hs, hsc, rows, items, down, dres, total;
 };
 
 __host__ __device__ inline OneSmem one_layout(const LayerArgs& a) {
@@ -81,8 +80,7 @@ __host__ __device__ inline OneSmem one_layout(const LayerArgs& a) {
     L.tsall = align_up(sizeof(OneSmall), 128);
     L.xs = align_up(L.tsall + 12 * (size_t)a.E, 128);
     L.csc = align_up(L.xs + 2 * H, 128);
-    L.nred = align_up(L.csc + 4 * (H / 32), 128);
-    L.hs = align_up(L.nred + (a.norm.r ? 4 * (H / 32) : 0), 128);
+    L.hs = align_up(L.csc + 4 * (H / 32), 128);
     L.hsc = align_up(L.hs + 2 * nh, 128);
     L.rows = align_up(L.hsc + 4 * (nh / 32), 128);
     L.items = align_up(L.rows + 2 * (size_t)a.rpc * H, 128);
@@ -176,7 +174,7 @@ __device__ __forceinline__ void stage_h_quarters(const uint16_t* hr, const uint1
     } while (0)
 #endif
 
-template <bool NORM, bool GIVEN>
+template <bool GIVEN>
 __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_one_kernel(const LayerArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const OneSmem L = one_layout(a);
@@ -338,28 +336,21 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
     if (lane == 0)
         for (int ch = warp; ch < cs0; ch += W) issue_chunk(ch);
     if (has_sh && warp == TOPW && lane == 0 && nrows > 0) issue_down(k);
-    // x (or the norm's inputs) and the header into L2: the previous kernel may
-    // still be writing them (L2 is where its writes land), so only the
-    // address translation and a first copy are warmed, no data is read
+    // x and the header into L2: the previous kernel may still be writing them
+    // (L2 is where its writes land), so only the address translation and a
+    // first copy are warmed, no data is read
     const bool x_early = GIVEN && a.x_early;
     if (warp == TOPW - 1 && !x_early) {
         const size_t xb = (size_t)H * 2;
-        for (size_t o = (size_t)lane * 128; o < xb; o += 32 * 128) {
-            if constexpr (NORM) {
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.norm.r) + o));
-                if (a.norm.y) asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.norm.y) + o));
-            } else {
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.x) + o));
-            }
-        }
+        for (size_t o = (size_t)lane * 128; o < xb; o += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.x) + o));
         if (lane == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.hdr));
     }
-    const StageSrc xsrc[1] = {{a.x, xh, csc, 1, H}};
     // given routing right after the router on the same x: the router lets its
     // dependents launch only once its own wait has returned, so x is complete
     if (x_early) stage_x_quarters(a.x, H, xh, csc);
     pdl_launch_dependents();
-    pdl_wait();  // x (or the residual stream) comes from the previous kernel
+    pdl_wait();  // x comes from the previous kernel
     FLINT_PHASE(1);
 
     // ---- x, the header ------------------------------------------------------------------
@@ -369,10 +360,7 @@ __global__ void __launch_bounds__(kOneThreads, (kOneWarps <= 12 ? 2 : 1)) layer_
         sm.hdr[0] = h0.x; sm.hdr[1] = h0.y; sm.hdr[2] = h0.z; sm.hdr[3] = h0.w;
         sm.hdr[4] = h1.x; sm.hdr[5] = h1.y; sm.hdr[6] = h1.z; sm.hdr[7] = h1.w;
     }
-    if constexpr (NORM)
-        stage_norm_f16<true>(a.norm, xsrc[0], reinterpret_cast<float*>(smem + L.nred), &sm.ninv, c, G);
-    else if (!x_early)
-        stage_x_quarters(a.x, H, xh, csc);
+    if (!x_early) stage_x_quarters(a.x, H, xh, csc);
     __syncthreads();
     FLINT_PHASE(2);
     const uint64_t budget = sm.hdr[kHdrBudget] ? (uint64_t)sm.hdr[kHdrBudget] * 1000ull : kWaitBudgetNs;
